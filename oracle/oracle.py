@@ -1,0 +1,165 @@
+"""ctypes front end of the fp64 CPU oracle (``prnn_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this module; the CUDA library and its
+Python binding never do, and share no code with it.
+
+Every input is widened to float64 exactly (fp16 and fp32 values are exactly
+representable in fp64), so the oracle sees the same numbers the GPU path is
+given.  What the C side computes, and the passages it follows, is stated in the
+header of ``prnn_oracle.c``.
+
+Parity pins: every function here is pinned by the CPU tests in
+``tests/test_oracle_pins.py`` (hand-computed steps, closed forms, exact
+rational brute force, the linear regime, homogeneity, chaining, sparse versus
+densified equality) -- none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "prnn_oracle.c")
+LIB = os.path.join(_HERE, "_build", "liboracle.so")
+
+_D = ctypes.POINTER(ctypes.c_double)
+_L = ctypes.POINTER(ctypes.c_long)
+_l = ctypes.c_long
+
+
+def compile_oracle(source: str = SOURCE, out: str = LIB) -> str:
+    """Compile the C oracle with gcc into a shared library and return its path.
+    Floating-point contraction is off so that x86 and Arm hosts give the same
+    bits."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-shared", "-fPIC", "-o", out, source]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: Optional[np.ndarray], t=_D):
+    return None if a is None else a.ctypes.data_as(t)
+
+
+class Oracle:
+    """The fp64 reference.  ``Oracle(path)`` loads a given build of it (the
+    mutation tests load deliberately broken copies)."""
+
+    def __init__(self, lib_path: str = LIB):
+        if not os.path.exists(lib_path):
+            if lib_path != LIB:
+                raise FileNotFoundError(lib_path)
+            compile_oracle()
+        self.lib = ctypes.CDLL(lib_path)
+        L = self.lib
+        L.oracle_rnn_forward_dense.argtypes = [_l, _l, _l, _l, _D, _D, _D, _D, _D, _D]
+        L.oracle_rnn_forward_dense.restype = ctypes.c_int
+        L.oracle_rnn_forward_sparse.argtypes = [_l, _l, _l, _l, _l, _D, _D, _D, _L, _D,
+                                                _D, _D]
+        L.oracle_rnn_forward_sparse.restype = ctypes.c_int
+        L.oracle_rnn_input_projection.argtypes = [_l, _l, _l, _l, _D, _D, _D, _D]
+        L.oracle_rnn_input_projection.restype = ctypes.c_int
+        L.oracle_rnn_cell_dense.argtypes = [_l, _l, _l, _D, _D, _D, _D, _D]
+        L.oracle_rnn_cell_dense.restype = ctypes.c_double
+        L.oracle_rnn_cell_sparse.argtypes = [_l, _l, _l, _l, _D, _D, _D, _L, _D, _D]
+        L.oracle_rnn_cell_sparse.restype = ctypes.c_double
+
+    # -- whole sequences -------------------------------------------------
+    def forward_dense(self, x, Wx, Wh, b, h0=None) -> np.ndarray:
+        """y[T,B,H] for dense Wh[H,H]; x[T,B,I], Wx[H,I], b[H], h0[B,H]|None."""
+        x, Wx, Wh, b = _f64(x), _f64(Wx), _f64(Wh), _f64(b)
+        T, B, I = x.shape
+        H = Wh.shape[0]
+        assert Wx.shape == (H, I) and Wh.shape == (H, H) and b.shape == (H,)
+        h0 = None if h0 is None else _f64(h0)
+        assert h0 is None or h0.shape == (B, H)
+        y = np.zeros((T, B, H), dtype=np.float64)
+        rc = self.lib.oracle_rnn_forward_dense(T, B, H, I, _ptr(x), _ptr(Wx), _ptr(Wh),
+                                               _ptr(b), _ptr(h0), _ptr(y))
+        if rc != 0:
+            raise ValueError("oracle_rnn_forward_dense rejected its arguments")
+        return y
+
+    def forward_sparse(self, x, Wx, vals, cols, b, h0=None) -> np.ndarray:
+        """y[T,B,H] for row-balanced Wh given as vals[H,k], cols[H,k]."""
+        x, Wx, vals, b = _f64(x), _f64(Wx), _f64(vals), _f64(b)
+        cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+        T, B, I = x.shape
+        H, k = vals.shape
+        assert cols.shape == (H, k) and Wx.shape == (H, I) and b.shape == (H,)
+        h0 = None if h0 is None else _f64(h0)
+        assert h0 is None or h0.shape == (B, H)
+        y = np.zeros((T, B, H), dtype=np.float64)
+        rc = self.lib.oracle_rnn_forward_sparse(T, B, H, I, k, _ptr(x), _ptr(Wx),
+                                                _ptr(vals), _ptr(cols, _L), _ptr(b),
+                                                _ptr(h0), _ptr(y))
+        if rc != 0:
+            raise ValueError("oracle_rnn_forward_sparse rejected its arguments")
+        return y
+
+    def forward(self, p, T: Optional[int] = None) -> np.ndarray:
+        """Run a ``synth.Problem`` (optionally only its first ``T`` steps)."""
+        x = p.x if T is None else p.x[:T]
+        if p.sparse:
+            return self.forward_sparse(x, p.Wx, p.vals, p.cols, p.b, p.h0)
+        return self.forward_dense(x, p.Wx, p.Wh, p.b, p.h0)
+
+    # -- pieces ----------------------------------------------------------
+    def input_projection(self, x, Wx, b) -> np.ndarray:
+        """P[T,B,H] = Wx x + b for every step."""
+        x, Wx, b = _f64(x), _f64(Wx), _f64(b)
+        T, B, I = x.shape
+        H = Wx.shape[0]
+        P = np.zeros((T, B, H), dtype=np.float64)
+        rc = self.lib.oracle_rnn_input_projection(T, B, H, I, _ptr(x), _ptr(Wx),
+                                                  _ptr(b), _ptr(P))
+        if rc != 0:
+            raise ValueError("oracle_rnn_input_projection rejected its arguments")
+        return P
+
+    def cells(self, p, samples, x_t_of, h_prev_of) -> np.ndarray:
+        """Single outputs of single steps: for each (t, b, r) in ``samples``,
+        ReLU(b[r] + Wx[r,:] x_t[b] + Wh[r,:] h_prev[b]) with x_t and h_prev
+        supplied by the callbacks (the teacher-forced check at full size)."""
+        Wx = _f64(p.Wx)
+        b = _f64(p.b)
+        H, I = Wx.shape
+        if p.sparse:
+            vals = _f64(p.vals)
+            cols = np.ascontiguousarray(p.cols.astype(np.int64))
+            k = vals.shape[1]
+        else:
+            Wh = _f64(p.Wh)
+        out = np.zeros(len(samples), dtype=np.float64)
+        for i, (t, bb, r) in enumerate(samples):
+            x_t = _f64(x_t_of(t, bb))
+            h_prev = _f64(h_prev_of(t, bb))
+            if p.sparse:
+                out[i] = self.lib.oracle_rnn_cell_sparse(H, I, k, r, _ptr(x_t), _ptr(Wx),
+                                                         _ptr(vals), _ptr(cols, _L),
+                                                         _ptr(b), _ptr(h_prev))
+            else:
+                out[i] = self.lib.oracle_rnn_cell_dense(H, I, r, _ptr(x_t), _ptr(Wx),
+                                                        _ptr(Wh), _ptr(b), _ptr(h_prev))
+        return out
+
+
+_DEFAULT: Optional[Oracle] = None
+
+
+def default() -> Oracle:
+    """The oracle built from ``prnn_oracle.c`` (compiled on first use)."""
+    global _DEFAULT
+    if _DEFAULT is None:
+        _DEFAULT = Oracle()
+    return _DEFAULT

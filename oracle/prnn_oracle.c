@@ -1,0 +1,124 @@
+/*
+ * prnn_oracle.c -- plain, slow, fp64 CPU oracle for the forward recurrence of a
+ * vanilla ReLU RNN layer.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check
+ * and the benchmark's CPU-baseline leg call it; the CUDA library never does,
+ * and the two share no code.
+ *
+ * What it computes (the basic, non-LSTM RNN layer of the persistent-rnn library
+ * page, gitmyhub.com/pineking/persistent-rnn, "Important Constraints"; the
+ * single-layer stage of "Optimizing Performance of Recurrent Neural Networks
+ * on GPUs", Abstract):
+ *
+ *     h_{-1} = h0 (zeros when h0 is NULL)
+ *     for t = 0 .. T-1, for every batch column b and hidden row r:
+ *         s        = bias[r] + sum_c Wx[r,c] x[t,b,c] + sum_c Wh[r,c] h_{t-1}[b,c]
+ *         h_t[b,r] = s > 0 ? s : 0                                      (ReLU)
+ *         y[t,b,r] = h_t[b,r]
+ *
+ * The sparse form takes Wh as k (value, column) pairs per row (the row-balanced
+ * layout of "Sparse Persistent RNNs: Squeezing Large Recurrent Networks
+ * On-Chip", measured-effects table, load-balanced pruning rows) and sums over
+ * the listed columns in the order given.  Persistence, sparsity tricks and
+ * timestamps change how fast the result is reached, never the result, so the
+ * oracle is the definition written out: one double accumulator per output,
+ * terms added in the order above, no blocking or reordering.
+ *
+ * Layouts (all row-major, time-major sequences):
+ *   x [T][B][I], Wx [H][I], Wh [H][H], vals/cols [H][k], bias [H],
+ *   h0 [B][H] or NULL, y [T][B][H].
+ * Return: 0 on success, -1 on bad sizes or NULL pointers.
+ */
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+
+static double relu(double s) { return s > 0.0 ? s : 0.0; }
+
+/* One output element of one step, dense Wh.  x_t is [I], h_prev is [H]. */
+double oracle_rnn_cell_dense(long H, long I, long r, const double* x_t,
+                             const double* Wx, const double* Wh,
+                             const double* bias, const double* h_prev) {
+    double s = bias[r];
+    for (long c = 0; c < I; ++c) s += Wx[r * I + c] * x_t[c];
+    for (long c = 0; c < H; ++c) s += Wh[r * H + c] * h_prev[c];
+    return relu(s);
+}
+
+/* One output element of one step, row-balanced sparse Wh (k entries per row). */
+double oracle_rnn_cell_sparse(long H, long I, long k, long r, const double* x_t,
+                              const double* Wx, const double* vals,
+                              const long* cols, const double* bias,
+                              const double* h_prev) {
+    (void)H;
+    double s = bias[r];
+    for (long c = 0; c < I; ++c) s += Wx[r * I + c] * x_t[c];
+    for (long j = 0; j < k; ++j) s += vals[r * k + j] * h_prev[cols[r * k + j]];
+    return relu(s);
+}
+
+/* Shared driver of the time loop.  Only the cell differs between the forms. */
+static int forward(long T, long B, long H, long I, long k, const double* x,
+                   const double* Wx, const double* Wh, const double* vals,
+                   const long* cols, const double* bias, const double* h0,
+                   double* y) {
+    if (T < 0 || B < 0 || H <= 0 || I <= 0) return -1;
+    if (!x || !Wx || !bias || !y) return -1;
+    if (!Wh && (!vals || !cols || k <= 0)) return -1;
+    if (T == 0 || B == 0) return 0;
+    double* zeros = NULL;
+    if (!h0) {
+        zeros = (double*)calloc((size_t)(B * H), sizeof(double));
+        if (!zeros) return -1;
+        h0 = zeros;
+    }
+    for (long t = 0; t < T; ++t) {
+        for (long b = 0; b < B; ++b) {
+            const double* x_t = x + (t * B + b) * I;
+            /* h_{t-1}: the previous step's output, or h0 at t = 0 */
+            const double* h_prev = (t == 0) ? h0 + b * H : y + ((t - 1) * B + b) * H;
+            double* out = y + (t * B + b) * H;
+            for (long r = 0; r < H; ++r) {
+                out[r] = Wh ? oracle_rnn_cell_dense(H, I, r, x_t, Wx, Wh, bias, h_prev)
+                            : oracle_rnn_cell_sparse(H, I, k, r, x_t, Wx, vals, cols,
+                                                     bias, h_prev);
+            }
+        }
+    }
+    free(zeros);
+    return 0;
+}
+
+int oracle_rnn_forward_dense(long T, long B, long H, long I, const double* x,
+                             const double* Wx, const double* Wh,
+                             const double* bias, const double* h0, double* y) {
+    if (!Wh) return -1;
+    return forward(T, B, H, I, 0, x, Wx, Wh, NULL, NULL, bias, h0, y);
+}
+
+int oracle_rnn_forward_sparse(long T, long B, long H, long I, long k,
+                              const double* x, const double* Wx,
+                              const double* vals, const long* cols,
+                              const double* bias, const double* h0, double* y) {
+    if (!vals || !cols || k <= 0 || k > H) return -1;
+    for (long i = 0; i < H * k; ++i)
+        if (cols[i] < 0 || cols[i] >= H) return -1;
+    return forward(T, B, H, I, k, x, Wx, NULL, vals, cols, bias, h0, y);
+}
+
+/*
+ * The input projection on its own, P[t,b,r] = bias[r] + sum_c Wx[r,c] x[t,b,c]:
+ * the part of every step that does not depend on h_{t-1} and so can be done for
+ * all steps at once ("exposing parallelism between operations", Abstract of
+ * "Optimizing Performance of Recurrent Neural Networks on GPUs").
+ */
+int oracle_rnn_input_projection(long T, long B, long H, long I, const double* x,
+                                const double* Wx, const double* bias, double* P) {
+    if (T < 0 || B < 0 || H <= 0 || I <= 0 || !x || !Wx || !bias || !P) return -1;
+    for (long m = 0; m < T * B; ++m)
+        for (long r = 0; r < H; ++r) {
+            double s = bias[r];
+            for (long c = 0; c < I; ++c) s += Wx[r * I + c] * x[m * I + c];
+            P[m * H + r] = s;
+        }
+    return 0;
+}

@@ -1,0 +1,202 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with:
+  * the hand-worked integer example in tests/golden/ (literal values),
+  * closed forms: Wh = 0 gives y_t = ReLU(Wx x_t + b); T = 1 gives
+    y_0 = ReLU(Wx x_0 + Wh h0 + b) (numpy matrix products, a different code path),
+  * the linear regime: with non-negative integer data ReLU is the identity, so
+    h_t = Wh^{t+1} h0 + sum_{j<=t} Wh^{t-j} (Wx x_j + b) exactly (Python ints),
+  * exact rational brute force on tiny sizes (tests/exact_rnn.py),
+  * positive homogeneity (x, b, h0 scaled by 2 scale y by exactly 2),
+  * sparse form equals the densified dense form bit for bit,
+  * chaining and batch independence (the recurrence's own structure).
+The mutation test runs all of them against deliberately broken oracle builds
+and requires each mistake to trip at least one pin.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+
+from tests.exact_rnn import densify, forward_exact
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _relu(a):
+    return np.where(a > 0, a, 0.0)
+
+
+def _rand(rng, *shape, scale=1.0):
+    return rng.normal(0.0, scale, size=shape)
+
+
+def _dyadic(rng, *shape, denom=8, lo=-12, hi=12):
+    """Small multiples of 1/denom: exact in fp16, fp64 and Fraction."""
+    return rng.integers(lo, hi + 1, size=shape).astype(np.float64) / denom
+
+
+def pin_hand_computed(o):
+    g = json.load(open(os.path.join(GOLDEN, "hand_h2_i2_b2_t3.json")))
+    y = o.forward_dense(np.array(g["x"], float), np.array(g["Wx"], float),
+                        np.array(g["Wh"], float), np.array(g["b"], float),
+                        np.array(g["h0"], float))
+    assert np.array_equal(y, np.array(g["y"], float)), y
+
+
+def pin_hand_computed_sparse(o):
+    """The same worked example with Wh given as 2 (value, column) pairs per row,
+    columns deliberately listed out of order in row 1."""
+    g = json.load(open(os.path.join(GOLDEN, "hand_h2_i2_b2_t3.json")))
+    Wh = np.array(g["Wh"], float)
+    vals = np.array([[Wh[0, 0], Wh[0, 1]], [Wh[1, 1], Wh[1, 0]]])
+    cols = np.array([[0, 1], [1, 0]])
+    y = o.forward_sparse(np.array(g["x"], float), np.array(g["Wx"], float), vals, cols,
+                         np.array(g["b"], float), np.array(g["h0"], float))
+    assert np.array_equal(y, np.array(g["y"], float)), y
+
+
+def pin_wh_zero_identity(o):
+    rng = np.random.default_rng(11)
+    T, B, H, I = 4, 3, 7, 5
+    x, Wx, b = _rand(rng, T, B, I), _rand(rng, H, I), _rand(rng, H)
+    h0 = _rand(rng, B, H)
+    y = o.forward_dense(x, Wx, np.zeros((H, H)), b, h0)
+    ref = _relu(np.einsum("tbi,ri->tbr", x, Wx) + b)
+    assert np.allclose(y, ref, rtol=1e-13, atol=1e-13), np.abs(y - ref).max()
+    # the projection alone is the pre-activation of the same closed form
+    P = o.input_projection(x, Wx, b)
+    assert np.allclose(P, np.einsum("tbi,ri->tbr", x, Wx) + b, rtol=1e-13, atol=1e-13)
+
+
+def pin_t1_closed_form(o):
+    rng = np.random.default_rng(12)
+    B, H, I = 3, 6, 9
+    x, Wx, Wh, b = _rand(rng, 1, B, I), _rand(rng, H, I), _rand(rng, H, H), _rand(rng, H)
+    h0 = _rand(rng, B, H)
+    y = o.forward_dense(x, Wx, Wh, b, h0)
+    ref = _relu(x[0] @ Wx.T + h0 @ Wh.T + b)
+    assert np.allclose(y[0], ref, rtol=1e-13, atol=1e-13), np.abs(y[0] - ref).max()
+    # h0 = NULL means zeros
+    y0 = o.forward_dense(x, Wx, Wh, b, None)
+    assert np.allclose(y0[0], _relu(x[0] @ Wx.T + b), rtol=1e-13, atol=1e-13)
+
+
+def pin_linear_regime_exact(o):
+    """Non-negative integers: every pre-activation is >= 0, ReLU is the
+    identity, and the recurrence is a linear system with an exact
+    matrix-power solution (computed with Python integers)."""
+    rng = np.random.default_rng(13)
+    T, B, H, I = 5, 2, 3, 2
+    x = rng.integers(0, 3, size=(T, B, I))
+    Wx = rng.integers(0, 3, size=(H, I))
+    Wh = rng.integers(0, 2, size=(H, H))
+    Wh[0, 2] = 1
+    Wh[2, 0] = 0                       # make Wh asymmetric
+    b = rng.integers(0, 3, size=H)
+    h0 = rng.integers(0, 3, size=(B, H))
+    y = o.forward_dense(x, Wx, Wh, b, h0)
+    Whi = [[int(v) for v in row] for row in Wh]
+
+    def matvec(M, v):
+        return [sum(M[r][c] * v[c] for c in range(len(v))) for r in range(len(M))]
+
+    for bb in range(B):
+        for t in range(T):
+            acc = [int(v) for v in h0[bb]]
+            for _ in range(t + 1):
+                acc = matvec(Whi, acc)                    # Wh^{t+1} h0
+            for j in range(t + 1):
+                u = [int(b[r]) + sum(int(Wx[r][i]) * int(x[j][bb][i]) for i in range(I))
+                     for r in range(H)]
+                for _ in range(t - j):
+                    u = matvec(Whi, u)                    # Wh^{t-j} (Wx x_j + b)
+                acc = [a + c for a, c in zip(acc, u)]
+            assert [float(v) for v in acc] == list(y[t, bb]), (t, bb, acc, y[t, bb])
+
+
+def pin_exact_rational(o):
+    rng = np.random.default_rng(14)
+    for (T, B, H, I) in [(4, 2, 4, 3), (3, 1, 2, 4), (4, 3, 3, 3)]:
+        x = _dyadic(rng, T, B, I)
+        Wx, Wh = _dyadic(rng, H, I), _dyadic(rng, H, H)
+        b, h0 = _dyadic(rng, H), _dyadic(rng, B, H)
+        y = o.forward_dense(x, Wx, Wh, b, h0)
+        ref = forward_exact(x.tolist(), Wx.tolist(), Wh.tolist(), b.tolist(), h0.tolist())
+        for t in range(T):
+            for bb in range(B):
+                for r in range(H):
+                    assert y[t, bb, r] == float(ref[t][bb][r]), (T, B, H, I, t, bb, r)
+    # sparse: rational brute force on the densified matrix
+    H, k, T, B = 4, 2, 4, 2
+    cols = np.array([[3, 1], [0, 2], [2, 3], [1, 0]])
+    vals = _dyadic(rng, H, k)
+    x, Wx, b = _dyadic(rng, T, B, H), _dyadic(rng, H, H), _dyadic(rng, H)
+    y = o.forward_sparse(x, Wx, vals, cols, b, None)
+    W = densify(vals.tolist(), cols.tolist(), H)
+    ref = forward_exact(x.tolist(), Wx.tolist(), [[float(v) for v in r] for r in W],
+                        b.tolist(), None)
+    for t in range(T):
+        for bb in range(B):
+            assert list(y[t, bb]) == [float(v) for v in ref[t][bb]], (t, bb)
+
+
+def pin_homogeneity(o):
+    rng = np.random.default_rng(15)
+    T, B, H, I = 6, 2, 8, 5
+    x, Wx, Wh, b = _rand(rng, T, B, I), _rand(rng, H, I), _rand(rng, H, H, scale=0.3), \
+        _rand(rng, H)
+    h0 = _rand(rng, B, H)
+    y1 = o.forward_dense(x, Wx, Wh, b, h0)
+    y2 = o.forward_dense(2 * x, Wx, Wh, 2 * b, 2 * h0)
+    assert np.array_equal(y2, 2 * y1)
+    assert (y1 > 0).any() and (y1 == 0).any()      # both ReLU branches taken
+
+
+def pin_sparse_equals_densified(o):
+    rng = np.random.default_rng(16)
+    T, B, H, I, k = 5, 3, 33, 20, 5
+    cols = np.stack([np.sort(rng.choice(H, k, replace=False)) for _ in range(H)])
+    vals = _rand(rng, H, k, scale=0.5)
+    Wh = np.zeros((H, H))
+    for r in range(H):
+        Wh[r, cols[r]] = vals[r]
+    x, Wx, b, h0 = _rand(rng, T, B, I), _rand(rng, H, I), _rand(rng, H), _rand(rng, B, H)
+    ys = o.forward_sparse(x, Wx, vals, cols, b, h0)
+    yd = o.forward_dense(x, Wx, Wh, b, h0)
+    assert np.array_equal(ys, yd)
+
+
+def pin_chaining(o):
+    rng = np.random.default_rng(17)
+    T1, T2, B, H, I = 3, 4, 2, 9, 9
+    x, Wx, Wh, b = _rand(rng, T1 + T2, B, I), _rand(rng, H, I), \
+        _rand(rng, H, H, scale=0.3), _rand(rng, H)
+    h0 = _rand(rng, B, H)
+    y = o.forward_dense(x, Wx, Wh, b, h0)
+    ya = o.forward_dense(x[:T1], Wx, Wh, b, h0)
+    yb = o.forward_dense(x[T1:], Wx, Wh, b, ya[-1])
+    assert np.array_equal(y, np.concatenate([ya, yb]))
+
+
+def pin_batch_independence(o):
+    rng = np.random.default_rng(18)
+    T, B, H, I = 4, 3, 10, 6
+    x, Wx, Wh, b = _rand(rng, T, B, I), _rand(rng, H, I), _rand(rng, H, H, scale=0.3), \
+        _rand(rng, H)
+    h0 = _rand(rng, B, H)
+    y = o.forward_dense(x, Wx, Wh, b, h0)
+    for bb in range(B):
+        yi = o.forward_dense(x[:, bb:bb + 1], Wx, Wh, b, h0[bb:bb + 1])
+        assert np.array_equal(yi[:, 0], y[:, bb])
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+def run_all(o):
+    for pin in ALL_PINS:
+        pin(o)

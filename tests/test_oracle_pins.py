@@ -1,0 +1,80 @@
+"""CPU tests: the fp64 oracle against its pins, and the pins' own strength."""
+import os
+import shutil
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.default()
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(o, pin):
+    pin(o)
+
+
+def test_cells_match_forward(o):
+    """The single-output entry the full-size checks use agrees with the
+    whole-sequence driver, element for element."""
+    from persistent_rnn_recurrence_gb300 import synth
+    for p in (synth.make_problem(H=40, B=3, T=3, I=24, wdtype="f32", seed=3, h0_std=0.5),
+              synth.make_problem(H=40, B=3, T=3, k=7, seed=4)):
+        y = o.forward(p)
+        samples = [(t, b, r) for t in range(p.T) for b in range(p.B) for r in (0, 17, 39)]
+        h0 = np.zeros((p.B, p.H)) if p.h0 is None else p.h0
+        got = o.cells(p, samples, lambda t, b: p.x[t, b],
+                      lambda t, b: h0[b] if t == 0 else y[t - 1, b])
+        want = np.array([y[t, b, r] for (t, b, r) in samples])
+        assert np.array_equal(got, want)
+
+
+def test_rejects_bad_arguments(o):
+    x = np.zeros((1, 1, 2))
+    with pytest.raises(ValueError):
+        o.forward_sparse(x, np.zeros((2, 2)), np.ones((2, 1)), np.array([[0], [2]]),
+                         np.zeros(2))
+    assert o.forward_dense(np.zeros((0, 1, 2)), np.zeros((2, 2)), np.zeros((2, 2)),
+                           np.zeros(2)).shape == (0, 1, 2)
+
+
+# Plausible mistakes, planted in a copy of the oracle's source.  Each must make
+# at least one pin fail (the copy runs in a child process).
+MUTANTS = {
+    "dropped_bias": ("double s = bias[r];", "double s = 0.0;"),
+    "transposed_wh": ("Wh[r * H + c]", "Wh[c * H + r]"),
+    "transposed_wx": ("Wx[r * I + c] * x_t[c]", "Wx[(c % H) * I + (r % I)] * x_t[c]"),
+    "in_place_h": ("y + ((t - 1) * B + b) * H", "y + (t * B + b) * H"),
+    "no_relu": ("return s > 0.0 ? s : 0.0;", "return s;"),
+    "h0_batch_offset": ("h0 + b * H :", "h0 :"),
+    "sparse_wrong_column": ("h_prev[cols[r * k + j]]", "h_prev[j]"),
+    "x_batch_index": ("x + (t * B + b) * I", "x + (t * B) * I"),
+    "x_time_shift": ("x + (t * B + b) * I", "x + (((t + 1) % T) * B + b) * I"),
+    "dropped_recurrent_term": ("s += Wh[r * H + c] * h_prev[c];", "(void)h_prev;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(oracle.oracle.SOURCE).read()
+    assert old in src, f"mutation anchor for {name} not found"
+    mutant = tmp_path / "mutant.c"
+    mutant.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    oracle.compile_oracle(str(mutant), str(lib))
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "import oracle\nfrom tests import oracle_pins\n"
+            "oracle_pins.run_all(oracle.Oracle(%r))\n") % (ROOT, str(lib))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                       cwd=ROOT, timeout=120)
+    assert r.returncode != 0, f"mutant {name} passed every pin"
