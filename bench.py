@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Benchmark of the persistent ReLU-RNN forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--algo persistent|per_step] [--impl ours|reference]
+
+One step = one prnn_forward over the whole workload (projection of all T
+steps + the T-step recurrence) with inputs resident in HBM.  The default
+workload is the sparse layer the headline metric is quoted on: H = 1792,
+B = 4, T = 256, Wh row-balanced at 10 % (179 non-zeros per row), fp16 weights,
+fp32 activations and accumulation.  Inputs are smaller than L2, so L2 is
+flushed (a 256 MiB write) between timed steps, outside the timed events.
+
+Prints one JSON line (rank 0).  Multi-GPU: replicas only (every rank runs the
+same layer on its own GPU, no collective on the data path); value is the
+timesteps all ranks processed divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = "sparse_f16_h1792_d10_b4_t256"
+METRIC = "RNN timesteps/s (H=1792, B=4, T=256, 10% row-balanced sparse Wh)"
+FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--algo", default="persistent", choices=["persistent", "per_step"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip e2e / sync floor / per-step comparison (for profiling runs)")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def workload_flops(p) -> dict:
+    """Algorithmic FLOPs of one forward: projection 2*T*B*H*I, recurrence
+    2*T*B*nnz (nnz = H*H dense, H*k sparse)."""
+    proj = 2.0 * p.T * p.B * p.H * p.I
+    rec = 2.0 * p.T * p.B * p.nnz
+    return {"projection": proj, "recurrence": rec, "total": proj + rec,
+            "recurrence_dense_equiv": 2.0 * p.T * p.B * p.H * p.H}
+
+
+# ---- clocks ---------------------------------------------------------------------
+CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self) -> dict:
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), f[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = sorted(r[0] for r in rows)
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[2][i] == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---- reference arm: the fp64 CPU oracle -------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np  # noqa: F401
+    import oracle
+    from persistent_rnn_recurrence_gb300 import synth
+    p = synth.named_problem(args.config)
+    o = oracle.default()
+    # size one step at about one second of oracle work
+    t0 = time.perf_counter()
+    o.forward(p, T=2)
+    per_t = (time.perf_counter() - t0) / 2
+    Ts = int(max(1, min(p.T, round(1.0 / max(per_t, 1e-6)))))
+    for _ in range(args.warmup):
+        o.forward(p, T=Ts)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        o.forward(p, T=Ts)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = Ts * args.steps / total
+    sample = f"first {Ts} of {p.T} timesteps of the workload per step, single thread"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "timesteps/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(p, args, "fp64 CPU oracle"),
+        "cpu_baseline": {"value": value, "unit": "timesteps/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "timesteps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_dict(p, args, path):
+    return {"workload": p.name, "H": p.H, "I": p.I, "B": p.B, "T": p.T,
+            "weights": ("row-balanced sparse, k=%d (%.1f%%)" % (p.k, 100.0 * p.k / p.H))
+            if p.sparse else "dense", "wdtype": p.wdtype, "path": path,
+            "l2": "flushed between timed steps (256 MiB write)", "global_batch": p.B,
+            "seq_len": p.T, "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+
+
+def cpu_baseline(p) -> dict:
+    """The oracle as it stands, single-threaded, on a bounded sample of the
+    same workload (about 10-20 s of CPU work)."""
+    import oracle
+    o = oracle.default()
+    t0 = time.perf_counter()
+    o.forward(p, T=2)
+    per_t = (time.perf_counter() - t0) / 2
+    Ts = int(max(1, min(p.T, round(12.0 / max(per_t, 1e-6)))))
+    t0 = time.perf_counter()
+    o.forward(p, T=Ts)
+    dt = time.perf_counter() - t0
+    return {"value": Ts / dt, "unit": "timesteps/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {Ts} of {p.T} timesteps, B={p.B}, one run, single thread",
+            "seconds": dt}
+
+
+# ---- our arm ----------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np  # noqa: F401
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from persistent_rnn_recurrence_gb300 import prnn, synth
+
+    p = synth.named_problem(args.config)
+    lay = prnn.Layer.from_problem(p, algo=args.algo)
+    lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+    info = lay.info()
+    x = torch.from_numpy(p.x).to(dev)
+    h0 = None if p.h0 is None else torch.from_numpy(p.h0).to(dev)
+    y = torch.empty((p.T, p.B, p.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    fl = workload_flops(p)
+
+    def step():
+        prnn.prnn_forward(lay.h, p.T, p.B, x, h0, y, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if lay.status() != prnn.PRNN_OK:
+        raise RuntimeError("warm-up forward reported " + prnn.prnn_status_string(lay.status()))
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    stage = []
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") \
+        else str(gpu_id if gpu_id is not None else local)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(1.0)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+            stage.append(prnn.prnn_get_timing(lay.h))   # synchronizes on the forward
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    torch.cuda.synchronize()
+    if lay.status() != prnn.PRNN_OK:
+        raise RuntimeError("timed forward reported " + prnn.prnn_status_string(lay.status()))
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
+    ms_step = 1e3 * total_s / args.steps
+    value = world * p.T * args.steps / total_s
+    rec_ms = sorted(s[1] for s in stage)
+    proj_ms = sorted(s[0] for s in stage)
+    rec_med = rec_ms[len(rec_ms) // 2]
+    proj_med = proj_ms[len(proj_ms) // 2]
+    clocks = clk.summary()
+
+    extras = {}
+    if not args.no_extras:
+        extras = measure_extras(args, p, lay, x, h0, y, flush, stream, dev, world)
+
+    # roofline of the dominant (recurrent) kernel: on-chip bound, FP32 FMA pipe
+    sm_count = info["sm_count"] or props.multi_processor_count
+    peaks = load_peaks()
+    sm_max_mhz = peaks.get("sm_max_mhz", 2070.0)
+    fma_peak_tflops = sm_count * 128 * 2 * sm_max_mhz * 1e6 / 1e12
+    smem_peak_tbs = sm_count * 128 * sm_max_mhz * 1e6 / 1e12
+    w_bytes = (4.0 * p.nnz) if p.sparse else (p.H * p.H * (2.0 if p.wdtype == "f16" else 4.0))
+    t_fma = (2.0 * p.B * p.nnz) / (fma_peak_tflops * 1e12)
+    t_smem = w_bytes / (smem_peak_tbs * 1e12)
+    rec_tflops = fl["recurrence"] / (rec_med * 1e-3) / 1e12
+    roof = {"bound": "alu", "kernel": "recur_sparse_kernel" if p.sparse else "recur_dense_kernel",
+            "achieved": rec_tflops, "peak": fma_peak_tflops, "unit": "TFLOP/s",
+            "frac": rec_tflops / fma_peak_tflops, "traffic": load_traffic(p.name, args.algo),
+            "peak_source": f"derived: {sm_count} SMs x 128 FP32 lanes x 2 FLOP x {sm_max_mhz:.0f} MHz",
+            "t_roof_step_ns": 1e9 * max(t_fma, t_smem),
+            "t_step_ns": 1e6 * rec_med / p.T,
+            "frac_of_step_roofline": 1e9 * max(t_fma, t_smem) / (1e6 * rec_med / p.T)}
+    if args.algo == "per_step":
+        roof["kernel"] = "step kernels (T launches)"
+
+    line = {
+        "metric": METRIC if args.config == DEFAULT_CONFIG else f"RNN timesteps/s ({p.name})",
+        "value": value, "unit": "timesteps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_dict(p, args, args.algo),
+        "gflops_effective": fl["total"] / (ms_step * 1e-3) / 1e9 * world,
+        "gflops_dense_equivalent": (fl["projection"] + fl["recurrence_dense_equiv"])
+        / (ms_step * 1e-3) / 1e9 * world,
+        "stage_ms": {"projection": proj_med, "recurrence": rec_med},
+        "roofline": roof,
+        "clocks": clocks,
+        "gpu_launches": args.steps * (2 if args.algo == "persistent" else 1 + p.T),
+        "wall_s": wall,
+        "plan": {k: info[k] for k in ("n_cta", "rows_per_cta", "threads_per_cta",
+                                      "threads_per_row", "k_padded", "smem_bytes",
+                                      "onchip_weight_bytes", "projection_tensor_cores")},
+    }
+    line.update(extras)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(p)
+    lay.close()
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_extras(args, p, lay, x, h0, y, flush, stream, dev, world):
+    import torch
+    from persistent_rnn_recurrence_gb300 import prnn
+    out = {}
+    K = max(3, min(args.steps, 10))
+    # end to end through the public API from pinned host memory
+    xh = torch.from_numpy(p.x).pin_memory()
+    yh = torch.empty((p.T, p.B, p.H), dtype=torch.float32).pin_memory()
+    xd = torch.empty_like(x)
+    for _ in range(2):
+        xd.copy_(xh, non_blocking=True)
+        prnn.prnn_forward(lay.h, p.T, p.B, xd, h0, y, stream)
+        yh.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(K):
+        flush.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        xd.copy_(xh, non_blocking=True)
+        prnn.prnn_forward(lay.h, p.T, p.B, xd, h0, y, stream)
+        yh.copy_(y, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    e2e_s = max_over_ranks(sum(ms) / 1e3, world, dev)
+    out["e2e"] = {"value": world * p.T * K / e2e_s, "unit": "timesteps/s",
+                  "h2d_bytes_per_step": xh.numel() * 4, "d2h_bytes_per_step": yh.numel() * 4}
+    # step-synchronisation floor of the same grid
+    if args.algo == "persistent":
+        ys = torch.empty_like(y)
+        fl_ms = []
+        for _ in range(K):
+            prnn.prnn_probe_sync_floor(lay.h, p.T, p.B, ys, stream)
+            fl_ms.append(prnn.prnn_get_timing(lay.h)[1])
+        fl_ms.sort()
+        out["sync_floor_ns_per_step"] = 1e6 * fl_ms[len(fl_ms) // 2] / p.T
+        # in-house per-step path on the same workload, for the persistent/per-step ratio
+        from persistent_rnn_recurrence_gb300 import synth  # noqa: F401
+        ps = prnn.Layer.from_problem(p, algo="per_step")
+        ps.set_option(prnn.PRNN_OPT_TIMING, 1)
+        for _ in range(3):
+            prnn.prnn_forward(ps.h, p.T, p.B, x, h0, y, stream)
+        pm = []
+        for _ in range(K):
+            flush.fill_(1.0)
+            prnn.prnn_forward(ps.h, p.T, p.B, x, h0, y, stream)
+            pm.append(prnn.prnn_get_timing(ps.h))
+        ps.close()
+        rec = sorted(v[1] for v in pm)
+        out["per_step_path"] = {"recurrence_ms": rec[len(rec) // 2],
+                                "timesteps_per_s_recurrence": 1e3 * p.T / rec[len(rec) // 2]}
+    return out
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def load_traffic(workload: str, algo: str):
+    """DRAM bytes per launch of the recurrent kernel from the committed ncu
+    summary (profiles/traffic.json), or None when not captured for this
+    kernel version."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get(f"{workload}/{algo}")
+    except (OSError, ValueError):
+        return None
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

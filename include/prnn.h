@@ -1,0 +1,163 @@
+/*
+ * prnn.h -- C ABI of the persistent ReLU-RNN recurrence library (libprnn.so),
+ * written for GB300 (sm_103a).
+ *
+ * The operation is the forward pass of one vanilla ("basic", non-LSTM) RNN
+ * layer, the only layer kind of the persistent-rnn library page
+ * (gitmyhub.com/pineking/persistent-rnn, "Important Constraints"):
+ *
+ *     h_t = ReLU(Wx x_t + Wh h_{t-1} + b),   t = 0 .. T-1,   y[t] = h_t
+ *
+ * computed in two stages: the input projection Wx x_t + b for every step at
+ * once (the parallel work the "Optimizing Performance of Recurrent Neural
+ * Networks on GPUs" abstract exposes), then the serial recurrence in one
+ * persistent kernel that keeps Wh on chip for the whole sequence instead of
+ * re-reading it every step (persistent-rnn page, "What This Project Does").
+ * Wh is dense, or row-balanced sparse with the same number of non-zeros in
+ * every row (load-balanced pruning, "Sparse Persistent RNNs: Squeezing Large
+ * Recurrent Networks On-Chip", measured-effects table).  The call sequence
+ * follows the cuDNN-like shape the persistent-rnn page describes ("Who Would
+ * Use This"): create a handle for one layer shape, set weights, run forward.
+ *
+ * Conventions for every call:
+ *  - Every function returns a prnn_status_t; nothing throws, nothing aborts.
+ *  - Matrices are row-major, y = W x (W is [rows][columns]).
+ *  - Sequences are time-major: x[T][B][I], y[T][B][H]; h0 is [B][H].
+ *  - x, h0 and y are fp32.  Weights are fp32 or fp16 (IEEE binary16 bits
+ *    passed as uint16_t); the bias is fp32; column indices are uint16_t.
+ *  - A "stream" is a cudaStream_t passed as void*; NULL means the legacy
+ *    default stream.
+ *  - The library owns everything it allocates (packed weights, workspaces,
+ *    the status word); the caller owns every pointer it passes in.
+ */
+#ifndef PRNN_H
+#define PRNN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct prnn_handle* prnn_t;
+
+typedef enum {
+  PRNN_OK = 0,
+  PRNN_ERR_INVALID_ARG = 1,  /* bad pointer, size, index set, alignment or aliasing */
+  PRNN_ERR_UNSUPPORTED = 2,  /* layer does not fit on chip, or no usable GPU        */
+  PRNN_ERR_NOT_READY = 3,    /* forward before weights were set                     */
+  PRNN_ERR_CUDA = 4,         /* a CUDA runtime call failed                          */
+  PRNN_ERR_OOM = 5,          /* device allocation failed                            */
+  PRNN_ERR_TIMEOUT = 6       /* a step wait in the persistent kernel ran out (sticky) */
+} prnn_status_t;
+
+typedef enum { PRNN_F32 = 0, PRNN_F16 = 1 } prnn_dtype_t;
+
+typedef enum {
+  PRNN_ALGO_PERSISTENT = 0,  /* one persistent launch for all T steps, Wh on chip      */
+  PRNN_ALGO_PER_STEP = 1     /* T launches (one CUDA graph), Wh re-read every step      */
+} prnn_algo_t;
+
+/* Tunables and test hooks for prnn_set_option(). */
+typedef enum {
+  PRNN_OPT_WAIT_TIMEOUT_US = 0,   /* limit of one step wait, microseconds (default 500000)    */
+  PRNN_OPT_SYNC_MODE = 1,         /* 0: flags carried in the data (default); 1: grid barrier  */
+  PRNN_OPT_DEBUG_DROP_CTA = 2,    /* fault hook: CTA that skips one publish (-1 = off)         */
+  PRNN_OPT_DEBUG_DROP_STEP = 3,   /* fault hook: the step whose publish it skips               */
+  PRNN_OPT_TIMING = 4,            /* 1: record CUDA events around each stage of forward        */
+  PRNN_OPT_PROJECTION = 5         /* 0: tensor cores when possible (default); 1: fp32 CUDA cores */
+} prnn_option_t;
+
+/* Plan and sizes chosen at create / set_weights time (read-only report). */
+typedef struct {
+  int hidden, input, max_batch;
+  int wdtype, algo, sparse, weights_set;
+  int k, k_padded;                 /* sparse: non-zeros per row, and per row after padding  */
+  int sm_count, n_cta, rows_per_cta, threads_per_cta, threads_per_row;
+  int projection_tensor_cores;     /* 1 if forward uses the tcgen05 projection               */
+  size_t smem_bytes;               /* dynamic shared memory per CTA at max_batch             */
+  size_t onchip_weight_bytes;      /* packed Wh bytes held on chip, all CTAs                 */
+  size_t nnz;                      /* non-zeros of Wh (H*H when dense)                       */
+} prnn_info_t;
+
+/*
+ * Create a handle for one layer shape on the current CUDA device.
+ *   hidden    H >= 1, input I >= 1, 1 <= max_batch <= 32: upper bound of B in
+ *             forward (the library targets the small-batch regime).
+ *   wdtype    storage type of Wx and Wh.
+ *   algo      PRNN_ALGO_PERSISTENT or PRNN_ALGO_PER_STEP.
+ * Returns PRNN_ERR_UNSUPPORTED when the device is not sm_103 / lacks
+ * cooperative launch, or when the dense layer cannot fit on chip (the
+ * persistent-rnn page's "limits on how large a layer can be").  *out is NULL
+ * on failure.
+ */
+prnn_status_t prnn_create(prnn_t* out, int hidden, int input, int max_batch,
+                          prnn_dtype_t wdtype, prnn_algo_t algo);
+
+/*
+ * Set dense weights.  Wx [H][I] and Wh [H][H] in the handle's wdtype, bias [H]
+ * fp32.  Pointers may be device, managed or host memory.  The library copies
+ * and repacks them and synchronizes `stream` before returning, so the caller
+ * may free its buffers on return.
+ */
+prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
+                                     const float* bias, void* stream);
+
+/*
+ * Set row-balanced sparse recurrent weights: every row r holds exactly k
+ * non-zeros, vals[r][j] (fp16 bits) at column cols[r][j].  Columns must lie in
+ * [0, H) and be distinct within a row (any order); H <= 65535, 0 < k <= H,
+ * handle wdtype PRNN_F16.  Wx [H][I] fp16 and bias [H] as for the dense call.
+ * Invalid index sets give PRNN_ERR_INVALID_ARG and leave the handle unchanged.
+ */
+prnn_status_t prnn_set_weights_sparse(prnn_t h, const void* Wx, int k,
+                                      const uint16_t* vals, const uint16_t* cols,
+                                      const float* bias, void* stream);
+
+/*
+ * Forward pass: y[t] = h_t for t < T.  x [T][B][I], h0 [B][H] (NULL = zeros),
+ * y [T][B][H], all fp32 DEVICE pointers, 16-byte aligned; y must not overlap
+ * x or h0.  1 <= B <= max_batch; T == 0 or B == 0 is a no-op.  Asynchronous
+ * on `stream`.  y is fully overwritten.  If a step wait times out, y is
+ * undefined and this and every later call on the handle return
+ * PRNN_ERR_TIMEOUT (see prnn_get_status).
+ */
+prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* h0,
+                           float* y, void* stream);
+
+/* Release everything the handle owns.  NULL is accepted. */
+prnn_status_t prnn_destroy(prnn_t h);
+
+/* Synchronize `stream` and report the device-side status of past forwards
+ * (PRNN_ERR_TIMEOUT once a step wait has run out; sticky). */
+prnn_status_t prnn_get_status(prnn_t h, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* prnn_status_string(prnn_status_t s);
+
+prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value);
+prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info);
+
+/*
+ * Stage times of the most recent forward, in milliseconds, measured with CUDA
+ * events on the forward's stream (PRNN_OPT_TIMING must be 1).  Synchronizes.
+ * ms_projection covers input staging + projection; ms_recurrence covers the
+ * recurrent kernel (or the T per-step launches).  Either pointer may be NULL.
+ */
+prnn_status_t prnn_get_timing(prnn_t h, float* ms_projection, float* ms_recurrence);
+
+/*
+ * Step-synchronisation floor: runs the persistent grid of this handle for T
+ * steps doing only the step-to-step exchange (every CTA waits for all of
+ * h_{t-1}, then publishes its rows of h_t) with no arithmetic, so its time per
+ * step is the latency floor of the recurrent kernel.  y [T][B][H] fp32 device
+ * scratch.  Its time is reported by prnn_get_timing as ms_recurrence.
+ */
+prnn_status_t prnn_probe_sync_floor(prnn_t h, int T, int B, float* y, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PRNN_H */

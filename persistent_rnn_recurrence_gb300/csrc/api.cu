@@ -1,0 +1,684 @@
+// api.cu -- the C ABI of libprnn.so: handle, validation, planning, weight
+// packing, forward orchestration, status and timing.  Declarations and the
+// contract of every call are in include/prnn.h.
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "prnn.h"
+#include "prnn_internal.h"
+
+using namespace prnn;
+
+namespace {
+
+constexpr int kMaxBatch = 32;
+constexpr int kSparseMaxThreads = 512;
+constexpr int kDenseMaxThreads = 256;
+
+}  // namespace
+
+struct prnn_handle {
+  int H = 0, I = 0, maxB = 0;
+  prnn_dtype_t wdtype = PRNN_F32;
+  prnn_algo_t algo = PRNN_ALGO_PERSISTENT;
+  int device = 0, sm_count = 0;
+  size_t smem_optin = 0;
+  bool weights_set = false, sparse = false;
+  int k = 0;
+  // persistent plan
+  int n_cta = 0, R = 0, nthreads = 0, cpt = 0, tpr = 0, kp = 0, ept = 0;
+  size_t onchip_bytes = 0, smem_at_max = 0;
+  bool tc_proj = false;
+  int Kp = 0;  // I rounded up to 64 (tcgen05 projection)
+  // device buffers owned by the handle
+  void* Wx = nullptr;        // [H][I] in wdtype
+  __half_raw* Wx16 = nullptr;  // [H][Kp] fp16, zero padded (tcgen05 projection)
+  float* bias = nullptr;
+  void* Wpk = nullptr;       // persistent packed recurrent weights
+  void* Wstep = nullptr;     // per-step layout of the recurrent weights
+  float* P = nullptr;
+  size_t P_cap = 0;
+  __half_raw* x16 = nullptr;
+  size_t x16_cap = 0;
+  int* status = nullptr;     // device int[4]
+  unsigned* bar = nullptr;   // grid-barrier counter
+  // options
+  long long timeout_us = 500000;
+  int sync_mode = 0, drop_cta = -1, drop_step = -1, timing = 0, proj_mode = 0;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  bool ev_valid = false;
+  bool sticky_timeout = false;
+  // per-step graph cache
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t gexec = nullptr;
+  int g_T = -1, g_B = -1;
+  const void *g_h0 = nullptr, *g_y = nullptr, *g_P = nullptr, *g_W = nullptr;
+};
+
+namespace {
+
+prnn_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PRNN_OK;
+  if (e == cudaErrorMemoryAllocation) return PRNN_ERR_OOM;
+  if (e == cudaErrorCooperativeLaunchTooLarge) return PRNN_ERR_UNSUPPORTED;
+  return PRNN_ERR_CUDA;
+}
+
+#define PRNN_TRY(expr)                                  \
+  do {                                                  \
+    cudaError_t e_ = (expr);                            \
+    if (e_ != cudaSuccess) return cuda_status(e_);      \
+  } while (0)
+
+template <typename T>
+void free_dev(T*& p) {
+  if (p) cudaFree((void*)p);
+  p = nullptr;
+}
+
+// Copy n bytes from any CUDA-readable pointer (device, managed, host) to host.
+cudaError_t to_host(void* dst, const void* src, size_t n) {
+  return cudaMemcpy(dst, src, n, cudaMemcpyDefault);
+}
+
+template <typename T>
+cudaError_t upload(T** dptr, const void* src, size_t bytes) {
+  T* p = nullptr;
+  cudaError_t e = cudaMalloc((void**)&p, bytes ? bytes : 16);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpy(p, src, bytes, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(p);
+    return e;
+  }
+  *dptr = p;
+  return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const char* pa = static_cast<const char*>(a);
+  const char* pb = static_cast<const char*>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+// ---- planning ----------------------------------------------------------
+struct DensePlan {
+  int R, n_cta, nthreads, cpt;
+  size_t smem;
+  bool ok;
+};
+
+DensePlan plan_dense(const prnn_handle* h) {
+  DensePlan p{};
+  const int H = h->H;
+  p.R = (H + h->sm_count - 1) / h->sm_count;
+  p.n_cta = (H + p.R - 1) / p.R;
+  const int nchunks = H / 4;
+  p.nthreads = std::min(kDenseMaxThreads, std::max(32, round_up(nchunks, 32)));
+  p.cpt = (nchunks + p.nthreads - 1) / p.nthreads;
+  p.ok = (H % 4 == 0) && recur_dense_rmax(p.R) != 0 && p.cpt <= 4;
+  p.smem = p.ok ? recur_dense_smem(p.R, p.cpt, p.nthreads, h->wdtype == PRNN_F16) : 0;
+  p.ok = p.ok && p.smem <= h->smem_optin;
+  return p;
+}
+
+struct SparsePlan {
+  int R, n_cta, tpr, kp, ept, nthreads;
+  bool ok;
+};
+
+SparsePlan plan_sparse(const prnn_handle* h, int k) {
+  SparsePlan p{};
+  const int H = h->H;
+  p.R = (H + h->sm_count - 1) / h->sm_count;
+  p.n_cta = (H + p.R - 1) / p.R;
+  // threads per row: the widest split whose padding stays under ~15 % and
+  // whose R * tpr threads fit one CTA; else the least padding that fits.
+  int best = -1;
+  double best_waste = 1e30;
+  for (int t = 32; t >= 1; t >>= 1) {
+    if (p.R * t > kSparseMaxThreads) continue;
+    const int kp = round_up(k, 4 * t);
+    const double waste = (double)kp / k;
+    if (waste <= 1.15) {
+      best = t;
+      break;
+    }
+    if (waste < best_waste) {
+      best_waste = waste;
+      best = t;
+    }
+  }
+  p.ok = best > 0 && H % 4 == 0;
+  if (!p.ok) return p;
+  p.tpr = best;
+  p.kp = round_up(k, 4 * best);
+  p.ept = p.kp / best;
+  p.nthreads = std::min(kSparseMaxThreads, std::max(256, round_up(p.R * best, 32)));
+  return p;
+}
+
+// Batch group and staging buffers of the sparse kernel for a given B.
+bool sparse_batch_plan(const prnn_handle* h, int B, int* bgroup, bool* dbuf, size_t* smem) {
+  int want = 4;
+  while (want < B && want < 32) want *= 2;
+  for (int bg = want; bg >= 4; bg /= 2) {
+    for (int db = 1; db >= 0; --db) {
+      const size_t s = recur_sparse_smem(h->H, h->R, h->ept, h->tpr, bg, db == 1);
+      if (s <= h->smem_optin) {
+        *bgroup = bg;
+        *dbuf = db == 1;
+        *smem = s;
+        return true;
+      }
+    }
+  }
+  return false;
+}
+
+void invalidate_graph(prnn_handle* h) {
+  if (h->gexec) cudaGraphExecDestroy(h->gexec);
+  h->gexec = nullptr;
+  h->g_T = h->g_B = -1;
+}
+
+cudaError_t ensure_P(prnn_handle* h, size_t n) {
+  if (n <= h->P_cap) return cudaSuccess;
+  invalidate_graph(h);
+  free_dev(h->P);
+  cudaError_t e = cudaMalloc((void**)&h->P, n * sizeof(float));
+  if (e != cudaSuccess) {
+    h->P_cap = 0;
+    return e;
+  }
+  h->P_cap = n;
+  return cudaSuccess;
+}
+
+cudaError_t ensure_x16(prnn_handle* h, size_t n) {
+  if (n <= h->x16_cap) return cudaSuccess;
+  free_dev(h->x16);
+  cudaError_t e = cudaMalloc((void**)&h->x16, n * sizeof(__half_raw));
+  if (e != cudaSuccess) {
+    h->x16_cap = 0;
+    return e;
+  }
+  h->x16_cap = n;
+  return cudaSuccess;
+}
+
+// Wx in the handle's dtype ([H][I]) plus, for fp16, a [H][Kp] zero-padded
+// copy for the tensor-core projection.  Host vectors in, device buffers out.
+prnn_status_t stage_wx_bias(prnn_handle* h, const void* Wx, const float* bias,
+                            void** dWx, __half_raw** dWx16, float** dbias) {
+  const size_t esz = h->wdtype == PRNN_F16 ? 2 : 4;
+  std::vector<unsigned char> wx((size_t)h->H * h->I * esz);
+  std::vector<float> b((size_t)h->H);
+  PRNN_TRY(to_host(wx.data(), Wx, wx.size()));
+  PRNN_TRY(to_host(b.data(), bias, b.size() * sizeof(float)));
+  PRNN_TRY(upload(dWx, wx.data(), wx.size()));
+  PRNN_TRY(upload(dbias, b.data(), b.size() * sizeof(float)));
+  if (h->wdtype == PRNN_F16) {
+    std::vector<uint16_t> w16((size_t)h->H * h->Kp, 0);
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(wx.data());
+    for (int r = 0; r < h->H; ++r)
+      std::memcpy(&w16[(size_t)r * h->Kp], src + (size_t)r * h->I, (size_t)h->I * 2);
+    PRNN_TRY(upload(dWx16, w16.data(), w16.size() * 2));
+  }
+  return PRNN_OK;
+}
+
+void free_weights(prnn_handle* h) {
+  invalidate_graph(h);
+  free_dev(h->Wx);
+  free_dev(h->Wx16);
+  free_dev(h->bias);
+  free_dev(h->Wpk);
+  free_dev(h->Wstep);
+  h->weights_set = false;
+}
+
+RecurCommon common_args(const prnn_handle* h, int T, int B, const float* h0, float* y) {
+  RecurCommon c{};
+  c.T = T;
+  c.B = B;
+  c.H = h->H;
+  c.n_cta = h->n_cta;
+  c.R = h->R;
+  c.nthreads = h->nthreads;
+  c.P = h->P;
+  c.h0 = h0;
+  c.y = y;
+  c.status = h->status;
+  c.timeout_ns = h->timeout_us * 1000LL;
+  c.sync_mode = h->sync_mode;
+  c.bar = h->bar;
+  c.drop_cta = h->drop_cta;
+  c.drop_step = h->drop_step;
+  return c;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* prnn_status_string(prnn_status_t s) {
+  switch (s) {
+    case PRNN_OK: return "PRNN_OK";
+    case PRNN_ERR_INVALID_ARG: return "PRNN_ERR_INVALID_ARG";
+    case PRNN_ERR_UNSUPPORTED: return "PRNN_ERR_UNSUPPORTED";
+    case PRNN_ERR_NOT_READY: return "PRNN_ERR_NOT_READY";
+    case PRNN_ERR_CUDA: return "PRNN_ERR_CUDA";
+    case PRNN_ERR_OOM: return "PRNN_ERR_OOM";
+    case PRNN_ERR_TIMEOUT: return "PRNN_ERR_TIMEOUT";
+  }
+  return "PRNN_ERR_UNKNOWN";
+}
+
+prnn_status_t prnn_create(prnn_t* out, int hidden, int input, int max_batch,
+                          prnn_dtype_t wdtype, prnn_algo_t algo) {
+  if (!out) return PRNN_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (hidden < 1 || input < 1 || max_batch < 1 || max_batch > kMaxBatch)
+    return PRNN_ERR_INVALID_ARG;
+  if (wdtype != PRNN_F32 && wdtype != PRNN_F16) return PRNN_ERR_INVALID_ARG;
+  if (algo != PRNN_ALGO_PERSISTENT && algo != PRNN_ALGO_PER_STEP) return PRNN_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PRNN_ERR_UNSUPPORTED;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return PRNN_ERR_UNSUPPORTED;
+  if (prop.major != 10 || prop.minor != 3) return PRNN_ERR_UNSUPPORTED;  // built for sm_103a
+  if (!prop.cooperativeLaunch) return PRNN_ERR_UNSUPPORTED;
+  prnn_handle* h = new (std::nothrow) prnn_handle();
+  if (!h) return PRNN_ERR_OOM;
+  h->H = hidden;
+  h->I = input;
+  h->maxB = max_batch;
+  h->wdtype = wdtype;
+  h->algo = algo;
+  h->device = dev;
+  h->sm_count = prop.multiProcessorCount;
+  h->smem_optin = prop.sharedMemPerBlockOptin;
+  h->Kp = round_up(input, 64);
+  prnn_status_t st = PRNN_OK;
+  if (cudaMalloc((void**)&h->status, 4 * sizeof(int)) != cudaSuccess ||
+      cudaMalloc((void**)&h->bar, sizeof(unsigned)) != cudaSuccess ||
+      cudaMemset(h->status, 0, 4 * sizeof(int)) != cudaSuccess ||
+      cudaMemset(h->bar, 0, sizeof(unsigned)) != cudaSuccess)
+    st = PRNN_ERR_OOM;
+  for (int i = 0; i < 3 && st == PRNN_OK; ++i)
+    if (cudaEventCreate(&h->ev[i]) != cudaSuccess) st = PRNN_ERR_CUDA;
+  if (st == PRNN_OK &&
+      cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
+    st = PRNN_ERR_CUDA;
+  if (st != PRNN_OK) {
+    prnn_destroy(h);
+    return st;
+  }
+  *out = h;
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_destroy(prnn_t h) {
+  if (!h) return PRNN_OK;
+  cudaSetDevice(h->device);
+  free_weights(h);
+  free_dev(h->P);
+  free_dev(h->x16);
+  free_dev(h->status);
+  free_dev(h->bar);
+  for (auto& e : h->ev)
+    if (e) cudaEventDestroy(e);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  delete h;
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
+                                     const float* bias, void* stream) {
+  if (!h || !Wx || !Wh || !bias) return PRNN_ERR_INVALID_ARG;
+  if (h->sticky_timeout) return PRNN_ERR_TIMEOUT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PRNN_TRY(cudaStreamSynchronize(s));
+  const int H = h->H;
+  const size_t esz = h->wdtype == PRNN_F16 ? 2 : 4;
+  DensePlan plan{};
+  if (h->algo == PRNN_ALGO_PERSISTENT) {
+    plan = plan_dense(h);
+    if (!plan.ok) return PRNN_ERR_UNSUPPORTED;
+  }
+  std::vector<unsigned char> wh((size_t)H * H * esz);
+  PRNN_TRY(to_host(wh.data(), Wh, wh.size()));
+
+  free_weights(h);
+  prnn_status_t st = stage_wx_bias(h, Wx, bias, &h->Wx, &h->Wx16, &h->bias);
+  if (st != PRNN_OK) return st;
+  if (h->algo == PRNN_ALGO_PERSISTENT) {
+    // per CTA: [chunk slot j][row r][thread i] -> 4 weights of row cta*R+r,
+    // columns 4*(i + j*nthreads) .. +3 (zero outside the matrix)
+    const int NT = plan.nthreads, nchunks = H / 4;
+    const size_t vec = 4 * esz;
+    std::vector<unsigned char> pk((size_t)plan.n_cta * plan.cpt * plan.R * NT * vec, 0);
+    for (int cta = 0; cta < plan.n_cta; ++cta)
+      for (int j = 0; j < plan.cpt; ++j)
+        for (int r = 0; r < plan.R; ++r)
+          for (int i = 0; i < NT; ++i) {
+            const int row = cta * plan.R + r, ch = i + j * NT;
+            if (row >= H || ch >= nchunks) continue;
+            const size_t dst = ((((size_t)cta * plan.cpt + j) * plan.R + r) * NT + i) * vec;
+            std::memcpy(&pk[dst], &wh[((size_t)row * H + (size_t)ch * 4) * esz], vec);
+          }
+    PRNN_TRY(upload(&h->Wpk, pk.data(), pk.size()));
+    h->n_cta = plan.n_cta;
+    h->R = plan.R;
+    h->nthreads = plan.nthreads;
+    h->cpt = plan.cpt;
+    h->smem_at_max = plan.smem;
+    h->onchip_bytes = pk.size();
+  } else {
+    PRNN_TRY(upload(&h->Wstep, wh.data(), wh.size()));
+    h->onchip_bytes = 0;
+  }
+  h->sparse = false;
+  h->k = H;
+  h->tc_proj = false;
+  h->weights_set = true;
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_set_weights_sparse(prnn_t h, const void* Wx, int k, const uint16_t* vals,
+                                      const uint16_t* cols, const float* bias, void* stream) {
+  if (!h || !Wx || !vals || !cols || !bias) return PRNN_ERR_INVALID_ARG;
+  if (h->sticky_timeout) return PRNN_ERR_TIMEOUT;
+  if (h->wdtype != PRNN_F16) return PRNN_ERR_INVALID_ARG;
+  const int H = h->H;
+  if (H > 65535 || k < 1 || k > H) return PRNN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PRNN_TRY(cudaStreamSynchronize(s));
+  std::vector<uint16_t> hv((size_t)H * k), hc((size_t)H * k);
+  PRNN_TRY(to_host(hv.data(), vals, hv.size() * 2));
+  PRNN_TRY(to_host(hc.data(), cols, hc.size() * 2));
+  // validate: columns in range, distinct within each row; sort each row by column
+  std::vector<int> seen((size_t)H, -1);
+  std::vector<std::pair<uint16_t, uint16_t>> row(k);
+  for (int r = 0; r < H; ++r) {
+    for (int j = 0; j < k; ++j) {
+      const int c = hc[(size_t)r * k + j];
+      if (c >= H || seen[c] == r) return PRNN_ERR_INVALID_ARG;
+      seen[c] = r;
+      row[j] = {hc[(size_t)r * k + j], hv[(size_t)r * k + j]};
+    }
+    std::sort(row.begin(), row.end(),
+              [](const std::pair<uint16_t, uint16_t>& a, const std::pair<uint16_t, uint16_t>& b) {
+                return a.first < b.first;
+              });
+    for (int j = 0; j < k; ++j) {
+      hc[(size_t)r * k + j] = row[j].first;
+      hv[(size_t)r * k + j] = row[j].second;
+    }
+  }
+  SparsePlan plan{};
+  if (h->algo == PRNN_ALGO_PERSISTENT) {
+    plan = plan_sparse(h, k);
+    if (!plan.ok) return PRNN_ERR_UNSUPPORTED;
+    // check that at least the smallest batch group fits
+    const size_t s4 = recur_sparse_smem(H, plan.R, plan.ept, plan.tpr, 4, false);
+    if (s4 > h->smem_optin) return PRNN_ERR_UNSUPPORTED;
+  }
+  free_weights(h);
+  prnn_status_t st = stage_wx_bias(h, Wx, bias, &h->Wx, &h->Wx16, &h->bias);
+  if (st != PRNN_OK) return st;
+  auto entry = [&](int r, int j) -> uint32_t {
+    return (uint32_t)hv[(size_t)r * k + j] | ((uint32_t)hc[(size_t)r * k + j] << 16);
+  };
+  if (h->algo == PRNN_ALGO_PERSISTENT) {
+    // per CTA: [row r][group q][thread seg s] uint4; thread s of row r owns
+    // the entries s*ept .. s*ept+ept-1 of the row (sorted by column), padding
+    // entries (j >= k) have value 0 and the row's last column.
+    const int q4 = plan.ept / 4;
+    std::vector<uint32_t> pk((size_t)plan.n_cta * plan.R * plan.kp, 0);
+    for (int cta = 0; cta < plan.n_cta; ++cta)
+      for (int r = 0; r < plan.R; ++r) {
+        const int grow = cta * plan.R + r;
+        for (int sg = 0; sg < plan.tpr; ++sg)
+          for (int q = 0; q < q4; ++q)
+            for (int w = 0; w < 4; ++w) {
+              const int j = sg * plan.ept + q * 4 + w;
+              uint32_t e = 0;
+              if (grow < H) e = j < k ? entry(grow, j) : ((uint32_t)hc[(size_t)grow * k + k - 1] << 16);
+              const size_t dst = ((((size_t)cta * plan.R + r) * q4 + q) * plan.tpr + sg) * 4 + w;
+              pk[dst] = e;
+            }
+      }
+    PRNN_TRY(upload(&h->Wpk, pk.data(), pk.size() * 4));
+    h->n_cta = plan.n_cta;
+    h->R = plan.R;
+    h->nthreads = plan.nthreads;
+    h->tpr = plan.tpr;
+    h->kp = plan.kp;
+    h->ept = plan.ept;
+    h->onchip_bytes = (size_t)H * plan.kp * 4;
+    int bg = 4;
+    bool db = false;
+    size_t sm = 0;
+    sparse_batch_plan(h, h->maxB, &bg, &db, &sm);
+    h->smem_at_max = sm;
+  } else {
+    std::vector<uint32_t> ws((size_t)H * k);
+    for (int r = 0; r < H; ++r)
+      for (int j = 0; j < k; ++j) ws[(size_t)r * k + j] = entry(r, j);
+    PRNN_TRY(upload(&h->Wstep, ws.data(), ws.size() * 4));
+    h->onchip_bytes = 0;
+    h->kp = k;
+  }
+  h->sparse = true;
+  h->k = k;
+  h->tc_proj = false;
+  h->weights_set = true;
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* h0, float* y,
+                           void* stream) {
+  if (!h) return PRNN_ERR_INVALID_ARG;
+  if (h->sticky_timeout) return PRNN_ERR_TIMEOUT;
+  if (!h->weights_set) return PRNN_ERR_NOT_READY;
+  if (T < 0 || B < 0 || B > h->maxB) return PRNN_ERR_INVALID_ARG;
+  if (T == 0 || B == 0) return PRNN_OK;
+  if (!x || !y) return PRNN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || (h0 && !aligned16(h0))) return PRNN_ERR_INVALID_ARG;
+  const size_t ny = (size_t)T * B * h->H;
+  if (overlaps(y, ny * 4, x, (size_t)T * B * h->I * 4)) return PRNN_ERR_INVALID_ARG;
+  if (h0 && overlaps(y, ny * 4, h0, (size_t)B * h->H * 4)) return PRNN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PRNN_TRY(ensure_P(h, ny));
+  const bool persistent = h->algo == PRNN_ALGO_PERSISTENT;
+  if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[0], s));
+
+  // 1. projection for all steps (+ sentinel fill of y on the persistent path)
+  ProjArgs pa{T * B, h->H, h->I, x, h->Wx, h->bias, h->P, persistent ? y : nullptr};
+  PRNN_TRY(launch_projection_simt(pa, h->wdtype == PRNN_F16, s));
+  if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[1], s));
+
+  // 2. recurrence
+  if (persistent) {
+    RecurCommon c = common_args(h, T, B, h0, y);
+    if (h->sync_mode == 1) PRNN_TRY(cudaMemsetAsync(h->bar, 0, sizeof(unsigned), s));
+    if (h->sparse) {
+      SparseRecurArgs a{};
+      int bg = 4;
+      bool db = false;
+      size_t sm = 0;
+      if (!sparse_batch_plan(h, B, &bg, &db, &sm)) return PRNN_ERR_UNSUPPORTED;
+      c.smem = sm;
+      a.c = c;
+      a.Wpk = static_cast<const uint32_t*>(h->Wpk);
+      a.tpr = h->tpr;
+      a.ept = h->ept;
+      a.bgroup = bg;
+      a.dbuf = db ? 1 : 0;
+      PRNN_TRY(launch_recur_sparse(a, s));
+    } else {
+      DenseRecurArgs a{};
+      c.smem = h->smem_at_max;
+      a.c = c;
+      a.Wpk = h->Wpk;
+      a.cpt = h->cpt;
+      a.wfp16 = h->wdtype == PRNN_F16;
+      PRNN_TRY(launch_recur_dense(a, s));
+    }
+  } else {
+    const bool hit = h->gexec && h->g_T == T && h->g_B == B && h->g_h0 == h0 && h->g_y == y &&
+                     h->g_P == h->P && h->g_W == h->Wstep;
+    if (!hit) {
+      invalidate_graph(h);
+      PRNN_TRY(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+      cudaError_t e = cudaSuccess;
+      for (int t = 0; t < T && e == cudaSuccess; ++t) {
+        StepArgs sa{};
+        sa.t = t;
+        sa.B = B;
+        sa.H = h->H;
+        sa.P = h->P;
+        sa.hprev = t == 0 ? h0 : y + (size_t)(t - 1) * B * h->H;
+        sa.y = y;
+        sa.W = h->Wstep;
+        sa.wfp16 = h->wdtype == PRNN_F16;
+        sa.sparse = h->sparse;
+        sa.kp = h->kp;
+        e = launch_step(sa, h->cap_stream);
+      }
+      cudaGraph_t g = nullptr;
+      cudaError_t e2 = cudaStreamEndCapture(h->cap_stream, &g);
+      if (e == cudaSuccess) e = e2;
+      if (e == cudaSuccess) e = cudaGraphInstantiate(&h->gexec, g, 0);
+      if (g) cudaGraphDestroy(g);
+      if (e != cudaSuccess) {
+        h->gexec = nullptr;
+        return cuda_status(e);
+      }
+      h->g_T = T;
+      h->g_B = B;
+      h->g_h0 = h0;
+      h->g_y = y;
+      h->g_P = h->P;
+      h->g_W = h->Wstep;
+    }
+    PRNN_TRY(cudaGraphLaunch(h->gexec, s));
+  }
+  if (h->timing) {
+    PRNN_TRY(cudaEventRecord(h->ev[2], s));
+    h->ev_valid = true;
+  }
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_get_status(prnn_t h, void* stream) {
+  if (!h) return PRNN_ERR_INVALID_ARG;
+  PRNN_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  int st[4] = {0, 0, 0, 0};
+  PRNN_TRY(cudaMemcpy(st, h->status, sizeof(st), cudaMemcpyDeviceToHost));
+  if (st[0] != 0) h->sticky_timeout = true;
+  return h->sticky_timeout ? PRNN_ERR_TIMEOUT : PRNN_OK;
+}
+
+prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
+  if (!h) return PRNN_ERR_INVALID_ARG;
+  switch (opt) {
+    case PRNN_OPT_WAIT_TIMEOUT_US:
+      if (value < 1 || value > 60LL * 1000 * 1000) return PRNN_ERR_INVALID_ARG;
+      h->timeout_us = value;
+      return PRNN_OK;
+    case PRNN_OPT_SYNC_MODE:
+      if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
+      h->sync_mode = (int)value;
+      return PRNN_OK;
+    case PRNN_OPT_DEBUG_DROP_CTA:
+      if (value < -1 || value > 1 << 20) return PRNN_ERR_INVALID_ARG;
+      h->drop_cta = (int)value;
+      return PRNN_OK;
+    case PRNN_OPT_DEBUG_DROP_STEP:
+      if (value < -1 || value > 1 << 30) return PRNN_ERR_INVALID_ARG;
+      h->drop_step = (int)value;
+      return PRNN_OK;
+    case PRNN_OPT_TIMING:
+      if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
+      h->timing = (int)value;
+      h->ev_valid = false;
+      return PRNN_OK;
+    case PRNN_OPT_PROJECTION:
+      if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
+      h->proj_mode = (int)value;
+      return PRNN_OK;
+  }
+  return PRNN_ERR_INVALID_ARG;
+}
+
+prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
+  if (!h || !info) return PRNN_ERR_INVALID_ARG;
+  std::memset(info, 0, sizeof(*info));
+  info->hidden = h->H;
+  info->input = h->I;
+  info->max_batch = h->maxB;
+  info->wdtype = h->wdtype;
+  info->algo = h->algo;
+  info->sparse = h->sparse;
+  info->weights_set = h->weights_set;
+  info->k = h->k;
+  info->k_padded = h->sparse ? h->kp : h->H;
+  info->sm_count = h->sm_count;
+  info->n_cta = h->n_cta;
+  info->rows_per_cta = h->R;
+  info->threads_per_cta = h->nthreads;
+  info->threads_per_row = h->tpr;
+  info->projection_tensor_cores = h->tc_proj;
+  info->smem_bytes = h->smem_at_max;
+  info->onchip_weight_bytes = h->onchip_bytes;
+  info->nnz = h->sparse ? (size_t)h->H * h->k : (size_t)h->H * h->H;
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_get_timing(prnn_t h, float* ms_projection, float* ms_recurrence) {
+  if (!h) return PRNN_ERR_INVALID_ARG;
+  if (!h->timing || !h->ev_valid) return PRNN_ERR_NOT_READY;
+  PRNN_TRY(cudaEventSynchronize(h->ev[2]));
+  float a = 0.f, b = 0.f;
+  PRNN_TRY(cudaEventElapsedTime(&a, h->ev[0], h->ev[1]));
+  PRNN_TRY(cudaEventElapsedTime(&b, h->ev[1], h->ev[2]));
+  if (ms_projection) *ms_projection = a;
+  if (ms_recurrence) *ms_recurrence = b;
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_probe_sync_floor(prnn_t h, int T, int B, float* y, void* stream) {
+  if (!h) return PRNN_ERR_INVALID_ARG;
+  if (h->sticky_timeout) return PRNN_ERR_TIMEOUT;
+  if (!h->weights_set || h->algo != PRNN_ALGO_PERSISTENT) return PRNN_ERR_NOT_READY;
+  if (T < 0 || B < 0 || B > h->maxB) return PRNN_ERR_INVALID_ARG;
+  if (T == 0 || B == 0) return PRNN_OK;
+  if (!y || !aligned16(y)) return PRNN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int bg = std::min(32, std::max(4, round_up(B, 4)));
+  RecurCommon c = common_args(h, T, B, nullptr, y);
+  c.smem = sync_probe_smem(h->H, bg);
+  if (c.smem > h->smem_optin) return PRNN_ERR_UNSUPPORTED;
+  if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[0], s));
+  PRNN_TRY(launch_fill_sentinel(y, (size_t)T * B * h->H, s));
+  if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[1], s));
+  PRNN_TRY(launch_sync_probe(c, bg, s));
+  if (h->timing) {
+    PRNN_TRY(cudaEventRecord(h->ev[2], s));
+    h->ev_valid = true;
+  }
+  return PRNN_OK;
+}
+
+}  // extern "C"

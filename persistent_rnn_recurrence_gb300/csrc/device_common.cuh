@@ -1,0 +1,128 @@
+// device_common.cuh -- device helpers shared by the recurrent kernels:
+// coherent (L1-bypassing) loads and stores of step data, the "not yet written"
+// sentinel, bounded waiting with an error status, and warp reductions.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace prnn {
+
+// A y word that has not been produced yet holds this bit pattern.  It is a
+// NaN, and the ReLU used here (v > 0 ? v : +0) never returns a NaN, so no
+// published value can be mistaken for it.
+constexpr uint32_t kSentinel = 0xFFFFFFFFu;
+
+// Status words in device memory (one int[4] per handle).
+//   [0] error code (0 = ok, kStatusTimeout), [1] step, [2] CTA, [3] spare.
+constexpr int kStatusTimeout = 6;
+
+__device__ __forceinline__ bool is_sentinel(float v) {
+  return __float_as_uint(v) == kSentinel;
+}
+__device__ __forceinline__ bool ready4(const float4& v) {
+  return !(is_sentinel(v.x) | is_sentinel(v.y) | is_sentinel(v.z) | is_sentinel(v.w));
+}
+
+// Relaxed, gpu-scope accesses: each 32-bit element is single-copy atomic and
+// bypasses the non-coherent L1, so a consumer polling a word eventually sees
+// the producer's store.  The data word itself is the flag.
+__device__ __forceinline__ float4 ld_relaxed_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_relaxed_f(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_f(float* p, float v) {
+  asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ int ld_relaxed_i(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ float relu(float s) { return s > 0.f ? s : 0.f; }
+
+// Record the first failure; later ones keep the first record.
+__device__ __forceinline__ void report_timeout(int* status, int step, int cta) {
+  if (atomicCAS(status, 0, kStatusTimeout) == 0) {
+    status[1] = step;
+    status[2] = cta;
+  }
+}
+
+// Bounded wait state.  `deadline` is absolute globaltimer ns.
+struct Waiter {
+  uint64_t deadline;
+  const int* status;
+  // true = keep waiting; false = give up (deadline passed or another CTA failed)
+  __device__ __forceinline__ bool still_ok(uint32_t& spins) {
+    if ((++spins & 63u) != 0u) return true;
+    if (ld_relaxed_i(status) != 0) return false;
+    return global_ns() < deadline;
+  }
+};
+
+// Poll one float4 of step data until none of its words is the sentinel.
+// Returns false if the wait gave up.
+__device__ __forceinline__ bool poll_f4(const float* p, float4& v, Waiter& w) {
+  uint32_t spins = 0;
+  while (!ready4(v)) {
+    if (!w.still_ok(spins)) return false;
+    v = ld_relaxed_f4(p);
+  }
+  return true;
+}
+__device__ __forceinline__ bool poll_f(const float* p, float& v, Waiter& w) {
+  uint32_t spins = 0;
+  while (is_sentinel(v)) {
+    if (!w.still_ok(spins)) return false;
+    v = ld_relaxed_f(p);
+  }
+  return true;
+}
+
+// Warp reduce-scatter of V partial sums (V a power of two).  On return lane L
+// holds, in v[0 .. max(V/32,1)-1], the warp-wide sums of value indices
+// L*V/32 + i (V >= 32), or of index L / (32/V) (V < 32; replicated across
+// 32/V lanes).  Costs V-1 shuffles for V <= 32.
+template <int V>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[V], int lane) {
+  constexpr unsigned kFull = 0xffffffffu;
+  int n = V;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (n > 1) {
+      const bool upper = (lane & o) != 0;
+      const int h = n >> 1;
+#pragma unroll
+      for (int i = 0; i < V / 2; ++i) {
+        if (i < h) {
+          float send = upper ? v[i] : v[i + h];
+          float keep = upper ? v[i + h] : v[i];
+          v[i] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+      }
+      n = h;
+    } else {
+      v[0] += __shfl_xor_sync(kFull, v[0], o);
+    }
+  }
+}
+
+}  // namespace prnn

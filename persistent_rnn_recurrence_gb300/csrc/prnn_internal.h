@@ -1,0 +1,96 @@
+// prnn_internal.h -- shapes, plans and kernel launchers shared by the
+// translation units of libprnn.so (not part of the public ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace prnn {
+
+// ---- input projection: P[m][n] = bias[n] + sum_k x[m][k] * Wx[n][k] -------
+// m < M = T*B, n < N = H, k < K = I.  Optionally also fills y (same shape as
+// P) with the "not yet written" sentinel.
+struct ProjArgs {
+  int M, N, K;
+  const float* x;      // [M][K] fp32
+  const void* Wx;      // [N][K] fp32 or fp16
+  const float* bias;   // [N]
+  float* P;            // [M][N]
+  float* y_fill;       // [M][N] or nullptr
+};
+cudaError_t launch_projection_simt(const ProjArgs& a, bool wx_fp16, cudaStream_t s);
+
+// tcgen05 projection: x is converted to fp16 into x16 [M][Kp] (Kp = K rounded
+// up to 64, zero padded), Wx16 is [N][Kp] fp16 zero padded.
+struct ProjTcArgs {
+  int M, N, K, Kp;
+  const float* x;        // [M][K] fp32
+  __half_raw* x16;       // [M][Kp] workspace
+  const __half_raw* Wx16;// [N][Kp]
+  const float* bias;     // [N]
+  float* P;              // [M][N]
+  float* y_fill;         // [M][N] or nullptr
+};
+bool projection_tc_supported();
+cudaError_t launch_projection_tc(const ProjTcArgs& a, cudaStream_t s);
+
+// ---- persistent recurrent kernels --------------------------------------
+struct RecurCommon {
+  int T, B, H;
+  int n_cta, R;          // CTAs and rows per CTA (last CTA may own fewer)
+  int nthreads;
+  size_t smem;           // dynamic shared memory bytes
+  const float* P;        // [T][B][H] projection (bias included)
+  const float* h0;       // [B][H] or nullptr
+  float* y;              // [T][B][H], pre-filled with the sentinel
+  int* status;           // int[4]
+  long long timeout_ns;
+  int sync_mode;         // 0 flags in data, 1 grid barrier
+  unsigned* bar;         // grid barrier counter (sync_mode 1)
+  int drop_cta, drop_step;  // fault hook (-1 = off)
+};
+
+// Dense: thread i owns 4-column chunks i, i+nthreads, ...; weights packed as
+// [chunk-slot j][row][thread] vectors of 4 (fp16: 8 bytes, fp32: 16 bytes).
+struct DenseRecurArgs {
+  RecurCommon c;
+  const void* Wpk;       // packed per CTA: n_cta blocks of cpt*R*nthreads vec4
+  int cpt;               // chunk slots per thread = ceil((H/4) / nthreads)
+  int wfp16;
+};
+cudaError_t launch_recur_dense(const DenseRecurArgs& a, cudaStream_t s);
+size_t recur_dense_smem(int R, int cpt, int nthreads, bool fp16);
+int recur_dense_rmax(int R);   // 0 if R unsupported
+
+// Sparse row-balanced: per CTA, R rows x kp entries; thread (row, seg) with
+// seg < tpr owns ept = kp/tpr entries, read as uint4 (4 packed entries).
+// Packed entry = fp16 value bits | (column << 16).
+struct SparseRecurArgs {
+  RecurCommon c;
+  const uint32_t* Wpk;   // [n_cta][R][ept/4][tpr] uint4
+  int tpr, ept;
+  int bgroup;            // batch columns staged per pass: 4, 8, 16 or 32
+  int dbuf;              // 1: two h staging buffers (one CTA barrier per pass)
+};
+cudaError_t launch_recur_sparse(const SparseRecurArgs& a, cudaStream_t s);
+size_t recur_sparse_smem(int H, int R, int ept, int tpr, int bgroup, bool dbuf);
+
+cudaError_t launch_sync_probe(const RecurCommon& c, int bgroup, cudaStream_t s);
+size_t sync_probe_smem(int H, int bgroup);
+
+// ---- per-step path ------------------------------------------------------
+struct StepArgs {
+  int t, B, H;
+  const float* P;        // [T][B][H]
+  const float* hprev;    // [B][H] (h0, or y[t-1])
+  float* y;              // [T][B][H]
+  const void* W;         // dense: [H][H] (fp16 or fp32); sparse: [H][kp] packed
+  int wfp16, sparse, kp;
+};
+cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
+
+cudaError_t launch_fill_sentinel(float* y, size_t n, cudaStream_t s);
+
+}  // namespace prnn

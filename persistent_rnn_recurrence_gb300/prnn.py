@@ -1,0 +1,222 @@
+"""Thin ctypes binding of libprnn.so (declarations in include/prnn.h).
+
+Every function here marshals arguments and calls the C ABI function of the same
+name; every step of the computation runs in the library's CUDA kernels.
+PyTorch only supplies device memory and streams.  Importing this module loads
+the library and raises ImportError if it has not been built -- there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libprnn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      "`python -m persistent_rnn_recurrence_gb300.build`")
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---- enums (mirror include/prnn.h) ------------------------------------------
+PRNN_OK, PRNN_ERR_INVALID_ARG, PRNN_ERR_UNSUPPORTED, PRNN_ERR_NOT_READY, \
+    PRNN_ERR_CUDA, PRNN_ERR_OOM, PRNN_ERR_TIMEOUT = range(7)
+PRNN_F32, PRNN_F16 = 0, 1
+PRNN_ALGO_PERSISTENT, PRNN_ALGO_PER_STEP = 0, 1
+PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA, \
+    PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION = range(6)
+
+EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
+           "prnn_forward", "prnn_destroy", "prnn_get_status", "prnn_status_string",
+           "prnn_set_option", "prnn_get_info", "prnn_get_timing", "prnn_probe_sync_floor"]
+
+
+class prnn_info_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "hidden", "input", "max_batch", "wdtype", "algo", "sparse", "weights_set", "k",
+        "k_padded", "sm_count", "n_cta", "rows_per_cta", "threads_per_cta",
+        "threads_per_row", "projection_tensor_cores")] + [
+        ("smem_bytes", ctypes.c_size_t), ("onchip_weight_bytes", ctypes.c_size_t),
+        ("nnz", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_sig = {
+    "prnn_create": ([ctypes.POINTER(_P), _I, _I, _I, _I, _I], _I),
+    "prnn_set_weights_dense": ([_P, _P, _P, _P, _P], _I),
+    "prnn_set_weights_sparse": ([_P, _P, _I, _P, _P, _P, _P], _I),
+    "prnn_forward": ([_P, _I, _I, _P, _P, _P, _P], _I),
+    "prnn_destroy": ([_P], _I),
+    "prnn_get_status": ([_P, _P], _I),
+    "prnn_status_string": ([_I], ctypes.c_char_p),
+    "prnn_set_option": ([_P, _I, ctypes.c_longlong], _I),
+    "prnn_get_info": ([_P, ctypes.POINTER(prnn_info_t)], _I),
+    "prnn_get_timing": ([_P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)], _I),
+    "prnn_probe_sync_floor": ([_P, _I, _I, _P, _P], _I),
+}
+for _name, (_args, _res) in _sig.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+
+class PrnnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {prnn_status_string(status)}")
+
+
+def prnn_status_string(status: int) -> str:
+    return _lib.prnn_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> int:
+    if status != PRNN_OK:
+        raise PrnnError(status, where)
+    return status
+
+
+def _ptr(t) -> Optional[int]:
+    """Device/host address of a tensor (or None)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---- the C ABI, one Python function per C function ---------------------------
+def prnn_create(hidden: int, input: int, max_batch: int, wdtype: int, algo: int) -> int:
+    h = _P()
+    _check(_lib.prnn_create(ctypes.byref(h), hidden, input, max_batch, wdtype, algo),
+           "prnn_create")
+    return h.value
+
+
+def prnn_set_weights_dense(h: int, Wx, Wh, bias, stream=None) -> None:
+    _check(_lib.prnn_set_weights_dense(h, _ptr(Wx), _ptr(Wh), _ptr(bias), _stream(stream)),
+           "prnn_set_weights_dense")
+
+
+def prnn_set_weights_sparse(h: int, Wx, k: int, vals, cols, bias, stream=None) -> None:
+    _check(_lib.prnn_set_weights_sparse(h, _ptr(Wx), int(k), _ptr(vals), _ptr(cols),
+                                        _ptr(bias), _stream(stream)),
+           "prnn_set_weights_sparse")
+
+
+def prnn_forward(h: int, T: int, B: int, x, h0, y, stream=None) -> None:
+    _check(_lib.prnn_forward(h, T, B, _ptr(x), _ptr(h0), _ptr(y), _stream(stream)),
+           "prnn_forward")
+
+
+def prnn_destroy(h: int) -> None:
+    _check(_lib.prnn_destroy(h), "prnn_destroy")
+
+
+def prnn_get_status(h: int, stream=None) -> int:
+    """Returns the status code (PRNN_OK or PRNN_ERR_TIMEOUT); does not raise
+    for a timeout, so callers can test for it."""
+    return _lib.prnn_get_status(h, _stream(stream))
+
+
+def prnn_set_option(h: int, opt: int, value: int) -> None:
+    _check(_lib.prnn_set_option(h, opt, int(value)), "prnn_set_option")
+
+
+def prnn_get_info(h: int) -> dict:
+    info = prnn_info_t()
+    _check(_lib.prnn_get_info(h, ctypes.byref(info)), "prnn_get_info")
+    return info.as_dict()
+
+
+def prnn_get_timing(h: int):
+    a, b = ctypes.c_float(), ctypes.c_float()
+    _check(_lib.prnn_get_timing(h, ctypes.byref(a), ctypes.byref(b)), "prnn_get_timing")
+    return a.value, b.value
+
+
+def prnn_probe_sync_floor(h: int, T: int, B: int, y, stream=None) -> None:
+    _check(_lib.prnn_probe_sync_floor(h, T, B, _ptr(y), _stream(stream)),
+           "prnn_probe_sync_floor")
+
+
+# ---- convenience wrapper used by the tests and the benchmark ------------------
+class Layer:
+    """One RNN layer handle.  ``Layer.from_problem(p)`` uploads a
+    ``synth.Problem``'s weights (as device tensors) and returns the layer."""
+
+    def __init__(self, hidden, input, max_batch, wdtype="f16", algo="persistent"):
+        self.hidden, self.input, self.max_batch = hidden, input, max_batch
+        wd = {"f32": PRNN_F32, "f16": PRNN_F16}[wdtype]
+        al = {"persistent": PRNN_ALGO_PERSISTENT, "per_step": PRNN_ALGO_PER_STEP}[algo]
+        self.h = prnn_create(hidden, input, max_batch, wd, al)
+
+    @classmethod
+    def from_problem(cls, p, algo="persistent", max_batch=None, device="cuda"):
+        import torch
+        lay = cls(p.H, p.I, max_batch or max(1, p.B), p.wdtype, algo)
+        try:
+            lay.set_problem_weights(p, device)
+        except Exception:
+            lay.close()
+            raise
+        return lay
+
+    def set_problem_weights(self, p, device="cuda"):
+        import numpy as np
+        import torch
+        wt = torch.float16 if p.wdtype == "f16" else torch.float32
+        Wx = torch.from_numpy(np.ascontiguousarray(p.Wx)).to(device=device, dtype=wt)
+        b = torch.from_numpy(np.ascontiguousarray(p.b)).to(device)
+        if p.sparse:
+            vals = torch.from_numpy(np.ascontiguousarray(p.vals).view(np.int16)).to(device)
+            cols = torch.from_numpy(np.ascontiguousarray(p.cols).view(np.int16)).to(device)
+            prnn_set_weights_sparse(self.h, Wx, p.k, vals, cols, b)
+        else:
+            Wh = torch.from_numpy(np.ascontiguousarray(p.Wh)).to(device=device, dtype=wt)
+            prnn_set_weights_dense(self.h, Wx, Wh, b)
+        torch.cuda.synchronize()
+
+    def forward(self, x, h0=None, y=None, stream=None):
+        """x: [T,B,I] fp32 CUDA tensor; returns y [T,B,H] fp32."""
+        import torch
+        T, B, _ = x.shape
+        if y is None:
+            y = torch.empty((T, B, self.hidden), dtype=torch.float32, device=x.device)
+        prnn_forward(self.h, T, B, x, h0, y, stream)
+        return y
+
+    def status(self, stream=None) -> int:
+        return prnn_get_status(self.h, stream)
+
+    def info(self) -> dict:
+        return prnn_get_info(self.h)
+
+    def set_option(self, opt, value):
+        prnn_set_option(self.h, opt, value)
+
+    def close(self):
+        if getattr(self, "h", None):
+            prnn_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,289 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Rule for every comparison, over the whole sequence:
+    max |y_gpu - y_oracle| <= tol * max |y_oracle|
+with tol = 1e-4 for fp32 weights and 2e-2 for fp16 weights (fp32 accumulation).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from persistent_rnn_recurrence_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "f16": 2e-2}
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from persistent_rnn_recurrence_gb300 import build
+    build.build()
+    from persistent_rnn_recurrence_gb300 import prnn
+    return torch, prnn, oracle.default()
+
+
+def run_gpu(env, p, algo="persistent", T=None, max_batch=None, options=None):
+    torch, prnn, _ = env
+    lay = prnn.Layer.from_problem(p, algo=algo, max_batch=max_batch)
+    try:
+        for k, v in (options or {}).items():
+            lay.set_option(k, v)
+        x = torch.from_numpy(p.x if T is None else p.x[:T]).cuda()
+        h0 = None if p.h0 is None else torch.from_numpy(p.h0).cuda()
+        y = lay.forward(x, h0)
+        st = lay.status()
+        assert st == prnn.PRNN_OK, prnn.prnn_status_string(st)
+        return y.cpu().numpy(), lay.info()
+    finally:
+        lay.close()
+
+
+def check(y, ref, wdtype, what=""):
+    scale = float(np.abs(ref).max())
+    err = float(np.abs(y.astype(np.float64) - ref).max())
+    assert np.isfinite(y).all(), f"{what}: non-finite output"
+    assert err <= TOL[wdtype] * scale, f"{what}: max err {err:.3e} vs {TOL[wdtype] * scale:.3e}"
+    return err / max(scale, 1e-30)
+
+
+# --- full-sequence parity: small and full configurations ----------------------
+FULL = ["dense_f32_h256_b4_t32", "dense_f16_h1152_b4_t256", "sparse_f16_h1792_d10_b4_t256"]
+
+
+@pytest.mark.parametrize("algo", ["persistent", "per_step"])
+@pytest.mark.parametrize("name", FULL)
+def test_named_full_sequence(env, name, algo):
+    p = synth.named_problem(name)
+    y, _ = run_gpu(env, p, algo)
+    ref = env[2].forward(p)
+    check(y, ref, p.wdtype, f"{name}/{algo}")
+
+
+@pytest.mark.parametrize("algo", ["persistent", "per_step"])
+@pytest.mark.parametrize("name", ["sparse_f16_h5760_d1_b4_t256", "sparse_f16_h5760_d5_b4_t256"])
+def test_large_sparse_short_sequence(env, name, algo):
+    p = synth.named_problem(name, T=8)
+    y, _ = run_gpu(env, p, algo)
+    check(y, env[2].forward(p), p.wdtype, f"{name}/{algo}")
+
+
+@pytest.mark.parametrize("name", ["sparse_f16_h5760_d1_b4_t256", "sparse_f16_h5760_d5_b4_t256",
+                                  "sparse_f16_h1792_d10_b4_t256"])
+def test_full_size_teacher_forced_samples(env, name):
+    """Full T = 256 in the benchmarked launch configuration: every sampled
+    output must equal one oracle step applied to the GPU's own previous
+    state, ReLU(b + Wx x_t + Wh y_gpu[t-1]) (a property that holds at any
+    size), plus no sentinel or non-finite value anywhere."""
+    p = synth.named_problem(name)
+    y, _ = run_gpu(env, p)
+    assert np.isfinite(y).all()
+    rng = np.random.default_rng(5)
+    samples = [(int(t), int(b), int(r)) for t, b, r in zip(
+        rng.integers(0, p.T, 300), rng.integers(0, p.B, 300), rng.integers(0, p.H, 300))]
+    samples += [(p.T - 1, p.B - 1, p.H - 1), (0, 0, 0)]
+    h0 = np.zeros((p.B, p.H)) if p.h0 is None else p.h0
+    got = np.array([y[t, b, r] for t, b, r in samples], dtype=np.float64)
+    want = env[2].cells(p, samples, lambda t, b: p.x[t, b],
+                        lambda t, b: h0[b] if t == 0 else y[t - 1, b])
+    scale = float(np.abs(y).max())
+    assert np.abs(got - want).max() <= TOL[p.wdtype] * scale
+
+
+# --- ragged shapes and edge cases ----------------------------------------------
+RAGGED = [
+    dict(H=300, I=200, B=3, T=5, wdtype="f16", h0_std=0.3),
+    dict(H=300, I=200, B=3, T=5, wdtype="f32", h0_std=0.3),
+    dict(H=300, I=200, B=3, T=5, k=17),
+    dict(H=260, I=96, B=1, T=7, k=3),
+    dict(H=132, I=40, B=5, T=6, wdtype="f16"),            # two batch groups (dense)
+    dict(H=132, I=40, B=9, T=4, k=12, h0_std=0.5),       # batch group of 16 (sparse)
+    dict(H=640, I=640, B=32, T=3, k=64),                 # largest batch
+    dict(H=640, I=640, B=32, T=3, wdtype="f16"),
+    dict(H=4, I=4, B=2, T=3, wdtype="f32", h0_std=1.0),  # fewer rows than SMs
+    dict(H=1024, I=64, B=4, T=1, k=1024 // 4, h0_std=1.0),  # T = 1
+]
+
+
+@pytest.mark.parametrize("algo", ["persistent", "per_step"])
+@pytest.mark.parametrize("i", range(len(RAGGED)))
+def test_ragged_shapes(env, i, algo):
+    spec = dict(RAGGED[i])
+    p = synth.make_problem(seed=100 + i, **spec)
+    y, info = run_gpu(env, p, algo)
+    check(y, env[2].forward(p), p.wdtype, f"ragged{i}/{algo}")
+
+
+def test_wh_zero_gives_projection(env):
+    """Wh = 0: y_t = ReLU(Wx x_t + b); exercises the projection alone."""
+    p = synth.make_problem(H=384, I=320, B=4, T=6, wdtype="f16", seed=31, h0_std=1.0)
+    p.Wh[:] = 0
+    y, _ = run_gpu(env, p)
+    ref = env[2].forward(p)
+    check(y, ref, "f16", "wh0")
+    # stronger than the rule: only the fp16 rounding of x separates them
+    assert np.abs(y - ref).max() <= 5e-3 * np.abs(ref).max()
+
+
+def test_h0_none_equals_zeros(env):
+    torch, prnn, _ = env
+    p = synth.make_problem(H=256, B=2, T=4, k=20, seed=32)
+    lay = prnn.Layer.from_problem(p)
+    x = torch.from_numpy(p.x).cuda()
+    y1 = lay.forward(x, None)
+    y2 = lay.forward(x, torch.zeros(p.B, p.H, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    lay.close()
+
+
+# --- exact properties of the CUDA path -----------------------------------------
+@pytest.mark.parametrize("spec", [dict(H=1152, B=4, T=16, wdtype="f16"),
+                                  dict(H=1792, B=4, T=16, k=179)])
+def test_determinism_chaining_batch_independence(env, spec):
+    torch, prnn, _ = env
+    p = synth.make_problem(seed=41, h0_std=0.1, **spec)
+    lay = prnn.Layer.from_problem(p)
+    x = torch.from_numpy(p.x).cuda()
+    h0 = torch.from_numpy(p.h0).cuda()
+    y = lay.forward(x, h0)
+    y_again = lay.forward(x, h0)
+    # chaining: T1 steps then T2 steps from h0 = y[T1-1]
+    ya = lay.forward(x[:7].contiguous(), h0)
+    yb = lay.forward(x[7:].contiguous(), ya[-1].contiguous())
+    # batch independence: each batch column alone
+    ys = [lay.forward(x[:, b:b + 1].contiguous(), h0[b:b + 1].contiguous()) for b in range(p.B)]
+    torch.cuda.synchronize()
+    assert lay.status() == prnn.PRNN_OK
+    assert torch.equal(y, y_again)
+    assert torch.equal(torch.cat([ya, yb]), y)
+    for b in range(p.B):
+        assert torch.equal(ys[b][:, 0], y[:, b])
+    lay.close()
+
+
+@pytest.mark.parametrize("spec", [dict(H=1152, B=4, T=12, wdtype="f16"),
+                                  dict(H=1792, B=4, T=12, k=179)])
+def test_grid_barrier_mode_matches_flag_mode(env, spec):
+    _, prnn, o = env
+    p = synth.make_problem(seed=43, **spec)
+    y0, _ = run_gpu(env, p)
+    y1, _ = run_gpu(env, p, options={prnn.PRNN_OPT_SYNC_MODE: 1})
+    assert np.array_equal(y0, y1)
+    check(y1, o.forward(p), "f16", "gridbar")
+
+
+# --- API behaviour ---------------------------------------------------------------
+def test_plan_report(env):
+    _, prnn, _ = env
+    p = synth.named_problem("sparse_f16_h1792_d10_b4_t256", T=2)
+    lay = prnn.Layer.from_problem(p)
+    info = lay.info()
+    lay.close()
+    assert info["sparse"] == 1 and info["k"] == 179 and info["nnz"] == 1792 * 179
+    assert info["k_padded"] % (4 * info["threads_per_row"]) == 0
+    assert info["n_cta"] * info["rows_per_cta"] >= 1792
+    assert info["n_cta"] <= info["sm_count"]
+    assert info["onchip_weight_bytes"] == 1792 * info["k_padded"] * 4
+
+
+def test_errors(env):
+    torch, prnn, _ = env
+    p = synth.make_problem(H=64, B=2, T=3, k=8, seed=50)
+    lay = prnn.prnn_create(64, 64, 2, prnn.PRNN_F16, prnn.PRNN_ALGO_PERSISTENT)
+    x = torch.from_numpy(p.x).cuda()
+    y = torch.empty(3, 2, 64, device="cuda")
+    with pytest.raises(prnn.PrnnError) as e:
+        prnn.prnn_forward(lay, 3, 2, x, None, y)
+    assert e.value.status == prnn.PRNN_ERR_NOT_READY
+    Wx = torch.from_numpy(p.Wx).cuda()
+    b = torch.from_numpy(p.b).cuda()
+    vals = torch.from_numpy(p.vals.view(np.int16)).cuda()
+    bad = p.cols.copy()
+    bad[5, 1] = bad[5, 0]                                     # duplicate column
+    with pytest.raises(prnn.PrnnError) as e:
+        prnn.prnn_set_weights_sparse(lay, Wx, 8, vals, torch.from_numpy(bad.view(np.int16)).cuda(), b)
+    assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    bad = p.cols.copy()
+    bad[0, 0] = 64                                            # out of range
+    with pytest.raises(prnn.PrnnError) as e:
+        prnn.prnn_set_weights_sparse(lay, Wx, 8, vals, torch.from_numpy(bad.view(np.int16)).cuda(), b)
+    assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    prnn.prnn_set_weights_sparse(lay, Wx, 8, vals, torch.from_numpy(p.cols.view(np.int16)).cuda(), b)
+    for B_, what in ((3, "B > max_batch"),):
+        with pytest.raises(prnn.PrnnError) as e:
+            prnn.prnn_forward(lay, 3, B_, x, None, y)
+        assert e.value.status == prnn.PRNN_ERR_INVALID_ARG, what
+    ybig = torch.empty(3 * 2 * 64 + 4, device="cuda")
+    with pytest.raises(prnn.PrnnError) as e:                   # misaligned y
+        prnn.prnn_forward(lay, 3, 2, x, None, ybig[1:].data_ptr())
+    assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    with pytest.raises(prnn.PrnnError) as e:                   # y overlaps x
+        prnn.prnn_forward(lay, 3, 2, x, None, x)
+    assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    prnn.prnn_forward(lay, 0, 2, x, None, y)                   # T = 0: no-op
+    prnn.prnn_forward(lay, 3, 0, x, None, y)                   # B = 0: no-op
+    assert prnn.prnn_get_status(lay) == prnn.PRNN_OK
+    prnn.prnn_destroy(lay)
+    # a dense layer too large for the chip is refused, not silently degraded
+    big = prnn.prnn_create(8192, 64, 4, prnn.PRNN_F16, prnn.PRNN_ALGO_PERSISTENT)
+    Wh = torch.zeros(8192, 8192, dtype=torch.float16, device="cuda")
+    with pytest.raises(prnn.PrnnError) as e:
+        prnn.prnn_set_weights_dense(big, torch.zeros(8192, 64, dtype=torch.float16, device="cuda"),
+                                    Wh, torch.zeros(8192, device="cuda"))
+    assert e.value.status == prnn.PRNN_ERR_UNSUPPORTED
+    prnn.prnn_destroy(big)
+
+
+def test_host_weight_pointers(env):
+    """set_weights accepts host memory too (the library copies)."""
+    torch, prnn, o = env
+    p = synth.make_problem(H=256, B=2, T=5, k=25, seed=51)
+    lay = prnn.prnn_create(256, 256, 2, prnn.PRNN_F16, prnn.PRNN_ALGO_PERSISTENT)
+    prnn.prnn_set_weights_sparse(lay, p.Wx.ctypes.data, p.k, p.vals.ctypes.data,
+                                 p.cols.ctypes.data, p.b.ctypes.data)
+    x = torch.from_numpy(p.x).cuda()
+    y = torch.empty(5, 2, 256, device="cuda")
+    prnn.prnn_forward(lay, 5, 2, x, None, y)
+    assert prnn.prnn_get_status(lay) == prnn.PRNN_OK
+    prnn.prnn_destroy(lay)
+    check(y.cpu().numpy(), o.forward(p), "f16", "host pointers")
+
+
+# --- bounded waits: a publish that never happens ends in a status, not a hang --------
+@pytest.mark.parametrize("spec", [dict(H=512, B=4, T=6, k=40), dict(H=512, B=4, T=6, wdtype="f16")])
+def test_dropped_publish_times_out_cleanly(env, spec):
+    torch, prnn, o = env
+    p = synth.make_problem(seed=60, **spec)
+    lay = prnn.Layer.from_problem(p)
+    lay.set_option(prnn.PRNN_OPT_WAIT_TIMEOUT_US, 20000)
+    lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_CTA, 3)
+    lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_STEP, 2)
+    x = torch.from_numpy(p.x).cuda()
+    lay.forward(x)
+    assert lay.status() == prnn.PRNN_ERR_TIMEOUT
+    with pytest.raises(prnn.PrnnError) as e:                   # sticky
+        lay.forward(x)
+    assert e.value.status == prnn.PRNN_ERR_TIMEOUT
+    lay.close()
+    # the context is still usable: a fresh handle computes correctly
+    y, _ = run_gpu(env, p)
+    check(y, o.forward(p), "f16", "after timeout")
+
+
+def test_sync_floor_probe(env):
+    torch, prnn, _ = env
+    p = synth.named_problem("sparse_f16_h1792_d10_b4_t256", T=2)
+    lay = prnn.Layer.from_problem(p)
+    lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+    y = torch.empty(64, 4, 1792, device="cuda")
+    prnn.prnn_probe_sync_floor(lay.h, 64, 4, y)
+    assert lay.status() == prnn.PRNN_OK
+    _, ms = prnn.prnn_get_timing(lay.h)
+    lay.close()
+    t = torch.arange(1, 65, dtype=torch.float32, device="cuda").view(64, 1, 1)
+    assert torch.equal(y, t.expand(64, 4, 1792))
+    assert ms > 0
