@@ -66,7 +66,9 @@ typedef enum {
   PRNN_OPT_DEBUG_DROP_CTA = 2,    /* fault hook: CTA that skips one publish (-1 = off)         */
   PRNN_OPT_DEBUG_DROP_STEP = 3,   /* fault hook: the step whose publish it skips               */
   PRNN_OPT_TIMING = 4,            /* 1: record CUDA events around each stage of forward        */
-  PRNN_OPT_PROJECTION = 5         /* 0: tensor cores when possible (default); 1: fp32 CUDA cores */
+  PRNN_OPT_PROJECTION = 5,        /* 0: tensor cores when possible (default); 1: fp32 CUDA cores */
+  PRNN_OPT_CTA_GROUPS = 6         /* persistent: CTA groups splitting the batch (0 = automatic);
+                                     takes effect at the next set_weights call                 */
 } prnn_option_t;
 
 /* Plan and sizes chosen at create / set_weights time (read-only report). */
@@ -76,6 +78,8 @@ typedef struct {
   int k, k_padded;                 /* sparse: non-zeros per row, and per row after padding  */
   int sm_count, n_cta, rows_per_cta, threads_per_cta, threads_per_row;
   int projection_tensor_cores;     /* 1 if forward uses the tcgen05 projection               */
+  int sparse_bank_cap;             /* sparse: max lanes of a warp sharing a bank per gather  */
+  int cta_groups;                  /* CTA groups, each owning a slice of the batch columns   */
   size_t smem_bytes;               /* dynamic shared memory per CTA at max_batch             */
   size_t onchip_weight_bytes;      /* packed Wh bytes held on chip, all CTAs                 */
   size_t nnz;                      /* non-zeros of Wh (H*H when dense)                       */
@@ -155,6 +159,26 @@ prnn_status_t prnn_get_timing(prnn_t h, float* ms_projection, float* ms_recurren
  * scratch.  Its time is reported by prnn_get_timing as ms_recurrence.
  */
 prnn_status_t prnn_probe_sync_floor(prnn_t h, int T, int B, float* y, void* stream);
+
+/*
+ * Host only (no GPU): the packing the persistent sparse kernel applies to
+ * row-balanced weights, exposed so the layout can be checked bit for bit.
+ * Rows are split over n_cta CTAs of rows_per_cta rows; each row over
+ * threads_per_row (1, 2, 4, 8, 16 or 32) threads holding the same number of
+ * entries each.  Output: packed[n_cta][rows_per_cta][ept/4][threads_per_row][4]
+ * 32-bit words, word = fp16 value bits | column << 16, padding words have value
+ * 0.  Within a row, entries are permuted among the row's threads so that in
+ * every gather slot the 32 lanes of a warp use different shared-memory banks
+ * (column mod 32) where possible (bank-aware layout, sparse persistent RNN
+ * ablation table).  *ept receives the entries per thread (a multiple of 4),
+ * *bank_cap the most lanes that had to share a bank.  capacity_words is the
+ * size of `packed`; if it is too small the call returns PRNN_ERR_INVALID_ARG
+ * with *ept set, so the caller can size the buffer and call again.
+ */
+prnn_status_t prnn_pack_sparse_host(int hidden, int k, int n_cta, int rows_per_cta,
+                                    int threads_per_row, const uint16_t* vals,
+                                    const uint16_t* cols, uint32_t* packed,
+                                    size_t capacity_words, int* ept, int* bank_cap);
 
 #ifdef __cplusplus
 }

@@ -30,7 +30,8 @@ struct prnn_handle {
   bool weights_set = false, sparse = false;
   int k = 0;
   // persistent plan
-  int n_cta = 0, R = 0, nthreads = 0, cpt = 0, tpr = 0, kp = 0, ept = 0;
+  int n_cta = 0, R = 0, nthreads = 0, cpt = 0, tpr = 0, kp = 0, ept = 0, pack_cap = 0;
+  int G = 1, cpg = 0, groups_opt = 0;
   size_t onchip_bytes = 0, smem_at_max = 0;
   bool tc_proj = false;
   int Kp = 0;  // I rounded up to 64 (tcgen05 projection)
@@ -111,35 +112,67 @@ int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
 // ---- planning ----------------------------------------------------------
 struct DensePlan {
-  int R, n_cta, nthreads, cpt;
+  int G, cpg, R, n_cta, nthreads, cpt, bw;
   size_t smem;
   bool ok;
 };
 
-DensePlan plan_dense(const prnn_handle* h) {
+// Candidate CTA-group counts, largest first: G groups of SMs/G CTAs, each
+// group owning ceil(B/G) batch columns and a full copy of Wh.
+int max_groups(const prnn_handle* h) {
+  if (h->groups_opt > 0) return std::min(h->groups_opt, h->maxB);
+  return std::min(h->maxB, 8);
+}
+
+DensePlan plan_dense_g(const prnn_handle* h, int G) {
   DensePlan p{};
   const int H = h->H;
-  p.R = (H + h->sm_count - 1) / h->sm_count;
-  p.n_cta = (H + p.R - 1) / p.R;
+  p.G = G;
+  p.cpg = h->sm_count / G;
+  p.ok = false;
+  if (p.cpg < 1 || H % 4 != 0) return p;
+  p.R = (H + p.cpg - 1) / p.cpg;
+  p.cpg = (H + p.R - 1) / p.R;
+  p.n_cta = p.G * p.cpg;
+  p.bw = recur_dense_bw((h->maxB + G - 1) / G);
+  if (recur_dense_rmax(p.R) == 0) return p;
   const int nchunks = H / 4;
-  p.nthreads = std::min(kDenseMaxThreads, std::max(32, round_up(nchunks, 32)));
-  p.cpt = (nchunks + p.nthreads - 1) / p.nthreads;
-  p.ok = (H % 4 == 0) && recur_dense_rmax(p.R) != 0 && p.cpt <= 4;
-  p.smem = p.ok ? recur_dense_smem(p.R, p.cpt, p.nthreads, h->wdtype == PRNN_F16) : 0;
-  p.ok = p.ok && p.smem <= h->smem_optin;
+  const int max_nt = recur_dense_max_threads(p.R, p.bw);
+  p.cpt = (nchunks + max_nt - 1) / max_nt;
+  if (p.cpt > 4) return p;
+  // equal chunk counts per thread where the sizes allow
+  p.nthreads = std::max(32, round_up((nchunks + p.cpt - 1) / p.cpt, 32));
+  p.smem = recur_dense_smem(p.R, p.cpt, p.nthreads, h->wdtype == PRNN_F16, p.bw);
+  p.ok = p.smem <= h->smem_optin;
   return p;
 }
 
+DensePlan plan_dense(const prnn_handle* h) {
+  for (int G = max_groups(h); G >= 1; --G) {
+    if (h->groups_opt == 0 && G > 1 && (G & (G - 1)) != 0) continue;
+    DensePlan p = plan_dense_g(h, G);
+    if (h->groups_opt > 0) return p;
+    // automatic: at most 16 rows per CTA (more rows lengthen every thread's
+    // per-step chain more than the smaller exchange saves)
+    if (p.ok && (p.R <= 16 || G == 1)) return p;
+  }
+  return DensePlan{};
+}
+
 struct SparsePlan {
-  int R, n_cta, tpr, kp, ept, nthreads;
+  int G, cpg, R, n_cta, tpr, kp, ept, nthreads;
   bool ok;
 };
 
-SparsePlan plan_sparse(const prnn_handle* h, int k) {
+SparsePlan plan_sparse_g(const prnn_handle* h, int k, int G) {
   SparsePlan p{};
   const int H = h->H;
-  p.R = (H + h->sm_count - 1) / h->sm_count;
-  p.n_cta = (H + p.R - 1) / p.R;
+  p.G = G;
+  p.cpg = h->sm_count / G;
+  if (p.cpg < 1 || H % 4 != 0) return p;
+  p.R = (H + p.cpg - 1) / p.cpg;
+  p.cpg = (H + p.R - 1) / p.R;
+  p.n_cta = p.G * p.cpg;
   // threads per row: the widest split whose padding stays under ~15 % and
   // whose R * tpr threads fit one CTA; else the least padding that fits.
   int best = -1;
@@ -157,20 +190,65 @@ SparsePlan plan_sparse(const prnn_handle* h, int k) {
       best = t;
     }
   }
-  p.ok = best > 0 && H % 4 == 0;
-  if (!p.ok) return p;
+  if (best <= 0) return p;
   p.tpr = best;
-  p.kp = round_up(k, 4 * best);
-  p.ept = p.kp / best;
-  p.nthreads = std::min(kSparseMaxThreads, std::max(256, round_up(p.R * best, 32)));
+  p.ept = ((k + best - 1) / best + 3) / 4 * 4;
+  p.kp = p.ept * best;
+  // enough threads to keep one staging round of the group's columns in flight
+  const int bl = std::min(4, (h->maxB + G - 1) / G);
+  const int stage_threads = round_up((H * std::max(bl, 1) / 4 + 11) / 12, 32);
+  p.nthreads = std::min(kSparseMaxThreads,
+                        std::max({256, round_up(p.R * best, 32), stage_threads}));
+  // at least a one-column batch pass must fit
+  p.ok = recur_sparse_smem(H, p.R, p.ept, p.tpr, 1, false) <= h->smem_optin;
   return p;
+}
+
+// Estimated ns per step of a sparse plan (model fitted to GB300 measurements
+// of this kernel): the step exchange costs ~1.0 us plus ~17 ns per KiB of
+// h that each CTA pulls from L2; the gather-multiply costs ~1.9 shared-memory
+// wavefronts per gather slot (bank-aware packing) plus the wavefronts of the
+// weights kept in smem rather than registers, and each thread's chain of ept
+// dependent updates.
+double sparse_step_ns(const prnn_handle* h, const SparsePlan& p) {
+  const int bl = (h->maxB + p.G - 1) / p.G;
+  const double kib = (double)bl * h->H * 4.0 / 1024.0;
+  const double warps = (double)((p.R * p.tpr + 31) / 32);
+  const double gather = warps * p.ept * bl * 1.9;
+  const double wsmem = warps * std::max(0, p.ept / 4 - 4) * 4.0;
+  const double chain = p.ept * 4.0 * bl + 60.0;
+  const double ghz = 1.9;
+  return 1000.0 + 17.0 * kib + (gather + wsmem) / ghz + chain / ghz;
+}
+
+// Feasible plans, fastest (by the model) first; a forced group count gives
+// exactly that plan.
+std::vector<SparsePlan> plan_sparse(const prnn_handle* h, int k) {
+  std::vector<std::pair<double, SparsePlan>> cand;
+  for (int G = max_groups(h); G >= 1; --G) {
+    if (h->groups_opt == 0 && G > 1 && (G & (G - 1)) != 0) continue;
+    SparsePlan p = plan_sparse_g(h, k, G);
+    if (h->groups_opt > 0) {
+      if (p.ok) cand.push_back({0.0, p});
+      break;
+    }
+    if (p.ok) cand.push_back({sparse_step_ns(h, p), p});
+  }
+  std::stable_sort(cand.begin(), cand.end(),
+                   [](const std::pair<double, SparsePlan>& a, const std::pair<double, SparsePlan>& b) {
+                     return a.first < b.first;
+                   });
+  std::vector<SparsePlan> out;
+  for (auto& c : cand) out.push_back(c.second);
+  return out;
 }
 
 // Batch group and staging buffers of the sparse kernel for a given B.
 bool sparse_batch_plan(const prnn_handle* h, int B, int* bgroup, bool* dbuf, size_t* smem) {
-  int want = 4;
-  while (want < B && want < 32) want *= 2;
-  for (int bg = want; bg >= 4; bg /= 2) {
+  const int bl = (B + h->G - 1) / h->G;  // batch columns of one CTA group
+  int want = 1;
+  while (want < bl && want < 32) want *= 2;
+  for (int bg = want; bg >= 1; bg /= 2) {
     for (int db = 1; db >= 0; --db) {
       const size_t s = recur_sparse_smem(h->H, h->R, h->ept, h->tpr, bg, db == 1);
       if (s <= h->smem_optin) {
@@ -253,6 +331,8 @@ RecurCommon common_args(const prnn_handle* h, int T, int B, const float* h0, flo
   c.H = h->H;
   c.n_cta = h->n_cta;
   c.R = h->R;
+  c.G = h->G;
+  c.cpg = h->cpg;
   c.nthreads = h->nthreads;
   c.P = h->P;
   c.h0 = h0;
@@ -366,8 +446,9 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
     // columns 4*(i + j*nthreads) .. +3 (zero outside the matrix)
     const int NT = plan.nthreads, nchunks = H / 4;
     const size_t vec = 4 * esz;
-    std::vector<unsigned char> pk((size_t)plan.n_cta * plan.cpt * plan.R * NT * vec, 0);
-    for (int cta = 0; cta < plan.n_cta; ++cta)
+    // one block per CTA of a group; every group reads the same blocks
+    std::vector<unsigned char> pk((size_t)plan.cpg * plan.cpt * plan.R * NT * vec, 0);
+    for (int cta = 0; cta < plan.cpg; ++cta)
       for (int j = 0; j < plan.cpt; ++j)
         for (int r = 0; r < plan.R; ++r)
           for (int i = 0; i < NT; ++i) {
@@ -379,10 +460,12 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
     PRNN_TRY(upload(&h->Wpk, pk.data(), pk.size()));
     h->n_cta = plan.n_cta;
     h->R = plan.R;
+    h->G = plan.G;
+    h->cpg = plan.cpg;
     h->nthreads = plan.nthreads;
     h->cpt = plan.cpt;
     h->smem_at_max = plan.smem;
-    h->onchip_bytes = pk.size();
+    h->onchip_bytes = pk.size() * plan.G;
   } else {
     PRNN_TRY(upload(&h->Wstep, wh.data(), wh.size()));
     h->onchip_bytes = 0;
@@ -426,12 +509,25 @@ prnn_status_t prnn_set_weights_sparse(prnn_t h, const void* Wx, int k, const uin
     }
   }
   SparsePlan plan{};
+  std::vector<uint32_t> pk;
+  PackStats pst;
   if (h->algo == PRNN_ALGO_PERSISTENT) {
-    plan = plan_sparse(h, k);
-    if (!plan.ok) return PRNN_ERR_UNSUPPORTED;
-    // check that at least the smallest batch group fits
-    const size_t s4 = recur_sparse_smem(H, plan.R, plan.ept, plan.tpr, 4, false);
-    if (s4 > h->smem_optin) return PRNN_ERR_UNSUPPORTED;
+    bool packed = false;
+    for (const SparsePlan& cand : plan_sparse(h, k)) {
+      // largest entries-per-thread whose weights plus one h column fit in smem
+      const size_t hs1 = (size_t)H * sizeof(float);
+      if (hs1 >= h->smem_optin) continue;
+      const int max_ept = (int)(((h->smem_optin - hs1) / ((size_t)cand.R * cand.tpr * 4)) / 4 * 4);
+      plan = cand;
+      plan.ept = pack_sparse_rows(H, k, plan.R, plan.cpg, plan.tpr, hv.data(), hc.data(), pk,
+                                  &pst, max_ept);
+      if (plan.ept > 0) {
+        packed = true;
+        break;
+      }
+    }
+    if (!packed) return PRNN_ERR_UNSUPPORTED;
+    plan.kp = plan.ept * plan.tpr;
   }
   free_weights(h);
   prnn_status_t st = stage_wx_bias(h, Wx, bias, &h->Wx, &h->Wx16, &h->bias);
@@ -440,32 +536,17 @@ prnn_status_t prnn_set_weights_sparse(prnn_t h, const void* Wx, int k, const uin
     return (uint32_t)hv[(size_t)r * k + j] | ((uint32_t)hc[(size_t)r * k + j] << 16);
   };
   if (h->algo == PRNN_ALGO_PERSISTENT) {
-    // per CTA: [row r][group q][thread seg s] uint4; thread s of row r owns
-    // the entries s*ept .. s*ept+ept-1 of the row (sorted by column), padding
-    // entries (j >= k) have value 0 and the row's last column.
-    const int q4 = plan.ept / 4;
-    std::vector<uint32_t> pk((size_t)plan.n_cta * plan.R * plan.kp, 0);
-    for (int cta = 0; cta < plan.n_cta; ++cta)
-      for (int r = 0; r < plan.R; ++r) {
-        const int grow = cta * plan.R + r;
-        for (int sg = 0; sg < plan.tpr; ++sg)
-          for (int q = 0; q < q4; ++q)
-            for (int w = 0; w < 4; ++w) {
-              const int j = sg * plan.ept + q * 4 + w;
-              uint32_t e = 0;
-              if (grow < H) e = j < k ? entry(grow, j) : ((uint32_t)hc[(size_t)grow * k + k - 1] << 16);
-              const size_t dst = ((((size_t)cta * plan.R + r) * q4 + q) * plan.tpr + sg) * 4 + w;
-              pk[dst] = e;
-            }
-      }
     PRNN_TRY(upload(&h->Wpk, pk.data(), pk.size() * 4));
     h->n_cta = plan.n_cta;
     h->R = plan.R;
+    h->G = plan.G;
+    h->cpg = plan.cpg;
     h->nthreads = plan.nthreads;
     h->tpr = plan.tpr;
     h->kp = plan.kp;
     h->ept = plan.ept;
-    h->onchip_bytes = (size_t)H * plan.kp * 4;
+    h->pack_cap = pst.cap;
+    h->onchip_bytes = (size_t)plan.n_cta * plan.R * plan.kp * 4;  // all groups' copies
     int bg = 4;
     bool db = false;
     size_t sm = 0;
@@ -528,12 +609,13 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
       PRNN_TRY(launch_recur_sparse(a, s));
     } else {
       DenseRecurArgs a{};
-      c.smem = h->smem_at_max;
+      const int bw = recur_dense_bw((B + h->G - 1) / h->G);
+      c.smem = recur_dense_smem(h->R, h->cpt, h->nthreads, h->wdtype == PRNN_F16, bw);
       a.c = c;
       a.Wpk = h->Wpk;
       a.cpt = h->cpt;
       a.wfp16 = h->wdtype == PRNN_F16;
-      PRNN_TRY(launch_recur_dense(a, s));
+      PRNN_TRY(launch_recur_dense(a, bw, s));
     }
   } else {
     const bool hit = h->gexec && h->g_T == T && h->g_B == B && h->g_h0 == h0 && h->g_y == y &&
@@ -618,6 +700,10 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
       if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
       h->proj_mode = (int)value;
       return PRNN_OK;
+    case PRNN_OPT_CTA_GROUPS:
+      if (value < 0 || value > 32) return PRNN_ERR_INVALID_ARG;
+      h->groups_opt = (int)value;
+      return PRNN_OK;
   }
   return PRNN_ERR_INVALID_ARG;
 }
@@ -640,6 +726,8 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
   info->threads_per_cta = h->nthreads;
   info->threads_per_row = h->tpr;
   info->projection_tensor_cores = h->tc_proj;
+  info->sparse_bank_cap = h->sparse ? h->pack_cap : 0;
+  info->cta_groups = h->G;
   info->smem_bytes = h->smem_at_max;
   info->onchip_weight_bytes = h->onchip_bytes;
   info->nnz = h->sparse ? (size_t)h->H * h->k : (size_t)h->H * h->H;
@@ -666,7 +754,8 @@ prnn_status_t prnn_probe_sync_floor(prnn_t h, int T, int B, float* y, void* stre
   if (T == 0 || B == 0) return PRNN_OK;
   if (!y || !aligned16(y)) return PRNN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int bg = std::min(32, std::max(4, round_up(B, 4)));
+  const int bl = (B + h->G - 1) / h->G;
+  const int bg = std::min(32, std::max(4, round_up(bl, 4)));
   RecurCommon c = common_args(h, T, B, nullptr, y);
   c.smem = sync_probe_smem(h->H, bg);
   if (c.smem > h->smem_optin) return PRNN_ERR_UNSUPPORTED;
@@ -678,6 +767,32 @@ prnn_status_t prnn_probe_sync_floor(prnn_t h, int T, int B, float* y, void* stre
     PRNN_TRY(cudaEventRecord(h->ev[2], s));
     h->ev_valid = true;
   }
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_pack_sparse_host(int hidden, int k, int n_cta, int rows_per_cta,
+                                    int threads_per_row, const uint16_t* vals,
+                                    const uint16_t* cols, uint32_t* packed,
+                                    size_t capacity_words, int* ept, int* bank_cap) {
+  const int H = hidden, R = rows_per_cta, tpr = threads_per_row;
+  if (H < 1 || H > 65535 || k < 1 || k > H || n_cta < 1 || R < 1 || (size_t)n_cta * R < (size_t)H)
+    return PRNN_ERR_INVALID_ARG;
+  if (tpr != 1 && tpr != 2 && tpr != 4 && tpr != 8 && tpr != 16 && tpr != 32)
+    return PRNN_ERR_INVALID_ARG;
+  if (!vals || !cols || !ept) return PRNN_ERR_INVALID_ARG;
+  std::vector<int> seen((size_t)H, -1);
+  for (int r = 0; r < H; ++r)
+    for (int j = 0; j < k; ++j) {
+      const int c = cols[(size_t)r * k + j];
+      if (c >= H || seen[c] == r) return PRNN_ERR_INVALID_ARG;
+      seen[c] = r;
+    }
+  std::vector<uint32_t> pk;
+  PackStats st;
+  *ept = pack_sparse_rows(H, k, R, n_cta, tpr, vals, cols, pk, &st);
+  if (bank_cap) *bank_cap = st.cap;
+  if (!packed || capacity_words < pk.size()) return PRNN_ERR_INVALID_ARG;
+  std::memcpy(packed, pk.data(), pk.size() * sizeof(uint32_t));
   return PRNN_OK;
 }
 

@@ -50,6 +50,14 @@ __device__ __forceinline__ int ld_relaxed_i(const int* p) {
   return v;
 }
 
+// Read-only load that the compiler may not move: used to issue the next step's
+// projection value early so its latency hides behind the step exchange.
+__device__ __forceinline__ float ld_nc_pinned(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -66,13 +74,21 @@ __device__ __forceinline__ void report_timeout(int* status, int step, int cta) {
   }
 }
 
-// Bounded wait state.  `deadline` is absolute globaltimer ns.
+// Bounded wait state.  The deadline (globaltimer ns) is armed lazily, on the
+// first stale poll of a step, so steps whose data is already there never
+// read the timer.  Call new_step() at the start of every step.
 struct Waiter {
   uint64_t deadline;
+  long long timeout_ns;
   const int* status;
+  __device__ __forceinline__ void new_step() { deadline = 0; }
   // true = keep waiting; false = give up (deadline passed or another CTA failed)
   __device__ __forceinline__ bool still_ok(uint32_t& spins) {
-    if ((++spins & 63u) != 0u) return true;
+    if ((++spins & 63u) != 1u) return true;
+    if (deadline == 0) {
+      deadline = global_ns() + (uint64_t)timeout_ns;
+      return true;
+    }
     if (ld_relaxed_i(status) != 0) return false;
     return global_ns() < deadline;
   }

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -39,7 +40,8 @@ cudaError_t launch_projection_tc(const ProjTcArgs& a, cudaStream_t s);
 // ---- persistent recurrent kernels --------------------------------------
 struct RecurCommon {
   int T, B, H;
-  int n_cta, R;          // CTAs and rows per CTA (last CTA may own fewer)
+  int n_cta, R;          // CTAs (G * cpg) and rows per CTA (last CTA of a group may own fewer)
+  int G, cpg;            // CTA groups (each owns a contiguous slice of the batch) and CTAs per group
   int nthreads;
   size_t smem;           // dynamic shared memory bytes
   const float* P;        // [T][B][H] projection (bias included)
@@ -60,9 +62,11 @@ struct DenseRecurArgs {
   int cpt;               // chunk slots per thread = ceil((H/4) / nthreads)
   int wfp16;
 };
-cudaError_t launch_recur_dense(const DenseRecurArgs& a, cudaStream_t s);
-size_t recur_dense_smem(int R, int cpt, int nthreads, bool fp16);
+cudaError_t launch_recur_dense(const DenseRecurArgs& a, int bw, cudaStream_t s);
+size_t recur_dense_smem(int R, int cpt, int nthreads, bool fp16, int bw);
 int recur_dense_rmax(int R);   // 0 if R unsupported
+int recur_dense_bw(int batch_cols);          // batch columns per pass: 1, 2 or 4
+int recur_dense_max_threads(int R, int bw);  // launch bound of that instantiation
 
 // Sparse row-balanced: per CTA, R rows x kp entries; thread (row, seg) with
 // seg < tpr owns ept = kp/tpr entries, read as uint4 (4 packed entries).
@@ -78,6 +82,17 @@ cudaError_t launch_recur_sparse(const SparseRecurArgs& a, cudaStream_t s);
 size_t recur_sparse_smem(int H, int R, int ept, int tpr, int bgroup, bool dbuf);
 
 cudaError_t launch_sync_probe(const RecurCommon& c, int bgroup, cudaStream_t s);
+
+// Host packing of row-balanced sparse rows into the kernel layout (pack.cu).
+// vals/cols: [H][k]; writes out_packed[n_cta][R][ept/4][tpr][4]; returns ept.
+struct PackStats {
+  int ept = 0;               // entries per thread (multiple of 4)
+  int cap = 0;               // max lanes per bank residue per slot that was needed
+  long long conflicts = 0;   // lane-slots that share a bank with an earlier lane
+};
+int pack_sparse_rows(int H, int k, int R, int n_cta, int tpr, const uint16_t* vals,
+                     const uint16_t* cols, std::vector<uint32_t>& out_packed, PackStats* stats,
+                     int max_ept = 1 << 30);
 size_t sync_probe_smem(int H, int bgroup);
 
 // ---- per-step path ------------------------------------------------------

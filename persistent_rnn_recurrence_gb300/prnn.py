@@ -26,18 +26,19 @@ PRNN_OK, PRNN_ERR_INVALID_ARG, PRNN_ERR_UNSUPPORTED, PRNN_ERR_NOT_READY, \
 PRNN_F32, PRNN_F16 = 0, 1
 PRNN_ALGO_PERSISTENT, PRNN_ALGO_PER_STEP = 0, 1
 PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA, \
-    PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION = range(6)
+    PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION, PRNN_OPT_CTA_GROUPS = range(7)
 
 EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
            "prnn_forward", "prnn_destroy", "prnn_get_status", "prnn_status_string",
-           "prnn_set_option", "prnn_get_info", "prnn_get_timing", "prnn_probe_sync_floor"]
+           "prnn_set_option", "prnn_get_info", "prnn_get_timing", "prnn_probe_sync_floor",
+           "prnn_pack_sparse_host"]
 
 
 class prnn_info_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "hidden", "input", "max_batch", "wdtype", "algo", "sparse", "weights_set", "k",
         "k_padded", "sm_count", "n_cta", "rows_per_cta", "threads_per_cta",
-        "threads_per_row", "projection_tensor_cores")] + [
+        "threads_per_row", "projection_tensor_cores", "sparse_bank_cap", "cta_groups")] + [
         ("smem_bytes", ctypes.c_size_t), ("onchip_weight_bytes", ctypes.c_size_t),
         ("nnz", ctypes.c_size_t)]
 
@@ -59,6 +60,8 @@ _sig = {
     "prnn_get_info": ([_P, ctypes.POINTER(prnn_info_t)], _I),
     "prnn_get_timing": ([_P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)], _I),
     "prnn_probe_sync_floor": ([_P, _I, _I, _P, _P], _I),
+    "prnn_pack_sparse_host": ([_I, _I, _I, _I, _I, _P, _P, _P, ctypes.c_size_t,
+                               ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
 }
 for _name, (_args, _res) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -153,6 +156,26 @@ def prnn_get_timing(h: int):
 def prnn_probe_sync_floor(h: int, T: int, B: int, y, stream=None) -> None:
     _check(_lib.prnn_probe_sync_floor(h, T, B, _ptr(y), _stream(stream)),
            "prnn_probe_sync_floor")
+
+
+def prnn_pack_sparse_host(hidden, k, n_cta, rows_per_cta, threads_per_row, vals, cols):
+    """Host-only packing (numpy in, numpy out): returns (packed[n_cta, R, ept/4,
+    tpr, 4] uint32, ept, bank_cap)."""
+    import numpy as np
+    vals = np.ascontiguousarray(vals).view(np.uint16)
+    cols = np.ascontiguousarray(cols, dtype=np.uint16)
+    ept, cap = _I(), _I()
+    st = _lib.prnn_pack_sparse_host(hidden, k, n_cta, rows_per_cta, threads_per_row,
+                                    vals.ctypes.data, cols.ctypes.data, None, 0,
+                                    ctypes.byref(ept), ctypes.byref(cap))
+    if st != PRNN_ERR_INVALID_ARG or ept.value <= 0:
+        _check(st if st != PRNN_OK else PRNN_ERR_INVALID_ARG, "prnn_pack_sparse_host")
+    out = np.zeros((n_cta, rows_per_cta, ept.value // 4, threads_per_row, 4), dtype=np.uint32)
+    _check(_lib.prnn_pack_sparse_host(hidden, k, n_cta, rows_per_cta, threads_per_row,
+                                      vals.ctypes.data, cols.ctypes.data, out.ctypes.data,
+                                      out.size, ctypes.byref(ept), ctypes.byref(cap)),
+           "prnn_pack_sparse_host")
+    return out, ept.value, cap.value
 
 
 # ---- convenience wrapper used by the tests and the benchmark ------------------

@@ -187,7 +187,8 @@ def test_plan_report(env):
     assert info["k_padded"] % (4 * info["threads_per_row"]) == 0
     assert info["n_cta"] * info["rows_per_cta"] >= 1792
     assert info["n_cta"] <= info["sm_count"]
-    assert info["onchip_weight_bytes"] == 1792 * info["k_padded"] * 4
+    assert info["onchip_weight_bytes"] == (info["n_cta"] * info["rows_per_cta"]
+                                           * info["k_padded"] * 4)
 
 
 def test_errors(env):
