@@ -180,6 +180,37 @@ prnn_status_t prnn_pack_sparse_host(int hidden, int k, int n_cta, int rows_per_c
                                     const uint16_t* cols, uint32_t* packed,
                                     size_t capacity_words, int* ept, int* bank_cap);
 
+/*
+ * Forward pass that allocates no device memory.  The pages have no
+ * counterpart to this call: it exists for callers that cannot call
+ * cudaMalloc -- code in a latency-critical loop where cudaMalloc/cudaFree may
+ * synchronize the whole device, or a process whose device memory is owned by
+ * another allocator or capped by a fixed budget.
+ *
+ * Computes the same layer as prnn_forward with dense weights, straight from
+ * the caller's buffers (no handle, no repacking): x [T][B][I] fp32, Wx [H][I]
+ * and Wh [H][H] row-major in `wdtype`, bias [H] fp32, h0 [B][H] fp32 or NULL
+ * (zeros), y [T][B][H] fp32 -- all DEVICE pointers; Wh, y and h0 16-byte
+ * aligned.  It runs the per-step path: the fp32 CUDA-core projection, then T
+ * step kernels reading Wh from memory each step.
+ *
+ * Scratch: the projection P [T][B][H] lives in a file-scope device array of
+ * 4 Mi floats (16 MiB) that the library's CUDA module carries; every GPU on
+ * which the library's kernels are loaded holds it until the process exits.
+ * Limits: T*B*H <= 4194304 and 1 <= B <= 32, else PRNN_ERR_INVALID_ARG.
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress) and caches it; make that first call before
+ * any stream capture.  Every call shares the one array and it keeps the last
+ * call's contents (P is fully rewritten before use, nothing needs zeroing):
+ * calls whose work overlaps on the GPU -- on different streams, or from
+ * different threads -- race on it and must be serialized by the caller.
+ * Asynchronous on `stream`; T == 0 or B == 0 is a no-op.
+ */
+prnn_status_t prnn_forward_dense_noalloc(int T, int B, int H, int I, prnn_dtype_t wdtype,
+                                         const float* x, const void* Wx, const void* Wh,
+                                         const float* bias, const float* h0, float* y,
+                                         void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA, \
 EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
            "prnn_forward", "prnn_destroy", "prnn_get_status", "prnn_status_string",
            "prnn_set_option", "prnn_get_info", "prnn_get_timing", "prnn_probe_sync_floor",
-           "prnn_pack_sparse_host"]
+           "prnn_pack_sparse_host", "prnn_forward_dense_noalloc"]
 
 
 class prnn_info_t(ctypes.Structure):
@@ -62,6 +62,7 @@ _sig = {
     "prnn_probe_sync_floor": ([_P, _I, _I, _P, _P], _I),
     "prnn_pack_sparse_host": ([_I, _I, _I, _I, _I, _P, _P, _P, ctypes.c_size_t,
                                ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
+    "prnn_forward_dense_noalloc": ([_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
 }
 for _name, (_args, _res) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -176,6 +177,14 @@ def prnn_pack_sparse_host(hidden, k, n_cta, rows_per_cta, threads_per_row, vals,
                                       out.size, ctypes.byref(ept), ctypes.byref(cap)),
            "prnn_pack_sparse_host")
     return out, ept.value, cap.value
+
+
+def prnn_forward_dense_noalloc(T, B, H, I, wdtype, x, Wx, Wh, bias, h0, y, stream=None) -> None:
+    """Dense forward from the caller's own device buffers, allocating nothing
+    (see include/prnn.h for the scratch limits and the sharing rules)."""
+    _check(_lib.prnn_forward_dense_noalloc(T, B, H, I, wdtype, _ptr(x), _ptr(Wx), _ptr(Wh),
+                                           _ptr(bias), _ptr(h0), _ptr(y), _stream(stream)),
+           "prnn_forward_dense_noalloc")
 
 
 # ---- convenience wrapper used by the tests and the benchmark ------------------
