@@ -17,7 +17,6 @@ namespace {
 
 constexpr int kMaxBatch = 32;
 constexpr int kSparseMaxThreads = 512;
-constexpr int kDenseMaxThreads = 256;
 
 }  // namespace
 
@@ -472,7 +471,7 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
   }
   h->sparse = false;
   h->k = H;
-  h->tc_proj = false;
+  h->tc_proj = h->wdtype == PRNN_F16 && projection_tc_supported();
   h->weights_set = true;
   return PRNN_OK;
 }
@@ -562,7 +561,7 @@ prnn_status_t prnn_set_weights_sparse(prnn_t h, const void* Wx, int k, const uin
   }
   h->sparse = true;
   h->k = k;
-  h->tc_proj = false;
+  h->tc_proj = h->wdtype == PRNN_F16 && projection_tc_supported();
   h->weights_set = true;
   return PRNN_OK;
 }
@@ -585,8 +584,15 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
   if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[0], s));
 
   // 1. projection for all steps (+ sentinel fill of y on the persistent path)
-  ProjArgs pa{T * B, h->H, h->I, x, h->Wx, h->bias, h->P, persistent ? y : nullptr};
-  PRNN_TRY(launch_projection_simt(pa, h->wdtype == PRNN_F16, s));
+  if (h->tc_proj && h->proj_mode == 0) {
+    PRNN_TRY(ensure_x16(h, (size_t)T * B * h->Kp));
+    ProjTcArgs ta{T * B, h->H, h->I, h->Kp, x, h->x16, h->Wx16, h->bias, h->P,
+                  persistent ? y : nullptr};
+    PRNN_TRY(launch_projection_tc(ta, h->status, s));
+  } else {
+    ProjArgs pa{T * B, h->H, h->I, x, h->Wx, h->bias, h->P, persistent ? y : nullptr};
+    PRNN_TRY(launch_projection_simt(pa, h->wdtype == PRNN_F16, s));
+  }
   if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[1], s));
 
   // 2. recurrence
@@ -725,7 +731,7 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
   info->rows_per_cta = h->R;
   info->threads_per_cta = h->nthreads;
   info->threads_per_row = h->tpr;
-  info->projection_tensor_cores = h->tc_proj;
+  info->projection_tensor_cores = h->tc_proj && h->proj_mode == 0;
   info->sparse_bank_cap = h->sparse ? h->pack_cap : 0;
   info->cta_groups = h->G;
   info->smem_bytes = h->smem_at_max;

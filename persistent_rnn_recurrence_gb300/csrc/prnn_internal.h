@@ -35,7 +35,7 @@ struct ProjTcArgs {
   float* y_fill;         // [M][N] or nullptr
 };
 bool projection_tc_supported();
-cudaError_t launch_projection_tc(const ProjTcArgs& a, cudaStream_t s);
+cudaError_t launch_projection_tc(const ProjTcArgs& a, int* status, cudaStream_t s);
 
 // ---- persistent recurrent kernels --------------------------------------
 struct RecurCommon {

@@ -1,0 +1,377 @@
+// projection_tc.cu -- the input projection on the 5th-generation tensor cores.
+//
+// P[m][n] = bias[n] + sum_k x16[m][k] * Wx16[n][k] for all m = t*B + b at
+// once: the input half of every step does not depend on h_{t-1}, so it is
+// taken out of the serial loop as one dense matrix product ("exposing
+// parallelism between operations", Abstract of "Optimizing Performance of
+// Recurrent Neural Networks on GPUs").  x is rounded to fp16 (RNE) by a
+// staging kernel into a K-padded buffer; Wx is stored fp16, K-padded, at
+// set_weights time; accumulation is fp32 in tensor memory.
+//
+// One CTA computes one 128 x 128 tile of P:
+//   warp 0 / lane 0  TMA producer: 64-wide K slices of the A (x16) and B (Wx16)
+//                    tiles into a 4-stage smem ring (128-byte swizzle),
+//                    completion signalled on a per-stage mbarrier;
+//   warp 1 / lane 0  MMA issuer: 4 x tcgen05.mma (M=128, N=128, K=16) per
+//                    slice into a TMEM accumulator, tcgen05.commit frees the
+//                    slice's stage;
+//   warps 0-3        epilogue: tcgen05.ld of the warp's 32 TMEM lanes (rows),
+//                    + bias, fp32 stores to P (and the sentinel fill of y).
+// Every mbarrier wait is bounded; a timeout sets the status word and the CTA
+// still waits for its issued work, frees its TMEM and returns.
+#include <cuda.h>
+
+#include <cstdint>
+#include <cstdio>
+
+#include "device_common.cuh"
+#include "prnn_internal.h"
+
+namespace prnn {
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64, kStages = 4;
+constexpr int kThreads = 128;
+constexpr uint32_t kTileA = BM * BK * 2;  // 16 KiB
+constexpr uint32_t kTileB = BN * BK * 2;  // 16 KiB
+constexpr uint32_t kStageBytes = kTileA + kTileB;
+constexpr uint32_t kTmemCols = 128;        // fp32 accumulator: 128 lanes x 128 columns
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;  // + alignment slack
+constexpr long long kWaitNs = 200LL * 1000 * 1000;                   // 200 ms per wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "  selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity; false once the deadline passes.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t deadline) {
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++n & 255u) == 0u && global_ns() > deadline) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes (64 fp16), 8-row groups 1024 bytes
+// apart (stride byte offset), tile base 1024-byte aligned.  Fields: start
+// address >> 4 [0,14), leading byte offset >> 4 [16,30) (unused for this
+// layout), stride byte offset >> 4 [32,46), descriptor version 1 [46,48),
+// layout type [61,64) = 2 (128-byte swizzle).
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 [4,6)=1, A fp16
+// [7,10)=0, B fp16 [10,13)=0, both K-major (bits 15, 16 = 0), N >> 3 at
+// [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t f16_idesc(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_load_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+      " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct TcKernelArgs {
+  int M, N, Kp;
+  const float* bias;
+  float* P;
+  float* y_fill;
+  int* status;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    proj_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcKernelArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ __align__(8) uint64_t done_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_err;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int nkb = a.Kp / BK;
+  // 1024-byte aligned ring of stages: [A tile | B tile] per stage
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&done_bar, 1);
+    s_err = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = s_tmem;
+  const uint64_t deadline = global_ns() + (uint64_t)kWaitNs;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer ----
+    int issued = 0;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % kStages;
+      const int round = kb / kStages;
+      if (round > 0 && !mbar_wait(&empty_bar[s], (round - 1) & 1, deadline)) {
+        atomicExch(&s_err, 1);
+        break;
+      }
+      const uint32_t sa = base + (uint32_t)s * kStageBytes;
+      mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
+      tma_load_2d(sa, &tmA, &full_bar[s], kb * BK, m0);
+      tma_load_2d(sa + kTileA, &tmB, &full_bar[s], kb * BK, n0);
+      ++issued;
+    }
+    // every issued load lands before the CTA may leave
+    for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
+      mbar_wait(&full_bar[kb % kStages], (kb / kStages) & 1, deadline + (uint64_t)kWaitNs);
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer ----
+    constexpr uint32_t idesc = f16_idesc(BM, BN);
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % kStages;
+      if (!mbar_wait(&full_bar[s], (kb / kStages) & 1, deadline)) {
+        atomicExch(&s_err, 1);
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t sa = base + (uint32_t)s * kStageBytes;
+#pragma unroll
+      for (int k = 0; k < BK / 16; ++k) {
+        // advancing K by 16 fp16 = 32 bytes inside the 128-byte swizzle atom
+        const uint64_t adesc = sw128_kmajor_desc(sa + (uint32_t)k * 32u);
+        const uint64_t bdesc = sw128_kmajor_desc(sa + kTileA + (uint32_t)k * 32u);
+        umma_f16(tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+      }
+      umma_commit(&empty_bar[s]);  // stage free once these MMAs have read it
+    }
+    umma_commit(&done_bar);        // accumulator complete (or all issued MMAs retired)
+  }
+
+  // ---- epilogue: all four warps, warp w owns TMEM lanes / tile rows 32w..32w+31 ----
+  __syncwarp();
+  const bool ok = mbar_wait(&done_bar, 0, deadline + (uint64_t)kWaitNs);
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (!ok) atomicExch(&s_err, 1);
+  __syncthreads();
+  const bool good = (s_err == 0);
+  if (good) {
+    const int m = m0 + warp * 32 + lane;
+    const bool vec = (a.N & 3) == 0;
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+      uint32_t r[32];
+      tmem_load_32cols(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * 32), r);
+      const int nb = n0 + j * 32;
+      if (m < a.M) {
+        float* prow = a.P + (size_t)m * a.N;
+        float* yrow = a.y_fill ? a.y_fill + (size_t)m * a.N : nullptr;
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const int n = nb + c;
+          if (vec && n + 3 < a.N) {
+            const float4 bv = __ldg(reinterpret_cast<const float4*>(a.bias + n));
+            float4 o;
+            o.x = __uint_as_float(r[c + 0]) + bv.x;
+            o.y = __uint_as_float(r[c + 1]) + bv.y;
+            o.z = __uint_as_float(r[c + 2]) + bv.z;
+            o.w = __uint_as_float(r[c + 3]) + bv.w;
+            *reinterpret_cast<float4*>(prow + n) = o;
+            if (yrow) {
+              const float sv = __uint_as_float(kSentinel);
+              *reinterpret_cast<float4*>(yrow + n) = make_float4(sv, sv, sv, sv);
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (n + q < a.N) {
+                prow[n + q] = __uint_as_float(r[c + q]) + __ldg(a.bias + n + q);
+                if (yrow) yrow[n + q] = __uint_as_float(kSentinel);
+              }
+            }
+          }
+        }
+      }
+    }
+  } else if (tid == 0) {
+    report_timeout(a.status, -1, blockIdx.y * gridDim.x + blockIdx.x);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// x [M][K] fp32 -> x16 [M][Kp] fp16 (round to nearest even), zero for k >= K.
+__global__ void stage_x_f16_kernel(const float* __restrict__ x, __half* __restrict__ x16, int M,
+                                   int K, int Kp) {
+  const int groups = Kp / 8;
+  const size_t total = (size_t)M * groups;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int m = (int)(i / groups), k0 = (int)(i % groups) * 8;
+    const float* row = x + (size_t)m * K;
+    __align__(16) __half h[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) h[j] = __float2half_rn(k0 + j < K ? row[k0 + j] : 0.f);
+    *reinterpret_cast<uint4*>(x16 + (size_t)m * Kp + k0) = *reinterpret_cast<const uint4*>(h);
+  }
+}
+
+// Driver entry point for tensor-map encoding, fetched through the runtime so
+// the library needs no link-time dependency on libcuda.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D fp16 K-major map: dims {Kp, rows}, box {64, 128}, 128-byte swizzle,
+// out-of-range rows read as zeros.
+bool encode_kmajor(CUtensorMap* map, const void* base, int Kp, int rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)Kp * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool projection_tc_supported() { return encode_fn() != nullptr; }
+
+cudaError_t launch_projection_tc(const ProjTcArgs& a, int* status, cudaStream_t s) {
+  if (a.M == 0 || a.N == 0) return cudaSuccess;
+  if (a.Kp % BK != 0 || a.Kp < a.K) return cudaErrorInvalidValue;
+  // 1. x -> fp16, K-padded
+  {
+    const size_t total = (size_t)a.M * (a.Kp / 8);
+    const int blocks = (int)((total + 255) / 256 < 8192 ? (total + 255) / 256 : 8192);
+    stage_x_f16_kernel<<<blocks, 256, 0, s>>>(a.x, reinterpret_cast<__half*>(a.x16), a.M, a.K,
+                                              a.Kp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // 2. tensor-core GEMM
+  CUtensorMap tmA, tmB;
+  if (!encode_kmajor(&tmA, a.x16, a.Kp, a.M, BM) || !encode_kmajor(&tmB, a.Wx16, a.Kp, a.N, BN))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  TcKernelArgs ka{a.M, a.N, a.Kp, a.bias, a.P, a.y_fill, status};
+  const dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
+  proj_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, ka);
+  return cudaGetLastError();
+}
+
+}  // namespace prnn

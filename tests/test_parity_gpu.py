@@ -128,6 +128,25 @@ def test_wh_zero_gives_projection(env):
     assert np.abs(y - ref).max() <= 5e-3 * np.abs(ref).max()
 
 
+@pytest.mark.parametrize("spec", [dict(H=1792, B=4, T=64, k=179),
+                                  dict(H=300, I=200, B=3, T=5, wdtype="f16"),
+                                  dict(H=132, I=40, B=5, T=6, k=12)])
+def test_tensor_core_projection_matches_cuda_core(env, spec):
+    """The tcgen05 projection (x rounded to fp16, fp32 accumulation) and the
+    fp32 CUDA-core projection agree within the fp16 rounding of x, and both
+    paths stay within the oracle rule."""
+    _, prnn, o = env
+    p = synth.make_problem(seed=33, **spec)
+    y_tc, info = run_gpu(env, p)
+    assert info["projection_tensor_cores"] == 1
+    y_cc, info2 = run_gpu(env, p, options={prnn.PRNN_OPT_PROJECTION: 1})
+    assert info2["projection_tensor_cores"] == 0
+    ref = o.forward(p)
+    check(y_tc, ref, "f16", "tc")
+    check(y_cc, ref, "f16", "cuda cores")
+    assert np.abs(y_tc - y_cc).max() <= 5e-3 * np.abs(ref).max()
+
+
 def test_h0_none_equals_zeros(env):
     torch, prnn, _ = env
     p = synth.make_problem(H=256, B=2, T=4, k=20, seed=32)
