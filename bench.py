@@ -276,7 +276,8 @@ def run_ours(args):
     rec_tflops = fl["recurrence"] / (rec_med * 1e-3) / 1e12
     roof = {"bound": "alu", "kernel": "recur_sparse_kernel" if p.sparse else "recur_dense_kernel",
             "achieved": rec_tflops, "peak": fma_peak_tflops, "unit": "TFLOP/s",
-            "frac": rec_tflops / fma_peak_tflops, "traffic": load_traffic(p.name, args.algo),
+            "frac": rec_tflops / fma_peak_tflops,
+            "traffic": load_traffic(p.name, args.algo, p.sparse),
             "peak_source": f"derived: {sm_count} SMs x 128 FP32 lanes x 2 FLOP x {sm_max_mhz:.0f} MHz",
             "t_roof_step_ns": 1e9 * max(t_fma, t_smem),
             "t_step_ns": 1e6 * rec_med / p.T,
@@ -296,7 +297,8 @@ def run_ours(args):
         "stage_ms": {"projection": proj_med, "recurrence": rec_med},
         "roofline": roof,
         "clocks": clocks,
-        "gpu_launches": args.steps * (2 if args.algo == "persistent" else 1 + p.T),
+        "gpu_launches": args.steps * ((2 if info["projection_tensor_cores"] else 1)
+                                      + (1 if args.algo == "persistent" else p.T)),
         "wall_s": wall,
         "plan": {k: info[k] for k in ("n_cta", "rows_per_cta", "threads_per_cta",
                                       "threads_per_row", "k_padded", "smem_bytes",
@@ -378,16 +380,34 @@ def load_peaks() -> dict:
         return {}
 
 
-def load_traffic(workload: str, algo: str):
+KERNEL_SOURCES = {
+    True: ["persistent_sparse.cu", "persistent_common.cuh", "device_common.cuh"],
+    False: ["persistent_dense.cu", "persistent_common.cuh", "device_common.cuh"],
+}
+
+
+def kernel_source_sha1(sparse: bool) -> str:
+    import hashlib
+    h = hashlib.sha1()
+    for name in KERNEL_SOURCES[sparse]:
+        with open(os.path.join(ROOT, "persistent_rnn_recurrence_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def load_traffic(workload: str, algo: str, sparse: bool):
     """DRAM bytes per launch of the recurrent kernel from the committed ncu
-    summary (profiles/traffic.json), or None when not captured for this
-    kernel version."""
+    capture (profiles/traffic.json), or None when it was not captured for this
+    workload or the kernel's source has changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            return json.load(f).get(f"{workload}/{algo}")
+            rec = json.load(f).get(f"{workload}/{algo}")
     except (OSError, ValueError):
         return None
+    if not rec or rec.get("kernel_source_sha1") != kernel_source_sha1(sparse):
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 def main(argv=None):

@@ -1,0 +1,60 @@
+"""CPU tests of the benchmark's multi-rank bookkeeping (replicas only: no
+collective on the data path; the slowest rank's time sets the whole-job
+value).  Two gloo ranks on 127.0.0.1."""
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    r, w, lr = bench.dist_env()
+    bench.barrier(w)
+    # per-rank timed seconds: rank 1 is the slow one
+    t = bench.max_over_ranks(1.5 + rank, w, "cpu")
+    out[rank] = (r, w, lr, t)
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_over_ranks():
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    with ctx.Manager() as m:
+        out = m.dict()
+        procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        res = dict(out)
+    assert res[0] == (0, 2, 0, 2.5) and res[1] == (1, 2, 1, 2.5)
+
+
+def test_single_rank_is_identity():
+    import bench
+    assert bench.max_over_ranks(3.25, 1) == 3.25
+    assert bench.dist_env()[1] == int(os.environ.get("WORLD_SIZE", 1))
+
+
+def test_workload_flops():
+    import bench
+    from persistent_rnn_recurrence_gb300 import synth
+    p = synth.named_problem("sparse_f16_h1792_d10_b4_t256", T=2)
+    f = bench.workload_flops(p)
+    assert f["projection"] == 2.0 * 2 * 4 * 1792 * 1792
+    assert f["recurrence"] == 2.0 * 2 * 4 * 1792 * 179
