@@ -44,6 +44,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip e2e / sync floor / per-step comparison (for profiling runs)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the H x B x density sweep, persistent vs per-step path "
+                         "(one JSON line per point)")
+    ap.add_argument("--sweep-filter", default="", help="only sweep points whose name contains this")
     return ap.parse_args(argv)
 
 
@@ -410,10 +414,59 @@ def load_traffic(workload: str, algo: str, sparse: bool):
     return rec.get("dram_bytes_per_launch")
 
 
+def run_sweep(args):
+    """Persistent vs per-step recurrence time for every sweep point (T = 256,
+    fp16 weights), forward time and per-step time, L2 flushed before each
+    timed forward.  Points whose layer does not fit on chip are reported as
+    unsupported rather than skipped."""
+    import torch
+    from persistent_rnn_recurrence_gb300 import prnn, synth
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    reps = max(3, min(args.steps, 5))
+    for name, kw in synth.sweep_points():
+        if args.sweep_filter and args.sweep_filter not in name:
+            continue
+        p = synth.make_problem(name=name, **kw)
+        x = torch.from_numpy(p.x).to(dev)
+        y = torch.empty((p.T, p.B, p.H), dtype=torch.float32, device=dev)
+        line = {"point": name, "H": p.H, "B": p.B, "k": p.k, "density": p.k / p.H}
+        for algo in ("persistent", "per_step"):
+            try:
+                lay = prnn.Layer.from_problem(p, algo=algo)
+            except prnn.PrnnError as e:
+                line[algo] = {"unsupported": str(e)}
+                continue
+            lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+            prnn.prnn_forward(lay.h, p.T, p.B, x, None, y)
+            ms = []
+            for _ in range(reps):
+                flush.fill_(1.0)
+                prnn.prnn_forward(lay.h, p.T, p.B, x, None, y)
+                ms.append(prnn.prnn_get_timing(lay.h))
+            st = lay.status()
+            info = lay.info()
+            lay.close()
+            rec = sorted(m[1] for m in ms)[len(ms) // 2]
+            proj = sorted(m[0] for m in ms)[len(ms) // 2]
+            line[algo] = {"recurrence_us_per_step": 1e3 * rec / p.T, "projection_ms": proj,
+                          "timesteps_per_s": 1e3 * p.T / (rec + proj),
+                          "status": prnn.prnn_status_string(st),
+                          "groups": info["cta_groups"], "n_cta": info["n_cta"]}
+        if "recurrence_us_per_step" in line.get("persistent", {}) and \
+                "recurrence_us_per_step" in line.get("per_step", {}):
+            line["persistent_speedup"] = (line["per_step"]["recurrence_us_per_step"]
+                                          / line["persistent"]["recurrence_us_per_step"])
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 

@@ -30,7 +30,7 @@ struct prnn_handle {
   int k = 0;
   // persistent plan
   int n_cta = 0, R = 0, nthreads = 0, cpt = 0, tpr = 0, kp = 0, ept = 0, pack_cap = 0;
-  int G = 1, cpg = 0, groups_opt = 0;
+  int G = 1, cpg = 0, groups_opt = 0, dense_bw = 4;
   size_t onchip_bytes = 0, smem_at_max = 0;
   bool tc_proj = false;
   int Kp = 0;  // I rounded up to 64 (tcgen05 projection)
@@ -126,6 +126,7 @@ int max_groups(const prnn_handle* h) {
 DensePlan plan_dense_g(const prnn_handle* h, int G) {
   DensePlan p{};
   const int H = h->H;
+  const bool f16 = h->wdtype == PRNN_F16;
   p.G = G;
   p.cpg = h->sm_count / G;
   p.ok = false;
@@ -133,16 +134,28 @@ DensePlan plan_dense_g(const prnn_handle* h, int G) {
   p.R = (H + p.cpg - 1) / p.cpg;
   p.cpg = (H + p.R - 1) / p.R;
   p.n_cta = p.G * p.cpg;
-  p.bw = recur_dense_bw((h->maxB + G - 1) / G);
-  if (recur_dense_rmax(p.R) == 0) return p;
+  const int rmax = recur_dense_rmax(p.R);
+  if (rmax == 0) return p;
   const int nchunks = H / 4;
-  const int max_nt = recur_dense_max_threads(p.R, p.bw);
-  p.cpt = (nchunks + max_nt - 1) / max_nt;
-  if (p.cpt > 4) return p;
-  // equal chunk counts per thread where the sizes allow
-  p.nthreads = std::max(32, round_up((nchunks + p.cpt - 1) / p.cpt, 32));
-  p.smem = recur_dense_smem(p.R, p.cpt, p.nthreads, h->wdtype == PRNN_F16, p.bw);
-  p.ok = p.smem <= h->smem_optin;
+  // widest batch pass first; within it the most threads; skip variants the
+  // register model says would spill
+  for (int bw = recur_dense_bw((h->maxB + G - 1) / G); bw >= 1; bw /= 2) {
+    for (int cap : {512, 256}) {
+      const int cpt = (nchunks + cap - 1) / cap;
+      if (cpt > 4) continue;
+      const int nt = std::max(32, round_up((nchunks + cpt - 1) / cpt, 32));
+      if (nt > dense_launch_bound(f16, rmax, bw, cpt)) continue;
+      if (dense_reg_estimate(f16, rmax, bw, cpt) > 240) continue;
+      const size_t sm = recur_dense_smem(p.R, cpt, nt, f16, bw);
+      if (sm > h->smem_optin) continue;
+      p.bw = bw;
+      p.cpt = cpt;
+      p.nthreads = nt;
+      p.smem = sm;
+      p.ok = true;
+      return p;
+    }
+  }
   return p;
 }
 
@@ -463,6 +476,7 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
     h->cpg = plan.cpg;
     h->nthreads = plan.nthreads;
     h->cpt = plan.cpt;
+    h->dense_bw = plan.bw;
     h->smem_at_max = plan.smem;
     h->onchip_bytes = pk.size() * plan.G;
   } else {
@@ -615,7 +629,7 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
       PRNN_TRY(launch_recur_sparse(a, s));
     } else {
       DenseRecurArgs a{};
-      const int bw = recur_dense_bw((B + h->G - 1) / h->G);
+      const int bw = std::min(recur_dense_bw((B + h->G - 1) / h->G), h->dense_bw);
       c.smem = recur_dense_smem(h->R, h->cpt, h->nthreads, h->wdtype == PRNN_F16, bw);
       a.c = c;
       a.Wpk = h->Wpk;

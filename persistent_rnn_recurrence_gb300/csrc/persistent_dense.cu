@@ -40,8 +40,8 @@ namespace {
 // warp by a reduce-scatter and across warps through smem.  BW batch columns
 // are processed per pass.
 // ---------------------------------------------------------------------------
-template <bool F16, int RMAX, int BW>
-__global__ void __launch_bounds__((RMAX * BW >= 64) ? 256 : 512, 1)
+template <bool F16, int RMAX, int BW, int CPT>
+__global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
     recur_dense_kernel(const DenseRecurArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int s_abort;
@@ -52,22 +52,32 @@ __global__ void __launch_bounds__((RMAX * BW >= 64) ? 256 : 512, 1)
   const int H = c.H, B = c.B, R = c.R;
   const Place pl = place_of(c);
   const int nchunks = H >> 2;
-  const int cpt = a.cpt;
   constexpr int VB = F16 ? 8 : 16;
   constexpr int V = RMAX * BW;
 
-  unsigned char* Ws = smem;
-  float* red = reinterpret_cast<float*>(smem + (size_t)cpt * R * NT * VB);
+  float* red = reinterpret_cast<float*>(smem + (size_t)CPT * R * NT * VB);
 
   {  // this CTA's weights, loaded once for the whole sequence
-    const size_t bytes = (size_t)cpt * R * NT * VB;
+    const size_t bytes = (size_t)CPT * R * NT * VB;
     const uint4* src = reinterpret_cast<const uint4*>(
         static_cast<const unsigned char*>(a.Wpk) + (size_t)pl.lc * bytes);
-    uint4* dst = reinterpret_cast<uint4*>(Ws);
+    uint4* dst = reinterpret_cast<uint4*>(smem);
     for (size_t i = tid; i < bytes / 16; i += NT) dst[i] = __ldg(src + i);
   }
   if (tid == 0) s_abort = 0;
   __syncthreads();
+
+  // No guards inside the unrolled loops (they stop the compiler from batching
+  // the shared loads): chunk slots past the matrix read chunk 0 of h, rows
+  // past R read row R-1's weights; both multiply zero-padded weights or feed
+  // sums that are never stored.
+  int chv[CPT];
+  bool chok[CPT];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    chok[j] = tid + j * NT < nchunks;
+    chv[j] = chok[j] ? tid + j * NT : 0;
+  }
 
   Waiter w;
   w.status = c.status;
@@ -91,16 +101,17 @@ __global__ void __launch_bounds__((RMAX * BW >= 64) ? 256 : 512, 1)
           pv = ld_nc_pinned(Pt + (size_t)ob * H + orow);
         }
       }
-      // issue every load of h_{t-1} this thread needs, then wait on them
-      float4 hv[kCptMax][BW];
+      // issue every load of h_{t-1} this thread needs (batch columns past nb
+      // reuse column b0), then wait on them
+      float4 hv[CPT][BW];
 #pragma unroll
-      for (int j = 0; j < kCptMax; ++j) {
-        const int ch = tid + j * NT;
+      for (int j = 0; j < CPT; ++j) {
 #pragma unroll
         for (int bb = 0; bb < BW; ++bb) {
+          const int b = bb < nb ? b0 + bb : b0;
           hv[j][bb] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (j < cpt && ch < nchunks && bb < nb && hprev != nullptr) {
-            const float* p = hprev + (size_t)(b0 + bb) * H + ch * 4;
+          if (hprev != nullptr) {
+            const float* p = hprev + (size_t)b * H + chv[j] * 4;
             hv[j][bb] = (t == 0) ? __ldg(reinterpret_cast<const float4*>(p)) : ld_relaxed_f4(p);
           }
         }
@@ -112,22 +123,21 @@ __global__ void __launch_bounds__((RMAX * BW >= 64) ? 256 : 512, 1)
         for (;;) {
           unsigned stale = 0;
 #pragma unroll
-          for (int j = 0; j < kCptMax; ++j)
+          for (int j = 0; j < CPT; ++j)
 #pragma unroll
             for (int bb = 0; bb < BW; ++bb)
-              if (j < cpt && tid + j * NT < nchunks && bb < nb && !ready4(hv[j][bb]))
-                stale |= 1u << (j * BW + bb);
+              if (!ready4(hv[j][bb])) stale |= 1u << (j * BW + bb);
           if (stale == 0u) break;
           if (!w.still_ok(spins)) {
             ok = false;
             break;
           }
 #pragma unroll
-          for (int j = 0; j < kCptMax; ++j)
+          for (int j = 0; j < CPT; ++j)
 #pragma unroll
             for (int bb = 0; bb < BW; ++bb)
               if ((stale >> (j * BW + bb)) & 1u)
-                hv[j][bb] = ld_relaxed_f4(hprev + (size_t)(b0 + bb) * H + (tid + j * NT) * 4);
+                hv[j][bb] = ld_relaxed_f4(hprev + (size_t)(bb < nb ? b0 + bb : b0) * H + chv[j] * 4);
         }
       }
       float acc[RMAX][BW];
@@ -135,36 +145,40 @@ __global__ void __launch_bounds__((RMAX * BW >= 64) ? 256 : 512, 1)
       for (int r = 0; r < RMAX; ++r)
 #pragma unroll
         for (int bb = 0; bb < BW; ++bb) acc[r][bb] = 0.f;
+      // rows in blocks of RB; between blocks the empty asm keeps the next
+      // block's weight loads from being hoisted (bounds the registers in flight)
+      constexpr int RB = dense_row_block(F16, RMAX, BW, CPT);
 #pragma unroll
-      for (int j = 0; j < kCptMax; ++j) {
-        const int ch = tid + j * NT;
-        if (j < cpt && ch < nchunks) {
-          const int wv = j * R * NT + tid;  // vector index of (slot j, row 0)
+      for (int r0 = 0; r0 < RMAX; r0 += RB) {
+        if (RB < RMAX) asm volatile("" ::: "memory");
 #pragma unroll
-          for (int r = 0; r < RMAX; ++r) {
-            if (r < R) {
-              float w0, w1, w2, w3;
-              if constexpr (F16) {
-                const uint2 u = reinterpret_cast<const uint2*>(smem)[wv + r * NT];
-                const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-                const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-                w0 = fa.x; w1 = fa.y; w2 = fb.x; w3 = fb.y;
-              } else {
-                const float4 f = reinterpret_cast<const float4*>(smem)[wv + r * NT];
-                w0 = f.x; w1 = f.y; w2 = f.z; w3 = f.w;
-              }
+      for (int j = 0; j < CPT; ++j) {
+        const int wv = j * R * NT + tid;  // vector index of (slot j, row 0)
 #pragma unroll
-              for (int bb = 0; bb < BW; ++bb) {
-                float s = acc[r][bb];
-                s = fmaf(w0, hv[j][bb].x, s);
-                s = fmaf(w1, hv[j][bb].y, s);
-                s = fmaf(w2, hv[j][bb].z, s);
-                s = fmaf(w3, hv[j][bb].w, s);
-                acc[r][bb] = s;
-              }
-            }
+        for (int r = r0; r < (r0 + RB < RMAX ? r0 + RB : RMAX); ++r) {
+          const int rr = r < R ? r : R - 1;
+          float w0, w1, w2, w3;
+          if constexpr (F16) {
+            const uint2 u = reinterpret_cast<const uint2*>(smem)[wv + rr * NT];
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+            w0 = fa.x; w1 = fa.y; w2 = fb.x; w3 = fb.y;
+          } else {
+            const float4 f = reinterpret_cast<const float4*>(smem)[wv + rr * NT];
+            w0 = f.x; w1 = f.y; w2 = f.z; w3 = f.w;
+          }
+          if (!chok[j]) w0 = w1 = w2 = w3 = 0.f;  // slot past the matrix: chunk 0 was loaded
+#pragma unroll
+          for (int bb = 0; bb < BW; ++bb) {
+            float s = acc[r][bb];
+            s = fmaf(w0, hv[j][bb].x, s);
+            s = fmaf(w1, hv[j][bb].y, s);
+            s = fmaf(w2, hv[j][bb].z, s);
+            s = fmaf(w3, hv[j][bb].w, s);
+            acc[r][bb] = s;
           }
         }
+      }
       }
       float v[V];
 #pragma unroll
@@ -212,10 +226,6 @@ int recur_dense_rmax(int R) {
 
 int recur_dense_bw(int bl) { return bl <= 1 ? 1 : bl <= 2 ? 2 : 4; }
 
-int recur_dense_max_threads(int R, int bw) {
-  return recur_dense_rmax(R) * bw >= 64 ? 256 : 512;
-}
-
 size_t recur_dense_smem(int R, int cpt, int nthreads, bool fp16, int bw) {
   const int rmax = recur_dense_rmax(R);
   return (size_t)cpt * R * nthreads * (fp16 ? 8 : 16) +
@@ -227,13 +237,19 @@ cudaError_t launch_recur_dense(const DenseRecurArgs& a, int bw, cudaStream_t s) 
   const int rmax = recur_dense_rmax(a.c.R);
   const int g = a.c.n_cta, nt = a.c.nthreads;
   const size_t sm = a.c.smem;
-#define PRNN_DENSE_CASE(F, RM, BW_) \
-  if (a.wfp16 == F && rmax == RM && bw == BW_) \
-    return coop_launch(recur_dense_kernel<F, RM, BW_>, g, nt, sm, s, args);
-#define PRNN_DENSE_ROW(F, RM) PRNN_DENSE_CASE(F, RM, 1) PRNN_DENSE_CASE(F, RM, 2) PRNN_DENSE_CASE(F, RM, 4)
+  const int cpt = a.cpt;
+#define PRNN_DENSE_CASE(F, RM, BW_, CP) \
+  if (a.wfp16 == F && rmax == RM && bw == BW_ && cpt == CP) \
+    return coop_launch(recur_dense_kernel<F, RM, BW_, CP>, g, nt, sm, s, args);
+#define PRNN_DENSE_CPT(F, RM, BW_) \
+  PRNN_DENSE_CASE(F, RM, BW_, 1) PRNN_DENSE_CASE(F, RM, BW_, 2) \
+  PRNN_DENSE_CASE(F, RM, BW_, 3) PRNN_DENSE_CASE(F, RM, BW_, 4)
+#define PRNN_DENSE_ROW(F, RM) \
+  PRNN_DENSE_CPT(F, RM, 1) PRNN_DENSE_CPT(F, RM, 2) PRNN_DENSE_CPT(F, RM, 4)
   PRNN_DENSE_ROW(1, 4) PRNN_DENSE_ROW(1, 8) PRNN_DENSE_ROW(1, 16) PRNN_DENSE_ROW(1, 32)
   PRNN_DENSE_ROW(0, 4) PRNN_DENSE_ROW(0, 8) PRNN_DENSE_ROW(0, 16) PRNN_DENSE_ROW(0, 32)
 #undef PRNN_DENSE_ROW
+#undef PRNN_DENSE_CPT
 #undef PRNN_DENSE_CASE
   return cudaErrorInvalidValue;
 }

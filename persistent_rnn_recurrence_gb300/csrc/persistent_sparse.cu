@@ -120,17 +120,16 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
 #pragma unroll
       for (int i = 0; i < BG; ++i) acc[i] = 0.f;
       if (has_row) {
+        // groups past q4 hold zero words (value 0 at column 0): no guard needed
 #pragma unroll
         for (int i = 0; i < REGQ; ++i) {
-          if (i < q4) {
-            const uint32_t ws4[4] = {wr[i].x, wr[i].y, wr[i].z, wr[i].w};
+          const uint32_t ws4[4] = {wr[i].x, wr[i].y, wr[i].z, wr[i].w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float val = __half2float(__ushort_as_half((unsigned short)(ws4[q] & 0xffffu)));
-              const int hi = hs_off + (int)(ws4[q] >> 16);
+          for (int q = 0; q < 4; ++q) {
+            const float val = __half2float(__ushort_as_half((unsigned short)(ws4[q] & 0xffffu)));
+            const int hi = hs_off + (int)(ws4[q] >> 16);
 #pragma unroll
-              for (int b = 0; b < BG; ++b) acc[b] = fmaf(val, smem_f[hi + b * H], acc[b]);
-            }
+            for (int b = 0; b < BG; ++b) acc[b] = fmaf(val, smem_f[hi + b * H], acc[b]);
           }
         }
         for (int i = REGQ; i < q4; ++i) {

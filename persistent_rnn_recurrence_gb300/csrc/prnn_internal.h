@@ -66,7 +66,25 @@ cudaError_t launch_recur_dense(const DenseRecurArgs& a, int bw, cudaStream_t s);
 size_t recur_dense_smem(int R, int cpt, int nthreads, bool fp16, int bw);
 int recur_dense_rmax(int R);   // 0 if R unsupported
 int recur_dense_bw(int batch_cols);          // batch columns per pass: 1, 2 or 4
-int recur_dense_max_threads(int R, int bw);  // launch bound of that instantiation
+
+// Register model of recur_dense_kernel<F16, RMAX, BW, CPT>: accumulators,
+// the thread's h chunks, the weights of RB rows in flight, overhead.  The
+// compiler hoists every weight load of the unrolled loop (best ILP); when
+// that would not fit in registers the rows are processed in blocks of
+// RB = 8.  The model sets the kernel's launch bound (512 threads when it fits
+// 128 registers, else 256) and lets the planner avoid variants that spill.
+__host__ __device__ constexpr int dense_regs_rows(bool f16, int rmax, int bw, int cpt, int rb) {
+  return rmax * bw + cpt * bw * 4 + rb * cpt * (f16 ? 2 : 4) + 32;
+}
+__host__ __device__ constexpr int dense_row_block(bool f16, int rmax, int bw, int cpt) {
+  return dense_regs_rows(f16, rmax, bw, cpt, rmax) <= 240 ? rmax : 8;
+}
+__host__ __device__ constexpr int dense_reg_estimate(bool f16, int rmax, int bw, int cpt) {
+  return dense_regs_rows(f16, rmax, bw, cpt, dense_row_block(f16, rmax, bw, cpt));
+}
+__host__ __device__ constexpr int dense_launch_bound(bool f16, int rmax, int bw, int cpt) {
+  return dense_reg_estimate(f16, rmax, bw, cpt) <= 120 ? 512 : 256;
+}
 
 // Sparse row-balanced: per CTA, R rows x kp entries; thread (row, seg) with
 // seg < tpr owns ept = kp/tpr entries, read as uint4 (4 packed entries).
