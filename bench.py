@@ -48,6 +48,10 @@ def parse_args(argv=None):
                     help="time the H x B x density sweep, persistent vs per-step path "
                          "(one JSON line per point)")
     ap.add_argument("--sweep-filter", default="", help="only sweep points whose name contains this")
+    ap.add_argument("--ablation", action="store_true",
+                    help="the sparse persistent RNN ablation at H=1152, B=4, 10 %%, T=256: "
+                         "plain -> +wide loads -> +bank-aware layout -> +flags in the data, "
+                         "each against the per-step dense path")
     return ap.parse_args(argv)
 
 
@@ -461,12 +465,69 @@ def run_sweep(args):
     return 0
 
 
+def run_ablation(args):
+    """The ablation rows of the sparse persistent RNN measurements (H=1152,
+    B=4, 10 %, T=256), reproduced with this library's switches: each row adds
+    one feature; speedups are against the non-persistent per-step path on the
+    densified matrix (the dense-GEMM-per-step analogue)."""
+    import numpy as np
+    import torch
+    from persistent_rnn_recurrence_gb300 import prnn, synth
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    p = synth.make_problem(H=1152, B=4, T=256, k=synth.sparse_k(1152, 0.10), seed=3000,
+                           name="ablation_sparse_h1152_d10_b4_t256")
+    x = torch.from_numpy(p.x).to(dev)
+    y = torch.empty((p.T, p.B, p.H), dtype=torch.float32, device=dev)
+    reps = max(5, min(args.steps, 10))
+
+    def rec_us(lay):
+        lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+        prnn.prnn_forward(lay.h, p.T, p.B, x, None, y)
+        ms = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            prnn.prnn_forward(lay.h, p.T, p.B, x, None, y)
+            ms.append(prnn.prnn_get_timing(lay.h)[1])
+        assert lay.status() == prnn.PRNN_OK
+        return 1e3 * sorted(ms)[len(ms) // 2] / p.T
+
+    # per-step dense path on the densified matrix
+    dense = synth.Problem(name="densified", T=p.T, B=p.B, H=p.H, I=p.I, wdtype="f16", x=p.x,
+                          Wx=p.Wx, b=p.b, h0=None, Wh=np.zeros((p.H, p.H), np.float16))
+    for r in range(p.H):
+        dense.Wh[r, p.cols[r].astype(np.int64)] = p.vals[r]
+    lay = prnn.Layer.from_problem(dense, algo="per_step")
+    base = rec_us(lay)
+    lay.close()
+    rows = [("sparse persistent, 32-bit loads, plain layout, grid barrier", 0, 0, 1),
+            ("+ wide (128-bit) loads", 1, 0, 1),
+            ("+ bank-aware layout", 1, 1, 1),
+            ("+ flags in the data (no grid barrier)", 1, 1, 0)]
+    out = {"workload": p.name, "per_step_dense_us_per_step": base, "rows": []}
+    for label, wide, bank, barrier in rows:
+        lay = prnn.Layer(p.H, p.I, p.B, "f16", "persistent")
+        lay.set_option(prnn.PRNN_OPT_BANK_AWARE, bank)
+        lay.set_problem_weights(p)
+        lay.set_option(prnn.PRNN_OPT_WIDE_LOADS, wide)
+        lay.set_option(prnn.PRNN_OPT_SYNC_MODE, barrier)
+        us = rec_us(lay)
+        info = lay.info()
+        lay.close()
+        out["rows"].append({"row": label, "us_per_step": us, "speedup_vs_per_step_dense": base / us,
+                            "bank_cap": info["sparse_bank_cap"], "groups": info["cta_groups"]})
+    print(json.dumps(out))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.ablation:
+        return run_ablation(args)
     return run_ours(args)
 
 

@@ -67,7 +67,10 @@ typedef enum {
   PRNN_OPT_DEBUG_DROP_STEP = 3,   /* fault hook: the step whose publish it skips               */
   PRNN_OPT_TIMING = 4,            /* 1: record CUDA events around each stage of forward        */
   PRNN_OPT_PROJECTION = 5,        /* 0: tensor cores when possible (default); 1: fp32 CUDA cores */
-  PRNN_OPT_CTA_GROUPS = 6         /* persistent: CTA groups splitting the batch (0 = automatic);
+  PRNN_OPT_CTA_GROUPS = 6,        /* persistent: CTA groups splitting the batch (0 = automatic);
+                                     takes effect at the next set_weights call                 */
+  PRNN_OPT_WIDE_LOADS = 7,        /* sparse: 1 = stage h with 128-bit loads (default); 0 = 32-bit */
+  PRNN_OPT_BANK_AWARE = 8         /* sparse: 1 = bank-aware entry placement (default); 0 = plain,
                                      takes effect at the next set_weights call                 */
 } prnn_option_t;
 

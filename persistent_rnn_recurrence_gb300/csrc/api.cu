@@ -31,6 +31,7 @@ struct prnn_handle {
   // persistent plan
   int n_cta = 0, R = 0, nthreads = 0, cpt = 0, tpr = 0, kp = 0, ept = 0, pack_cap = 0;
   int G = 1, cpg = 0, groups_opt = 0, dense_bw = 4;
+  int wide_loads = 1, bank_aware = 1;
   size_t onchip_bytes = 0, smem_at_max = 0;
   bool tc_proj = false;
   int Kp = 0;  // I rounded up to 64 (tcgen05 projection)
@@ -533,7 +534,7 @@ prnn_status_t prnn_set_weights_sparse(prnn_t h, const void* Wx, int k, const uin
       const int max_ept = (int)(((h->smem_optin - hs1) / ((size_t)cand.R * cand.tpr * 4)) / 4 * 4);
       plan = cand;
       plan.ept = pack_sparse_rows(H, k, plan.R, plan.cpg, plan.tpr, hv.data(), hc.data(), pk,
-                                  &pst, max_ept);
+                                  &pst, max_ept, h->bank_aware != 0);
       if (plan.ept > 0) {
         packed = true;
         break;
@@ -626,6 +627,7 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
       a.ept = h->ept;
       a.bgroup = bg;
       a.dbuf = db ? 1 : 0;
+      a.narrow = h->wide_loads ? 0 : 1;
       PRNN_TRY(launch_recur_sparse(a, s));
     } else {
       DenseRecurArgs a{};
@@ -723,6 +725,14 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
     case PRNN_OPT_CTA_GROUPS:
       if (value < 0 || value > 32) return PRNN_ERR_INVALID_ARG;
       h->groups_opt = (int)value;
+      return PRNN_OK;
+    case PRNN_OPT_WIDE_LOADS:
+      if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
+      h->wide_loads = (int)value;
+      return PRNN_OK;
+    case PRNN_OPT_BANK_AWARE:
+      if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
+      h->bank_aware = (int)value;
       return PRNN_OK;
   }
   return PRNN_ERR_INVALID_ARG;

@@ -135,9 +135,28 @@ bool colour_warp(const std::vector<std::vector<Entry>>& rows, int tpr, int S, in
 // residue), i.e. shared-memory wavefronts plus per-slot instruction issue,
 // with S <= max_ept (the caller's on-chip capacity).  Returns 0 when even
 // s_min exceeds max_ept.  out_packed is sized n_cta*R*tpr*ept.
+// Plain placement (the "without bank-aware layout" side of the ablation):
+// each row sorted by column, lane l of the row takes entries l*S .. l*S+S-1,
+// padding (value 0, the row's last column) at the end.
+void plain_warp(const std::vector<std::vector<Entry>>& rows, int tpr, int S,
+                std::vector<uint32_t>& out) {
+  out.assign((size_t)32 * S, 0u);
+  for (size_t i = 0; i < rows.size(); ++i) {
+    std::vector<Entry> e = rows[i];
+    if (e.empty()) continue;
+    std::sort(e.begin(), e.end());
+    for (int n = 0; n < tpr * S; ++n) {
+      const int lane = (int)i * tpr + n / S, j = n % S;
+      out[(size_t)lane * S + j] = n < (int)e.size()
+                                      ? ((uint32_t)e[n].second | ((uint32_t)e[n].first << 16))
+                                      : ((uint32_t)e.back().first << 16);
+    }
+  }
+}
+
 int pack_sparse_rows(int H, int k, int R, int n_cta, int tpr, const uint16_t* vals,
                      const uint16_t* cols, std::vector<uint32_t>& out_packed,
-                     PackStats* stats, int max_ept) {
+                     PackStats* stats, int max_ept, bool bank_aware) {
   const int rpw = tpr >= 32 ? 1 : 32 / tpr;
   const int s_min = ((k + tpr - 1) / tpr + 3) / 4 * 4;
   const int warps_per_cta = (R + rpw - 1) / rpw;
@@ -174,10 +193,16 @@ int pack_sparse_rows(int H, int k, int R, int n_cta, int tpr, const uint16_t* va
   }
   std::vector<std::vector<uint32_t>> placed(nwarps);
   int mult = 0;
+  if (!bank_aware) S = s_min;
   for (size_t wi = 0; wi < nwarps; ++wi) {
     int mm = 0;
-    // the degree bounds hold by construction, so the colouring always succeeds
-    colour_warp(wrows[wi], tpr, S, cap_for(dw[wi], S), H, placed[wi], &mm);
+    if (bank_aware) {
+      // the degree bounds hold by construction, so the colouring always succeeds
+      colour_warp(wrows[wi], tpr, S, cap_for(dw[wi], S), H, placed[wi], &mm);
+    } else {
+      plain_warp(wrows[wi], tpr, S, placed[wi]);
+      mm = 32;  // unbounded
+    }
     mult = std::max(mult, mm);
   }
   const int q4 = S / 4;

@@ -132,6 +132,44 @@ __device__ __forceinline__ bool stage_rows(const float* hprev, bool poll, int H,
   return true;
 }
 
+// The same staging with 32-bit loads and stores: the "without wide memory
+// loads" side of the ablation (four times the load instructions and poll
+// checks for the same bytes).
+template <int UMAX>
+__device__ __forceinline__ bool stage_rows_narrow(const float* hprev, bool poll, int H,
+                                                  int b_start, int nb, float* hs, Waiter& w) {
+  const int NT = blockDim.x, tid = threadIdx.x;
+  const int n = nb * H;
+  const float* src = hprev + (size_t)b_start * H;
+  for (int base = tid; base < n; base += UMAX * NT) {
+    float v[UMAX];
+#pragma unroll
+    for (int u = 0; u < UMAX; ++u) {
+      const int i = base + u * NT;
+      v[u] = 0.f;
+      if (i < n && hprev != nullptr) v[u] = poll ? ld_relaxed_f(src + i) : __ldg(src + i);
+    }
+    if (poll) {
+      uint32_t spins = 0;
+      for (;;) {
+        unsigned stale = 0;
+#pragma unroll
+        for (int u = 0; u < UMAX; ++u)
+          if (base + u * NT < n && is_sentinel(v[u])) stale |= 1u << u;
+        if (stale == 0u) break;
+        if (!w.still_ok(spins)) return false;
+#pragma unroll
+        for (int u = 0; u < UMAX; ++u)
+          if ((stale >> u) & 1u) v[u] = ld_relaxed_f(src + base + u * NT);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UMAX; ++u)
+      if (base + u * NT < n) hs[base + u * NT] = v[u];
+  }
+  return true;
+}
+
 template <typename K>
 cudaError_t coop_launch(K kernel, int grid, int block, size_t smem, cudaStream_t s, void** args) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -106,7 +106,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
           owns = true;
         }
       }
-      const bool ok = stage_rows<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w);
+      const bool ok = a.narrow
+                          ? stage_rows_narrow<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w)
+                          : stage_rows<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w);
       if (!ok) {
         report_timeout(c.status, t, cta);
         s_abort = 1;

@@ -93,8 +93,9 @@ struct SparseRecurArgs {
   RecurCommon c;
   const uint32_t* Wpk;   // [n_cta][R][ept/4][tpr] uint4
   int tpr, ept;
-  int bgroup;            // batch columns staged per pass: 4, 8, 16 or 32
+  int bgroup;            // batch columns staged per pass: 1, 2, 4, 8, 16 or 32
   int dbuf;              // 1: two h staging buffers (one CTA barrier per pass)
+  int narrow;            // 1: stage h with 32-bit loads (ablation); 0: 128-bit
 };
 cudaError_t launch_recur_sparse(const SparseRecurArgs& a, cudaStream_t s);
 size_t recur_sparse_smem(int H, int R, int ept, int tpr, int bgroup, bool dbuf);
@@ -110,7 +111,7 @@ struct PackStats {
 };
 int pack_sparse_rows(int H, int k, int R, int n_cta, int tpr, const uint16_t* vals,
                      const uint16_t* cols, std::vector<uint32_t>& out_packed, PackStats* stats,
-                     int max_ept = 1 << 30);
+                     int max_ept = 1 << 30, bool bank_aware = true);
 size_t sync_probe_smem(int H, int bgroup);
 
 // ---- per-step path ------------------------------------------------------

@@ -26,7 +26,8 @@ PRNN_OK, PRNN_ERR_INVALID_ARG, PRNN_ERR_UNSUPPORTED, PRNN_ERR_NOT_READY, \
 PRNN_F32, PRNN_F16 = 0, 1
 PRNN_ALGO_PERSISTENT, PRNN_ALGO_PER_STEP = 0, 1
 PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA, \
-    PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION, PRNN_OPT_CTA_GROUPS = range(7)
+    PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION, PRNN_OPT_CTA_GROUPS, \
+    PRNN_OPT_WIDE_LOADS, PRNN_OPT_BANK_AWARE = range(9)
 
 EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
            "prnn_forward", "prnn_destroy", "prnn_get_status", "prnn_status_string",

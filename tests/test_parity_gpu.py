@@ -195,6 +195,23 @@ def test_grid_barrier_mode_matches_flag_mode(env, spec):
     check(y1, o.forward(p), "f16", "gridbar")
 
 
+@pytest.mark.parametrize("wide,bank,barrier", [(0, 0, 1), (1, 0, 1), (1, 1, 1), (0, 1, 0)])
+def test_ablation_variants_match_oracle(env, wide, bank, barrier):
+    """The ablation switches (32-bit staging loads, plain entry placement,
+    grid barrier) change speed only: results stay within the rule."""
+    torch, prnn, o = env
+    p = synth.make_problem(H=1152, B=4, T=10, k=115, seed=44)
+    lay = prnn.Layer(p.H, p.I, p.B, "f16", "persistent")
+    lay.set_option(prnn.PRNN_OPT_BANK_AWARE, bank)
+    lay.set_problem_weights(p)
+    lay.set_option(prnn.PRNN_OPT_WIDE_LOADS, wide)
+    lay.set_option(prnn.PRNN_OPT_SYNC_MODE, barrier)
+    y = lay.forward(torch.from_numpy(p.x).cuda())
+    assert lay.status() == prnn.PRNN_OK
+    lay.close()
+    check(y.cpu().numpy(), o.forward(p), "f16", f"ablation {wide}{bank}{barrier}")
+
+
 # --- API behaviour ---------------------------------------------------------------
 def test_plan_report(env):
     _, prnn, _ = env
