@@ -36,7 +36,7 @@ FLUSH_BYTES = 256 << 20
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--algo", default="persistent", choices=["persistent", "per_step"])
@@ -52,6 +52,9 @@ def parse_args(argv=None):
                     help="the sparse persistent RNN ablation at H=1152, B=4, 10 %%, T=256: "
                          "plain -> +wide loads -> +bank-aware layout -> +flags in the data, "
                          "each against the per-step dense path")
+    ap.add_argument("--balance", action="store_true",
+                    help="load-balanced versus globally pruned (unbalanced) sparse layers of "
+                         "equal non-zero count, persistent, against the per-step dense path")
     return ap.parse_args(argv)
 
 
@@ -92,12 +95,80 @@ CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+_REASON_BITS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40),
+                ("sw_thermal_slowdown", 0x20), ("sw_power_cap", 0x4))
+
+
+class _NvmlPoller:
+    """Reads the SM clock and the clock-event-reason mask through NVML (read
+    only) every ``period_s`` on a background thread, so that even a timed
+    region of a few milliseconds gets samples."""
+
+    def __init__(self, gpu_id: str, period_s: float = 0.002):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(gpu_id.encode(), ctypes.byref(self.dev)) != 0:
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.dev)) != 0:
+                raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) \
+            or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self.rows = []
+        self.period = period_s
+        self.stop = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _sample(self):
+        ct = self.ct
+        mhz, mask = ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(mhz)) != 0:
+            return
+        if self.reasons_fn(self.dev, ct.byref(mask)) != 0:
+            return
+        self.rows.append((float(mhz.value), self.max_mhz,
+                          ["Active" if mask.value & bit else "Not Active"
+                           for _, bit in _REASON_BITS]))
+
+    def _run(self):
+        while not self.stop.is_set():
+            self._sample()
+            self.stop.wait(self.period)
+
+    def start(self):
+        self._sample()
+        self.thread.start()
+
+    def finish(self):
+        self.stop.set()
+        self.thread.join(timeout=5)
+        self._sample()
+        self.lib.nvmlShutdown()
+        return self.rows
+
+
 class ClockSampler:
+    """SM clocks and throttle reasons during the timed region: NVML polled
+    every 2 ms where the library loads, else ``nvidia-smi -lms 200``."""
+
     def __init__(self, gpu_id: str):
         self.proc = None
+        self.nvml = None
         self.gpu_id = gpu_id
 
     def __enter__(self):
+        try:
+            self.nvml = _NvmlPoller(self.gpu_id)
+            self.nvml.start()
+            return self
+        except (OSError, AttributeError):
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={CLOCK_FIELDS}",
@@ -109,6 +180,9 @@ class ClockSampler:
 
     def __exit__(self, *exc):
         self.out = ""
+        self.rows = None
+        if self.nvml is not None:
+            self.rows = self.nvml.finish()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -119,7 +193,7 @@ class ClockSampler:
         return False
 
     def summary(self) -> dict:
-        rows = []
+        rows = list(self.rows or [])
         for line in (self.out or "").strip().splitlines():
             f = [c.strip() for c in line.split(",")]
             if len(f) < 8:
@@ -131,10 +205,11 @@ class ClockSampler:
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         sm = sorted(r[0] for r in rows)
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        names = tuple(n for n, _ in _REASON_BITS)
         reasons = sorted({names[i] for r in rows for i in range(4) if r[2][i] == "Active"})
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows),
+                "source": "nvml 2 ms" if self.rows else "nvidia-smi 200 ms"}
 
 
 # ---- reference arm: the fp64 CPU oracle -------------------------------------------
@@ -520,6 +595,68 @@ def run_ablation(args):
     return 0
 
 
+def run_balance(args):
+    """Load-balanced versus straightforward pruning: one layer pruned to the
+    same number of non-zeros by global magnitude pruning (rows of unequal
+    length, compressed-row weights) and by per-row pruning (every row the
+    same length), each run persistent; plus the per-step path on the
+    densified unbalanced matrix as the non-persistent baseline."""
+    import numpy as np
+    import torch
+    from persistent_rnn_recurrence_gb300 import prnn, synth
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    reps = max(5, min(args.steps, 10))
+    out = []
+    for H, d in ((2304, 0.25), (1792, 0.10), (5760, 0.05)):
+        unb, bal = synth.make_pruned_pair(H=H, B=4, T=256, density=d, seed=3100 + H,
+                                          name=f"pruned_h{H}_d{int(round(d * 100))}_b4_t256")
+        x = torch.from_numpy(unb.x).to(dev)
+        y = torch.empty((unb.T, unb.B, unb.H), dtype=torch.float32, device=dev)
+
+        def rec_us(p, algo):
+            try:
+                lay = prnn.Layer.from_problem(p, algo=algo)
+            except prnn.PrnnError as e:
+                return None, {"error": str(e)}
+            try:
+                lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+                prnn.prnn_forward(lay.h, p.T, p.B, x, None, y)
+                ms = []
+                for _ in range(reps):
+                    flush.fill_(1.0)
+                    prnn.prnn_forward(lay.h, p.T, p.B, x, None, y)
+                    ms.append(prnn.prnn_get_timing(lay.h)[1])
+                assert lay.status() == prnn.PRNN_OK
+                return 1e3 * sorted(ms)[len(ms) // 2] / p.T, lay.info()
+            except prnn.PrnnError as e:
+                return None, {"error": str(e)}
+            finally:
+                lay.close()
+
+        dense = synth.Problem(name="densified", T=unb.T, B=unb.B, H=H, I=H, wdtype="f16",
+                              x=unb.x, Wx=unb.Wx, b=unb.b, h0=None,
+                              Wh=np.zeros((H, H), np.float16))
+        rows = np.repeat(np.arange(H), np.diff(unb.row_ptr))
+        dense.Wh[rows, unb.cols.astype(np.int64)] = unb.vals
+        lens = np.diff(unb.row_ptr)
+        rec = {"workload": unb.name, "nnz": unb.nnz, "row_len_mean": float(lens.mean()),
+               "row_len_max": int(lens.max()), "row_len_min": int(lens.min())}
+        for key, p, algo in (("per_step_dense", dense, "per_step"),
+                             ("persistent_unbalanced", unb, "persistent"),
+                             ("persistent_balanced", bal, "persistent")):
+            us, info = rec_us(p, algo)
+            rec[key + "_us_per_step"] = us
+            if "error" in info:
+                rec[key + "_error"] = info["error"]
+        if rec["persistent_balanced_us_per_step"] and rec["persistent_unbalanced_us_per_step"]:
+            rec["balanced_speedup"] = (rec["persistent_unbalanced_us_per_step"]
+                                       / rec["persistent_balanced_us_per_step"])
+        out.append(rec)
+    print(json.dumps({"balance": out}))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -528,6 +665,8 @@ def main(argv=None):
         return run_sweep(args)
     if args.ablation:
         return run_ablation(args)
+    if args.balance:
+        return run_balance(args)
     return run_ours(args)
 
 

@@ -123,6 +123,22 @@ prnn_status_t prnn_set_weights_sparse(prnn_t h, const void* Wx, int k,
                                       const float* bias, void* stream);
 
 /*
+ * Set unbalanced sparse recurrent weights in compressed-row form: row r holds
+ * the entries row_ptr[r] .. row_ptr[r+1]-1 of cols (uint16) and vals (fp16
+ * bits); row_ptr has H+1 int32 entries from 0 to nnz; rows may differ in
+ * length (or be empty) -- the matrix straightforward global magnitude pruning
+ * leaves, the comparison point of the load-balanced pruning rows ("Sparse
+ * Persistent RNNs: Squeezing Large Recurrent Networks On-Chip",
+ * measured-effects table).  Columns in [0, H), distinct within a row.  The
+ * library pads every row to the longest row's length with zero-valued
+ * entries, so each row costs as much as the longest: prnn_get_info reports
+ * that length as k.  Otherwise as prnn_set_weights_sparse.
+ */
+prnn_status_t prnn_set_weights_csr(prnn_t h, const void* Wx, int nnz, const int32_t* row_ptr,
+                                   const uint16_t* cols, const uint16_t* vals,
+                                   const float* bias, void* stream);
+
+/*
  * Forward pass: y[t] = h_t for t < T.  x [T][B][I], h0 [B][H] (NULL = zeros),
  * y [T][B][H], all fp32 DEVICE pointers, 16-byte aligned; y must not overlap
  * x or h0.  1 <= B <= max_batch; T == 0 or B == 0 is a no-op.  Asynchronous

@@ -73,6 +73,10 @@ class Oracle:
         L.oracle_rnn_cell_dense.restype = ctypes.c_double
         L.oracle_rnn_cell_sparse.argtypes = [_l, _l, _l, _l, _D, _D, _D, _L, _D, _D]
         L.oracle_rnn_cell_sparse.restype = ctypes.c_double
+        L.oracle_rnn_forward_csr.argtypes = [_l, _l, _l, _l, _D, _D, _L, _D, _L, _D, _D, _D]
+        L.oracle_rnn_forward_csr.restype = ctypes.c_int
+        L.oracle_rnn_cell_csr.argtypes = [_l, _l, _l, _D, _D, _L, _D, _L, _D, _D]
+        L.oracle_rnn_cell_csr.restype = ctypes.c_double
 
     # -- whole sequences -------------------------------------------------
     def forward_dense(self, x, Wx, Wh, b, h0=None) -> np.ndarray:
@@ -107,9 +111,29 @@ class Oracle:
             raise ValueError("oracle_rnn_forward_sparse rejected its arguments")
         return y
 
+    def forward_csr(self, x, Wx, row_ptr, cols, vals, b, h0=None) -> np.ndarray:
+        """y[T,B,H] for unbalanced sparse Wh in compressed-row form:
+        row_ptr[H+1], cols[nnz], vals[nnz]."""
+        x, Wx, vals, b = _f64(x), _f64(Wx), _f64(vals), _f64(b)
+        row_ptr = np.ascontiguousarray(np.asarray(row_ptr, dtype=np.int64))
+        cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+        T, B, I = x.shape
+        H = Wx.shape[0]
+        assert row_ptr.shape == (H + 1,) and cols.shape == vals.shape
+        h0 = None if h0 is None else _f64(h0)
+        y = np.zeros((T, B, H), dtype=np.float64)
+        rc = self.lib.oracle_rnn_forward_csr(T, B, H, I, _ptr(x), _ptr(Wx), _ptr(row_ptr, _L),
+                                             _ptr(vals), _ptr(cols, _L), _ptr(b), _ptr(h0),
+                                             _ptr(y))
+        if rc != 0:
+            raise ValueError("oracle_rnn_forward_csr rejected its arguments")
+        return y
+
     def forward(self, p, T: Optional[int] = None) -> np.ndarray:
         """Run a ``synth.Problem`` (optionally only its first ``T`` steps)."""
         x = p.x if T is None else p.x[:T]
+        if getattr(p, "row_ptr", None) is not None:
+            return self.forward_csr(x, p.Wx, p.row_ptr, p.cols, p.vals, p.b, p.h0)
         if p.sparse:
             return self.forward_sparse(x, p.Wx, p.vals, p.cols, p.b, p.h0)
         return self.forward_dense(x, p.Wx, p.Wh, p.b, p.h0)
@@ -134,7 +158,12 @@ class Oracle:
         Wx = _f64(p.Wx)
         b = _f64(p.b)
         H, I = Wx.shape
-        if p.sparse:
+        csr = getattr(p, "row_ptr", None) is not None
+        if csr:
+            vals = _f64(p.vals)
+            cols = np.ascontiguousarray(p.cols.astype(np.int64))
+            row_ptr = np.ascontiguousarray(p.row_ptr.astype(np.int64))
+        elif p.sparse:
             vals = _f64(p.vals)
             cols = np.ascontiguousarray(p.cols.astype(np.int64))
             k = vals.shape[1]
@@ -144,7 +173,11 @@ class Oracle:
         for i, (t, bb, r) in enumerate(samples):
             x_t = _f64(x_t_of(t, bb))
             h_prev = _f64(h_prev_of(t, bb))
-            if p.sparse:
+            if csr:
+                out[i] = self.lib.oracle_rnn_cell_csr(H, I, r, _ptr(x_t), _ptr(Wx),
+                                                      _ptr(row_ptr, _L), _ptr(vals),
+                                                      _ptr(cols, _L), _ptr(b), _ptr(h_prev))
+            elif p.sparse:
                 out[i] = self.lib.oracle_rnn_cell_sparse(H, I, k, r, _ptr(x_t), _ptr(Wx),
                                                          _ptr(vals), _ptr(cols, _L),
                                                          _ptr(b), _ptr(h_prev))

@@ -106,6 +106,55 @@ int oracle_rnn_forward_sparse(long T, long B, long H, long I, long k,
 }
 
 /*
+ * Unbalanced sparse Wh in compressed-row form: row r holds the entries
+ * row_ptr[r] .. row_ptr[r+1]-1 of (vals, cols), summed in the order given.
+ * This is the matrix straightforward (global, not per-row) magnitude pruning
+ * leaves behind -- rows of unequal length -- the comparison point of the
+ * load-balanced pruning rows of "Sparse Persistent RNNs: Squeezing Large
+ * Recurrent Networks On-Chip" (measured-effects table).
+ */
+double oracle_rnn_cell_csr(long H, long I, long r, const double* x_t, const double* Wx,
+                           const long* row_ptr, const double* vals, const long* cols,
+                           const double* bias, const double* h_prev) {
+    (void)H;
+    double s = bias[r];
+    for (long c = 0; c < I; ++c) s += Wx[r * I + c] * x_t[c];
+    for (long j = row_ptr[r]; j < row_ptr[r + 1]; ++j) s += vals[j] * h_prev[cols[j]];
+    return relu(s);
+}
+
+int oracle_rnn_forward_csr(long T, long B, long H, long I, const double* x,
+                           const double* Wx, const long* row_ptr, const double* vals,
+                           const long* cols, const double* bias, const double* h0,
+                           double* y) {
+    if (T < 0 || B < 0 || H <= 0 || I <= 0) return -1;
+    if (!x || !Wx || !row_ptr || !bias || !y) return -1;
+    if (row_ptr[0] != 0) return -1;
+    for (long r = 0; r < H; ++r)
+        if (row_ptr[r + 1] < row_ptr[r]) return -1;
+    for (long j = 0; j < row_ptr[H]; ++j)
+        if (!vals || !cols || cols[j] < 0 || cols[j] >= H) return -1;
+    if (T == 0 || B == 0) return 0;
+    double* zeros = NULL;
+    if (!h0) {
+        zeros = (double*)calloc((size_t)(B * H), sizeof(double));
+        if (!zeros) return -1;
+        h0 = zeros;
+    }
+    for (long t = 0; t < T; ++t)
+        for (long b = 0; b < B; ++b) {
+            const double* x_t = x + (t * B + b) * I;
+            const double* h_prev = (t == 0) ? h0 + b * H : y + ((t - 1) * B + b) * H;
+            double* out = y + (t * B + b) * H;
+            for (long r = 0; r < H; ++r)
+                out[r] = oracle_rnn_cell_csr(H, I, r, x_t, Wx, row_ptr, vals, cols, bias,
+                                             h_prev);
+        }
+    free(zeros);
+    return 0;
+}
+
+/*
  * The input projection on its own, P[t,b,r] = bias[r] + sum_c Wx[r,c] x[t,b,c]:
  * the part of every step that does not depend on h_{t-1} and so can be done for
  * all steps at once ("exposing parallelism between operations", Abstract of

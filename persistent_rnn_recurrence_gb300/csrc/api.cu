@@ -361,6 +361,72 @@ RecurCommon common_args(const prnn_handle* h, int T, int B, const float* h0, flo
 
 }  // namespace
 
+// Plan, pack and upload row-padded sparse weights: hv/hc are [H][k] with each
+// row sorted by column (padding entries: value 0).  Shared by the
+// row-balanced and the compressed-row entry points.
+static prnn_status_t install_sparse(prnn_t h, const void* Wx, const float* bias,
+                                    std::vector<uint16_t>& hv, std::vector<uint16_t>& hc, int k) {
+  const int H = h->H;
+  SparsePlan plan{};
+  std::vector<uint32_t> pk;
+  PackStats pst;
+  if (h->algo == PRNN_ALGO_PERSISTENT) {
+    bool packed = false;
+    for (const SparsePlan& cand : plan_sparse(h, k)) {
+      // largest entries-per-thread whose weights plus one h column fit in smem
+      const size_t hs1 = (size_t)H * sizeof(float);
+      if (hs1 >= h->smem_optin) continue;
+      const int max_ept = (int)(((h->smem_optin - hs1) / ((size_t)cand.R * cand.tpr * 4)) / 4 * 4);
+      plan = cand;
+      plan.ept = pack_sparse_rows(H, k, plan.R, plan.cpg, plan.tpr, hv.data(), hc.data(), pk,
+                                  &pst, max_ept, h->bank_aware != 0);
+      if (plan.ept > 0) {
+        packed = true;
+        break;
+      }
+    }
+    if (!packed) return PRNN_ERR_UNSUPPORTED;
+    plan.kp = plan.ept * plan.tpr;
+  }
+  free_weights(h);
+  prnn_status_t st = stage_wx_bias(h, Wx, bias, &h->Wx, &h->Wx16, &h->bias);
+  if (st != PRNN_OK) return st;
+  auto entry = [&](int r, int j) -> uint32_t {
+    return (uint32_t)hv[(size_t)r * k + j] | ((uint32_t)hc[(size_t)r * k + j] << 16);
+  };
+  if (h->algo == PRNN_ALGO_PERSISTENT) {
+    PRNN_TRY(upload(&h->Wpk, pk.data(), pk.size() * 4));
+    h->n_cta = plan.n_cta;
+    h->R = plan.R;
+    h->G = plan.G;
+    h->cpg = plan.cpg;
+    h->nthreads = plan.nthreads;
+    h->tpr = plan.tpr;
+    h->kp = plan.kp;
+    h->ept = plan.ept;
+    h->pack_cap = pst.cap;
+    h->onchip_bytes = (size_t)plan.n_cta * plan.R * plan.kp * 4;  // all groups' copies
+    int bg = 4;
+    bool db = false;
+    size_t sm = 0;
+    sparse_batch_plan(h, h->maxB, &bg, &db, &sm);
+    h->smem_at_max = sm;
+  } else {
+    std::vector<uint32_t> ws((size_t)H * k);
+    for (int r = 0; r < H; ++r)
+      for (int j = 0; j < k; ++j) ws[(size_t)r * k + j] = entry(r, j);
+    PRNN_TRY(upload(&h->Wstep, ws.data(), ws.size() * 4));
+    h->onchip_bytes = 0;
+    h->kp = k;
+  }
+  h->sparse = true;
+  h->k = k;
+  h->tc_proj = h->wdtype == PRNN_F16 && projection_tc_supported();
+  h->weights_set = true;
+  return PRNN_OK;
+}
+
+
 extern "C" {
 
 const char* prnn_status_string(prnn_status_t s) {
@@ -522,63 +588,66 @@ prnn_status_t prnn_set_weights_sparse(prnn_t h, const void* Wx, int k, const uin
       hv[(size_t)r * k + j] = row[j].second;
     }
   }
-  SparsePlan plan{};
-  std::vector<uint32_t> pk;
-  PackStats pst;
-  if (h->algo == PRNN_ALGO_PERSISTENT) {
-    bool packed = false;
-    for (const SparsePlan& cand : plan_sparse(h, k)) {
-      // largest entries-per-thread whose weights plus one h column fit in smem
-      const size_t hs1 = (size_t)H * sizeof(float);
-      if (hs1 >= h->smem_optin) continue;
-      const int max_ept = (int)(((h->smem_optin - hs1) / ((size_t)cand.R * cand.tpr * 4)) / 4 * 4);
-      plan = cand;
-      plan.ept = pack_sparse_rows(H, k, plan.R, plan.cpg, plan.tpr, hv.data(), hc.data(), pk,
-                                  &pst, max_ept, h->bank_aware != 0);
-      if (plan.ept > 0) {
-        packed = true;
-        break;
-      }
+  return install_sparse(h, Wx, bias, hv, hc, k);
+}
+
+prnn_status_t prnn_set_weights_csr(prnn_t h, const void* Wx, int nnz, const int32_t* row_ptr,
+                                   const uint16_t* cols, const uint16_t* vals, const float* bias,
+                                   void* stream) {
+  if (!h || !Wx || !row_ptr || !bias || nnz < 0) return PRNN_ERR_INVALID_ARG;
+  if (nnz > 0 && (!cols || !vals)) return PRNN_ERR_INVALID_ARG;
+  if (h->sticky_timeout) return PRNN_ERR_TIMEOUT;
+  if (h->wdtype != PRNN_F16) return PRNN_ERR_INVALID_ARG;
+  const int H = h->H;
+  if (H > 65535) return PRNN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PRNN_TRY(cudaStreamSynchronize(s));
+  std::vector<int32_t> rp((size_t)H + 1);
+  std::vector<uint16_t> cv((size_t)nnz), vv((size_t)nnz);
+  PRNN_TRY(to_host(rp.data(), row_ptr, rp.size() * 4));
+  if (nnz > 0) {
+    PRNN_TRY(to_host(cv.data(), cols, cv.size() * 2));
+    PRNN_TRY(to_host(vv.data(), vals, vv.size() * 2));
+  }
+  // validate: offsets monotone from 0 to nnz, columns in range and distinct per row
+  if (rp[0] != 0 || rp[H] != nnz) return PRNN_ERR_INVALID_ARG;
+  int kmax = 1;
+  for (int r = 0; r < H; ++r) {
+    if (rp[r + 1] < rp[r]) return PRNN_ERR_INVALID_ARG;
+    kmax = std::max(kmax, rp[r + 1] - rp[r]);
+  }
+  std::vector<int> seen((size_t)H, -1);
+  for (int r = 0; r < H; ++r)
+    for (int j = rp[r]; j < rp[r + 1]; ++j) {
+      const int c = cv[j];
+      if (c >= H || seen[c] == r) return PRNN_ERR_INVALID_ARG;
+      seen[c] = r;
     }
-    if (!packed) return PRNN_ERR_UNSUPPORTED;
-    plan.kp = plan.ept * plan.tpr;
+  // pad every row to the longest one with zero-valued entries: the kernels
+  // then give every row kmax entries of work (the cost of imbalance).  The
+  // padding takes the columns the row lacks, in ascending order, so padded
+  // rows keep distinct columns spread over the shared-memory banks.
+  std::vector<uint16_t> hv((size_t)H * kmax, 0), hc((size_t)H * kmax, 0);
+  std::vector<std::pair<uint16_t, uint16_t>> row;
+  std::vector<int> in_row((size_t)H, -1);
+  for (int r = 0; r < H; ++r) {
+    row.clear();
+    for (int j = rp[r]; j < rp[r + 1]; ++j) {
+      row.push_back({cv[j], vv[j]});
+      in_row[cv[j]] = r;
+    }
+    for (int c = 0; c < H && (int)row.size() < kmax; ++c)
+      if (in_row[c] != r) row.push_back({(uint16_t)c, 0});
+    std::sort(row.begin(), row.end(),
+              [](const std::pair<uint16_t, uint16_t>& a, const std::pair<uint16_t, uint16_t>& b) {
+                return a.first < b.first;
+              });
+    for (int j = 0; j < kmax; ++j) {
+      hc[(size_t)r * kmax + j] = row[j].first;
+      hv[(size_t)r * kmax + j] = row[j].second;
+    }
   }
-  free_weights(h);
-  prnn_status_t st = stage_wx_bias(h, Wx, bias, &h->Wx, &h->Wx16, &h->bias);
-  if (st != PRNN_OK) return st;
-  auto entry = [&](int r, int j) -> uint32_t {
-    return (uint32_t)hv[(size_t)r * k + j] | ((uint32_t)hc[(size_t)r * k + j] << 16);
-  };
-  if (h->algo == PRNN_ALGO_PERSISTENT) {
-    PRNN_TRY(upload(&h->Wpk, pk.data(), pk.size() * 4));
-    h->n_cta = plan.n_cta;
-    h->R = plan.R;
-    h->G = plan.G;
-    h->cpg = plan.cpg;
-    h->nthreads = plan.nthreads;
-    h->tpr = plan.tpr;
-    h->kp = plan.kp;
-    h->ept = plan.ept;
-    h->pack_cap = pst.cap;
-    h->onchip_bytes = (size_t)plan.n_cta * plan.R * plan.kp * 4;  // all groups' copies
-    int bg = 4;
-    bool db = false;
-    size_t sm = 0;
-    sparse_batch_plan(h, h->maxB, &bg, &db, &sm);
-    h->smem_at_max = sm;
-  } else {
-    std::vector<uint32_t> ws((size_t)H * k);
-    for (int r = 0; r < H; ++r)
-      for (int j = 0; j < k; ++j) ws[(size_t)r * k + j] = entry(r, j);
-    PRNN_TRY(upload(&h->Wstep, ws.data(), ws.size() * 4));
-    h->onchip_bytes = 0;
-    h->kp = k;
-  }
-  h->sparse = true;
-  h->k = k;
-  h->tc_proj = h->wdtype == PRNN_F16 && projection_tc_supported();
-  h->weights_set = true;
-  return PRNN_OK;
+  return install_sparse(h, Wx, bias, hv, hc, kmax);
 }
 
 prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* h0, float* y,

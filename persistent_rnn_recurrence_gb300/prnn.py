@@ -32,7 +32,7 @@ PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA, \
 EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
            "prnn_forward", "prnn_destroy", "prnn_get_status", "prnn_status_string",
            "prnn_set_option", "prnn_get_info", "prnn_get_timing", "prnn_probe_sync_floor",
-           "prnn_pack_sparse_host", "prnn_forward_dense_noalloc"]
+           "prnn_pack_sparse_host", "prnn_forward_dense_noalloc", "prnn_set_weights_csr"]
 
 
 class prnn_info_t(ctypes.Structure):
@@ -64,6 +64,7 @@ _sig = {
     "prnn_pack_sparse_host": ([_I, _I, _I, _I, _I, _P, _P, _P, ctypes.c_size_t,
                                ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
     "prnn_forward_dense_noalloc": ([_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
+    "prnn_set_weights_csr": ([_P, _P, _I, _P, _P, _P, _P, _P], _I),
 }
 for _name, (_args, _res) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -122,6 +123,12 @@ def prnn_set_weights_sparse(h: int, Wx, k: int, vals, cols, bias, stream=None) -
     _check(_lib.prnn_set_weights_sparse(h, _ptr(Wx), int(k), _ptr(vals), _ptr(cols),
                                         _ptr(bias), _stream(stream)),
            "prnn_set_weights_sparse")
+
+
+def prnn_set_weights_csr(h: int, Wx, nnz: int, row_ptr, cols, vals, bias, stream=None) -> None:
+    _check(_lib.prnn_set_weights_csr(h, _ptr(Wx), int(nnz), _ptr(row_ptr), _ptr(cols),
+                                     _ptr(vals), _ptr(bias), _stream(stream)),
+           "prnn_set_weights_csr")
 
 
 def prnn_forward(h: int, T: int, B: int, x, h0, y, stream=None) -> None:
@@ -216,7 +223,12 @@ class Layer:
         wt = torch.float16 if p.wdtype == "f16" else torch.float32
         Wx = torch.from_numpy(np.ascontiguousarray(p.Wx)).to(device=device, dtype=wt)
         b = torch.from_numpy(np.ascontiguousarray(p.b)).to(device)
-        if p.sparse:
+        if getattr(p, "row_ptr", None) is not None:
+            rp = torch.from_numpy(np.ascontiguousarray(p.row_ptr, dtype=np.int32)).to(device)
+            vals = torch.from_numpy(np.ascontiguousarray(p.vals).view(np.int16)).to(device)
+            cols = torch.from_numpy(np.ascontiguousarray(p.cols).view(np.int16)).to(device)
+            prnn_set_weights_csr(self.h, Wx, int(p.vals.size), rp, cols, vals, b)
+        elif p.sparse:
             vals = torch.from_numpy(np.ascontiguousarray(p.vals).view(np.int16)).to(device)
             cols = torch.from_numpy(np.ascontiguousarray(p.cols).view(np.int16)).to(device)
             prnn_set_weights_sparse(self.h, Wx, p.k, vals, cols, b)

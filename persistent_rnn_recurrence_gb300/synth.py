@@ -25,7 +25,7 @@ from typing import Optional
 import numpy as np
 
 __all__ = ["Problem", "make_problem", "named_problem", "NAMED", "sweep_points",
-           "sparse_k"]
+           "sparse_k", "make_pruned_pair"]
 
 
 @dataclasses.dataclass
@@ -42,9 +42,10 @@ class Problem:
     b: np.ndarray                    # float32 [H]
     h0: Optional[np.ndarray]         # float32 [B, H] or None (zeros)
     Wh: Optional[np.ndarray] = None  # wdtype [H, H] (dense problems)
-    vals: Optional[np.ndarray] = None  # float16 [H, k] (sparse problems)
-    cols: Optional[np.ndarray] = None  # uint16 [H, k], ascending, distinct per row
+    vals: Optional[np.ndarray] = None  # float16 [H, k] (sparse) or [nnz] (compressed rows)
+    cols: Optional[np.ndarray] = None  # uint16 [H, k] ascending, distinct per row; or [nnz]
     seed: int = 0
+    row_ptr: Optional[np.ndarray] = None  # int32 [H+1]: unbalanced compressed-row form
 
     @property
     def sparse(self) -> bool:
@@ -52,10 +53,15 @@ class Problem:
 
     @property
     def k(self) -> int:
+        """Non-zeros per row (compressed rows: the longest row)."""
+        if self.row_ptr is not None:
+            return int(np.diff(self.row_ptr).max())
         return int(self.vals.shape[1]) if self.sparse else self.H
 
     @property
     def nnz(self) -> int:
+        if self.row_ptr is not None:
+            return int(self.vals.size)
         return self.H * self.k
 
 
@@ -164,3 +170,40 @@ def sweep_points():
                 name = f"sweep_h{H}_b{B}_d{int(round(d * 100))}"
                 yield name, kw
                 i += 1
+
+
+def make_pruned_pair(*, H: int, B: int, T: int, density: float, seed: int,
+                     row_sigma: float = 0.25, name: str = "pruned"):
+    """The same layer pruned two ways, for the balanced-versus-unbalanced
+    comparison: a dense score matrix Z[r][c] = s_r * N(0,1) with per-row
+    scales s_r = exp(row_sigma * N(0,1)) (rows of a trained layer differ in
+    magnitude), then
+      * unbalanced: keep the floor(density*H*H) largest |Z| over the whole
+        matrix (global magnitude pruning) -> rows of unequal length;
+      * balanced: keep the k = floor(density*H) largest |Z| of every row.
+    Kept positions get fresh values N(0, 0.9/sqrt(row length)) (fp16), so both
+    recurrences stay stable.  x, Wx, b are shared.  Returns (unbalanced,
+    balanced) Problems; the unbalanced one is in compressed-row form."""
+    rng = np.random.default_rng(seed)
+    x = rng.normal(0.0, 1.0, size=(T, B, H)).astype(np.float32)
+    Wx = rng.normal(0.0, 1.0 / math.sqrt(H), size=(H, H)).astype(np.float16)
+    b = rng.uniform(-0.1, 0.1, size=(H,)).astype(np.float32)
+    scale = np.exp(row_sigma * rng.standard_normal(H)).astype(np.float32)
+    Z = np.abs(rng.standard_normal((H, H)).astype(np.float32)) * scale[:, None]
+    k = sparse_k(H, density)
+    keep = H * k
+    thr = np.partition(Z.ravel(), Z.size - keep)[Z.size - keep]
+    mask = Z >= thr
+    lens = mask.sum(axis=1)
+    row_ptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cols_u = np.nonzero(mask)[1].astype(np.uint16)            # row-major, ascending per row
+    vals_u = np.concatenate([rng.normal(0.0, 0.9 / math.sqrt(max(n, 1)), size=n)
+                             for n in lens]).astype(np.float16)
+    top = np.argpartition(-Z, k - 1, axis=1)[:, :k]
+    cols_b = np.sort(top, axis=1).astype(np.uint16)
+    vals_b = rng.normal(0.0, 0.9 / math.sqrt(k), size=(H, k)).astype(np.float16)
+    unb = Problem(name=name + "_unbalanced", T=T, B=B, H=H, I=H, wdtype="f16", x=x, Wx=Wx,
+                  b=b, h0=None, vals=vals_u, cols=cols_u, seed=seed, row_ptr=row_ptr)
+    bal = Problem(name=name + "_balanced", T=T, B=B, H=H, I=H, wdtype="f16", x=x, Wx=Wx,
+                  b=b, h0=None, vals=vals_b, cols=cols_b, seed=seed)
+    return unb, bal

@@ -170,6 +170,29 @@ def pin_sparse_equals_densified(o):
     assert np.array_equal(ys, yd)
 
 
+def pin_csr_equals_densified_and_balanced(o):
+    """Unbalanced compressed rows (some empty, some full): bit-identical to
+    the dense form of the same matrix (entries sorted by column), and to the
+    row-balanced form when every row has the same length."""
+    rng = np.random.default_rng(19)
+    T, B, H, I = 4, 2, 9, 6
+    lens = np.array([0, 9, 3, 1, 5, 2, 7, 4, 3])
+    row_ptr = np.concatenate([[0], np.cumsum(lens)])
+    cols = np.concatenate([np.sort(rng.choice(H, n, replace=False)) for n in lens])
+    vals = _rand(rng, int(lens.sum()), scale=0.4)
+    x, Wx, b, h0 = _rand(rng, T, B, I), _rand(rng, H, I), _rand(rng, H), _rand(rng, B, H)
+    Wh = np.zeros((H, H))
+    for r in range(H):
+        Wh[r, cols[row_ptr[r]:row_ptr[r + 1]]] = vals[row_ptr[r]:row_ptr[r + 1]]
+    assert np.array_equal(o.forward_csr(x, Wx, row_ptr, cols, vals, b, h0),
+                          o.forward_dense(x, Wx, Wh, b, h0))
+    k = 3
+    bc = np.stack([np.sort(rng.choice(H, k, replace=False)) for _ in range(H)])
+    bv = _rand(rng, H, k, scale=0.4)
+    assert np.array_equal(o.forward_csr(x, Wx, np.arange(H + 1) * k, bc.ravel(), bv.ravel(), b),
+                          o.forward_sparse(x, Wx, bv, bc, b))
+
+
 def pin_chaining(o):
     rng = np.random.default_rng(17)
     T1, T2, B, H, I = 3, 4, 2, 9, 9

@@ -28,7 +28,8 @@ def test_cells_match_forward(o):
     whole-sequence driver, element for element."""
     from persistent_rnn_recurrence_gb300 import synth
     for p in (synth.make_problem(H=40, B=3, T=3, I=24, wdtype="f32", seed=3, h0_std=0.5),
-              synth.make_problem(H=40, B=3, T=3, k=7, seed=4)):
+              synth.make_problem(H=40, B=3, T=3, k=7, seed=4),
+              synth.make_pruned_pair(H=40, B=3, T=3, density=0.1, seed=5, row_sigma=1.0)[0]):
         y = o.forward(p)
         samples = [(t, b, r) for t in range(p.T) for b in range(p.B) for r in (0, 17, 39)]
         h0 = np.zeros((p.B, p.H)) if p.h0 is None else p.h0
@@ -60,6 +61,7 @@ MUTANTS = {
     "x_batch_index": ("x + (t * B + b) * I", "x + (t * B) * I"),
     "x_time_shift": ("x + (t * B + b) * I", "x + (((t + 1) % T) * B + b) * I"),
     "dropped_recurrent_term": ("s += Wh[r * H + c] * h_prev[c];", "(void)h_prev;"),
+    "csr_row_end_off_by_one": ("j < row_ptr[r + 1]; ++j", "j < row_ptr[r + 1] - 1; ++j"),
 }
 
 

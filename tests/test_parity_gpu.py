@@ -290,6 +290,74 @@ def test_host_weight_pointers(env):
     check(y.cpu().numpy(), o.forward(p), "f16", "host pointers")
 
 
+# --- unbalanced compressed rows (global magnitude pruning) ---------------------------
+@pytest.mark.parametrize("algo", ["persistent", "per_step"])
+@pytest.mark.parametrize("spec", [dict(H=300, B=3, T=6, density=0.05, row_sigma=1.0),
+                                  dict(H=40, B=2, T=5, density=0.1, row_sigma=1.0),
+                                  dict(H=2304, B=4, T=12, density=0.25, row_sigma=0.25)])
+def test_csr_unbalanced_matches_oracle(env, spec, algo):
+    """Rows of unequal length, empty rows included: the library pads each row
+    to the longest one; the result is that of the compressed-row definition."""
+    unb, bal = synth.make_pruned_pair(seed=70, **spec)
+    assert (np.diff(unb.row_ptr) != unb.k).any()
+    for p in (unb, bal):
+        y, info = run_gpu(env, p, algo)
+        assert info["k"] == p.k
+        check(y, env[2].forward(p), "f16", f"{p.name}/{algo}")
+
+
+def test_csr_full_size_teacher_forced_samples(env):
+    """The 25 %-dense H = 2304 globally pruned layer at T = 256 in the
+    benchmarked configuration, checked by one oracle step per sampled output
+    applied to the GPU's own previous state."""
+    p, _ = synth.make_pruned_pair(H=2304, B=4, T=256, density=0.25, seed=71)
+    y, _ = run_gpu(env, p)
+    assert np.isfinite(y).all()
+    rng = np.random.default_rng(6)
+    samples = [(int(t), int(b), int(r)) for t, b, r in zip(
+        rng.integers(0, p.T, 200), rng.integers(0, p.B, 200), rng.integers(0, p.H, 200))]
+    samples.append((p.T - 1, p.B - 1, int(np.argmax(np.diff(p.row_ptr)))))
+    got = np.array([y[t, b, r] for t, b, r in samples], dtype=np.float64)
+    want = env[2].cells(p, samples, lambda t, b: p.x[t, b],
+                        lambda t, b: np.zeros(p.H) if t == 0 else y[t - 1, b])
+    assert np.abs(got - want).max() <= TOL["f16"] * float(np.abs(y).max())
+
+
+def test_csr_errors(env):
+    torch, prnn, _ = env
+    p, _ = synth.make_pruned_pair(H=64, B=2, T=3, density=0.1, seed=72, row_sigma=1.0)
+    lay = prnn.prnn_create(64, 64, 2, prnn.PRNN_F16, prnn.PRNN_ALGO_PERSISTENT)
+    Wx = torch.from_numpy(p.Wx).cuda()
+    b = torch.from_numpy(p.b).cuda()
+    vals = torch.from_numpy(p.vals.view(np.int16)).cuda()
+    nnz = p.nnz
+
+    def put(rp, cols, n=nnz):
+        return prnn.prnn_set_weights_csr(
+            lay, Wx, n, torch.from_numpy(rp.astype(np.int32)).cuda(),
+            torch.from_numpy(cols.view(np.int16)).cuda(), vals, b)
+
+    bad_rp = p.row_ptr.copy()
+    bad_rp[10], bad_rp[11] = bad_rp[11] + 1, bad_rp[10]       # decreasing offsets
+    for rp, cols, n in ((bad_rp, p.cols, nnz), (p.row_ptr, p.cols, nnz - 1)):
+        with pytest.raises(prnn.PrnnError) as e:
+            put(rp, cols, n)
+        assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    lens = np.diff(p.row_ptr)
+    r = int(np.argmax(lens >= 2))
+    dup = p.cols.copy()
+    dup[p.row_ptr[r] + 1] = dup[p.row_ptr[r]]                 # duplicate column in a row
+    oob = p.cols.copy()
+    oob[0] = 64                                               # column out of range
+    for cols in (dup, oob):
+        with pytest.raises(prnn.PrnnError) as e:
+            put(p.row_ptr, cols)
+        assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    put(p.row_ptr, p.cols)
+    assert prnn.prnn_get_info(lay)["k"] == int(lens.max())
+    prnn.prnn_destroy(lay)
+
+
 # --- bounded waits: a publish that never happens ends in a status, not a hang --------
 @pytest.mark.parametrize("spec", [dict(H=512, B=4, T=6, k=40), dict(H=512, B=4, T=6, wdtype="f16")])
 def test_dropped_publish_times_out_cleanly(env, spec):
