@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--balance", action="store_true",
                     help="load-balanced versus globally pruned (unbalanced) sparse layers of "
                          "equal non-zero count, persistent, against the per-step dense path")
+    ap.add_argument("--stack", action="store_true",
+                    help="stacked layers: one-launch wavefront vs layer by layer, L = 1, 2, 4")
     return ap.parse_args(argv)
 
 
@@ -657,6 +659,54 @@ def run_balance(args):
     return 0
 
 
+def run_stack(args):
+    """Stacked dense fp16 layers (H=1152, B=4, T=256): the one-launch wavefront
+    against the layer-by-layer path (batched projection + persistent
+    recurrence per layer), L = 1, 2, 4."""
+    import torch
+    from persistent_rnn_recurrence_gb300 import prnn, synth
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    reps = max(5, min(args.steps, 20))
+    out = []
+    for L in (1, 2, 4):
+        p = synth.make_stack_problem(L=L, H=1152, B=4, T=256, wdtype="f16", seed=3200 + L,
+                                     name=f"stack_l{L}_h1152_b4_t256")
+        x = torch.from_numpy(p.x).to(dev)
+        y = torch.empty((L, p.T, p.B, p.H), dtype=torch.float32, device=dev)
+        rec = {"workload": p.name, "layers": L}
+        for algo in ("wavefront", "layerwise"):
+            try:
+                st = prnn.Stack.from_problem(p, algo=algo)
+            except prnn.PrnnError as e:
+                rec[algo] = {"error": str(e)}
+                continue
+            try:
+                st.set_option(prnn.PRNN_OPT_TIMING, 1)
+                for _ in range(3):
+                    flush.fill_(1.0)
+                    st.forward(x, None, y)
+                ms = []
+                for _ in range(reps):
+                    flush.fill_(1.0)
+                    st.forward(x, None, y)
+                    ms.append(prnn.prnn_stack_get_timing(st.h))
+                assert st.status() == prnn.PRNN_OK
+                med = sorted(ms)[len(ms) // 2]
+                rec[algo] = {"ms_per_forward": med, "ms_min": min(ms), "ms_max": max(ms),
+                             "timesteps_per_s": p.T / (med * 1e-3),
+                             "us_per_step": 1e3 * med / p.T, "plan": st.info()}
+            finally:
+                st.close()
+        if "ms_per_forward" in rec.get("wavefront", {}) and \
+                "ms_per_forward" in rec.get("layerwise", {}):
+            rec["wavefront_speedup"] = (rec["layerwise"]["ms_per_forward"]
+                                        / rec["wavefront"]["ms_per_forward"])
+        out.append(rec)
+    print(json.dumps({"stack": out}))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -667,6 +717,8 @@ def main(argv=None):
         return run_ablation(args)
     if args.balance:
         return run_balance(args)
+    if args.stack:
+        return run_stack(args)
     return run_ours(args)
 
 

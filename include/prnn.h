@@ -230,6 +230,95 @@ prnn_status_t prnn_forward_dense_noalloc(int T, int B, int H, int I, prnn_dtype_
                                          const float* bias, const float* h0, float* y,
                                          void* stream);
 
+/* ---- stacked layers ---------------------------------------------------
+ *
+ * A stack of L dense ReLU RNN layers, each with `hidden` units: layer 0 reads
+ * x, layer l > 0 reads layer l-1's output sequence:
+ *
+ *     h^l_t = ReLU(b_l + Wx_l h^{l-1}_t + Wh_l h^l_{t-1}),   h^{-1}_t = x_t,
+ *
+ * the multi-layer network that "Optimizing Performance of Recurrent Neural
+ * Networks on GPUs" (Abstract) optimises as a whole, with the on-chip weights
+ * of the persistent-rnn page ("What This Project Does").
+ *
+ * PRNN_STACK_WAVEFRONT runs the whole stack in ONE persistent cooperative
+ * launch: the SMs are split into L slices, slice l keeps [Wx_l | Wh_l] on
+ * chip and computes step t of layer l as soon as layer l-1 has published its
+ * step t, so the stack takes about T + L - 1 step times instead of L * T.
+ * All L layers' weights must fit on chip at once (about
+ * L * hidden * (hidden + input) * weight-size bytes over the SMs' shared
+ * memory), else PRNN_ERR_UNSUPPORTED from prnn_stack_create.
+ * PRNN_STACK_LAYERWISE runs the layers one after another, each as
+ * prnn_forward does (batched input projection, then its persistent
+ * recurrence); it is the comparison point of the wavefront.
+ */
+typedef struct prnn_stack* prnn_stack_t;
+
+typedef enum {
+  PRNN_STACK_WAVEFRONT = 0,
+  PRNN_STACK_LAYERWISE = 1
+} prnn_stack_algo_t;
+
+/*
+ * Create a stack: 1 <= layers <= 8; hidden, input >= 1 and, for the
+ * wavefront, multiples of 4; 1 <= max_batch <= 32; weights fp32 or fp16.
+ * Plans the launch for the current device.  Errors: INVALID_ARG (sizes),
+ * UNSUPPORTED (weights cannot all be on chip, or no usable GPU), OOM.
+ */
+prnn_status_t prnn_stack_create(prnn_stack_t* out, int layers, int hidden, int input,
+                                int max_batch, prnn_dtype_t wdtype, prnn_stack_algo_t algo);
+
+/*
+ * Set layer `layer` (0 .. layers-1): Wx [hidden][I_l] with I_0 = input and
+ * I_l = hidden for l > 0, Wh [hidden][hidden], both row-major in the stack's
+ * dtype; bias [hidden] fp32.  Device or host pointers; the library copies and
+ * repacks them, synchronizing `stream` first, so the caller may free them on
+ * return.
+ */
+prnn_status_t prnn_stack_set_layer(prnn_stack_t s, int layer, const void* Wx, const void* Wh,
+                                   const float* bias, void* stream);
+
+/*
+ * Forward the stack over T steps for B <= max_batch sequences: x [T][B][input]
+ * fp32; h0 [layers][B][hidden] fp32 or NULL (zeros); y [layers][T][B][hidden]
+ * fp32 receives every layer's output sequence (the top layer is
+ * y + (layers-1)*T*B*hidden).  Device pointers, 16-byte aligned; y must not
+ * overlap x or h0.  Asynchronous on `stream`; T == 0 or B == 0 is a no-op.
+ * Errors: NOT_READY until every layer is set; INVALID_ARG; a wait that runs
+ * out inside the launch makes the stack report PRNN_ERR_TIMEOUT from then on.
+ */
+prnn_status_t prnn_stack_forward(prnn_stack_t s, int T, int B, const float* x, const float* h0,
+                                 float* y, void* stream);
+
+/* Synchronize `stream`, then report the stack's device status (sticky TIMEOUT). */
+prnn_status_t prnn_stack_get_status(prnn_stack_t s, void* stream);
+
+/*
+ * Options: PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_TIMING (events around the last
+ * forward, read with prnn_stack_get_timing), PRNN_OPT_DEBUG_DROP_CTA /
+ * PRNN_OPT_DEBUG_DROP_STEP (the CTA index counts over all slices; wavefront
+ * only), PRNN_OPT_CTA_GROUPS (wavefront: force the batch groups per slice;
+ * re-plans and clears the layers, which must be set again).  Others:
+ * INVALID_ARG.
+ */
+prnn_status_t prnn_stack_set_option(prnn_stack_t s, prnn_option_t opt, long long value);
+
+/* Milliseconds of the last timed forward (PRNN_ERR_NOT_READY if none). */
+prnn_status_t prnn_stack_get_timing(prnn_stack_t s, float* ms);
+
+typedef struct {
+  int layers, hidden, input, max_batch, wdtype, algo, layers_set;
+  int n_cta_per_layer;     /* wavefront: CTAs of one layer slice                     */
+  int rows_per_cta, threads_per_cta, cta_groups, batch_per_pass, chunks_per_thread;
+  long long smem_bytes;    /* dynamic shared memory per CTA                          */
+  long long onchip_weight_bytes;  /* all slices, all groups                          */
+} prnn_stack_info_t;
+
+prnn_status_t prnn_stack_get_info(prnn_stack_t s, prnn_stack_info_t* info);
+
+/* Free everything the stack owns.  NULL is accepted. */
+prnn_status_t prnn_stack_destroy(prnn_stack_t s);
+
 #ifdef __cplusplus
 }
 #endif

@@ -129,9 +129,26 @@ class Oracle:
             raise ValueError("oracle_rnn_forward_csr rejected its arguments")
         return y
 
+    def forward_stack(self, x, layers, h0=None) -> np.ndarray:
+        """y[L,T,B,H] of a stack of dense layers: layer 0 reads x, layer l > 0
+        reads layer l-1's output sequence; layers[l] = (Wx_l, Wh_l, b_l),
+        h0[L,B,H] or None.  The definition of stacking written out: each
+        layer is the pinned single-layer oracle applied to the layer below's
+        output ("Optimizing Performance of Recurrent Neural Networks on
+        GPUs", Abstract: multi-layer networks)."""
+        ys = []
+        inp = x
+        for l, (Wx, Wh, b) in enumerate(layers):
+            y = self.forward_dense(inp, Wx, Wh, b, None if h0 is None else h0[l])
+            ys.append(y)
+            inp = y
+        return np.stack(ys)
+
     def forward(self, p, T: Optional[int] = None) -> np.ndarray:
         """Run a ``synth.Problem`` (optionally only its first ``T`` steps)."""
         x = p.x if T is None else p.x[:T]
+        if getattr(p, "layers", None) is not None:
+            return self.forward_stack(x, p.layers, p.h0)
         if getattr(p, "row_ptr", None) is not None:
             return self.forward_csr(x, p.Wx, p.row_ptr, p.cols, p.vals, p.b, p.h0)
         if p.sparse:

@@ -172,8 +172,20 @@ __device__ __forceinline__ bool stage_rows_narrow(const float* hprev, bool poll,
 
 template <typename K>
 cudaError_t coop_launch(K kernel, int grid, int block, size_t smem, cudaStream_t s, void** args) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  // One CTA per SM: a persistent grid with fewer CTAs than SMs must not have
+  // two CTAs share an SM (the block scheduler may pack them when registers and
+  // shared memory allow, and the shared SM then sets every step's pace).
+  // Asking for more than half of an SM's shared memory rules that out.
+  int dev = 0, per_sm_smem = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&per_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  const size_t one_per_sm = (size_t)per_sm_smem / 2 + 1024;
+  if (smem < one_per_sm && one_per_sm <= (size_t)optin) smem = one_per_sm;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, smem);

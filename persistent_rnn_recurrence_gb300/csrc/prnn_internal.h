@@ -86,6 +86,35 @@ __host__ __device__ constexpr int dense_launch_bound(bool f16, int rmax, int bw,
   return dense_reg_estimate(f16, rmax, bw, cpt) <= 120 ? 512 : 256;
 }
 
+// Stacked dense layers in one persistent launch (persistent_stack.cu).  Grid
+// = L slices of c.n_cta CTAs; slice l computes layer l from the concatenated
+// weights [Wx_l | Wh_l] (K = I_l + H columns), packed per CTA like the dense
+// kernel's weights.  All layers share H, R, G, cpg, nthreads and cpt.
+constexpr int kStackMaxLayers = 8;
+struct StackLayerArgs {
+  const void* Wpk;       // [cpg][cpt][R][nthreads] vec4 of [Wx_l | Wh_l]
+  const float* bias;     // [H]
+  const float* xin;      // [T][B][I]: x (layer 0) or y of layer l-1
+  float* y;              // [T][B][H], pre-filled with the sentinel
+  const float* h0;       // [B][H] or nullptr
+  int I;                 // input width (multiple of 4)
+  int poll_in;           // 1: xin is produced during this launch (poll it)
+};
+struct StackArgs {
+  RecurCommon c;         // per-slice plan; c.P, c.y, c.h0 unused
+  int L, cpt, wfp16;
+  StackLayerArgs layer[kStackMaxLayers];
+};
+cudaError_t launch_recur_stack(const StackArgs& a, int bw, cudaStream_t s);
+// Variants of the stack kernel that compile without spills (measured with
+// -Xptxas -v): the dense register model plus the per-slot source offsets,
+// and no 32-row variant with 8 or more (batch x chunk) vectors in flight.
+__host__ __device__ constexpr bool stack_variant_ok(bool f16, int rmax, int bw, int cpt) {
+  return dense_reg_estimate(f16, rmax, bw, cpt) + 4 * cpt + 8 <= 240 &&
+         !(rmax == 32 && bw * cpt >= 8) && !(rmax == 32 && !f16 && cpt == 4);
+}
+size_t recur_stack_smem(int R, int cpt, int nthreads, bool fp16, int bw);
+
 // Sparse row-balanced: per CTA, R rows x kp entries; thread (row, seg) with
 // seg < tpr owns ept = kp/tpr entries, read as uint4 (4 packed entries).
 // Packed entry = fp16 value bits | (column << 16).

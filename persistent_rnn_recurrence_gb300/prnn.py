@@ -29,10 +29,15 @@ PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA, \
     PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION, PRNN_OPT_CTA_GROUPS, \
     PRNN_OPT_WIDE_LOADS, PRNN_OPT_BANK_AWARE = range(9)
 
+PRNN_STACK_WAVEFRONT, PRNN_STACK_LAYERWISE = 0, 1
+
 EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
            "prnn_forward", "prnn_destroy", "prnn_get_status", "prnn_status_string",
            "prnn_set_option", "prnn_get_info", "prnn_get_timing", "prnn_probe_sync_floor",
-           "prnn_pack_sparse_host", "prnn_forward_dense_noalloc", "prnn_set_weights_csr"]
+           "prnn_pack_sparse_host", "prnn_forward_dense_noalloc", "prnn_set_weights_csr",
+           "prnn_stack_create", "prnn_stack_set_layer", "prnn_stack_forward",
+           "prnn_stack_get_status", "prnn_stack_set_option", "prnn_stack_get_timing",
+           "prnn_stack_get_info", "prnn_stack_destroy"]
 
 
 class prnn_info_t(ctypes.Structure):
@@ -42,6 +47,17 @@ class prnn_info_t(ctypes.Structure):
         "threads_per_row", "projection_tensor_cores", "sparse_bank_cap", "cta_groups")] + [
         ("smem_bytes", ctypes.c_size_t), ("onchip_weight_bytes", ctypes.c_size_t),
         ("nnz", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class prnn_stack_info_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "layers", "hidden", "input", "max_batch", "wdtype", "algo", "layers_set",
+        "n_cta_per_layer", "rows_per_cta", "threads_per_cta", "cta_groups", "batch_per_pass",
+        "chunks_per_thread")] + [
+        ("smem_bytes", ctypes.c_longlong), ("onchip_weight_bytes", ctypes.c_longlong)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -65,6 +81,14 @@ _sig = {
                                ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
     "prnn_forward_dense_noalloc": ([_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
     "prnn_set_weights_csr": ([_P, _P, _I, _P, _P, _P, _P, _P], _I),
+    "prnn_stack_create": ([ctypes.POINTER(_P), _I, _I, _I, _I, _I, _I], _I),
+    "prnn_stack_set_layer": ([_P, _I, _P, _P, _P, _P], _I),
+    "prnn_stack_forward": ([_P, _I, _I, _P, _P, _P, _P], _I),
+    "prnn_stack_get_status": ([_P, _P], _I),
+    "prnn_stack_set_option": ([_P, _I, ctypes.c_longlong], _I),
+    "prnn_stack_get_timing": ([_P, ctypes.POINTER(ctypes.c_float)], _I),
+    "prnn_stack_get_info": ([_P, ctypes.POINTER(prnn_stack_info_t)], _I),
+    "prnn_stack_destroy": ([_P], _I),
 }
 for _name, (_args, _res) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -195,6 +219,48 @@ def prnn_forward_dense_noalloc(T, B, H, I, wdtype, x, Wx, Wh, bias, h0, y, strea
            "prnn_forward_dense_noalloc")
 
 
+def prnn_stack_create(layers: int, hidden: int, input: int, max_batch: int, wdtype: int,
+                      algo: int) -> int:
+    out = _P()
+    _check(_lib.prnn_stack_create(ctypes.byref(out), layers, hidden, input, max_batch, wdtype,
+                                  algo), "prnn_stack_create")
+    return out.value
+
+
+def prnn_stack_set_layer(s: int, layer: int, Wx, Wh, bias, stream=None) -> None:
+    _check(_lib.prnn_stack_set_layer(s, layer, _ptr(Wx), _ptr(Wh), _ptr(bias), _stream(stream)),
+           "prnn_stack_set_layer")
+
+
+def prnn_stack_forward(s: int, T: int, B: int, x, h0, y, stream=None) -> None:
+    _check(_lib.prnn_stack_forward(s, T, B, _ptr(x), _ptr(h0), _ptr(y), _stream(stream)),
+           "prnn_stack_forward")
+
+
+def prnn_stack_get_status(s: int, stream=None) -> int:
+    return _lib.prnn_stack_get_status(s, _stream(stream))
+
+
+def prnn_stack_set_option(s: int, opt: int, value: int) -> None:
+    _check(_lib.prnn_stack_set_option(s, opt, int(value)), "prnn_stack_set_option")
+
+
+def prnn_stack_get_timing(s: int) -> float:
+    ms = ctypes.c_float()
+    _check(_lib.prnn_stack_get_timing(s, ctypes.byref(ms)), "prnn_stack_get_timing")
+    return ms.value
+
+
+def prnn_stack_get_info(s: int) -> dict:
+    info = prnn_stack_info_t()
+    _check(_lib.prnn_stack_get_info(s, ctypes.byref(info)), "prnn_stack_get_info")
+    return info.as_dict()
+
+
+def prnn_stack_destroy(s: int) -> None:
+    _check(_lib.prnn_stack_destroy(s), "prnn_stack_destroy")
+
+
 # ---- convenience wrapper used by the tests and the benchmark ------------------
 class Layer:
     """One RNN layer handle.  ``Layer.from_problem(p)`` uploads a
@@ -258,6 +324,67 @@ class Layer:
     def close(self):
         if getattr(self, "h", None):
             prnn_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Stack:
+    """A stack of dense layers (``prnn_stack_*``).  ``Stack.from_problem(p)``
+    uploads a ``synth.StackProblem``'s weights and returns the stack."""
+
+    def __init__(self, layers, hidden, input, max_batch, wdtype="f16", algo="wavefront"):
+        self.layers, self.hidden, self.input = layers, hidden, input
+        wd = {"f32": PRNN_F32, "f16": PRNN_F16}[wdtype]
+        al = {"wavefront": PRNN_STACK_WAVEFRONT, "layerwise": PRNN_STACK_LAYERWISE}[algo]
+        self.h = prnn_stack_create(layers, hidden, input, max_batch, wd, al)
+
+    @classmethod
+    def from_problem(cls, p, algo="wavefront", max_batch=None, device="cuda"):
+        st = cls(p.L, p.H, p.I, max_batch or max(1, p.B), p.wdtype, algo)
+        try:
+            st.set_problem_weights(p, device)
+        except Exception:
+            st.close()
+            raise
+        return st
+
+    def set_problem_weights(self, p, device="cuda"):
+        import numpy as np
+        import torch
+        wt = torch.float16 if p.wdtype == "f16" else torch.float32
+        for l, (Wx, Wh, b) in enumerate(p.layers):
+            prnn_stack_set_layer(
+                self.h, l, torch.from_numpy(np.ascontiguousarray(Wx)).to(device=device, dtype=wt),
+                torch.from_numpy(np.ascontiguousarray(Wh)).to(device=device, dtype=wt),
+                torch.from_numpy(np.ascontiguousarray(b)).to(device))
+        torch.cuda.synchronize()
+
+    def forward(self, x, h0=None, y=None, stream=None):
+        """x: [T,B,I] fp32 CUDA tensor; returns y [L,T,B,H] (every layer's output)."""
+        import torch
+        T, B, _ = x.shape
+        if y is None:
+            y = torch.empty((self.layers, T, B, self.hidden), dtype=torch.float32, device=x.device)
+        prnn_stack_forward(self.h, T, B, x, h0, y, stream)
+        return y
+
+    def status(self, stream=None) -> int:
+        return prnn_stack_get_status(self.h, stream)
+
+    def info(self) -> dict:
+        return prnn_stack_get_info(self.h)
+
+    def set_option(self, opt, value):
+        prnn_stack_set_option(self.h, opt, value)
+
+    def close(self):
+        if getattr(self, "h", None):
+            prnn_stack_destroy(self.h)
             self.h = None
 
     def __del__(self):

@@ -25,7 +25,7 @@ from typing import Optional
 import numpy as np
 
 __all__ = ["Problem", "make_problem", "named_problem", "NAMED", "sweep_points",
-           "sparse_k", "make_pruned_pair"]
+           "sparse_k", "make_pruned_pair", "StackProblem", "make_stack_problem"]
 
 
 @dataclasses.dataclass
@@ -207,3 +207,47 @@ def make_pruned_pair(*, H: int, B: int, T: int, density: float, seed: int,
     bal = Problem(name=name + "_balanced", T=T, B=B, H=H, I=H, wdtype="f16", x=x, Wx=Wx,
                   b=b, h0=None, vals=vals_b, cols=cols_b, seed=seed)
     return unb, bal
+
+
+@dataclasses.dataclass
+class StackProblem:
+    """L dense layers: layer 0 reads x [T,B,I], layer l > 0 reads layer l-1's
+    output; every layer has H units.  layers[l] = (Wx [H, I_l], Wh [H, H],
+    b [H]); h0 [L, B, H] or None (zeros)."""
+    name: str
+    T: int
+    B: int
+    H: int
+    I: int
+    L: int
+    wdtype: str
+    x: np.ndarray
+    layers: list
+    h0: Optional[np.ndarray]
+    seed: int = 0
+
+
+def make_stack_problem(*, L: int, H: int, B: int, T: int, I: Optional[int] = None,
+                       wdtype: str = "f16", seed: int = 0, h0_std: Optional[float] = None,
+                       name: str = "stack") -> StackProblem:
+    """Draw order from ``default_rng(seed)``: x ~ N(0, 1); then per layer
+    Wx ~ N(0, 0.9/sqrt(I_l)), Wh ~ N(0, 0.9/sqrt(H)), b ~ U(-0.1, 0.1);
+    then h0 ~ N(0, h0_std) if asked."""
+    I = H if I is None else I
+    if L < 1 or T < 0 or B < 0 or H <= 0 or I <= 0:
+        raise ValueError("need L >= 1, T, B >= 0 and H, I > 0")
+    wt = _np_dtype(wdtype)
+    rng = np.random.default_rng(seed)
+    x = rng.normal(0.0, 1.0, size=(T, B, I)).astype(np.float32)
+    layers = []
+    for l in range(L):
+        il = I if l == 0 else H
+        Wx = rng.normal(0.0, 0.9 / math.sqrt(il), size=(H, il)).astype(wt)
+        Wh = rng.normal(0.0, 0.9 / math.sqrt(H), size=(H, H)).astype(wt)
+        b = rng.uniform(-0.1, 0.1, size=(H,)).astype(np.float32)
+        layers.append((Wx, Wh, b))
+    h0 = None
+    if h0_std is not None:
+        h0 = rng.normal(0.0, h0_std, size=(L, B, H)).astype(np.float32)
+    return StackProblem(name=name, T=T, B=B, H=H, I=I, L=L, wdtype=wdtype, x=x, layers=layers,
+                        h0=h0, seed=seed)

@@ -193,6 +193,38 @@ def pin_csr_equals_densified_and_balanced(o):
                           o.forward_sparse(x, Wx, bv, bc, b))
 
 
+def pin_stack_definition(o):
+    """Stacked layers: (1) one layer is the single-layer oracle; (2) a top
+    layer with Wx = identity, Wh = 0, b = 0 reproduces the layer below exactly
+    (ReLU of a non-negative sequence is itself), which a top layer reading x
+    instead of the layer below, or taking another layer's h0, breaks; (3) two
+    layers of dyadic data with distinct h0 per layer equal exact rational
+    brute force applied layer on layer."""
+    rng = np.random.default_rng(20)
+    T, B, H, I = 4, 2, 5, 3
+    x = _rand(rng, T, B, I)
+    Wx0, Wh0, b0 = _rand(rng, H, I), _rand(rng, H, H, scale=0.4), _rand(rng, H)
+    h0 = _rand(rng, 2, B, H)
+    y1 = o.forward_stack(x, [(Wx0, Wh0, b0)], h0[:1])
+    assert y1.shape == (1, T, B, H)
+    assert np.array_equal(y1[0], o.forward_dense(x, Wx0, Wh0, b0, h0[0]))
+    ident = (np.eye(H), np.zeros((H, H)), np.zeros(H))
+    y2 = o.forward_stack(x, [(Wx0, Wh0, b0), ident], np.stack([h0[0], 5.0 + h0[1]]))
+    assert np.array_equal(y2[1], y2[0]) and (y2[0] > 0).any()
+    # exact rational, two layers
+    xd = _dyadic(rng, T, B, I)
+    L0 = (_dyadic(rng, H, I), _dyadic(rng, H, H), _dyadic(rng, H))
+    L1 = (_dyadic(rng, H, H), _dyadic(rng, H, H), _dyadic(rng, H))
+    hd = _dyadic(rng, 2, B, H)
+    y = o.forward_stack(xd, [L0, L1], hd)
+    r0 = forward_exact(xd.tolist(), L0[0].tolist(), L0[1].tolist(), L0[2].tolist(), hd[0].tolist())
+    assert y[0].tolist() == [[[float(v) for v in row] for row in step] for step in r0]
+    r1 = forward_exact(y[0].tolist(), L1[0].tolist(), L1[1].tolist(), L1[2].tolist(),
+                       hd[1].tolist())
+    assert y[1].tolist() == [[[float(v) for v in row] for row in step] for step in r1]
+    assert (y[1] > 0).any() and (y[1] == 0).any()
+
+
 def pin_chaining(o):
     rng = np.random.default_rng(17)
     T1, T2, B, H, I = 3, 4, 2, 9, 9

@@ -80,3 +80,27 @@ def test_pins_catch_planted_mistake(tmp_path, name):
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
                        cwd=ROOT, timeout=120)
     assert r.returncode != 0, f"mutant {name} passed every pin"
+
+
+# Plausible mistakes in the Python part of the oracle (the stacking of
+# layers), planted in a copy of oracle.py loaded as a separate module.
+PY_MUTANTS = {
+    "stack_reads_x": ("            inp = y\n", "            inp = x\n"),
+    "stack_same_h0": ("None if h0 is None else h0[l]", "None if h0 is None else h0[0]"),
+    "stack_reversed": ("enumerate(layers)", "enumerate(layers[::-1])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_stack_pins_catch_planted_mistake(name):
+    import types
+    old, new = PY_MUTANTS[name]
+    path = os.path.join(ROOT, "oracle", "oracle.py")
+    src = open(path).read()
+    assert old in src, f"mutation anchor for {name} not found"
+    mod = types.ModuleType("oracle_mutant")
+    mod.__file__ = path
+    exec(compile(src.replace(old, new), path, "exec"), mod.__dict__)
+    o = mod.Oracle(oracle.oracle.LIB)
+    with pytest.raises(AssertionError):
+        oracle_pins.pin_stack_definition(o)
