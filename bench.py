@@ -56,7 +56,8 @@ def parse_args(argv=None):
                     help="load-balanced versus globally pruned (unbalanced) sparse layers of "
                          "equal non-zero count, persistent, against the per-step dense path")
     ap.add_argument("--stack", action="store_true",
-                    help="stacked layers: one-launch wavefront vs layer by layer, L = 1, 2, 4")
+                    help="stacked layers: one-launch wavefront vs layer by layer, "
+                         "H = 256 / 512 / 1152, L = 1 .. 8")
     return ap.parse_args(argv)
 
 
@@ -660,21 +661,22 @@ def run_balance(args):
 
 
 def run_stack(args):
-    """Stacked dense fp16 layers (H=1152, B=4, T=256): the one-launch wavefront
-    against the layer-by-layer path (batched projection + persistent
-    recurrence per layer), L = 1, 2, 4."""
+    """Stacked dense fp16 layers (B=4, T=256): the one-launch wavefront against
+    the layer-by-layer path (batched projection + persistent recurrence per
+    layer), for H = 256, 512, 1152 and L = 1, 2, 4, 8 (where the weights fit)."""
     import torch
     from persistent_rnn_recurrence_gb300 import prnn, synth
     dev = torch.device("cuda", 0)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     reps = max(5, min(args.steps, 20))
     out = []
-    for L in (1, 2, 4):
-        p = synth.make_stack_problem(L=L, H=1152, B=4, T=256, wdtype="f16", seed=3200 + L,
-                                     name=f"stack_l{L}_h1152_b4_t256")
+    for H, L in ((256, 1), (256, 2), (256, 4), (256, 8), (512, 2), (512, 4), (512, 8),
+                 (1152, 1), (1152, 2), (1152, 4)):
+        p = synth.make_stack_problem(L=L, H=H, B=4, T=256, wdtype="f16", seed=3200 + L,
+                                     name=f"stack_l{L}_h{H}_b4_t256")
         x = torch.from_numpy(p.x).to(dev)
         y = torch.empty((L, p.T, p.B, p.H), dtype=torch.float32, device=dev)
-        rec = {"workload": p.name, "layers": L}
+        rec = {"workload": p.name, "layers": L, "H": H}
         for algo in ("wavefront", "layerwise"):
             try:
                 st = prnn.Stack.from_problem(p, algo=algo)
