@@ -50,6 +50,7 @@ struct prnn_handle {
   unsigned* bar = nullptr;   // grid-barrier counter
   // options
   long long timeout_us = 500000;
+  int poll_delay_ns = -1, clock_khz = 0;  // -1: the kernel family's default
   int sync_mode = 0, drop_cta = -1, drop_step = -1, timing = 0, proj_mode = 0;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   bool ev_valid = false;
@@ -307,6 +308,9 @@ RecurCommon common_args(const prnn_handle* h, int T, int B, const float* h0, flo
   c.y = y;
   c.status = h->status;
   c.timeout_ns = h->timeout_us * 1000LL;
+  const int delay_ns = h->poll_delay_ns >= 0 ? h->poll_delay_ns
+                                            : (h->sparse ? kSparseDelayNs : kDenseDelayNs);
+  c.poll_delay = (int)((long long)delay_ns * h->clock_khz / 1000000LL);
   c.sync_mode = h->sync_mode;
   c.bar = h->bar;
   c.drop_cta = h->drop_cta;
@@ -421,6 +425,8 @@ prnn_status_t prnn_create(prnn_t* out, int hidden, int input, int max_batch,
   h->device = dev;
   h->sm_count = prop.multiProcessorCount;
   h->smem_optin = prop.sharedMemPerBlockOptin;
+  if (cudaDeviceGetAttribute(&h->clock_khz, cudaDevAttrClockRate, dev) != cudaSuccess)
+    h->clock_khz = 2000000;
   h->Kp = round_up(input, 64);
   prnn_status_t st = PRNN_OK;
   if (cudaMalloc((void**)&h->status, 4 * sizeof(int)) != cudaSuccess ||
@@ -757,6 +763,10 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
     case PRNN_OPT_BANK_AWARE:
       if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
       h->bank_aware = (int)value;
+      return PRNN_OK;
+    case PRNN_OPT_POLL_DELAY_NS:
+      if (value < 0 || value > 10000) return PRNN_ERR_INVALID_ARG;
+      h->poll_delay_ns = (int)value;
       return PRNN_OK;
   }
   return PRNN_ERR_INVALID_ARG;

@@ -66,6 +66,18 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 __device__ __forceinline__ float relu(float s) { return s > 0.f ? s : 0.f; }
 
+// Busy-wait n SM cycles without touching memory.  The persistent kernels
+// wait this long after publishing a step before their first poll of the
+// next one: a first poll that reaches the L2 before the producers' stores
+// have landed turns into re-poll rounds that contend with those stores, and
+// on some GB300 machines the exchange then settles into a state 3x slower.
+__device__ __forceinline__ void spin_cycles(int n) {
+  if (n <= 0) return;
+  const long long t0 = clock64();
+  while (clock64() - t0 < (long long)n) {
+  }
+}
+
 // Record the first failure; later ones keep the first record.
 __device__ __forceinline__ void report_timeout(int* status, int step, int cta) {
   if (atomicCAS(status, 0, kStatusTimeout) == 0) {

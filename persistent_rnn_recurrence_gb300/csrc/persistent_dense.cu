@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
       }
       // issue every load of h_{t-1} this thread needs (batch columns past nb
       // reuse column b0), then wait on them
+      if (t > 0 && b0 == pl.b_lo) spin_cycles(c.poll_delay);
       float4 hv[CPT][BW];
 #pragma unroll
       for (int j = 0; j < CPT; ++j) {

@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
           owns = true;
         }
       }
+      if (t > 0 && bs == pl.b_lo) spin_cycles(c.poll_delay);
       const bool ok = a.narrow
                           ? stage_rows_narrow<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w)
                           : stage_rows<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w);
@@ -186,6 +187,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sync_probe_kernel(const Rec
     for (int bs = pl.b_lo; bs < pl.b_hi; bs += BG) {
       const int nbg = min(BG, pl.b_hi - bs);
       bool ok = true;
+      if (t > 0 && bs == pl.b_lo) spin_cycles(c.poll_delay);
       if (t > 0) ok = stage_rows<8>(hprev, true, H, bs, nbg, hs, w);
       if (!ok) {
         report_timeout(c.status, t, cta);

@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
       }
       // issue every load; polled ones: the layer input when it is produced in
       // this launch, and h_{t-1} for t > 0
+      if ((t > 0 || L.poll_in) && b0 == pl.b_lo) spin_cycles(c.poll_delay);
       float4 hv[CPT][BW];
       unsigned pollmask = 0;
 #pragma unroll

@@ -38,6 +38,14 @@ bool projection_tc_supported();
 cudaError_t launch_projection_tc(const ProjTcArgs& a, int* status, cudaStream_t s);
 
 // ---- persistent recurrent kernels --------------------------------------
+// Default pause (ns) before the first poll of a step's input (see
+// spin_cycles), per kernel family, from sweeps on GB300: the dense kernels
+// (every thread polls its own chunks straight into registers) gain from
+// 50-100 ns and need it on boxes where the exchange otherwise settles into
+// its slow state; the sparse kernels (h staged through shared memory) are
+// fastest without it.
+constexpr int kDenseDelayNs = 100;
+constexpr int kSparseDelayNs = 0;
 struct RecurCommon {
   int T, B, H;
   int n_cta, R;          // CTAs (G * cpg) and rows per CTA (last CTA of a group may own fewer)
@@ -49,6 +57,7 @@ struct RecurCommon {
   float* y;              // [T][B][H], pre-filled with the sentinel
   int* status;           // int[4]
   long long timeout_ns;
+  int poll_delay;        // SM cycles between publishing a step and the first poll of the next
   int sync_mode;         // 0 flags in data, 1 grid barrier
   unsigned* bar;         // grid barrier counter (sync_mode 1)
   int drop_cta, drop_step;  // fault hook (-1 = off)

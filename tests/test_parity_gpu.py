@@ -392,3 +392,23 @@ def test_sync_floor_probe(env):
     t = torch.arange(1, 65, dtype=torch.float32, device="cuda").view(64, 1, 1)
     assert torch.equal(y, t.expand(64, 4, 1792))
     assert ms > 0
+
+
+@pytest.mark.parametrize("spec", [dict(H=1152, B=4, T=20, wdtype="f16"),
+                                  dict(H=1792, B=4, T=20, k=179)])
+def test_poll_delay_changes_timing_not_results(env, spec):
+    """The pause before each step's first poll only shifts when data is read:
+    results are bit-identical for 0, the default and a long pause."""
+    torch, prnn, o = env
+    p = synth.make_problem(seed=80, **spec)
+    ys = []
+    for d in (None, 0, 2000):
+        y, _ = run_gpu(env, p, options={} if d is None else {prnn.PRNN_OPT_POLL_DELAY_NS: d})
+        ys.append(y)
+    assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[0], ys[2])
+    check(ys[0], o.forward(p), p.wdtype, "poll delay")
+    lay = prnn.Layer.from_problem(p)
+    with pytest.raises(prnn.PrnnError) as e:
+        lay.set_option(prnn.PRNN_OPT_POLL_DELAY_NS, -1)
+    assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    lay.close()
