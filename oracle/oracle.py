@@ -11,8 +11,10 @@ header of ``prnn_oracle.c``.
 
 Parity pins: every function here is pinned by the CPU tests in
 ``tests/test_oracle_pins.py`` (hand-computed steps, closed forms, exact
-rational brute force, the linear regime, homogeneity, chaining, sparse versus
-densified equality) -- none is "parity unpinned".
+rational brute force, the linear regime, homogeneity, chaining, sparse and
+compressed-row versus densified equality, stacking identities, and for the
+backward pass exact-rational central differences of the loss and the linear
+regime of the reverse recurrence) -- none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -77,6 +79,11 @@ class Oracle:
         L.oracle_rnn_forward_csr.restype = ctypes.c_int
         L.oracle_rnn_cell_csr.argtypes = [_l, _l, _l, _D, _D, _L, _D, _L, _D, _D]
         L.oracle_rnn_cell_csr.restype = ctypes.c_double
+        L.oracle_rnn_backward_dense.argtypes = [_l, _l, _l, _l, _D, _D, _D, _D, _D, _D, _D, _D,
+                                                _D, _D, _D, _D]
+        L.oracle_rnn_backward_dense.restype = ctypes.c_int
+        L.oracle_rnn_delta_cell_dense.argtypes = [_l, _l, _D, _D, _D, _D]
+        L.oracle_rnn_delta_cell_dense.restype = ctypes.c_double
 
     # -- whole sequences -------------------------------------------------
     def forward_dense(self, x, Wx, Wh, b, h0=None) -> np.ndarray:
@@ -154,6 +161,63 @@ class Oracle:
         if p.sparse:
             return self.forward_sparse(x, p.Wx, p.vals, p.cols, p.b, p.h0)
         return self.forward_dense(x, p.Wx, p.Wh, p.b, p.h0)
+
+    # -- backward (BPTT) ---------------------------------------------------
+    def backward_dense(self, x, Wx, Wh, b, h0, dy) -> dict:
+        """Gradients of L = sum(dy * y) for dense Wh: keys delta [T,B,H],
+        dx [T,B,I], dh0 [B,H], dWx [H,I], dWh [H,H], db [H] (the C function
+        runs its own forward for y)."""
+        x, Wx, Wh, b, dy = _f64(x), _f64(Wx), _f64(Wh), _f64(b), _f64(dy)
+        T, B, I = x.shape
+        H = Wh.shape[0]
+        assert dy.shape == (T, B, H) and Wx.shape == (H, I) and Wh.shape == (H, H)
+        h0 = None if h0 is None else _f64(h0)
+        out = {"delta": np.zeros((T, B, H)), "dx": np.zeros((T, B, I)),
+               "dh0": np.zeros((B, H)), "dWx": np.zeros((H, I)), "dWh": np.zeros((H, H)),
+               "db": np.zeros(H)}
+        rc = self.lib.oracle_rnn_backward_dense(
+            T, B, H, I, _ptr(x), _ptr(Wx), _ptr(Wh), _ptr(b), _ptr(h0), _ptr(dy),
+            _ptr(out["delta"]), _ptr(out["dx"]), _ptr(out["dh0"]), _ptr(out["dWx"]),
+            _ptr(out["dWh"]), _ptr(out["db"]))
+        if rc != 0:
+            raise ValueError("oracle_rnn_backward_dense rejected its arguments")
+        return out
+
+    def backward(self, p, dy) -> dict:
+        """Gradients for a ``synth.Problem``.  Sparse weights: the loss depends on
+        a stored entry (r, cols[r][j]) only through that position of the
+        matrix, so its gradient is dWh[r, cols[r][j]] of the same matrix held
+        densely; returned as dvals in the storage order ([H,k], or [nnz] for
+        compressed rows) next to the dense dWh."""
+        if p.sparse:
+            Wh = np.zeros((p.H, p.H))
+            if getattr(p, "row_ptr", None) is not None:
+                rows = np.repeat(np.arange(p.H), np.diff(p.row_ptr))
+                cols = p.cols.astype(np.int64)
+                Wh[rows, cols] = p.vals.astype(np.float64)
+            else:
+                rows = np.repeat(np.arange(p.H), p.k)
+                cols = p.cols.astype(np.int64).ravel()
+                Wh[rows, cols] = p.vals.astype(np.float64).ravel()
+            g = self.backward_dense(p.x, p.Wx, Wh, p.b, p.h0, dy)
+            dv = g["dWh"][rows, cols]
+            g["dvals"] = dv if getattr(p, "row_ptr", None) is not None else dv.reshape(p.H, p.k)
+            return g
+        return self.backward_dense(p.x, p.Wx, p.Wh, p.b, p.h0, dy)
+
+    def delta_cells(self, Wh, samples, dy_of, y_of, delta_next_of) -> np.ndarray:
+        """Single elements of the reverse recurrence: for each (t, b, r),
+        [y_t > 0] * (dy_t[r] + sum_c Wh[c, r] delta_{t+1}[c]) with the three
+        vectors supplied by the callbacks (delta_next_of may return None)."""
+        Wh = _f64(Wh)
+        H = Wh.shape[0]
+        out = np.zeros(len(samples))
+        for i, (t, bb, r) in enumerate(samples):
+            nx = delta_next_of(t, bb)
+            out[i] = self.lib.oracle_rnn_delta_cell_dense(
+                H, r, _ptr(Wh), _ptr(_f64(dy_of(t, bb))), _ptr(_f64(y_of(t, bb))),
+                None if nx is None else _ptr(_f64(nx)))
+        return out
 
     # -- pieces ----------------------------------------------------------
     def input_projection(self, x, Wx, b) -> np.ndarray:

@@ -171,3 +171,100 @@ int oracle_rnn_input_projection(long T, long B, long H, long I, const double* x,
         }
     return 0;
 }
+
+/*
+ * Backward pass (backpropagation through time) of the same layer, for the
+ * scalar objective L = sum_{t,b,r} dy[t,b,r] * y[t,b,r] -- dy is the gradient
+ * of the training loss with respect to every output.  Training is what the
+ * persistent kernels are built for ("Optimizing Performance of Recurrent
+ * Neural Networks on GPUs", Abstract: training recurrent networks); the
+ * steps are those of the chain rule applied to the forward definition above:
+ *
+ *   delta_T = 0
+ *   for t = T-1 .. 0:   g = dy_t + Wh^T delta_{t+1}
+ *                       delta_t[r] = y_t[r] > 0 ? g[r] : 0      (ReLU'(a) = [a > 0])
+ *   db[r]     = sum_{t,b} delta_t[b,r]
+ *   dWh[r,c]  = sum_{t,b} delta_t[b,r] * h_{t-1}[b,c]          (h_{-1} = h0)
+ *   dWx[r,c]  = sum_{t,b} delta_t[b,r] * x_t[b,c]
+ *   dx_t[b,c] = sum_r Wx[r,c] * delta_t[b,r]
+ *   dh0[b,c]  = sum_r Wh[r,c] * delta_0[b,r]
+ *
+ * y is the oracle's own forward output (this function runs the forward
+ * first).  delta [T][B][H] is returned too.  Any output pointer may be NULL.
+ * Returns 0, or -1 on bad arguments.
+ */
+/* One element of the reverse recurrence, given delta_{t+1} ([H], NULL = 0). */
+double oracle_rnn_delta_cell_dense(long H, long r, const double* Wh, const double* dy_t,
+                                   const double* y_t, const double* delta_next) {
+    double g = dy_t[r];
+    if (delta_next)
+        for (long c = 0; c < H; ++c) g += Wh[c * H + r] * delta_next[c];
+    return y_t[r] > 0.0 ? g : 0.0;
+}
+
+int oracle_rnn_backward_dense(long T, long B, long H, long I, const double* x, const double* Wx,
+                              const double* Wh, const double* bias, const double* h0,
+                              const double* dy, double* delta, double* dx, double* dh0,
+                              double* dWx, double* dWh, double* db) {
+    if (T < 0 || B < 0 || H <= 0 || I <= 0 || !x || !Wx || !Wh || !bias || !dy) return -1;
+    double* y = (double*)calloc((size_t)(T * B * H) + 1, sizeof(double));
+    double* d = delta ? delta : (double*)calloc((size_t)(T * B * H) + 1, sizeof(double));
+    if (!y || !d) { free(y); if (!delta) free(d); return -1; }
+    if (oracle_rnn_forward_dense(T, B, H, I, x, Wx, Wh, bias, h0, y) != 0) {
+        free(y); if (!delta) free(d); return -1;
+    }
+    for (long t = T - 1; t >= 0; --t)
+        for (long b = 0; b < B; ++b) {
+            const double* next = (t == T - 1) ? NULL : d + ((t + 1) * B + b) * H;
+            for (long r = 0; r < H; ++r)
+                d[(t * B + b) * H + r] = oracle_rnn_delta_cell_dense(
+                    H, r, Wh, dy + (t * B + b) * H, y + (t * B + b) * H, next);
+        }
+    if (db)
+        for (long r = 0; r < H; ++r) {
+            double s = 0.0;
+            for (long t = 0; t < T; ++t)
+                for (long b = 0; b < B; ++b) s += d[(t * B + b) * H + r];
+            db[r] = s;
+        }
+    if (dWh)
+        for (long r = 0; r < H; ++r)
+            for (long c = 0; c < H; ++c) {
+                double s = 0.0;
+                for (long t = 0; t < T; ++t)
+                    for (long b = 0; b < B; ++b) {
+                        const double hp = (t == 0) ? (h0 ? h0[b * H + c] : 0.0)
+                                                   : y[((t - 1) * B + b) * H + c];
+                        s += d[(t * B + b) * H + r] * hp;
+                    }
+                dWh[r * H + c] = s;
+            }
+    if (dWx)
+        for (long r = 0; r < H; ++r)
+            for (long c = 0; c < I; ++c) {
+                double s = 0.0;
+                for (long t = 0; t < T; ++t)
+                    for (long b = 0; b < B; ++b)
+                        s += d[(t * B + b) * H + r] * x[(t * B + b) * I + c];
+                dWx[r * I + c] = s;
+            }
+    if (dx)
+        for (long t = 0; t < T; ++t)
+            for (long b = 0; b < B; ++b)
+                for (long c = 0; c < I; ++c) {
+                    double s = 0.0;
+                    for (long r = 0; r < H; ++r) s += Wx[r * I + c] * d[(t * B + b) * H + r];
+                    dx[(t * B + b) * I + c] = s;
+                }
+    if (dh0)
+        for (long b = 0; b < B; ++b)
+            for (long c = 0; c < H; ++c) {
+                double s = 0.0;
+                if (T > 0)
+                    for (long r = 0; r < H; ++r) s += Wh[r * H + c] * d[b * H + r];
+                dh0[b * H + c] = s;
+            }
+    free(y);
+    if (!delta) free(d);
+    return 0;
+}

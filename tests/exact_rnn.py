@@ -8,7 +8,7 @@ from fractions import Fraction
 
 
 def _q(v) -> Fraction:
-    return Fraction(float(v))
+    return v if isinstance(v, Fraction) else Fraction(float(v))
 
 
 def forward_exact(x, Wx, Wh, b, h0=None):

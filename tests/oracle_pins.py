@@ -225,6 +225,124 @@ def pin_stack_definition(o):
     assert (y[1] > 0).any() and (y[1] == 0).any()
 
 
+def _exact_loss(x, Wx, Wh, b, h0, dy):
+    """L = sum(dy * y) in exact rationals (tests/exact_rnn.py)."""
+    from fractions import Fraction
+    y = forward_exact(x, Wx, Wh, b, h0)
+    return sum((Fraction(float(dy[t][bb][r])) * y[t][bb][r]
+                for t in range(len(y)) for bb in range(len(y[0])) for r in range(len(y[0][0]))),
+               Fraction(0))
+
+
+def _preacts_nonzero(x, Wx, Wh, b, h0):
+    """True when no pre-activation of the exact forward is exactly 0 (the
+    loss is then differentiable at this point)."""
+    from fractions import Fraction
+    T, B, H, I = len(x), len(x[0]), len(Wx), len(Wx[0])
+    q = lambda v: Fraction(float(v))
+    h = [[Fraction(0)] * H for _ in range(B)] if h0 is None else [[q(v) for v in row] for row in h0]
+    for t in range(T):
+        nh = []
+        for bb in range(B):
+            row = []
+            for r in range(H):
+                a = q(b[r]) + sum(q(Wx[r][i]) * q(x[t][bb][i]) for i in range(I)) + \
+                    sum(q(Wh[r][c]) * h[bb][c] for c in range(H))
+                if a == 0:
+                    return False
+                row.append(a if a > 0 else Fraction(0))
+            nh.append(row)
+        h = nh
+    return True
+
+
+def pin_backward_finite_differences(o):
+    """Every gradient of L = sum(dy * y) against exact central differences:
+    the loss is evaluated in exact rationals at theta +- eps with
+    eps = 1e-30 (the loss is piecewise polynomial in each parameter, so the
+    difference quotient is exact up to O(eps^2)), at points with no zero
+    pre-activation.  Covers dWh, dWx, db, dh0 and dx, both ReLU branches."""
+    from fractions import Fraction
+    rng = np.random.default_rng(21)
+    eps = Fraction(1, 10 ** 30)
+    for (T, B, H, I) in [(3, 2, 3, 2), (2, 1, 4, 3)]:
+        while True:
+            x, Wx, Wh = _dyadic(rng, T, B, I), _dyadic(rng, H, I), _dyadic(rng, H, H, lo=-6, hi=6)
+            b, h0, dy = _dyadic(rng, H), _dyadic(rng, B, H), _dyadic(rng, T, B, H)
+            if _preacts_nonzero(x.tolist(), Wx.tolist(), Wh.tolist(), b.tolist(), h0.tolist()):
+                break
+        g = o.backward_dense(x, Wx, Wh, b, h0, dy)
+        y = o.forward_dense(x, Wx, Wh, b, h0)
+        assert (y > 0).any() and (y == 0).any()
+        params = {"Wx": (Wx, "dWx"), "Wh": (Wh, "dWh"), "b": (b, "db"), "h0": (h0, "dh0"),
+                  "x": (x, "dx")}
+        for name, (arr, gname) in params.items():
+            for idx in np.ndindex(arr.shape):
+                vals = {}
+                for sgn in (1, -1):
+                    args = {"x": x.tolist(), "Wx": Wx.tolist(), "Wh": Wh.tolist(),
+                            "b": b.tolist(), "h0": h0.tolist()}
+                    a = args[name]
+                    ref = a
+                    for k in idx[:-1]:
+                        ref = ref[k]
+                    ref[idx[-1]] = Fraction(float(ref[idx[-1]])) + sgn * eps
+                    vals[sgn] = _exact_loss(args["x"], args["Wx"], args["Wh"], args["b"],
+                                            args["h0"], dy.tolist())
+                fd = float((vals[1] - vals[-1]) / (2 * eps))
+                got = g[gname][idx]
+                assert abs(got - fd) <= 1e-12 * max(1.0, abs(fd)), (name, idx, got, fd)
+
+
+def pin_backward_linear_regime(o):
+    """Non-negative integers keep every unit active, so the reverse
+    recurrence is linear: delta_t = sum_{s>=t} (Wh^T)^{s-t} dy_s exactly
+    (Python integers), and db = sum over t, b of delta_t."""
+    rng = np.random.default_rng(22)
+    T, B, H, I = 4, 2, 3, 2
+    x = rng.integers(0, 3, size=(T, B, I))
+    Wx = rng.integers(1, 3, size=(H, I))
+    Wh = rng.integers(0, 2, size=(H, H))
+    Wh[0, 1], Wh[1, 0] = 1, 0
+    b = rng.integers(1, 3, size=H)
+    dy = rng.integers(-3, 4, size=(T, B, H))
+    g = o.backward_dense(x, Wx, Wh, b, None, dy)
+    WT = [[int(Wh[c][r]) for c in range(H)] for r in range(H)]
+    for bb in range(B):
+        for t in range(T):
+            acc = [0] * H
+            for s in range(t, T):
+                v = [int(u) for u in dy[s][bb]]
+                for _ in range(s - t):
+                    v = [sum(WT[r][c] * v[c] for c in range(H)) for r in range(H)]
+                acc = [p + q for p, q in zip(acc, v)]
+            assert [float(v) for v in acc] == list(g["delta"][t, bb]), (t, bb)
+    assert np.array_equal(g["db"], g["delta"].sum(axis=(0, 1)))
+
+
+def pin_backward_sparse_is_dense_gather(o):
+    """Sparse gradients: dvals[r][j] equals the dense gradient at
+    (r, cols[r][j]), and perturbing one stored value changes the loss at
+    that rate (fp64 central difference, eps = 1e-6, well inside every
+    ReLU branch for this draw)."""
+    from persistent_rnn_recurrence_gb300 import synth
+    p = synth.make_problem(H=12, B=2, T=4, k=3, seed=23, h0_std=0.5)
+    rng = np.random.default_rng(24)
+    dy = rng.normal(size=(p.T, p.B, p.H))
+    g = o.backward(p, dy)
+    for r in (0, 5, 11):
+        for j in range(p.k):
+            c = int(p.cols[r, j])
+            assert g["dvals"][r, j] == g["dWh"][r, c]
+            base = p.vals.astype(np.float64)
+            lo, hi = base.copy(), base.copy()
+            lo[r, j] -= 1e-6
+            hi[r, j] += 1e-6
+            f = lambda v: float((o.forward_sparse(p.x, p.Wx, v, p.cols, p.b, p.h0) * dy).sum())
+            fd = (f(hi) - f(lo)) / 2e-6
+            assert abs(fd - g["dvals"][r, j]) <= 1e-6 * max(1.0, abs(fd)), (r, j, fd)
+
+
 def pin_chaining(o):
     rng = np.random.default_rng(17)
     T1, T2, B, H, I = 3, 4, 2, 9, 9

@@ -62,6 +62,15 @@ MUTANTS = {
     "x_time_shift": ("x + (t * B + b) * I", "x + (((t + 1) % T) * B + b) * I"),
     "dropped_recurrent_term": ("s += Wh[r * H + c] * h_prev[c];", "(void)h_prev;"),
     "csr_row_end_off_by_one": ("j < row_ptr[r + 1]; ++j", "j < row_ptr[r + 1] - 1; ++j"),
+    "bwd_untransposed_wh": ("g += Wh[c * H + r] * delta_next[c];",
+                            "g += Wh[r * H + c] * delta_next[c];"),
+    "bwd_no_relu_mask": ("return y_t[r] > 0.0 ? g : 0.0;", "return g;"),
+    "bwd_dwh_same_step_h": ("y[((t - 1) * B + b) * H + c];", "y[(t * B + b) * H + c];"),
+    "bwd_dx_uses_wh": ("s += Wx[r * I + c] * d[(t * B + b) * H + r];",
+                       "s += Wx[(r * I + c) % (H * I)] * d[(t * B + b) * H + (r + 1) % H];"),
+    "bwd_dh0_last_delta": ("s += Wh[r * H + c] * d[b * H + r];",
+                           "s += Wh[r * H + c] * d[((T - 1) * B + b) * H + r];"),
+    "bwd_dwx_time_shift": ("* x[(t * B + b) * I + c];", "* x[(((t + 1) % T) * B + b) * I + c];"),
 }
 
 
