@@ -155,6 +155,35 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
 /* Release everything the handle owns.  NULL is accepted. */
 prnn_status_t prnn_destroy(prnn_t h);
 
+/*
+ * Backward pass (backpropagation through time) of the layer for the loss L
+ * whose gradient with respect to the outputs is dy = dL/dy:
+ *
+ *   delta_T = 0;  for t = T-1 .. 0:  delta_t = [y_t > 0] (dy_t + Wh^T delta_{t+1})
+ *   db = sum_{t,b} delta_t,  dWh = sum_{t,b} delta_t h_{t-1}^T (h_{-1} = h0),
+ *   dWx = sum_{t,b} delta_t x_t^T,  dx_t = Wx^T delta_t,  dh0 = Wh^T delta_0
+ *
+ * -- training is what the persistent kernels are for ("Optimizing
+ * Performance of Recurrent Neural Networks on GPUs", Abstract).  The serial
+ * reverse recurrence runs in the same persistent kernel as the forward with
+ * Wh^T held on chip (a transposed copy packed at set_weights time); the five
+ * gradients are batched products over all T*B rows.  The derivative of ReLU
+ * at 0 is taken as 0 (y_t = 0 gives delta_t = 0).
+ *
+ * Inputs (device, fp32, 16-byte aligned): x [T][B][I] and h0 [B][H] (NULL =
+ * zeros) as given to prnn_forward, y [T][B][H] the output prnn_forward
+ * produced for them with these weights, dy [T][B][H].  Outputs (device, fp32,
+ * overwritten; NULL skips that gradient): delta [T][B][H] (dL/da_t, the
+ * gradient at the pre-activations; the library's workspace is used when
+ * NULL), dx [T][B][I], dh0 [B][H], dWx [H][I], dWh [H][H], db [H].  Outputs must not overlap the inputs or each
+ * other.  Asynchronous on `stream`; T == 0 or B == 0 writes zero gradients.
+ * Dense persistent handles (PRNN_ERR_UNSUPPORTED otherwise).  After a timed
+ * backward, prnn_get_timing reports (gradient products, reverse recurrence).
+ */
+prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float* h0,
+                            const float* y, const float* dy, float* delta, float* dx, float* dh0,
+                            float* dWx, float* dWh, float* db, void* stream);
+
 /* Synchronize `stream` and report the device-side status of past forwards
  * (PRNN_ERR_TIMEOUT once a step wait has run out; sticky). */
 prnn_status_t prnn_get_status(prnn_t h, void* stream);

@@ -41,6 +41,8 @@ struct prnn_handle {
   __half_raw* Wx16 = nullptr;  // [H][Kp] fp16, zero padded (tcgen05 projection)
   float* bias = nullptr;
   void* Wpk = nullptr;       // persistent packed recurrent weights
+  void* Wpk_T = nullptr;     // the same packing of Wh^T (backward pass, dense)
+  void* Wh_nat = nullptr;    // Wh row-major [H][H] in wdtype (backward pass, dense)
   void* Wstep = nullptr;     // per-step layout of the recurrent weights
   float* P = nullptr;
   size_t P_cap = 0;
@@ -54,6 +56,7 @@ struct prnn_handle {
   int sync_mode = 0, drop_cta = -1, drop_step = -1, timing = 0, proj_mode = 0;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   bool ev_valid = false;
+  bool last_backward = false;  // which call the timing events belong to
   bool sticky_timeout = false;
   // per-step graph cache
   cudaStream_t cap_stream = nullptr;
@@ -289,6 +292,8 @@ void free_weights(prnn_handle* h) {
   free_dev(h->Wx16);
   free_dev(h->bias);
   free_dev(h->Wpk);
+  free_dev(h->Wpk_T);
+  free_dev(h->Wh_nat);
   free_dev(h->Wstep);
   h->weights_set = false;
 }
@@ -488,6 +493,7 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
     const size_t vec = 4 * esz;
     // one block per CTA of a group; every group reads the same blocks
     std::vector<unsigned char> pk((size_t)plan.cpg * plan.cpt * plan.R * NT * vec, 0);
+    std::vector<unsigned char> pt(pk.size(), 0);  // the same layout of Wh^T (backward)
     for (int cta = 0; cta < plan.cpg; ++cta)
       for (int j = 0; j < plan.cpt; ++j)
         for (int r = 0; r < plan.R; ++r)
@@ -496,8 +502,12 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
             if (row >= H || ch >= nchunks) continue;
             const size_t dst = ((((size_t)cta * plan.cpt + j) * plan.R + r) * NT + i) * vec;
             std::memcpy(&pk[dst], &wh[((size_t)row * H + (size_t)ch * 4) * esz], vec);
+            for (int q = 0; q < 4; ++q)  // Wh^T[row][4ch + q] = Wh[4ch + q][row]
+              std::memcpy(&pt[dst + q * esz], &wh[((size_t)(ch * 4 + q) * H + row) * esz], esz);
           }
     PRNN_TRY(upload(&h->Wpk, pk.data(), pk.size()));
+    PRNN_TRY(upload(&h->Wpk_T, pt.data(), pt.size()));
+    PRNN_TRY(upload(&h->Wh_nat, wh.data(), wh.size()));
     h->n_cta = plan.n_cta;
     h->R = plan.R;
     h->G = plan.G;
@@ -627,6 +637,7 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
   PRNN_TRY(ensure_P(h, ny));
   const bool persistent = h->algo == PRNN_ALGO_PERSISTENT;
   if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[0], s));
+  h->last_backward = false;
 
   // 1. projection for all steps (+ sentinel fill of y on the persistent path)
   if (h->tc_proj && h->proj_mode == 0) {
@@ -711,6 +722,94 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
   if (h->timing) {
     PRNN_TRY(cudaEventRecord(h->ev[2], s));
     h->ev_valid = true;
+  }
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float* h0,
+                            const float* y, const float* dy, float* delta_out, float* dx,
+                            float* dh0, float* dWx, float* dWh, float* db, void* stream) {
+  if (!h) return PRNN_ERR_INVALID_ARG;
+  if (h->sticky_timeout) return PRNN_ERR_TIMEOUT;
+  if (!h->weights_set) return PRNN_ERR_NOT_READY;
+  if (h->algo != PRNN_ALGO_PERSISTENT || h->sparse) return PRNN_ERR_UNSUPPORTED;
+  if (T < 0 || B < 0 || B > h->maxB) return PRNN_ERR_INVALID_ARG;
+  const int H = h->H, I = h->I;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0 || B == 0) {  // no steps: every gradient is zero
+    if (dWx) PRNN_TRY(cudaMemsetAsync(dWx, 0, (size_t)H * I * 4, s));
+    if (dWh) PRNN_TRY(cudaMemsetAsync(dWh, 0, (size_t)H * H * 4, s));
+    if (db) PRNN_TRY(cudaMemsetAsync(db, 0, (size_t)H * 4, s));
+    if (dh0 && B > 0) PRNN_TRY(cudaMemsetAsync(dh0, 0, (size_t)B * H * 4, s));
+    return PRNN_OK;
+  }
+  if (!x || !y || !dy) return PRNN_ERR_INVALID_ARG;
+  const void* ins[] = {x, h0, y, dy};
+  const void* outs[] = {dx, dh0, dWx, dWh, db, delta_out};
+  for (const void* p : ins)
+    if (p && !aligned16(p)) return PRNN_ERR_INVALID_ARG;
+  for (const void* p : outs)
+    if (p && !aligned16(p)) return PRNN_ERR_INVALID_ARG;
+  const size_t ny = (size_t)T * B * H;
+  const size_t out_bytes[] = {(size_t)T * B * I * 4, (size_t)B * H * 4, (size_t)H * I * 4,
+                              (size_t)H * H * 4, (size_t)H * 4, ny * 4};
+  const size_t in_bytes[] = {(size_t)T * B * I * 4, (size_t)B * H * 4, ny * 4, ny * 4};
+  for (int o = 0; o < 6; ++o) {
+    if (!outs[o]) continue;
+    for (int i = 0; i < 4; ++i)
+      if (ins[i] && overlaps(outs[o], out_bytes[o], ins[i], in_bytes[i])) return PRNN_ERR_INVALID_ARG;
+    for (int o2 = 0; o2 < o; ++o2)
+      if (outs[o2] && overlaps(outs[o], out_bytes[o], outs[o2], out_bytes[o2]))
+        return PRNN_ERR_INVALID_ARG;
+  }
+  float* delta = delta_out;
+  if (!delta) {
+    PRNN_TRY(ensure_P(h, ny));  // the projection workspace holds the deltas
+    delta = h->P;
+  }
+  if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[0], s));
+
+  // 1. reverse recurrence: delta_t = [y_t > 0] (dy_t + Wh^T delta_{t+1})
+  PRNN_TRY(launch_fill_sentinel(delta, ny, s));
+  RecurCommon c = common_args(h, T, B, nullptr, delta);
+  c.P = dy;
+  c.reverse = 1;
+  c.mask = y;
+  c.sync_mode = 0;
+  DenseRecurArgs a{};
+  const int bw = std::min(recur_dense_bw((B + h->G - 1) / h->G), h->dense_bw);
+  c.smem = recur_dense_smem(h->R, h->cpt, h->nthreads, h->wdtype == PRNN_F16, bw);
+  a.c = c;
+  a.Wpk = h->Wpk_T;
+  a.cpt = h->cpt;
+  a.wfp16 = h->wdtype == PRNN_F16;
+  PRNN_TRY(launch_recur_dense(a, bw, s));
+  if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[1], s));
+
+  // 2. batched gradients over all T*B rows of delta
+  const int K = T * B;
+  const bool f16 = h->wdtype == PRNN_F16;
+  if (db) PRNN_TRY(launch_colsum(delta, K, H, db, s));
+  if (dWh) {
+    GemmTnArgs g{H, H, K, B, delta, H, h0, y, H, dWh};
+    PRNN_TRY(launch_gemm_tn(g, s));
+  }
+  if (dWx) {
+    GemmTnArgs g{H, I, K, 0, delta, H, nullptr, x, I, dWx};
+    PRNN_TRY(launch_gemm_tn(g, s));
+  }
+  if (dx) {
+    GemmNnArgs g{K, I, H, delta, H, h->Wx, I, f16 ? 1 : 0, dx};
+    PRNN_TRY(launch_gemm_nn(g, s));
+  }
+  if (dh0) {
+    GemmNnArgs g{B, H, H, delta, H, h->Wh_nat, H, f16 ? 1 : 0, dh0};
+    PRNN_TRY(launch_gemm_nn(g, s));
+  }
+  if (h->timing) {
+    PRNN_TRY(cudaEventRecord(h->ev[2], s));
+    h->ev_valid = true;
+    h->last_backward = true;
   }
   return PRNN_OK;
 }
@@ -805,8 +904,9 @@ prnn_status_t prnn_get_timing(prnn_t h, float* ms_projection, float* ms_recurren
   float a = 0.f, b = 0.f;
   PRNN_TRY(cudaEventElapsedTime(&a, h->ev[0], h->ev[1]));
   PRNN_TRY(cudaEventElapsedTime(&b, h->ev[1], h->ev[2]));
-  if (ms_projection) *ms_projection = a;
-  if (ms_recurrence) *ms_recurrence = b;
+  // forward: (projection, recurrence); backward: (gradient products, reverse recurrence)
+  if (ms_projection) *ms_projection = h->last_backward ? b : a;
+  if (ms_recurrence) *ms_recurrence = h->last_backward ? a : b;
   return PRNN_OK;
 }
 
@@ -824,6 +924,7 @@ prnn_status_t prnn_probe_sync_floor(prnn_t h, int T, int B, float* y, void* stre
   c.smem = sync_probe_smem(h->H, bg);
   if (c.smem > h->smem_optin) return PRNN_ERR_UNSUPPORTED;
   if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[0], s));
+  h->last_backward = false;
   PRNN_TRY(launch_fill_sentinel(y, (size_t)T * B * h->H, s));
   if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[1], s));
   PRNN_TRY(launch_sync_probe(c, bg, s));

@@ -86,23 +86,26 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
   w.timeout_ns = c.timeout_ns;
   int seq = 0;
   for (int t = 0; t < c.T; ++t) {
-    const float* hprev = (t == 0) ? c.h0 : c.y + (size_t)(t - 1) * B * H;
-    const float* Pt = c.P + (size_t)t * B * H;
-    float* yt = c.y + (size_t)t * B * H;
+    const int tt = c.reverse ? c.T - 1 - t : t;  // time index of this step
+    const float* hprev = (t == 0) ? c.h0 : c.y + (size_t)(c.reverse ? tt + 1 : tt - 1) * B * H;
+    const float* Pt = c.P + (size_t)tt * B * H;
+    float* yt = c.y + (size_t)tt * B * H;
     w.new_step();
     for (int bs = pl.b_lo; bs < pl.b_hi; bs += BG, ++seq) {
       const int nbg = min(BG, pl.b_hi - bs);
       const int hs_off = hs_base + ((nbuf == 2) ? (seq & 1) : 0) * H * BG;
       // P for this lane's outputs, fetched before the wait
-      float pv[NOUT];
+      float pv[NOUT], mv[NOUT];
       bool owns = false;
 #pragma unroll
       for (int i = 0; i < NOUT; ++i) {
         pv[i] = 0.f;
+        mv[i] = 1.f;
         const int idx = (BG >= TPR) ? gl * NOUT + i : gl / REP;
         const bool mine = (gl % REP) == 0;
         if (has_row && mine && idx < nbg) {
           pv[i] = ld_nc_pinned(Pt + (size_t)(bs + idx) * H + row);
+          if (c.mask) mv[i] = ld_nc_pinned(c.mask + ((size_t)tt * B + bs + idx) * H + row);
           owns = true;
         }
       }
@@ -152,7 +155,11 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
 #pragma unroll
         for (int i = 0; i < NOUT; ++i) {
           const int idx = (BG >= TPR) ? gl * NOUT + i : gl / REP;
-          if (idx < nbg) st_relaxed_f(yt + (size_t)(bs + idx) * H + row, relu(acc[i] + pv[i]));
+          if (idx < nbg) {
+            const float s = acc[i] + pv[i];
+            st_relaxed_f(yt + (size_t)(bs + idx) * H + row,
+                         c.mask ? (mv[i] > 0.f ? s : 0.f) : relu(s));
+          }
         }
       }
       if (nbuf == 1) __syncthreads();  // hs is overwritten by the next staging

@@ -55,6 +55,11 @@ struct RecurCommon {
   const float* P;        // [T][B][H] projection (bias included)
   const float* h0;       // [B][H] or nullptr
   float* y;              // [T][B][H], pre-filled with the sentinel
+  // Reverse mode (the backward pass): steps run t = T-1 .. 0, h_prev is
+  // y[t+1], and the output is P + sum masked by mask[t] > 0 instead of ReLU
+  // (P = dy, W = Wh^T, y = delta, mask = the forward output).
+  int reverse;
+  const float* mask;     // [T][B][H] or nullptr
   int* status;           // int[4]
   long long timeout_ns;
   int poll_delay;        // SM cycles between publishing a step and the first poll of the next
@@ -164,5 +169,30 @@ struct StepArgs {
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 
 cudaError_t launch_fill_sentinel(float* y, size_t n, cudaStream_t s);
+
+// ---- backward: batched gradient products (grad.cu) ----------------------
+// C[M][N] = sum_k A[k][m] * Brow(k)[n]; Brow(k) = B0 + k*ldb for k < K0
+// (zeros if B0 is null), else B1 + (k-K0)*ldb.
+struct GemmTnArgs {
+  int M, N, K, K0;
+  const float* A;
+  int lda;
+  const float* B0;
+  const float* B1;
+  int ldb;
+  float* C;              // [M][N]
+};
+// C[M][N] = sum_k A[m][k] * W[k][n]; W fp32 or fp16.
+struct GemmNnArgs {
+  int M, N, K;
+  const float* A;
+  int lda;
+  const void* W;
+  int ldw, wf16;
+  float* C;              // [M][N]
+};
+cudaError_t launch_gemm_tn(const GemmTnArgs& g, cudaStream_t s);
+cudaError_t launch_gemm_nn(const GemmNnArgs& g, cudaStream_t s);
+cudaError_t launch_colsum(const float* A, int K, int N, float* out, cudaStream_t s);
 
 }  // namespace prnn

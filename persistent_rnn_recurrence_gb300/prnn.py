@@ -37,7 +37,7 @@ EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
            "prnn_pack_sparse_host", "prnn_forward_dense_noalloc", "prnn_set_weights_csr",
            "prnn_stack_create", "prnn_stack_set_layer", "prnn_stack_forward",
            "prnn_stack_get_status", "prnn_stack_set_option", "prnn_stack_get_timing",
-           "prnn_stack_get_info", "prnn_stack_destroy"]
+           "prnn_stack_get_info", "prnn_stack_destroy", "prnn_backward"]
 
 
 class prnn_info_t(ctypes.Structure):
@@ -89,6 +89,7 @@ _sig = {
     "prnn_stack_get_timing": ([_P, ctypes.POINTER(ctypes.c_float)], _I),
     "prnn_stack_get_info": ([_P, ctypes.POINTER(prnn_stack_info_t)], _I),
     "prnn_stack_destroy": ([_P], _I),
+    "prnn_backward": ([_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
 }
 for _name, (_args, _res) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -219,6 +220,13 @@ def prnn_forward_dense_noalloc(T, B, H, I, wdtype, x, Wx, Wh, bias, h0, y, strea
            "prnn_forward_dense_noalloc")
 
 
+def prnn_backward(h: int, T: int, B: int, x, h0, y, dy, delta=None, dx=None, dh0=None, dWx=None,
+                  dWh=None, db=None, stream=None) -> None:
+    _check(_lib.prnn_backward(h, T, B, _ptr(x), _ptr(h0), _ptr(y), _ptr(dy), _ptr(delta), _ptr(dx),
+                              _ptr(dh0), _ptr(dWx), _ptr(dWh), _ptr(db), _stream(stream)),
+           "prnn_backward")
+
+
 def prnn_stack_create(layers: int, hidden: int, input: int, max_batch: int, wdtype: int,
                       algo: int) -> int:
     out = _P()
@@ -311,6 +319,21 @@ class Layer:
             y = torch.empty((T, B, self.hidden), dtype=torch.float32, device=x.device)
         prnn_forward(self.h, T, B, x, h0, y, stream)
         return y
+
+    def backward(self, x, y, dy, h0=None, stream=None) -> dict:
+        """Gradients of the loss with dL/dy = dy for the forward (x, h0) -> y:
+        dict of fp32 CUDA tensors delta, dx, dh0, dWx, dWh, db."""
+        import torch
+        T, B, _ = x.shape
+        dev = x.device
+        g = {"delta": torch.empty_like(y),
+             "dx": torch.empty_like(x), "dh0": torch.empty(B, self.hidden, device=dev),
+             "dWx": torch.empty(self.hidden, self.input, device=dev),
+             "dWh": torch.empty(self.hidden, self.hidden, device=dev),
+             "db": torch.empty(self.hidden, device=dev)}
+        prnn_backward(self.h, T, B, x, h0, y, dy, g["delta"], g["dx"], g["dh0"], g["dWx"], g["dWh"],
+                      g["db"], stream)
+        return g
 
     def status(self, stream=None) -> int:
         return prnn_get_status(self.h, stream)

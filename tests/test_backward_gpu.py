@@ -1,0 +1,201 @@
+"""GPU parity of the backward pass (prnn_backward) against the fp64 oracle.
+
+Three kinds of check:
+  * exact-arithmetic problems (dyadic values with few non-zeros per row of
+    Wh, so every fp32 sum on the GPU is exact): the GPU forward output equals
+    the oracle's bit for bit, so both sides take the same ReLU mask decisions,
+    and every gradient must match the oracle's within 1e-6 of its scale;
+  * random fp32-weight problems whose pre-activations all stay further from 0
+    than the fp32 rounding of the forward (checked on the oracle's side), so
+    the masks agree again: every gradient within 1e-4 of its scale;
+  * fp16-weight and full-size problems, where forward rounding can flip the
+    mask of pre-activations near 0: properties that hold at any size --
+    every sampled delta equals one oracle step of the reverse recurrence
+    applied to the GPU's own y and delta_{t+1} (teacher forcing), and every
+    gradient equals its batched product (fp64 numpy) of the GPU's deltas.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from persistent_rnn_recurrence_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from persistent_rnn_recurrence_gb300 import build
+    build.build()
+    from persistent_rnn_recurrence_gb300 import prnn
+    return torch, prnn, oracle.default()
+
+
+def run(env, p, dy):
+    torch, prnn, _ = env
+    lay = prnn.Layer.from_problem(p)
+    try:
+        x = torch.from_numpy(p.x).cuda()
+        h0 = None if p.h0 is None else torch.from_numpy(p.h0).cuda()
+        y = lay.forward(x, h0)
+        g = lay.backward(x, y, torch.from_numpy(dy).cuda(), h0)
+        assert lay.status() == prnn.PRNN_OK
+        return y.cpu().numpy().astype(np.float64), {k: v.cpu().numpy().astype(np.float64)
+                                                    for k, v in g.items()}
+    finally:
+        lay.close()
+
+
+def rel_err(a, b):
+    return float(np.abs(a - b).max()) / max(float(np.abs(b).max()), 1e-30)
+
+
+def dyadic_problem(seed, H, I, B, T, wdtype, nnz_row=3):
+    rng = np.random.default_rng(seed)
+    q = lambda *s, lo=-8, hi=8: rng.integers(lo, hi + 1, size=s).astype(np.float64) / 8
+    Wh = np.zeros((H, H))
+    for r in range(H):
+        Wh[r, rng.choice(H, nnz_row, replace=False)] = rng.choice([-0.5, 0.5], nnz_row)
+    wt = np.float16 if wdtype == "f16" else np.float32
+    p = synth.Problem(name="dyadic", T=T, B=B, H=H, I=I, wdtype=wdtype,
+                      x=q(T, B, I).astype(np.float32), Wx=(q(H, I) / 4).astype(wt),
+                      b=q(H).astype(np.float32), h0=q(B, H).astype(np.float32), Wh=Wh.astype(wt))
+    dy = q(T, B, H)
+    return p, dy
+
+
+@pytest.mark.parametrize("wdtype", ["f32", "f16"])
+@pytest.mark.parametrize("shape", [dict(H=64, I=32, B=3, T=6), dict(H=300, I=100, B=5, T=5),
+                                   dict(H=1152, I=1152, B=4, T=4)])
+def test_backward_exact_problems(env, wdtype, shape):
+    p, dy = dyadic_problem(500 + shape["H"], wdtype=wdtype, **shape)
+    o = env[2]
+    y, g = run(env, p, dy.astype(np.float32))
+    assert np.array_equal(y, o.forward(p)), "forward not exact: masks could differ"
+    ref = o.backward(p, dy)
+    for k in ("delta", "dx", "dh0", "dWx", "dWh", "db"):
+        assert rel_err(g[k], ref[k]) <= 1e-6, (k, rel_err(g[k], ref[k]))
+
+
+def _min_abs_preact(o, p):
+    y = o.forward(p)
+    P = o.input_projection(p.x, p.Wx, p.b)
+    h0 = np.zeros((p.B, p.H)) if p.h0 is None else p.h0.astype(np.float64)
+    prev = np.concatenate([h0[None], y[:-1]], axis=0)
+    a = P + np.einsum("tbc,rc->tbr", prev, p.Wh.astype(np.float64))
+    return float(np.abs(a).min())
+
+
+@pytest.mark.parametrize("shape", [dict(H=256, I=128, B=4, T=16), dict(H=132, I=70, B=2, T=9)])
+def test_backward_random_fp32(env, shape):
+    """Random fp32 weights; the seed is the first one (from a fixed list)
+    whose pre-activations all stay 1e-4 away from 0 in the oracle."""
+    o = env[2]
+    for seed in range(600, 640):
+        p = synth.make_problem(seed=seed, wdtype="f32", h0_std=0.5, **shape)
+        if _min_abs_preact(o, p) > 1e-4:
+            break
+    else:
+        pytest.fail("no seed with pre-activations away from 0")
+    dy = np.random.default_rng(seed).normal(size=(p.T, p.B, p.H))
+    y, g = run(env, p, dy.astype(np.float32))
+    ref = o.backward(p, dy.astype(np.float32))
+    for k in ("delta", "dx", "dh0", "dWx", "dWh", "db"):
+        assert rel_err(g[k], ref[k]) <= 1e-4, (k, rel_err(g[k], ref[k]))
+
+
+def check_by_properties(env, p, dy, y, g, n_samples=300):
+    """Teacher-forced reverse recurrence on sampled (t, b, r), and every
+    gradient as its batched product of the GPU's own deltas."""
+    o = env[2]
+    Wh = p.Wh.astype(np.float64)
+    d = g["delta"]
+    rng = np.random.default_rng(7)
+    samples = [(int(t), int(b), int(r)) for t, b, r in zip(
+        rng.integers(0, p.T, n_samples), rng.integers(0, p.B, n_samples),
+        rng.integers(0, p.H, n_samples))]
+    samples += [(p.T - 1, 0, 0), (0, p.B - 1, p.H - 1)]
+    want = o.delta_cells(Wh, samples, lambda t, b: dy[t, b], lambda t, b: y[t, b],
+                         lambda t, b: None if t == p.T - 1 else d[t + 1, b])
+    got = np.array([d[t, b, r] for t, b, r in samples])
+    assert np.abs(got - want).max() <= 1e-4 * max(float(np.abs(d).max()), 1e-30)
+    h0 = np.zeros((p.B, p.H)) if p.h0 is None else p.h0.astype(np.float64)
+    prev = np.concatenate([h0[None], y[:-1]], axis=0)
+    x = p.x.astype(np.float64)
+    Wx = p.Wx.astype(np.float64)
+    refs = {"db": d.sum(axis=(0, 1)),
+            "dWh": np.einsum("tbr,tbc->rc", d, prev),
+            "dWx": np.einsum("tbr,tbc->rc", d, x),
+            "dx": np.einsum("tbr,rc->tbc", d, Wx),
+            "dh0": d[0] @ Wh}
+    for k, ref in refs.items():
+        assert rel_err(g[k], ref) <= 1e-4, (k, rel_err(g[k], ref))
+
+
+@pytest.mark.parametrize("spec", [dict(H=1152, B=4, T=32, wdtype="f16", h0_std=0.1),
+                                  dict(H=260, I=96, B=7, T=11, wdtype="f16"),
+                                  dict(H=4, I=4, B=2, T=3, wdtype="f32", h0_std=1.0),
+                                  dict(H=640, B=32, T=3, wdtype="f16")])
+def test_backward_properties(env, spec):
+    p = synth.make_problem(seed=700, **spec)
+    dy = np.random.default_rng(701).normal(size=(p.T, p.B, p.H)).astype(np.float32)
+    y, g = run(env, p, dy)
+    check_by_properties(env, p, dy.astype(np.float64), y, g)
+
+
+def test_backward_full_size(env):
+    """The dense fp16 H = 1152, B = 4 layer over the full 256 steps."""
+    p = synth.named_problem("dense_f16_h1152_b4_t256")
+    dy = np.random.default_rng(702).normal(size=(p.T, p.B, p.H)).astype(np.float32)
+    y, g = run(env, p, dy)
+    check_by_properties(env, p, dy.astype(np.float64), y, g, n_samples=400)
+
+
+def test_backward_errors_and_edges(env):
+    torch, prnn, _ = env
+    p = synth.make_problem(H=64, B=2, T=3, wdtype="f16", seed=703)
+    lay = prnn.prnn_create(64, 64, 2, prnn.PRNN_F16, prnn.PRNN_ALGO_PERSISTENT)
+    x = torch.from_numpy(p.x).cuda()
+    y = torch.zeros(3, 2, 64, device="cuda")
+    dy = torch.ones(3, 2, 64, device="cuda")
+    db = torch.full((64,), 7.0, device="cuda")
+    with pytest.raises(prnn.PrnnError) as e:
+        prnn.prnn_backward(lay, 3, 2, x, None, y, dy, db=db)
+    assert e.value.status == prnn.PRNN_ERR_NOT_READY
+    prnn.prnn_set_weights_dense(lay, torch.from_numpy(p.Wx).cuda(), torch.from_numpy(p.Wh).cuda(),
+                                torch.from_numpy(p.b).cuda())
+    prnn.prnn_backward(lay, 0, 2, x, None, y, dy, db=db)      # no steps: zero gradients
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(db).item() == 0
+    with pytest.raises(prnn.PrnnError) as e:                  # output overlaps an input
+        prnn.prnn_backward(lay, 3, 2, x, None, y, dy, dx=x)
+    assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    big = torch.zeros(64 * 64 + 4, device="cuda")
+    with pytest.raises(prnn.PrnnError) as e:                  # misaligned output
+        prnn.prnn_backward(lay, 3, 2, x, None, y, dy, dWh=big[1:].data_ptr())
+    assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    prnn.prnn_destroy(lay)
+    ps = prnn.prnn_create(64, 64, 2, prnn.PRNN_F16, prnn.PRNN_ALGO_PER_STEP)
+    prnn.prnn_set_weights_dense(ps, torch.from_numpy(p.Wx).cuda(), torch.from_numpy(p.Wh).cuda(),
+                                torch.from_numpy(p.b).cuda())
+    with pytest.raises(prnn.PrnnError) as e:
+        prnn.prnn_backward(ps, 3, 2, x, None, y, dy, db=db)
+    assert e.value.status == prnn.PRNN_ERR_UNSUPPORTED
+    prnn.prnn_destroy(ps)
+
+
+def test_backward_dropped_publish_times_out(env):
+    torch, prnn, o = env
+    p = synth.make_problem(H=512, B=4, T=6, wdtype="f16", seed=704)
+    lay = prnn.Layer.from_problem(p)
+    x = torch.from_numpy(p.x).cuda()
+    y = lay.forward(x)
+    lay.set_option(prnn.PRNN_OPT_WAIT_TIMEOUT_US, 20000)
+    lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_CTA, 3)
+    lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_STEP, 2)
+    lay.backward(x, y, torch.ones_like(y))
+    assert lay.status() == prnn.PRNN_ERR_TIMEOUT
+    lay.close()
