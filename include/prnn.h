@@ -175,9 +175,13 @@ prnn_status_t prnn_destroy(prnn_t h);
  * produced for them with these weights, dy [T][B][H].  Outputs (device, fp32,
  * overwritten; NULL skips that gradient): delta [T][B][H] (dL/da_t, the
  * gradient at the pre-activations; the library's workspace is used when
- * NULL), dx [T][B][I], dh0 [B][H], dWx [H][I], dWh [H][H], db [H].  Outputs must not overlap the inputs or each
- * other.  Asynchronous on `stream`; T == 0 or B == 0 writes zero gradients.
- * Dense persistent handles (PRNN_ERR_UNSUPPORTED otherwise).  After a timed
+ * NULL), dx [T][B][I], dh0 [B][H], dWx [H][I], db [H], and dWh: [H][H] for
+ * dense weights; for sparse weights the gradient of every stored value, in
+ * the order the values were passed to set_weights ([H][k] row-balanced, or
+ * [nnz] compressed rows).  Outputs must not overlap the inputs or each other.
+ * Asynchronous on `stream`; T == 0 or B == 0 writes zero gradients.
+ * Persistent handles (PRNN_ERR_UNSUPPORTED for PRNN_ALGO_PER_STEP, or when
+ * the transposed sparse matrix does not fit on chip).  After a timed
  * backward, prnn_get_timing reports (gradient products, reverse recurrence).
  */
 prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float* h0,

@@ -43,6 +43,19 @@ struct prnn_handle {
   void* Wpk = nullptr;       // persistent packed recurrent weights
   void* Wpk_T = nullptr;     // the same packing of Wh^T (backward pass, dense)
   void* Wh_nat = nullptr;    // Wh row-major [H][H] in wdtype (backward pass, dense)
+  // sparse backward: plan of the persistent kernel for Wh^T (packed in
+  // Wpk_T), the forward's padded column lists and each padded entry's index
+  // in the caller's order, Wh^T padded to kT entries per row, and the
+  // transposed-delta workspace
+  bool bwd_ok = false;
+  size_t n_caller = 0;            // entries the caller passed (H*k, or nnz)
+  int b_n_cta = 0, b_R = 0, b_G = 1, b_cpg = 0, b_nthreads = 0, b_tpr = 0, b_ept = 0, kT = 0;
+  uint16_t* cols_pad = nullptr;   // [H][k]
+  int32_t* caller_pos = nullptr;  // [H][k], -1 for padding
+  uint16_t* valsT = nullptr;      // [H][kT] fp16 bits
+  uint16_t* colsT = nullptr;      // [H][kT]
+  float* tws = nullptr;           // [2][H][T*B]
+  size_t tws_cap = 0;
   void* Wstep = nullptr;     // per-step layout of the recurrent weights
   float* P = nullptr;
   size_t P_cap = 0;
@@ -215,14 +228,18 @@ std::vector<SparsePlan> plan_sparse(const prnn_handle* h, int k) {
   return out;
 }
 
-// Batch group and staging buffers of the sparse kernel for a given B.
-bool sparse_batch_plan(const prnn_handle* h, int B, int* bgroup, bool* dbuf, size_t* smem) {
-  const int bl = (B + h->G - 1) / h->G;  // batch columns of one CTA group
+// Batch group and staging buffers of the sparse kernel for a given B, for
+// the plan (G, R, ept, tpr): the forward's by default.
+bool sparse_batch_plan(const prnn_handle* h, int B, int* bgroup, bool* dbuf, size_t* smem,
+                       bool transposed = false) {
+  const int G = transposed ? h->b_G : h->G, R = transposed ? h->b_R : h->R;
+  const int ept = transposed ? h->b_ept : h->ept, tpr = transposed ? h->b_tpr : h->tpr;
+  const int bl = (B + G - 1) / G;  // batch columns of one CTA group
   int want = 1;
   while (want < bl && want < 32) want *= 2;
   for (int bg = want; bg >= 1; bg /= 2) {
     for (int db = 1; db >= 0; --db) {
-      const size_t s = recur_sparse_smem(h->H, h->R, h->ept, h->tpr, bg, db == 1);
+      const size_t s = recur_sparse_smem(h->H, R, ept, tpr, bg, db == 1);
       if (s <= h->smem_optin) {
         *bgroup = bg;
         *dbuf = db == 1;
@@ -294,6 +311,11 @@ void free_weights(prnn_handle* h) {
   free_dev(h->Wpk);
   free_dev(h->Wpk_T);
   free_dev(h->Wh_nat);
+  free_dev(h->cols_pad);
+  free_dev(h->caller_pos);
+  free_dev(h->valsT);
+  free_dev(h->colsT);
+  h->bwd_ok = false;
   free_dev(h->Wstep);
   h->weights_set = false;
 }
@@ -325,33 +347,74 @@ RecurCommon common_args(const prnn_handle* h, int T, int B, const float* h0, flo
 
 }  // namespace
 
-// Plan, pack and upload row-padded sparse weights: hv/hc are [H][k] with each
-// row sorted by column (padding entries: value 0).  Shared by the
-// row-balanced and the compressed-row entry points.
+// Plan and pack [H][k] row-padded sparse rows for the persistent kernel:
+// the first plan (fastest by the model) whose packing fits shared memory.
+static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
+                          const std::vector<uint16_t>& hc, SparsePlan* plan,
+                          std::vector<uint32_t>* pk, PackStats* pst) {
+  const int H = h->H;
+  for (const SparsePlan& cand : plan_sparse(h, k)) {
+    // largest entries-per-thread whose weights plus one h column fit in smem
+    const size_t hs1 = (size_t)H * sizeof(float);
+    if (hs1 >= h->smem_optin) continue;
+    const int max_ept = (int)(((h->smem_optin - hs1) / ((size_t)cand.R * cand.tpr * 4)) / 4 * 4);
+    *plan = cand;
+    plan->ept = pack_sparse_rows(H, k, plan->R, plan->cpg, plan->tpr, hv.data(), hc.data(), *pk,
+                                 pst, max_ept, h->bank_aware != 0);
+    if (plan->ept > 0) {
+      plan->kp = plan->ept * plan->tpr;
+      return true;
+    }
+  }
+  return false;
+}
+
+// Plan, pack and upload row-padded sparse weights (hv/hc [H][k], each row
+// sorted by column, padding entries valued 0), and build the packed Wh^T and
+// the index maps the backward pass uses.  Shared by the row-balanced and the
+// compressed-row entry points.
+// caller_pos[r*k + j] is the index of padded entry (r, j) in the caller's
+// value array, -1 for padding.
 static prnn_status_t install_sparse(prnn_t h, const void* Wx, const float* bias,
-                                    std::vector<uint16_t>& hv, std::vector<uint16_t>& hc, int k) {
+                                    std::vector<uint16_t>& hv, std::vector<uint16_t>& hc, int k,
+                                    const std::vector<int32_t>& caller_pos) {
   const int H = h->H;
   SparsePlan plan{};
   std::vector<uint32_t> pk;
   PackStats pst;
-  if (h->algo == PRNN_ALGO_PERSISTENT) {
-    bool packed = false;
-    for (const SparsePlan& cand : plan_sparse(h, k)) {
-      // largest entries-per-thread whose weights plus one h column fit in smem
-      const size_t hs1 = (size_t)H * sizeof(float);
-      if (hs1 >= h->smem_optin) continue;
-      const int max_ept = (int)(((h->smem_optin - hs1) / ((size_t)cand.R * cand.tpr * 4)) / 4 * 4);
-      plan = cand;
-      plan.ept = pack_sparse_rows(H, k, plan.R, plan.cpg, plan.tpr, hv.data(), hc.data(), pk,
-                                  &pst, max_ept, h->bank_aware != 0);
-      if (plan.ept > 0) {
-        packed = true;
-        break;
+  if (h->algo == PRNN_ALGO_PERSISTENT && !plan_and_pack(h, k, hv, hc, &plan, &pk, &pst))
+    return PRNN_ERR_UNSUPPORTED;
+  // Wh^T: row c lists the stored (r, value) of column c in ascending r,
+  // padded to the longest such list with zero-valued absent columns
+  std::vector<std::vector<std::pair<uint16_t, uint16_t>>> tr((size_t)H);
+  for (int r = 0; r < H; ++r)
+    for (int j = 0; j < k; ++j)
+      if (caller_pos[(size_t)r * k + j] >= 0)
+        tr[hc[(size_t)r * k + j]].push_back({(uint16_t)r, hv[(size_t)r * k + j]});
+  int kT = 1;
+  for (const auto& v : tr) kT = std::max(kT, (int)v.size());
+  std::vector<uint16_t> hvT((size_t)H * kT, 0), hcT((size_t)H * kT, 0);
+  {
+    std::vector<int> in_row((size_t)H, -1);
+    for (int c = 0; c < H; ++c) {
+      auto& v = tr[c];
+      for (const auto& e : v) in_row[e.first] = c;
+      for (int r = 0; r < H && (int)v.size() < kT; ++r)
+        if (in_row[r] != c) v.push_back({(uint16_t)r, 0});
+      std::sort(v.begin(), v.end(),
+                [](const std::pair<uint16_t, uint16_t>& a, const std::pair<uint16_t, uint16_t>& b) {
+                  return a.first < b.first;
+                });
+      for (int j = 0; j < kT; ++j) {
+        hcT[(size_t)c * kT + j] = v[j].first;
+        hvT[(size_t)c * kT + j] = v[j].second;
       }
     }
-    if (!packed) return PRNN_ERR_UNSUPPORTED;
-    plan.kp = plan.ept * plan.tpr;
   }
+  SparsePlan tplan{};
+  std::vector<uint32_t> pkT;
+  PackStats pstT;
+  const bool bwd = h->algo == PRNN_ALGO_PERSISTENT && plan_and_pack(h, kT, hvT, hcT, &tplan, &pkT, &pstT);
   free_weights(h);
   prnn_status_t st = stage_wx_bias(h, Wx, bias, &h->Wx, &h->Wx16, &h->bias);
   if (st != PRNN_OK) return st;
@@ -375,6 +438,25 @@ static prnn_status_t install_sparse(prnn_t h, const void* Wx, const float* bias,
     size_t sm = 0;
     sparse_batch_plan(h, h->maxB, &bg, &db, &sm);
     h->smem_at_max = sm;
+    if (bwd) {
+      PRNN_TRY(upload(&h->Wpk_T, pkT.data(), pkT.size() * 4));
+      PRNN_TRY(upload(&h->cols_pad, hc.data(), hc.size() * 2));
+      PRNN_TRY(upload(&h->caller_pos, caller_pos.data(), caller_pos.size() * 4));
+      PRNN_TRY(upload(&h->valsT, hvT.data(), hvT.size() * 2));
+      PRNN_TRY(upload(&h->colsT, hcT.data(), hcT.size() * 2));
+      h->b_n_cta = tplan.n_cta;
+      h->b_R = tplan.R;
+      h->b_G = tplan.G;
+      h->b_cpg = tplan.cpg;
+      h->b_nthreads = tplan.nthreads;
+      h->b_tpr = tplan.tpr;
+      h->b_ept = tplan.ept;
+      h->kT = kT;
+      h->bwd_ok = true;
+      size_t n = 0;
+      for (int32_t p : caller_pos) n += p >= 0 ? 1 : 0;
+      h->n_caller = n;
+    }
   } else {
     std::vector<uint32_t> ws((size_t)H * k);
     for (int r = 0; r < H; ++r)
@@ -458,6 +540,7 @@ prnn_status_t prnn_destroy(prnn_t h) {
   free_weights(h);
   free_dev(h->P);
   free_dev(h->x16);
+  free_dev(h->tws);
   free_dev(h->status);
   free_dev(h->bar);
   for (auto& e : h->ev)
@@ -542,24 +625,28 @@ prnn_status_t prnn_set_weights_sparse(prnn_t h, const void* Wx, int k, const uin
   PRNN_TRY(to_host(hc.data(), cols, hc.size() * 2));
   // validate: columns in range, distinct within each row; sort each row by column
   std::vector<int> seen((size_t)H, -1);
-  std::vector<std::pair<uint16_t, uint16_t>> row(k);
+  std::vector<int32_t> pos((size_t)H * k);
+  std::vector<std::pair<uint16_t, int>> row(k);  // (column, index in the caller's row)
+  std::vector<uint16_t> rv(k);
   for (int r = 0; r < H; ++r) {
     for (int j = 0; j < k; ++j) {
       const int c = hc[(size_t)r * k + j];
       if (c >= H || seen[c] == r) return PRNN_ERR_INVALID_ARG;
       seen[c] = r;
-      row[j] = {hc[(size_t)r * k + j], hv[(size_t)r * k + j]};
+      row[j] = {hc[(size_t)r * k + j], j};
+      rv[j] = hv[(size_t)r * k + j];
     }
     std::sort(row.begin(), row.end(),
-              [](const std::pair<uint16_t, uint16_t>& a, const std::pair<uint16_t, uint16_t>& b) {
+              [](const std::pair<uint16_t, int>& a, const std::pair<uint16_t, int>& b) {
                 return a.first < b.first;
               });
     for (int j = 0; j < k; ++j) {
       hc[(size_t)r * k + j] = row[j].first;
-      hv[(size_t)r * k + j] = row[j].second;
+      hv[(size_t)r * k + j] = rv[row[j].second];
+      pos[(size_t)r * k + j] = r * k + row[j].second;
     }
   }
-  return install_sparse(h, Wx, bias, hv, hc, k);
+  return install_sparse(h, Wx, bias, hv, hc, k, pos);
 }
 
 prnn_status_t prnn_set_weights_csr(prnn_t h, const void* Wx, int nnz, const int32_t* row_ptr,
@@ -599,26 +686,29 @@ prnn_status_t prnn_set_weights_csr(prnn_t h, const void* Wx, int nnz, const int3
   // padding takes the columns the row lacks, in ascending order, so padded
   // rows keep distinct columns spread over the shared-memory banks.
   std::vector<uint16_t> hv((size_t)H * kmax, 0), hc((size_t)H * kmax, 0);
-  std::vector<std::pair<uint16_t, uint16_t>> row;
+  std::vector<int32_t> pos((size_t)H * kmax, -1);
+  struct Ent {
+    uint16_t col, val;
+    int32_t src;  // index in the caller's arrays, -1 for padding
+  };
+  std::vector<Ent> row;
   std::vector<int> in_row((size_t)H, -1);
   for (int r = 0; r < H; ++r) {
     row.clear();
     for (int j = rp[r]; j < rp[r + 1]; ++j) {
-      row.push_back({cv[j], vv[j]});
+      row.push_back({cv[j], vv[j], j});
       in_row[cv[j]] = r;
     }
     for (int c = 0; c < H && (int)row.size() < kmax; ++c)
-      if (in_row[c] != r) row.push_back({(uint16_t)c, 0});
-    std::sort(row.begin(), row.end(),
-              [](const std::pair<uint16_t, uint16_t>& a, const std::pair<uint16_t, uint16_t>& b) {
-                return a.first < b.first;
-              });
+      if (in_row[c] != r) row.push_back({(uint16_t)c, 0, -1});
+    std::sort(row.begin(), row.end(), [](const Ent& a, const Ent& b) { return a.col < b.col; });
     for (int j = 0; j < kmax; ++j) {
-      hc[(size_t)r * kmax + j] = row[j].first;
-      hv[(size_t)r * kmax + j] = row[j].second;
+      hc[(size_t)r * kmax + j] = row[j].col;
+      hv[(size_t)r * kmax + j] = row[j].val;
+      pos[(size_t)r * kmax + j] = row[j].src;
     }
   }
-  return install_sparse(h, Wx, bias, hv, hc, kmax);
+  return install_sparse(h, Wx, bias, hv, hc, kmax, pos);
 }
 
 prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* h0, float* y,
@@ -732,13 +822,13 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
   if (!h) return PRNN_ERR_INVALID_ARG;
   if (h->sticky_timeout) return PRNN_ERR_TIMEOUT;
   if (!h->weights_set) return PRNN_ERR_NOT_READY;
-  if (h->algo != PRNN_ALGO_PERSISTENT || h->sparse) return PRNN_ERR_UNSUPPORTED;
+  if (h->algo != PRNN_ALGO_PERSISTENT || (h->sparse && !h->bwd_ok)) return PRNN_ERR_UNSUPPORTED;
   if (T < 0 || B < 0 || B > h->maxB) return PRNN_ERR_INVALID_ARG;
   const int H = h->H, I = h->I;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (T == 0 || B == 0) {  // no steps: every gradient is zero
     if (dWx) PRNN_TRY(cudaMemsetAsync(dWx, 0, (size_t)H * I * 4, s));
-    if (dWh) PRNN_TRY(cudaMemsetAsync(dWh, 0, (size_t)H * H * 4, s));
+    if (dWh) PRNN_TRY(cudaMemsetAsync(dWh, 0, (h->sparse ? h->n_caller : (size_t)H * H) * 4, s));
     if (db) PRNN_TRY(cudaMemsetAsync(db, 0, (size_t)H * 4, s));
     if (dh0 && B > 0) PRNN_TRY(cudaMemsetAsync(dh0, 0, (size_t)B * H * 4, s));
     return PRNN_OK;
@@ -751,8 +841,9 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
   for (const void* p : outs)
     if (p && !aligned16(p)) return PRNN_ERR_INVALID_ARG;
   const size_t ny = (size_t)T * B * H;
+  const size_t dwh_n = h->sparse ? h->n_caller : (size_t)H * H;
   const size_t out_bytes[] = {(size_t)T * B * I * 4, (size_t)B * H * 4, (size_t)H * I * 4,
-                              (size_t)H * H * 4, (size_t)H * 4, ny * 4};
+                              dwh_n * 4, (size_t)H * 4, ny * 4};
   const size_t in_bytes[] = {(size_t)T * B * I * 4, (size_t)B * H * 4, ny * 4, ny * 4};
   for (int o = 0; o < 6; ++o) {
     if (!outs[o]) continue;
@@ -776,23 +867,61 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
   c.reverse = 1;
   c.mask = y;
   c.sync_mode = 0;
-  DenseRecurArgs a{};
-  const int bw = std::min(recur_dense_bw((B + h->G - 1) / h->G), h->dense_bw);
-  c.smem = recur_dense_smem(h->R, h->cpt, h->nthreads, h->wdtype == PRNN_F16, bw);
-  a.c = c;
-  a.Wpk = h->Wpk_T;
-  a.cpt = h->cpt;
-  a.wfp16 = h->wdtype == PRNN_F16;
-  PRNN_TRY(launch_recur_dense(a, bw, s));
+  if (h->sparse) {  // Wh^T has its own plan (its rows are Wh's columns)
+    c.n_cta = h->b_n_cta;
+    c.R = h->b_R;
+    c.G = h->b_G;
+    c.cpg = h->b_cpg;
+    c.nthreads = h->b_nthreads;
+    c.poll_delay = h->poll_delay_ns >= 0 ? (int)((long long)h->poll_delay_ns * h->clock_khz / 1000000LL)
+                                         : (int)((long long)kSparseDelayNs * h->clock_khz / 1000000LL);
+    SparseRecurArgs a{};
+    int bg = 4;
+    bool dbuf = false;
+    size_t sm = 0;
+    if (!sparse_batch_plan(h, B, &bg, &dbuf, &sm, true)) return PRNN_ERR_UNSUPPORTED;
+    c.smem = sm;
+    a.c = c;
+    a.Wpk = static_cast<const uint32_t*>(h->Wpk_T);
+    a.tpr = h->b_tpr;
+    a.ept = h->b_ept;
+    a.bgroup = bg;
+    a.dbuf = dbuf ? 1 : 0;
+    a.narrow = 0;
+    PRNN_TRY(launch_recur_sparse(a, s));
+  } else {
+    DenseRecurArgs a{};
+    const int bw = std::min(recur_dense_bw((B + h->G - 1) / h->G), h->dense_bw);
+    c.smem = recur_dense_smem(h->R, h->cpt, h->nthreads, h->wdtype == PRNN_F16, bw);
+    a.c = c;
+    a.Wpk = h->Wpk_T;
+    a.cpt = h->cpt;
+    a.wfp16 = h->wdtype == PRNN_F16;
+    PRNN_TRY(launch_recur_dense(a, bw, s));
+  }
   if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[1], s));
 
   // 2. batched gradients over all T*B rows of delta
   const int K = T * B;
   const bool f16 = h->wdtype == PRNN_F16;
   if (db) PRNN_TRY(launch_colsum(delta, K, H, db, s));
-  if (dWh) {
+  if (dWh && !h->sparse) {
     GemmTnArgs g{H, H, K, B, delta, H, h0, y, H, dWh};
     PRNN_TRY(launch_gemm_tn(g, s));
+  }
+  if (dWh && h->sparse) {  // only at the stored entries, in the caller's order
+    const size_t need = (size_t)2 * H * K;
+    if (need > h->tws_cap) {
+      free_dev(h->tws);
+      h->tws_cap = 0;
+      PRNN_TRY(cudaMalloc((void**)&h->tws, need * sizeof(float)));
+      h->tws_cap = need;
+    }
+    float* dT = h->tws;
+    float* hT = h->tws + (size_t)H * K;
+    PRNN_TRY(launch_transpose_rows(K, H, 0, nullptr, delta, H, dT, s));
+    PRNN_TRY(launch_transpose_rows(K, H, B, h0, y, H, hT, s));
+    PRNN_TRY(launch_sddmm(H, h->k, K, dT, hT, h->cols_pad, h->caller_pos, dWh, s));
   }
   if (dWx) {
     GemmTnArgs g{H, I, K, 0, delta, H, nullptr, x, I, dWx};
@@ -802,10 +931,11 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
     GemmNnArgs g{K, I, H, delta, H, h->Wx, I, f16 ? 1 : 0, dx};
     PRNN_TRY(launch_gemm_nn(g, s));
   }
-  if (dh0) {
+  if (dh0 && !h->sparse) {
     GemmNnArgs g{B, H, H, delta, H, h->Wh_nat, H, f16 ? 1 : 0, dh0};
     PRNN_TRY(launch_gemm_nn(g, s));
   }
+  if (dh0 && h->sparse) PRNN_TRY(launch_sparse_dh0(B, H, h->kT, h->valsT, h->colsT, delta, dh0, s));
   if (h->timing) {
     PRNN_TRY(cudaEventRecord(h->ev[2], s));
     h->ev_valid = true;

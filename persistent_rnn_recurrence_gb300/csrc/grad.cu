@@ -7,6 +7,11 @@
 //   dWh = delta^T [h0 ; y_0 .. y_{T-2}]              (gemm_tn_kernel)
 //   dWx = delta^T x                                  (gemm_tn_kernel)
 //   dx  = delta Wx,  dh0 = delta_0 Wh                (gemm_nn_kernel)
+// For sparse Wh the weight gradient is needed only at the stored entries:
+//   dvals[r][j] = sum_k delta[k][r] * Hprev[k][cols[r][j]]     (sddmm_kernel)
+// computed as dot products of rows of the transposed delta and Hprev (each
+// a contiguous T*B vector), and dh0 = Wh^T delta_0 walks the rows of the
+// padded Wh^T (sparse_dh0_kernel).
 // They are the products the chain rule gives for the layer's two matrix
 // products; like the forward projection they carry no dependence between
 // steps and run as whole-sequence GEMMs ("Optimizing Performance of
@@ -15,6 +20,7 @@
 // slices staged in shared memory, 4 x 4 outputs per thread): the gradients
 // are kept in full fp32, and these GEMMs are a few percent of a training
 // step next to the serial recurrences.
+#include <cstdint>
 #include <cuda_fp16.h>
 
 #include "prnn_internal.h"
@@ -139,7 +145,89 @@ __global__ void colsum_kernel(const float* A, int K, int N, float* out) {
   out[n] = s;
 }
 
+// out[n][k] = Brow(k)[n] for k < K, n < N (Brow as in gemm_tn: B0 rows for
+// k < K0, zeros if B0 is null, then B1 rows); 32 x 32 tiles through smem.
+__global__ void transpose_rows_kernel(int K, int N, int K0, const float* B0, const float* B1,
+                                      int ldb, float* out) {
+  __shared__ float tile[32][33];
+  const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8 threads
+  for (int i = ty; i < 32; i += 8) {
+    const int k = k0 + i, n = n0 + tx;
+    float v = 0.f;
+    if (k < K && n < N) {
+      const float* row = k < K0 ? (B0 ? B0 + (size_t)k * ldb : nullptr)
+                                : B1 + (size_t)(k - K0) * ldb;
+      if (row) v = row[n];
+    }
+    tile[i][tx] = v;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int n = n0 + i, k = k0 + tx;
+    if (n < N && k < K) out[(size_t)n * K + k] = tile[tx][i];
+  }
+}
+
+// One warp per row r of the padded forward layout: for each stored entry
+// (r, cols[r][j]) the dot product of dT[r] and hT[cols[r][j]] (length K),
+// written to out[caller_pos[r][j]] (padding entries are skipped).
+__global__ void sddmm_kernel(int H, int kp, int K, const float* dT, const float* hT,
+                             const uint16_t* cols, const int32_t* caller_pos, float* out) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= H) return;
+  const int r = warp;
+  const float* dr = dT + (size_t)r * K;
+  for (int j = 0; j < kp; ++j) {
+    const int pos = caller_pos[(size_t)r * kp + j];
+    if (pos < 0) continue;
+    const float* hc = hT + (size_t)cols[(size_t)r * kp + j] * K;
+    float s = 0.f;
+    for (int k = lane; k < K; k += 32) s = fmaf(dr[k], hc[k], s);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) out[pos] = s;
+  }
+}
+
+// dh0[b][c] = sum_j valsT[c][j] * delta0[b][colsT[c][j]] (Wh^T padded rows).
+__global__ void sparse_dh0_kernel(int B, int H, int kT, const uint16_t* valsT,
+                                  const uint16_t* colsT, const float* delta0, float* dh0) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= B * H) return;
+  const int b = i / H, c = i % H;
+  float s = 0.f;
+  for (int j = 0; j < kT; ++j) {
+    const float v = __half2float(__ushort_as_half(valsT[(size_t)c * kT + j]));
+    s = fmaf(v, delta0[(size_t)b * H + colsT[(size_t)c * kT + j]], s);
+  }
+  dh0[i] = s;
+}
+
 }  // namespace
+
+cudaError_t launch_transpose_rows(int K, int N, int K0, const float* B0, const float* B1, int ldb,
+                                  float* out, cudaStream_t s) {
+  if (K <= 0 || N <= 0) return cudaSuccess;
+  dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
+  transpose_rows_kernel<<<grid, block, 0, s>>>(K, N, K0, B0, B1, ldb, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sddmm(int H, int kp, int K, const float* dT, const float* hT,
+                         const uint16_t* cols, const int32_t* caller_pos, float* out,
+                         cudaStream_t s) {
+  if (H <= 0) return cudaSuccess;
+  sddmm_kernel<<<(H * 32 + 255) / 256, 256, 0, s>>>(H, kp, K, dT, hT, cols, caller_pos, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_dh0(int B, int H, int kT, const uint16_t* valsT, const uint16_t* colsT,
+                              const float* delta0, float* dh0, cudaStream_t s) {
+  if (B * H <= 0) return cudaSuccess;
+  sparse_dh0_kernel<<<(B * H + 255) / 256, 256, 0, s>>>(B, H, kT, valsT, colsT, delta0, dh0);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemm_tn(const GemmTnArgs& g, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;

@@ -194,5 +194,12 @@ struct GemmNnArgs {
 cudaError_t launch_gemm_tn(const GemmTnArgs& g, cudaStream_t s);
 cudaError_t launch_gemm_nn(const GemmNnArgs& g, cudaStream_t s);
 cudaError_t launch_colsum(const float* A, int K, int N, float* out, cudaStream_t s);
+cudaError_t launch_transpose_rows(int K, int N, int K0, const float* B0, const float* B1, int ldb,
+                                  float* out, cudaStream_t s);
+cudaError_t launch_sddmm(int H, int kp, int K, const float* dT, const float* hT,
+                         const uint16_t* cols, const int32_t* caller_pos, float* out,
+                         cudaStream_t s);
+cudaError_t launch_sparse_dh0(int B, int H, int kT, const uint16_t* valsT, const uint16_t* colsT,
+                              const float* delta0, float* dh0, cudaStream_t s);
 
 }  // namespace prnn

@@ -302,6 +302,7 @@ class Layer:
             vals = torch.from_numpy(np.ascontiguousarray(p.vals).view(np.int16)).to(device)
             cols = torch.from_numpy(np.ascontiguousarray(p.cols).view(np.int16)).to(device)
             prnn_set_weights_csr(self.h, Wx, int(p.vals.size), rp, cols, vals, b)
+            self.n_values = int(p.vals.size)
         elif p.sparse:
             vals = torch.from_numpy(np.ascontiguousarray(p.vals).view(np.int16)).to(device)
             cols = torch.from_numpy(np.ascontiguousarray(p.cols).view(np.int16)).to(device)
@@ -326,10 +327,15 @@ class Layer:
         import torch
         T, B, _ = x.shape
         dev = x.device
+        info = self.info()
+        if info["sparse"]:
+            nv = self.n_values if getattr(self, "n_values", None) else info["hidden"] * info["k"]
+            dwh = torch.empty(nv, device=dev)
+        else:
+            dwh = torch.empty(self.hidden, self.hidden, device=dev)
         g = {"delta": torch.empty_like(y),
              "dx": torch.empty_like(x), "dh0": torch.empty(B, self.hidden, device=dev),
-             "dWx": torch.empty(self.hidden, self.input, device=dev),
-             "dWh": torch.empty(self.hidden, self.hidden, device=dev),
+             "dWx": torch.empty(self.hidden, self.input, device=dev), "dWh": dwh,
              "db": torch.empty(self.hidden, device=dev)}
         prnn_backward(self.h, T, B, x, h0, y, dy, g["delta"], g["dx"], g["dh0"], g["dWx"], g["dWh"],
                       g["db"], stream)

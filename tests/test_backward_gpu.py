@@ -199,3 +199,95 @@ def test_backward_dropped_publish_times_out(env):
     lay.backward(x, y, torch.ones_like(y))
     assert lay.status() == prnn.PRNN_ERR_TIMEOUT
     lay.close()
+
+
+# --- sparse weights -------------------------------------------------------------
+def dense_of(p):
+    Wh = np.zeros((p.H, p.H))
+    if getattr(p, "row_ptr", None) is not None:
+        rows = np.repeat(np.arange(p.H), np.diff(p.row_ptr))
+        Wh[rows, p.cols.astype(np.int64)] = p.vals.astype(np.float64)
+    else:
+        rows = np.repeat(np.arange(p.H), p.k)
+        Wh[rows, p.cols.astype(np.int64).ravel()] = p.vals.astype(np.float64).ravel()
+    return Wh
+
+
+def dyadic_sparse_problem(seed, H, I, B, T, k, csr=False):
+    """Row-balanced (or, with csr, rows of 0..2k entries) Wh of +-0.5 values;
+    columns deliberately unsorted; every fp32 sum on the GPU exact."""
+    rng = np.random.default_rng(seed)
+    q = lambda *s: rng.integers(-8, 9, size=s).astype(np.float64) / 8
+    if csr:
+        lens = rng.integers(0, 2 * k + 1, size=H)
+        lens[0] = 0
+        row_ptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        cols = np.concatenate([rng.choice(H, n, replace=False) for n in lens]).astype(np.uint16)
+        vals = rng.choice([-0.5, 0.5], size=int(lens.sum())).astype(np.float16)
+    else:
+        row_ptr = None
+        cols = np.stack([rng.choice(H, k, replace=False) for _ in range(H)]).astype(np.uint16)
+        vals = rng.choice([-0.5, 0.5], size=(H, k)).astype(np.float16)
+    p = synth.Problem(name="dyadic_sparse", T=T, B=B, H=H, I=I, wdtype="f16",
+                      x=q(T, B, I).astype(np.float32), Wx=(q(H, I) / 4).astype(np.float16),
+                      b=q(H).astype(np.float32), h0=q(B, H).astype(np.float32), vals=vals,
+                      cols=cols, row_ptr=row_ptr)
+    return p, q(T, B, H)
+
+
+@pytest.mark.parametrize("csr", [False, True])
+@pytest.mark.parametrize("shape", [dict(H=64, I=32, B=3, T=6, k=3), dict(H=512, I=96, B=4, T=5, k=3)])
+def test_sparse_backward_exact_problems(env, csr, shape):
+    p, dy = dyadic_sparse_problem(800 + shape["H"], csr=csr, **shape)
+    o = env[2]
+    y, g = run(env, p, dy.astype(np.float32))
+    assert np.array_equal(y, o.forward(p)), "forward not exact: masks could differ"
+    ref = o.backward(p, dy)
+    assert rel_err(g["dWh"], ref["dvals"].ravel()) <= 1e-6
+    for k in ("delta", "dx", "dh0", "dWx", "db"):
+        assert rel_err(g[k], ref[k]) <= 1e-6, (k, rel_err(g[k], ref[k]))
+
+
+def check_sparse_by_properties(env, p, dy, y, g, n_samples=300):
+    o = env[2]
+    Wh = dense_of(p)
+    d = g["delta"]
+    rng = np.random.default_rng(8)
+    samples = [(int(t), int(b), int(r)) for t, b, r in zip(
+        rng.integers(0, p.T, n_samples), rng.integers(0, p.B, n_samples),
+        rng.integers(0, p.H, n_samples))]
+    want = o.delta_cells(Wh, samples, lambda t, b: dy[t, b], lambda t, b: y[t, b],
+                         lambda t, b: None if t == p.T - 1 else d[t + 1, b])
+    got = np.array([d[t, b, r] for t, b, r in samples])
+    assert np.abs(got - want).max() <= 1e-4 * max(float(np.abs(d).max()), 1e-30)
+    h0 = np.zeros((p.B, p.H)) if p.h0 is None else p.h0.astype(np.float64)
+    prev = np.concatenate([h0[None], y[:-1]], axis=0)
+    dense_grad = np.einsum("tbr,tbc->rc", d, prev)
+    if getattr(p, "row_ptr", None) is not None:
+        rows = np.repeat(np.arange(p.H), np.diff(p.row_ptr))
+        dvals = dense_grad[rows, p.cols.astype(np.int64)]
+    else:
+        dvals = dense_grad[np.repeat(np.arange(p.H), p.k), p.cols.astype(np.int64).ravel()]
+    assert rel_err(g["dWh"], dvals) <= 1e-4
+    refs = {"db": d.sum(axis=(0, 1)), "dWx": np.einsum("tbr,tbc->rc", d, p.x.astype(np.float64)),
+            "dx": np.einsum("tbr,rc->tbc", d, p.Wx.astype(np.float64)), "dh0": d[0] @ Wh}
+    for k, ref in refs.items():
+        assert rel_err(g[k], ref) <= 1e-4, (k, rel_err(g[k], ref))
+
+
+@pytest.mark.parametrize("name,T", [("sparse_f16_h1792_d10_b4_t256", 32),
+                                    ("sparse_f16_h1792_d10_b4_t256", None),
+                                    ("sparse_f16_h5760_d1_b4_t256", 16)])
+def test_sparse_backward_properties(env, name, T):
+    p = synth.named_problem(name, T=T)
+    dy = np.random.default_rng(705).normal(size=(p.T, p.B, p.H)).astype(np.float32)
+    y, g = run(env, p, dy)
+    check_sparse_by_properties(env, p, dy.astype(np.float64), y, g)
+
+
+def test_csr_backward_properties(env):
+    p, _ = synth.make_pruned_pair(H=1792, B=4, T=24, density=0.10, seed=706)
+    dy = np.random.default_rng(707).normal(size=(p.T, p.B, p.H)).astype(np.float32)
+    y, g = run(env, p, dy)
+    assert g["dWh"].shape == (p.nnz,)
+    check_sparse_by_properties(env, p, dy.astype(np.float64), y, g)
