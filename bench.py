@@ -58,6 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--stack", action="store_true",
                     help="stacked layers: one-launch wavefront vs layer by layer, "
                          "H = 256 / 512 / 1152, L = 1 .. 8")
+    ap.add_argument("--backward", action="store_true",
+                    help="training step (forward + backward through time) of the named workloads")
     return ap.parse_args(argv)
 
 
@@ -709,6 +711,55 @@ def run_stack(args):
     return 0
 
 
+def run_backward(args):
+    """Training-step timing (forward + backward through time) for the named
+    workloads at T = 256: the forward, the reverse recurrence and the batched
+    gradient products, CUDA events, L2 flushed before every step."""
+    import numpy as np
+    import torch
+    from persistent_rnn_recurrence_gb300 import prnn, synth
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    reps = max(5, min(args.steps, 20))
+    out = []
+    for name in ("sparse_f16_h1792_d10_b4_t256", "dense_f16_h1152_b4_t256",
+                 "sparse_f16_h5760_d1_b4_t256", "sparse_f16_h5760_d5_b4_t256"):
+        p = synth.named_problem(name)
+        lay = prnn.Layer.from_problem(p)
+        lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+        x = torch.from_numpy(p.x).to(dev)
+        h0 = None if p.h0 is None else torch.from_numpy(p.h0).to(dev)
+        y = torch.empty((p.T, p.B, p.H), dtype=torch.float32, device=dev)
+        dy = torch.from_numpy(np.random.default_rng(9).normal(
+            size=(p.T, p.B, p.H)).astype(np.float32)).to(dev)
+        g = lay.backward(x, lay.forward(x, h0, y), dy, h0)
+        fwd, rev, prod, tot = [], [], [], []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            prnn.prnn_forward(lay.h, p.T, p.B, x, h0, y)
+            f = prnn.prnn_get_timing(lay.h)
+            prnn.prnn_backward(lay.h, p.T, p.B, x, h0, y, dy, g["delta"], g["dx"], g["dh0"],
+                               g["dWx"], g["dWh"], g["db"])
+            e1.record()
+            b = prnn.prnn_get_timing(lay.h)
+            torch.cuda.synchronize()
+            fwd.append(f[0] + f[1])
+            prod.append(b[0])
+            rev.append(b[1])
+            tot.append(e0.elapsed_time(e1))
+        assert lay.status() == prnn.PRNN_OK
+        lay.close()
+        med = lambda v: sorted(v)[len(v) // 2]
+        out.append({"workload": name, "ms_train_step": med(tot), "ms_forward": med(fwd),
+                    "ms_reverse_recurrence": med(rev), "ms_gradient_products": med(prod),
+                    "us_per_step_reverse": 1e3 * med(rev) / p.T,
+                    "train_timesteps_per_s": p.T / (med(tot) * 1e-3)})
+    print(json.dumps({"backward": out}))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -721,6 +772,8 @@ def main(argv=None):
         return run_balance(args)
     if args.stack:
         return run_stack(args)
+    if args.backward:
+        return run_backward(args)
     return run_ours(args)
 
 

@@ -56,6 +56,11 @@ struct prnn_handle {
   uint16_t* colsT = nullptr;      // [H][kT]
   float* tws = nullptr;           // [2][H][T*B]
   size_t tws_cap = 0;
+  // tensor-core gradient products (fp16 handles): Wx^T in bf16 [I][Hp]
+  // (Hp = H rounded up to 64), and bf16 staging of delta, h and x
+  uint16_t* WxT16 = nullptr;
+  uint16_t* gws16 = nullptr;
+  size_t gws16_cap = 0;
   void* Wstep = nullptr;     // per-step layout of the recurrent weights
   float* P = nullptr;
   size_t P_cap = 0;
@@ -282,8 +287,37 @@ cudaError_t ensure_x16(prnn_handle* h, size_t n) {
   return cudaSuccess;
 }
 
+// IEEE binary16 bits -> float (exact), and float -> bfloat16 bits rounded to
+// nearest even (finite inputs).
+float half_bits_to_float(uint16_t h) {
+  const uint32_t sign = (uint32_t)(h >> 15) << 31;
+  const int exp = (h >> 10) & 0x1f;
+  const uint32_t man = h & 0x3ff;
+  float v;
+  if (exp == 0) {
+    v = (float)man * (1.0f / 16777216.0f);  // subnormal: man * 2^-24
+  } else if (exp == 31) {
+    v = man ? __builtin_nanf("") : __builtin_inff();
+  } else {
+    uint32_t bits = ((uint32_t)(exp - 15 + 127) << 23) | (man << 13);
+    std::memcpy(&v, &bits, 4);
+  }
+  uint32_t b;
+  std::memcpy(&b, &v, 4);
+  b |= sign;
+  std::memcpy(&v, &b, 4);
+  return v;
+}
+uint16_t float_to_bf16_bits(float f) {
+  uint32_t b;
+  std::memcpy(&b, &f, 4);
+  b += 0x7fffu + ((b >> 16) & 1u);
+  return (uint16_t)(b >> 16);
+}
+
 // Wx in the handle's dtype ([H][I]) plus, for fp16, a [H][Kp] zero-padded
-// copy for the tensor-core projection.  Host vectors in, device buffers out.
+// copy for the tensor-core projection and Wx^T in bf16 [I][Hp] for the
+// tensor-core input gradient.  Host vectors in, device buffers out.
 prnn_status_t stage_wx_bias(prnn_handle* h, const void* Wx, const float* bias,
                             void** dWx, __half_raw** dWx16, float** dbias) {
   const size_t esz = h->wdtype == PRNN_F16 ? 2 : 4;
@@ -299,6 +333,12 @@ prnn_status_t stage_wx_bias(prnn_handle* h, const void* Wx, const float* bias,
     for (int r = 0; r < h->H; ++r)
       std::memcpy(&w16[(size_t)r * h->Kp], src + (size_t)r * h->I, (size_t)h->I * 2);
     PRNN_TRY(upload(dWx16, w16.data(), w16.size() * 2));
+    const int Hp = round_up(h->H, 64);
+    std::vector<uint16_t> wt((size_t)h->I * Hp, 0);
+    for (int r = 0; r < h->H; ++r)
+      for (int c = 0; c < h->I; ++c)
+        wt[(size_t)c * Hp + r] = float_to_bf16_bits(half_bits_to_float(src[(size_t)r * h->I + c]));
+    PRNN_TRY(upload(&h->WxT16, wt.data(), wt.size() * 2));
   }
   return PRNN_OK;
 }
@@ -315,6 +355,7 @@ void free_weights(prnn_handle* h) {
   free_dev(h->caller_pos);
   free_dev(h->valsT);
   free_dev(h->colsT);
+  free_dev(h->WxT16);
   h->bwd_ok = false;
   free_dev(h->Wstep);
   h->weights_set = false;
@@ -541,6 +582,7 @@ prnn_status_t prnn_destroy(prnn_t h) {
   free_dev(h->P);
   free_dev(h->x16);
   free_dev(h->tws);
+  free_dev(h->gws16);
   free_dev(h->status);
   free_dev(h->bar);
   for (auto& e : h->ev)
@@ -904,7 +946,46 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
   // 2. batched gradients over all T*B rows of delta
   const int K = T * B;
   const bool f16 = h->wdtype == PRNN_F16;
+  // fp16 weights: the three large products on the tensor cores in bf16
+  // (fp32 accumulation); fp32 weights keep full fp32 CUDA-core products
+  const bool tc = f16 && h->tc_proj && h->proj_mode == 0 && h->WxT16;
   if (db) PRNN_TRY(launch_colsum(delta, K, H, db, s));
+  if (tc && (dWx || dx || (dWh && !h->sparse))) {
+    const int Kp = round_up(K, 64), Hp = round_up(H, 64);
+    const size_t n_dT = (size_t)H * Kp, n_hT = (size_t)H * Kp, n_xT = (size_t)I * Kp;
+    const size_t n_d = (size_t)K * Hp;
+    const size_t need = n_dT + n_hT + n_xT + n_d;
+    if (need > h->gws16_cap) {
+      free_dev(h->gws16);
+      h->gws16_cap = 0;
+      PRNN_TRY(cudaMalloc((void**)&h->gws16, need * 2));
+      h->gws16_cap = need;
+    }
+    uint16_t* dT16 = h->gws16;
+    uint16_t* hT16 = dT16 + n_dT;
+    uint16_t* xT16 = hT16 + n_hT;
+    uint16_t* d16 = xT16 + n_xT;
+    if (dWx || (dWh && !h->sparse))
+      PRNN_TRY(launch_transpose_bf16(K, Kp, H, 0, nullptr, delta, H, dT16, s));
+    if (dWh && !h->sparse) {
+      PRNN_TRY(launch_transpose_bf16(K, Kp, H, B, h0, y, H, hT16, s));
+      GemmTcArgs g{H, H, Kp, dT16, hT16, true, dWh};
+      PRNN_TRY(launch_gemm_tc(g, h->status, s));
+    }
+    if (dWx) {
+      PRNN_TRY(launch_transpose_bf16(K, Kp, I, 0, nullptr, x, I, xT16, s));
+      GemmTcArgs g{H, I, Kp, dT16, xT16, true, dWx};
+      PRNN_TRY(launch_gemm_tc(g, h->status, s));
+    }
+    if (dx) {
+      PRNN_TRY(launch_rows_bf16(K, H, Hp, delta, d16, s));
+      GemmTcArgs g{K, I, Hp, d16, h->WxT16, true, dx};
+      PRNN_TRY(launch_gemm_tc(g, h->status, s));
+    }
+    dWx = nullptr;  // done
+    dx = nullptr;
+    if (!h->sparse) dWh = nullptr;
+  }
   if (dWh && !h->sparse) {
     GemmTnArgs g{H, H, K, B, delta, H, h0, y, H, dWh};
     PRNN_TRY(launch_gemm_tn(g, s));

@@ -21,6 +21,7 @@
 // are kept in full fp32, and these GEMMs are a few percent of a training
 // step next to the serial recurrences.
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "prnn_internal.h"
@@ -204,7 +205,59 @@ __global__ void sparse_dh0_kernel(int B, int H, int kT, const uint16_t* valsT,
   dh0[i] = s;
 }
 
+// out[n][k] = bf16(Brow(k)[n]) for k < K, 0 for K <= k < Kp (Brow as in
+// transpose_rows_kernel): the K-major bf16 operands of the tensor-core
+// gradient products.
+__global__ void transpose_bf16_kernel(int K, int Kp, int N, int K0, const float* B0,
+                                      const float* B1, int ldb, __nv_bfloat16* out) {
+  __shared__ float tile[32][33];
+  const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8 threads
+  for (int i = ty; i < 32; i += 8) {
+    const int k = k0 + i, n = n0 + tx;
+    float v = 0.f;
+    if (k < K && n < N) {
+      const float* row = k < K0 ? (B0 ? B0 + (size_t)k * ldb : nullptr)
+                                : B1 + (size_t)(k - K0) * ldb;
+      if (row) v = row[n];
+    }
+    tile[i][tx] = v;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int n = n0 + i, k = k0 + tx;
+    if (n < N && k < Kp) out[(size_t)n * Kp + k] = __float2bfloat16_rn(tile[tx][i]);
+  }
+}
+
+// out[m][k] = bf16(src[m][k]) for k < K, 0 for K <= k < Kp.
+__global__ void rows_bf16_kernel(int M, int K, int Kp, const float* src, __nv_bfloat16* out) {
+  const size_t total = (size_t)M * Kp;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int m = (int)(i / Kp), k = (int)(i % Kp);
+    out[i] = __float2bfloat16_rn(k < K ? src[(size_t)m * K + k] : 0.f);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_transpose_bf16(int K, int Kp, int N, int K0, const float* B0, const float* B1,
+                                  int ldb, void* out, cudaStream_t s) {
+  if (Kp <= 0 || N <= 0) return cudaSuccess;
+  dim3 grid((N + 31) / 32, (Kp + 31) / 32), block(32, 8);
+  transpose_bf16_kernel<<<grid, block, 0, s>>>(K, Kp, N, K0, B0, B1, ldb,
+                                               static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rows_bf16(int M, int K, int Kp, const float* src, void* out, cudaStream_t s) {
+  if (M <= 0 || Kp <= 0) return cudaSuccess;
+  const size_t total = (size_t)M * Kp;
+  const int blocks = (int)((total + 255) / 256 < 8192 ? (total + 255) / 256 : 8192);
+  rows_bf16_kernel<<<blocks, 256, 0, s>>>(M, K, Kp, src, static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_transpose_rows(int K, int N, int K0, const float* B0, const float* B1, int ldb,
                                   float* out, cudaStream_t s) {

@@ -36,6 +36,17 @@ struct ProjTcArgs {
 };
 bool projection_tc_supported();
 cudaError_t launch_projection_tc(const ProjTcArgs& a, int* status, cudaStream_t s);
+// C[M][N] (fp32, row-major) = sum_k A[m][k] * B[n][k] on the tensor cores;
+// A [M][Kp] and B [N][Kp] fp16 or bf16, K-major, Kp a multiple of 64 (zero
+// padded), 16-byte aligned.
+struct GemmTcArgs {
+  int M, N, Kp;
+  const void* A;
+  const void* B;
+  bool bf16;
+  float* C;
+};
+cudaError_t launch_gemm_tc(const GemmTcArgs& g, int* status, cudaStream_t s);
 
 // ---- persistent recurrent kernels --------------------------------------
 // Default pause (ns) before the first poll of a step's input (see
@@ -199,6 +210,9 @@ cudaError_t launch_transpose_rows(int K, int N, int K0, const float* B0, const f
 cudaError_t launch_sddmm(int H, int kp, int K, const float* dT, const float* hT,
                          const uint16_t* cols, const int32_t* caller_pos, float* out,
                          cudaStream_t s);
+cudaError_t launch_transpose_bf16(int K, int Kp, int N, int K0, const float* B0, const float* B1,
+                                  int ldb, void* out, cudaStream_t s);
+cudaError_t launch_rows_bf16(int M, int K, int Kp, const float* src, void* out, cudaStream_t s);
 cudaError_t launch_sparse_dh0(int B, int H, int kT, const uint16_t* valsT, const uint16_t* colsT,
                               const float* delta0, float* dh0, cudaStream_t s);
 

@@ -19,6 +19,10 @@
 //                    + bias, fp32 stores to P (and the sentinel fill of y).
 // Every mbarrier wait is bounded; a timeout sets the status word and the CTA
 // still waits for its issued work, frees its TMEM and returns.
+//
+// The same kernel, without bias and with bf16 operands, computes the weight
+// and input gradients of the backward pass (launch_gemm_tc): C[m][n] =
+// sum_k A[m][k] * B[n][k] with both operands K-major.
 #include <cuda.h>
 
 #include <cstdint>
@@ -106,6 +110,10 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t f16_idesc(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same with A and B in bf16 (format 1 in both operand fields).
+__host__ __device__ constexpr uint32_t bf16_idesc(int M, int N) {
+  return f16_idesc(M, N) | (1u << 7) | (1u << 10);
+}
 
 __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {
@@ -142,10 +150,11 @@ __device__ __forceinline__ void tmem_load_32cols(uint32_t taddr, uint32_t (&r)[3
 
 struct TcKernelArgs {
   int M, N, Kp;
-  const float* bias;
+  const float* bias;     // [N] or nullptr (no bias)
   float* P;
   float* y_fill;
   int* status;
+  uint32_t idesc;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -209,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&full_bar[kb % kStages], (kb / kStages) & 1, deadline + (uint64_t)kWaitNs);
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
-    constexpr uint32_t idesc = f16_idesc(BM, BN);
+    const uint32_t idesc = a.idesc;
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % kStages;
       if (!mbar_wait(&full_bar[s], (kb / kStages) & 1, deadline)) {
@@ -252,7 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 32; c += 4) {
           const int n = nb + c;
           if (vec && n + 3 < a.N) {
-            const float4 bv = __ldg(reinterpret_cast<const float4*>(a.bias + n));
+            const float4 bv = a.bias ? __ldg(reinterpret_cast<const float4*>(a.bias + n))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
             float4 o;
             o.x = __uint_as_float(r[c + 0]) + bv.x;
             o.y = __uint_as_float(r[c + 1]) + bv.y;
@@ -267,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               if (n + q < a.N) {
-                prow[n + q] = __uint_as_float(r[c + q]) + __ldg(a.bias + n + q);
+                prow[n + q] = __uint_as_float(r[c + q]) + (a.bias ? __ldg(a.bias + n + q) : 0.f);
                 if (yrow) yrow[n + q] = __uint_as_float(kSentinel);
               }
             }
@@ -326,16 +336,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D fp16 K-major map: dims {Kp, rows}, box {64, 128}, 128-byte swizzle,
-// out-of-range rows read as zeros.
-bool encode_kmajor(CUtensorMap* map, const void* base, int Kp, int rows, int box_rows) {
+// 2-D fp16 (or bf16) K-major map: dims {Kp, rows}, box {64, 128}, 128-byte
+// swizzle, out-of-range rows read as zeros.
+bool encode_kmajor(CUtensorMap* map, const void* base, int Kp, int rows, int box_rows,
+                   bool bf16 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)Kp * 2};
   const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -368,8 +380,25 @@ cudaError_t launch_projection_tc(const ProjTcArgs& a, int* status, cudaStream_t 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  TcKernelArgs ka{a.M, a.N, a.Kp, a.bias, a.P, a.y_fill, status};
+  TcKernelArgs ka{a.M, a.N, a.Kp, a.bias, a.P, a.y_fill, status, f16_idesc(BM, BN)};
   const dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
+  proj_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, ka);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(const GemmTcArgs& g, int* status, cudaStream_t s) {
+  if (g.M == 0 || g.N == 0) return cudaSuccess;
+  if (g.Kp % BK != 0) return cudaErrorInvalidValue;
+  CUtensorMap tmA, tmB;
+  if (!encode_kmajor(&tmA, g.A, g.Kp, g.M, BM, g.bf16) ||
+      !encode_kmajor(&tmB, g.B, g.Kp, g.N, BN, g.bf16))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  TcKernelArgs ka{g.M, g.N, g.Kp, nullptr, g.C, nullptr, status,
+                  g.bf16 ? bf16_idesc(BM, BN) : f16_idesc(BM, BN)};
+  const dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
   proj_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, ka);
   return cudaGetLastError();
 }
