@@ -168,7 +168,9 @@ prnn_status_t prnn_destroy(prnn_t h);
  * reverse recurrence runs in the same persistent kernel as the forward with
  * Wh^T held on chip (a transposed copy packed at set_weights time); the five
  * gradients are batched products over all T*B rows.  The derivative of ReLU
- * at 0 is taken as 0 (y_t = 0 gives delta_t = 0).
+ * at 0 is taken as 0 (y_t = 0 gives delta_t = 0); internally the mask is
+ * folded into a copy of dy as one NaN bit pattern (0x7fc0beef), so a dy word
+ * holding exactly that pattern reads as masked.
  *
  * Inputs (device, fp32, 16-byte aligned): x [T][B][I] and h0 [B][H] (NULL =
  * zeros) as given to prnn_forward, y [T][B][H] the output prnn_forward

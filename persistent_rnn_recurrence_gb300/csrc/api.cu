@@ -54,7 +54,7 @@ struct prnn_handle {
   int32_t* caller_pos = nullptr;  // [H][k], -1 for padding
   uint16_t* valsT = nullptr;      // [H][kT] fp16 bits
   uint16_t* colsT = nullptr;      // [H][kT]
-  float* tws = nullptr;           // [2][H][T*B]
+  float* tws = nullptr;           // max(2*H*T*B, T*B*H): masked dy, then transposes
   size_t tws_cap = 0;
   // tensor-core gradient products (fp16 handles): Wx^T in bf16 [I][Hp]
   // (Hp = H rounded up to 64), and bf16 staging of delta, h and x
@@ -902,12 +902,21 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
   }
   if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[0], s));
 
-  // 1. reverse recurrence: delta_t = [y_t > 0] (dy_t + Wh^T delta_{t+1})
+  // 1. reverse recurrence: delta_t = [y_t > 0] (dy_t + Wh^T delta_{t+1}),
+  // the mask folded into a copy of dy in the transposed-delta workspace
+  const size_t need_tws = std::max((size_t)2 * H * T * B, ny);
+  if (need_tws > h->tws_cap) {
+    free_dev(h->tws);
+    h->tws_cap = 0;
+    PRNN_TRY(cudaMalloc((void**)&h->tws, need_tws * sizeof(float)));
+    h->tws_cap = need_tws;
+  }
+  PRNN_TRY(launch_fold_mask(dy, y, ny, h->tws, s));
   PRNN_TRY(launch_fill_sentinel(delta, ny, s));
   RecurCommon c = common_args(h, T, B, nullptr, delta);
-  c.P = dy;
+  c.P = h->tws;
   c.reverse = 1;
-  c.mask = y;
+  c.p_masked = 1;
   c.sync_mode = 0;
   if (h->sparse) {  // Wh^T has its own plan (its rows are Wh's columns)
     c.n_cta = h->b_n_cta;
@@ -991,14 +1000,7 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
     PRNN_TRY(launch_gemm_tn(g, s));
   }
   if (dWh && h->sparse) {  // only at the stored entries, in the caller's order
-    const size_t need = (size_t)2 * H * K;
-    if (need > h->tws_cap) {
-      free_dev(h->tws);
-      h->tws_cap = 0;
-      PRNN_TRY(cudaMalloc((void**)&h->tws, need * sizeof(float)));
-      h->tws_cap = need;
-    }
-    float* dT = h->tws;
+    float* dT = h->tws;  // the folded dy is no longer needed: 2*H*K floats
     float* hT = h->tws + (size_t)H * K;
     PRNN_TRY(launch_transpose_rows(K, H, 0, nullptr, delta, H, dT, s));
     PRNN_TRY(launch_transpose_rows(K, H, B, h0, y, H, hT, s));

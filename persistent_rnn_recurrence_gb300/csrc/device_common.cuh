@@ -18,6 +18,12 @@ constexpr uint32_t kSentinel = 0xFFFFFFFFu;
 //   [0] error code (0 = ok, kStatusTimeout), [1] step, [2] CTA, [3] spare.
 constexpr int kStatusTimeout = 6;
 
+// In the backward pass a P word with this bit pattern (a quiet NaN other
+// than the sentinel) marks an output whose forward value was 0: its delta is
+// 0 (the ReLU derivative) whatever the sum.  Folding the mask into P keeps
+// the reverse kernel at one early load per output, like the forward.
+constexpr uint32_t kMaskedMarker = 0x7fc0beefu;
+
 __device__ __forceinline__ bool is_sentinel(float v) {
   return __float_as_uint(v) == kSentinel;
 }

@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "device_common.cuh"
 #include "prnn_internal.h"
 
 namespace prnn {
@@ -240,7 +241,23 @@ __global__ void rows_bf16_kernel(int M, int K, int Kp, const float* src, __nv_bf
   }
 }
 
+// out[i] = y[i] > 0 ? dy[i] : kMaskedMarker: the ReLU mask folded into the
+// reverse recurrence's P (see kMaskedMarker).
+__global__ void fold_mask_kernel(const float* dy, const float* y, size_t n, float* out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    out[i] = y[i] > 0.f ? dy[i] : __uint_as_float(kMaskedMarker);
+}
+
 }  // namespace
+
+cudaError_t launch_fold_mask(const float* dy, const float* y, size_t n, float* out,
+                             cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int blocks = (int)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
+  fold_mask_kernel<<<blocks, 256, 0, s>>>(dy, y, n, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_transpose_bf16(int K, int Kp, int N, int K0, const float* B0, const float* B1,
                                   int ldb, void* out, cudaStream_t s) {

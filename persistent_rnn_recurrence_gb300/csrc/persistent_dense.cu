@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
     for (int b0 = pl.b_lo; b0 < pl.b_hi; b0 += BW, ++seq) {
       const int nb = min(BW, pl.b_hi - b0);
       // P for the output this thread finalizes (index tid = r*BW + b)
-      float pv = 0.f, mv = 1.f;
+      float pv = 0.f;
       int orow = -1, ob = -1;
       if (tid < V) {
         const int r = tid / BW, bb = tid % BW;
@@ -100,7 +100,6 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
           orow = pl.row0 + r;
           ob = b0 + bb;
           pv = ld_nc_pinned(Pt + (size_t)ob * H + orow);
-          if (c.mask) mv = ld_nc_pinned(c.mask + ((size_t)tt * B + ob) * H + orow);
         }
       }
       // issue every load of h_{t-1} this thread needs (batch columns past nb
@@ -207,7 +206,8 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
         float s = pv;
         for (int ww = 0; ww < nwarps; ++ww) s += rb[ww * V + tid];
         if (!(cta == c.drop_cta && t == c.drop_step))
-          st_relaxed_f(yt + (size_t)ob * H + orow, c.mask ? (mv > 0.f ? s : 0.f) : relu(s));
+          st_relaxed_f(yt + (size_t)ob * H + orow,
+                       c.p_masked ? (__float_as_uint(pv) == kMaskedMarker ? 0.f : s) : relu(s));
       }
     }
     if (c.sync_mode == 1) {

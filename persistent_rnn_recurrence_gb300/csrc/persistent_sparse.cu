@@ -95,17 +95,15 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
       const int nbg = min(BG, pl.b_hi - bs);
       const int hs_off = hs_base + ((nbuf == 2) ? (seq & 1) : 0) * H * BG;
       // P for this lane's outputs, fetched before the wait
-      float pv[NOUT], mv[NOUT];
+      float pv[NOUT];
       bool owns = false;
 #pragma unroll
       for (int i = 0; i < NOUT; ++i) {
         pv[i] = 0.f;
-        mv[i] = 1.f;
         const int idx = (BG >= TPR) ? gl * NOUT + i : gl / REP;
         const bool mine = (gl % REP) == 0;
         if (has_row && mine && idx < nbg) {
           pv[i] = ld_nc_pinned(Pt + (size_t)(bs + idx) * H + row);
-          if (c.mask) mv[i] = ld_nc_pinned(c.mask + ((size_t)tt * B + bs + idx) * H + row);
           owns = true;
         }
       }
@@ -158,7 +156,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
           if (idx < nbg) {
             const float s = acc[i] + pv[i];
             st_relaxed_f(yt + (size_t)(bs + idx) * H + row,
-                         c.mask ? (mv[i] > 0.f ? s : 0.f) : relu(s));
+                         c.p_masked ? (__float_as_uint(pv[i]) == kMaskedMarker ? 0.f : s)
+                                    : relu(s));
           }
         }
       }

@@ -67,10 +67,10 @@ struct RecurCommon {
   const float* h0;       // [B][H] or nullptr
   float* y;              // [T][B][H], pre-filled with the sentinel
   // Reverse mode (the backward pass): steps run t = T-1 .. 0, h_prev is
-  // y[t+1], and the output is P + sum masked by mask[t] > 0 instead of ReLU
-  // (P = dy, W = Wh^T, y = delta, mask = the forward output).
+  // y[t+1] (P = the masked dy, W = Wh^T, y = delta).  With p_masked the
+  // output is P + sum, or 0 where P holds kMaskedMarker, instead of ReLU.
   int reverse;
-  const float* mask;     // [T][B][H] or nullptr
+  int p_masked;
   int* status;           // int[4]
   long long timeout_ns;
   int poll_delay;        // SM cycles between publishing a step and the first poll of the next
@@ -210,6 +210,8 @@ cudaError_t launch_transpose_rows(int K, int N, int K0, const float* B0, const f
 cudaError_t launch_sddmm(int H, int kp, int K, const float* dT, const float* hT,
                          const uint16_t* cols, const int32_t* caller_pos, float* out,
                          cudaStream_t s);
+cudaError_t launch_fold_mask(const float* dy, const float* y, size_t n, float* out,
+                             cudaStream_t s);
 cudaError_t launch_transpose_bf16(int K, int Kp, int N, int K0, const float* B0, const float* B1,
                                   int ldb, void* out, cudaStream_t s);
 cudaError_t launch_rows_bf16(int M, int K, int Kp, const float* src, void* out, cudaStream_t s);
