@@ -58,6 +58,9 @@ def parse_args(argv=None):
     ap.add_argument("--stack", action="store_true",
                     help="stacked layers: one-launch wavefront vs layer by layer, "
                          "H = 256 / 512 / 1152, L = 1 .. 8")
+    ap.add_argument("--vendor", action="store_true",
+                    help="persistent kernels vs per-step cuBLAS / cuSPARSE products (one JSON "
+                         "line per workload)")
     ap.add_argument("--backward", action="store_true",
                     help="training step (forward + backward through time) of the named workloads")
     return ap.parse_args(argv)
@@ -760,6 +763,125 @@ def run_backward(args):
     return 0
 
 
+def run_vendor(args):
+    """The pages' comparison points, restated on GB300: the persistent
+    kernels against per-step vendor-library products (cuBLAS dense GEMM via
+    torch.addmm, cuSPARSE CSR SpMM via torch.sparse.mm), each step
+    h_t = ReLU(P_t + Wh h_{t-1}) with P precomputed, T steps captured in one
+    CUDA graph where the library allows it.  The libraries run as shipped;
+    nothing of theirs is inspected."""
+    import numpy as np
+    import torch
+    from persistent_rnn_recurrence_gb300 import prnn, synth
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    reps = max(5, min(args.steps, 10))
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return sorted(ms)[len(ms) // 2]
+
+    def per_step(T, P, h0, step):
+        """T steps of `step` (h_prev -> h) into static buffers, as a CUDA graph
+        when capture succeeds; returns (callable, captured)."""
+        hs = [h0] + [torch.empty_like(h0) for _ in range(T)]
+
+        def run():
+            for t in range(T):
+                step(hs[t], P[t], hs[t + 1])
+        run()
+        torch.cuda.synchronize()
+        try:
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                run()
+            torch.cuda.current_stream().wait_stream(s)
+            with torch.cuda.graph(g):
+                run()
+            return g.replay, True
+        except Exception:
+            return run, False
+
+    cases = [("dense_f16_h1152_b4_t256", None), ("sparse_f16_h1792_d10_b4_t256", None)]
+    extra = [(1152, 0.10), (1792, 0.01), (2304, 0.10), (5760, 0.01), (5760, 0.05)]
+    out = []
+    problems = [synth.named_problem(n) for n, _ in cases]
+    problems += [synth.make_problem(H=H, B=4, T=256, k=synth.sparse_k(H, d), seed=3300 + i,
+                                    name=f"sparse_f16_h{H}_d{int(round(d * 100))}_b4_t256")
+                 for i, (H, d) in enumerate(extra)]
+    for p in problems:
+        rec = {"workload": p.name}
+        lay = prnn.Layer.from_problem(p)
+        lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+        x = torch.from_numpy(p.x).to(dev)
+        h0 = torch.zeros(p.B, p.H, device=dev) if p.h0 is None else torch.from_numpy(p.h0).to(dev)
+        y = torch.empty(p.T, p.B, p.H, device=dev)
+        rec_ms = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            prnn.prnn_forward(lay.h, p.T, p.B, x, h0, y)
+            rec_ms.append(prnn.prnn_get_timing(lay.h)[1])
+        lay.close()
+        rec["persistent_us_per_step"] = 1e3 * sorted(rec_ms)[len(rec_ms) // 2] / p.T
+        # the same P for the vendor loops
+        Wx = torch.from_numpy(p.Wx.astype(np.float32)).to(dev)
+        P = (x.reshape(-1, p.I) @ Wx.T + torch.from_numpy(p.b).to(dev)).reshape(p.T, p.B, p.H)
+        if p.sparse:
+            Wd = np.zeros((p.H, p.H), np.float32)
+            Wd[np.repeat(np.arange(p.H), p.k), p.cols.astype(np.int64).ravel()] = \
+                p.vals.astype(np.float32).ravel()
+        else:
+            Wd = p.Wh.astype(np.float32)
+        WdT = torch.from_numpy(Wd).to(dev).T.contiguous()
+        WdT16 = WdT.half()
+        P16 = P.half()
+
+        def dense32(hp, Pt, hn):
+            torch.addmm(Pt, hp, WdT, out=hn)
+            hn.relu_()
+
+        def dense16(hp, Pt, hn):
+            torch.addmm(Pt, hp, WdT16, out=hn)
+            hn.relu_()
+        for key, fn, Pv, hv in (("cublas_sgemm", dense32, P, h0),
+                                ("cublas_hgemm", dense16, P16, h0.half())):
+            f, cap = per_step(p.T, Pv, hv, fn)
+            rec[key + "_us_per_step"] = 1e3 * timed(f) / p.T
+            rec[key + "_graph"] = cap
+        if p.sparse:
+            Wcsr = torch.from_numpy(Wd).to(dev).to_sparse_csr()
+
+            def sparse32(hp, Pt, hn):
+                hn.copy_(torch.sparse.mm(Wcsr, hp.T).T)
+                hn.add_(Pt).relu_()
+            try:
+                f, cap = per_step(p.T, P, h0, sparse32)
+                rec["cusparse_spmm_us_per_step"] = 1e3 * timed(f) / p.T
+                rec["cusparse_spmm_graph"] = cap
+            except Exception as e:  # library path unavailable in this build
+                rec["cusparse_spmm_error"] = str(e)[:120]
+        best_dense = min(rec["cublas_sgemm_us_per_step"], rec["cublas_hgemm_us_per_step"])
+        rec["persistent_vs_dense_gemm"] = best_dense / rec["persistent_us_per_step"]
+        if "cusparse_spmm_us_per_step" in rec:
+            rec["persistent_vs_sparse_gemm"] = (rec["cusparse_spmm_us_per_step"]
+                                                / rec["persistent_us_per_step"])
+        out.append(rec)
+        print(json.dumps(rec), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -774,6 +896,8 @@ def main(argv=None):
         return run_stack(args)
     if args.backward:
         return run_backward(args)
+    if args.vendor:
+        return run_vendor(args)
     return run_ours(args)
 
 
