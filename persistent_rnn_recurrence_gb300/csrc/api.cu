@@ -54,7 +54,7 @@ struct prnn_handle {
   int32_t* caller_pos = nullptr;  // [H][k], -1 for padding
   uint16_t* valsT = nullptr;      // [H][kT] fp16 bits
   uint16_t* colsT = nullptr;      // [H][kT]
-  float* tws = nullptr;           // max(2*H*T*B, T*B*H): masked dy, then transposes
+  float* tws = nullptr;           // masked dy, then transposes or a dense dWh
   size_t tws_cap = 0;
   // tensor-core gradient products (fp16 handles): Wx^T in bf16 [I][Hp]
   // (Hp = H rounded up to 64), and bf16 staging of delta, h and x
@@ -904,7 +904,12 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
 
   // 1. reverse recurrence: delta_t = [y_t > 0] (dy_t + Wh^T delta_{t+1}),
   // the mask folded into a copy of dy in the transposed-delta workspace
-  const size_t need_tws = std::max((size_t)2 * H * T * B, ny);
+  // (sized once here for every later use: the masked dy, the transposed
+  // delta and h of the fp32 value gradients, the dense product of the
+  // tensor-core value gradients)
+  const bool tc_vals = h->sparse && h->wdtype == PRNN_F16 && h->tc_proj && h->proj_mode == 0 &&
+                       h->WxT16;
+  const size_t need_tws = std::max({(size_t)2 * H * T * B, ny, tc_vals ? (size_t)H * H : 0});
   if (need_tws > h->tws_cap) {
     free_dev(h->tws);
     h->tws_cap = 0;
@@ -959,7 +964,7 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
   // (fp32 accumulation); fp32 weights keep full fp32 CUDA-core products
   const bool tc = f16 && h->tc_proj && h->proj_mode == 0 && h->WxT16;
   if (db) PRNN_TRY(launch_colsum(delta, K, H, db, s));
-  if (tc && (dWx || dx || (dWh && !h->sparse))) {
+  if (tc && (dWx || dx || dWh)) {
     const int Kp = round_up(K, 64), Hp = round_up(H, 64);
     const size_t n_dT = (size_t)H * Kp, n_hT = (size_t)H * Kp, n_xT = (size_t)I * Kp;
     const size_t n_d = (size_t)K * Hp;
@@ -974,12 +979,15 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
     uint16_t* hT16 = dT16 + n_dT;
     uint16_t* xT16 = hT16 + n_hT;
     uint16_t* d16 = xT16 + n_xT;
-    if (dWx || (dWh && !h->sparse))
-      PRNN_TRY(launch_transpose_bf16(K, Kp, H, 0, nullptr, delta, H, dT16, s));
-    if (dWh && !h->sparse) {
+    if (dWx || dWh) PRNN_TRY(launch_transpose_bf16(K, Kp, H, 0, nullptr, delta, H, dT16, s));
+    if (dWh) {
       PRNN_TRY(launch_transpose_bf16(K, Kp, H, B, h0, y, H, hT16, s));
-      GemmTcArgs g{H, H, Kp, dT16, hT16, true, dWh};
+      float* dense = dWh;
+      if (h->sparse) dense = h->tws;  // the dense product, then the stored entries
+      GemmTcArgs g{H, H, Kp, dT16, hT16, true, dense};
       PRNN_TRY(launch_gemm_tc(g, h->status, s));
+      if (h->sparse)
+        PRNN_TRY(launch_gather_pattern(H, h->k, dense, h->cols_pad, h->caller_pos, dWh, s));
     }
     if (dWx) {
       PRNN_TRY(launch_transpose_bf16(K, Kp, I, 0, nullptr, x, I, xT16, s));
@@ -993,7 +1001,7 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
     }
     dWx = nullptr;  // done
     dx = nullptr;
-    if (!h->sparse) dWh = nullptr;
+    dWh = nullptr;
   }
   if (dWh && !h->sparse) {
     GemmTnArgs g{H, H, K, B, delta, H, h0, y, H, dWh};

@@ -8,10 +8,11 @@
 //   dWx = delta^T x                                  (gemm_tn_kernel)
 //   dx  = delta Wx,  dh0 = delta_0 Wh                (gemm_nn_kernel)
 // For sparse Wh the weight gradient is needed only at the stored entries:
-//   dvals[r][j] = sum_k delta[k][r] * Hprev[k][cols[r][j]]     (sddmm_kernel)
-// computed as dot products of rows of the transposed delta and Hprev (each
-// a contiguous T*B vector), and dh0 = Wh^T delta_0 walks the rows of the
-// padded Wh^T (sparse_dh0_kernel).
+//   dvals[r][j] = sum_k delta[k][r] * Hprev[k][cols[r][j]]
+// in fp32 as dot products of rows of the transposed delta and Hprev (each a
+// contiguous T*B vector; sddmm_kernel), or for fp16 layers as the dense
+// product on the tensor cores picked at the pattern (gather_pattern_kernel);
+// dh0 = Wh^T delta_0 walks the rows of the padded Wh^T (sparse_dh0_kernel).
 // They are the products the chain rule gives for the layer's two matrix
 // products; like the forward projection they carry no dependence between
 // steps and run as whole-sequence GEMMs ("Optimizing Performance of
@@ -249,7 +250,28 @@ __global__ void fold_mask_kernel(const float* dy, const float* y, size_t n, floa
     out[i] = y[i] > 0.f ? dy[i] : __uint_as_float(kMaskedMarker);
 }
 
+// out[caller_pos[r][j]] = dense[r][cols[r][j]] for the stored entries: the
+// sparse value gradients picked out of a dense dWh.
+__global__ void gather_pattern_kernel(int H, int kp, const float* dense, const uint16_t* cols,
+                                      const int32_t* caller_pos, float* out) {
+  const size_t n = (size_t)H * kp;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int pos = caller_pos[i];
+    if (pos >= 0) out[pos] = dense[(i / kp) * H + cols[i]];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_pattern(int H, int kp, const float* dense, const uint16_t* cols,
+                                  const int32_t* caller_pos, float* out, cudaStream_t s) {
+  const size_t n = (size_t)H * kp;
+  if (n == 0) return cudaSuccess;
+  const int blocks = (int)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
+  gather_pattern_kernel<<<blocks, 256, 0, s>>>(H, kp, dense, cols, caller_pos, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fold_mask(const float* dy, const float* y, size_t n, float* out,
                              cudaStream_t s) {

@@ -210,6 +210,8 @@ cudaError_t launch_transpose_rows(int K, int N, int K0, const float* B0, const f
 cudaError_t launch_sddmm(int H, int kp, int K, const float* dT, const float* hT,
                          const uint16_t* cols, const int32_t* caller_pos, float* out,
                          cudaStream_t s);
+cudaError_t launch_gather_pattern(int H, int kp, const float* dense, const uint16_t* cols,
+                                  const int32_t* caller_pos, float* out, cudaStream_t s);
 cudaError_t launch_fold_mask(const float* dy, const float* y, size_t n, float* out,
                              cudaStream_t s);
 cudaError_t launch_transpose_bf16(int K, int Kp, int N, int K0, const float* B0, const float* B1,
