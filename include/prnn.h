@@ -72,9 +72,12 @@ typedef enum {
   PRNN_OPT_WIDE_LOADS = 7,        /* sparse: 1 = stage h with 128-bit loads (default); 0 = 32-bit */
   PRNN_OPT_BANK_AWARE = 8,        /* sparse: 1 = bank-aware entry placement (default); 0 = plain,
                                      takes effect at the next set_weights call                 */
-  PRNN_OPT_POLL_DELAY_NS = 9      /* persistent: pause after publishing a step before the first
+  PRNN_OPT_POLL_DELAY_NS = 9,     /* persistent: pause after publishing a step before the first
                                      poll of the next, ns, 0 .. 10000 (default: 100 for the
                                      dense and stacked kernels, 0 for the sparse kernels)       */
+  PRNN_OPT_POLL_BACKOFF_NS = 10   /* persistent: pause before re-polling stale step data, ns,
+                                     doubling per round up to 4x; 0 .. 10000 (default: 0, and
+                                     250 for stacks)                                            */
 } prnn_option_t;
 
 /* Plan and sizes chosen at create / set_weights time (read-only report). */
@@ -332,7 +335,8 @@ prnn_status_t prnn_stack_forward(prnn_stack_t s, int T, int B, const float* x, c
 prnn_status_t prnn_stack_get_status(prnn_stack_t s, void* stream);
 
 /*
- * Options: PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_POLL_DELAY_NS, PRNN_OPT_TIMING (events around the last
+ * Options: PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_POLL_DELAY_NS, PRNN_OPT_POLL_BACKOFF_NS,
+ * PRNN_OPT_TIMING (events around the last
  * forward, read with prnn_stack_get_timing), PRNN_OPT_DEBUG_DROP_CTA /
  * PRNN_OPT_DEBUG_DROP_STEP (the CTA index counts over all slices; wavefront
  * only), PRNN_OPT_CTA_GROUPS (wavefront: force the batch groups per slice;

@@ -71,6 +71,7 @@ struct prnn_handle {
   // options
   long long timeout_us = 500000;
   int poll_delay_ns = -1, clock_khz = 0;  // -1: the kernel family's default
+  int backoff_ns = kBackoffNs;
   int sync_mode = 0, drop_cta = -1, drop_step = -1, timing = 0, proj_mode = 0;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   bool ev_valid = false;
@@ -379,6 +380,7 @@ RecurCommon common_args(const prnn_handle* h, int T, int B, const float* h0, flo
   const int delay_ns = h->poll_delay_ns >= 0 ? h->poll_delay_ns
                                             : (h->sparse ? kSparseDelayNs : kDenseDelayNs);
   c.poll_delay = (int)((long long)delay_ns * h->clock_khz / 1000000LL);
+  c.poll_backoff = (int)((long long)h->backoff_ns * h->clock_khz / 1000000LL);
   c.sync_mode = h->sync_mode;
   c.bar = h->bar;
   c.drop_cta = h->drop_cta;
@@ -1087,6 +1089,10 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
     case PRNN_OPT_POLL_DELAY_NS:
       if (value < 0 || value > 10000) return PRNN_ERR_INVALID_ARG;
       h->poll_delay_ns = (int)value;
+      return PRNN_OK;
+    case PRNN_OPT_POLL_BACKOFF_NS:
+      if (value < 0 || value > 10000) return PRNN_ERR_INVALID_ARG;
+      h->backoff_ns = (int)value;
       return PRNN_OK;
   }
   return PRNN_ERR_INVALID_ARG;

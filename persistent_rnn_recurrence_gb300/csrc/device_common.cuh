@@ -99,7 +99,16 @@ struct Waiter {
   uint64_t deadline;
   long long timeout_ns;
   const int* status;
+  int backoff;  // SM cycles before re-polling stale data (0: none); x2 per round up to x4
   __device__ __forceinline__ void new_step() { deadline = 0; }
+  // Pause (a clock64 busy-wait, no memory traffic) before re-issuing stale
+  // polls.  Without it, many CTAs re-polling the lines a producer is about to
+  // write can delay that write at the L2 long enough to need more rounds,
+  // and the exchange settles into a state several times slower.
+  __device__ __forceinline__ void pause(uint32_t& round) {
+    if (backoff > 0) spin_cycles(backoff << (round < 2u ? round : 2u));
+    ++round;
+  }
   // true = keep waiting; false = give up (deadline passed or another CTA failed)
   __device__ __forceinline__ bool still_ok(uint32_t& spins) {
     if ((++spins & 63u) != 1u) return true;

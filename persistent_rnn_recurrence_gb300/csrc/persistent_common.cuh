@@ -112,7 +112,7 @@ __device__ __forceinline__ bool stage_rows(const float* hprev, bool poll, int H,
         v[u] = poll ? ld_relaxed_f4(reinterpret_cast<const float*>(src + i)) : __ldg(src + i);
     }
     if (poll) {
-      uint32_t spins = 0;
+      uint32_t spins = 0, round = 0;
       for (;;) {
         unsigned stale = 0;
 #pragma unroll
@@ -120,6 +120,7 @@ __device__ __forceinline__ bool stage_rows(const float* hprev, bool poll, int H,
           if (base + u * NT < nf4 && !ready4(v[u])) stale |= 1u << u;
         if (stale == 0u) break;
         if (!w.still_ok(spins)) return false;
+        w.pause(round);
 #pragma unroll
         for (int u = 0; u < UMAX; ++u)
           if ((stale >> u) & 1u) v[u] = ld_relaxed_f4(reinterpret_cast<const float*>(src + base + u * NT));
@@ -150,7 +151,7 @@ __device__ __forceinline__ bool stage_rows_narrow(const float* hprev, bool poll,
       if (i < n && hprev != nullptr) v[u] = poll ? ld_relaxed_f(src + i) : __ldg(src + i);
     }
     if (poll) {
-      uint32_t spins = 0;
+      uint32_t spins = 0, round = 0;
       for (;;) {
         unsigned stale = 0;
 #pragma unroll
@@ -158,6 +159,7 @@ __device__ __forceinline__ bool stage_rows_narrow(const float* hprev, bool poll,
           if (base + u * NT < n && is_sentinel(v[u])) stale |= 1u << u;
         if (stale == 0u) break;
         if (!w.still_ok(spins)) return false;
+        w.pause(round);
 #pragma unroll
         for (int u = 0; u < UMAX; ++u)
           if ((stale >> u) & 1u) v[u] = ld_relaxed_f(src + base + u * NT);

@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
   Waiter w;
   w.status = c.status;
   w.timeout_ns = c.timeout_ns;
+  w.backoff = c.poll_backoff;
   int seq = 0;
   for (int t = 0; t < c.T; ++t) {
     const int tt = c.reverse ? c.T - 1 - t : t;  // time index of this step
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
       // wait until every loaded chunk is fresh, re-issuing all stale loads each round
       bool ok = true;
       if (t > 0) {
-        uint32_t spins = 0;
+        uint32_t spins = 0, round = 0;
         for (;;) {
           unsigned stale = 0;
 #pragma unroll
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
             ok = false;
             break;
           }
+          w.pause(round);
 #pragma unroll
           for (int j = 0; j < CPT; ++j)
 #pragma unroll

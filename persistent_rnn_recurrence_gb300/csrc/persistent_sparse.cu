@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
   Waiter w;
   w.status = c.status;
   w.timeout_ns = c.timeout_ns;
+  w.backoff = c.poll_backoff;
   int seq = 0;
   for (int t = 0; t < c.T; ++t) {
     const int tt = c.reverse ? c.T - 1 - t : t;  // time index of this step
@@ -186,6 +187,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sync_probe_kernel(const Rec
   Waiter w;
   w.status = c.status;
   w.timeout_ns = c.timeout_ns;
+  w.backoff = c.poll_backoff;
   for (int t = 0; t < c.T; ++t) {
     const float* hprev = (t == 0) ? nullptr : c.y + (size_t)(t - 1) * B * H;
     float* yt = c.y + (size_t)t * B * H;

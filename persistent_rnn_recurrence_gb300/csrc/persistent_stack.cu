@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
   Waiter w;
   w.status = c.status;
   w.timeout_ns = c.timeout_ns;
+  w.backoff = c.poll_backoff;
   int seq = 0;
   for (int t = 0; t < c.T; ++t) {
     const float* xt = L.xin + (size_t)t * B * I;
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
       }
       bool ok = true;
       if (pollmask != 0u) {
-        uint32_t spins = 0;
+        uint32_t spins = 0, round = 0;
         for (;;) {
           unsigned stale = 0;
 #pragma unroll
@@ -148,6 +149,7 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
             ok = false;
             break;
           }
+          w.pause(round);
 #pragma unroll
           for (int j = 0; j < CPT; ++j)
 #pragma unroll

@@ -57,6 +57,12 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int* status, cudaStream_t s);
 // fastest without it.
 constexpr int kDenseDelayNs = 100;
 constexpr int kSparseDelayNs = 0;
+// Default first pause (ns) before re-polling stale step data (Waiter::pause):
+// none for the single-layer kernels (it only slows them), 250 ns for the
+// stacked kernel, whose slices otherwise fall into the slow exchange state
+// (H=1152, L=2: 11.6 -> 3.6 us/step; H=256, L=4: 4.5 -> 1.4).
+constexpr int kBackoffNs = 0;
+constexpr int kStackBackoffNs = 250;
 struct RecurCommon {
   int T, B, H;
   int n_cta, R;          // CTAs (G * cpg) and rows per CTA (last CTA of a group may own fewer)
@@ -74,6 +80,7 @@ struct RecurCommon {
   int* status;           // int[4]
   long long timeout_ns;
   int poll_delay;        // SM cycles between publishing a step and the first poll of the next
+  int poll_backoff;      // SM cycles before re-polling stale data (doubling, up to 4x)
   int sync_mode;         // 0 flags in data, 1 grid barrier
   unsigned* bar;         // grid barrier counter (sync_mode 1)
   int drop_cta, drop_step;  // fault hook (-1 = off)

@@ -32,6 +32,7 @@ struct prnn_stack {
   int* status = nullptr;       // device int[4]
   long long timeout_us = 500000;
   int poll_delay_ns = kDenseDelayNs, clock_khz = 2000000;
+  int backoff_ns = kStackBackoffNs;
   int drop_cta = -1, drop_step = -1, timing = 0;
   cudaEvent_t ev[2] = {nullptr, nullptr};
   bool ev_valid = false, sticky_timeout = false;
@@ -258,6 +259,7 @@ prnn_status_t prnn_stack_forward(prnn_stack_t s, int T, int B, const float* x, c
     c.status = s->status;
     c.timeout_ns = s->timeout_us * 1000LL;
     c.poll_delay = (int)((long long)s->poll_delay_ns * s->clock_khz / 1000000LL);
+    c.poll_backoff = (int)((long long)s->backoff_ns * s->clock_khz / 1000000LL);
     c.drop_cta = s->drop_cta;
     c.drop_step = s->drop_step;
     a.L = s->L;
@@ -307,6 +309,11 @@ prnn_status_t prnn_stack_set_option(prnn_stack_t s, prnn_option_t opt, long long
     case PRNN_OPT_POLL_DELAY_NS:
       if (value < 0 || value > 10000) return PRNN_ERR_INVALID_ARG;
       s->poll_delay_ns = (int)value;
+      for (prnn_t h : s->layer) prnn_set_option(h, opt, value);
+      return PRNN_OK;
+    case PRNN_OPT_POLL_BACKOFF_NS:
+      if (value < 0 || value > 10000) return PRNN_ERR_INVALID_ARG;
+      s->backoff_ns = (int)value;
       for (prnn_t h : s->layer) prnn_set_option(h, opt, value);
       return PRNN_OK;
     case PRNN_OPT_TIMING:

@@ -27,7 +27,8 @@ PRNN_F32, PRNN_F16 = 0, 1
 PRNN_ALGO_PERSISTENT, PRNN_ALGO_PER_STEP = 0, 1
 PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA, \
     PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION, PRNN_OPT_CTA_GROUPS, \
-    PRNN_OPT_WIDE_LOADS, PRNN_OPT_BANK_AWARE, PRNN_OPT_POLL_DELAY_NS = range(10)
+    PRNN_OPT_WIDE_LOADS, PRNN_OPT_BANK_AWARE, PRNN_OPT_POLL_DELAY_NS, \
+    PRNN_OPT_POLL_BACKOFF_NS = range(11)
 
 PRNN_STACK_WAVEFRONT, PRNN_STACK_LAYERWISE = 0, 1
 
