@@ -75,9 +75,12 @@ typedef enum {
   PRNN_OPT_POLL_DELAY_NS = 9,     /* persistent: pause after publishing a step before the first
                                      poll of the next, ns, 0 .. 10000 (default: 100 for the
                                      dense and stacked kernels, 0 for the sparse kernels)       */
-  PRNN_OPT_POLL_BACKOFF_NS = 10   /* persistent: pause before re-polling stale step data, ns,
+  PRNN_OPT_POLL_BACKOFF_NS = 10,  /* persistent: pause before re-polling stale step data, ns,
                                      doubling per round up to 4x; 0 .. 10000 (default: 0, and
                                      250 for stacks)                                            */
+  PRNN_OPT_RECURRENT_TC = 11      /* dense fp16 persistent: 0 = tcgen05 recurrence when
+                                     max_batch >= 16 (default), 1 = never, 2 = whenever it
+                                     fits; takes effect at the next set_weights call            */
 } prnn_option_t;
 
 /* Plan and sizes chosen at create / set_weights time (read-only report). */
@@ -92,6 +95,7 @@ typedef struct {
   size_t smem_bytes;               /* dynamic shared memory per CTA at max_batch             */
   size_t onchip_weight_bytes;      /* packed Wh bytes held on chip, all CTAs                 */
   size_t nnz;                      /* non-zeros of Wh (H*H when dense)                       */
+  int recurrent_tensor_cores;      /* 1 if the dense recurrence runs on tcgen05 (wide batch) */
 } prnn_info_t;
 
 /*

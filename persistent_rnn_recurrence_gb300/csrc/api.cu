@@ -32,6 +32,11 @@ struct prnn_handle {
   // persistent plan
   int n_cta = 0, R = 0, nthreads = 0, cpt = 0, tpr = 0, kp = 0, ept = 0, pack_cap = 0;
   int G = 1, cpg = 0, groups_opt = 0, dense_bw = 4;
+  // tensor-core dense recurrence (wide batch): its own plan and weight image
+  int rtc_opt = 0;
+  bool rtc = false;
+  int t_n_cta = 0, t_R = 0, t_G = 1, t_cpg = 0, t_N = 0;
+  void* Wimg = nullptr;
   int wide_loads = 1, bank_aware = 1;
   size_t onchip_bytes = 0, smem_at_max = 0;
   bool tc_proj = false;
@@ -136,6 +141,40 @@ DensePlan plan_dense_g(const prnn_handle* h, int G) {
     }
   }
   return p;
+}
+
+// Tensor-core dense plan: G groups (batch columns Bl = ceil(maxB/G) <= 32),
+// R = ceil(H/cpg) <= 32 rows per CTA (N = R rounded up to 16), weights image
+// plus the A ring within shared memory; among the fits, the least estimated
+// step time: exchange ~1.1 us + ~17 ns per KiB of h each CTA pulls + the
+// MMAs (M = 128 rows of A, N, K = H at ~14.8 TFLOP/s per SM).
+struct TcPlan {
+  int G, cpg, R, N, n_cta;
+  size_t smem;
+  bool ok;
+};
+TcPlan plan_dense_tc(const prnn_handle* h) {
+  TcPlan best{};
+  double best_ns = 1e30;
+  if (h->wdtype != PRNN_F16 || h->H % 64 != 0) return best;
+  for (int G = 1; G <= std::min(h->maxB, 8); G *= 2) {
+    const int bl = (h->maxB + G - 1) / G;
+    if (bl > 32) continue;
+    int cpg = h->sm_count / G;
+    if (cpg < 1) continue;
+    const int R = (h->H + cpg - 1) / cpg;
+    cpg = (h->H + R - 1) / R;
+    const int N = round_up(R, 16);
+    if (N > 32) continue;
+    const size_t sm = recur_dense_tc_smem(h->H, N);
+    if (sm > h->smem_optin) continue;
+    const double ns = 1100.0 + 17.0 * bl * h->H * 4 / 1024.0 + 2.0 * 128 * N * h->H / 14800.0;
+    if (ns < best_ns) {
+      best_ns = ns;
+      best = TcPlan{G, cpg, R, N, G * cpg, sm, true};
+    }
+  }
+  return best;
 }
 
 DensePlan plan_dense(const prnn_handle* h) {
@@ -352,6 +391,8 @@ void free_weights(prnn_handle* h) {
   free_dev(h->Wpk);
   free_dev(h->Wpk_T);
   free_dev(h->Wh_nat);
+  free_dev(h->Wimg);
+  h->rtc = false;
   free_dev(h->cols_pad);
   free_dev(h->caller_pos);
   free_dev(h->valsT);
@@ -635,6 +676,33 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
     PRNN_TRY(upload(&h->Wpk, pk.data(), pk.size()));
     PRNN_TRY(upload(&h->Wpk_T, pt.data(), pt.size()));
     PRNN_TRY(upload(&h->Wh_nat, wh.data(), wh.size()));
+    // tensor-core recurrence for wide batches: per CTA, K slice s of 64
+    // columns holds N rows of 128 bytes, 16-byte chunk c of row n at
+    // c ^ (n & 7) (the 128-byte swizzle of the K-major MMA operand)
+    const TcPlan tp = plan_dense_tc(h);
+    const bool want = h->rtc_opt == 2 || (h->rtc_opt == 0 && h->maxB >= 16);
+    if (tp.ok && want) {
+      const int nsl = H / 64;
+      std::vector<uint16_t> img((size_t)tp.cpg * nsl * tp.N * 64, 0);
+      const uint16_t* w16 = reinterpret_cast<const uint16_t*>(wh.data());
+      for (int cta = 0; cta < tp.cpg; ++cta)
+        for (int s = 0; s < nsl; ++s)
+          for (int n = 0; n < tp.R; ++n) {
+            const int row = cta * tp.R + n;
+            if (row >= H) continue;
+            for (int c = 0; c < 8; ++c)
+              for (int e = 0; e < 8; ++e)
+                img[(((size_t)cta * nsl + s) * tp.N + n) * 64 + ((c ^ (n & 7)) * 8) + e] =
+                    w16[(size_t)row * H + s * 64 + c * 8 + e];
+          }
+      PRNN_TRY(upload(&h->Wimg, img.data(), img.size() * 2));
+      h->rtc = true;
+      h->t_n_cta = tp.n_cta;
+      h->t_R = tp.R;
+      h->t_G = tp.G;
+      h->t_cpg = tp.cpg;
+      h->t_N = tp.N;
+    }
     h->n_cta = plan.n_cta;
     h->R = plan.R;
     h->G = plan.G;
@@ -804,6 +872,19 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
       a.dbuf = db ? 1 : 0;
       a.narrow = h->wide_loads ? 0 : 1;
       PRNN_TRY(launch_recur_sparse(a, s));
+    } else if (h->rtc && h->sync_mode == 0) {
+      DenseTcArgs a{};
+      c.n_cta = h->t_n_cta;
+      c.R = h->t_R;
+      c.G = h->t_G;
+      c.cpg = h->t_cpg;
+      c.nthreads = recur_dense_tc_threads();
+      c.smem = recur_dense_tc_smem(h->H, h->t_N);
+      a.c = c;
+      a.Wimg = h->Wimg;
+      a.N = h->t_N;
+      a.nslices = h->H / 64;
+      PRNN_TRY(launch_recur_dense_tc(a, s));
     } else {
       DenseRecurArgs a{};
       const int bw = std::min(recur_dense_bw((B + h->G - 1) / h->G), h->dense_bw);
@@ -1094,6 +1175,10 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
       if (value < 0 || value > 10000) return PRNN_ERR_INVALID_ARG;
       h->backoff_ns = (int)value;
       return PRNN_OK;
+    case PRNN_OPT_RECURRENT_TC:
+      if (value < 0 || value > 2) return PRNN_ERR_INVALID_ARG;
+      h->rtc_opt = (int)value;
+      return PRNN_OK;
   }
   return PRNN_ERR_INVALID_ARG;
 }
@@ -1121,6 +1206,14 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
   info->smem_bytes = h->smem_at_max;
   info->onchip_weight_bytes = h->onchip_bytes;
   info->nnz = h->sparse ? (size_t)h->H * h->k : (size_t)h->H * h->H;
+  info->recurrent_tensor_cores = h->rtc ? 1 : 0;
+  if (h->rtc) {
+    info->n_cta = h->t_n_cta;
+    info->rows_per_cta = h->t_R;
+    info->threads_per_cta = recur_dense_tc_threads();
+    info->cta_groups = h->t_G;
+    info->smem_bytes = recur_dense_tc_smem(h->H, h->t_N);
+  }
   return PRNN_OK;
 }
 

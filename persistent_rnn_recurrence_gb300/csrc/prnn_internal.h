@@ -95,6 +95,19 @@ struct DenseRecurArgs {
   int wfp16;
 };
 cudaError_t launch_recur_dense(const DenseRecurArgs& a, int bw, cudaStream_t s);
+
+// Dense fp16 on the tensor cores (persistent_dense_tc.cu): per CTA an image of
+// its rows of Wh, nslices = H/64 K slices of N rows x 128 bytes (fp16,
+// 128-byte swizzle, rows past R zero), N = R rounded up to 16, N <= 32; the
+// group's batch columns Bl <= 32.
+struct DenseTcArgs {
+  RecurCommon c;
+  const void* Wimg;
+  int N, nslices;
+};
+cudaError_t launch_recur_dense_tc(const DenseTcArgs& a, cudaStream_t s);
+size_t recur_dense_tc_smem(int H, int N);
+int recur_dense_tc_threads();
 size_t recur_dense_smem(int R, int cpt, int nthreads, bool fp16, int bw);
 int recur_dense_rmax(int R);   // 0 if R unsupported
 int recur_dense_bw(int batch_cols);          // batch columns per pass: 1, 2 or 4

@@ -28,7 +28,7 @@ PRNN_ALGO_PERSISTENT, PRNN_ALGO_PER_STEP = 0, 1
 PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA, \
     PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION, PRNN_OPT_CTA_GROUPS, \
     PRNN_OPT_WIDE_LOADS, PRNN_OPT_BANK_AWARE, PRNN_OPT_POLL_DELAY_NS, \
-    PRNN_OPT_POLL_BACKOFF_NS = range(11)
+    PRNN_OPT_POLL_BACKOFF_NS, PRNN_OPT_RECURRENT_TC = range(12)
 
 PRNN_STACK_WAVEFRONT, PRNN_STACK_LAYERWISE = 0, 1
 
@@ -47,7 +47,7 @@ class prnn_info_t(ctypes.Structure):
         "k_padded", "sm_count", "n_cta", "rows_per_cta", "threads_per_cta",
         "threads_per_row", "projection_tensor_cores", "sparse_bank_cap", "cta_groups")] + [
         ("smem_bytes", ctypes.c_size_t), ("onchip_weight_bytes", ctypes.c_size_t),
-        ("nnz", ctypes.c_size_t)]
+        ("nnz", ctypes.c_size_t), ("recurrent_tensor_cores", ctypes.c_int)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

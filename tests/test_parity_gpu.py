@@ -412,3 +412,79 @@ def test_poll_delay_changes_timing_not_results(env, spec):
         lay.set_option(prnn.PRNN_OPT_POLL_DELAY_NS, -1)
     assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
     lay.close()
+
+
+# --- tensor-core dense recurrence (wide batches) --------------------------------------
+@pytest.mark.parametrize("spec,force", [(dict(H=1152, B=16, T=64, wdtype="f16"), None),
+                                        (dict(H=2304, B=32, T=24, wdtype="f16", h0_std=0.2), None),
+                                        (dict(H=640, I=200, B=20, T=12, wdtype="f16"), None),
+                                        (dict(H=1152, B=4, T=32, wdtype="f16"), 2),
+                                        (dict(H=128, B=9, T=7, wdtype="f16", h0_std=1.0), 2)])
+def test_tensor_core_recurrence_matches_oracle(env, spec, force):
+    torch, prnn, o = env
+    p = synth.make_problem(seed=90, **spec)
+    lay = prnn.Layer(p.H, p.I, p.B, "f16", "persistent")
+    try:
+        if force is not None:
+            lay.set_option(prnn.PRNN_OPT_RECURRENT_TC, force)
+        lay.set_problem_weights(p)
+        assert lay.info()["recurrent_tensor_cores"] == 1
+        x = torch.from_numpy(p.x).cuda()
+        h0 = None if p.h0 is None else torch.from_numpy(p.h0).cuda()
+        y = lay.forward(x, h0)
+        assert lay.status() == prnn.PRNN_OK
+    finally:
+        lay.close()
+    check(y.cpu().numpy(), o.forward(p), "f16", f"tc {spec}")
+
+
+def test_tensor_core_recurrence_off_and_fallback(env):
+    torch, prnn, o = env
+    p = synth.make_problem(H=1152, B=16, T=8, wdtype="f16", seed=91)
+    y_tc, info = run_gpu(env, p)
+    assert info["recurrent_tensor_cores"] == 1
+    lay = prnn.Layer(p.H, p.I, p.B, "f16", "persistent")
+    lay.set_option(prnn.PRNN_OPT_RECURRENT_TC, 1)
+    lay.set_problem_weights(p)
+    assert lay.info()["recurrent_tensor_cores"] == 0
+    y_off = lay.forward(torch.from_numpy(p.x).cuda()).cpu().numpy()
+    lay.close()
+    ref = o.forward(p)
+    check(y_off, ref, "f16", "cuda cores")
+    check(y_tc, ref, "f16", "tensor cores")
+    # H not a multiple of 64: CUDA-core kernel whatever the batch
+    q = synth.make_problem(H=300, B=16, T=4, wdtype="f16", seed=92)
+    y, info = run_gpu(env, q)
+    assert info["recurrent_tensor_cores"] == 0
+    check(y, o.forward(q), "f16", "fallback")
+
+
+def test_tensor_core_recurrence_full_size_teacher_forced(env):
+    """H = 2304, B = 32, T = 256 (a sweep point): sampled outputs against one
+    oracle step on the GPU's own previous state."""
+    torch, prnn, o = env
+    p = synth.make_problem(H=2304, B=32, T=256, wdtype="f16", seed=93)
+    y, info = run_gpu(env, p)
+    assert info["recurrent_tensor_cores"] == 1 and np.isfinite(y).all()
+    rng = np.random.default_rng(10)
+    samples = [(int(t), int(b), int(r)) for t, b, r in zip(
+        rng.integers(0, p.T, 200), rng.integers(0, p.B, 200), rng.integers(0, p.H, 200))]
+    got = np.array([y[t, b, r] for t, b, r in samples], dtype=np.float64)
+    want = o.cells(p, samples, lambda t, b: p.x[t, b],
+                   lambda t, b: np.zeros(p.H) if t == 0 else y[t - 1, b])
+    assert np.abs(got - want).max() <= TOL["f16"] * float(np.abs(y).max())
+
+
+def test_tensor_core_recurrence_times_out_cleanly(env):
+    torch, prnn, o = env
+    p = synth.make_problem(H=1152, B=16, T=6, wdtype="f16", seed=94)
+    lay = prnn.Layer.from_problem(p)
+    assert lay.info()["recurrent_tensor_cores"] == 1
+    lay.set_option(prnn.PRNN_OPT_WAIT_TIMEOUT_US, 20000)
+    lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_CTA, 5)
+    lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_STEP, 2)
+    lay.forward(torch.from_numpy(p.x).cuda())
+    assert lay.status() == prnn.PRNN_ERR_TIMEOUT
+    lay.close()
+    y, _ = run_gpu(env, p)
+    check(y, o.forward(p), "f16", "after timeout")
