@@ -79,8 +79,10 @@ typedef enum {
                                      doubling per round up to 4x; 0 .. 10000 (default: 0, and
                                      250 for stacks)                                            */
   PRNN_OPT_RECURRENT_TC = 11      /* dense fp16 persistent: 0 = tcgen05 recurrence when
-                                     max_batch >= 16 (default), 1 = never, 2 = whenever it
-                                     fits; takes effect at the next set_weights call            */
+                                     max_batch >= 16, 1 = never (default: at B <= 32 its chain
+                                     of small dependent MMAs is slower than the CUDA-core
+                                     kernel), 2 = whenever it fits; takes effect at the next
+                                     set_weights call                                           */
 } prnn_option_t;
 
 /* Plan and sizes chosen at create / set_weights time (read-only report). */

@@ -33,9 +33,9 @@ struct prnn_handle {
   int n_cta = 0, R = 0, nthreads = 0, cpt = 0, tpr = 0, kp = 0, ept = 0, pack_cap = 0;
   int G = 1, cpg = 0, groups_opt = 0, dense_bw = 4;
   // tensor-core dense recurrence (wide batch): its own plan and weight image
-  int rtc_opt = 0;
+  int rtc_opt = 1;  // the tensor-core recurrence is opt-in (slower than the CUDA cores so far)
   bool rtc = false;
-  int t_n_cta = 0, t_R = 0, t_G = 1, t_cpg = 0, t_N = 0;
+  int t_n_cta = 0, t_R = 0, t_G = 1, t_cpg = 0, t_N = 0, t_ring = 0;
   void* Wimg = nullptr;
   int wide_loads = 1, bank_aware = 1;
   size_t onchip_bytes = 0, smem_at_max = 0;
@@ -149,7 +149,7 @@ DensePlan plan_dense_g(const prnn_handle* h, int G) {
 // step time: exchange ~1.1 us + ~17 ns per KiB of h each CTA pulls + the
 // MMAs (M = 128 rows of A, N, K = H at ~14.8 TFLOP/s per SM).
 struct TcPlan {
-  int G, cpg, R, N, n_cta;
+  int G, cpg, R, N, n_cta, nring;
   size_t smem;
   bool ok;
 };
@@ -166,12 +166,13 @@ TcPlan plan_dense_tc(const prnn_handle* h) {
     cpg = (h->H + R - 1) / R;
     const int N = round_up(R, 16);
     if (N > 32) continue;
-    const size_t sm = recur_dense_tc_smem(h->H, N);
-    if (sm > h->smem_optin) continue;
+    const int nring = recur_dense_tc_ring(h->H, N, h->smem_optin);
+    if (nring < 2) continue;
+    const size_t sm = recur_dense_tc_smem(h->H, N, nring);
     const double ns = 1100.0 + 17.0 * bl * h->H * 4 / 1024.0 + 2.0 * 128 * N * h->H / 14800.0;
     if (ns < best_ns) {
       best_ns = ns;
-      best = TcPlan{G, cpg, R, N, G * cpg, sm, true};
+      best = TcPlan{G, cpg, R, N, G * cpg, nring, sm, true};
     }
   }
   return best;
@@ -680,7 +681,7 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
     // columns holds N rows of 128 bytes, 16-byte chunk c of row n at
     // c ^ (n & 7) (the 128-byte swizzle of the K-major MMA operand)
     const TcPlan tp = plan_dense_tc(h);
-    const bool want = h->rtc_opt == 2 || (h->rtc_opt == 0 && h->maxB >= 16);
+    const bool want = h->rtc_opt == 2 || (h->rtc_opt == 0 && h->maxB >= 16);  // 1: off
     if (tp.ok && want) {
       const int nsl = H / 64;
       std::vector<uint16_t> img((size_t)tp.cpg * nsl * tp.N * 64, 0);
@@ -702,6 +703,7 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
       h->t_G = tp.G;
       h->t_cpg = tp.cpg;
       h->t_N = tp.N;
+      h->t_ring = tp.nring;
     }
     h->n_cta = plan.n_cta;
     h->R = plan.R;
@@ -879,11 +881,12 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
       c.G = h->t_G;
       c.cpg = h->t_cpg;
       c.nthreads = recur_dense_tc_threads();
-      c.smem = recur_dense_tc_smem(h->H, h->t_N);
+      c.smem = recur_dense_tc_smem(h->H, h->t_N, h->t_ring);
       a.c = c;
       a.Wimg = h->Wimg;
       a.N = h->t_N;
       a.nslices = h->H / 64;
+      a.nring = h->t_ring;
       PRNN_TRY(launch_recur_dense_tc(a, s));
     } else {
       DenseRecurArgs a{};
@@ -1212,7 +1215,7 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
     info->rows_per_cta = h->t_R;
     info->threads_per_cta = recur_dense_tc_threads();
     info->cta_groups = h->t_G;
-    info->smem_bytes = recur_dense_tc_smem(h->H, h->t_N);
+    info->smem_bytes = recur_dense_tc_smem(h->H, h->t_N, h->t_ring);
   }
   return PRNN_OK;
 }

@@ -103,10 +103,11 @@ cudaError_t launch_recur_dense(const DenseRecurArgs& a, int bw, cudaStream_t s);
 struct DenseTcArgs {
   RecurCommon c;
   const void* Wimg;
-  int N, nslices;
+  int N, nslices, nring;  // nring: A slots (2 .. 8)
 };
 cudaError_t launch_recur_dense_tc(const DenseTcArgs& a, cudaStream_t s);
-size_t recur_dense_tc_smem(int H, int N);
+size_t recur_dense_tc_smem(int H, int N, int nring);
+int recur_dense_tc_ring(int H, int N, size_t smem_optin);  // 0: does not fit
 int recur_dense_tc_threads();
 size_t recur_dense_smem(int R, int cpt, int nthreads, bool fp16, int bw);
 int recur_dense_rmax(int R);   // 0 if R unsupported

@@ -26,9 +26,16 @@ def env():
     return torch, prnn, oracle.default()
 
 
-def run_gpu(env, p, algo="persistent", T=None, max_batch=None, options=None):
+def run_gpu(env, p, algo="persistent", T=None, max_batch=None, options=None, pre_options=None):
+    """pre_options are set before the weights (options that act at set_weights)."""
     torch, prnn, _ = env
-    lay = prnn.Layer.from_problem(p, algo=algo, max_batch=max_batch)
+    if pre_options:
+        lay = prnn.Layer(p.H, p.I, max_batch or max(1, p.B), p.wdtype, algo)
+        for k, v in pre_options.items():
+            lay.set_option(k, v)
+        lay.set_problem_weights(p)
+    else:
+        lay = prnn.Layer.from_problem(p, algo=algo, max_batch=max_batch)
     try:
         for k, v in (options or {}).items():
             lay.set_option(k, v)
@@ -415,9 +422,9 @@ def test_poll_delay_changes_timing_not_results(env, spec):
 
 
 # --- tensor-core dense recurrence (wide batches) --------------------------------------
-@pytest.mark.parametrize("spec,force", [(dict(H=1152, B=16, T=64, wdtype="f16"), None),
-                                        (dict(H=2304, B=32, T=24, wdtype="f16", h0_std=0.2), None),
-                                        (dict(H=640, I=200, B=20, T=12, wdtype="f16"), None),
+@pytest.mark.parametrize("spec,force", [(dict(H=1152, B=16, T=64, wdtype="f16"), 0),
+                                        (dict(H=2304, B=32, T=24, wdtype="f16", h0_std=0.2), 0),
+                                        (dict(H=640, I=200, B=20, T=12, wdtype="f16"), 0),
                                         (dict(H=1152, B=4, T=32, wdtype="f16"), 2),
                                         (dict(H=128, B=9, T=7, wdtype="f16", h0_std=1.0), 2)])
 def test_tensor_core_recurrence_matches_oracle(env, spec, force):
@@ -441,20 +448,20 @@ def test_tensor_core_recurrence_matches_oracle(env, spec, force):
 def test_tensor_core_recurrence_off_and_fallback(env):
     torch, prnn, o = env
     p = synth.make_problem(H=1152, B=16, T=8, wdtype="f16", seed=91)
-    y_tc, info = run_gpu(env, p)
-    assert info["recurrent_tensor_cores"] == 1
+    y_tc, info = run_gpu(env, p, options=None)
+    assert info["recurrent_tensor_cores"] == 0  # opt-in
     lay = prnn.Layer(p.H, p.I, p.B, "f16", "persistent")
-    lay.set_option(prnn.PRNN_OPT_RECURRENT_TC, 1)
+    lay.set_option(prnn.PRNN_OPT_RECURRENT_TC, 2)
     lay.set_problem_weights(p)
-    assert lay.info()["recurrent_tensor_cores"] == 0
-    y_off = lay.forward(torch.from_numpy(p.x).cuda()).cpu().numpy()
+    assert lay.info()["recurrent_tensor_cores"] == 1
+    y_on = lay.forward(torch.from_numpy(p.x).cuda()).cpu().numpy()
     lay.close()
     ref = o.forward(p)
-    check(y_off, ref, "f16", "cuda cores")
-    check(y_tc, ref, "f16", "tensor cores")
-    # H not a multiple of 64: CUDA-core kernel whatever the batch
+    check(y_tc, ref, "f16", "cuda cores")
+    check(y_on, ref, "f16", "tensor cores")
+    # H not a multiple of 64: CUDA-core kernel even when asked
     q = synth.make_problem(H=300, B=16, T=4, wdtype="f16", seed=92)
-    y, info = run_gpu(env, q)
+    y, info = run_gpu(env, q, pre_options={prnn.PRNN_OPT_RECURRENT_TC: 2})
     assert info["recurrent_tensor_cores"] == 0
     check(y, o.forward(q), "f16", "fallback")
 
@@ -464,7 +471,7 @@ def test_tensor_core_recurrence_full_size_teacher_forced(env):
     oracle step on the GPU's own previous state."""
     torch, prnn, o = env
     p = synth.make_problem(H=2304, B=32, T=256, wdtype="f16", seed=93)
-    y, info = run_gpu(env, p)
+    y, info = run_gpu(env, p, pre_options={prnn.PRNN_OPT_RECURRENT_TC: 2})
     assert info["recurrent_tensor_cores"] == 1 and np.isfinite(y).all()
     rng = np.random.default_rng(10)
     samples = [(int(t), int(b), int(r)) for t, b, r in zip(
@@ -478,7 +485,9 @@ def test_tensor_core_recurrence_full_size_teacher_forced(env):
 def test_tensor_core_recurrence_times_out_cleanly(env):
     torch, prnn, o = env
     p = synth.make_problem(H=1152, B=16, T=6, wdtype="f16", seed=94)
-    lay = prnn.Layer.from_problem(p)
+    lay = prnn.Layer(p.H, p.I, p.B, "f16", "persistent")
+    lay.set_option(prnn.PRNN_OPT_RECURRENT_TC, 2)
+    lay.set_problem_weights(p)
     assert lay.info()["recurrent_tensor_cores"] == 1
     lay.set_option(prnn.PRNN_OPT_WAIT_TIMEOUT_US, 20000)
     lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_CTA, 5)
