@@ -139,13 +139,24 @@ __global__ void __launch_bounds__(kThreads) gemm_nn_kernel(GemmNnArgs g) {
   }
 }
 
-// out[n] = sum_k A[k][n] for k < K (A row-major [K][N]).
+// out[n] = sum_k A[k][n] for k < K (A row-major [K][N]): a block of 32 x 32
+// threads owns 32 columns; thread (x, y) sums rows y, y + 32, ... of column
+// x (coalesced over x), then the 32 partial sums of a column are added in
+// shared memory in a fixed order.
 __global__ void colsum_kernel(const float* A, int K, int N, float* out) {
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= N) return;
+  __shared__ float part[32][33];
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int n = blockIdx.x * 32 + tx;
   float s = 0.f;
-  for (int k = 0; k < K; ++k) s += A[(size_t)k * N + n];
-  out[n] = s;
+  if (n < N)
+    for (int k = ty; k < K; k += 32) s += A[(size_t)k * N + n];
+  part[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && n < N) {
+    float t = 0.f;
+    for (int i = 0; i < 32; ++i) t += part[i][tx];
+    out[n] = t;
+  }
 }
 
 // out[n][k] = Brow(k)[n] for k < K, n < N (Brow as in gemm_tn: B0 rows for
@@ -337,7 +348,7 @@ cudaError_t launch_gemm_nn(const GemmNnArgs& g, cudaStream_t s) {
 
 cudaError_t launch_colsum(const float* A, int K, int N, float* out, cudaStream_t s) {
   if (N <= 0) return cudaSuccess;
-  colsum_kernel<<<(N + 255) / 256, 256, 0, s>>>(A, K, N, out);
+  colsum_kernel<<<(N + 31) / 32, dim3(32, 32), 0, s>>>(A, K, N, out);
   return cudaGetLastError();
 }
 
