@@ -74,3 +74,57 @@ def test_product_path_fails_loudly_without_library(tmp_path, monkeypatch):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def test_enum_values_match_the_header(lib):
+    """Every PRNN_* enumerator of the header has the same value in the binding."""
+    from persistent_rnn_recurrence_gb300 import prnn
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    pairs = re.findall(r"\b(PRNN_[A-Z0-9_]+)\s*=\s*(\d+)", text)
+    assert len(pairs) >= 25
+    for name, value in pairs:
+        assert getattr(prnn, name) == int(value), name
+
+
+def test_struct_layouts_match_the_header(lib, tmp_path):
+    """Field offsets and sizes of the info structs as the C compiler lays them
+    out from include/prnn.h equal the binding's ctypes mirrors."""
+    import shutil
+    import subprocess
+    from persistent_rnn_recurrence_gb300 import prnn
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "prnn.h"', 'int main(void) {']
+    for cname, cls in (("prnn_info_t", prnn.prnn_info_t), ("prnn_stack_info_t", prnn.prnn_stack_info_t)):
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in cls._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for cname, cls in (("prnn_info_t", prnn.prnn_info_t), ("prnn_stack_info_t", prnn.prnn_stack_info_t)):
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for f, _ in cls._fields_:
+            assert got[(cname, f)] == getattr(cls, f).offset, (cname, f)
+
+
+def test_stack_and_backward_argument_checks_without_gpu(lib):
+    from persistent_rnn_recurrence_gb300 import prnn
+    f = prnn._lib
+    assert f.prnn_stack_create(None, 2, 8, 8, 1, 0, 0) == prnn.PRNN_ERR_INVALID_ARG
+    s = ctypes.c_void_p()
+    assert f.prnn_stack_create(ctypes.byref(s), 0, 8, 8, 1, 0, 0) == prnn.PRNN_ERR_INVALID_ARG
+    assert f.prnn_stack_create(ctypes.byref(s), 9, 8, 8, 1, 0, 0) == prnn.PRNN_ERR_INVALID_ARG
+    assert f.prnn_stack_create(ctypes.byref(s), 2, 6, 8, 1, 0, 0) == prnn.PRNN_ERR_INVALID_ARG
+    assert s.value is None
+    assert f.prnn_stack_destroy(None) == prnn.PRNN_OK
+    assert f.prnn_stack_forward(None, 1, 1, None, None, None, None) == prnn.PRNN_ERR_INVALID_ARG
+    assert f.prnn_backward(None, 1, 1, None, None, None, None, None, None, None, None, None,
+                           None, None) == prnn.PRNN_ERR_INVALID_ARG
+    assert f.prnn_set_weights_csr(None, None, 0, None, None, None, None, None) == \
+        prnn.PRNN_ERR_INVALID_ARG
