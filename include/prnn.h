@@ -74,7 +74,7 @@ typedef enum {
                                      takes effect at the next set_weights call                 */
   PRNN_OPT_POLL_DELAY_NS = 9,     /* persistent: pause after publishing a step before the first
                                      poll of the next, ns, 0 .. 10000 (default: 100 for the
-                                     dense and stacked kernels, 0 for the sparse kernels)       */
+                                     dense and stacked kernels; sparse: 0, or 100 for H > 4096) */
   PRNN_OPT_POLL_BACKOFF_NS = 10,  /* persistent: pause before re-polling stale step data, ns,
                                      doubling per round up to 4x; 0 .. 10000 (default: 0, and
                                      250 for stacks)                                            */

@@ -420,7 +420,7 @@ RecurCommon common_args(const prnn_handle* h, int T, int B, const float* h0, flo
   c.status = h->status;
   c.timeout_ns = h->timeout_us * 1000LL;
   const int delay_ns = h->poll_delay_ns >= 0 ? h->poll_delay_ns
-                                            : (h->sparse ? kSparseDelayNs : kDenseDelayNs);
+                                            : (h->sparse ? sparse_delay_ns(h->H) : kDenseDelayNs);
   c.poll_delay = (int)((long long)delay_ns * h->clock_khz / 1000000LL);
   c.poll_backoff = (int)((long long)h->backoff_ns * h->clock_khz / 1000000LL);
   c.sync_mode = h->sync_mode;
@@ -1015,8 +1015,9 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
     c.G = h->b_G;
     c.cpg = h->b_cpg;
     c.nthreads = h->b_nthreads;
-    c.poll_delay = h->poll_delay_ns >= 0 ? (int)((long long)h->poll_delay_ns * h->clock_khz / 1000000LL)
-                                         : (int)((long long)kSparseDelayNs * h->clock_khz / 1000000LL);
+    c.poll_delay = h->poll_delay_ns >= 0
+                       ? (int)((long long)h->poll_delay_ns * h->clock_khz / 1000000LL)
+                       : (int)((long long)sparse_delay_ns(h->H) * h->clock_khz / 1000000LL);
     SparseRecurArgs a{};
     int bg = 4;
     bool dbuf = false;

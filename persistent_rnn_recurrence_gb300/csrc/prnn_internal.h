@@ -54,9 +54,10 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int* status, cudaStream_t s);
 // (every thread polls its own chunks straight into registers) gain from
 // 50-100 ns and need it on boxes where the exchange otherwise settles into
 // its slow state; the sparse kernels (h staged through shared memory) are
-// fastest without it.
+// fastest without it up to H ~ 2000 (H=1792: 1.58 / 1.63 us/step at 0 / 50
+// ns) and gain 3-8 % from 100 ns at H = 5760.
 constexpr int kDenseDelayNs = 100;
-constexpr int kSparseDelayNs = 0;
+__host__ __device__ constexpr int sparse_delay_ns(int H) { return H > 4096 ? 100 : 0; }
 // Default first pause (ns) before re-polling stale step data (Waiter::pause):
 // none for the single-layer kernels (it only slows them), 250 ns for the
 // stacked kernel, whose slices otherwise fall into the slow exchange state
