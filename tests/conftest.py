@@ -7,5 +7,5 @@ if ROOT not in sys.path:
 
 
 def pytest_configure(config):
-    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs on the GB300 box)")
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103)")
     config.addinivalue_line("markers", "slow: long-running CPU test")
