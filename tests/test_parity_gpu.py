@@ -272,6 +272,12 @@ def test_errors(env):
     prnn.prnn_forward(lay, 3, 0, x, None, y)                   # B = 0: no-op
     assert prnn.prnn_get_status(lay) == prnn.PRNN_OK
     prnn.prnn_destroy(lay)
+    # uint16 column indices: a sparse layer needs H <= 65535
+    wide = prnn.prnn_create(65536, 64, 2, prnn.PRNN_F16, prnn.PRNN_ALGO_PERSISTENT)
+    with pytest.raises(prnn.PrnnError) as e:
+        prnn.prnn_set_weights_sparse(wide, Wx, 8, vals, torch.from_numpy(p.cols.view(np.int16)).cuda(), b)
+    assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    prnn.prnn_destroy(wide)
     # a dense layer too large for the chip is refused, not silently degraded
     big = prnn.prnn_create(8192, 64, 4, prnn.PRNN_F16, prnn.PRNN_ALGO_PERSISTENT)
     Wh = torch.zeros(8192, 8192, dtype=torch.float16, device="cuda")
