@@ -270,18 +270,25 @@ def config_dict(p, args, path):
 
 def cpu_baseline(p) -> dict:
     """The oracle as it stands, single-threaded, on a bounded sample of the
-    same workload (about 10-20 s of CPU work)."""
+    same workload: about 12 s of CPU work. A sequence the oracle finishes in
+    less than that is run again until the time is reached; a longer one is cut
+    to its first timesteps."""
     import oracle
     o = oracle.default()
+    budget = 12.0
     t0 = time.perf_counter()
     o.forward(p, T=2)
     per_t = (time.perf_counter() - t0) / 2
-    Ts = int(max(1, min(p.T, round(12.0 / max(per_t, 1e-6)))))
-    t0 = time.perf_counter()
-    o.forward(p, T=Ts)
-    dt = time.perf_counter() - t0
-    return {"value": Ts / dt, "unit": "timesteps/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {Ts} of {p.T} timesteps, B={p.B}, one run, single thread",
+    Ts = int(max(1, min(p.T, round(budget / max(per_t, 1e-6)))))
+    runs, dt = 0, 0.0
+    while runs == 0 or dt < budget:
+        t0 = time.perf_counter()
+        o.forward(p, T=Ts)
+        dt += time.perf_counter() - t0
+        runs += 1
+    return {"value": runs * Ts / dt, "unit": "timesteps/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {Ts} of {p.T} timesteps, B={p.B}, {runs} run(s) back to back, "
+                      f"single thread",
             "seconds": dt}
 
 
