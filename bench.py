@@ -252,7 +252,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(p, args, "fp64 CPU oracle"),
         "cpu_baseline": {"value": value, "unit": "timesteps/s", "cores": 1,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "host": host_cpu()},
         "e2e": {"value": value, "unit": "timesteps/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -268,28 +268,70 @@ def config_dict(p, args, path):
             "seq_len": p.T, "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
 
-def cpu_baseline(p) -> dict:
-    """The oracle as it stands, single-threaded, on a bounded sample of the
-    same workload: about 12 s of CPU work. A sequence the oracle finishes in
-    less than that is run again until the time is reached; a longer one is cut
-    to its first timesteps."""
+def host_cpu() -> dict:
+    """Core count and CPU model of the host the oracle is timed on."""
+    usable = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith("model name"):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    if model is None:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"cpu_count": os.cpu_count(), "usable_cores": usable, "cpu_model": model}
+
+
+def time_oracle(p, threads: int = 1, budget: float = 12.0) -> dict:
+    """The oracle on a bounded sample of the workload: about ``budget`` seconds
+    of work.  A sequence it finishes in less than that is run again until the
+    time is reached; a longer one is cut to its first timesteps."""
     import oracle
     o = oracle.default()
-    budget = 12.0
     t0 = time.perf_counter()
-    o.forward(p, T=2)
+    o.forward(p, T=2, threads=threads)
     per_t = (time.perf_counter() - t0) / 2
     Ts = int(max(1, min(p.T, round(budget / max(per_t, 1e-6)))))
     runs, dt = 0, 0.0
     while runs == 0 or dt < budget:
         t0 = time.perf_counter()
-        o.forward(p, T=Ts)
+        o.forward(p, T=Ts, threads=threads)
         dt += time.perf_counter() - t0
         runs += 1
-    return {"value": runs * Ts / dt, "unit": "timesteps/s", "cores": 1, "kind": "oracle",
+    how = "single thread" if threads == 1 else f"{threads} threads"
+    return {"value": runs * Ts / dt, "unit": "timesteps/s", "cores": threads, "kind": "oracle",
             "sample": f"first {Ts} of {p.T} timesteps, B={p.B}, {runs} run(s) back to back, "
-                      f"single thread",
+                      f"{how}",
             "seconds": dt}
+
+
+def cpu_baseline(p) -> dict:
+    """The oracle as it stands, single-threaded, about 12 s of CPU work."""
+    out = time_oracle(p, threads=1)
+    out["host"] = host_cpu()
+    return out
+
+
+def cpu_baseline_all_cores(p) -> dict:
+    """The oracle's threaded driver (the same cell arithmetic, each step's
+    outputs split over every usable host core), about 12 s of CPU work."""
+    n = host_cpu()["usable_cores"] or 1
+    out = time_oracle(p, threads=n)
+    out["kind"] = "oracle, threaded driver (bit-identical output)"
+    return out
 
 
 # ---- our arm ----------------------------------------------------------------------------
@@ -405,6 +447,8 @@ def run_ours(args):
     line.update(extras)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
+        if getattr(p, "row_ptr", None) is None:
+            line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(p)
     lay.close()
     if rank == 0:
         print(json.dumps(line))

@@ -39,7 +39,7 @@ def compile_oracle(source: str = SOURCE, out: str = LIB) -> str:
     Floating-point contraction is off so that x86 and Arm hosts give the same
     bits."""
     os.makedirs(os.path.dirname(out), exist_ok=True)
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-pthread",
            "-shared", "-fPIC", "-o", out, source]
     subprocess.run(cmd, check=True)
     return out
@@ -58,10 +58,11 @@ class Oracle:
     mutation tests load deliberately broken copies)."""
 
     def __init__(self, lib_path: str = LIB):
-        if not os.path.exists(lib_path):
-            if lib_path != LIB:
-                raise FileNotFoundError(lib_path)
-            compile_oracle()
+        if lib_path == LIB:
+            if not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SOURCE):
+                compile_oracle()
+        elif not os.path.exists(lib_path):
+            raise FileNotFoundError(lib_path)
         self.lib = ctypes.CDLL(lib_path)
         L = self.lib
         L.oracle_rnn_forward_dense.argtypes = [_l, _l, _l, _l, _D, _D, _D, _D, _D, _D]
@@ -69,6 +70,9 @@ class Oracle:
         L.oracle_rnn_forward_sparse.argtypes = [_l, _l, _l, _l, _l, _D, _D, _D, _L, _D,
                                                 _D, _D]
         L.oracle_rnn_forward_sparse.restype = ctypes.c_int
+        L.oracle_rnn_forward_threads.argtypes = [_l, _l, _l, _l, _l, _D, _D, _D, _D, _L, _D,
+                                                 _D, _D, _l]
+        L.oracle_rnn_forward_threads.restype = ctypes.c_int
         L.oracle_rnn_input_projection.argtypes = [_l, _l, _l, _l, _D, _D, _D, _D]
         L.oracle_rnn_input_projection.restype = ctypes.c_int
         L.oracle_rnn_cell_dense.argtypes = [_l, _l, _l, _D, _D, _D, _D, _D]
@@ -118,6 +122,34 @@ class Oracle:
             raise ValueError("oracle_rnn_forward_sparse rejected its arguments")
         return y
 
+    def forward_threads(self, x, Wx, b, h0=None, *, Wh=None, vals=None, cols=None,
+                        threads: int = 1) -> np.ndarray:
+        """The dense (``Wh``) or row-balanced sparse (``vals``, ``cols``) forward
+        with each step's outputs split over ``threads`` host threads; the same
+        cell arithmetic as the one-thread drivers, so the same bits."""
+        x, Wx, b = _f64(x), _f64(Wx), _f64(b)
+        T, B, I = x.shape
+        H = Wx.shape[0]
+        assert b.shape == (H,) and (Wh is None) != (vals is None)
+        k = 0
+        if Wh is not None:
+            Wh = _f64(Wh)
+            assert Wh.shape == (H, H)
+        else:
+            vals = _f64(vals)
+            cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+            k = vals.shape[1]
+            assert vals.shape == (H, k) and cols.shape == (H, k)
+        h0 = None if h0 is None else _f64(h0)
+        assert h0 is None or h0.shape == (B, H)
+        y = np.zeros((T, B, H), dtype=np.float64)
+        rc = self.lib.oracle_rnn_forward_threads(T, B, H, I, k, _ptr(x), _ptr(Wx), _ptr(Wh),
+                                                 _ptr(vals), _ptr(cols, _L), _ptr(b),
+                                                 _ptr(h0), _ptr(y), int(threads))
+        if rc != 0:
+            raise ValueError("oracle_rnn_forward_threads rejected its arguments")
+        return y
+
     def forward_csr(self, x, Wx, row_ptr, cols, vals, b, h0=None) -> np.ndarray:
         """y[T,B,H] for unbalanced sparse Wh in compressed-row form:
         row_ptr[H+1], cols[nnz], vals[nnz]."""
@@ -151,9 +183,17 @@ class Oracle:
             inp = y
         return np.stack(ys)
 
-    def forward(self, p, T: Optional[int] = None) -> np.ndarray:
-        """Run a ``synth.Problem`` (optionally only its first ``T`` steps)."""
+    def forward(self, p, T: Optional[int] = None, threads: int = 1) -> np.ndarray:
+        """Run a ``synth.Problem`` (optionally only its first ``T`` steps);
+        ``threads`` > 1 runs a single dense or row-balanced layer on that many
+        host threads."""
         x = p.x if T is None else p.x[:T]
+        if threads > 1:
+            assert getattr(p, "layers", None) is None and getattr(p, "row_ptr", None) is None
+            if p.sparse:
+                return self.forward_threads(x, p.Wx, p.b, p.h0, vals=p.vals, cols=p.cols,
+                                            threads=threads)
+            return self.forward_threads(x, p.Wx, p.b, p.h0, Wh=p.Wh, threads=threads)
         if getattr(p, "layers", None) is not None:
             return self.forward_stack(x, p.layers, p.h0)
         if getattr(p, "row_ptr", None) is not None:

@@ -28,6 +28,8 @@
  *   h0 [B][H] or NULL, y [T][B][H].
  * Return: 0 on success, -1 on bad sizes or NULL pointers.
  */
+#define _POSIX_C_SOURCE 200809L
+#include <pthread.h>
 #include <stddef.h>
 #include <stdlib.h>
 #include <string.h>
@@ -103,6 +105,115 @@ int oracle_rnn_forward_sparse(long T, long B, long H, long I, long k,
     for (long i = 0; i < H * k; ++i)
         if (cols[i] < 0 || cols[i] >= H) return -1;
     return forward(T, B, H, I, k, x, Wx, NULL, vals, cols, bias, h0, y);
+}
+
+/*
+ * The same time loop run by a team of POSIX threads, for timing the oracle on
+ * every host core.  Each step's B*H outputs are split into contiguous runs of
+ * (b, r), one per thread, and a barrier separates the steps (step t reads all
+ * of h_{t-1}).  Every output is computed by the same cell function as the
+ * one-thread driver above, from the same inputs, so y is bit-identical to it;
+ * only the order in which outputs are produced differs.  Wh != NULL selects the
+ * dense form, else the row-balanced sparse form (k, vals, cols).
+ */
+typedef struct {
+    long T, B, H, I, k;
+    const double *x, *Wx, *Wh, *vals, *bias, *h0;
+    const long* cols;
+    double* y;
+    pthread_mutex_t gate_m;
+    pthread_cond_t gate_c;
+    int started;
+    long nlive; /* threads that take part, set before the gate opens */
+    pthread_barrier_t step;
+} team_t;
+
+typedef struct {
+    team_t* team;
+    long id;
+} member_t;
+
+static void team_work(team_t* tm, long id) {
+    pthread_mutex_lock(&tm->gate_m);
+    while (!tm->started) pthread_cond_wait(&tm->gate_c, &tm->gate_m);
+    pthread_mutex_unlock(&tm->gate_m);
+    const long n = tm->B * tm->H;
+    const long i0 = n * id / tm->nlive, i1 = n * (id + 1) / tm->nlive;
+    for (long t = 0; t < tm->T; ++t) {
+        for (long i = i0; i < i1; ++i) {
+            const long b = i / tm->H, r = i % tm->H;
+            const double* x_t = tm->x + (t * tm->B + b) * tm->I;
+            const double* h_prev =
+                (t == 0) ? tm->h0 + b * tm->H : tm->y + ((t - 1) * tm->B + b) * tm->H;
+            tm->y[(t * tm->B + b) * tm->H + r] =
+                tm->Wh ? oracle_rnn_cell_dense(tm->H, tm->I, r, x_t, tm->Wx, tm->Wh, tm->bias,
+                                               h_prev)
+                       : oracle_rnn_cell_sparse(tm->H, tm->I, tm->k, r, x_t, tm->Wx, tm->vals,
+                                                tm->cols, tm->bias, h_prev);
+        }
+        pthread_barrier_wait(&tm->step);
+    }
+}
+
+static void* team_member(void* arg) {
+    member_t* m = (member_t*)arg;
+    team_work(m->team, m->id);
+    return NULL;
+}
+
+int oracle_rnn_forward_threads(long T, long B, long H, long I, long k, const double* x,
+                               const double* Wx, const double* Wh, const double* vals,
+                               const long* cols, const double* bias, const double* h0,
+                               double* y, long nthreads) {
+    if (T < 0 || B < 0 || H <= 0 || I <= 0 || nthreads < 1 || nthreads > 1024) return -1;
+    if (!x || !Wx || !bias || !y) return -1;
+    if (!Wh) {
+        if (!vals || !cols || k <= 0 || k > H) return -1;
+        for (long i = 0; i < H * k; ++i)
+            if (cols[i] < 0 || cols[i] >= H) return -1;
+    }
+    if (T == 0 || B == 0) return 0;
+    double* zeros = NULL;
+    if (!h0) {
+        zeros = (double*)calloc((size_t)(B * H), sizeof(double));
+        if (!zeros) return -1;
+        h0 = zeros;
+    }
+    pthread_t* tids = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    member_t* members = (member_t*)calloc((size_t)nthreads, sizeof(member_t));
+    if (!tids || !members) {
+        free(tids);
+        free(members);
+        free(zeros);
+        return -1;
+    }
+    team_t tm = {T, B, H, I, k, x, Wx, Wh, vals, bias, h0, cols, y};
+    pthread_mutex_init(&tm.gate_m, NULL);
+    pthread_cond_init(&tm.gate_c, NULL);
+    tm.started = 0;
+    /* the calling thread is member 0; members 1.. are started until one fails */
+    long nlive = 1;
+    for (long id = 1; id < nthreads; ++id) {
+        members[id].team = &tm;
+        members[id].id = id;
+        if (pthread_create(&tids[id], NULL, team_member, &members[id]) != 0) break;
+        ++nlive;
+    }
+    tm.nlive = nlive;
+    pthread_barrier_init(&tm.step, NULL, (unsigned)nlive);
+    pthread_mutex_lock(&tm.gate_m);
+    tm.started = 1;
+    pthread_cond_broadcast(&tm.gate_c);
+    pthread_mutex_unlock(&tm.gate_m);
+    team_work(&tm, 0);
+    for (long id = 1; id < nlive; ++id) pthread_join(tids[id], NULL);
+    pthread_barrier_destroy(&tm.step);
+    pthread_cond_destroy(&tm.gate_c);
+    pthread_mutex_destroy(&tm.gate_m);
+    free(tids);
+    free(members);
+    free(zeros);
+    return 0;
 }
 
 /*

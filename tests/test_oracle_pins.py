@@ -39,6 +39,28 @@ def test_cells_match_forward(o):
         assert np.array_equal(got, want)
 
 
+def test_threaded_driver_gives_the_same_bits(o):
+    """The all-cores timing driver splits each step over threads but computes
+    every output with the same cell function: the result must be bit-identical
+    to the one-thread driver for any team size, including teams larger than
+    the number of outputs of a step."""
+    from persistent_rnn_recurrence_gb300 import synth
+    probs = (synth.make_problem(H=40, B=3, T=5, I=24, wdtype="f32", seed=6, h0_std=0.5),
+             synth.make_problem(H=40, B=3, T=5, k=7, seed=7),
+             synth.make_problem(H=5, B=1, T=3, I=4, wdtype="f32", seed=8))
+    for p in probs:
+        y = o.forward(p)
+        for n in (1, 2, 3, 8, 64):
+            assert np.array_equal(o.forward(p, threads=n), y), (p.H, p.sparse, n)
+    p = probs[0]
+    with pytest.raises(ValueError):
+        o.forward_threads(p.x, p.Wx, p.b, Wh=p.Wh, threads=0)
+    with pytest.raises(ValueError):
+        o.forward_threads(p.x, p.Wx, p.b, vals=np.ones((40, 1)), cols=np.full((40, 1), 40),
+                          threads=2)
+    assert o.forward_threads(p.x[:0], p.Wx, p.b, Wh=p.Wh, threads=4).shape == (0, 3, 40)
+
+
 def test_rejects_bad_arguments(o):
     x = np.zeros((1, 1, 2))
     with pytest.raises(ValueError):
