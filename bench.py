@@ -434,7 +434,10 @@ def run_ours(args):
         "gflops_effective": fl["total"] / (ms_step * 1e-3) / 1e9 * world,
         "gflops_dense_equivalent": (fl["projection"] + fl["recurrence_dense_equiv"])
         / (ms_step * 1e-3) / 1e9 * world,
-        "stage_ms": {"projection": proj_med, "recurrence": rec_med},
+        "step_ms_stats": {"median": sorted(step_ms)[len(step_ms) // 2], "min": min(step_ms),
+                          "max": max(step_ms)},
+        "stage_ms": {"projection": proj_med, "recurrence": rec_med,
+                     "projection_min": proj_ms[0], "recurrence_min": rec_ms[0]},
         "roofline": roof,
         "clocks": clocks,
         "gpu_launches": args.steps * ((2 if info["projection_tensor_cores"] else 1)
@@ -523,7 +526,8 @@ def load_peaks() -> dict:
 
 
 KERNEL_SOURCES = {
-    True: ["persistent_sparse.cu", "persistent_common.cuh", "device_common.cuh"],
+    True: ["persistent_sparse.cu", "persistent_sparse.cuh", "persistent_common.cuh",
+           "device_common.cuh"],
     False: ["persistent_dense.cu", "persistent_common.cuh", "device_common.cuh"],
 }
 
@@ -634,14 +638,16 @@ def run_ablation(args):
     lay = prnn.Layer.from_problem(dense, algo="per_step")
     base = rec_us(lay)
     lay.close()
-    rows = [("sparse persistent, 32-bit loads, plain layout, grid barrier", 0, 0, 1),
-            ("+ wide (128-bit) loads", 1, 0, 1),
-            ("+ bank-aware layout", 1, 1, 1),
-            ("+ flags in the data (no grid barrier)", 1, 1, 0)]
+    rows = [("sparse persistent, 32-bit loads, plain layout, grid barrier", 0, 0, 1, 0),
+            ("+ wide (128-bit) loads", 1, 0, 1, 0),
+            ("+ bank-aware layout", 1, 1, 1, 0),
+            ("+ flags in the data (no grid barrier)", 1, 1, 0, 0),
+            ("+ per-CTA bank-balancing order of the staged h", 1, 1, 0, 1)]
     out = {"workload": p.name, "per_step_dense_us_per_step": base, "rows": []}
-    for label, wide, bank, barrier in rows:
+    for label, wide, bank, barrier, staged in rows:
         lay = prnn.Layer(p.H, p.I, p.B, "f16", "persistent")
         lay.set_option(prnn.PRNN_OPT_BANK_AWARE, bank)
+        lay.set_option(prnn.PRNN_OPT_STAGED_ORDER, staged)
         lay.set_problem_weights(p)
         lay.set_option(prnn.PRNN_OPT_WIDE_LOADS, wide)
         lay.set_option(prnn.PRNN_OPT_SYNC_MODE, barrier)
@@ -651,6 +657,31 @@ def run_ablation(args):
         out["rows"].append({"row": label, "us_per_step": us, "speedup_vs_per_step_dense": base / us,
                             "bank_cap": info["sparse_bank_cap"], "groups": info["cta_groups"]})
     print(json.dumps(out))
+    # the staged order on the named sparse layers, column order vs staged, same box
+    for name in [n for n in synth.NAMED if n.startswith("sparse")]:
+        q = synth.named_problem(name)
+        xq = torch.from_numpy(q.x).to(dev)
+        yq = torch.empty((q.T, q.B, q.H), dtype=torch.float32, device=dev)
+        line = {"workload": name}
+        for staged in (0, 1):
+            lay = prnn.Layer(q.H, q.I, q.B, "f16", "persistent")
+            lay.set_option(prnn.PRNN_OPT_STAGED_ORDER, staged)
+            lay.set_problem_weights(q)
+            lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+            prnn.prnn_forward(lay.h, q.T, q.B, xq, None, yq)
+            ms = []
+            for _ in range(reps):
+                flush.fill_(1.0)
+                prnn.prnn_forward(lay.h, q.T, q.B, xq, None, yq)
+                ms.append(prnn.prnn_get_timing(lay.h)[1])
+            assert lay.status() == prnn.PRNN_OK
+            info = lay.info()
+            lay.close()
+            key = "staged_order" if staged else "column_order"
+            line[key] = {"us_per_step": 1e3 * sorted(ms)[len(ms) // 2] / q.T,
+                         "bank_cap": info["sparse_bank_cap"], "k_padded": info["k_padded"],
+                         "staged": info["sparse_staged_order"]}
+        print(json.dumps(line))
     return 0
 
 

@@ -78,10 +78,15 @@ typedef enum {
   PRNN_OPT_POLL_BACKOFF_NS = 10,  /* persistent: pause before re-polling stale step data, ns,
                                      doubling per round up to 4x; 0 .. 10000 (default: 0, and
                                      250 for stacks)                                            */
-  PRNN_OPT_RECURRENT_TC = 11      /* dense fp16 persistent: 0 = tcgen05 recurrence when
+  PRNN_OPT_RECURRENT_TC = 11,     /* dense fp16 persistent: 0 = tcgen05 recurrence when
                                      max_batch >= 16, 1 = never (default: at B <= 32 its chain
                                      of small dependent MMAs is slower than the CUDA-core
                                      kernel), 2 = whenever it fits; takes effect at the next
+                                     set_weights call                                           */
+  PRNN_OPT_STAGED_ORDER = 12      /* sparse, bank-aware, H % 128 == 0: 1 = each CTA stages h in
+                                     its own bank-balancing order (one lane per bank in every
+                                     gather slot, at the cost of scattered staging stores);
+                                     0 = column order (default); takes effect at the next
                                      set_weights call                                           */
 } prnn_option_t;
 
@@ -98,6 +103,8 @@ typedef struct {
   size_t onchip_weight_bytes;      /* packed Wh bytes held on chip, all CTAs                 */
   size_t nnz;                      /* non-zeros of Wh (H*H when dense)                       */
   int recurrent_tensor_cores;      /* 1 if the dense recurrence runs on tcgen05 (wide batch) */
+  int sparse_staged_order;         /* sparse: 1 if each CTA stages h_{t-1} in its own
+                                      bank-balancing order (prnn_pack_sparse_host_placed)   */
 } prnn_info_t;
 
 /*
@@ -245,6 +252,33 @@ prnn_status_t prnn_pack_sparse_host(int hidden, int k, int n_cta, int rows_per_c
                                     int threads_per_row, const uint16_t* vals,
                                     const uint16_t* cols, uint32_t* packed,
                                     size_t capacity_words, int* ept, int* bank_cap);
+
+/*
+ * Host only (no GPU): the packing the persistent sparse kernel actually uses
+ * for bank-aware layers whose hidden size is a multiple of 128.  Each CTA
+ * stages h_{t-1} in shared memory in an order of its own, chosen so that the
+ * entries of every warp spread evenly over the 32 banks (so that the
+ * bank-aware placement above can give each lane of a gather slot its own
+ * bank); the index field of each packed word is then the staged position of
+ * the column instead of the column itself.
+ *   place [n_cta][hidden/4] receives one word per group of four columns g:
+ *   byte j (0..3) is a bank b_j, and column 4g+j is staged at
+ *       128*(g/32) + 32*j + b_j.
+ *   Within each class (one block of 128 columns, one j) the 32 banks are a
+ *   permutation of 0..31, so the staging stores of a warp are conflict-free.
+ * *placed = 1 when the staged order is used; 0 for hidden not a multiple of
+ * 128, where columns stay in order, packed equals prnn_pack_sparse_host's
+ * output and place is not written.  place_capacity_words is the size of
+ * place (n_cta*hidden/4 words needed when *placed = 1).  The other arguments,
+ * the sizing protocol and the errors are those of prnn_pack_sparse_host;
+ * placed must not be NULL.
+ */
+prnn_status_t prnn_pack_sparse_host_placed(int hidden, int k, int n_cta, int rows_per_cta,
+                                           int threads_per_row, const uint16_t* vals,
+                                           const uint16_t* cols, uint32_t* packed,
+                                           size_t capacity_words, uint32_t* place,
+                                           size_t place_capacity_words, int* ept,
+                                           int* bank_cap, int* placed);
 
 /*
  * Forward pass that allocates no device memory.  The pages have no

@@ -37,7 +37,7 @@ struct prnn_handle {
   bool rtc = false;
   int t_n_cta = 0, t_R = 0, t_G = 1, t_cpg = 0, t_N = 0, t_ring = 0;
   void* Wimg = nullptr;
-  int wide_loads = 1, bank_aware = 1;
+  int wide_loads = 1, bank_aware = 1, staged_order = 0;
   size_t onchip_bytes = 0, smem_at_max = 0;
   bool tc_proj = false;
   int Kp = 0;  // I rounded up to 64 (tcgen05 projection)
@@ -47,6 +47,8 @@ struct prnn_handle {
   float* bias = nullptr;
   void* Wpk = nullptr;       // persistent packed recurrent weights
   void* Wpk_T = nullptr;     // the same packing of Wh^T (backward pass, dense)
+  uint32_t* place = nullptr;    // sparse: per-CTA staging order of h ([cpg][H/4]) or null
+  uint32_t* place_T = nullptr;  // the same for the Wh^T plan of the backward pass
   void* Wh_nat = nullptr;    // Wh row-major [H][H] in wdtype (backward pass, dense)
   // sparse backward: plan of the persistent kernel for Wh^T (packed in
   // Wpk_T), the forward's padded column lists and each padded entry's index
@@ -391,6 +393,8 @@ void free_weights(prnn_handle* h) {
   free_dev(h->bias);
   free_dev(h->Wpk);
   free_dev(h->Wpk_T);
+  free_dev(h->place);
+  free_dev(h->place_T);
   free_dev(h->Wh_nat);
   free_dev(h->Wimg);
   h->rtc = false;
@@ -436,7 +440,8 @@ RecurCommon common_args(const prnn_handle* h, int T, int B, const float* h0, flo
 // the first plan (fastest by the model) whose packing fits shared memory.
 static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
                           const std::vector<uint16_t>& hc, SparsePlan* plan,
-                          std::vector<uint32_t>* pk, PackStats* pst) {
+                          std::vector<uint32_t>* pk, PackStats* pst,
+                          std::vector<uint32_t>* place) {
   const int H = h->H;
   for (const SparsePlan& cand : plan_sparse(h, k)) {
     // largest entries-per-thread whose weights plus one h column fit in smem
@@ -445,7 +450,8 @@ static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
     const int max_ept = (int)(((h->smem_optin - hs1) / ((size_t)cand.R * cand.tpr * 4)) / 4 * 4);
     *plan = cand;
     plan->ept = pack_sparse_rows(H, k, plan->R, plan->cpg, plan->tpr, hv.data(), hc.data(), *pk,
-                                 pst, max_ept, h->bank_aware != 0);
+                                 pst, max_ept, h->bank_aware != 0,
+                                 h->staged_order ? place : nullptr);
     if (plan->ept > 0) {
       plan->kp = plan->ept * plan->tpr;
       return true;
@@ -465,9 +471,9 @@ static prnn_status_t install_sparse(prnn_t h, const void* Wx, const float* bias,
                                     const std::vector<int32_t>& caller_pos) {
   const int H = h->H;
   SparsePlan plan{};
-  std::vector<uint32_t> pk;
+  std::vector<uint32_t> pk, place;
   PackStats pst;
-  if (h->algo == PRNN_ALGO_PERSISTENT && !plan_and_pack(h, k, hv, hc, &plan, &pk, &pst))
+  if (h->algo == PRNN_ALGO_PERSISTENT && !plan_and_pack(h, k, hv, hc, &plan, &pk, &pst, &place))
     return PRNN_ERR_UNSUPPORTED;
   // Wh^T: row c lists the stored (r, value) of column c in ascending r,
   // padded to the longest such list with zero-valued absent columns
@@ -497,9 +503,10 @@ static prnn_status_t install_sparse(prnn_t h, const void* Wx, const float* bias,
     }
   }
   SparsePlan tplan{};
-  std::vector<uint32_t> pkT;
+  std::vector<uint32_t> pkT, placeT;
   PackStats pstT;
-  const bool bwd = h->algo == PRNN_ALGO_PERSISTENT && plan_and_pack(h, kT, hvT, hcT, &tplan, &pkT, &pstT);
+  const bool bwd = h->algo == PRNN_ALGO_PERSISTENT &&
+                   plan_and_pack(h, kT, hvT, hcT, &tplan, &pkT, &pstT, &placeT);
   free_weights(h);
   prnn_status_t st = stage_wx_bias(h, Wx, bias, &h->Wx, &h->Wx16, &h->bias);
   if (st != PRNN_OK) return st;
@@ -508,6 +515,7 @@ static prnn_status_t install_sparse(prnn_t h, const void* Wx, const float* bias,
   };
   if (h->algo == PRNN_ALGO_PERSISTENT) {
     PRNN_TRY(upload(&h->Wpk, pk.data(), pk.size() * 4));
+    if (!place.empty()) PRNN_TRY(upload(&h->place, place.data(), place.size() * 4));
     h->n_cta = plan.n_cta;
     h->R = plan.R;
     h->G = plan.G;
@@ -525,6 +533,7 @@ static prnn_status_t install_sparse(prnn_t h, const void* Wx, const float* bias,
     h->smem_at_max = sm;
     if (bwd) {
       PRNN_TRY(upload(&h->Wpk_T, pkT.data(), pkT.size() * 4));
+      if (!placeT.empty()) PRNN_TRY(upload(&h->place_T, placeT.data(), placeT.size() * 4));
       PRNN_TRY(upload(&h->cols_pad, hc.data(), hc.size() * 2));
       PRNN_TRY(upload(&h->caller_pos, caller_pos.data(), caller_pos.size() * 4));
       PRNN_TRY(upload(&h->valsT, hvT.data(), hvT.size() * 2));
@@ -873,6 +882,7 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
       a.bgroup = bg;
       a.dbuf = db ? 1 : 0;
       a.narrow = h->wide_loads ? 0 : 1;
+      a.place = h->place;
       PRNN_TRY(launch_recur_sparse(a, s));
     } else if (h->rtc && h->sync_mode == 0) {
       DenseTcArgs a{};
@@ -1031,6 +1041,7 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
     a.bgroup = bg;
     a.dbuf = dbuf ? 1 : 0;
     a.narrow = 0;
+    a.place = h->place_T;
     PRNN_TRY(launch_recur_sparse(a, s));
   } else {
     DenseRecurArgs a{};
@@ -1183,6 +1194,10 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
       if (value < 0 || value > 2) return PRNN_ERR_INVALID_ARG;
       h->rtc_opt = (int)value;
       return PRNN_OK;
+    case PRNN_OPT_STAGED_ORDER:
+      if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
+      h->staged_order = (int)value;
+      return PRNN_OK;
   }
   return PRNN_ERR_INVALID_ARG;
 }
@@ -1211,6 +1226,7 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
   info->onchip_weight_bytes = h->onchip_bytes;
   info->nnz = h->sparse ? (size_t)h->H * h->k : (size_t)h->H * h->H;
   info->recurrent_tensor_cores = h->rtc ? 1 : 0;
+  info->sparse_staged_order = h->sparse && h->place != nullptr ? 1 : 0;
   if (h->rtc) {
     info->n_cta = h->t_n_cta;
     info->rows_per_cta = h->t_R;
@@ -1282,6 +1298,37 @@ prnn_status_t prnn_pack_sparse_host(int hidden, int k, int n_cta, int rows_per_c
   if (bank_cap) *bank_cap = st.cap;
   if (!packed || capacity_words < pk.size()) return PRNN_ERR_INVALID_ARG;
   std::memcpy(packed, pk.data(), pk.size() * sizeof(uint32_t));
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_pack_sparse_host_placed(int hidden, int k, int n_cta, int rows_per_cta,
+                                           int threads_per_row, const uint16_t* vals,
+                                           const uint16_t* cols, uint32_t* packed,
+                                           size_t capacity_words, uint32_t* place,
+                                           size_t place_capacity_words, int* ept,
+                                           int* bank_cap, int* placed) {
+  const int H = hidden, R = rows_per_cta, tpr = threads_per_row;
+  if (H < 1 || H > 65535 || k < 1 || k > H || n_cta < 1 || R < 1 || (size_t)n_cta * R < (size_t)H)
+    return PRNN_ERR_INVALID_ARG;
+  if (tpr != 1 && tpr != 2 && tpr != 4 && tpr != 8 && tpr != 16 && tpr != 32)
+    return PRNN_ERR_INVALID_ARG;
+  if (!vals || !cols || !ept || !placed) return PRNN_ERR_INVALID_ARG;
+  std::vector<int> seen((size_t)H, -1);
+  for (int r = 0; r < H; ++r)
+    for (int j = 0; j < k; ++j) {
+      const int c = cols[(size_t)r * k + j];
+      if (c >= H || seen[c] == r) return PRNN_ERR_INVALID_ARG;
+      seen[c] = r;
+    }
+  std::vector<uint32_t> pk, pl;
+  PackStats st;
+  *ept = pack_sparse_rows(H, k, R, n_cta, tpr, vals, cols, pk, &st, 1 << 30, true, &pl);
+  *placed = pl.empty() ? 0 : 1;
+  if (bank_cap) *bank_cap = st.cap;
+  if (!packed || capacity_words < pk.size()) return PRNN_ERR_INVALID_ARG;
+  if (!pl.empty() && (!place || place_capacity_words < pl.size())) return PRNN_ERR_INVALID_ARG;
+  std::memcpy(packed, pk.data(), pk.size() * sizeof(uint32_t));
+  if (!pl.empty()) std::memcpy(place, pl.data(), pl.size() * sizeof(uint32_t));
   return PRNN_OK;
 }
 

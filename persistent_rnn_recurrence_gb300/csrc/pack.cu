@@ -15,9 +15,29 @@
 // slot share a bank; padding entries take the least-used residue.  The
 // placement only permutes each row's entries among its own threads, so the
 // row sums are unchanged up to fp32 rounding order.
+//
+// Staged-h placement (opt-in): a bank-aware colouring can put one lane per
+// bank in every slot only if no bank carries more of a warp's entries than
+// there are slots.  With h staged in column order the bank of an entry is its
+// column mod 32, and the busiest bank of a warp typically carries 1.5x the
+// mean, so most slots need two shared-memory wavefronts.  On request each CTA
+// stages h_{t-1} in an order of its own, chosen so that every warp's entries
+// spread evenly over the banks; the packed index field then holds the staged
+// position instead of the column.  (On GB300 the scattered staging this needs
+// costs more per step than the wavefronts it saves, so column order is the
+// default.)  The order keeps the staging stores
+// conflict-free: column c = 4g + j (group g, component j) goes to
+//     pos(c) = 128*(g / 32) + 32*j + bank_{g/32, j}(g % 32),
+// where each bank_{blk, j} is a permutation of the 32 banks.  The staging
+// thread that loads the float4 of group g (lane g % 32 of its warp) stores
+// its four components with four 32-bit stores, and for each store the 32
+// lanes of the warp hit 32 different banks.  One table word per group holds
+// the four banks (byte j = bank of component j).  Layers whose H is not a
+// multiple of 128 keep the column order.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <random>
 #include <vector>
 
 #include "prnn_internal.h"
@@ -126,7 +146,110 @@ bool colour_warp(const std::vector<std::vector<Entry>>& rows, int tpr, int S, in
   return true;
 }
 
+// Staged position of column c under one CTA's table (one word per group).
+inline int placed_pos(const uint32_t* tab, int c) {
+  const int g = c >> 2, j = c & 3;
+  return 128 * (g >> 5) + 32 * j + (int)((tab[g] >> (8 * j)) & 31u);
+}
+
+// Search one CTA's staging order.  mult[w][c] = entries of column c in warp w
+// (nw warps).  Local search over swaps of two columns of one class (same
+// block of 128 columns, same component): a swap exchanges their banks and so
+// keeps every class a permutation of the banks.  The objective is
+// sum over (warp, bank) of max(0, D - S)^2, D = the warp's entries on that
+// bank; a move is taken when it lowers the objective, or keeps it equal with
+// probability 1/4 (a walk along plateaus).  Deterministic for a given seed.
+// Returns the largest D left (<= S when the search succeeded).
+int place_cta(int H, int nw, const std::vector<uint8_t>& mult, int S, uint32_t seed,
+              uint32_t* tab /* H/4 words */) {
+  const int ncls = H / 32;  // (H/128 blocks) x 4 components, 32 columns each
+  std::mt19937 rng(seed);
+  // at[cls*32 + b] = column staged on bank b of class cls; bank[c] its inverse
+  std::vector<int> at((size_t)ncls * 32), bank((size_t)H);
+  for (int cls = 0; cls < ncls; ++cls) {
+    int perm[32];
+    for (int i = 0; i < 32; ++i) perm[i] = i;
+    std::shuffle(perm, perm + 32, rng);
+    const int blk = cls >> 2, j = cls & 3;
+    for (int l = 0; l < 32; ++l) {
+      const int c = 128 * blk + 4 * l + j;
+      bank[c] = perm[l];
+      at[(size_t)cls * 32 + perm[l]] = c;
+    }
+  }
+  auto M = [&](int w, int c) { return (int)mult[(size_t)w * H + c]; };
+  std::vector<int> D((size_t)nw * 32, 0);
+  for (int w = 0; w < nw; ++w)
+    for (int c = 0; c < H; ++c) D[(size_t)w * 32 + bank[c]] += M(w, c);
+  auto ex = [&](int d) { return d > S ? (long long)(d - S) * (d - S) : 0LL; };
+  long long E = 0;
+  for (int d : D) E += ex(d);
+  std::vector<int> viol, cand;
+  // bounded work: stop after max_iter moves, or after `patience` moves
+  // without a new lowest objective
+  const long max_iter = 20000, patience = 4000;
+  long long best_E = E;
+  long since_best = 0;
+  for (long it = 0; it < max_iter && E > 0 && since_best < patience; ++it) {
+    if (E < best_E) {
+      best_E = E;
+      since_best = 0;
+    } else {
+      ++since_best;
+    }
+    viol.clear();
+    for (int i = 0; i < nw * 32; ++i)
+      if (D[i] > S) viol.push_back(i);
+    const int pick = viol[rng() % viol.size()];
+    const int w0 = pick / 32, b0 = pick % 32;
+    cand.clear();
+    for (int cls = 0; cls < ncls; ++cls) {
+      const int c = at[(size_t)cls * 32 + b0];
+      if (M(w0, c) > 0) cand.push_back(c);
+    }
+    const int c1 = cand[rng() % cand.size()];
+    const int cls1 = 4 * (c1 >> 7) + (c1 & 3);  // 4 * block + component
+    long long best = 1;
+    int best_b = -1;
+    for (int b1 = 0; b1 < 32; ++b1) {
+      if (b1 == b0) continue;
+      const int c2 = at[(size_t)cls1 * 32 + b1];
+      long long delta = 0;
+      for (int w = 0; w < nw; ++w) {
+        const int d = M(w, c1) - M(w, c2);
+        if (d == 0) continue;
+        const int x0 = D[(size_t)w * 32 + b0], x1 = D[(size_t)w * 32 + b1];
+        delta += ex(x0 - d) + ex(x1 + d) - ex(x0) - ex(x1);
+      }
+      if (delta < best || (delta == 0 && best > 0 && (rng() & 3u) == 0u)) {
+        best = delta;
+        best_b = b1;
+      }
+    }
+    if (best_b < 0 || best > 0) continue;
+    const int c2 = at[(size_t)cls1 * 32 + best_b];
+    for (int w = 0; w < nw; ++w) {
+      const int d = M(w, c1) - M(w, c2);
+      D[(size_t)w * 32 + b0] -= d;
+      D[(size_t)w * 32 + best_b] += d;
+    }
+    bank[c1] = best_b;
+    bank[c2] = b0;
+    at[(size_t)cls1 * 32 + best_b] = c1;
+    at[(size_t)cls1 * 32 + b0] = c2;
+    E += best;
+  }
+  for (int g = 0; g < H / 4; ++g)
+    tab[g] = (uint32_t)bank[4 * g] | ((uint32_t)bank[4 * g + 1] << 8) |
+             ((uint32_t)bank[4 * g + 2] << 16) | ((uint32_t)bank[4 * g + 3] << 24);
+  int dmax = 0;
+  for (int d : D) dmax = std::max(dmax, d);
+  return dmax;
+}
+
 }  // namespace
+
+bool staging_placement_supported(int H) { return H >= 128 && H % 128 == 0; }
 
 // Entries per thread (a multiple of 4) and the bank-aware placement for all
 // warps.  S (uniform over the layer) is chosen among s_min, s_min + 4, ...,
@@ -156,7 +279,8 @@ void plain_warp(const std::vector<std::vector<Entry>>& rows, int tpr, int S,
 
 int pack_sparse_rows(int H, int k, int R, int n_cta, int tpr, const uint16_t* vals,
                      const uint16_t* cols, std::vector<uint32_t>& out_packed,
-                     PackStats* stats, int max_ept, bool bank_aware) {
+                     PackStats* stats, int max_ept, bool bank_aware,
+                     std::vector<uint32_t>* place_out) {
   const int rpw = tpr >= 32 ? 1 : 32 / tpr;
   const int s_min = ((k + tpr - 1) / tpr + 3) / 4 * 4;
   const int warps_per_cta = (R + rpw - 1) / rpw;
@@ -179,6 +303,44 @@ int pack_sparse_rows(int H, int k, int R, int n_cta, int tpr, const uint16_t* va
         }
       }
     }
+  // staged-h placement: per CTA, stage h so that each warp's entries spread
+  // evenly over the banks, then index entries by staged position
+  const bool use_place = bank_aware && place_out != nullptr && staging_placement_supported(H);
+  if (place_out) place_out->clear();
+  if (use_place) {
+    place_out->assign((size_t)n_cta * (H / 4), 0u);
+    std::vector<uint8_t> mult;
+    for (int c = 0; c < n_cta; ++c) {
+      mult.assign((size_t)warps_per_cta * H, 0);
+      for (int w = 0; w < warps_per_cta; ++w)
+        for (const std::vector<Entry>& row : wrows[(size_t)c * warps_per_cta + w])
+          for (const Entry& e : row) ++mult[(size_t)w * H + e.first];
+      // target: the fewest slots that leave >= 6 % of a warp's slot-lanes free
+      // (a warp whose entries fill every lane of every slot admits no
+      // placement better than its column order's bank counts allow)
+      int most = 0;
+      for (int w = 0; w < warps_per_cta; ++w) {
+        int n = 0;
+        for (const std::vector<Entry>& row : wrows[(size_t)c * warps_per_cta + w])
+          n += (int)row.size();
+        most = std::max(most, n);
+      }
+      int S_t = s_min;
+      while ((double)most > 0.94 * 32.0 * S_t) S_t += 4;
+      uint32_t* tab = place_out->data() + (size_t)c * (H / 4);
+      place_cta(H, warps_per_cta, mult, S_t, 0x9e3779b9u ^ (uint32_t)c, tab);
+      for (int w = 0; w < warps_per_cta; ++w) {
+        const size_t wi = (size_t)c * warps_per_cta + w;
+        int rc[32] = {0};
+        dw[wi] = 0;
+        for (std::vector<Entry>& row : wrows[wi])
+          for (Entry& e : row) {
+            e.first = (uint16_t)placed_pos(tab, e.first);
+            dw[wi] = std::max(dw[wi], ++rc[e.first % 32]);
+          }
+      }
+    }
+  }
   auto cap_for = [](int d, int S) { return std::max(1, (d + S - 1) / S); };
   int S = s_min;
   double best_cost = -1.0;

@@ -1,0 +1,330 @@
+// persistent_sparse.cuh -- the persistent recurrent kernel for row-balanced
+// sparse Wh (a template over threads per row, batch columns per pass and the
+// staging order of h) and its launch dispatch.  persistent_sparse.cu
+// instantiates it with h staged in column order, persistent_sparse_placed.cu
+// with each CTA's own bank-balancing order, so that neither set of kernels
+// carries the other's staging code or registers.
+//
+// One cooperative launch runs all T steps of h_t = ReLU(P_t + Wh h_{t-1})
+// (P_t = Wx x_t + b comes from the projection kernel).  Each CTA owns a block
+// of R consecutive rows of Wh and loads them into shared memory / registers
+// once, so the weights stay on chip for the whole sequence instead of being
+// re-read every step (persistent-rnn page, "What This Project Does"; "Sparse
+// Persistent RNNs: Squeezing Large Recurrent Networks On-Chip").
+//
+// CTA groups: the batch columns of the recurrence are independent, so the
+// grid is split into G groups of cpg CTAs; group gi owns the contiguous batch
+// columns [gi*Bl, gi*Bl + Bl) and holds its own on-chip copy of Wh.  A CTA
+// only ever waits for the CTAs of its own group, and reads only its group's
+// Bl columns of h_{t-1} per step, which cuts the data each SM pulls from L2
+// per step by G.
+//
+// Step exchange: h_t is published by storing it into y[t] (pre-filled with a
+// NaN sentinel); consumers poll y[t-1] with relaxed gpu-scope loads until no
+// word is the sentinel.  The data word is its own "ready" flag, so there is no
+// grid barrier between steps (the Lamport-timestamp row of the sparse
+// persistent RNN ablation).  A grid-barrier mode is kept for that ablation.
+//
+// Every wait is bounded (globaltimer deadline); on expiry the kernel records
+// a status word and every CTA leaves its time loop.
+#pragma once
+#include "persistent_common.cuh"
+
+namespace prnn {
+
+using namespace pk;
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Staging into a per-CTA placement of h (the packer's bank-balancing order;
+// opt-in): column 4g+j of batch row b goes to
+//     b*H + 128*(g/32) + 32*j + byte j of place[g],
+// four 32-bit stores per float4.  Each 32-column class's bytes are a
+// permutation of the banks, so the 32 lanes of a warp hit 32 different banks
+// per store.  Requires H % 128 == 0; every index stays inside its batch row
+// for any table contents (bytes masked to 0..31, block start <= H - 128).
+// Loads, polls and the bounded wait are those of stage_rows; the batch row and
+// group of each load are stepped, not divided.
+// ---------------------------------------------------------------------------
+template <int UMAX>
+__device__ __forceinline__ bool stage_rows_placed(const float* hprev, bool poll, int H,
+                                                  int b_start, int nb, float* hs, Waiter& w,
+                                                  const uint32_t* place) {
+  const int NT = blockDim.x, tid = threadIdx.x;
+  const int ng = H >> 2, nf4 = nb * ng;
+  const float4* src = reinterpret_cast<const float4*>(hprev + (size_t)b_start * H);
+  for (int base = tid; base < nf4; base += UMAX * NT) {
+    float4 v[UMAX];
+    uint32_t pw[UMAX];
+    const int b0 = base / ng, g0 = base - b0 * ng;
+    int b = b0, g = g0;
+#pragma unroll
+    for (int u = 0; u < UMAX; ++u) {
+      const int i = base + u * NT;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      pw[u] = 0u;
+      if (i < nf4) {
+        pw[u] = __ldg(place + g);
+        if (hprev != nullptr)
+          v[u] = poll ? ld_relaxed_f4(reinterpret_cast<const float*>(src + i)) : __ldg(src + i);
+      }
+      g += NT;
+      while (g >= ng) {
+        g -= ng;
+        ++b;
+      }
+    }
+    if (poll) {
+      uint32_t spins = 0, round = 0;
+      for (;;) {
+        unsigned stale = 0;
+#pragma unroll
+        for (int u = 0; u < UMAX; ++u)
+          if (base + u * NT < nf4 && !ready4(v[u])) stale |= 1u << u;
+        if (stale == 0u) break;
+        if (!w.still_ok(spins)) return false;
+        w.pause(round);
+#pragma unroll
+        for (int u = 0; u < UMAX; ++u)
+          if ((stale >> u) & 1u) v[u] = ld_relaxed_f4(reinterpret_cast<const float*>(src + base + u * NT));
+      }
+    }
+    b = b0;
+    g = g0;
+#pragma unroll
+    for (int u = 0; u < UMAX; ++u) {
+      if (base + u * NT < nf4) {
+        float* blk = hs + b * H + ((g >> 5) << 7);
+        blk[pw[u] & 31u] = v[u].x;
+        blk[32 + ((pw[u] >> 8) & 31u)] = v[u].y;
+        blk[64 + ((pw[u] >> 16) & 31u)] = v[u].z;
+        blk[96 + ((pw[u] >> 24) & 31u)] = v[u].w;
+      }
+      g += NT;
+      while (g >= ng) {
+        g -= ng;
+        ++b;
+      }
+    }
+  }
+  return true;
+}
+
+// stage_rows_narrow into the same placement (the ablation's 32-bit staging).
+template <int UMAX>
+__device__ __forceinline__ bool stage_rows_narrow_placed(const float* hprev, bool poll, int H,
+                                                         int b_start, int nb, float* hs,
+                                                         Waiter& w, const uint32_t* place) {
+  const int NT = blockDim.x, tid = threadIdx.x;
+  const int n = nb * H;
+  const float* src = hprev + (size_t)b_start * H;
+  for (int base = tid; base < n; base += UMAX * NT) {
+    float v[UMAX];
+#pragma unroll
+    for (int u = 0; u < UMAX; ++u) {
+      const int i = base + u * NT;
+      v[u] = 0.f;
+      if (i < n && hprev != nullptr) v[u] = poll ? ld_relaxed_f(src + i) : __ldg(src + i);
+    }
+    if (poll) {
+      uint32_t spins = 0, round = 0;
+      for (;;) {
+        unsigned stale = 0;
+#pragma unroll
+        for (int u = 0; u < UMAX; ++u)
+          if (base + u * NT < n && is_sentinel(v[u])) stale |= 1u << u;
+        if (stale == 0u) break;
+        if (!w.still_ok(spins)) return false;
+        w.pause(round);
+#pragma unroll
+        for (int u = 0; u < UMAX; ++u)
+          if ((stale >> u) & 1u) v[u] = ld_relaxed_f(src + base + u * NT);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UMAX; ++u) {
+      const int i = base + u * NT;
+      if (i < n) {
+        const int b = i / H, c = i - b * H, g = c >> 2, j = c & 3;
+        const uint32_t pw = __ldg(place + g);
+        hs[(size_t)b * H + ((g >> 5) << 7) + 32 * j + ((pw >> (8 * j)) & 31u)] = v[u];
+      }
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Sparse row-balanced kernel.  Thread (r, s) = (tid / TPR, tid % TPR) owns
+// ept entries of row r, packed 4 to a uint4 (wide loads); entry = fp16 value
+// | index << 16, padding entries have value 0.  The host places entries so
+// that the 32 lanes of a warp gather from different banks in each slot.  The
+// first kRegQ uint4 groups live in registers, the rest in smem.  The group's
+// h_{t-1} columns are staged in smem as [b][H] per batch pass of BG columns
+// (double-buffered when it fits, so one CTA barrier per pass); the index is
+// the column's position in that staging, which is the column itself or, with
+// a placement table, this CTA's bank-balancing order of the columns.
+// ---------------------------------------------------------------------------
+template <int TPR, int BG, bool PLACED>
+__global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const SparseRecurArgs a) {
+  extern __shared__ __align__(16) float smem_f[];
+  __shared__ int s_abort;
+  constexpr int UMAX = (BG >= 16) ? 4 : (BG == 8 ? 8 : 12);
+  const RecurCommon& c = a.c;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int NT = blockDim.x;
+  const int cta = blockIdx.x;
+  const int H = c.H, B = c.B, R = c.R;
+  const Place pl = place_of(c);
+  const int q4 = a.ept >> 2;
+  const int nbuf = a.dbuf ? 2 : 1;
+
+  // smem: packed weights (R*q4*TPR uint4), then nbuf staging buffers of BG*H floats
+  uint4* Ws = reinterpret_cast<uint4*>(smem_f);
+  const int hs_base = R * q4 * TPR * 4;  // float index of the first staging buffer
+
+  {
+    const size_t n16 = (size_t)R * q4 * TPR;
+    const uint4* src = reinterpret_cast<const uint4*>(a.Wpk) + (size_t)pl.lc * n16;
+    for (size_t i = tid; i < n16; i += NT) Ws[i] = __ldg(src + i);
+  }
+  if (tid == 0) s_abort = 0;
+  __syncthreads();
+
+  const int r = tid / TPR, s = tid % TPR;
+  const bool has_row = r < pl.rows;
+  const int row = pl.row0 + r;
+  constexpr int REGQ = (BG >= 16) ? 2 : kRegQ;
+  uint4 wr[REGQ];
+#pragma unroll
+  for (int i = 0; i < REGQ; ++i) {
+    wr[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (has_row && i < q4) wr[i] = Ws[((size_t)r * q4 + i) * TPR + s];
+  }
+  // output slots of this lane after the reduce-scatter
+  constexpr int NOUT = (BG >= TPR) ? BG / TPR : 1;
+  constexpr int REP = (BG >= TPR) ? 1 : TPR / BG;  // lanes holding copies of one sum
+  const int gl = lane % TPR;
+
+  Waiter w;
+  w.status = c.status;
+  w.timeout_ns = c.timeout_ns;
+  w.backoff = c.poll_backoff;
+  int seq = 0;
+  for (int t = 0; t < c.T; ++t) {
+    const int tt = c.reverse ? c.T - 1 - t : t;  // time index of this step
+    const float* hprev = (t == 0) ? c.h0 : c.y + (size_t)(c.reverse ? tt + 1 : tt - 1) * B * H;
+    const float* Pt = c.P + (size_t)tt * B * H;
+    float* yt = c.y + (size_t)tt * B * H;
+    w.new_step();
+    for (int bs = pl.b_lo; bs < pl.b_hi; bs += BG, ++seq) {
+      const int nbg = min(BG, pl.b_hi - bs);
+      const int hs_off = hs_base + ((nbuf == 2) ? (seq & 1) : 0) * H * BG;
+      // P for this lane's outputs, fetched before the wait
+      float pv[NOUT];
+      bool owns = false;
+#pragma unroll
+      for (int i = 0; i < NOUT; ++i) {
+        pv[i] = 0.f;
+        const int idx = (BG >= TPR) ? gl * NOUT + i : gl / REP;
+        const bool mine = (gl % REP) == 0;
+        if (has_row && mine && idx < nbg) {
+          pv[i] = ld_nc_pinned(Pt + (size_t)(bs + idx) * H + row);
+          owns = true;
+        }
+      }
+      if (t > 0 && bs == pl.b_lo) spin_cycles(c.poll_delay);
+      // the placed staging keeps fewer loads in flight (its table words take
+      // registers of their own)
+      constexpr int UPL = UMAX > 4 ? UMAX / 2 : UMAX;
+      const bool ok =
+          PLACED ? (a.narrow ? stage_rows_narrow_placed<UPL>(hprev, t > 0, H, bs, nbg,
+                                                             smem_f + hs_off, w,
+                                                             a.place + (size_t)pl.lc * (H >> 2))
+                             : stage_rows_placed<UPL>(hprev, t > 0, H, bs, nbg, smem_f + hs_off,
+                                                      w, a.place + (size_t)pl.lc * (H >> 2)))
+                 : (a.narrow ? stage_rows_narrow<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w)
+                             : stage_rows<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w));
+      if (!ok) {
+        report_timeout(c.status, t, cta);
+        s_abort = 1;
+      }
+      __syncthreads();
+      if (s_abort) return;
+
+      // gather-multiply: entry = fp16 value (low half) | column << 16.  Batch
+      // columns past nbg read a zero-filled or stale row and are never stored.
+      float acc[BG];
+#pragma unroll
+      for (int i = 0; i < BG; ++i) acc[i] = 0.f;
+      if (has_row) {
+        // groups past q4 hold zero words (value 0 at column 0): no guard needed
+#pragma unroll
+        for (int i = 0; i < REGQ; ++i) {
+          const uint32_t ws4[4] = {wr[i].x, wr[i].y, wr[i].z, wr[i].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float val = __half2float(__ushort_as_half((unsigned short)(ws4[q] & 0xffffu)));
+            const int hi = hs_off + (int)(ws4[q] >> 16);
+#pragma unroll
+            for (int b = 0; b < BG; ++b) acc[b] = fmaf(val, smem_f[hi + b * H], acc[b]);
+          }
+        }
+        for (int i = REGQ; i < q4; ++i) {
+          const uint4 e = Ws[((size_t)r * q4 + i) * TPR + s];
+          const uint32_t ws4[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float val = __half2float(__ushort_as_half((unsigned short)(ws4[q] & 0xffffu)));
+            const int hi = hs_off + (int)(ws4[q] >> 16);
+#pragma unroll
+            for (int b = 0; b < BG; ++b) acc[b] = fmaf(val, smem_f[hi + b * H], acc[b]);
+          }
+        }
+      }
+      if (TPR > 1) seg_reduce_scatter<BG, TPR>(acc, lane);
+      if (owns && !(cta == c.drop_cta && t == c.drop_step)) {
+#pragma unroll
+        for (int i = 0; i < NOUT; ++i) {
+          const int idx = (BG >= TPR) ? gl * NOUT + i : gl / REP;
+          if (idx < nbg) {
+            const float s = acc[i] + pv[i];
+            st_relaxed_f(yt + (size_t)(bs + idx) * H + row,
+                         c.p_masked ? (__float_as_uint(pv[i]) == kMaskedMarker ? 0.f : s)
+                                    : relu(s));
+          }
+        }
+      }
+      if (nbuf == 1) __syncthreads();  // hs is overwritten by the next staging
+    }
+    if (c.sync_mode == 1) {
+      grid_barrier(c, t, w, &s_abort);
+      if (s_abort) return;
+    }
+  }
+}
+
+}  // namespace
+
+// Launch recur_sparse_kernel<tpr, bgroup, PLACED> for the plan in a.
+template <bool PLACED>
+cudaError_t launch_recur_sparse_impl(const SparseRecurArgs& a, cudaStream_t s) {
+  void* args[] = {const_cast<SparseRecurArgs*>(&a)};
+  const int g = a.c.n_cta, nt = a.c.nthreads;
+  const size_t sm = a.c.smem;
+  const int bg = a.bgroup;
+#define PRNN_SPARSE_CASE(T_, BG_) \
+  if (a.tpr == T_ && bg == BG_)   \
+    return coop_launch(recur_sparse_kernel<T_, BG_, PLACED>, g, nt, sm, s, args);
+#define PRNN_SPARSE_ROW(T_)                                                           \
+  PRNN_SPARSE_CASE(T_, 1) PRNN_SPARSE_CASE(T_, 2) PRNN_SPARSE_CASE(T_, 4) PRNN_SPARSE_CASE(T_, 8) \
+  PRNN_SPARSE_CASE(T_, 16) PRNN_SPARSE_CASE(T_, 32)
+  PRNN_SPARSE_ROW(1) PRNN_SPARSE_ROW(2) PRNN_SPARSE_ROW(4) PRNN_SPARSE_ROW(8)
+  PRNN_SPARSE_ROW(16) PRNN_SPARSE_ROW(32)
+#undef PRNN_SPARSE_ROW
+#undef PRNN_SPARSE_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace prnn

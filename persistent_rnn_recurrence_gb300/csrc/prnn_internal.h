@@ -172,8 +172,12 @@ struct SparseRecurArgs {
   int bgroup;            // batch columns staged per pass: 1, 2, 4, 8, 16 or 32
   int dbuf;              // 1: two h staging buffers (one CTA barrier per pass)
   int narrow;            // 1: stage h with 32-bit loads (ablation); 0: 128-bit
+  const uint32_t* place; // [cpg][H/4] staging order of h (H % 128 == 0), or null:
+                         // column c of group g = c/4 is staged at
+                         // 128*(g/32) + 32*(c%4) + byte (c%4) of place[g]
 };
 cudaError_t launch_recur_sparse(const SparseRecurArgs& a, cudaStream_t s);
+cudaError_t launch_recur_sparse_placed(const SparseRecurArgs& a, cudaStream_t s);
 size_t recur_sparse_smem(int H, int R, int ept, int tpr, int bgroup, bool dbuf);
 
 cudaError_t launch_sync_probe(const RecurCommon& c, int bgroup, cudaStream_t s);
@@ -185,9 +189,15 @@ struct PackStats {
   int cap = 0;               // max lanes per bank residue per slot that was needed
   long long conflicts = 0;   // lane-slots that share a bank with an earlier lane
 };
+// place_out (optional): per-CTA staging order of h, [n_cta][H/4] words, one
+// per group of 4 columns, byte j = bank of column 4g+j within its class; the
+// packed index field is then the staged position (see pack.cu).  Left empty
+// when the layer keeps column order (not bank-aware, or H % 128 != 0).
 int pack_sparse_rows(int H, int k, int R, int n_cta, int tpr, const uint16_t* vals,
                      const uint16_t* cols, std::vector<uint32_t>& out_packed, PackStats* stats,
-                     int max_ept = 1 << 30, bool bank_aware = true);
+                     int max_ept = 1 << 30, bool bank_aware = true,
+                     std::vector<uint32_t>* place_out = nullptr);
+bool staging_placement_supported(int H);
 size_t sync_probe_smem(int H, int bgroup);
 
 // ---- per-step path ------------------------------------------------------

@@ -28,14 +28,15 @@ PRNN_ALGO_PERSISTENT, PRNN_ALGO_PER_STEP = 0, 1
 PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA, \
     PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION, PRNN_OPT_CTA_GROUPS, \
     PRNN_OPT_WIDE_LOADS, PRNN_OPT_BANK_AWARE, PRNN_OPT_POLL_DELAY_NS, \
-    PRNN_OPT_POLL_BACKOFF_NS, PRNN_OPT_RECURRENT_TC = range(12)
+    PRNN_OPT_POLL_BACKOFF_NS, PRNN_OPT_RECURRENT_TC, PRNN_OPT_STAGED_ORDER = range(13)
 
 PRNN_STACK_WAVEFRONT, PRNN_STACK_LAYERWISE = 0, 1
 
 EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
            "prnn_forward", "prnn_destroy", "prnn_get_status", "prnn_status_string",
            "prnn_set_option", "prnn_get_info", "prnn_get_timing", "prnn_probe_sync_floor",
-           "prnn_pack_sparse_host", "prnn_forward_dense_noalloc", "prnn_set_weights_csr",
+           "prnn_pack_sparse_host", "prnn_pack_sparse_host_placed", "prnn_forward_dense_noalloc",
+           "prnn_set_weights_csr",
            "prnn_stack_create", "prnn_stack_set_layer", "prnn_stack_forward",
            "prnn_stack_get_status", "prnn_stack_set_option", "prnn_stack_get_timing",
            "prnn_stack_get_info", "prnn_stack_destroy", "prnn_backward"]
@@ -47,7 +48,8 @@ class prnn_info_t(ctypes.Structure):
         "k_padded", "sm_count", "n_cta", "rows_per_cta", "threads_per_cta",
         "threads_per_row", "projection_tensor_cores", "sparse_bank_cap", "cta_groups")] + [
         ("smem_bytes", ctypes.c_size_t), ("onchip_weight_bytes", ctypes.c_size_t),
-        ("nnz", ctypes.c_size_t), ("recurrent_tensor_cores", ctypes.c_int)]
+        ("nnz", ctypes.c_size_t), ("recurrent_tensor_cores", ctypes.c_int),
+        ("sparse_staged_order", ctypes.c_int)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -80,6 +82,9 @@ _sig = {
     "prnn_probe_sync_floor": ([_P, _I, _I, _P, _P], _I),
     "prnn_pack_sparse_host": ([_I, _I, _I, _I, _I, _P, _P, _P, ctypes.c_size_t,
                                ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
+    "prnn_pack_sparse_host_placed": ([_I, _I, _I, _I, _I, _P, _P, _P, ctypes.c_size_t, _P,
+                                      ctypes.c_size_t, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                                      ctypes.POINTER(_I)], _I),
     "prnn_forward_dense_noalloc": ([_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
     "prnn_set_weights_csr": ([_P, _P, _I, _P, _P, _P, _P, _P], _I),
     "prnn_stack_create": ([ctypes.POINTER(_P), _I, _I, _I, _I, _I, _I], _I),
@@ -186,6 +191,30 @@ def prnn_get_timing(h: int):
     a, b = ctypes.c_float(), ctypes.c_float()
     _check(_lib.prnn_get_timing(h, ctypes.byref(a), ctypes.byref(b)), "prnn_get_timing")
     return a.value, b.value
+
+
+def prnn_pack_sparse_host_placed(hidden, k, n_cta, rows_per_cta, threads_per_row, vals, cols):
+    """Host-only packing with the per-CTA staging order of h: returns
+    (packed[n_cta, R, ept/4, tpr, 4] uint32, place[n_cta, hidden/4] uint32 or
+    None when columns stay in order, ept, bank_cap)."""
+    import numpy as np
+    vals = np.ascontiguousarray(vals).view(np.uint16)
+    cols = np.ascontiguousarray(cols, dtype=np.uint16)
+    ept, cap, placed = _I(), _I(), _I()
+    st = _lib.prnn_pack_sparse_host_placed(hidden, k, n_cta, rows_per_cta, threads_per_row,
+                                           vals.ctypes.data, cols.ctypes.data, None, 0, None, 0,
+                                           ctypes.byref(ept), ctypes.byref(cap),
+                                           ctypes.byref(placed))
+    if st != PRNN_ERR_INVALID_ARG or ept.value <= 0:
+        _check(st if st != PRNN_OK else PRNN_ERR_INVALID_ARG, "prnn_pack_sparse_host_placed")
+    out = np.zeros((n_cta, rows_per_cta, ept.value // 4, threads_per_row, 4), dtype=np.uint32)
+    place = np.zeros((n_cta, hidden // 4), dtype=np.uint32) if placed.value else None
+    _check(_lib.prnn_pack_sparse_host_placed(
+        hidden, k, n_cta, rows_per_cta, threads_per_row, vals.ctypes.data, cols.ctypes.data,
+        out.ctypes.data, out.size, None if place is None else place.ctypes.data,
+        0 if place is None else place.size, ctypes.byref(ept), ctypes.byref(cap),
+        ctypes.byref(placed)), "prnn_pack_sparse_host_placed")
+    return out, place, ept.value, cap.value
 
 
 def prnn_probe_sync_floor(h: int, T: int, B: int, y, stream=None) -> None:

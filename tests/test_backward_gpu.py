@@ -34,9 +34,16 @@ def env():
     return torch, prnn, oracle.default()
 
 
-def run(env, p, dy, options=None):
+def run(env, p, dy, options=None, pre_options=None):
+    """pre_options are set before the weights (options that act at set_weights)."""
     torch, prnn, _ = env
-    lay = prnn.Layer.from_problem(p)
+    if pre_options:
+        lay = prnn.Layer(p.H, p.I, max(1, p.B), p.wdtype, "persistent")
+        for k, v in pre_options.items():
+            lay.set_option(k, v)
+        lay.set_problem_weights(p)
+    else:
+        lay = prnn.Layer.from_problem(p)
     try:
         for k, v in (options or {}).items():
             lay.set_option(k, v)
@@ -247,12 +254,15 @@ def dyadic_sparse_problem(seed, H, I, B, T, k, csr=False):
     return p, q(T, B, H)
 
 
-@pytest.mark.parametrize("csr", [False, True])
+@pytest.mark.parametrize("csr,staged", [(False, 0), (True, 0), (False, 1), (True, 1)])
 @pytest.mark.parametrize("shape", [dict(H=64, I=32, B=3, T=6, k=3), dict(H=512, I=96, B=4, T=5, k=3)])
-def test_sparse_backward_exact_problems(env, csr, shape):
+def test_sparse_backward_exact_problems(env, csr, staged, shape):
+    """staged = 1: the forward and the reverse recurrence stage h / delta in
+    each CTA's bank-balancing order (H = 512; H = 64 keeps column order)."""
     p, dy = dyadic_sparse_problem(800 + shape["H"], csr=csr, **shape)
     o = env[2]
-    y, g = run(env, p, dy.astype(np.float32), {env[1].PRNN_OPT_PROJECTION: 1})
+    y, g = run(env, p, dy.astype(np.float32), {env[1].PRNN_OPT_PROJECTION: 1},
+               pre_options={env[1].PRNN_OPT_STAGED_ORDER: staged})
     assert np.array_equal(y, o.forward(p)), "forward not exact: masks could differ"
     ref = o.backward(p, dy)
     assert rel_err(g["dWh"], ref["dvals"].ravel()) <= 1e-6
@@ -287,13 +297,15 @@ def check_sparse_by_properties(env, p, dy, y, g, n_samples=300):
         assert rel_err(g[k], ref) <= product_tol(p, k), (k, rel_err(g[k], ref))
 
 
-@pytest.mark.parametrize("name,T", [("sparse_f16_h1792_d10_b4_t256", 32),
-                                    ("sparse_f16_h1792_d10_b4_t256", None),
-                                    ("sparse_f16_h5760_d1_b4_t256", 16)])
-def test_sparse_backward_properties(env, name, T):
+@pytest.mark.parametrize("name,T,staged", [("sparse_f16_h1792_d10_b4_t256", 32, 0),
+                                           ("sparse_f16_h1792_d10_b4_t256", None, 0),
+                                           ("sparse_f16_h5760_d1_b4_t256", 16, 0),
+                                           ("sparse_f16_h1792_d10_b4_t256", 32, 1),
+                                           ("sparse_f16_h5760_d5_b4_t256", 8, 1)])
+def test_sparse_backward_properties(env, name, T, staged):
     p = synth.named_problem(name, T=T)
     dy = np.random.default_rng(705).normal(size=(p.T, p.B, p.H)).astype(np.float32)
-    y, g = run(env, p, dy)
+    y, g = run(env, p, dy, pre_options={env[1].PRNN_OPT_STAGED_ORDER: staged})
     check_sparse_by_properties(env, p, dy.astype(np.float64), y, g)
 
 

@@ -88,3 +88,88 @@ def test_pack_rejects_bad_indices(prnn):
         prnn.prnn_pack_sparse_host(64, 8, 64, 1, 3, p.vals, p.cols)
     with pytest.raises(prnn.PrnnError):                      # too few rows
         prnn.prnn_pack_sparse_host(64, 8, 10, 1, 8, p.vals, p.cols)
+
+
+PLACED_CASES = [  # (H, k, tpr, R, n_cta): the benchmarked layouts, full-slot and ragged ones
+    (1792, 179, 8, 48, 38), (5760, 57, 8, 152, 38), (5760, 288, 8, 152, 38),
+    (2304, 576, 16, 61, 38), (1152, 115, 8, 31, 38), (128, 16, 4, 8, 16), (300, 17, 4, 2, 150),
+]
+
+
+def staged_positions(place, H):
+    """Position of every column under one CTA's table, restated from the
+    documented rule: column 4g+j goes to 128*(g//32) + 32*j + byte j of place[g]."""
+    g = np.arange(H) // 4
+    j = np.arange(H) % 4
+    byte = (place[g].astype(np.int64) >> (8 * j)) & 0xFF
+    return 128 * (g // 32) + 32 * j + byte
+
+
+@pytest.mark.parametrize("H,k,tpr,R,n", PLACED_CASES)
+def test_placed_pack_keeps_rows_and_balances_banks(prnn, H, k, tpr, R, n):
+    p = synth.make_problem(H=H, B=1, T=1, k=k, seed=H + 7 * k)
+    out, place, ept, cap = prnn.prnn_pack_sparse_host_placed(H, k, n, R, tpr, p.vals, p.cols)
+    if H % 128:
+        # column order: exactly the unplaced packing
+        ref, ept0, cap0 = prnn.prnn_pack_sparse_host(H, k, n, R, tpr, p.vals, p.cols)
+        assert place is None and ept == ept0 and np.array_equal(out, ref)
+        return
+    assert place.shape == (n, H // 4)
+    e = unpack(out, ept)
+    vbits = (e & 0xFFFF).astype(np.uint16)
+    idx = (e >> 16).astype(np.int64)
+    rpw = 32 // tpr
+    for c in range(n):
+        # every class (block of 128 columns, component j) is a permutation of the banks
+        for blk in range(H // 128):
+            for j in range(4):
+                banks = (place[c, 32 * blk:32 * blk + 32].astype(np.int64) >> (8 * j)) & 0xFF
+                assert sorted(banks.tolist()) == list(range(32)), (c, blk, j)
+        pos = staged_positions(place[c], H)
+        assert sorted(pos.tolist()) == list(range(H))
+        col_at = np.empty(H, dtype=np.int64)
+        col_at[pos] = np.arange(H)
+        for r in range(R):
+            g = c * R + r
+            if g >= H:
+                assert (vbits[c, r] == 0).all()
+                continue
+            fv, fi = vbits[c, r].ravel(), idx[c, r].ravel()
+            pad = fv == 0
+            want = sorted((cc, v) for cc, v in zip(p.cols[g].astype(np.int64).tolist(),
+                                                    p.vals[g].view(np.uint16).tolist()) if v != 0)
+            got = sorted(zip(col_at[fi[~pad]].tolist(), fv[~pad].tolist()))
+            assert got == want, (c, r)
+        # gather slots: the lanes of a warp that own a row use distinct banks
+        for w in range((R + rpw - 1) // rpw):
+            rows = [r for r in range(w * rpw, min(R, w * rpw + rpw)) if c * R + r < H]
+            if not rows:
+                continue
+            blkidx = idx[c, rows].reshape(len(rows) * tpr, ept)
+            worst = max(np.bincount(blkidx[:, s] % 32, minlength=32).max() for s in range(ept))
+            assert worst <= cap
+    if (H, k) in ((1792, 179), (5760, 57), (5760, 288), (2304, 576)):
+        assert cap == 1
+
+
+def test_placed_pack_reproduces_the_product(prnn):
+    """Emulates one step of the kernel on the CPU: stage h by the documented
+    placement rule, gather every packed entry at its index, sum per row, and
+    compare with Wh @ h from the unpacked rows."""
+    H, k, tpr, R, n = 1792, 179, 8, 48, 38
+    p = synth.make_problem(H=H, B=1, T=1, k=k, seed=11)
+    out, place, ept, cap = prnn.prnn_pack_sparse_host_placed(H, k, n, R, tpr, p.vals, p.cols)
+    h = np.random.default_rng(5).standard_normal(H)
+    want = np.array([np.dot(p.vals[r].astype(np.float64), h[p.cols[r].astype(np.int64)])
+                     for r in range(H)])
+    e = unpack(out, ept)
+    got = np.zeros(H)
+    for c in range(n):
+        hs = np.full(H, np.nan)
+        hs[staged_positions(place[c], H)] = h
+        assert not np.isnan(hs).any()
+        vals = (e[c] & 0xFFFF).astype(np.uint16).view(np.float16).astype(np.float64)
+        prod = vals * hs[(e[c] >> 16).astype(np.int64)]
+        rows = min(R, H - c * R)
+        got[c * R:c * R + rows] = prod[:rows].reshape(rows, -1).sum(1)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)

@@ -427,6 +427,38 @@ def test_poll_delay_changes_timing_not_results(env, spec):
     lay.close()
 
 
+@pytest.mark.parametrize("spec", [dict(H=1792, B=4, T=24, k=179),
+                                  dict(H=1152, B=9, T=10, k=115, h0_std=0.5),
+                                  dict(H=256, B=32, T=6, k=40),
+                                  dict(H=300, B=3, T=8, k=17)])
+def test_staged_order_matches_column_order(env, spec):
+    """Each CTA staging h_{t-1} in its own bank-balancing order (opt-in)
+    changes where the gathers read, not what they read: both orders match the
+    oracle, and ragged H (not a multiple of 128) keeps column order."""
+    torch, prnn, o = env
+    p = synth.make_problem(seed=81, **spec)
+    ref = o.forward(p)
+    y_on, info_on = run_gpu(env, p, pre_options={prnn.PRNN_OPT_STAGED_ORDER: 1})
+    y_off, info_off = run_gpu(env, p)  # column order is the default
+    check(y_on, ref, "f16", "staged order")
+    check(y_off, ref, "f16", "column order")
+    assert info_on["sparse_staged_order"] == (1 if p.H % 128 == 0 else 0)
+    assert info_off["sparse_staged_order"] == 0
+    if p.H % 128 == 0:
+        assert info_on["sparse_bank_cap"] <= info_off["sparse_bank_cap"]
+    # the same through the narrow (32-bit) staging of the ablation
+    y_nar, _ = run_gpu(env, p, options={prnn.PRNN_OPT_WIDE_LOADS: 0},
+                       pre_options={prnn.PRNN_OPT_STAGED_ORDER: 1})
+    check(y_nar, ref, "f16", "staged order, narrow staging")
+    lay = prnn.Layer.from_problem(p)
+    try:
+        with pytest.raises(prnn.PrnnError) as e:
+            lay.set_option(prnn.PRNN_OPT_STAGED_ORDER, 2)
+        assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    finally:
+        lay.close()
+
+
 # --- tensor-core dense recurrence (wide batches) --------------------------------------
 @pytest.mark.parametrize("spec,force", [(dict(H=1152, B=16, T=64, wdtype="f16"), 0),
                                         (dict(H=2304, B=32, T=24, wdtype="f16", h0_std=0.2), 0),
