@@ -466,29 +466,45 @@ def measure_extras(args, p, lay, x, h0, y, flush, stream, dev, world):
     from persistent_rnn_recurrence_gb300 import prnn
     out = {}
     K = max(3, min(args.steps, 10))
-    # end to end through the public API from pinned host memory
+    # end to end from pinned host memory: prnn_forward_host (x and h0 copied in,
+    # y written to the host by the recurrent kernel as it is published), and for
+    # comparison host copies around prnn_forward on device buffers
     xh = torch.from_numpy(p.x).pin_memory()
+    h0h = None if h0 is None else h0.cpu().pin_memory()
     yh = torch.empty((p.T, p.B, p.H), dtype=torch.float32).pin_memory()
     xd = torch.empty_like(x)
-    for _ in range(2):
+
+    def via_host_call():
+        prnn.prnn_forward_host(lay.h, p.T, p.B, xh, h0h, yh, stream)
+
+    def via_copies():
         xd.copy_(xh, non_blocking=True)
         prnn.prnn_forward(lay.h, p.T, p.B, xd, h0, y, stream)
         yh.copy_(y, non_blocking=True)
-    torch.cuda.synchronize()
-    ms = []
-    for _ in range(K):
-        flush.fill_(1.0)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        xd.copy_(xh, non_blocking=True)
-        prnn.prnn_forward(lay.h, p.T, p.B, xd, h0, y, stream)
-        yh.copy_(y, non_blocking=True)
-        b.record(stream)
-        b.synchronize()
-        ms.append(a.elapsed_time(b))
-    e2e_s = max_over_ranks(sum(ms) / 1e3, world, dev)
-    out["e2e"] = {"value": world * p.T * K / e2e_s, "unit": "timesteps/s",
-                  "h2d_bytes_per_step": xh.numel() * 4, "d2h_bytes_per_step": yh.numel() * 4}
+
+    def time_e2e(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(K):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return world * p.T * K / max_over_ranks(sum(ms) / 1e3, world, dev)
+
+    h2d = (xh.numel() + (0 if h0h is None else h0h.numel())) * 4
+    out["e2e"] = {"value": time_e2e(via_host_call), "unit": "timesteps/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": yh.numel() * 4,
+                  "call": "prnn_forward_host on pinned host buffers"}
+    out["e2e_device_call_with_copies"] = {
+        "value": time_e2e(via_copies), "unit": "timesteps/s", "h2d_bytes_per_step": h2d,
+        "d2h_bytes_per_step": yh.numel() * 4,
+        "call": "H2D copy, prnn_forward on device buffers, D2H copy"}
     # step-synchronisation floor of the same grid
     if args.algo == "persistent":
         ys = torch.empty_like(y)

@@ -168,6 +168,25 @@ prnn_status_t prnn_set_weights_csr(prnn_t h, const void* Wx, int nnz, const int3
 prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* h0,
                            float* y, void* stream);
 
+/*
+ * The same forward pass on HOST buffers: x [T][B][I], h0 [B][H] (NULL =
+ * zeros) and y [T][B][H] are fp32 in page-locked host memory that the device
+ * can address (cudaHostAlloc / cudaMallocHost, or cudaHostRegister'ed), each
+ * float-aligned and holding at least the elements its shape says; y must not
+ * overlap x or h0.  x and h0 are copied to device workspaces owned by the
+ * handle (grown on demand, freed by prnn_destroy).  The persistent CUDA-core
+ * recurrent kernels write every output into y itself, over the host link, as
+ * they publish it, so the result needs no separate copy back; the per-step
+ * path and the tcgen05 dense recurrence copy y back after the recurrence.
+ * Asynchronous on `stream`: x, h0 and y belong to the library until the stream
+ * is synchronized.  Results are bit-identical to prnn_forward on device copies
+ * of the same inputs.  Errors: PRNN_ERR_INVALID_ARG for a pointer that CUDA
+ * does not report as page-locked host memory (pageable or device memory),
+ * otherwise as prnn_forward.
+ */
+prnn_status_t prnn_forward_host(prnn_t h, int T, int B, const float* x, const float* h0,
+                                float* y, void* stream);
+
 /* Release everything the handle owns.  NULL is accepted. */
 prnn_status_t prnn_destroy(prnn_t h);
 

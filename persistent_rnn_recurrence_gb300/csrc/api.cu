@@ -71,6 +71,11 @@ struct prnn_handle {
   void* Wstep = nullptr;     // per-step layout of the recurrent weights
   float* P = nullptr;
   size_t P_cap = 0;
+  // device copies of x, h0 and y for prnn_forward_host
+  float* hx = nullptr;
+  float* hh0 = nullptr;
+  float* hy = nullptr;
+  size_t hx_cap = 0, hh0_cap = 0, hy_cap = 0;
   __half_raw* x16 = nullptr;
   size_t x16_cap = 0;
   int* status = nullptr;     // device int[4]
@@ -316,6 +321,33 @@ cudaError_t ensure_P(prnn_handle* h, size_t n) {
   }
   h->P_cap = n;
   return cudaSuccess;
+}
+
+// Grow a float device buffer to at least n elements (contents not kept).
+cudaError_t ensure_f32(float** p, size_t* cap, size_t n) {
+  if (n <= *cap) return cudaSuccess;
+  free_dev(*p);
+  *cap = 0;
+  cudaError_t e = cudaMalloc((void**)p, n * sizeof(float));
+  if (e == cudaSuccess) *cap = n;
+  return e;
+}
+
+// The device address of page-locked host memory, or nullptr for anything
+// else (pageable or device memory, or a pointer CUDA does not know).
+const void* mapped_host(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost) return nullptr;
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, const_cast<void*>(p), 0) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return d;
 }
 
 cudaError_t ensure_x16(prnn_handle* h, size_t n) {
@@ -634,6 +666,9 @@ prnn_status_t prnn_destroy(prnn_t h) {
   free_weights(h);
   free_dev(h->P);
   free_dev(h->x16);
+  free_dev(h->hx);
+  free_dev(h->hh0);
+  free_dev(h->hy);
   free_dev(h->tws);
   free_dev(h->gws16);
   free_dev(h->status);
@@ -834,19 +869,18 @@ prnn_status_t prnn_set_weights_csr(prnn_t h, const void* Wx, int nnz, const int3
   return install_sparse(h, Wx, bias, hv, hc, kmax, pos);
 }
 
-prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* h0, float* y,
-                           void* stream) {
-  if (!h) return PRNN_ERR_INVALID_ARG;
-  if (h->sticky_timeout) return PRNN_ERR_TIMEOUT;
-  if (!h->weights_set) return PRNN_ERR_NOT_READY;
-  if (T < 0 || B < 0 || B > h->maxB) return PRNN_ERR_INVALID_ARG;
-  if (T == 0 || B == 0) return PRNN_OK;
-  if (!x || !y) return PRNN_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y) || (h0 && !aligned16(h0))) return PRNN_ERR_INVALID_ARG;
+// Whether the recurrent kernel prnn_forward would launch can also write every
+// output into a second buffer (the persistent CUDA-core kernels can).
+static bool recurrence_mirrors(const prnn_t h) {
+  return h->algo == PRNN_ALGO_PERSISTENT && (h->sparse || !(h->rtc && h->sync_mode == 0));
+}
+
+// The forward on device buffers; y_mirror (nullptr, or a device-addressable
+// [T][B][H] buffer; only when recurrence_mirrors) receives a copy of every
+// output as the recurrence publishes it.  Arguments are checked by the callers.
+static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const float* h0,
+                                  float* y, float* y_mirror, cudaStream_t s) {
   const size_t ny = (size_t)T * B * h->H;
-  if (overlaps(y, ny * 4, x, (size_t)T * B * h->I * 4)) return PRNN_ERR_INVALID_ARG;
-  if (h0 && overlaps(y, ny * 4, h0, (size_t)B * h->H * 4)) return PRNN_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   PRNN_TRY(ensure_P(h, ny));
   const bool persistent = h->algo == PRNN_ALGO_PERSISTENT;
   if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[0], s));
@@ -867,6 +901,7 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
   // 2. recurrence
   if (persistent) {
     RecurCommon c = common_args(h, T, B, h0, y);
+    c.y_mirror = y_mirror;
     if (h->sync_mode == 1) PRNN_TRY(cudaMemsetAsync(h->bar, 0, sizeof(unsigned), s));
     if (h->sparse) {
       SparseRecurArgs a{};
@@ -951,6 +986,54 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
     PRNN_TRY(cudaEventRecord(h->ev[2], s));
     h->ev_valid = true;
   }
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* h0, float* y,
+                           void* stream) {
+  if (!h) return PRNN_ERR_INVALID_ARG;
+  if (h->sticky_timeout) return PRNN_ERR_TIMEOUT;
+  if (!h->weights_set) return PRNN_ERR_NOT_READY;
+  if (T < 0 || B < 0 || B > h->maxB) return PRNN_ERR_INVALID_ARG;
+  if (T == 0 || B == 0) return PRNN_OK;
+  if (!x || !y) return PRNN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || (h0 && !aligned16(h0))) return PRNN_ERR_INVALID_ARG;
+  const size_t ny = (size_t)T * B * h->H;
+  if (overlaps(y, ny * 4, x, (size_t)T * B * h->I * 4)) return PRNN_ERR_INVALID_ARG;
+  if (h0 && overlaps(y, ny * 4, h0, (size_t)B * h->H * 4)) return PRNN_ERR_INVALID_ARG;
+  return forward_impl(h, T, B, x, h0, y, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+prnn_status_t prnn_forward_host(prnn_t h, int T, int B, const float* x, const float* h0,
+                                float* y, void* stream) {
+  if (!h) return PRNN_ERR_INVALID_ARG;
+  if (h->sticky_timeout) return PRNN_ERR_TIMEOUT;
+  if (!h->weights_set) return PRNN_ERR_NOT_READY;
+  if (T < 0 || B < 0 || B > h->maxB) return PRNN_ERR_INVALID_ARG;
+  if (T == 0 || B == 0) return PRNN_OK;
+  if (!x || !y) return PRNN_ERR_INVALID_ARG;
+  const size_t nx = (size_t)T * B * h->I, ny = (size_t)T * B * h->H, n0 = (size_t)B * h->H;
+  if (((uintptr_t)x | (uintptr_t)y | (uintptr_t)h0) & 3u) return PRNN_ERR_INVALID_ARG;
+  if (overlaps(y, ny * 4, x, nx * 4)) return PRNN_ERR_INVALID_ARG;
+  if (h0 && overlaps(y, ny * 4, h0, n0 * 4)) return PRNN_ERR_INVALID_ARG;
+  // all three must be page-locked host memory the device can address; the
+  // last element too (a buffer shorter than the sizes say is refused when
+  // its end falls outside any page-locked allocation)
+  float* ydev = static_cast<float*>(const_cast<void*>(mapped_host(y)));
+  if (!mapped_host(x) || !mapped_host(x + nx - 1) || !ydev || !mapped_host(y + ny - 1) ||
+      (h0 && (!mapped_host(h0) || !mapped_host(h0 + n0 - 1))))
+    return PRNN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PRNN_TRY(ensure_f32(&h->hx, &h->hx_cap, nx));
+  PRNN_TRY(ensure_f32(&h->hy, &h->hy_cap, ny));
+  if (h0) PRNN_TRY(ensure_f32(&h->hh0, &h->hh0_cap, n0));
+  PRNN_TRY(cudaMemcpyAsync(h->hx, x, nx * 4, cudaMemcpyHostToDevice, s));
+  if (h0) PRNN_TRY(cudaMemcpyAsync(h->hh0, h0, n0 * 4, cudaMemcpyHostToDevice, s));
+  const bool mirror = recurrence_mirrors(h);
+  const prnn_status_t st =
+      forward_impl(h, T, B, h->hx, h0 ? h->hh0 : nullptr, h->hy, mirror ? ydev : nullptr, s);
+  if (st != PRNN_OK) return st;
+  if (!mirror) PRNN_TRY(cudaMemcpyAsync(y, h->hy, ny * 4, cudaMemcpyDeviceToHost, s));
   return PRNN_OK;
 }
 

@@ -207,9 +207,11 @@ __global__ void __launch_bounds__(dense_launch_bound(F16, RMAX, BW, CPT), 1)
       if (orow >= 0) {
         float s = pv;
         for (int ww = 0; ww < nwarps; ++ww) s += rb[ww * V + tid];
-        if (!(cta == c.drop_cta && t == c.drop_step))
-          st_relaxed_f(yt + (size_t)ob * H + orow,
-                       c.p_masked ? (__float_as_uint(pv) == kMaskedMarker ? 0.f : s) : relu(s));
+        if (!(cta == c.drop_cta && t == c.drop_step)) {
+          const float out = c.p_masked ? (__float_as_uint(pv) == kMaskedMarker ? 0.f : s) : relu(s);
+          st_relaxed_f(yt + (size_t)ob * H + orow, out);
+          if (c.y_mirror) c.y_mirror[(size_t)tt * B * H + (size_t)ob * H + orow] = out;
+        }
       }
     }
     if (c.sync_mode == 1) {

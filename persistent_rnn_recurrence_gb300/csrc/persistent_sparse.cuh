@@ -290,9 +290,10 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
           const int idx = (BG >= TPR) ? gl * NOUT + i : gl / REP;
           if (idx < nbg) {
             const float s = acc[i] + pv[i];
-            st_relaxed_f(yt + (size_t)(bs + idx) * H + row,
-                         c.p_masked ? (__float_as_uint(pv[i]) == kMaskedMarker ? 0.f : s)
-                                    : relu(s));
+            const float out = c.p_masked ? (__float_as_uint(pv[i]) == kMaskedMarker ? 0.f : s)
+                                         : relu(s);
+            st_relaxed_f(yt + (size_t)(bs + idx) * H + row, out);
+            if (c.y_mirror) c.y_mirror[(size_t)tt * B * H + (size_t)(bs + idx) * H + row] = out;
           }
         }
       }

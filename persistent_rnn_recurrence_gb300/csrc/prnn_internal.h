@@ -85,6 +85,10 @@ struct RecurCommon {
   int sync_mode;         // 0 flags in data, 1 grid barrier
   unsigned* bar;         // grid barrier counter (sync_mode 1)
   int drop_cta, drop_step;  // fault hook (-1 = off)
+  // nullptr, or a second [T][B][H] destination of every output the kernel
+  // publishes (plain stores): a page-locked host buffer the device can
+  // address, so the result reaches the host while the recurrence runs
+  float* y_mirror;
 };
 
 // Dense: thread i owns 4-column chunks i, i+nthreads, ...; weights packed as

@@ -33,7 +33,7 @@ PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA, \
 PRNN_STACK_WAVEFRONT, PRNN_STACK_LAYERWISE = 0, 1
 
 EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
-           "prnn_forward", "prnn_destroy", "prnn_get_status", "prnn_status_string",
+           "prnn_forward", "prnn_forward_host", "prnn_destroy", "prnn_get_status", "prnn_status_string",
            "prnn_set_option", "prnn_get_info", "prnn_get_timing", "prnn_probe_sync_floor",
            "prnn_pack_sparse_host", "prnn_pack_sparse_host_placed", "prnn_forward_dense_noalloc",
            "prnn_set_weights_csr",
@@ -73,6 +73,7 @@ _sig = {
     "prnn_set_weights_dense": ([_P, _P, _P, _P, _P], _I),
     "prnn_set_weights_sparse": ([_P, _P, _I, _P, _P, _P, _P], _I),
     "prnn_forward": ([_P, _I, _I, _P, _P, _P, _P], _I),
+    "prnn_forward_host": ([_P, _I, _I, _P, _P, _P, _P], _I),
     "prnn_destroy": ([_P], _I),
     "prnn_get_status": ([_P, _P], _I),
     "prnn_status_string": ([_I], ctypes.c_char_p),
@@ -165,6 +166,13 @@ def prnn_set_weights_csr(h: int, Wx, nnz: int, row_ptr, cols, vals, bias, stream
 def prnn_forward(h: int, T: int, B: int, x, h0, y, stream=None) -> None:
     _check(_lib.prnn_forward(h, T, B, _ptr(x), _ptr(h0), _ptr(y), _stream(stream)),
            "prnn_forward")
+
+
+def prnn_forward_host(h: int, T: int, B: int, x, h0, y, stream=None) -> None:
+    """x, h0 (or None) and y are page-locked host buffers (e.g. pinned CPU
+    tensors)."""
+    _check(_lib.prnn_forward_host(h, T, B, _ptr(x), _ptr(h0), _ptr(y), _stream(stream)),
+           "prnn_forward_host")
 
 
 def prnn_destroy(h: int) -> None:

@@ -54,6 +54,7 @@ def test_null_arguments_rejected_without_gpu(lib):
     from persistent_rnn_recurrence_gb300 import prnn
     f = prnn._lib
     assert f.prnn_forward(None, 1, 1, None, None, None, None) == prnn.PRNN_ERR_INVALID_ARG
+    assert f.prnn_forward_host(None, 1, 1, None, None, None, None) == prnn.PRNN_ERR_INVALID_ARG
     assert f.prnn_destroy(None) == prnn.PRNN_OK
     assert f.prnn_set_option(None, 0, 1) == prnn.PRNN_ERR_INVALID_ARG
     assert f.prnn_create(None, 8, 8, 1, 0, 0) == prnn.PRNN_ERR_INVALID_ARG

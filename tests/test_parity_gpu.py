@@ -459,6 +459,52 @@ def test_staged_order_matches_column_order(env, spec):
         lay.close()
 
 
+@pytest.mark.parametrize("spec,algo,opts", [
+    (dict(H=1792, B=4, T=40, k=179), "persistent", {}),
+    (dict(H=1152, B=4, T=24, wdtype="f16", h0_std=0.3), "persistent", {}),
+    (dict(H=256, I=100, B=5, T=9, wdtype="f32", h0_std=0.5), "persistent", {}),
+    (dict(H=300, B=3, T=7, k=17), "per_step", {}),
+    (dict(H=1152, B=16, T=8, wdtype="f16"), "persistent", {"PRNN_OPT_RECURRENT_TC": 2}),
+    (dict(H=512, B=4, T=6, k=51), "persistent", {"PRNN_OPT_SYNC_MODE": 1})])
+def test_forward_host_buffers(env, spec, algo, opts):
+    """prnn_forward_host on pinned host buffers gives the bits prnn_forward
+    gives on device copies (persistent kernels write y over the host link; the
+    per-step path and the tcgen05 dense recurrence copy it back), and refuses
+    pageable and device memory."""
+    torch, prnn, o = env
+    p = synth.make_problem(seed=83, **spec)
+    pre = {getattr(prnn, k): v for k, v in opts.items() if k == "PRNN_OPT_RECURRENT_TC"}
+    post = {getattr(prnn, k): v for k, v in opts.items() if k != "PRNN_OPT_RECURRENT_TC"}
+    y_dev, _ = run_gpu(env, p, algo=algo, options=post, pre_options=pre or None)
+    if pre:
+        lay = prnn.Layer(p.H, p.I, max(1, p.B), p.wdtype, algo)
+        for k, v in pre.items():
+            lay.set_option(k, v)
+        lay.set_problem_weights(p)
+    else:
+        lay = prnn.Layer.from_problem(p, algo=algo)
+    try:
+        for k, v in post.items():
+            lay.set_option(k, v)
+        xh = torch.from_numpy(p.x).pin_memory()
+        h0h = None if p.h0 is None else torch.from_numpy(p.h0).pin_memory()
+        yh = torch.full((p.T, p.B, p.H), -1.0).pin_memory()
+        for _ in range(2):  # twice: the workspaces are reused
+            prnn.prnn_forward_host(lay.h, p.T, p.B, xh, h0h, yh)
+            torch.cuda.synchronize()
+            assert lay.status() == prnn.PRNN_OK
+            assert np.array_equal(yh.numpy(), y_dev)
+        with pytest.raises(prnn.PrnnError) as e:           # pageable host memory
+            prnn.prnn_forward_host(lay.h, p.T, p.B, torch.from_numpy(p.x.copy()), None, yh)
+        assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+        with pytest.raises(prnn.PrnnError) as e:           # device memory
+            prnn.prnn_forward_host(lay.h, p.T, p.B, xh, None, yh.cuda())
+        assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    finally:
+        lay.close()
+    check(y_dev, o.forward(p), p.wdtype, "host buffers")
+
+
 # --- tensor-core dense recurrence (wide batches) --------------------------------------
 @pytest.mark.parametrize("spec,force", [(dict(H=1152, B=16, T=64, wdtype="f16"), 0),
                                         (dict(H=2304, B=32, T=24, wdtype="f16", h0_std=0.2), 0),
