@@ -58,3 +58,23 @@ def test_workload_flops():
     f = bench.workload_flops(p)
     assert f["projection"] == 2.0 * 2 * 4 * 1792 * 1792
     assert f["recurrence"] == 2.0 * 2 * 4 * 1792 * 179
+
+
+def test_oracle_timing_legs():
+    """The CPU-baseline legs: a bounded sample of the workload, the rate
+    derived from the timesteps actually run, the host described."""
+    import bench
+    from persistent_rnn_recurrence_gb300 import synth
+    host = bench.host_cpu()
+    assert host["cpu_count"] >= 1 and 1 <= host["usable_cores"] <= host["cpu_count"]
+    assert isinstance(host["cpu_model"], str) and host["cpu_model"]
+    p = synth.named_problem("dense_f32_h256_b4_t32")
+    one = bench.time_oracle(p, threads=1, budget=0.2)
+    many = bench.time_oracle(p, threads=3, budget=0.2)
+    for leg, n in ((one, 1), (many, 3)):
+        assert leg["cores"] == n and leg["kind"] == "oracle" and leg["unit"] == "timesteps/s"
+        assert leg["seconds"] >= 0.2 and leg["value"] > 0
+        runs = int(leg["sample"].split(" run(s)")[0].split(", ")[-1])
+        ts = int(leg["sample"].split("first ")[1].split(" of")[0])
+        assert ts == p.T   # a sequence this short runs whole, repeated
+        assert abs(leg["value"] - runs * ts / leg["seconds"]) <= 1e-9 * leg["value"]
