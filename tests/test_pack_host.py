@@ -173,3 +173,15 @@ def test_placed_pack_reproduces_the_product(prnn):
         rows = min(R, H - c * R)
         got[c * R:c * R + rows] = prod[:rows].reshape(rows, -1).sum(1)
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_placed_pack_is_deterministic(prnn):
+    """The placement search is seeded: packing the same weights twice gives
+    the same tables and the same packed words."""
+    H, k, tpr, R, n = 1152, 115, 8, 31, 38
+    p = synth.make_problem(H=H, B=1, T=1, k=k, seed=12)
+    a = prnn.prnn_pack_sparse_host_placed(H, k, n, R, tpr, p.vals, p.cols)
+    b = prnn.prnn_pack_sparse_host_placed(H, k, n, R, tpr, p.vals, p.cols)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and a[2:] == b[2:]
+    # CTAs get different orders (each balances its own warps)
+    assert not np.array_equal(a[1][0], a[1][1])
