@@ -29,6 +29,10 @@
  *    default stream.
  *  - The library owns everything it allocates (packed weights, workspaces,
  *    the status word); the caller owns every pointer it passes in.
+ *  - A handle's calls share its workspaces, so they must not overlap: call a
+ *    handle from one host thread at a time, and keep its forward and backward
+ *    passes ordered (one stream, or synchronize between streams).  Different
+ *    handles are independent.
  */
 #ifndef PRNN_H
 #define PRNN_H
