@@ -185,3 +185,69 @@ def test_placed_pack_is_deterministic(prnn):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and a[2:] == b[2:]
     # CTAs get different orders (each balances its own warps)
     assert not np.array_equal(a[1][0], a[1][1])
+
+
+def _random_layouts(n):
+    rng = np.random.default_rng(2024)
+    out = []
+    while len(out) < n:
+        H = int(rng.choice([128, 256, 384, 40, 97, 130]))
+        tpr = int(rng.choice([1, 2, 4, 8, 16, 32]))
+        k = int(rng.choice([1, 2, 3, max(1, H // 10), H // 2, H]))
+        R = int(rng.integers(1, 9))
+        n_cta = -(-H // R)
+        out.append((H, k, tpr, R, n_cta, int(rng.integers(1 << 30))))
+    return out
+
+
+@pytest.mark.parametrize("H,k,tpr,R,n,seed", _random_layouts(24))
+def test_random_layouts_pack_exactly(prnn, H, k, tpr, R, n, seed):
+    """Both packings on random small layouts (k = 1 .. H, every threads-per-row,
+    ragged row counts): every row keeps exactly its (column, value) entries,
+    padding is zero-valued, indices stay on the staged h, and no gather slot
+    puts more lanes on a bank than the reported cap."""
+    rng = np.random.default_rng(seed)
+    cols = np.stack([np.sort(rng.choice(H, k, replace=False)) for _ in range(H)]).astype(np.uint16)
+    vals = rng.standard_normal((H, k)).astype(np.float16)
+    vals[vals == 0] = np.float16(0.5)          # keep every real entry non-zero
+    for placed in (False, True):
+        if placed:
+            out, place, ept, cap = prnn.prnn_pack_sparse_host_placed(H, k, n, R, tpr, vals, cols)
+            col_of = []
+            for c in range(n):
+                if place is None:
+                    col_of.append(np.arange(H))
+                else:
+                    pos = staged_positions(place[c], H)
+                    inv = np.empty(H, dtype=np.int64)
+                    inv[pos] = np.arange(H)
+                    col_of.append(inv)
+        else:
+            out, ept, cap = prnn.prnn_pack_sparse_host(H, k, n, R, tpr, vals, cols)
+            col_of = [np.arange(H)] * n
+        e = unpack(out, ept)
+        v = (e & 0xFFFF).astype(np.uint16)
+        idx = (e >> 16).astype(np.int64)
+        assert idx.max() < H
+        rpw = max(1, 32 // tpr)
+        for c in range(n):
+            for r in range(R):
+                g = c * R + r
+                if g >= H:
+                    continue
+                fv, fi = v[c, r].ravel(), idx[c, r].ravel()
+                real = fv != 0
+                got = sorted(zip(col_of[c][fi[real]].tolist(), fv[real].tolist()))
+                want = sorted(zip(cols[g].astype(np.int64).tolist(), vals[g].view(np.uint16).tolist()))
+                assert got == want, (placed, c, r)
+            for w in range(-(-R // rpw)):
+                rows = [r for r in range(w * rpw, min(R, w * rpw + rpw)) if c * R + r < H]
+                if not rows:
+                    continue
+                lanes = idx[c, rows].reshape(len(rows) * tpr, ept)
+                for j in range(ept):
+                    # wavefronts of this slot: the most distinct addresses on one bank
+                    # (lanes reading the same word share it)
+                    addrs = np.unique(lanes[:, j])
+                    assert np.bincount(addrs % 32, minlength=32).max() <= max(cap, 1), \
+                        (placed, c, w, j)
