@@ -157,8 +157,10 @@ inline int placed_pos(const uint32_t* tab, int c) {
 // block of 128 columns, same component): a swap exchanges their banks and so
 // keeps every class a permutation of the banks.  The objective is
 // sum over (warp, bank) of max(0, D - S)^2, D = the warp's entries on that
-// bank; a move is taken when it lowers the objective, or keeps it equal with
-// probability 1/4 (a walk along plateaus).  Deterministic for a given seed.
+// bank.  Each round takes the best swap that lowers the objective; when none
+// does, a swap that keeps it equal may be taken instead (each such candidate
+// with probability 1/4: a walk along plateaus).  Deterministic for a given
+// seed and standard library.
 // Returns the largest D left (<= S when the search succeeded).
 int place_cta(int H, int nw, const std::vector<uint8_t>& mult, int S, uint32_t seed,
               uint32_t* tab /* H/4 words */) {
