@@ -78,3 +78,33 @@ def test_oracle_timing_legs():
         ts = int(leg["sample"].split("first ")[1].split(" of")[0])
         assert ts == p.T   # a sequence this short runs whole, repeated
         assert abs(leg["value"] - runs * ts / leg["seconds"]) <= 1e-9 * leg["value"]
+
+
+def test_reference_arm_contract():
+    """bench.py --impl reference (the fp64 oracle timed on the host cores) prints
+    one JSON line with the headline's metric, unit and config and the keys the
+    contract names; a rank other than 0 exits 0 without output."""
+    import json
+    import subprocess
+    import sys
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "1"]
+    r = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["unit"] == "timesteps/s" and d["higher_is_better"] is True and d["value"] > 0
+    assert d["n_gpus"] == 1 and d["steps"] == 1 and d["dtype"] == "f64"
+    assert d["config"]["workload"] == bench.DEFAULT_CONFIG
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"]
+    assert cb["sample"] and cb["host"]["cpu_count"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "timesteps/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    env1 = dict(env, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r1 = subprocess.run(cmd, cwd=root, env=env1, capture_output=True, text=True, timeout=300)
+    assert r1.returncode == 0 and not r1.stdout.strip()
