@@ -108,3 +108,19 @@ def test_reference_arm_contract():
     env1 = dict(env, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
     r1 = subprocess.run(cmd, cwd=root, env=env1, capture_output=True, text=True, timeout=300)
     assert r1.returncode == 0 and not r1.stdout.strip()
+
+
+def test_traffic_is_null_once_the_kernel_changes(monkeypatch):
+    """The DRAM traffic in the bench line comes from the committed capture only
+    while the recurrent kernel's sources hash to the captured value."""
+    import json
+    import bench
+    path = os.path.join(bench.ROOT, "profiles", "traffic.json")
+    rec = json.load(open(path))
+    key = "sparse_f16_h1792_d10_b4_t256/persistent"
+    want = rec[key]["dram_bytes_per_launch"]
+    monkeypatch.setattr(bench, "kernel_source_sha1", lambda sparse: rec[key]["kernel_source_sha1"])
+    assert bench.load_traffic("sparse_f16_h1792_d10_b4_t256", "persistent", True) == want
+    monkeypatch.setattr(bench, "kernel_source_sha1", lambda sparse: "0" * 40)
+    assert bench.load_traffic("sparse_f16_h1792_d10_b4_t256", "persistent", True) is None
+    assert bench.load_traffic("no_such_workload", "persistent", True) is None
