@@ -187,7 +187,8 @@ int oracle_rnn_forward_threads(long T, long B, long H, long I, long k, const dou
         free(zeros);
         return -1;
     }
-    team_t tm = {T, B, H, I, k, x, Wx, Wh, vals, bias, h0, cols, y};
+    team_t tm = {.T = T, .B = B, .H = H, .I = I, .k = k, .x = x, .Wx = Wx, .Wh = Wh,
+                 .vals = vals, .bias = bias, .h0 = h0, .cols = cols, .y = y};
     pthread_mutex_init(&tm.gate_m, NULL);
     pthread_cond_init(&tm.gate_c, NULL);
     tm.started = 0;
