@@ -18,6 +18,7 @@ timesteps all ranks processed divided by the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import subprocess
@@ -61,6 +62,10 @@ def parse_args(argv=None):
     ap.add_argument("--vendor", action="store_true",
                     help="persistent kernels vs per-step cuBLAS / cuSPARSE products (one JSON "
                          "line per workload)")
+    ap.add_argument("--trace", action="store_true",
+                    help="phase trace of the sparse persistent kernel on the config's layer "
+                         "(first --trace-steps steps): where the time of a step goes")
+    ap.add_argument("--trace-steps", type=int, default=16)
     ap.add_argument("--backward", action="store_true",
                     help="training step (forward + backward through time) of the named workloads")
     return ap.parse_args(argv)
@@ -861,13 +866,73 @@ def run_backward(args):
     return 0
 
 
+def vendor_loops(p, dev):
+    """The per-step vendor-library recurrences of problem p, each step
+    h_t = ReLU(P_t + Wh h_{t-1}) with P = Wx x + b precomputed in fp32 by one
+    cuBLAS product: name -> (step(h_prev, P_t, h_next), P, h0).
+      cublas_sgemm   fp32 GEMM (torch.addmm, no TF32) with Wh held densely;
+      cublas_hgemm   the same in fp16 (h rounded to fp16 every step);
+      cusparse_spmm  CSR SpMM (torch.sparse.mm), sparse layers only.
+    The libraries run as shipped; nothing of theirs is inspected."""
+    import numpy as np
+    import torch
+    torch.backends.cuda.matmul.allow_tf32 = False
+    x = torch.from_numpy(p.x).to(dev)
+    h0 = torch.zeros(p.B, p.H, device=dev) if p.h0 is None else torch.from_numpy(p.h0).to(dev)
+    Wx = torch.from_numpy(p.Wx.astype(np.float32)).to(dev)
+    P = (x.reshape(-1, p.I) @ Wx.T + torch.from_numpy(p.b).to(dev)).reshape(p.T, p.B, p.H)
+    Wd = densified_wh(p)
+    WdT = torch.from_numpy(Wd).to(dev).T.contiguous()
+    WdT16 = WdT.half()
+
+    def dense32(hp, Pt, hn):
+        torch.addmm(Pt, hp, WdT, out=hn)
+        hn.relu_()
+
+    def dense16(hp, Pt, hn):
+        torch.addmm(Pt, hp, WdT16, out=hn)
+        hn.relu_()
+    loops = {"cublas_sgemm": (dense32, P, h0), "cublas_hgemm": (dense16, P.half(), h0.half())}
+    if p.sparse:
+        Wcsr = torch.from_numpy(Wd).to(dev).to_sparse_csr()
+
+        def sparse32(hp, Pt, hn):
+            hn.copy_(torch.sparse.mm(Wcsr, hp.T).T)
+            hn.add_(Pt).relu_()
+        loops["cusparse_spmm"] = (sparse32, P, h0)
+    return loops
+
+
+def densified_wh(p):
+    """Wh of problem p as a dense fp32 [H, H] array (exact: fp16 values)."""
+    import numpy as np
+    if not p.sparse:
+        return p.Wh.astype(np.float32)
+    Wd = np.zeros((p.H, p.H), np.float32)
+    if getattr(p, "row_ptr", None) is not None:
+        rows = np.repeat(np.arange(p.H), np.diff(p.row_ptr))
+        Wd[rows, p.cols.astype(np.int64)] = p.vals.astype(np.float32)
+    else:
+        Wd[np.repeat(np.arange(p.H), p.k), p.cols.astype(np.int64).ravel()] = \
+            p.vals.astype(np.float32).ravel()
+    return Wd
+
+
+def vendor_forward(step, P, h0, T):
+    """Run T steps of one vendor loop eagerly; y [T, B, H] as fp32."""
+    import torch
+    hs = [h0] + [torch.empty_like(h0) for _ in range(T)]
+    for t in range(T):
+        step(hs[t], P[t], hs[t + 1])
+    return torch.stack(hs[1:]).float()
+
+
 def run_vendor(args):
     """The pages' comparison points, restated on GB300: the persistent
-    kernels against per-step vendor-library products (cuBLAS dense GEMM via
-    torch.addmm, cuSPARSE CSR SpMM via torch.sparse.mm), each step
-    h_t = ReLU(P_t + Wh h_{t-1}) with P precomputed, T steps captured in one
-    CUDA graph where the library allows it.  The libraries run as shipped;
-    nothing of theirs is inspected."""
+    kernels against per-step vendor-library products (``vendor_loops``), T
+    steps captured in one CUDA graph where the library allows it, and for
+    sparse layers the dense persistent kernel on the same matrix held densely
+    (the sparse-versus-dense persistent row of the pages' table)."""
     import numpy as np
     import torch
     from persistent_rnn_recurrence_gb300 import prnn, synth
@@ -912,6 +977,18 @@ def run_vendor(args):
         except Exception:
             return run, False
 
+    def persistent_us(lay, p, x, h0, y):
+        lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+        rec_ms = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            prnn.prnn_forward(lay.h, p.T, p.B, x, h0, y)
+            rec_ms.append(prnn.prnn_get_timing(lay.h)[1])
+        st = lay.status()
+        if st != prnn.PRNN_OK:
+            raise RuntimeError(prnn.prnn_status_string(st))
+        return 1e3 * sorted(rec_ms)[len(rec_ms) // 2] / p.T
+
     cases = [("dense_f16_h1152_b4_t256", None), ("sparse_f16_h1792_d10_b4_t256", None)]
     extra = [(1152, 0.10), (1792, 0.01), (2304, 0.10), (5760, 0.01), (5760, 0.05)]
     out = []
@@ -921,55 +998,32 @@ def run_vendor(args):
                  for i, (H, d) in enumerate(extra)]
     for p in problems:
         rec = {"workload": p.name}
-        lay = prnn.Layer.from_problem(p)
-        lay.set_option(prnn.PRNN_OPT_TIMING, 1)
         x = torch.from_numpy(p.x).to(dev)
         h0 = torch.zeros(p.B, p.H, device=dev) if p.h0 is None else torch.from_numpy(p.h0).to(dev)
         y = torch.empty(p.T, p.B, p.H, device=dev)
-        rec_ms = []
-        for _ in range(reps):
-            flush.fill_(1.0)
-            prnn.prnn_forward(lay.h, p.T, p.B, x, h0, y)
-            rec_ms.append(prnn.prnn_get_timing(lay.h)[1])
+        lay = prnn.Layer.from_problem(p)
+        rec["persistent_us_per_step"] = persistent_us(lay, p, x, h0, y)
         lay.close()
-        rec["persistent_us_per_step"] = 1e3 * sorted(rec_ms)[len(rec_ms) // 2] / p.T
-        # the same P for the vendor loops
-        Wx = torch.from_numpy(p.Wx.astype(np.float32)).to(dev)
-        P = (x.reshape(-1, p.I) @ Wx.T + torch.from_numpy(p.b).to(dev)).reshape(p.T, p.B, p.H)
         if p.sparse:
-            Wd = np.zeros((p.H, p.H), np.float32)
-            Wd[np.repeat(np.arange(p.H), p.k), p.cols.astype(np.int64).ravel()] = \
-                p.vals.astype(np.float32).ravel()
-        else:
-            Wd = p.Wh.astype(np.float32)
-        WdT = torch.from_numpy(Wd).to(dev).T.contiguous()
-        WdT16 = WdT.half()
-        P16 = P.half()
-
-        def dense32(hp, Pt, hn):
-            torch.addmm(Pt, hp, WdT, out=hn)
-            hn.relu_()
-
-        def dense16(hp, Pt, hn):
-            torch.addmm(Pt, hp, WdT16, out=hn)
-            hn.relu_()
-        for key, fn, Pv, hv in (("cublas_sgemm", dense32, P, h0),
-                                ("cublas_hgemm", dense16, P16, h0.half())):
-            f, cap = per_step(p.T, Pv, hv, fn)
-            rec[key + "_us_per_step"] = 1e3 * timed(f) / p.T
-            rec[key + "_graph"] = cap
-        if p.sparse:
-            Wcsr = torch.from_numpy(Wd).to(dev).to_sparse_csr()
-
-            def sparse32(hp, Pt, hn):
-                hn.copy_(torch.sparse.mm(Wcsr, hp.T).T)
-                hn.add_(Pt).relu_()
+            # the same matrix held densely (fp16) in the dense persistent kernel
+            pd = dataclasses.replace(p, Wh=densified_wh(p).astype(np.float16), vals=None,
+                                     cols=None, row_ptr=None, name=p.name + "_held_densely")
             try:
-                f, cap = per_step(p.T, P, h0, sparse32)
-                rec["cusparse_spmm_us_per_step"] = 1e3 * timed(f) / p.T
-                rec["cusparse_spmm_graph"] = cap
-            except Exception as e:  # sparse product unavailable in the installed PyTorch
-                rec["cusparse_spmm_error"] = str(e)[:120]
+                lay = prnn.Layer.from_problem(pd)
+            except prnn.PrnnError as e:
+                rec["dense_persistent"] = {"unsupported": str(e)}
+            else:
+                rec["dense_persistent_us_per_step"] = persistent_us(lay, pd, x, h0, y)
+                rec["sparse_vs_dense_persistent"] = (rec["dense_persistent_us_per_step"]
+                                                     / rec["persistent_us_per_step"])
+                lay.close()
+        for key, (fn, Pv, hv) in vendor_loops(p, dev).items():
+            try:
+                f, cap = per_step(p.T, Pv, hv, fn)
+                rec[key + "_us_per_step"] = 1e3 * timed(f) / p.T
+                rec[key + "_graph"] = cap
+            except Exception as e:  # e.g. a sparse product missing from the installed PyTorch
+                rec[key + "_error"] = str(e)[:120]
         best_dense = min(rec["cublas_sgemm_us_per_step"], rec["cublas_hgemm_us_per_step"])
         rec["persistent_vs_dense_gemm"] = best_dense / rec["persistent_us_per_step"]
         if "cusparse_spmm_us_per_step" in rec:
@@ -978,6 +1032,100 @@ def run_vendor(args):
         out.append(rec)
         print(json.dumps(rec), flush=True)
     return 0
+
+
+TRACE_PHASES = ["pause", "wait_h", "stage_to_barrier", "gather", "reduce", "publish", "tail"]
+
+
+def trace_phases(rec, clock_mhz):
+    """Per-phase durations (ns) of a trace array rec [R, T, n_cta, 12] (uint32):
+    one sample per (run, step, CTA) for steps 1 .. T-2, each a difference of
+    stamps from one SM's clock.  Returns {phase: numpy array of ns} plus
+    "step" (pass start to the next step's pass start) and "rounds"."""
+    import numpy as np
+    r = rec.astype(np.int64)
+    c = r[..., 2:9]                          # 7 stamps: start, pause end, poll fresh, barrier,
+    d = lambda a, b: ((b - a) & 0xffffffff)  # gathers, reduction, publish (mod 2^32)
+    T = r.shape[1]
+    sl = slice(1, T - 1)
+    ns = 1e3 / clock_mhz
+    out = {}
+    for i, name in enumerate(TRACE_PHASES[:-1]):
+        out[name] = d(c[:, sl, :, i], c[:, sl, :, i + 1]).ravel() * ns
+    nxt = c[:, 2:T, :, 0]
+    out["tail"] = d(c[:, sl, :, 6], nxt).ravel() * ns
+    out["step"] = d(c[:, sl, :, 0], nxt).ravel() * ns
+    out["rounds"] = r[:, sl, :, 9].ravel()
+    return out
+
+
+def run_trace(args):
+    """Where the time of one step of the sparse persistent kernel goes: runs
+    the config's layer for --trace-steps steps with the phase trace on (L2
+    flushed before each forward), checks the traced output equals the
+    untraced one bit for bit, and prints one JSON line of per-phase medians
+    and spreads (ns), the re-poll statistics and the trace's own overhead."""
+    import numpy as np
+    import torch
+    from persistent_rnn_recurrence_gb300 import prnn, synth
+    dev = torch.device("cuda", 0)
+    p = synth.named_problem(args.config, T=args.trace_steps)
+    if not p.sparse:
+        raise SystemExit("--trace needs a sparse layer")
+    lay = prnn.Layer.from_problem(p)
+    lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+    info = lay.info()
+    x = torch.from_numpy(p.x).to(dev)
+    y0 = torch.empty(p.T, p.B, p.H, device=dev)
+    y1 = torch.empty_like(y0)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    n_cta = info["n_cta"]
+    buf = torch.zeros(p.T * n_cta * 12, dtype=torch.int32, device=dev)
+    reps = max(3, min(args.steps, 20))
+
+    def runs(traced):
+        prnn.prnn_set_trace_buffer(lay.h, buf if traced else None, buf.numel() * 4)
+        ms, recs = [], []
+        for i in range(reps + 2):
+            flush.fill_(1.0)
+            prnn.prnn_forward(lay.h, p.T, p.B, x, None, y1 if traced else y0)
+            t = prnn.prnn_get_timing(lay.h)[1]
+            if i >= 2:
+                ms.append(t)
+                if traced:
+                    recs.append(buf.view(p.T, n_cta, 12).cpu().numpy().view(np.uint32).copy())
+        return sorted(ms)[len(ms) // 2], recs
+
+    ms_plain, _ = runs(False)
+    ms_traced, recs = runs(True)
+    prnn.prnn_set_trace_buffer(lay.h, None, 0)
+    torch.cuda.synchronize()
+    st = lay.status()
+    lay.close()
+    same = bool(torch.equal(y0, y1))
+    clock_mhz = load_peaks().get("sm_max_mhz", 2070.0)  # the SM clock under load
+    ph = trace_phases(np.stack(recs), clock_mhz)
+
+    def stats(a):
+        a = np.sort(np.asarray(a, dtype=np.float64))
+        q = lambda f: float(a[min(len(a) - 1, int(f * len(a)))])
+        return {"median": q(0.5), "p10": q(0.1), "p90": q(0.9), "mean": float(a.mean())}
+
+    sm_ids = np.stack(recs)[..., 10]
+    line = {"trace": p.name, "T": p.T, "B": p.B, "n_cta": n_cta,
+            "cta_groups": info["cta_groups"], "rows_per_cta": info["rows_per_cta"],
+            "threads_per_cta": info["threads_per_cta"], "threads_per_row": info["threads_per_row"],
+            "k_padded": info["k_padded"], "status": prnn.prnn_status_string(st),
+            "traced_equals_untraced": same, "clock_mhz_assumed": clock_mhz,
+            "recurrence_us_per_step": {"plain": 1e3 * ms_plain / p.T,
+                                       "traced": 1e3 * ms_traced / p.T},
+            "samples": int(ph["step"].size), "distinct_sms": int(np.unique(sm_ids).size),
+            "phases_ns": {k: stats(ph[k]) for k in TRACE_PHASES + ["step"]},
+            "repoll": {"mean_rounds": float(ph["rounds"].mean()),
+                       "frac_ctas_first_poll_fresh": float((ph["rounds"] == 0).mean()),
+                       "max_rounds": int(ph["rounds"].max())}}
+    print(json.dumps(line), flush=True)
+    return 0 if same and st == prnn.PRNN_OK else 1
 
 
 def main(argv=None):
@@ -994,6 +1142,8 @@ def main(argv=None):
         return run_stack(args)
     if args.backward:
         return run_backward(args)
+    if args.trace:
+        return run_trace(args)
     if args.vendor:
         return run_vendor(args)
     return run_ours(args)

@@ -248,6 +248,27 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info);
 prnn_status_t prnn_get_timing(prnn_t h, float* ms_projection, float* ms_recurrence);
 
 /*
+ * Phase trace of the sparse persistent kernel (a diagnostic; off unless a
+ * buffer is set).  While `buffer` (a DEVICE pointer, 16-byte aligned, owned by
+ * the caller) is set, every prnn_forward / prnn_forward_host of this handle
+ * runs the trace build of the sparse kernel, which writes one record of 12
+ * uint32 words per step and CTA, [T][n_cta][12], for the step's first batch
+ * pass: globaltimer ns (low word, high word); SM clock (low 32 bits) at pass
+ * start, at the end of the pause before the first poll, when the CTA's last
+ * staging poll of h_{t-1} was fresh, after the CTA barrier, when the last warp
+ * finished its gathers, its reduction and its publish; the most re-poll
+ * rounds any thread needed; the SM id; the CTA index.  The pages time the
+ * effect of each measure on whole steps (Sparse Persistent RNNs, measured-
+ * effects table); this records where inside a step the time goes.  Results
+ * are the same bits as without the trace.  Requires `bytes` >= T * n_cta * 48
+ * at each forward (PRNN_ERR_INVALID_ARG otherwise) and a sparse layer on the
+ * persistent path with column-order, wide staging (PRNN_ERR_UNSUPPORTED
+ * otherwise).  buffer = NULL turns the trace off.  Errors: INVALID_ARG for a
+ * misaligned, too small or non-device buffer.
+ */
+prnn_status_t prnn_set_trace_buffer(prnn_t h, void* buffer, size_t bytes);
+
+/*
  * Step-synchronisation floor: runs the persistent grid of this handle for T
  * steps doing only the step-to-step exchange (every CTA waits for all of
  * h_{t-1}, then publishes its rows of h_t) with no arithmetic, so its time per
@@ -321,8 +342,10 @@ prnn_status_t prnn_pack_sparse_host_placed(int hidden, int k, int n_cta, int row
  * 4 Mi floats (16 MiB) that the library's CUDA module carries; every GPU on
  * which the library's kernels are loaded holds it until the process exits.
  * Limits: T*B*H <= 4194304 and 1 <= B <= 32, else PRNN_ERR_INVALID_ARG.
- * The first call on a device looks up the array's device address on that
- * device (cudaGetSymbolAddress) and caches it; make that first call before
+ * Every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress, a host-side query; nothing is cached, so a call after
+ * cudaDeviceReset finds the array where the reloaded module put it).  The
+ * first call on a device may load the library's module there: make it before
  * any stream capture.  Every call shares the one array and it keeps the last
  * call's contents (P is fully rewritten before use, nothing needs zeroing):
  * calls whose work overlaps on the GPU -- on different streams, or from

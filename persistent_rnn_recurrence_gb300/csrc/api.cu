@@ -80,6 +80,9 @@ struct prnn_handle {
   size_t x16_cap = 0;
   int* status = nullptr;     // device int[4]
   unsigned* bar = nullptr;   // grid-barrier counter
+  // caller's device buffer for the sparse kernel's phase trace (or null)
+  uint32_t* trace = nullptr;
+  size_t trace_words = 0;
   // options
   long long timeout_us = 500000;
   int poll_delay_ns = -1, clock_khz = 0;  // -1: the kernel family's default
@@ -880,6 +883,11 @@ static bool recurrence_mirrors(const prnn_t h) {
 // output as the recurrence publishes it.  Arguments are checked by the callers.
 static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const float* h0,
                                   float* y, float* y_mirror, cudaStream_t s) {
+  if (h->trace) {  // the phase trace: sparse persistent kernel, column order, wide staging
+    if (h->algo != PRNN_ALGO_PERSISTENT || !h->sparse || h->place || !h->wide_loads)
+      return PRNN_ERR_UNSUPPORTED;
+    if ((size_t)T * h->n_cta * kTraceWords > h->trace_words) return PRNN_ERR_INVALID_ARG;
+  }
   const size_t ny = (size_t)T * B * h->H;
   PRNN_TRY(ensure_P(h, ny));
   const bool persistent = h->algo == PRNN_ALGO_PERSISTENT;
@@ -918,6 +926,7 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
       a.dbuf = db ? 1 : 0;
       a.narrow = h->wide_loads ? 0 : 1;
       a.place = h->place;
+      a.trace = h->trace;
       PRNN_TRY(launch_recur_sparse(a, s));
     } else if (h->rtc && h->sync_mode == 0) {
       DenseTcArgs a{};
@@ -1330,6 +1339,25 @@ prnn_status_t prnn_get_timing(prnn_t h, float* ms_projection, float* ms_recurren
   // forward: (projection, recurrence); backward: (gradient products, reverse recurrence)
   if (ms_projection) *ms_projection = h->last_backward ? b : a;
   if (ms_recurrence) *ms_recurrence = h->last_backward ? a : b;
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_set_trace_buffer(prnn_t h, void* buffer, size_t bytes) {
+  if (!h) return PRNN_ERR_INVALID_ARG;
+  if (buffer == nullptr) {
+    h->trace = nullptr;
+    h->trace_words = 0;
+    return PRNN_OK;
+  }
+  if (!aligned16(buffer) || bytes < kTraceWords * sizeof(uint32_t)) return PRNN_ERR_INVALID_ARG;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, buffer) != cudaSuccess) {
+    cudaGetLastError();
+    return PRNN_ERR_INVALID_ARG;
+  }
+  if (at.type != cudaMemoryTypeDevice) return PRNN_ERR_INVALID_ARG;
+  h->trace = static_cast<uint32_t*>(buffer);
+  h->trace_words = bytes / sizeof(uint32_t);
   return PRNN_OK;
 }
 

@@ -13,8 +13,6 @@
 // It runs the per-step path: the fp32 CUDA-core projection writes
 // P = Wx x + b for all steps into the scratch array, then T step kernels each
 // read Wh (row-major, the caller's buffer) and y[t-1] and write y[t].
-#include <mutex>
-
 #include "prnn.h"
 #include "prnn_internal.h"
 
@@ -24,26 +22,17 @@ namespace {
 constexpr size_t kScratchFloats = (size_t)1 << 22;
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-float* g_scratch_ptr[kMaxDevices] = {};
-
 // Device address of the scratch array on the current device.  Host code may
 // not use the symbol itself (it is a host-side stand-in), so the address is
-// looked up once per device with that device current and cached.
+// looked up with that device current -- on every call, not cached: a cached
+// address would outlive a cudaDeviceReset (after which the module, and the
+// array, are loaded again, possibly elsewhere).  The lookup is a host-side
+// query; the first one on a device may load the library's module there.
 cudaError_t scratch_on_current_device(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+  *out = static_cast<float*>(p);
   return cudaSuccess;
 }
 

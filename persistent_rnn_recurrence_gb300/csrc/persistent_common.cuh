@@ -93,11 +93,13 @@ __device__ __forceinline__ void seg_reduce_scatter(float (&v)[V], int lane) {
 // conflict-free.  A thread keeps up to UMAX float4 loads in flight; while any
 // is still the sentinel it re-issues all of its stale loads together (one
 // round trip per round) until every word is fresh.  Returns false if the wait
-// gave up.
+// gave up.  With rounds_out (the phase trace), the largest number of re-poll
+// rounds any of the thread's load batches needed is recorded there.
 // ---------------------------------------------------------------------------
 template <int UMAX>
 __device__ __forceinline__ bool stage_rows(const float* hprev, bool poll, int H, int b_start,
-                                           int nb, float* hs, Waiter& w) {
+                                           int nb, float* hs, Waiter& w,
+                                           uint32_t* rounds_out = nullptr) {
   const int NT = blockDim.x, tid = threadIdx.x;
   const int nf4 = (nb * H) >> 2;
   const float4* src = reinterpret_cast<const float4*>(hprev + (size_t)b_start * H);
@@ -125,6 +127,7 @@ __device__ __forceinline__ bool stage_rows(const float* hprev, bool poll, int H,
         for (int u = 0; u < UMAX; ++u)
           if ((stale >> u) & 1u) v[u] = ld_relaxed_f4(reinterpret_cast<const float*>(src + base + u * NT));
       }
+      if (rounds_out != nullptr && round > *rounds_out) *rounds_out = round;
     }
 #pragma unroll
     for (int u = 0; u < UMAX; ++u)

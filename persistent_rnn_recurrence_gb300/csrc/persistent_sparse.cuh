@@ -27,6 +27,15 @@
 //
 // Every wait is bounded (globaltimer deadline); on expiry the kernel records
 // a status word and every CTA leaves its time loop.
+//
+// Phase trace (opt-in, TRACE instantiations only): per step and CTA, SM-clock
+// stamps of the step's first batch pass -- pass start, end of the pause before
+// the first poll, last staging poll fresh (latest thread), CTA barrier passed,
+// gathers done, reduction done, publish issued (each latest over the CTA's
+// warps) -- plus the most re-poll rounds any thread needed, into a caller's
+// buffer [T][n_cta][kTraceWords].  Stamps of one record come from one SM's
+// clock, so differences within a record are exact; records of different
+// CTAs are aligned only through the globaltimer word.
 #pragma once
 #include "persistent_common.cuh"
 
@@ -166,10 +175,13 @@ __device__ __forceinline__ bool stage_rows_narrow_placed(const float* hprev, boo
 // the column's position in that staging, which is the column itself or, with
 // a placement table, this CTA's bank-balancing order of the columns.
 // ---------------------------------------------------------------------------
-template <int TPR, int BG, bool PLACED>
+template <int TPR, int BG, bool PLACED, bool TRACE = false>
 __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const SparseRecurArgs a) {
   extern __shared__ __align__(16) float smem_f[];
   __shared__ int s_abort;
+  // phase stamps of the last three steps (slot t % 3: a slot is rewritten
+  // only after the CTA barrier that follows its flush)
+  __shared__ uint32_t s_tr[TRACE ? 3 : 1][TRACE ? 8 : 1];
   constexpr int UMAX = (BG >= 16) ? 4 : (BG == 8 ? 8 : 12);
   const RecurCommon& c = a.c;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -190,6 +202,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
     for (size_t i = tid; i < n16; i += NT) Ws[i] = __ldg(src + i);
   }
   if (tid == 0) s_abort = 0;
+  if (TRACE && tid < 24) (&s_tr[0][0])[tid] = 0u;
   __syncthreads();
 
   const int r = tid / TPR, s = tid % TPR;
@@ -211,6 +224,32 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
   w.status = c.status;
   w.timeout_ns = c.timeout_ns;
   w.backoff = c.poll_backoff;
+  // trace helpers: thread 0's own stamp, and the latest stamp over the CTA
+  // (warp maximum, then one shared atomic per warp)
+  uint64_t gt_cur = 0, gt_last = 0;
+  uint32_t rounds = 0;
+  auto stamp0 = [&](int t, int ph) {
+    if (TRACE && tid == 0) s_tr[t % 3][ph] = (uint32_t)clock64();
+  };
+  auto stamp_max = [&](int t, int ph, uint32_t v) {
+    if (TRACE) {
+      v = __reduce_max_sync(0xffffffffu, v);
+      if (lane == 0) atomicMax(&s_tr[t % 3][ph], v);
+    }
+  };
+  auto flush = [&](int t, uint64_t gt) {
+    if (TRACE && tid == 0 && a.trace != nullptr) {
+      uint32_t* rec = a.trace + ((size_t)t * c.n_cta + cta) * kTraceWords;
+      rec[0] = (uint32_t)gt;
+      rec[1] = (uint32_t)(gt >> 32);
+      for (int i = 0; i < 8; ++i) rec[2 + i] = s_tr[t % 3][i];
+      uint32_t sm;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+      rec[10] = sm;
+      rec[11] = (uint32_t)cta;
+      s_tr[t % 3][7] = 0u;  // the round count is a maximum, not a clock: restart it
+    }
+  };
   int seq = 0;
   for (int t = 0; t < c.T; ++t) {
     const int tt = c.reverse ? c.T - 1 - t : t;  // time index of this step
@@ -220,6 +259,15 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
     w.new_step();
     for (int bs = pl.b_lo; bs < pl.b_hi; bs += BG, ++seq) {
       const int nbg = min(BG, pl.b_hi - bs);
+      const bool tr = TRACE && bs == pl.b_lo;  // the trace records each step's first pass
+      if (tr) {
+        stamp0(t, 0);
+        if (tid == 0) {
+          gt_last = gt_cur;
+          gt_cur = global_ns();
+        }
+        rounds = 0;
+      }
       const int hs_off = hs_base + ((nbuf == 2) ? (seq & 1) : 0) * H * BG;
       // P for this lane's outputs, fetched before the wait
       float pv[NOUT];
@@ -235,6 +283,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
         }
       }
       if (t > 0 && bs == pl.b_lo) spin_cycles(c.poll_delay);
+      if (tr) stamp0(t, 1);
       // the placed staging keeps fewer loads in flight (its table words take
       // registers of their own)
       constexpr int UPL = UMAX > 4 ? UMAX / 2 : UMAX;
@@ -245,13 +294,22 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
                              : stage_rows_placed<UPL>(hprev, t > 0, H, bs, nbg, smem_f + hs_off,
                                                       w, a.place + (size_t)pl.lc * (H >> 2)))
                  : (a.narrow ? stage_rows_narrow<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w)
-                             : stage_rows<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w));
+                             : stage_rows<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w,
+                                                TRACE ? &rounds : nullptr));
+      if (tr) {
+        stamp_max(t, 2, (uint32_t)clock64());
+        stamp_max(t, 7, rounds);
+      }
       if (!ok) {
         report_timeout(c.status, t, cta);
         s_abort = 1;
       }
       __syncthreads();
       if (s_abort) return;
+      if (tr) {
+        stamp0(t, 3);
+        if (t > 0) flush(t - 1, gt_last);
+      }
 
       // gather-multiply: entry = fp16 value (low half) | column << 16.  Batch
       // columns past nbg read a zero-filled or stale row and are never stored.
@@ -283,7 +341,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
           }
         }
       }
+      if (tr) stamp_max(t, 4, (uint32_t)clock64());
       if (TPR > 1) seg_reduce_scatter<BG, TPR>(acc, lane);
+      if (tr) stamp_max(t, 5, (uint32_t)clock64());
       if (owns && !(cta == c.drop_cta && t == c.drop_step)) {
 #pragma unroll
         for (int i = 0; i < NOUT; ++i) {
@@ -297,6 +357,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
           }
         }
       }
+      if (tr) stamp_max(t, 6, (uint32_t)clock64());
       if (nbuf == 1) __syncthreads();  // hs is overwritten by the next staging
     }
     if (c.sync_mode == 1) {
@@ -304,12 +365,16 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
       if (s_abort) return;
     }
   }
+  if (TRACE) {  // CTAs of a group without batch columns record nothing
+    __syncthreads();
+    if (c.T > 0 && pl.b_lo < pl.b_hi) flush(c.T - 1, gt_cur);
+  }
 }
 
 }  // namespace
 
-// Launch recur_sparse_kernel<tpr, bgroup, PLACED> for the plan in a.
-template <bool PLACED>
+// Launch recur_sparse_kernel<tpr, bgroup, PLACED, TRACE> for the plan in a.
+template <bool PLACED, bool TRACE = false>
 cudaError_t launch_recur_sparse_impl(const SparseRecurArgs& a, cudaStream_t s) {
   void* args[] = {const_cast<SparseRecurArgs*>(&a)};
   const int g = a.c.n_cta, nt = a.c.nthreads;
@@ -317,7 +382,7 @@ cudaError_t launch_recur_sparse_impl(const SparseRecurArgs& a, cudaStream_t s) {
   const int bg = a.bgroup;
 #define PRNN_SPARSE_CASE(T_, BG_) \
   if (a.tpr == T_ && bg == BG_)   \
-    return coop_launch(recur_sparse_kernel<T_, BG_, PLACED>, g, nt, sm, s, args);
+    return coop_launch(recur_sparse_kernel<T_, BG_, PLACED, TRACE>, g, nt, sm, s, args);
 #define PRNN_SPARSE_ROW(T_)                                                           \
   PRNN_SPARSE_CASE(T_, 1) PRNN_SPARSE_CASE(T_, 2) PRNN_SPARSE_CASE(T_, 4) PRNN_SPARSE_CASE(T_, 8) \
   PRNN_SPARSE_CASE(T_, 16) PRNN_SPARSE_CASE(T_, 32)

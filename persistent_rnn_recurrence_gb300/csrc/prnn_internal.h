@@ -179,9 +179,17 @@ struct SparseRecurArgs {
   const uint32_t* place; // [cpg][H/4] staging order of h (H % 128 == 0), or null:
                          // column c of group g = c/4 is staged at
                          // 128*(g/32) + 32*(c%4) + byte (c%4) of place[g]
+  uint32_t* trace;       // null, or [T][n_cta][kTraceWords] phase records (column
+                         // order and wide staging only)
 };
+// Words of one phase-trace record: globaltimer (2 words), then SM-clock stamps
+// (low 32 bits) of pass start, pause end, last poll fresh, barrier passed,
+// gathers done, reduction done, publish issued, then the most re-poll rounds,
+// the SM id and the CTA index.
+constexpr int kTraceWords = 12;
 cudaError_t launch_recur_sparse(const SparseRecurArgs& a, cudaStream_t s);
 cudaError_t launch_recur_sparse_placed(const SparseRecurArgs& a, cudaStream_t s);
+cudaError_t launch_recur_sparse_trace(const SparseRecurArgs& a, cudaStream_t s);
 size_t recur_sparse_smem(int H, int R, int ept, int tpr, int bgroup, bool dbuf);
 
 cudaError_t launch_sync_probe(const RecurCommon& c, int bgroup, cudaStream_t s);

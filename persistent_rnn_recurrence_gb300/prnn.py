@@ -35,6 +35,7 @@ PRNN_STACK_WAVEFRONT, PRNN_STACK_LAYERWISE = 0, 1
 EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
            "prnn_forward", "prnn_forward_host", "prnn_destroy", "prnn_get_status", "prnn_status_string",
            "prnn_set_option", "prnn_get_info", "prnn_get_timing", "prnn_probe_sync_floor",
+           "prnn_set_trace_buffer",
            "prnn_pack_sparse_host", "prnn_pack_sparse_host_placed", "prnn_forward_dense_noalloc",
            "prnn_set_weights_csr",
            "prnn_stack_create", "prnn_stack_set_layer", "prnn_stack_forward",
@@ -81,6 +82,7 @@ _sig = {
     "prnn_get_info": ([_P, ctypes.POINTER(prnn_info_t)], _I),
     "prnn_get_timing": ([_P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)], _I),
     "prnn_probe_sync_floor": ([_P, _I, _I, _P, _P], _I),
+    "prnn_set_trace_buffer": ([_P, _P, ctypes.c_size_t], _I),
     "prnn_pack_sparse_host": ([_I, _I, _I, _I, _I, _P, _P, _P, ctypes.c_size_t,
                                ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
     "prnn_pack_sparse_host_placed": ([_I, _I, _I, _I, _I, _P, _P, _P, ctypes.c_size_t, _P,
@@ -228,6 +230,12 @@ def prnn_pack_sparse_host_placed(hidden, k, n_cta, rows_per_cta, threads_per_row
 def prnn_probe_sync_floor(h: int, T: int, B: int, y, stream=None) -> None:
     _check(_lib.prnn_probe_sync_floor(h, T, B, _ptr(y), _stream(stream)),
            "prnn_probe_sync_floor")
+
+
+def prnn_set_trace_buffer(h: int, buf, nbytes: int) -> None:
+    """Set (or, with buf None, clear) the device buffer of the sparse
+    kernel's phase trace: [T][n_cta][12] uint32 records per forward."""
+    _check(_lib.prnn_set_trace_buffer(h, _ptr(buf), int(nbytes)), "prnn_set_trace_buffer")
 
 
 def prnn_pack_sparse_host(hidden, k, n_cta, rows_per_cta, threads_per_row, vals, cols):

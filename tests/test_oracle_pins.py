@@ -39,6 +39,33 @@ def test_cells_match_forward(o):
         assert np.array_equal(got, want)
 
 
+def test_delta_cells_match_backward(o):
+    """The single-element entry of the reverse recurrence (used by the GPU
+    backward checks and the smoke check) agrees with the whole-sequence
+    backward, element for element: delta_t[b, r] from dy_t, y_t and
+    delta_{t+1} (none at the last step), for dense weights and for a sparse
+    layer held densely.  A wrong callback order, a transposed Wh or a
+    time-shifted delta_{t+1} in the wrapper fails here."""
+    from persistent_rnn_recurrence_gb300 import synth
+    for p in (synth.make_problem(H=40, B=3, T=4, I=24, wdtype="f32", seed=11, h0_std=0.5),
+              synth.make_problem(H=36, B=2, T=5, k=9, seed=12, h0_std=0.3)):
+        dy = np.random.default_rng(13).normal(size=(p.T, p.B, p.H))
+        g = o.backward(p, dy)
+        d = g["delta"]
+        y = o.forward(p)
+        if p.sparse:
+            Wh = np.zeros((p.H, p.H))
+            Wh[np.repeat(np.arange(p.H), p.k), p.cols.astype(np.int64).ravel()] = \
+                p.vals.astype(np.float64).ravel()
+        else:
+            Wh = p.Wh
+        samples = [(t, b, r) for t in range(p.T) for b in range(p.B) for r in range(p.H)]
+        got = o.delta_cells(Wh, samples, lambda t, b: dy[t, b], lambda t, b: y[t, b],
+                            lambda t, b: None if t == p.T - 1 else d[t + 1, b])
+        assert np.array_equal(got, d.reshape(-1))
+        assert np.count_nonzero(got) > len(samples) // 4   # the check is not vacuous
+
+
 def test_threaded_driver_gives_the_same_bits(o):
     """The all-cores timing driver splits each step over threads but computes
     every output with the same cell function: the result must be bit-identical
@@ -135,3 +162,29 @@ def test_stack_pins_catch_planted_mistake(name):
     o = mod.Oracle(oracle.oracle.LIB)
     with pytest.raises(AssertionError):
         oracle_pins.pin_stack_definition(o)
+
+
+# Plausible mistakes in the Python wrapper of the reverse-recurrence cell,
+# planted in a copy of oracle.py; each must fail the element-for-element
+# comparison with the whole-sequence backward.
+DELTA_MUTANTS = {
+    "dy_and_y_swapped": ("_ptr(_f64(dy_of(t, bb))), _ptr(_f64(y_of(t, bb)))",
+                         "_ptr(_f64(y_of(t, bb))), _ptr(_f64(dy_of(t, bb)))"),
+    "wh_transposed": ("        Wh = _f64(Wh)\n        H = Wh.shape[0]\n        out = np.zeros(len(samples))",
+                      "        Wh = _f64(Wh).T.copy()\n        H = Wh.shape[0]\n        out = np.zeros(len(samples))"),
+    "next_delta_dropped": ("None if nx is None else _ptr(_f64(nx))", "None"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DELTA_MUTANTS))
+def test_delta_cells_pin_catches_planted_mistake(name):
+    import types
+    old, new = DELTA_MUTANTS[name]
+    path = os.path.join(ROOT, "oracle", "oracle.py")
+    src = open(path).read()
+    assert old in src, f"mutation anchor for {name} not found"
+    mod = types.ModuleType("oracle_mutant")
+    mod.__file__ = path
+    exec(compile(src.replace(old, new), path, "exec"), mod.__dict__)
+    with pytest.raises(AssertionError):
+        test_delta_cells_match_backward(mod.Oracle(oracle.oracle.LIB))

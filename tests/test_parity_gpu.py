@@ -407,6 +407,63 @@ def test_sync_floor_probe(env):
     assert ms > 0
 
 
+@pytest.mark.parametrize("spec", [dict(H=1792, B=4, T=12, k=179), dict(H=300, B=9, T=7, k=17)])
+def test_phase_trace(env, spec):
+    """The phase-trace build of the sparse kernel gives the same bits as the
+    default build and writes one well-formed record per step and CTA: its
+    CTA index, an SM id below the SM count, and stamps in phase order."""
+    torch, prnn, o = env
+    p = synth.make_problem(seed=84, **spec)
+    lay = prnn.Layer.from_problem(p)
+    try:
+        info = lay.info()
+        n = info["n_cta"]
+        x = torch.from_numpy(p.x).cuda()
+        y0 = lay.forward(x)
+        buf = torch.full((p.T * n * 12,), -1, dtype=torch.int32, device="cuda")
+        with pytest.raises(prnn.PrnnError) as e:                # too small for T steps
+            prnn.prnn_set_trace_buffer(lay.h, buf, buf.numel() * 4 - 4)
+            lay.forward(x)
+        assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+        with pytest.raises(prnn.PrnnError) as e:                # host memory
+            prnn.prnn_set_trace_buffer(lay.h, buf.cpu().data_ptr(), buf.numel() * 4)
+        assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+        prnn.prnn_set_trace_buffer(lay.h, buf, buf.numel() * 4)
+        y1 = lay.forward(x)
+        torch.cuda.synchronize()
+        assert lay.status() == prnn.PRNN_OK
+        prnn.prnn_set_trace_buffer(lay.h, None, 0)
+        y2 = lay.forward(x)
+        torch.cuda.synchronize()
+    finally:
+        lay.close()
+    assert torch.equal(y0, y1) and torch.equal(y0, y2)
+    check(y1.cpu().numpy(), o.forward(p), "f16", "traced")
+    rec = buf.view(p.T, n, 12).cpu().numpy().view(np.uint32).astype(np.int64)
+    # CTAs of a group that owns batch columns record every step; the others none
+    G = info["cta_groups"]
+    bl = -(-p.B // G)
+    active = np.array([(c // (n // G)) * bl < p.B for c in range(n)])
+    assert active.any()
+    assert (rec[:, ~active, :] == 0xffffffff).all()
+    rec = rec[:, active, :]
+    assert (rec[:, :, 11] == np.arange(n)[active][None, :]).all()
+    assert (rec[:, :, 10] < info["sm_count"]).all()
+    stamps = rec[:, :, 2:9]
+    steps = (np.diff(stamps, axis=2) & 0xffffffff)
+    assert (steps < (1 << 28)).all()            # every phase ends after the one before it
+    # a dense layer has no traced kernel
+    q = synth.make_problem(H=256, B=2, T=3, wdtype="f16", seed=85)
+    lay = prnn.Layer.from_problem(q)
+    try:
+        prnn.prnn_set_trace_buffer(lay.h, buf, buf.numel() * 4)
+        with pytest.raises(prnn.PrnnError) as e:
+            lay.forward(torch.from_numpy(q.x).cuda())
+        assert e.value.status == prnn.PRNN_ERR_UNSUPPORTED
+    finally:
+        lay.close()
+
+
 @pytest.mark.parametrize("spec", [dict(H=1152, B=4, T=20, wdtype="f16"),
                                   dict(H=1792, B=4, T=20, k=179)])
 def test_poll_delay_changes_timing_not_results(env, spec):
