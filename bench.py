@@ -66,6 +66,7 @@ def parse_args(argv=None):
                     help="phase trace of the sparse persistent kernel on the config's layer "
                          "(first --trace-steps steps): where the time of a step goes")
     ap.add_argument("--trace-steps", type=int, default=16)
+    ap.add_argument("--trace-out", default="", help="save the raw trace records (.npy)")
     ap.add_argument("--backward", action="store_true",
                     help="training step (forward + backward through time) of the named workloads")
     return ap.parse_args(argv)
@@ -1034,28 +1035,62 @@ def run_vendor(args):
     return 0
 
 
-TRACE_PHASES = ["pause", "wait_h", "stage_to_barrier", "gather", "reduce", "publish", "tail"]
+TRACE_PHASES = ["loop", "p_request", "pause", "wait_h", "stage_to_barrier", "gather", "reduce",
+                "publish"]
 
 
-def trace_phases(rec, clock_mhz):
-    """Per-phase durations (ns) of a trace array rec [R, T, n_cta, 12] (uint32):
-    one sample per (run, step, CTA) for steps 1 .. T-2, each a difference of
-    stamps from one SM's clock.  Returns {phase: numpy array of ns} plus
-    "step" (pass start to the next step's pass start) and "rounds"."""
+def trace_phases(rec, clock_mhz, groups=1):
+    """Where a step's time goes, from trace records rec [R, T, n_cta, 17, 16]
+    (uint32; slot 0 the CTA header, slot 1 + w warp w).  For every working CTA
+    and step 1 .. T-1 the CTA's critical path is taken as the latest warp at
+    each stamp, and the step is cut at those stamps: previous publish -> pass
+    start -> projection value requested -> pause end -> last poll fresh ->
+    barrier -> gathers -> reduction -> publish (SM-clock differences, mod
+    2^32).  Across CTAs, the globaltimer readings give the exchange: for each
+    CTA, its barrier time minus the last publish of the previous step in its
+    group ("exchange"), and the spread of the group's publishes ("publish_skew").
+    Returns {name: ns array} plus "rounds" and the timer's resolution."""
     import numpy as np
     r = rec.astype(np.int64)
-    c = r[..., 2:9]                          # 7 stamps: start, pause end, poll fresh, barrier,
-    d = lambda a, b: ((b - a) & 0xffffffff)  # gathers, reduction, publish (mod 2^32)
-    T = r.shape[1]
-    sl = slice(1, T - 1)
+    hdr = r[:, :, :, 0, :]
+    nw = int(hdr[..., 2].max())
+    n = r.shape[2]
+    active = hdr[0, 0, :, 1] == np.arange(n)
+    cta_group = np.arange(n) // max(1, n // groups)
+    w = r[:, :, :, 1:1 + nw, :]
+    base = w[..., 0].min(axis=3, keepdims=True)            # unwrap relative to the pass start
+    rel = (w[..., :8] - base[..., None]) & 0xffffffff
+    rel = np.where(rel >= (1 << 31), rel - (1 << 32), rel)
+    m = rel.max(axis=3)                                     # [R, T, C, 8]: latest warp
+    pub = m[..., 7] + base[..., 0]                          # absolute publish (latest warp)
     ns = 1e3 / clock_mhz
-    out = {}
-    for i, name in enumerate(TRACE_PHASES[:-1]):
-        out[name] = d(c[:, sl, :, i], c[:, sl, :, i + 1]).ravel() * ns
-    nxt = c[:, 2:T, :, 0]
-    out["tail"] = d(c[:, sl, :, 6], nxt).ravel() * ns
-    out["step"] = d(c[:, sl, :, 0], nxt).ravel() * ns
-    out["rounds"] = r[:, sl, :, 9].ravel()
+    T = r.shape[1]
+    sl = slice(1, T)
+    d = lambda a, b: (((b - a) + (1 << 31)) & 0xffffffff) - (1 << 31)
+    out = {"loop": d(pub[:, :-1], m[:, sl, :, 0] + base[:, sl, :, 0])}
+    for i, name in enumerate(TRACE_PHASES[1:]):
+        out[name] = m[:, sl, :, i + 1] - m[:, sl, :, i]
+    out["step"] = d(pub[:, :-1], pub[:, sl])
+    out["gather_warp"] = rel[:, sl, :, :, 5] - rel[:, sl, :, :, 4]
+    out["trace_record_write"] = d(w[:, sl, :, :, 7], w[:, sl, :, :, 13])
+    out = {k: np.asarray(v, dtype=np.float64)[:, :, active].ravel() * ns if k != "gather_warp"
+           else np.asarray(v, dtype=np.float64)[:, :, active].ravel() * ns
+           for k, v in out.items()}
+    gbar = ((w[..., 10] << 32) | w[..., 9]).max(axis=3)      # [R, T, C] ns
+    gpub = ((w[..., 12] << 32) | w[..., 11]).max(axis=3)
+    exch, skew = [], []
+    for g in np.unique(cta_group[active]):
+        cs = np.nonzero(active & (cta_group == g))[0]
+        last_pub = gpub[:, :-1][:, :, cs].max(axis=2)        # [R, T-1]
+        first_pub = gpub[:, :-1][:, :, cs].min(axis=2)
+        exch.append((gbar[:, 1:][:, :, cs] - last_pub[:, :, None]).ravel())
+        skew.append((last_pub - first_pub).ravel())
+    out["exchange"] = np.concatenate(exch).astype(np.float64)
+    out["publish_skew"] = np.concatenate(skew).astype(np.float64)
+    out["rounds"] = w[:, sl, :, :, 8].max(axis=3)[:, :, active].ravel()
+    u = np.unique(gbar)
+    du = np.diff(u)
+    out["globaltimer_resolution_ns"] = float(du[du > 0].min()) if du.size else 0.0
     return out
 
 
@@ -1064,7 +1099,8 @@ def run_trace(args):
     the config's layer for --trace-steps steps with the phase trace on (L2
     flushed before each forward), checks the traced output equals the
     untraced one bit for bit, and prints one JSON line of per-phase medians
-    and spreads (ns), the re-poll statistics and the trace's own overhead."""
+    and spreads (ns), the re-poll statistics and the trace's own overhead.
+    --trace-out saves the raw records (numpy .npy)."""
     import numpy as np
     import torch
     from persistent_rnn_recurrence_gb300 import prnn, synth
@@ -1080,7 +1116,8 @@ def run_trace(args):
     y1 = torch.empty_like(y0)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     n_cta = info["n_cta"]
-    buf = torch.zeros(p.T * n_cta * 12, dtype=torch.int32, device=dev)
+    W = 17 * 16
+    buf = torch.full((p.T * n_cta * W,), -1, dtype=torch.int32, device=dev)
     reps = max(3, min(args.steps, 20))
 
     def runs(traced):
@@ -1093,7 +1130,7 @@ def run_trace(args):
             if i >= 2:
                 ms.append(t)
                 if traced:
-                    recs.append(buf.view(p.T, n_cta, 12).cpu().numpy().view(np.uint32).copy())
+                    recs.append(buf.view(p.T, n_cta, 17, 16).cpu().numpy().view(np.uint32).copy())
         return sorted(ms)[len(ms) // 2], recs
 
     ms_plain, _ = runs(False)
@@ -1104,14 +1141,16 @@ def run_trace(args):
     lay.close()
     same = bool(torch.equal(y0, y1))
     clock_mhz = load_peaks().get("sm_max_mhz", 2070.0)  # the SM clock under load
-    ph = trace_phases(np.stack(recs), clock_mhz)
+    rec = np.stack(recs)
+    if args.trace_out:
+        np.save(args.trace_out, rec[:2])
+    ph = trace_phases(rec, clock_mhz, info["cta_groups"])
 
     def stats(a):
         a = np.sort(np.asarray(a, dtype=np.float64))
         q = lambda f: float(a[min(len(a) - 1, int(f * len(a)))])
         return {"median": q(0.5), "p10": q(0.1), "p90": q(0.9), "mean": float(a.mean())}
 
-    sm_ids = np.stack(recs)[..., 10]
     line = {"trace": p.name, "T": p.T, "B": p.B, "n_cta": n_cta,
             "cta_groups": info["cta_groups"], "rows_per_cta": info["rows_per_cta"],
             "threads_per_cta": info["threads_per_cta"], "threads_per_row": info["threads_per_row"],
@@ -1119,11 +1158,14 @@ def run_trace(args):
             "traced_equals_untraced": same, "clock_mhz_assumed": clock_mhz,
             "recurrence_us_per_step": {"plain": 1e3 * ms_plain / p.T,
                                        "traced": 1e3 * ms_traced / p.T},
-            "samples": int(ph["step"].size), "distinct_sms": int(np.unique(sm_ids).size),
-            "phases_ns": {k: stats(ph[k]) for k in TRACE_PHASES + ["step"]},
+            "samples": int(ph["step"].size),
+            "phases_ns": {k: stats(ph[k]) for k in TRACE_PHASES + ["step", "gather_warp",
+                                                                  "trace_record_write",
+                                                                  "exchange", "publish_skew"]},
             "repoll": {"mean_rounds": float(ph["rounds"].mean()),
                        "frac_ctas_first_poll_fresh": float((ph["rounds"] == 0).mean()),
-                       "max_rounds": int(ph["rounds"].max())}}
+                       "max_rounds": int(ph["rounds"].max())},
+            "globaltimer_resolution_ns": ph["globaltimer_resolution_ns"]}
     print(json.dumps(line), flush=True)
     return 0 if same and st == prnn.PRNN_OK else 1
 

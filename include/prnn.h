@@ -87,11 +87,16 @@ typedef enum {
                                      of small dependent MMAs is slower than the CUDA-core
                                      kernel), 2 = whenever it fits; takes effect at the next
                                      set_weights call                                           */
-  PRNN_OPT_STAGED_ORDER = 12      /* sparse, bank-aware, H % 128 == 0: 1 = each CTA stages h in
+  PRNN_OPT_STAGED_ORDER = 12,     /* sparse, bank-aware, H % 128 == 0: 1 = each CTA stages h in
                                      its own bank-balancing order (one lane per bank in every
                                      gather slot, at the cost of scattered staging stores);
                                      0 = column order (default); takes effect at the next
                                      set_weights call                                           */
+  PRNN_OPT_SPARSE_REG_WEIGHTS = 13 /* sparse persistent: 1 = the register-weight build of the
+                                     kernel (launch bound 384 threads, each thread's first 24
+                                     entries in registers) wherever its plan fits: at most 384
+                                     threads, batch passes of at most 4 columns, column order,
+                                     at least 24 entries per thread (default); 0 = never       */
 } prnn_option_t;
 
 /* Plan and sizes chosen at create / set_weights time (read-only report). */
@@ -109,6 +114,8 @@ typedef struct {
   int recurrent_tensor_cores;      /* 1 if the dense recurrence runs on tcgen05 (wide batch) */
   int sparse_staged_order;         /* sparse: 1 if each CTA stages h_{t-1} in its own
                                       bank-balancing order (prnn_pack_sparse_host_placed)   */
+  int sparse_reg_weights;          /* sparse: 1 if the forward at max_batch runs the
+                                      register-weight build (PRNN_OPT_SPARSE_REG_WEIGHTS)   */
 } prnn_info_t;
 
 /*
@@ -251,20 +258,25 @@ prnn_status_t prnn_get_timing(prnn_t h, float* ms_projection, float* ms_recurren
  * Phase trace of the sparse persistent kernel (a diagnostic; off unless a
  * buffer is set).  While `buffer` (a DEVICE pointer, 16-byte aligned, owned by
  * the caller) is set, every prnn_forward / prnn_forward_host of this handle
- * runs the trace build of the sparse kernel, which writes one record of 12
- * uint32 words per step and CTA, [T][n_cta][12], for the step's first batch
- * pass: globaltimer ns (low word, high word); SM clock (low 32 bits) at pass
- * start, at the end of the pause before the first poll, when the CTA's last
- * staging poll of h_{t-1} was fresh, after the CTA barrier, when the last warp
- * finished its gathers, its reduction and its publish; the most re-poll
- * rounds any thread needed; the SM id; the CTA index.  The pages time the
- * effect of each measure on whole steps (Sparse Persistent RNNs, measured-
- * effects table); this records where inside a step the time goes.  Results
- * are the same bits as without the trace.  Requires `bytes` >= T * n_cta * 48
- * at each forward (PRNN_ERR_INVALID_ARG otherwise) and a sparse layer on the
- * persistent path with column-order, wide staging (PRNN_ERR_UNSUPPORTED
- * otherwise).  buffer = NULL turns the trace off.  Errors: INVALID_ARG for a
- * misaligned, too small or non-device buffer.
+ * runs the trace build of the sparse kernel, which writes one record of
+ * 17 x 16 uint32 words per step and CTA, [T][n_cta][17][16], for the step's
+ * first batch pass.  Slot 0: SM id, CTA index, number of warps, then unused.
+ * Slot 1 + w, warp w: SM clock (low 32 bits) at pass start, after its
+ * projection value was requested, at the end of the pause before the first
+ * poll, when the warp's last staging poll of h_{t-1} was fresh, after the CTA
+ * barrier, after its gathers, its reduction and its publish; the most
+ * re-poll rounds any of its lanes needed; globaltimer ns (a device-wide clock)
+ * after the barrier (low word, high word) and after the publish (low, high);
+ * the SM clock after those readings; 2 unused.  Slots of warps the CTA does
+ * not have, and records of CTAs whose group has no batch column, are left as
+ * they were.
+ * The pages time the effect of each measure on whole steps (Sparse
+ * Persistent RNNs, measured-effects table); this records where inside a step
+ * the time goes.  Results are the same bits as without the trace.  Requires
+ * `bytes` >= T * n_cta * 1088 at each forward (PRNN_ERR_INVALID_ARG otherwise)
+ * and a sparse layer on the persistent path with column-order, wide staging
+ * (PRNN_ERR_UNSUPPORTED otherwise).  buffer = NULL turns the trace off.
+ * Errors: INVALID_ARG for a misaligned, too small or non-device buffer.
  */
 prnn_status_t prnn_set_trace_buffer(prnn_t h, void* buffer, size_t bytes);
 

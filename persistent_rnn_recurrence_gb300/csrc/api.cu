@@ -38,6 +38,7 @@ struct prnn_handle {
   int t_n_cta = 0, t_R = 0, t_G = 1, t_cpg = 0, t_N = 0, t_ring = 0;
   void* Wimg = nullptr;
   int wide_loads = 1, bank_aware = 1, staged_order = 0;
+  int regw_opt = 1;  // sparse: register-weight build of the kernel where its plan fits
   size_t onchip_bytes = 0, smem_at_max = 0;
   bool tc_proj = false;
   int Kp = 0;  // I rounded up to 64 (tcgen05 projection)
@@ -927,6 +928,7 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
       a.narrow = h->wide_loads ? 0 : 1;
       a.place = h->place;
       a.trace = h->trace;
+      a.regw = h->regw_opt && sparse_regw_fits(c.nthreads, bg, h->ept, h->place != nullptr);
       PRNN_TRY(launch_recur_sparse(a, s));
     } else if (h->rtc && h->sync_mode == 0) {
       DenseTcArgs a{};
@@ -1134,6 +1136,7 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
     a.dbuf = dbuf ? 1 : 0;
     a.narrow = 0;
     a.place = h->place_T;
+    a.regw = h->regw_opt && sparse_regw_fits(c.nthreads, bg, h->b_ept, h->place_T != nullptr);
     PRNN_TRY(launch_recur_sparse(a, s));
   } else {
     DenseRecurArgs a{};
@@ -1290,6 +1293,10 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
       if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
       h->staged_order = (int)value;
       return PRNN_OK;
+    case PRNN_OPT_SPARSE_REG_WEIGHTS:
+      if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
+      h->regw_opt = (int)value;
+      return PRNN_OK;
   }
   return PRNN_ERR_INVALID_ARG;
 }
@@ -1319,6 +1326,16 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
   info->nnz = h->sparse ? (size_t)h->H * h->k : (size_t)h->H * h->H;
   info->recurrent_tensor_cores = h->rtc ? 1 : 0;
   info->sparse_staged_order = h->sparse && h->place != nullptr ? 1 : 0;
+  if (h->sparse && h->algo == PRNN_ALGO_PERSISTENT && h->weights_set) {
+    int bg = 4;
+    bool db = false;
+    size_t sm = 0;
+    info->sparse_reg_weights =
+        h->regw_opt && sparse_batch_plan(h, h->maxB, &bg, &db, &sm) &&
+                sparse_regw_fits(h->nthreads, bg, h->ept, h->place != nullptr)
+            ? 1
+            : 0;
+  }
   if (h->rtc) {
     info->n_cta = h->t_n_cta;
     info->rows_per_cta = h->t_R;

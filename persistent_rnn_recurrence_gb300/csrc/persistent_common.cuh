@@ -14,6 +14,8 @@ namespace pk {
 constexpr int kSparseThreads = 512;
 constexpr int kCptMax = 4;          // 4-column chunks per thread of the dense kernel
 constexpr int kRegQ = 4;            // sparse: uint4 weight groups held in registers
+constexpr int kRegWThreads = 384;   // sparse register-weight build: threads per CTA at most
+constexpr int kRegQWide = 6;        // ... and the uint4 weight groups it holds in registers
 
 __device__ __forceinline__ unsigned ld_acquire_u(const unsigned* p) {
   unsigned v;

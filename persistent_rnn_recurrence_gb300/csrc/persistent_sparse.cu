@@ -61,9 +61,10 @@ size_t recur_sparse_smem(int H, int R, int ept, int tpr, int bgroup, bool dbuf) 
 cudaError_t launch_recur_sparse(const SparseRecurArgs& a, cudaStream_t s) {
   if (a.trace != nullptr) {
     if (a.place != nullptr || a.narrow) return cudaErrorNotSupported;
-    return launch_recur_sparse_trace(a, s);
+    return a.regw ? launch_recur_sparse_trace_regw(a, s) : launch_recur_sparse_trace(a, s);
   }
   if (a.place != nullptr) return launch_recur_sparse_placed(a, s);
+  if (a.regw) return launch_recur_sparse_regw(a, s);
   return launch_recur_sparse_impl<false>(a, s);
 }
 

@@ -28,14 +28,18 @@
 // Every wait is bounded (globaltimer deadline); on expiry the kernel records
 // a status word and every CTA leaves its time loop.
 //
-// Phase trace (opt-in, TRACE instantiations only): per step and CTA, SM-clock
-// stamps of the step's first batch pass -- pass start, end of the pause before
-// the first poll, last staging poll fresh (latest thread), CTA barrier passed,
-// gathers done, reduction done, publish issued (each latest over the CTA's
-// warps) -- plus the most re-poll rounds any thread needed, into a caller's
-// buffer [T][n_cta][kTraceWords].  Stamps of one record come from one SM's
-// clock, so differences within a record are exact; records of different
-// CTAs are aligned only through the globaltimer word.
+// Phase trace (opt-in, TRACE instantiations only): for the first batch pass
+// of every step, each warp's lane 0 keeps SM-clock stamps in registers -- pass
+// start, projection value requested, end of the pause before the first poll,
+// the warp's last staging poll fresh, CTA barrier passed, gathers done,
+// reduction done, publish issued -- the most re-poll rounds any lane of the
+// warp needed, and globaltimer readings just after the barrier and just after
+// the publish (one device-wide clock, 32 ns steps on GB300, so a producer's
+// publish and a consumer's barrier can be compared across SMs), and writes
+// them with four vector stores after its publish; warp 0 also writes a header
+// (SM id, CTA, warps).  No shared memory and no atomics, so the trace
+// disturbs the step little.  Layout: [T][n_cta][17][16] words, slot 0 the
+// header, slot 1 + w warp w.
 #pragma once
 #include "persistent_common.cuh"
 
@@ -169,19 +173,19 @@ __device__ __forceinline__ bool stage_rows_narrow_placed(const float* hprev, boo
 // ept entries of row r, packed 4 to a uint4 (wide loads); entry = fp16 value
 // | index << 16, padding entries have value 0.  The host places entries so
 // that the 32 lanes of a warp gather from different banks in each slot.  The
-// first kRegQ uint4 groups live in registers, the rest in smem.  The group's
+// first REGQ uint4 groups live in registers, the rest in smem: kRegQ groups
+// in the build for up to 512 threads, kRegQWide in the build for up to
+// kRegWThreads threads (MAXT), whose larger register budget holds them
+// without spilling and lets the compiler keep more gathers in flight.  The group's
 // h_{t-1} columns are staged in smem as [b][H] per batch pass of BG columns
 // (double-buffered when it fits, so one CTA barrier per pass); the index is
 // the column's position in that staging, which is the column itself or, with
 // a placement table, this CTA's bank-balancing order of the columns.
 // ---------------------------------------------------------------------------
-template <int TPR, int BG, bool PLACED, bool TRACE = false>
-__global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const SparseRecurArgs a) {
+template <int TPR, int BG, bool PLACED, bool TRACE = false, int MAXT = kSparseThreads>
+__global__ void __launch_bounds__(MAXT, 1) recur_sparse_kernel(const SparseRecurArgs a) {
   extern __shared__ __align__(16) float smem_f[];
   __shared__ int s_abort;
-  // phase stamps of the last three steps (slot t % 3: a slot is rewritten
-  // only after the CTA barrier that follows its flush)
-  __shared__ uint32_t s_tr[TRACE ? 3 : 1][TRACE ? 8 : 1];
   constexpr int UMAX = (BG >= 16) ? 4 : (BG == 8 ? 8 : 12);
   const RecurCommon& c = a.c;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -202,13 +206,12 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
     for (size_t i = tid; i < n16; i += NT) Ws[i] = __ldg(src + i);
   }
   if (tid == 0) s_abort = 0;
-  if (TRACE && tid < 24) (&s_tr[0][0])[tid] = 0u;
   __syncthreads();
 
   const int r = tid / TPR, s = tid % TPR;
   const bool has_row = r < pl.rows;
   const int row = pl.row0 + r;
-  constexpr int REGQ = (BG >= 16) ? 2 : kRegQ;
+  constexpr int REGQ = (BG >= 16) ? 2 : (MAXT <= kRegWThreads ? kRegQWide : kRegQ);
   uint4 wr[REGQ];
 #pragma unroll
   for (int i = 0; i < REGQ; ++i) {
@@ -224,31 +227,12 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
   w.status = c.status;
   w.timeout_ns = c.timeout_ns;
   w.backoff = c.poll_backoff;
-  // trace helpers: thread 0's own stamp, and the latest stamp over the CTA
-  // (warp maximum, then one shared atomic per warp)
-  uint64_t gt_cur = 0, gt_last = 0;
+  // trace state (registers of every lane; lane 0 of each warp writes it)
+  uint32_t ts[9] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+  uint64_t gt_bar = 0, gt_pub = 0;
   uint32_t rounds = 0;
-  auto stamp0 = [&](int t, int ph) {
-    if (TRACE && tid == 0) s_tr[t % 3][ph] = (uint32_t)clock64();
-  };
-  auto stamp_max = [&](int t, int ph, uint32_t v) {
-    if (TRACE) {
-      v = __reduce_max_sync(0xffffffffu, v);
-      if (lane == 0) atomicMax(&s_tr[t % 3][ph], v);
-    }
-  };
-  auto flush = [&](int t, uint64_t gt) {
-    if (TRACE && tid == 0 && a.trace != nullptr) {
-      uint32_t* rec = a.trace + ((size_t)t * c.n_cta + cta) * kTraceWords;
-      rec[0] = (uint32_t)gt;
-      rec[1] = (uint32_t)(gt >> 32);
-      for (int i = 0; i < 8; ++i) rec[2 + i] = s_tr[t % 3][i];
-      uint32_t sm;
-      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
-      rec[10] = sm;
-      rec[11] = (uint32_t)cta;
-      s_tr[t % 3][7] = 0u;  // the round count is a maximum, not a clock: restart it
-    }
+  auto stamp = [&](int ph) {
+    if (TRACE) ts[ph] = (uint32_t)clock64();
   };
   int seq = 0;
   for (int t = 0; t < c.T; ++t) {
@@ -261,11 +245,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
       const int nbg = min(BG, pl.b_hi - bs);
       const bool tr = TRACE && bs == pl.b_lo;  // the trace records each step's first pass
       if (tr) {
-        stamp0(t, 0);
-        if (tid == 0) {
-          gt_last = gt_cur;
-          gt_cur = global_ns();
-        }
+        stamp(0);
         rounds = 0;
       }
       const int hs_off = hs_base + ((nbuf == 2) ? (seq & 1) : 0) * H * BG;
@@ -282,8 +262,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
           owns = true;
         }
       }
+      if (tr) stamp(1);
       if (t > 0 && bs == pl.b_lo) spin_cycles(c.poll_delay);
-      if (tr) stamp0(t, 1);
+      if (tr) stamp(2);
       // the placed staging keeps fewer loads in flight (its table words take
       // registers of their own)
       constexpr int UPL = UMAX > 4 ? UMAX / 2 : UMAX;
@@ -297,8 +278,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
                              : stage_rows<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w,
                                                 TRACE ? &rounds : nullptr));
       if (tr) {
-        stamp_max(t, 2, (uint32_t)clock64());
-        stamp_max(t, 7, rounds);
+        ts[3] = __reduce_max_sync(0xffffffffu, (uint32_t)clock64());
+        ts[8] = __reduce_max_sync(0xffffffffu, rounds);
       }
       if (!ok) {
         report_timeout(c.status, t, cta);
@@ -307,8 +288,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
       __syncthreads();
       if (s_abort) return;
       if (tr) {
-        stamp0(t, 3);
-        if (t > 0) flush(t - 1, gt_last);
+        stamp(4);
+        if (lane == 0) gt_bar = global_ns();
       }
 
       // gather-multiply: entry = fp16 value (low half) | column << 16.  Batch
@@ -341,9 +322,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
           }
         }
       }
-      if (tr) stamp_max(t, 4, (uint32_t)clock64());
+      if (tr) stamp(5);
       if (TPR > 1) seg_reduce_scatter<BG, TPR>(acc, lane);
-      if (tr) stamp_max(t, 5, (uint32_t)clock64());
+      if (tr) stamp(6);
       if (owns && !(cta == c.drop_cta && t == c.drop_step)) {
 #pragma unroll
         for (int i = 0; i < NOUT; ++i) {
@@ -357,7 +338,24 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
           }
         }
       }
-      if (tr) stamp_max(t, 6, (uint32_t)clock64());
+      if (tr) {
+        stamp(7);
+        if (lane == 0 && a.trace != nullptr) {
+          gt_pub = global_ns();
+          uint32_t* rec = a.trace + ((size_t)t * c.n_cta + cta) * kTraceWords;
+          uint4* wr4 = reinterpret_cast<uint4*>(rec + 16 * (1 + (tid >> 5)));
+          wr4[0] = make_uint4(ts[0], ts[1], ts[2], ts[3]);
+          wr4[1] = make_uint4(ts[4], ts[5], ts[6], ts[7]);
+          wr4[2] = make_uint4(ts[8], (uint32_t)gt_bar, (uint32_t)(gt_bar >> 32), (uint32_t)gt_pub);
+          wr4[3] = make_uint4((uint32_t)(gt_pub >> 32), (uint32_t)clock64(), 0u, 0u);
+          if (tid == 0) {
+            uint32_t sm;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+            reinterpret_cast<uint4*>(rec)[0] =
+                make_uint4(sm, (uint32_t)cta, (uint32_t)(NT >> 5), 0u);
+          }
+        }
+      }
       if (nbuf == 1) __syncthreads();  // hs is overwritten by the next staging
     }
     if (c.sync_mode == 1) {
@@ -365,24 +363,33 @@ __global__ void __launch_bounds__(kSparseThreads, 1) recur_sparse_kernel(const S
       if (s_abort) return;
     }
   }
-  if (TRACE) {  // CTAs of a group without batch columns record nothing
-    __syncthreads();
-    if (c.T > 0 && pl.b_lo < pl.b_hi) flush(c.T - 1, gt_cur);
-  }
 }
 
 }  // namespace
 
-// Launch recur_sparse_kernel<tpr, bgroup, PLACED, TRACE> for the plan in a.
-template <bool PLACED, bool TRACE = false>
+// One instantiation of the kernel, launched cooperatively; combinations the
+// register-weight build does not serve are never instantiated.
+template <int T_, int BG_, bool PLACED, bool TRACE, int MAXT>
+cudaError_t launch_sparse_case(int g, int nt, size_t sm, cudaStream_t s, void** args) {
+  if constexpr (MAXT > kRegWThreads || BG_ <= 4)
+    return coop_launch(recur_sparse_kernel<T_, BG_, PLACED, TRACE, MAXT>, g, nt, sm, s, args);
+  else
+    return cudaErrorInvalidValue;
+}
+
+// Launch recur_sparse_kernel<tpr, bgroup, PLACED, TRACE, MAXT> for the plan
+// in a.  The register-weight build (MAXT = kRegWThreads) exists for batch
+// passes of up to 4 columns.
+template <bool PLACED, bool TRACE = false, int MAXT = kSparseThreads>
 cudaError_t launch_recur_sparse_impl(const SparseRecurArgs& a, cudaStream_t s) {
   void* args[] = {const_cast<SparseRecurArgs*>(&a)};
   const int g = a.c.n_cta, nt = a.c.nthreads;
   const size_t sm = a.c.smem;
   const int bg = a.bgroup;
+  if (nt > MAXT) return cudaErrorInvalidValue;
 #define PRNN_SPARSE_CASE(T_, BG_) \
   if (a.tpr == T_ && bg == BG_)   \
-    return coop_launch(recur_sparse_kernel<T_, BG_, PLACED, TRACE>, g, nt, sm, s, args);
+    return launch_sparse_case<T_, BG_, PLACED, TRACE, MAXT>(g, nt, sm, s, args);
 #define PRNN_SPARSE_ROW(T_)                                                           \
   PRNN_SPARSE_CASE(T_, 1) PRNN_SPARSE_CASE(T_, 2) PRNN_SPARSE_CASE(T_, 4) PRNN_SPARSE_CASE(T_, 8) \
   PRNN_SPARSE_CASE(T_, 16) PRNN_SPARSE_CASE(T_, 32)

@@ -9,4 +9,8 @@ cudaError_t launch_recur_sparse_trace(const SparseRecurArgs& a, cudaStream_t s) 
   return launch_recur_sparse_impl<false, true>(a, s);
 }
 
+cudaError_t launch_recur_sparse_trace_regw(const SparseRecurArgs& a, cudaStream_t s) {
+  return launch_recur_sparse_impl<false, true, kRegWThreads>(a, s);
+}
+
 }  // namespace prnn

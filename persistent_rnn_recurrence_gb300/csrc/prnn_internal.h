@@ -181,15 +181,29 @@ struct SparseRecurArgs {
                          // 128*(g/32) + 32*(c%4) + byte (c%4) of place[g]
   uint32_t* trace;       // null, or [T][n_cta][kTraceWords] phase records (column
                          // order and wide staging only)
+  int regw;              // 1: the register-weight build (column order, nthreads <=
+                         // 384, bgroup <= 4; see sparse_regw_fits)
 };
-// Words of one phase-trace record: globaltimer (2 words), then SM-clock stamps
-// (low 32 bits) of pass start, pause end, last poll fresh, barrier passed,
-// gathers done, reduction done, publish issued, then the most re-poll rounds,
-// the SM id and the CTA index.
-constexpr int kTraceWords = 12;
+// Whether the register-weight build of the sparse kernel serves a plan: at
+// most 384 threads, batch passes of at most 4 columns, column-order staging,
+// and at least 6 uint4 weight groups per thread (fewer would leave registers
+// holding zero-valued padding groups that still cost gathers).
+inline bool sparse_regw_fits(int nthreads, int bgroup, int ept, bool placed) {
+  return nthreads <= 384 && bgroup <= 4 && ept / 4 >= 6 && !placed;
+}
+// Words of one phase-trace record (one step, one CTA): 17 slots of 16 words.
+// Slot 0: SM id, CTA index, warps, then unused.  Slot 1 + w, warp w: SM-clock
+// stamps (low 32 bits) of pass start, projection value requested, pause end,
+// the warp's last staging poll fresh, barrier passed, gathers done, reduction
+// done, publish issued; the most re-poll rounds of the warp's lanes;
+// globaltimer ns after the barrier (low, high) and after the publish (low,
+// high); the SM clock after the record's globaltimer reads; 2 unused.
+constexpr int kTraceWords = 17 * 16;
 cudaError_t launch_recur_sparse(const SparseRecurArgs& a, cudaStream_t s);
 cudaError_t launch_recur_sparse_placed(const SparseRecurArgs& a, cudaStream_t s);
 cudaError_t launch_recur_sparse_trace(const SparseRecurArgs& a, cudaStream_t s);
+cudaError_t launch_recur_sparse_regw(const SparseRecurArgs& a, cudaStream_t s);
+cudaError_t launch_recur_sparse_trace_regw(const SparseRecurArgs& a, cudaStream_t s);
 size_t recur_sparse_smem(int H, int R, int ept, int tpr, int bgroup, bool dbuf);
 
 cudaError_t launch_sync_probe(const RecurCommon& c, int bgroup, cudaStream_t s);

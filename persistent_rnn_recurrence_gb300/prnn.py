@@ -25,10 +25,11 @@ PRNN_OK, PRNN_ERR_INVALID_ARG, PRNN_ERR_UNSUPPORTED, PRNN_ERR_NOT_READY, \
     PRNN_ERR_CUDA, PRNN_ERR_OOM, PRNN_ERR_TIMEOUT = range(7)
 PRNN_F32, PRNN_F16 = 0, 1
 PRNN_ALGO_PERSISTENT, PRNN_ALGO_PER_STEP = 0, 1
-PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA, \
-    PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION, PRNN_OPT_CTA_GROUPS, \
-    PRNN_OPT_WIDE_LOADS, PRNN_OPT_BANK_AWARE, PRNN_OPT_POLL_DELAY_NS, \
-    PRNN_OPT_POLL_BACKOFF_NS, PRNN_OPT_RECURRENT_TC, PRNN_OPT_STAGED_ORDER = range(13)
+(PRNN_OPT_WAIT_TIMEOUT_US, PRNN_OPT_SYNC_MODE, PRNN_OPT_DEBUG_DROP_CTA,
+ PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION, PRNN_OPT_CTA_GROUPS,
+ PRNN_OPT_WIDE_LOADS, PRNN_OPT_BANK_AWARE, PRNN_OPT_POLL_DELAY_NS,
+ PRNN_OPT_POLL_BACKOFF_NS, PRNN_OPT_RECURRENT_TC, PRNN_OPT_STAGED_ORDER,
+ PRNN_OPT_SPARSE_REG_WEIGHTS) = range(14)
 
 PRNN_STACK_WAVEFRONT, PRNN_STACK_LAYERWISE = 0, 1
 
@@ -50,7 +51,7 @@ class prnn_info_t(ctypes.Structure):
         "threads_per_row", "projection_tensor_cores", "sparse_bank_cap", "cta_groups")] + [
         ("smem_bytes", ctypes.c_size_t), ("onchip_weight_bytes", ctypes.c_size_t),
         ("nnz", ctypes.c_size_t), ("recurrent_tensor_cores", ctypes.c_int),
-        ("sparse_staged_order", ctypes.c_int)]
+        ("sparse_staged_order", ctypes.c_int), ("sparse_reg_weights", ctypes.c_int)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -407,22 +407,68 @@ def test_sync_floor_probe(env):
     assert ms > 0
 
 
+@pytest.mark.parametrize("spec", [dict(H=1792, B=4, T=24, k=179),
+                                  dict(H=5760, B=4, T=10, k=57, h0_std=0.2),
+                                  dict(H=1152, B=2, T=16, k=230),
+                                  dict(H=640, B=3, T=9, k=96)])
+def test_register_weight_build_gives_the_same_bits(env, spec):
+    """The register-weight build of the sparse kernel (384-thread launch
+    bound, 24 entries per thread in registers) reads the same entries in the
+    same order as the default build: same bits, forward and backward, and
+    both within the rule of the oracle."""
+    torch, prnn, o = env
+    p = synth.make_problem(seed=86, **spec)
+    ys, deltas = [], []
+    for opt in (1, 0):
+        lay = prnn.Layer.from_problem(p)
+        try:
+            lay.set_option(prnn.PRNN_OPT_SPARSE_REG_WEIGHTS, opt)
+            info = lay.info()
+            x = torch.from_numpy(p.x).cuda()
+            h0 = None if p.h0 is None else torch.from_numpy(p.h0).cuda()
+            y = lay.forward(x, h0)
+            dy = torch.ones_like(y)
+            g = lay.backward(x, y, dy, h0)
+            torch.cuda.synchronize()
+            assert lay.status() == prnn.PRNN_OK
+        finally:
+            lay.close()
+        ys.append(y)
+        deltas.append(g["delta"])
+        if opt == 1:
+            fits = info["threads_per_cta"] <= 384 and info["k_padded"] // info["threads_per_row"] >= 24
+            assert info["sparse_reg_weights"] == (1 if fits else 0)
+        else:
+            assert info["sparse_reg_weights"] == 0
+    assert torch.equal(ys[0], ys[1]) and torch.equal(deltas[0], deltas[1])
+    check(ys[0].cpu().numpy(), o.forward(p), "f16", "register weights")
+    lay = prnn.Layer.from_problem(p)
+    try:
+        with pytest.raises(prnn.PrnnError) as e:
+            lay.set_option(prnn.PRNN_OPT_SPARSE_REG_WEIGHTS, 2)
+        assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+    finally:
+        lay.close()
+
+
 @pytest.mark.parametrize("spec", [dict(H=1792, B=4, T=12, k=179), dict(H=300, B=9, T=7, k=17)])
 def test_phase_trace(env, spec):
     """The phase-trace build of the sparse kernel gives the same bits as the
-    default build and writes one well-formed record per step and CTA: its
-    CTA index, an SM id below the SM count, and stamps in phase order."""
+    default build and writes one well-formed record per step and working CTA:
+    its CTA index, an SM id below the SM count, its warp count, and per warp
+    stamps in phase order; CTAs without batch columns write nothing."""
     torch, prnn, o = env
     p = synth.make_problem(seed=84, **spec)
+    W = 17 * 16
     lay = prnn.Layer.from_problem(p)
     try:
         info = lay.info()
         n = info["n_cta"]
         x = torch.from_numpy(p.x).cuda()
         y0 = lay.forward(x)
-        buf = torch.full((p.T * n * 12,), -1, dtype=torch.int32, device="cuda")
+        buf = torch.full((p.T * n * W,), -1, dtype=torch.int32, device="cuda")
         with pytest.raises(prnn.PrnnError) as e:                # too small for T steps
-            prnn.prnn_set_trace_buffer(lay.h, buf, buf.numel() * 4 - 4)
+            prnn.prnn_set_trace_buffer(lay.h, buf, buf.numel() * 4 - 16)
             lay.forward(x)
         assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
         with pytest.raises(prnn.PrnnError) as e:                # host memory
@@ -439,19 +485,24 @@ def test_phase_trace(env, spec):
         lay.close()
     assert torch.equal(y0, y1) and torch.equal(y0, y2)
     check(y1.cpu().numpy(), o.forward(p), "f16", "traced")
-    rec = buf.view(p.T, n, 12).cpu().numpy().view(np.uint32).astype(np.int64)
-    # CTAs of a group that owns batch columns record every step; the others none
+    rec = buf.view(p.T, n, 17, 16).cpu().numpy().view(np.uint32).astype(np.int64)
     G = info["cta_groups"]
     bl = -(-p.B // G)
     active = np.array([(c // (n // G)) * bl < p.B for c in range(n)])
     assert active.any()
-    assert (rec[:, ~active, :] == 0xffffffff).all()
-    rec = rec[:, active, :]
-    assert (rec[:, :, 11] == np.arange(n)[active][None, :]).all()
-    assert (rec[:, :, 10] < info["sm_count"]).all()
-    stamps = rec[:, :, 2:9]
-    steps = (np.diff(stamps, axis=2) & 0xffffffff)
-    assert (steps < (1 << 28)).all()            # every phase ends after the one before it
+    assert (rec[:, ~active] == 0xffffffff).all()
+    rec = rec[:, active]
+    nw = info["threads_per_cta"] // 32
+    assert (rec[:, :, 0, 1] == np.arange(n)[active][None, :]).all()
+    assert (rec[:, :, 0, 0] < info["sm_count"]).all()
+    assert (rec[:, :, 0, 2] == nw).all()
+    assert (rec[:, :, 1 + nw:] == 0xffffffff).all()
+    stamps = rec[:, :, 1:1 + nw, :8]
+    gaps = np.diff(stamps, axis=3) & 0xffffffff
+    assert (gaps < (1 << 28)).all()             # every phase ends after the one before it
+    gbar = (rec[:, :, 1:1 + nw, 10] << 32) | rec[:, :, 1:1 + nw, 9]
+    gpub = (rec[:, :, 1:1 + nw, 12] << 32) | rec[:, :, 1:1 + nw, 11]
+    assert (gpub >= gbar).all() and (np.diff(gpub.max(axis=2), axis=0) > 0).all()
     # a dense layer has no traced kernel
     q = synth.make_problem(H=256, B=2, T=3, wdtype="f16", seed=85)
     lay = prnn.Layer.from_problem(q)
