@@ -92,11 +92,16 @@ typedef enum {
                                      gather slot, at the cost of scattered staging stores);
                                      0 = column order (default); takes effect at the next
                                      set_weights call                                           */
-  PRNN_OPT_SPARSE_REG_WEIGHTS = 13 /* sparse persistent: 1 = the register-weight build of the
+  PRNN_OPT_SPARSE_REG_WEIGHTS = 13,/* sparse persistent: 1 = the register-weight build of the
                                      kernel (launch bound 384 threads, each thread's first 24
                                      entries in registers) wherever its plan fits: at most 384
                                      threads, batch passes of at most 4 columns, column order,
                                      at least 24 entries per thread (default); 0 = never       */
+  PRNN_OPT_SPARSE_STAGING_DEPTH = 14 /* sparse persistent, column order, passes of at most 4
+                                     columns: 1 = stage h_{t-1} with the fewest float4 loads in
+                                     flight per thread (2 or 6) that cover the thread's share of
+                                     a pass in one round (default); 0 = always 12.  The sync
+                                     floor probe follows the same choice                       */
 } prnn_option_t;
 
 /* Plan and sizes chosen at create / set_weights time (read-only report). */

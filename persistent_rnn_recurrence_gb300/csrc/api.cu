@@ -39,6 +39,7 @@ struct prnn_handle {
   void* Wimg = nullptr;
   int wide_loads = 1, bank_aware = 1, staged_order = 0;
   int regw_opt = 1;  // sparse: register-weight build of the kernel where its plan fits
+  int depth_opt = 1; // sparse: staging depth matched to the plan (0: always 12)
   size_t onchip_bytes = 0, smem_at_max = 0;
   bool tc_proj = false;
   int Kp = 0;  // I rounded up to 64 (tcgen05 projection)
@@ -929,6 +930,7 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
       a.place = h->place;
       a.trace = h->trace;
       a.regw = h->regw_opt && sparse_regw_fits(c.nthreads, bg, h->ept, h->place != nullptr);
+      a.umax = h->depth_opt ? sparse_staging_depth(h->H, bg, c.nthreads, h->place != nullptr) : 0;
       PRNN_TRY(launch_recur_sparse(a, s));
     } else if (h->rtc && h->sync_mode == 0) {
       DenseTcArgs a{};
@@ -1137,6 +1139,7 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
     a.narrow = 0;
     a.place = h->place_T;
     a.regw = h->regw_opt && sparse_regw_fits(c.nthreads, bg, h->b_ept, h->place_T != nullptr);
+    a.umax = h->depth_opt ? sparse_staging_depth(h->H, bg, c.nthreads, h->place_T != nullptr) : 0;
     PRNN_TRY(launch_recur_sparse(a, s));
   } else {
     DenseRecurArgs a{};
@@ -1297,6 +1300,10 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
       if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
       h->regw_opt = (int)value;
       return PRNN_OK;
+    case PRNN_OPT_SPARSE_STAGING_DEPTH:
+      if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
+      h->depth_opt = (int)value;
+      return PRNN_OK;
   }
   return PRNN_ERR_INVALID_ARG;
 }
@@ -1387,7 +1394,14 @@ prnn_status_t prnn_probe_sync_floor(prnn_t h, int T, int B, float* y, void* stre
   if (!y || !aligned16(y)) return PRNN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int bl = (B + h->G - 1) / h->G;
-  const int bg = std::min(32, std::max(4, round_up(bl, 4)));
+  int bg = std::min(32, std::max(4, round_up(bl, 4)));
+  int um = 0;
+  if (h->sparse) {  // the sparse forward's batch passes and staging depth
+    bool db = false;
+    size_t sm = 0;
+    if (!sparse_batch_plan(h, B, &bg, &db, &sm)) return PRNN_ERR_UNSUPPORTED;
+    um = h->depth_opt ? sparse_staging_depth(h->H, bg, h->nthreads, h->place != nullptr) : 0;
+  }
   RecurCommon c = common_args(h, T, B, nullptr, y);
   c.smem = sync_probe_smem(h->H, bg);
   if (c.smem > h->smem_optin) return PRNN_ERR_UNSUPPORTED;
@@ -1395,7 +1409,7 @@ prnn_status_t prnn_probe_sync_floor(prnn_t h, int T, int B, float* y, void* stre
   h->last_backward = false;
   PRNN_TRY(launch_fill_sentinel(y, (size_t)T * B * h->H, s));
   if (h->timing) PRNN_TRY(cudaEventRecord(h->ev[1], s));
-  PRNN_TRY(launch_sync_probe(c, bg, s));
+  PRNN_TRY(launch_sync_probe(c, bg, um, s));
   if (h->timing) {
     PRNN_TRY(cudaEventRecord(h->ev[2], s));
     h->ev_valid = true;

@@ -14,6 +14,7 @@ namespace {
 // Sync-floor probe: the sparse kernel's exchange (stage the group's columns of
 // h_{t-1}, one CTA barrier, publish R rows of h_t) with no arithmetic.
 // ---------------------------------------------------------------------------
+template <int UMAX>
 __global__ void __launch_bounds__(kSparseThreads, 1) sync_probe_kernel(const RecurCommon c, int BG) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int s_abort;
@@ -35,7 +36,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sync_probe_kernel(const Rec
       const int nbg = min(BG, pl.b_hi - bs);
       bool ok = true;
       if (t > 0 && bs == pl.b_lo) spin_cycles(c.poll_delay);
-      if (t > 0) ok = stage_rows<8>(hprev, true, H, bs, nbg, hs, w);
+      if (t > 0) ok = stage_rows<UMAX>(hprev, true, H, bs, nbg, hs, w);
       if (!ok) {
         report_timeout(c.status, t, cta);
         s_abort = 1;
@@ -65,15 +66,21 @@ cudaError_t launch_recur_sparse(const SparseRecurArgs& a, cudaStream_t s) {
   }
   if (a.place != nullptr) return launch_recur_sparse_placed(a, s);
   if (a.regw) return launch_recur_sparse_regw(a, s);
+  if (a.umax != 0) return launch_recur_sparse_um(a, s);
   return launch_recur_sparse_impl<false>(a, s);
 }
 
 size_t sync_probe_smem(int H, int bgroup) { return (size_t)H * bgroup * sizeof(float); }
 
-cudaError_t launch_sync_probe(const RecurCommon& c, int bgroup, cudaStream_t s) {
+cudaError_t launch_sync_probe(const RecurCommon& c, int bgroup, int umax, cudaStream_t s) {
   int bg = bgroup;
   void* args[] = {const_cast<RecurCommon*>(&c), &bg};
-  return coop_launch(sync_probe_kernel, c.n_cta, c.nthreads, c.smem, s, args);
+  switch (umax) {
+    case 0: return coop_launch(sync_probe_kernel<8>, c.n_cta, c.nthreads, c.smem, s, args);
+    case 2: return coop_launch(sync_probe_kernel<2>, c.n_cta, c.nthreads, c.smem, s, args);
+    case 6: return coop_launch(sync_probe_kernel<6>, c.n_cta, c.nthreads, c.smem, s, args);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace prnn

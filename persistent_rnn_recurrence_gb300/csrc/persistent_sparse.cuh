@@ -182,11 +182,20 @@ __device__ __forceinline__ bool stage_rows_narrow_placed(const float* hprev, boo
 // the column's position in that staging, which is the column itself or, with
 // a placement table, this CTA's bank-balancing order of the columns.
 // ---------------------------------------------------------------------------
-template <int TPR, int BG, bool PLACED, bool TRACE = false, int MAXT = kSparseThreads>
+//
+// Staging depth UM: the float4 loads of h_{t-1} a thread keeps in flight per
+// round.  The launcher picks the smallest of 2, 6 or 12 (UM = 0: 12, and 8 or
+// 4 for passes of 8 or more columns) that covers the thread's share of a pass
+// in one round: a deeper unrolled staging than the pass needs costs
+// registers and code on the step's critical path -- at the 10 % layer of
+// 1792 units, 12 slots where 2 suffice cost 0.38 us of a 1.66 us step.
+template <int TPR, int BG, bool PLACED, bool TRACE = false, int MAXT = kSparseThreads, int UM = 0>
 __global__ void __launch_bounds__(MAXT, 1) recur_sparse_kernel(const SparseRecurArgs a) {
   extern __shared__ __align__(16) float smem_f[];
   __shared__ int s_abort;
-  constexpr int UMAX = (BG >= 16) ? 4 : (BG == 8 ? 8 : 12);
+  constexpr int UMAX = UM > 0 ? UM : ((BG >= 16) ? 4 : (BG == 8 ? 8 : 12));
+  // the 32-bit staging of the ablation moves a quarter of the bytes per load
+  constexpr int UNAR = UM > 0 ? (4 * UM < 12 ? 4 * UM : 12) : UMAX;
   const RecurCommon& c = a.c;
   const int tid = threadIdx.x, lane = tid & 31;
   const int NT = blockDim.x;
@@ -274,7 +283,7 @@ __global__ void __launch_bounds__(MAXT, 1) recur_sparse_kernel(const SparseRecur
                                                              a.place + (size_t)pl.lc * (H >> 2))
                              : stage_rows_placed<UPL>(hprev, t > 0, H, bs, nbg, smem_f + hs_off,
                                                       w, a.place + (size_t)pl.lc * (H >> 2)))
-                 : (a.narrow ? stage_rows_narrow<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w)
+                 : (a.narrow ? stage_rows_narrow<UNAR>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w)
                              : stage_rows<UMAX>(hprev, t > 0, H, bs, nbg, smem_f + hs_off, w,
                                                 TRACE ? &rounds : nullptr));
       if (tr) {
@@ -367,20 +376,21 @@ __global__ void __launch_bounds__(MAXT, 1) recur_sparse_kernel(const SparseRecur
 
 }  // namespace
 
-// One instantiation of the kernel, launched cooperatively; combinations the
-// register-weight build does not serve are never instantiated.
-template <int T_, int BG_, bool PLACED, bool TRACE, int MAXT>
+// One instantiation of the kernel, launched cooperatively; combinations that
+// are never planned (the register-weight build or a chosen staging depth with
+// passes of more than 4 columns) are never instantiated.
+template <int T_, int BG_, bool PLACED, bool TRACE, int MAXT, int UM>
 cudaError_t launch_sparse_case(int g, int nt, size_t sm, cudaStream_t s, void** args) {
-  if constexpr (MAXT > kRegWThreads || BG_ <= 4)
-    return coop_launch(recur_sparse_kernel<T_, BG_, PLACED, TRACE, MAXT>, g, nt, sm, s, args);
+  if constexpr ((MAXT > kRegWThreads && UM == 0) || BG_ <= 4)
+    return coop_launch(recur_sparse_kernel<T_, BG_, PLACED, TRACE, MAXT, UM>, g, nt, sm, s, args);
   else
     return cudaErrorInvalidValue;
 }
 
-// Launch recur_sparse_kernel<tpr, bgroup, PLACED, TRACE, MAXT> for the plan
-// in a.  The register-weight build (MAXT = kRegWThreads) exists for batch
-// passes of up to 4 columns.
-template <bool PLACED, bool TRACE = false, int MAXT = kSparseThreads>
+// Launch recur_sparse_kernel<tpr, bgroup, PLACED, TRACE, MAXT, UM> for the
+// plan in a.  The register-weight build (MAXT = kRegWThreads) and the chosen
+// staging depths (UM > 0) exist for batch passes of up to 4 columns.
+template <bool PLACED, bool TRACE = false, int MAXT = kSparseThreads, int UM = 0>
 cudaError_t launch_recur_sparse_impl(const SparseRecurArgs& a, cudaStream_t s) {
   void* args[] = {const_cast<SparseRecurArgs*>(&a)};
   const int g = a.c.n_cta, nt = a.c.nthreads;
@@ -389,7 +399,7 @@ cudaError_t launch_recur_sparse_impl(const SparseRecurArgs& a, cudaStream_t s) {
   if (nt > MAXT) return cudaErrorInvalidValue;
 #define PRNN_SPARSE_CASE(T_, BG_) \
   if (a.tpr == T_ && bg == BG_)   \
-    return launch_sparse_case<T_, BG_, PLACED, TRACE, MAXT>(g, nt, sm, s, args);
+    return launch_sparse_case<T_, BG_, PLACED, TRACE, MAXT, UM>(g, nt, sm, s, args);
 #define PRNN_SPARSE_ROW(T_)                                                           \
   PRNN_SPARSE_CASE(T_, 1) PRNN_SPARSE_CASE(T_, 2) PRNN_SPARSE_CASE(T_, 4) PRNN_SPARSE_CASE(T_, 8) \
   PRNN_SPARSE_CASE(T_, 16) PRNN_SPARSE_CASE(T_, 32)
@@ -397,6 +407,18 @@ cudaError_t launch_recur_sparse_impl(const SparseRecurArgs& a, cudaStream_t s) {
   PRNN_SPARSE_ROW(16) PRNN_SPARSE_ROW(32)
 #undef PRNN_SPARSE_ROW
 #undef PRNN_SPARSE_CASE
+  return cudaErrorInvalidValue;
+}
+
+// The column-order builds of one launch bound and trace setting, for each
+// staging depth the launcher may choose (a.umax: 0, 2 or 6).
+template <bool TRACE, int MAXT>
+cudaError_t launch_recur_sparse_depth(const SparseRecurArgs& a, cudaStream_t s) {
+  switch (a.umax) {
+    case 0: return launch_recur_sparse_impl<false, TRACE, MAXT, 0>(a, s);
+    case 2: return launch_recur_sparse_impl<false, TRACE, MAXT, 2>(a, s);
+    case 6: return launch_recur_sparse_impl<false, TRACE, MAXT, 6>(a, s);
+  }
   return cudaErrorInvalidValue;
 }
 

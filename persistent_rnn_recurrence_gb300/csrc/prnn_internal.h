@@ -183,7 +183,18 @@ struct SparseRecurArgs {
                          // order and wide staging only)
   int regw;              // 1: the register-weight build (column order, nthreads <=
                          // 384, bgroup <= 4; see sparse_regw_fits)
+  int umax;              // staging depth (float4 loads per thread per round): 0 for
+                         // the default (12 for passes of <= 4 columns), or 2 or 6
+                         // (column order, bgroup <= 4; see sparse_staging_depth)
 };
+// The staging depth for a column-order pass of bgroup columns of H over
+// nthreads threads: the smallest of 2, 6 (else 0: the default 12) that covers
+// each thread's share of the pass in one round.
+inline int sparse_staging_depth(int H, int bgroup, int nthreads, bool placed) {
+  if (placed || bgroup > 4 || nthreads < 1) return 0;
+  const int need = (bgroup * (H / 4) + nthreads - 1) / nthreads;
+  return need <= 2 ? 2 : (need <= 6 ? 6 : 0);
+}
 // Whether the register-weight build of the sparse kernel serves a plan: at
 // most 384 threads, batch passes of at most 4 columns, column-order staging,
 // and at least 6 uint4 weight groups per thread (fewer would leave registers
@@ -202,11 +213,14 @@ constexpr int kTraceWords = 17 * 16;
 cudaError_t launch_recur_sparse(const SparseRecurArgs& a, cudaStream_t s);
 cudaError_t launch_recur_sparse_placed(const SparseRecurArgs& a, cudaStream_t s);
 cudaError_t launch_recur_sparse_trace(const SparseRecurArgs& a, cudaStream_t s);
+cudaError_t launch_recur_sparse_um(const SparseRecurArgs& a, cudaStream_t s);
 cudaError_t launch_recur_sparse_regw(const SparseRecurArgs& a, cudaStream_t s);
 cudaError_t launch_recur_sparse_trace_regw(const SparseRecurArgs& a, cudaStream_t s);
 size_t recur_sparse_smem(int H, int R, int ept, int tpr, int bgroup, bool dbuf);
 
-cudaError_t launch_sync_probe(const RecurCommon& c, int bgroup, cudaStream_t s);
+// The sparse kernel's exchange with no arithmetic; umax as in SparseRecurArgs
+// (0 here: 8 float4 in flight per thread).
+cudaError_t launch_sync_probe(const RecurCommon& c, int bgroup, int umax, cudaStream_t s);
 
 // Host packing of row-balanced sparse rows into the kernel layout (pack.cu).
 // vals/cols: [H][k]; writes out_packed[n_cta][R][ept/4][tpr][4]; returns ept.

@@ -410,19 +410,23 @@ def test_sync_floor_probe(env):
 @pytest.mark.parametrize("spec", [dict(H=1792, B=4, T=24, k=179),
                                   dict(H=5760, B=4, T=10, k=57, h0_std=0.2),
                                   dict(H=1152, B=2, T=16, k=230),
-                                  dict(H=640, B=3, T=9, k=96)])
+                                  dict(H=640, B=3, T=9, k=96),
+                                  dict(H=2304, B=16, T=8, k=230),
+                                  dict(H=4096, B=4, T=6, k=409, h0_std=0.2)])
 def test_register_weight_build_gives_the_same_bits(env, spec):
     """The register-weight build of the sparse kernel (384-thread launch
-    bound, 24 entries per thread in registers) reads the same entries in the
-    same order as the default build: same bits, forward and backward, and
-    both within the rule of the oracle."""
+    bound, 24 entries per thread in registers) and the plan-matched staging
+    depth (2 or 6 float4 loads in flight instead of 12) change where values
+    wait, not what is summed in which order: every on/off combination gives
+    the same bits, forward and backward, within the rule of the oracle."""
     torch, prnn, o = env
     p = synth.make_problem(seed=86, **spec)
     ys, deltas = [], []
-    for opt in (1, 0):
+    for regw, depth in ((1, 1), (0, 0), (1, 0), (0, 1)):
         lay = prnn.Layer.from_problem(p)
         try:
-            lay.set_option(prnn.PRNN_OPT_SPARSE_REG_WEIGHTS, opt)
+            lay.set_option(prnn.PRNN_OPT_SPARSE_REG_WEIGHTS, regw)
+            lay.set_option(prnn.PRNN_OPT_SPARSE_STAGING_DEPTH, depth)
             info = lay.info()
             x = torch.from_numpy(p.x).cuda()
             h0 = None if p.h0 is None else torch.from_numpy(p.h0).cuda()
@@ -435,18 +439,17 @@ def test_register_weight_build_gives_the_same_bits(env, spec):
             lay.close()
         ys.append(y)
         deltas.append(g["delta"])
-        if opt == 1:
-            fits = info["threads_per_cta"] <= 384 and info["k_padded"] // info["threads_per_row"] >= 24
-            assert info["sparse_reg_weights"] == (1 if fits else 0)
-        else:
-            assert info["sparse_reg_weights"] == 0
-    assert torch.equal(ys[0], ys[1]) and torch.equal(deltas[0], deltas[1])
+        fits = info["threads_per_cta"] <= 384 and info["k_padded"] // info["threads_per_row"] >= 24
+        assert info["sparse_reg_weights"] == (1 if fits and regw else 0)
+    for y, d in zip(ys[1:], deltas[1:]):
+        assert torch.equal(ys[0], y) and torch.equal(deltas[0], d)
     check(ys[0].cpu().numpy(), o.forward(p), "f16", "register weights")
     lay = prnn.Layer.from_problem(p)
     try:
-        with pytest.raises(prnn.PrnnError) as e:
-            lay.set_option(prnn.PRNN_OPT_SPARSE_REG_WEIGHTS, 2)
-        assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+        for opt in (prnn.PRNN_OPT_SPARSE_REG_WEIGHTS, prnn.PRNN_OPT_SPARSE_STAGING_DEPTH):
+            with pytest.raises(prnn.PrnnError) as e:
+                lay.set_option(opt, 2)
+            assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
     finally:
         lay.close()
 
