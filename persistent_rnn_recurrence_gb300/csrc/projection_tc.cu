@@ -8,11 +8,13 @@
 // staging kernel into a K-padded buffer; Wx is stored fp16, K-padded, at
 // set_weights time; accumulation is fp32 in tensor memory.
 //
-// One CTA computes one 128 x 128 tile of P:
+// One CTA computes one 128 x BN tile of P (BN = 128, 96 or 64, chosen per
+// launch so the tiles fill the SMs in as few waves as possible -- at
+// M = 1024, N = 1792, 96-wide tiles give exactly one CTA per SM of 152):
 //   warp 0 / lane 0  TMA producer: 64-wide K slices of the A (x16) and B (Wx16)
 //                    tiles into a 4-stage smem ring (128-byte swizzle),
 //                    completion signalled on a per-stage mbarrier;
-//   warp 1 / lane 0  MMA issuer: 4 x tcgen05.mma (M=128, N=128, K=16) per
+//   warp 1 / lane 0  MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16) per
 //                    slice into a TMEM accumulator, tcgen05.commit frees the
 //                    slice's stage;
 //   warps 0-3        epilogue: tcgen05.ld of the warp's 32 TMEM lanes (rows),
@@ -38,14 +40,21 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 128, BK = 64, kStages = 4;
+constexpr int BM = 128, BK = 64, kStages = 4;
 constexpr int kThreads = 128;
 constexpr uint32_t kTileA = BM * BK * 2;  // 16 KiB
-constexpr uint32_t kTileB = BN * BK * 2;  // 16 KiB
-constexpr uint32_t kStageBytes = kTileA + kTileB;
-constexpr uint32_t kTmemCols = 128;        // fp32 accumulator: 128 lanes x 128 columns
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;  // + alignment slack
 constexpr long long kWaitNs = 200LL * 1000 * 1000;                   // 200 ms per wait
+// Per tile width: B tile bytes, stage bytes (a multiple of 1024, so every
+// tile of the ring stays 1024-byte aligned for the 128-byte swizzle), TMEM
+// columns (a power of two >= 32 holding the BN fp32 accumulator columns).
+template <int BN>
+struct TileCfg {
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 128, "tile width");
+  static constexpr uint32_t kTileB = BN * BK * 2;
+  static constexpr uint32_t kStageBytes = kTileA + kTileB;
+  static constexpr uint32_t kTmemCols = BN <= 64 ? 64 : 128;
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;  // + alignment slack
+};
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1) {
@@ -65,9 +74,14 @@ struct TcKernelArgs {
   uint32_t idesc;
 };
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     proj_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcKernelArgs a) {
+  constexpr uint32_t kTileB = TileCfg<BN>::kTileB;
+  constexpr uint32_t kStageBytes = TileCfg<BN>::kStageBytes;
+  constexpr uint32_t kTmemCols = TileCfg<BN>::kTmemCols;
+  (void)kTileB;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -265,6 +279,57 @@ bool encode_kmajor(CUtensorMap* map, const void* base, int Kp, int rows, int box
 
 bool projection_tc_supported() { return encode_fn() != nullptr; }
 
+namespace {
+
+// Tile width for an M x N product: the fewest waves of one CTA per SM, each
+// wave costing in proportion to the tile's width (its MMAs and loads).
+int pick_bn(int M, int N) {
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    sms = 1;
+  int best = 128;
+  long long best_cost = -1;
+  for (int bn : {128, 96, 64}) {
+    const long long tiles = (long long)((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+    const long long cost = ((tiles + sms - 1) / sms) * bn;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+template <int BN>
+cudaError_t launch_tc_bn(const CUtensorMap& tmA, const void* Bp, int Kp, int N, bool bf16,
+                         const TcKernelArgs& ka, cudaStream_t s) {
+  CUtensorMap tmB;
+  if (!encode_kmajor(&tmB, Bp, Kp, N, BN, bf16)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel<BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)TileCfg<BN>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((ka.N + BN - 1) / BN, (ka.M + BM - 1) / BM);
+  proj_tc_kernel<BN><<<grid, kThreads, TileCfg<BN>::kSmemBytes, s>>>(tmA, tmB, ka);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc(const void* A, const void* B, int M, int N, int Kp, bool bf16,
+                      TcKernelArgs ka, cudaStream_t s) {
+  CUtensorMap tmA;
+  if (!encode_kmajor(&tmA, A, Kp, M, BM, bf16)) return cudaErrorInvalidValue;
+  const int bn = pick_bn(M, N);
+  ka.idesc = bf16 ? bf16_idesc(BM, bn) : f16_idesc(BM, bn);
+  switch (bn) {
+    case 64: return launch_tc_bn<64>(tmA, B, Kp, N, bf16, ka, s);
+    case 96: return launch_tc_bn<96>(tmA, B, Kp, N, bf16, ka, s);
+    default: return launch_tc_bn<128>(tmA, B, Kp, N, bf16, ka, s);
+  }
+}
+
+}  // namespace
+
 cudaError_t launch_projection_tc(const ProjTcArgs& a, int* status, cudaStream_t s) {
   if (a.M == 0 || a.N == 0) return cudaSuccess;
   if (a.Kp % BK != 0 || a.Kp < a.K) return cudaErrorInvalidValue;
@@ -278,37 +343,15 @@ cudaError_t launch_projection_tc(const ProjTcArgs& a, int* status, cudaStream_t 
     if (e != cudaSuccess) return e;
   }
   // 2. tensor-core GEMM
-  CUtensorMap tmA, tmB;
-  if (!encode_kmajor(&tmA, a.x16, a.Kp, a.M, BM) || !encode_kmajor(&tmB, a.Wx16, a.Kp, a.N, BN))
-    return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  TcKernelArgs ka{a.M, a.N, a.Kp, a.bias, a.P, a.y_fill, status, f16_idesc(BM, BN)};
-  const dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
-  proj_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, ka);
-  return cudaGetLastError();
+  TcKernelArgs ka{a.M, a.N, a.Kp, a.bias, a.P, a.y_fill, status, 0u};
+  return launch_tc(a.x16, a.Wx16, a.M, a.N, a.Kp, false, ka, s);
 }
 
 cudaError_t launch_gemm_tc(const GemmTcArgs& g, int* status, cudaStream_t s) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   if (g.Kp % BK != 0) return cudaErrorInvalidValue;
-  CUtensorMap tmA, tmB;
-  if (!encode_kmajor(&tmA, g.A, g.Kp, g.M, BM, g.bf16) ||
-      !encode_kmajor(&tmB, g.B, g.Kp, g.N, BN, g.bf16))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
-  if (e != cudaSuccess) return e;
-  TcKernelArgs ka{g.M, g.N, g.Kp, nullptr, g.C, nullptr, status,
-                  g.bf16 ? bf16_idesc(BM, BN) : f16_idesc(BM, BN)};
-  const dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
-  proj_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, ka);
-  return cudaGetLastError();
+  TcKernelArgs ka{g.M, g.N, g.Kp, nullptr, g.C, nullptr, status, 0u};
+  return launch_tc(g.A, g.B, g.M, g.N, g.Kp, g.bf16, ka, s);
 }
 
 }  // namespace prnn
