@@ -97,8 +97,8 @@ typedef enum {
                                      entries in registers) wherever its plan fits: at most 384
                                      threads, batch passes of at most 4 columns, column order,
                                      at least 24 entries per thread (default); 0 = never       */
-  PRNN_OPT_SPARSE_STAGING_DEPTH = 14 /* sparse persistent, column order, passes of at most 4
-                                     columns: 1 = stage h_{t-1} with the fewest float4 loads in
+  PRNN_OPT_SPARSE_STAGING_DEPTH = 14 /* sparse persistent, passes of at most 4 columns (either
+                                     staging order): 1 = stage h_{t-1} with the fewest float4 loads in
                                      flight per thread (2 or 6) that cover the thread's share of
                                      a pass in one round (default); 0 = always 12.  The sync
                                      floor probe follows the same choice                       */

@@ -410,14 +410,14 @@ cudaError_t launch_recur_sparse_impl(const SparseRecurArgs& a, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
-// The column-order builds of one launch bound and trace setting, for each
+// The builds of one staging order, launch bound and trace setting, for each
 // staging depth the launcher may choose (a.umax: 0, 2 or 6).
-template <bool TRACE, int MAXT>
+template <bool PLACED, bool TRACE, int MAXT>
 cudaError_t launch_recur_sparse_depth(const SparseRecurArgs& a, cudaStream_t s) {
   switch (a.umax) {
-    case 0: return launch_recur_sparse_impl<false, TRACE, MAXT, 0>(a, s);
-    case 2: return launch_recur_sparse_impl<false, TRACE, MAXT, 2>(a, s);
-    case 6: return launch_recur_sparse_impl<false, TRACE, MAXT, 6>(a, s);
+    case 0: return launch_recur_sparse_impl<PLACED, TRACE, MAXT, 0>(a, s);
+    case 2: return launch_recur_sparse_impl<PLACED, TRACE, MAXT, 2>(a, s);
+    case 6: return launch_recur_sparse_impl<PLACED, TRACE, MAXT, 6>(a, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -7,7 +7,7 @@
 namespace prnn {
 
 cudaError_t launch_recur_sparse_placed(const SparseRecurArgs& a, cudaStream_t s) {
-  return launch_recur_sparse_impl<true>(a, s);
+  return launch_recur_sparse_depth<true, false, kSparseThreads>(a, s);
 }
 
 }  // namespace prnn

@@ -10,7 +10,7 @@
 namespace prnn {
 
 cudaError_t launch_recur_sparse_regw(const SparseRecurArgs& a, cudaStream_t s) {
-  return launch_recur_sparse_depth<false, kRegWThreads>(a, s);
+  return launch_recur_sparse_depth<false, false, kRegWThreads>(a, s);
 }
 
 }  // namespace prnn

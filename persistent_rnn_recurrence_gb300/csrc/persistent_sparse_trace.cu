@@ -7,7 +7,7 @@
 namespace prnn {
 
 cudaError_t launch_recur_sparse_trace(const SparseRecurArgs& a, cudaStream_t s) {
-  return launch_recur_sparse_depth<true, kSparseThreads>(a, s);
+  return launch_recur_sparse_depth<false, true, kSparseThreads>(a, s);
 }
 
 }  // namespace prnn

@@ -6,7 +6,7 @@
 namespace prnn {
 
 cudaError_t launch_recur_sparse_trace_regw(const SparseRecurArgs& a, cudaStream_t s) {
-  return launch_recur_sparse_depth<true, kRegWThreads>(a, s);
+  return launch_recur_sparse_depth<false, true, kRegWThreads>(a, s);
 }
 
 }  // namespace prnn

@@ -185,13 +185,14 @@ struct SparseRecurArgs {
                          // 384, bgroup <= 4; see sparse_regw_fits)
   int umax;              // staging depth (float4 loads per thread per round): 0 for
                          // the default (12 for passes of <= 4 columns), or 2 or 6
-                         // (column order, bgroup <= 4; see sparse_staging_depth)
+                         // (bgroup <= 4; see sparse_staging_depth)
 };
-// The staging depth for a column-order pass of bgroup columns of H over
-// nthreads threads: the smallest of 2, 6 (else 0: the default 12) that covers
-// each thread's share of the pass in one round.
+// The staging depth for a pass of bgroup columns of H over nthreads threads:
+// the smallest of 2, 6 (else 0: the default 12) that covers each thread's
+// share of the pass in one round.
 inline int sparse_staging_depth(int H, int bgroup, int nthreads, bool placed) {
-  if (placed || bgroup > 4 || nthreads < 1) return 0;
+  (void)placed;
+  if (bgroup > 4 || nthreads < 1) return 0;
   const int need = (bgroup * (H / 4) + nthreads - 1) / nthreads;
   return need <= 2 ? 2 : (need <= 6 ? 6 : 0);
 }
