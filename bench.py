@@ -340,6 +340,34 @@ def cpu_baseline_all_cores(p) -> dict:
     return out
 
 
+SWEEP_SAMPLE_T = 32
+
+
+def sweep_cpu_baseline(p, ys: dict) -> dict:
+    """The sweep point's CPU-baseline leg: the oracle on every usable host core
+    over the point's first SWEEP_SAMPLE_T steps, timed, and -- from that same
+    output -- the parity of each GPU path's first steps (``ys``: path -> y
+    [T', B, H] as numpy) under the rule max|y - y_oracle| <= 2e-2 max|y_oracle|
+    (fp16 weights, fp32 accumulation)."""
+    import numpy as np
+    import oracle
+    n = host_cpu()["usable_cores"] or 1
+    Ts = min(SWEEP_SAMPLE_T, p.T)
+    t0 = time.perf_counter()
+    ref = oracle.default().forward(p, T=Ts, threads=n)
+    dt = time.perf_counter() - t0
+    scale = float(np.abs(ref).max())
+    parity = {"steps": Ts, "tol": 2e-2, "pass": True}
+    for path, y in ys.items():
+        err = float(np.abs(y[:Ts].astype(np.float64) - ref).max()) / max(scale, 1e-30)
+        parity[path + "_max_rel_err"] = err
+        parity["pass"] = parity["pass"] and bool(np.isfinite(y[:Ts]).all()) and err <= 2e-2
+    return {"cpu_baseline": {"value": Ts / dt, "unit": "timesteps/s", "cores": n,
+                             "kind": "oracle, threaded driver",
+                             "sample": f"first {Ts} of {p.T} timesteps, B={p.B}"},
+            "parity": parity}
+
+
 # ---- our arm ----------------------------------------------------------------------------
 def run_ours(args):
     import numpy as np  # noqa: F401
@@ -582,7 +610,9 @@ def run_sweep(args):
     """Persistent vs per-step recurrence time for every sweep point (T = 256,
     fp16 weights), forward time and per-step time, L2 flushed before each
     timed forward.  Points whose layer does not fit on chip are reported as
-    unsupported rather than skipped."""
+    unsupported rather than skipped.  Unless --no-cpu-baseline, each line also
+    carries its CPU-baseline leg: the oracle timed on the point's first
+    steps, and the parity of both paths' first steps against that output."""
     import torch
     from persistent_rnn_recurrence_gb300 import prnn, synth
     dev = torch.device("cuda", 0)
@@ -595,6 +625,7 @@ def run_sweep(args):
         x = torch.from_numpy(p.x).to(dev)
         y = torch.empty((p.T, p.B, p.H), dtype=torch.float32, device=dev)
         line = {"point": name, "H": p.H, "B": p.B, "k": p.k, "density": p.k / p.H}
+        first_steps = {}
         for algo in ("persistent", "per_step"):
             try:
                 lay = prnn.Layer.from_problem(p, algo=algo)
@@ -613,6 +644,7 @@ def run_sweep(args):
             lay.close()
             rec = sorted(m[1] for m in ms)[len(ms) // 2]
             proj = sorted(m[0] for m in ms)[len(ms) // 2]
+            first_steps[algo] = y[:SWEEP_SAMPLE_T].cpu().numpy()
             line[algo] = {"recurrence_us_per_step": 1e3 * rec / p.T, "projection_ms": proj,
                           "timesteps_per_s": 1e3 * p.T / (rec + proj),
                           "status": prnn.prnn_status_string(st),
@@ -621,6 +653,8 @@ def run_sweep(args):
                 "recurrence_us_per_step" in line.get("per_step", {}):
             line["persistent_speedup"] = (line["per_step"]["recurrence_us_per_step"]
                                           / line["persistent"]["recurrence_us_per_step"])
+        if not args.no_cpu_baseline and first_steps:
+            line.update(sweep_cpu_baseline(p, first_steps))
         print(json.dumps(line), flush=True)
     return 0
 

@@ -8,6 +8,10 @@ Three kinds of check:
   * random fp32-weight problems whose pre-activations all stay further from 0
     than the fp32 rounding of the forward (checked on the oracle's side), so
     the masks agree again: every gradient within 1e-4 of its scale;
+  * fp16-weight problems on the default path (tensor-core projection and
+    bf16 tensor-core gradient products): dyadic problems again, every
+    gradient against the oracle's, the bf16 products within their rounding
+    bound;
   * fp16-weight and full-size problems, where forward rounding can flip the
     mask of pre-activations near 0: properties that hold at any size --
     every sampled delta equals one oracle step of the reverse recurrence
@@ -74,6 +78,36 @@ def dyadic_problem(seed, H, I, B, T, wdtype, nnz_row=3):
                       b=q(H).astype(np.float32), h0=q(B, H).astype(np.float32), Wh=Wh.astype(wt))
     dy = q(T, B, H)
     return p, dy
+
+
+@pytest.mark.parametrize("sparse", [False, True])
+@pytest.mark.parametrize("shape", [dict(H=1152, I=1152, B=4, T=6), dict(H=640, I=320, B=8, T=5)])
+def test_tensor_core_gradients_against_oracle(env, sparse, shape):
+    """fp16-weight layers on the default path: tcgen05 projection (x rounded
+    to fp16) and tensor-core gradient products from bf16-rounded operands.
+    On dyadic problems the forward is exact on both sides (fp16 holds every
+    x and weight, fp32 every sum), so the GPU and the oracle take the same
+    ReLU decisions: delta, db and dh0 (fp32 arithmetic) must match the
+    oracle's gradients within 1e-6, and dWh (or the stored values' gradients),
+    dWx and dx -- the bf16 products -- within BF16_PRODUCT_TOL."""
+    o = env[2]
+    if sparse:
+        p, dy = dyadic_sparse_problem(900 + shape["H"], k=3, **shape)
+    else:
+        p, dy = dyadic_problem(910 + shape["H"], wdtype="f16", **shape)
+    y, g = run(env, p, dy.astype(np.float32))
+    assert np.array_equal(y, o.forward(p)), "forward not exact: masks could differ"
+    assert np.count_nonzero(y) > y.size // 4
+    ref = o.backward(p, dy)
+    errs = {}
+    for k in ("delta", "db", "dh0"):
+        errs[k] = rel_err(g[k], ref[k])
+        assert errs[k] <= 1e-6, (k, errs[k])
+    for k in ("dWx", "dx", "dWh"):
+        want = ref["dvals"].ravel() if (sparse and k == "dWh") else ref[k]
+        errs[k] = rel_err(g[k].ravel() if sparse and k == "dWh" else g[k], want)
+        assert errs[k] <= BF16_PRODUCT_TOL, (k, errs[k])
+    print("relative errors vs the oracle:", {k: f"{v:.2e}" for k, v in errs.items()})
 
 
 @pytest.mark.parametrize("wdtype", ["f32", "f16"])
@@ -146,12 +180,21 @@ def check_by_properties(env, p, dy, y, g, n_samples=300):
         assert rel_err(g[k], ref) <= product_tol(p, k), (k, rel_err(g[k], ref))
 
 
+# bf16 keeps 8 significant bits: each operand of a tensor-core gradient
+# product is rounded by at most 2^-9 of itself, so each product term by at
+# most ~2^-8, and a sum of such terms (fp32 accumulation) stays within 2^-8
+# of the sum of the terms' magnitudes.  Relative to the largest gradient
+# entry that is a few 2^-8 wherever the entries are of similar size; the
+# bound used below is 2^-6 (4 x 2^-8).
+BF16_PRODUCT_TOL = 2.0 ** -6
+
+
 def product_tol(p, k):
     """fp16-weight layers form dWh (dense, or the stored values of sparse
     weights), dWx and dx on the tensor cores from bf16-rounded operands (fp32
-    accumulation): the fp16 rule 2e-2 of the scale; everything else is fp32
+    accumulation): BF16_PRODUCT_TOL of the scale; everything else is fp32
     arithmetic: 1e-4."""
-    return 2e-2 if p.wdtype == "f16" and k in ("dWh", "dWx", "dx") else 1e-4
+    return BF16_PRODUCT_TOL if p.wdtype == "f16" and k in ("dWh", "dWx", "dx") else 1e-4
 
 
 @pytest.mark.parametrize("spec", [dict(H=1152, B=4, T=32, wdtype="f16", h0_std=0.1),

@@ -124,3 +124,25 @@ def test_traffic_is_null_once_the_kernel_changes(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_sha1", lambda sparse: "0" * 40)
     assert bench.load_traffic("sparse_f16_h1792_d10_b4_t256", "persistent", True) is None
     assert bench.load_traffic("no_such_workload", "persistent", True) is None
+
+
+def test_sweep_cpu_baseline_leg_checks_parity():
+    """The sweep's CPU-baseline leg times the oracle on a point's first steps
+    and judges each GPU path's first steps against that output: a path equal
+    to the oracle within the rule passes, one with a planted error of 5 % of
+    the scale, or a non-finite value, fails."""
+    import numpy as np
+    import bench
+    import oracle
+    from persistent_rnn_recurrence_gb300 import synth
+    p = synth.make_problem(H=64, B=2, T=40, k=7, seed=3, name="tiny_sweep_point")
+    ref = oracle.default().forward(p, T=bench.SWEEP_SAMPLE_T).astype(np.float32)
+    bad = ref.copy()
+    bad[3, 1, 5] += 0.05 * float(np.abs(ref).max())
+    nan = ref.copy()
+    nan[0, 0, 0] = np.nan
+    out = bench.sweep_cpu_baseline(p, {"persistent": ref, "per_step": ref})
+    assert out["parity"]["pass"] and out["parity"]["steps"] == bench.SWEEP_SAMPLE_T
+    assert out["cpu_baseline"]["kind"].startswith("oracle") and out["cpu_baseline"]["value"] > 0
+    assert not bench.sweep_cpu_baseline(p, {"persistent": ref, "per_step": bad})["parity"]["pass"]
+    assert not bench.sweep_cpu_baseline(p, {"persistent": nan, "per_step": ref})["parity"]["pass"]
