@@ -576,8 +576,8 @@ def load_peaks() -> dict:
 
 
 KERNEL_SOURCES = {
-    True: ["persistent_sparse.cu", "persistent_sparse.cuh", "persistent_common.cuh",
-           "device_common.cuh"],
+    True: ["persistent_sparse.cu", "persistent_sparse.cuh", "persistent_sparse_regw.cu",
+           "persistent_sparse_um.cu", "persistent_common.cuh", "device_common.cuh"],
     False: ["persistent_dense.cu", "persistent_common.cuh", "device_common.cuh"],
 }
 
