@@ -645,7 +645,10 @@ def run_sweep(args):
             rec = sorted(m[1] for m in ms)[len(ms) // 2]
             proj = sorted(m[0] for m in ms)[len(ms) // 2]
             first_steps[algo] = y[:SWEEP_SAMPLE_T].cpu().numpy()
+            fma_peak = (info["sm_count"] or 152) * 128 * 2 * \
+                load_peaks().get("sm_max_mhz", 2070.0) * 1e6
             line[algo] = {"recurrence_us_per_step": 1e3 * rec / p.T, "projection_ms": proj,
+                          "frac_of_fma_peak": (2.0 * p.nnz * p.B / fma_peak) / (1e-3 * rec / p.T),
                           "timesteps_per_s": 1e3 * p.T / (rec + proj),
                           "status": prnn.prnn_status_string(st),
                           "groups": info["cta_groups"], "n_cta": info["n_cta"]}

@@ -221,17 +221,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // x [M][K] fp32 -> x16 [M][Kp] fp16 (round to nearest even), zero for k >= K.
+// Each thread converts 8 consecutive values: two 16-byte loads when the row
+// holds all 8 and rows are 16-byte aligned (K % 4 == 0, x 16-byte aligned),
+// else scalar loads.
 __global__ void stage_x_f16_kernel(const float* __restrict__ x, __half* __restrict__ x16, int M,
                                    int K, int Kp) {
   const int groups = Kp / 8;
   const size_t total = (size_t)M * groups;
+  const bool vec_rows = (K & 3) == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
        i += (size_t)gridDim.x * blockDim.x) {
     const int m = (int)(i / groups), k0 = (int)(i % groups) * 8;
     const float* row = x + (size_t)m * K;
+    float v[8];
+    if (vec_rows && k0 + 8 <= K) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(row + k0));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(row + k0 + 4));
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = k0 + j < K ? row[k0 + j] : 0.f;
+    }
     __align__(16) __half h[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) h[j] = __float2half_rn(k0 + j < K ? row[k0 + j] : 0.f);
+    for (int j = 0; j < 8; ++j) h[j] = __float2half_rn(v[j]);
     *reinterpret_cast<uint4*>(x16 + (size_t)m * Kp + k0) = *reinterpret_cast<const uint4*>(h);
   }
 }
