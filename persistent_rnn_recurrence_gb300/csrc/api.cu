@@ -950,6 +950,11 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
       DenseRecurArgs a{};
       const int bw = std::min(recur_dense_bw((B + h->G - 1) / h->G), h->dense_bw);
       c.smem = recur_dense_smem(h->R, h->cpt, h->nthreads, h->wdtype == PRNN_F16, bw);
+      if (h->poll_delay_ns < 0) {
+        const int passes = ((B + h->G - 1) / h->G + bw - 1) / bw;
+        c.poll_delay =
+            (int)((long long)dense_delay_ns(h->H, bw, passes) * h->clock_khz / 1000000LL);
+      }
       a.c = c;
       a.Wpk = h->Wpk;
       a.cpt = h->cpt;
@@ -1145,6 +1150,11 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
     DenseRecurArgs a{};
     const int bw = std::min(recur_dense_bw((B + h->G - 1) / h->G), h->dense_bw);
     c.smem = recur_dense_smem(h->R, h->cpt, h->nthreads, h->wdtype == PRNN_F16, bw);
+    if (h->poll_delay_ns < 0) {
+      const int passes = ((B + h->G - 1) / h->G + bw - 1) / bw;
+      c.poll_delay =
+          (int)((long long)dense_delay_ns(h->H, bw, passes) * h->clock_khz / 1000000LL);
+    }
     a.c = c;
     a.Wpk = h->Wpk_T;
     a.cpt = h->cpt;

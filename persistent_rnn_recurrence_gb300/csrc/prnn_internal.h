@@ -57,6 +57,17 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int* status, cudaStream_t s);
 // fastest without it up to H ~ 2000 (H=1792: 1.58 / 1.63 us/step at 0 / 50
 // ns) and gain 3-8 % from 100 ns at H = 5760.
 constexpr int kDenseDelayNs = 100;
+// The dense kernel's first pass of a step polls bw batch columns of h (bw*H*4
+// bytes per CTA).  When that pass is the step's only one (its data was
+// published at the end of the previous step) and it polls more than 16 KiB,
+// the 100 ns pause does not keep the exchange in its fast state: with all 4
+// columns of B = 4 in one pass (one CTA group), H=1792 runs 4.4-7.5 us/step at
+// 100 ns and 2.4 at 200 ns, H=2048 6.0-7.0 and 2.4 (about 10 at 0 ns for H =
+// 1536 .. 2048).  With several passes the first pass reads data published
+// passes earlier, and 200 ns only costs 1-2 %.
+__host__ __device__ constexpr int dense_delay_ns(int H, int bw, int passes) {
+  return passes == 1 && (long long)bw * H * 4 > 16384 ? 200 : kDenseDelayNs;
+}
 __host__ __device__ constexpr int sparse_delay_ns(int H) { return H > 4096 ? 100 : 0; }
 // Default first pause (ns) before re-polling stale step data (Waiter::pause):
 // none for the single-layer kernels (it only slows them), 250 ns for the
