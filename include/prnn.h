@@ -132,7 +132,8 @@ typedef struct {
  *   algo      PRNN_ALGO_PERSISTENT or PRNN_ALGO_PER_STEP.
  * Returns PRNN_ERR_UNSUPPORTED when the device is not sm_103 / lacks
  * cooperative launch, or when the dense layer cannot fit on chip (the
- * persistent-rnn page's "limits on how large a layer can be").  *out is NULL
+ * persistent-rnn page notes that on-chip weights cap the layer size,
+ * "Important Constraints").  *out is NULL
  * on failure.
  */
 prnn_status_t prnn_create(prnn_t* out, int hidden, int input, int max_batch,
@@ -189,8 +190,12 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
  * The same forward pass on HOST buffers: x [T][B][I], h0 [B][H] (NULL =
  * zeros) and y [T][B][H] are fp32 in page-locked host memory that the device
  * can address (cudaHostAlloc / cudaMallocHost, or cudaHostRegister'ed), each
- * float-aligned and holding at least the elements its shape says; y must not
- * overlap x or h0.  x and h0 are copied to device workspaces owned by the
+ * float-aligned.  Precondition, which the library cannot verify: each buffer
+ * holds at least the elements its shape says within ONE allocation (the
+ * recurrent kernel stores into y at every [t][b][r] offset).  As a best-effort
+ * guard only, a buffer whose first or last element lies outside every
+ * page-locked allocation is refused; a short buffer followed by another
+ * page-locked allocation is not detected.  y must not overlap x or h0.  x and h0 are copied to device workspaces owned by the
  * handle (grown on demand, freed by prnn_destroy).  The persistent CUDA-core
  * recurrent kernels write every output into y itself, over the host link, as
  * they publish it, so the result needs no separate copy back; the per-step

@@ -269,8 +269,9 @@ int oracle_rnn_forward_csr(long T, long B, long H, long I, const double* x,
 /*
  * The input projection on its own, P[t,b,r] = bias[r] + sum_c Wx[r,c] x[t,b,c]:
  * the part of every step that does not depend on h_{t-1} and so can be done for
- * all steps at once ("exposing parallelism between operations", Abstract of
- * "Optimizing Performance of Recurrent Neural Networks on GPUs").
+ * all steps at once (work that does not depend on the previous step is batched
+ * across steps: Abstract of "Optimizing Performance of Recurrent Neural
+ * Networks on GPUs").
  */
 int oracle_rnn_input_projection(long T, long B, long H, long I, const double* x,
                                 const double* Wx, const double* bias, double* P) {

@@ -1034,9 +1034,11 @@ prnn_status_t prnn_forward_host(prnn_t h, int T, int B, const float* x, const fl
   if (((uintptr_t)x | (uintptr_t)y | (uintptr_t)h0) & 3u) return PRNN_ERR_INVALID_ARG;
   if (overlaps(y, ny * 4, x, nx * 4)) return PRNN_ERR_INVALID_ARG;
   if (h0 && overlaps(y, ny * 4, h0, n0 * 4)) return PRNN_ERR_INVALID_ARG;
-  // all three must be page-locked host memory the device can address; the
-  // last element too (a buffer shorter than the sizes say is refused when
-  // its end falls outside any page-locked allocation)
+  // all three must be page-locked host memory the device can address.  The
+  // last element is checked too, as a best-effort guard only: a buffer
+  // shorter than its shape is refused when its end falls outside every
+  // page-locked allocation, not when another allocation follows it (the
+  // element counts are the caller's precondition, include/prnn.h)
   float* ydev = static_cast<float*>(const_cast<void*>(mapped_host(y)));
   if (!mapped_host(x) || !mapped_host(x + nx - 1) || !ydev || !mapped_host(y + ny - 1) ||
       (h0 && (!mapped_host(h0) || !mapped_host(h0 + n0 - 1))))

@@ -16,8 +16,8 @@
 // They are the products the chain rule gives for the layer's two matrix
 // products; like the forward projection they carry no dependence between
 // steps and run as whole-sequence GEMMs ("Optimizing Performance of
-// Recurrent Neural Networks on GPUs", Abstract: exposing parallelism between
-// operations).  fp32 CUDA-core tiles (64 x 64 outputs per CTA, 16-deep K
+// Recurrent Neural Networks on GPUs", Abstract: independent operations are
+// batched rather than run step by step).  fp32 CUDA-core tiles (64 x 64 outputs per CTA, 16-deep K
 // slices staged in shared memory, 4 x 4 outputs per thread): the gradients
 // are kept in full fp32, and these GEMMs are a few percent of a training
 // step next to the serial recurrences.

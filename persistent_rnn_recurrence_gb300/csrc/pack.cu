@@ -7,7 +7,7 @@
 // 16-byte words (wide loads).  Entry = fp16 value bits | column << 16;
 // padding entries have value +0.
 //
-// Bank-aware placement (the "bank-aware weight layout" row of the sparse
+// Bank-aware placement (the bank-aware layout row of the sparse
 // persistent RNN ablation): the kernel gathers h[b][col] from shared memory
 // with one 32-bit load per lane per slot, so the 32 lanes of a warp hit 32
 // different banks exactly when their columns differ mod 32.  Entries are

@@ -1,7 +1,7 @@
 // per_step.cu -- the non-persistent comparison path: one launch per step,
 // y[t] = ReLU(P[t] + Wh h_{t-1}), with Wh read again from L2/HBM every step.
-// This is the "keep reloading the same weights" pattern the persistent-rnn
-// page contrasts its register-cached kernel with ("What This Project Does"),
+// This is the weights-re-read-every-step pattern that the persistent-rnn page
+// contrasts with its register-cached kernel ("What This Project Does"),
 // and the per-step dense / sparse matrix-product baselines of the sparse
 // persistent RNN measurements.  The T launches are replayed as one CUDA graph.
 #include "device_common.cuh"

@@ -10,9 +10,9 @@
 // is its own ready flag), so layer l starts step t as soon as layer l-1 has
 // published step t: after a fill of L-1 steps all layers advance together,
 // and the stack takes about T + L - 1 step times instead of L * T.  This is
-// the "whole network" persistent stage of "Optimizing Performance of
-// Recurrent Neural Networks on GPUs" (Abstract: exposing parallelism between
-// operations across layers) with the on-chip weights of the persistent-rnn
+// the multi-layer stage of "Optimizing Performance of Recurrent Neural
+// Networks on GPUs" (Abstract: the network is optimized as a whole, with work
+// of different layers overlapped) with the on-chip weights of the persistent-rnn
 // page ("What This Project Does").
 //
 // The inner structure is that of the single-layer dense kernel: thread i owns

@@ -2,9 +2,9 @@
 //
 // P[m][n] = bias[n] + sum_k x[m][k] * Wx[n][k] for all m = t*B + b at once:
 // the input half of every step does not depend on h_{t-1}, so it is taken out
-// of the serial loop as one matrix product ("exposing parallelism between
-// operations", Abstract of "Optimizing Performance of Recurrent Neural
-// Networks on GPUs").  This kernel is the fp32 path (fp32 weights need full
+// of the serial loop as one matrix product (work independent of the previous
+// step is batched across steps: Abstract of "Optimizing Performance of
+// Recurrent Neural Networks on GPUs").  This kernel is the fp32 path (fp32 weights need full
 // fp32 products; TF32 tensor cores would round x and Wx to 10-bit mantissas).
 // It also serves fp16 weights when tensor cores are switched off.
 #include "device_common.cuh"

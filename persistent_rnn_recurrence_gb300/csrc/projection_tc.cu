@@ -2,9 +2,9 @@
 //
 // P[m][n] = bias[n] + sum_k x16[m][k] * Wx16[n][k] for all m = t*B + b at
 // once: the input half of every step does not depend on h_{t-1}, so it is
-// taken out of the serial loop as one dense matrix product ("exposing
-// parallelism between operations", Abstract of "Optimizing Performance of
-// Recurrent Neural Networks on GPUs").  x is rounded to fp16 (RNE) by a
+// taken out of the serial loop as one dense matrix product (work independent
+// of the previous step batched across steps: Abstract of "Optimizing
+// Performance of Recurrent Neural Networks on GPUs").  x is rounded to fp16 (RNE) by a
 // staging kernel into a K-padded buffer; Wx is stored fp16, K-padded, at
 // set_weights time; accumulation is fp32 in tensor memory.
 //
