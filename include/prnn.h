@@ -98,11 +98,19 @@ typedef enum {
                                      entries in registers) wherever its plan fits: at most 384
                                      threads, batch passes of at most 4 columns, column order,
                                      at least 24 entries per thread (default); 0 = never       */
-  PRNN_OPT_SPARSE_STAGING_DEPTH = 14 /* sparse persistent, passes of at most 4 columns (either
+  PRNN_OPT_SPARSE_STAGING_DEPTH = 14,/* sparse persistent, passes of at most 4 columns (either
                                      staging order): 1 = stage h_{t-1} with the fewest float4 loads in
                                      flight per thread (2 or 6) that cover the thread's share of
                                      a pass in one round (default); 0 = always 12.  The sync
                                      floor probe follows the same choice                       */
+  PRNN_OPT_DENSE_WIDE = 15        /* dense fp16 persistent, flags in the data, H % 128 == 0 and
+                                     H / 16 CTAs fit: the wide-batch kernel (CTAs of 8 or 16
+                                     rows, passes of 8 batch columns staged by bulk copies a
+                                     pass ahead) for forwards of B >= 16.  1 = where it
+                                     measured faster than the B <= 4 kernel: B >= 17 with
+                                     H >= 1024, or B >= 16 with H >= 2048 (default); 2 = for
+                                     every B >= 16; 0 = never.  Takes effect at the next
+                                     forward                                                    */
 } prnn_option_t;
 
 /* Plan and sizes chosen at create / set_weights time (read-only report). */
@@ -122,6 +130,9 @@ typedef struct {
                                       bank-balancing order (prnn_pack_sparse_host_placed)   */
   int sparse_reg_weights;          /* sparse: 1 if the forward at max_batch runs the
                                       register-weight build (PRNN_OPT_SPARSE_REG_WEIGHTS)   */
+  int dense_wide_batch;            /* dense: 1 if the forward at max_batch runs the
+                                      wide-batch kernel (PRNN_OPT_DENSE_WIDE); the plan
+                                      fields above then describe that kernel's launch       */
 } prnn_info_t;
 
 /*

@@ -32,6 +32,14 @@ struct prnn_handle {
   // persistent plan
   int n_cta = 0, R = 0, nthreads = 0, cpt = 0, tpr = 0, kp = 0, ept = 0, pack_cap = 0;
   int G = 1, cpg = 0, groups_opt = 0, dense_bw = 4;
+  // dense fp16 for wide batches (CTA groups of >= 8 batch columns): its own
+  // plan, packed weights and a zero h0 for forwards without one
+  int wide_opt = 1;
+  bool wide = false;
+  int w_R = 0, w_S = 0, w_depth = 1;
+  size_t w_smem = 0;
+  void* Wpk_wide = nullptr;
+  float* zeros = nullptr;
   // tensor-core dense recurrence (wide batch): its own plan and weight image
   int rtc_opt = 1;  // the tensor-core recurrence is opt-in (slower than the CUDA cores so far)
   bool rtc = false;
@@ -435,6 +443,9 @@ void free_weights(prnn_handle* h) {
   free_dev(h->Wh_nat);
   free_dev(h->Wimg);
   h->rtc = false;
+  free_dev(h->Wpk_wide);
+  free_dev(h->zeros);
+  h->wide = false;
   free_dev(h->cols_pad);
   free_dev(h->caller_pos);
   free_dev(h->valsT);
@@ -754,6 +765,32 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
       h->t_N = tp.N;
       h->t_ring = tp.nring;
     }
+    // wide batches: CTAs of 8 or 16 rows, one group over all batch columns
+    int wR = 0, wS = 0, wD = 0;
+    size_t wsm = 0;
+    if (h->wdtype == PRNN_F16 && h->maxB >= kDenseWideMinB &&
+        recur_dense_wide_plan(H, h->sm_count, h->smem_optin, &wR, &wS, &wD, &wsm)) {
+      const int nch = H / 4, qg = wR / 4, ncta = H / wR;
+      const uint16_t* w16 = reinterpret_cast<const uint16_t*>(wh.data());
+      std::vector<uint16_t> img((size_t)ncta * 2 * qg * nch * 8);  // per CTA 2 x qg x nch uint4
+      for (int cta = 0; cta < ncta; ++cta)
+        for (int half = 0; half < 2; ++half)      // Wlo, Whi
+          for (int q = 0; q < qg; ++q)
+            for (int ch = 0; ch < nch; ++ch)
+              for (int i = 0; i < 2; ++i) {       // two rows per uint4
+                const int row = cta * wR + 4 * q + 2 * half + i;
+                const size_t dst = ((((size_t)cta * 2 + half) * qg + q) * nch + ch) * 8 + i * 4;
+                for (int e = 0; e < 4; ++e) img[dst + e] = w16[(size_t)row * H + ch * 4 + e];
+              }
+      PRNN_TRY(upload(&h->Wpk_wide, img.data(), img.size() * 2));
+      std::vector<float> z((size_t)h->maxB * H, 0.f);
+      PRNN_TRY(upload(&h->zeros, z.data(), z.size() * sizeof(float)));
+      h->wide = true;
+      h->w_R = wR;
+      h->w_S = wS;
+      h->w_depth = wD;
+      h->w_smem = wsm;
+    }
     h->n_cta = plan.n_cta;
     h->R = plan.R;
     h->G = plan.G;
@@ -874,6 +911,19 @@ prnn_status_t prnn_set_weights_csr(prnn_t h, const void* Wx, int nnz, const int3
   return install_sparse(h, Wx, bias, hv, hc, kmax, pos);
 }
 
+// Whether a dense persistent forward of B columns runs the wide-batch kernel:
+// planned at set_weights, enabled, flags in the data, and at least two
+// passes of 8 columns per step (so a pass's copy is fetched during the
+// previous pass).  By default only where it measured faster than the B <= 4
+// kernel: three or more passes at H >= 1024, two at H >= 2048.
+static bool dense_wide_for(const prnn_t h, int B) {
+  if (h->algo != PRNN_ALGO_PERSISTENT || h->sparse || !h->wide || h->wide_opt == 0 ||
+      h->sync_mode != 0 || h->rtc || B < kDenseWideMinB)
+    return false;
+  const int passes = (B + 7) / 8;
+  return h->wide_opt == 2 || (passes >= 3 ? h->H >= 1024 : h->H >= 2048);
+}
+
 // Whether the recurrent kernel prnn_forward would launch can also write every
 // output into a second buffer (the persistent CUDA-core kernels can).
 static bool recurrence_mirrors(const prnn_t h) {
@@ -946,6 +996,15 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
       a.nslices = h->H / 64;
       a.nring = h->t_ring;
       PRNN_TRY(launch_recur_dense_tc(a, s));
+    } else if (dense_wide_for(h, B)) {
+      c.R = h->w_R;
+      c.cpg = (h->H + h->w_R - 1) / h->w_R;
+      c.n_cta = c.cpg;
+      c.G = 1;
+      c.nthreads = h->w_R / 4 * h->w_S;
+      c.smem = h->w_smem;
+      DenseWideArgs a{c, h->Wpk_wide, h0 ? h0 : h->zeros, h->w_S, h->w_depth};
+      PRNN_TRY(launch_recur_dense_wide(a, s));
     } else {
       DenseRecurArgs a{};
       const int bw = std::min(recur_dense_bw((B + h->G - 1) / h->G), h->dense_bw);
@@ -1316,6 +1375,10 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
       if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
       h->depth_opt = (int)value;
       return PRNN_OK;
+    case PRNN_OPT_DENSE_WIDE:
+      if (value < 0 || value > 2) return PRNN_ERR_INVALID_ARG;
+      h->wide_opt = (int)value;
+      return PRNN_OK;
   }
   return PRNN_ERR_INVALID_ARG;
 }
@@ -1354,6 +1417,14 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
                 sparse_regw_fits(h->nthreads, bg, h->ept, h->place != nullptr)
             ? 1
             : 0;
+  }
+  if (h->weights_set && dense_wide_for(h, h->maxB)) {
+    info->dense_wide_batch = 1;
+    info->n_cta = (h->H + h->w_R - 1) / h->w_R;
+    info->rows_per_cta = h->w_R;
+    info->threads_per_cta = h->w_R / 4 * h->w_S;
+    info->cta_groups = 1;
+    info->smem_bytes = h->w_smem;
   }
   if (h->rtc) {
     info->n_cta = h->t_n_cta;

@@ -112,6 +112,25 @@ struct DenseRecurArgs {
 };
 cudaError_t launch_recur_dense(const DenseRecurArgs& a, int bw, cudaStream_t s);
 
+// Dense fp16 for wide batches (persistent_dense_wide.cu): CTAs of c.R rows
+// (8 or 16), R / 4 x S threads, passes of 8 batch columns staged by bulk
+// copies one or two passes ahead; one CTA group (c.G = 1).  Wpk per CTA: Wlo[R/4][H/4]
+// then Whi[R/4][H/4] uint4; Wlo[q][c] holds rows 4q, 4q+1 and Whi[q][c] rows
+// 4q+2, 4q+3 of columns 4c .. 4c+3 (fp16, row by row).
+constexpr int kDenseWideMinB = 16;  // two passes of 8 columns or more
+struct DenseWideArgs {
+  RecurCommon c;
+  const void* Wpk;
+  const float* h0_rows;  // [B][H]: h0, or zeros
+  int S;                 // threads per 4-row group: 96, 64 or 32, dividing H / 4
+  int depth;             // passes a copy is issued ahead (1 or 2; depth + 1 h buffers)
+};
+cudaError_t launch_recur_dense_wide(const DenseWideArgs& a, cudaStream_t s);
+// Whether the wide kernel serves H on this device; its rows per CTA, S,
+// prefetch depth and shared memory.
+bool recur_dense_wide_plan(int H, int sm_count, size_t smem_optin, int* R, int* S, int* depth,
+                           size_t* smem);
+
 // Dense fp16 on the tensor cores (persistent_dense_tc.cu): per CTA an image of
 // its rows of Wh, nslices = H/64 K slices of N rows x 128 bytes (fp16,
 // 128-byte swizzle, rows past R zero), N = R rounded up to 16, N <= 32; the

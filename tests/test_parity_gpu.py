@@ -576,6 +576,7 @@ def test_staged_order_matches_column_order(env, spec):
     (dict(H=256, I=100, B=5, T=9, wdtype="f32", h0_std=0.5), "persistent", {}),
     (dict(H=300, B=3, T=7, k=17), "per_step", {}),
     (dict(H=1152, B=16, T=8, wdtype="f16"), "persistent", {"PRNN_OPT_RECURRENT_TC": 2}),
+    (dict(H=1152, B=24, T=10, wdtype="f16", h0_std=0.2), "persistent", {}),
     (dict(H=512, B=4, T=6, k=51), "persistent", {"PRNN_OPT_SYNC_MODE": 1})])
 def test_forward_host_buffers(env, spec, algo, opts):
     """prnn_forward_host on pinned host buffers gives the bits prnn_forward
@@ -684,6 +685,125 @@ def test_tensor_core_recurrence_times_out_cleanly(env):
     lay.set_option(prnn.PRNN_OPT_RECURRENT_TC, 2)
     lay.set_problem_weights(p)
     assert lay.info()["recurrent_tensor_cores"] == 1
+    lay.set_option(prnn.PRNN_OPT_WAIT_TIMEOUT_US, 20000)
+    lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_CTA, 5)
+    lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_STEP, 2)
+    lay.forward(torch.from_numpy(p.x).cuda())
+    assert lay.status() == prnn.PRNN_ERR_TIMEOUT
+    lay.close()
+    y, _ = run_gpu(env, p)
+    check(y, o.forward(p), "f16", "after timeout")
+
+
+# --- dense fp16, wide batches: weights in registers, passes of 8 columns ------------
+WIDE = [dict(H=2304, B=32, T=24, wdtype="f16", h0_std=0.2),  # 16 rows per CTA, 4 passes
+        dict(H=1152, B=32, T=40, wdtype="f16"),              # 8 rows per CTA
+        dict(H=1152, B=16, T=40, wdtype="f16"),              # 2 passes
+        dict(H=1152, B=21, T=20, wdtype="f16", h0_std=0.5),  # passes of 8 + 8 + 5
+        dict(H=640, I=200, B=24, T=16, wdtype="f16", h0_std=1.0),
+        dict(H=256, B=17, T=30, wdtype="f16"),               # passes of 8 + 8 + 1
+        dict(H=1792, B=20, T=20, wdtype="f16"),
+        dict(H=1024, B=16, T=20, wdtype="f16"),
+        dict(H=2048, B=16, T=12, wdtype="f16", h0_std=0.3),
+        dict(H=128, I=64, B=32, T=50, wdtype="f16")]         # 4 weights per thread
+
+
+@pytest.mark.parametrize("spec", WIDE)
+def test_dense_wide_batch_matches_oracle(env, spec):
+    """The wide-batch kernel (forced on for every B >= 16) and the B <= 4
+    kernel both stay within the rule."""
+    _, prnn, o = env
+    p = synth.make_problem(seed=95, **spec)
+    ref = o.forward(p)
+    y, info = run_gpu(env, p, options={prnn.PRNN_OPT_DENSE_WIDE: 2})
+    assert info["dense_wide_batch"] == 1 and info["rows_per_cta"] in (8, 16)
+    assert info["n_cta"] == p.H // info["rows_per_cta"] <= info["sm_count"]
+    check(y, ref, "f16", f"wide {spec}")
+    y_old, info_old = run_gpu(env, p, options={prnn.PRNN_OPT_DENSE_WIDE: 0})
+    assert info_old["dense_wide_batch"] == 0
+    check(y_old, ref, "f16", f"wide off {spec}")
+
+
+def test_dense_wide_batch_exact_properties(env):
+    """Determinism, chaining, and batch independence across the forwards that
+    run the wide kernel (a column's arithmetic does not depend on its pass or
+    neighbours); a forward of fewer than 16 columns runs the B <= 4 kernel
+    and stays within the rule."""
+    torch, prnn, o = env
+    p = synth.make_problem(H=1152, B=32, T=16, wdtype="f16", seed=96, h0_std=0.1)
+    lay = prnn.Layer.from_problem(p)
+    try:
+        assert lay.info()["dense_wide_batch"] == 1  # by default: 4 passes, H >= 1024
+        lay.set_option(prnn.PRNN_OPT_DENSE_WIDE, 2)  # and for the B = 16 forwards below
+        info = lay.info()
+        assert info["dense_wide_batch"] == 1 and info["cta_groups"] == 1
+        assert info["n_cta"] == 144 and info["threads_per_cta"] == 192  # 2 x 96
+        x = torch.from_numpy(p.x).cuda()
+        h0 = torch.from_numpy(p.h0).cuda()
+        y = lay.forward(x, h0)
+        y_again = lay.forward(x, h0)
+        ya = lay.forward(x[:7].contiguous(), h0)
+        yb = lay.forward(x[7:].contiguous(), ya[-1].contiguous())
+        y16a = lay.forward(x[:, :16].contiguous(), h0[:16].contiguous())
+        y16b = lay.forward(x[:, 16:].contiguous(), h0[16:].contiguous())
+        y20 = lay.forward(x[:, 5:25].contiguous(), h0[5:25].contiguous())
+        y10 = lay.forward(x[:, :10].contiguous(), h0[:10].contiguous())  # B <= 4 kernel
+        torch.cuda.synchronize()
+        assert lay.status() == prnn.PRNN_OK
+    finally:
+        lay.close()
+    assert torch.equal(y, y_again)
+    assert torch.equal(torch.cat([ya, yb]), y)
+    assert torch.equal(torch.cat([y16a, y16b], dim=1), y)
+    assert torch.equal(y20, y[:, 5:25])
+    ref = o.forward(p)
+    check(y.cpu().numpy(), ref, "f16", "wide")
+    check(y10.cpu().numpy(), ref[:, :10], "f16", "fallback at 10 columns")
+
+
+def test_dense_wide_batch_full_size_teacher_forced(env):
+    """H = 2304, B = 32, T = 256 (a sweep point): sampled outputs against one
+    oracle step on the GPU's own previous state."""
+    _, _, o = env
+    p = synth.make_problem(H=2304, B=32, T=256, wdtype="f16", seed=97)
+    y, info = run_gpu(env, p)
+    assert info["dense_wide_batch"] == 1 and np.isfinite(y).all()
+    rng = np.random.default_rng(11)
+    samples = [(int(t), int(b), int(r)) for t, b, r in zip(
+        rng.integers(0, p.T, 300), rng.integers(0, p.B, 300), rng.integers(0, p.H, 300))]
+    got = np.array([y[t, b, r] for t, b, r in samples], dtype=np.float64)
+    want = o.cells(p, samples, lambda t, b: p.x[t, b],
+                   lambda t, b: np.zeros(p.H) if t == 0 else y[t - 1, b])
+    assert np.abs(got - want).max() <= TOL["f16"] * float(np.abs(y).max())
+
+
+def test_dense_wide_batch_default_rule(env):
+    """Option 1 (default) runs the wide kernel only where it measured faster;
+    option 0 never; option 2 for every B >= 16."""
+    _, prnn, _ = env
+    cases = [(1152, 32, 1), (1152, 16, 0), (2304, 16, 1), (2304, 32, 1), (640, 32, 0),
+             (1152, 8, 0)]
+    for H, B, want in cases:
+        lay = prnn.Layer(H, H, B, "f16", "persistent")
+        try:
+            p = synth.make_problem(H=H, B=B, T=1, wdtype="f16", seed=99)
+            lay.set_problem_weights(p)
+            assert lay.info()["dense_wide_batch"] == want, (H, B)
+            lay.set_option(prnn.PRNN_OPT_DENSE_WIDE, 0)
+            assert lay.info()["dense_wide_batch"] == 0
+            lay.set_option(prnn.PRNN_OPT_DENSE_WIDE, 2)
+            assert lay.info()["dense_wide_batch"] == (1 if B >= 16 else 0)
+            with pytest.raises(prnn.PrnnError):
+                lay.set_option(prnn.PRNN_OPT_DENSE_WIDE, 3)
+        finally:
+            lay.close()
+
+
+def test_dense_wide_batch_times_out_cleanly(env):
+    torch, prnn, o = env
+    p = synth.make_problem(H=1152, B=24, T=6, wdtype="f16", seed=98)
+    lay = prnn.Layer.from_problem(p)
+    assert lay.info()["dense_wide_batch"] == 1
     lay.set_option(prnn.PRNN_OPT_WAIT_TIMEOUT_US, 20000)
     lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_CTA, 5)
     lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_STEP, 2)
