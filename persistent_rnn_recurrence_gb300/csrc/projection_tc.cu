@@ -22,6 +22,12 @@
 // Every mbarrier wait is bounded; a timeout sets the status word and the CTA
 // still waits for its issued work, frees its TMEM and returns.
 //
+// In the forward the GEMM is launched as the programmatic dependent of the x
+// staging kernel: its launch, TMEM allocation and first weight stages overlap
+// the staging, and the producer waits for the staging grid
+// (griddepcontrol.wait) before its first x16 load (-2 us of the ~30 us
+// projection stage at M = 1024).
+//
 // The same kernel, without bias and with bf16 operands, computes the weight
 // and input gradients of the backward pass (launch_gemm_tc): C[m][n] =
 // sum_k A[m][k] * B[n][k] with both operands K-major.
@@ -40,7 +46,10 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BK = 64, kStages = 4;
+constexpr int BM = 128, BK = 64;
+// The projection GEMM starts as the programmatic dependent of the x staging
+// kernel (its set-up and first weight stages overlap the staging).
+constexpr bool kProjectionPdl = true;
 constexpr int kThreads = 128;
 constexpr uint32_t kTileA = BM * BK * 2;  // 16 KiB
 constexpr long long kWaitNs = 200LL * 1000 * 1000;                   // 200 ms per wait
@@ -53,6 +62,9 @@ struct TileCfg {
   static constexpr uint32_t kTileB = BN * BK * 2;
   static constexpr uint32_t kStageBytes = kTileA + kTileB;
   static constexpr uint32_t kTmemCols = BN <= 64 ? 64 : 128;
+  // a 4-stage ring: 7 or 8 stages (as many as shared memory holds) measured
+  // slower, at M = 1024 (+2 us) and M = 8192 (1.7x the GEMM time)
+  static constexpr int kStages = 4;
   static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;  // + alignment slack
 };
 
@@ -81,6 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kTileB = TileCfg<BN>::kTileB;
   constexpr uint32_t kStageBytes = TileCfg<BN>::kStageBytes;
   constexpr uint32_t kTmemCols = TileCfg<BN>::kTmemCols;
+  constexpr int kStages = TileCfg<BN>::kStages;
   (void)kTileB;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -121,6 +134,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---- TMA producer ----
+    // B (the weights) does not depend on the kernel before this one: its
+    // first stages are requested before waiting for that kernel (a no-op
+    // unless this grid was launched as its programmatic dependent), then A
+    const int pre = nkb < kStages ? nkb : kStages;
+    for (int kb = 0; kb < pre; ++kb) {
+      mbar_arrive_expect_tx(&full_bar[kb], kStageBytes);
+      tma_load_2d(base + (uint32_t)kb * kStageBytes + kTileA, &tmB, &full_bar[kb], kb * BK, n0);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     int issued = 0;
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % kStages;
@@ -130,9 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const uint32_t sa = base + (uint32_t)s * kStageBytes;
-      mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
+      if (kb >= pre) {
+        mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
+        tma_load_2d(sa + kTileA, &tmB, &full_bar[s], kb * BK, n0);
+      }
       tma_load_2d(sa, &tmA, &full_bar[s], kb * BK, m0);
-      tma_load_2d(sa + kTileA, &tmB, &full_bar[s], kb * BK, n0);
       ++issued;
     }
     // every issued load lands before the CTA may leave
@@ -226,6 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // else scalar loads.
 __global__ void stage_x_f16_kernel(const float* __restrict__ x, __half* __restrict__ x16, int M,
                                    int K, int Kp) {
+  // the GEMM launched after this kernel may start its set-up and weight
+  // loads now; it waits for this grid's completion before reading x16
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int groups = Kp / 8;
   const size_t total = (size_t)M * groups;
   const bool vec_rows = (K & 3) == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
@@ -315,30 +342,40 @@ int pick_bn(int M, int N) {
   return best;
 }
 
+// after_producer: launch as the programmatic dependent of the kernel before
+// it on the stream (that kernel must not write B, P or the y fill)
 template <int BN>
 cudaError_t launch_tc_bn(const CUtensorMap& tmA, const void* Bp, int Kp, int N, bool bf16,
-                         const TcKernelArgs& ka, cudaStream_t s) {
+                         const TcKernelArgs& ka, bool after_producer, cudaStream_t s) {
   CUtensorMap tmB;
   if (!encode_kmajor(&tmB, Bp, Kp, N, BN, bf16)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel<BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)TileCfg<BN>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const dim3 grid((ka.N + BN - 1) / BN, (ka.M + BM - 1) / BM);
-  proj_tc_kernel<BN><<<grid, kThreads, TileCfg<BN>::kSmemBytes, s>>>(tmA, tmB, ka);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((ka.N + BN - 1) / BN, (ka.M + BM - 1) / BM);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_producer ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, proj_tc_kernel<BN>, tmA, tmB, ka);
 }
 
 cudaError_t launch_tc(const void* A, const void* B, int M, int N, int Kp, bool bf16,
-                      TcKernelArgs ka, cudaStream_t s) {
+                      TcKernelArgs ka, bool after_producer, cudaStream_t s) {
   CUtensorMap tmA;
   if (!encode_kmajor(&tmA, A, Kp, M, BM, bf16)) return cudaErrorInvalidValue;
   const int bn = pick_bn(M, N);
   ka.idesc = bf16 ? bf16_idesc(BM, bn) : f16_idesc(BM, bn);
   switch (bn) {
-    case 64: return launch_tc_bn<64>(tmA, B, Kp, N, bf16, ka, s);
-    case 96: return launch_tc_bn<96>(tmA, B, Kp, N, bf16, ka, s);
-    default: return launch_tc_bn<128>(tmA, B, Kp, N, bf16, ka, s);
+    case 64: return launch_tc_bn<64>(tmA, B, Kp, N, bf16, ka, after_producer, s);
+    case 96: return launch_tc_bn<96>(tmA, B, Kp, N, bf16, ka, after_producer, s);
+    default: return launch_tc_bn<128>(tmA, B, Kp, N, bf16, ka, after_producer, s);
   }
 }
 
@@ -358,14 +395,14 @@ cudaError_t launch_projection_tc(const ProjTcArgs& a, int* status, cudaStream_t 
   }
   // 2. tensor-core GEMM
   TcKernelArgs ka{a.M, a.N, a.Kp, a.bias, a.P, a.y_fill, status, 0u};
-  return launch_tc(a.x16, a.Wx16, a.M, a.N, a.Kp, false, ka, s);
+  return launch_tc(a.x16, a.Wx16, a.M, a.N, a.Kp, false, ka, kProjectionPdl, s);
 }
 
 cudaError_t launch_gemm_tc(const GemmTcArgs& g, int* status, cudaStream_t s) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   if (g.Kp % BK != 0) return cudaErrorInvalidValue;
   TcKernelArgs ka{g.M, g.N, g.Kp, nullptr, g.C, nullptr, status, 0u};
-  return launch_tc(g.A, g.B, g.M, g.N, g.Kp, g.bf16, ka, s);
+  return launch_tc(g.A, g.B, g.M, g.N, g.Kp, g.bf16, ka, false, s);
 }
 
 }  // namespace prnn
