@@ -68,11 +68,16 @@ __device__ __forceinline__ bool wait_copy(uint64_t* bar, uint32_t parity, uint64
 // Re-poll the stale float4s among the n4 staged at hs (copied from src):
 // each thread checks slots tid, tid + NT, ... and re-issues, together, the
 // relaxed loads of up to 4 stale slots per round trip.  False if the wait
-// gave up.
+// gave up.  A thread that wrote into hs fences its writes against the async
+// proxy, so a later bulk copy into the same buffer is ordered after them
+// (with the CTA barrier that follows every call); the issuing thread fences
+// again before each copy.
 __device__ __forceinline__ bool fix_stale(const float* src, int n4, float* hs, Waiter& w) {
   const int NT = blockDim.x, tid = threadIdx.x;
   float4* h4 = reinterpret_cast<float4*>(hs);
   const float4* s4 = reinterpret_cast<const float4*>(src);
+  bool wrote = false;
+  bool ok = true;
   for (int base = tid; base < n4; base += 4 * NT) {
     float4 v[4];
     unsigned stale = 0;
@@ -85,6 +90,7 @@ __device__ __forceinline__ bool fix_stale(const float* src, int n4, float* hs, W
       }
     }
     if (stale == 0u) continue;
+    wrote = true;
     uint32_t spins = 0, round = 0;
     for (;;) {
 #pragma unroll
@@ -99,11 +105,16 @@ __device__ __forceinline__ bool fix_stale(const float* src, int n4, float* hs, W
         if (((stale & ~still) >> u) & 1u) h4[base + u * NT] = v[u];
       stale = still;
       if (stale == 0u) break;
-      if (!w.still_ok(spins)) return false;
+      if (!w.still_ok(spins)) {
+        ok = false;
+        break;
+      }
       w.pause(round);
     }
+    if (!ok) break;
   }
-  return true;
+  if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  return ok;
 }
 
 // 4-row x 4-column fp16 block -> fp32: lo holds rows 0, 1 and hi rows 2, 3
@@ -171,7 +182,7 @@ __global__ void __launch_bounds__(R / 4 * S, 1) recur_dense_wide_kernel(const De
     *bs = pl.b_lo + p * kWidePass;
     return min(kWidePass, pl.b_hi - *bs);
   };
-  auto issue = [&](int seq) {  // thread 0: bulk copy of pass seq into buffer seq % NB
+  auto issue = [&](int seq) {  // issuer: bulk copy of pass seq into buffer seq % NB
     const int t = seq / P;
     int bs;
     const int nb = pass_cols(seq, &bs);
@@ -194,8 +205,14 @@ __global__ void __launch_bounds__(R / 4 * S, 1) recur_dense_wide_kernel(const De
     return outs ? ld_nc_pinned(c.P + ((size_t)(seq / P) * B + bs + oc) * H + orow) : 0.f;
   };
 
-  int issued = -1;  // thread 0: last pass whose copy was issued
-  if (tid == 0)
+  // The copies are issued by the last thread.  When the CTA has more threads
+  // than outputs its warp has no output work after a pass's barrier, so it
+  // reaches the next pass's copy wait first and starts the following copy
+  // earlier than an output thread would (measured at H = 1792, B = 32:
+  // 9.8 against 11.4 us per step with thread 0 issuing).
+  const bool issuer = tid == (int)blockDim.x - 1;
+  int issued = -1;  // issuer: last pass whose copy was issued
+  if (issuer)
     for (int k = 0; k < D && k < nseq; ++k) issue(issued = k);
   float pv_next = nseq > 0 ? load_p(0) : 0.f;
   Waiter w;
@@ -218,7 +235,7 @@ __global__ void __launch_bounds__(R / 4 * S, 1) recur_dense_wide_kernel(const De
       report_timeout(c.status, t, cta);
       s_abort = 1;
     }
-    if (tid == 0 && seq + D < nseq && !s_abort) issue(issued = seq + D);
+    if (issuer && seq + D < nseq && !s_abort) issue(issued = seq + D);
     float* hs = hbuf + (size_t)buf * kWidePass * H;
     float* rb = red + (size_t)(seq & 1) * QG * WPQ * 32;
     // the copy of pass seq was issued P - D passes after this CTA published
@@ -285,8 +302,8 @@ __global__ void __launch_bounds__(R / 4 * S, 1) recur_dense_wide_kernel(const De
       __syncthreads();
     }
     if (s_abort) {
-      // let thread 0's copies in flight land before the CTA leaves
-      if (tid == 0)
+      // let the copies in flight land before the CTA leaves
+      if (issuer)
         for (int k = seq + 1; k <= issued; ++k)
           wait_copy(&full[k % NB], (uint32_t)(k / NB) & 1u, copy_limit_ns);
       return;
