@@ -206,8 +206,12 @@ prnn_status_t prnn_forward(prnn_t h, int T, int B, const float* x, const float* 
  * recurrent kernel stores into y at every [t][b][r] offset).  As a best-effort
  * guard only, a buffer whose first or last element lies outside every
  * page-locked allocation is refused; a short buffer followed by another
- * page-locked allocation is not detected.  y must not overlap x or h0.  x and h0 are copied to device workspaces owned by the
- * handle (grown on demand, freed by prnn_destroy).  The persistent CUDA-core
+ * page-locked allocation is not detected.  y must not overlap x or h0.  h0 is copied to a
+ * device workspace owned by the handle (grown on demand, freed by
+ * prnn_destroy).  With the tensor-core projection (prnn_info_t
+ * projection_tensor_cores = 1) the projection's staging kernel reads x
+ * straight from the host buffer, once; otherwise x is copied to a device
+ * workspace first.  The persistent CUDA-core
  * recurrent kernels write every output into y itself, over the host link, as
  * they publish it, so the result needs no separate copy back; the per-step
  * path and the tcgen05 dense recurrence copy y back after the recurrence.

@@ -346,6 +346,10 @@ cudaError_t ensure_f32(float** p, size_t* cap, size_t n) {
   return e;
 }
 
+// prnn_forward_host: the projection's staging kernel reads x from the host
+// buffer itself (no copy) when the layer uses the tensor-core projection.
+constexpr bool kHostXDirect = true;
+
 // The device address of page-locked host memory, or nullptr for anything
 // else (pageable or device memory, or a pointer CUDA does not know).
 const void* mapped_host(const void* p) {
@@ -1099,18 +1103,28 @@ prnn_status_t prnn_forward_host(prnn_t h, int T, int B, const float* x, const fl
   // page-locked allocation, not when another allocation follows it (the
   // element counts are the caller's precondition, include/prnn.h)
   float* ydev = static_cast<float*>(const_cast<void*>(mapped_host(y)));
-  if (!mapped_host(x) || !mapped_host(x + nx - 1) || !ydev || !mapped_host(y + ny - 1) ||
+  const float* xdev = static_cast<const float*>(mapped_host(x));
+  if (!xdev || !mapped_host(x + nx - 1) || !ydev || !mapped_host(y + ny - 1) ||
       (h0 && (!mapped_host(h0) || !mapped_host(h0 + n0 - 1))))
     return PRNN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  PRNN_TRY(ensure_f32(&h->hx, &h->hx_cap, nx));
+  // With the tensor-core projection x is read once, by its fp16 staging
+  // kernel, which then reads it straight from the host buffer over the host
+  // link: no copy of x.  The CUDA-core projection reads each x tile many
+  // times, so there x is copied to a device workspace first.
+  const bool x_direct = h->tc_proj && h->proj_mode == 0 && kHostXDirect;
+  const float* xin = xdev;
+  if (!x_direct) {
+    PRNN_TRY(ensure_f32(&h->hx, &h->hx_cap, nx));
+    PRNN_TRY(cudaMemcpyAsync(h->hx, x, nx * 4, cudaMemcpyHostToDevice, s));
+    xin = h->hx;
+  }
   PRNN_TRY(ensure_f32(&h->hy, &h->hy_cap, ny));
   if (h0) PRNN_TRY(ensure_f32(&h->hh0, &h->hh0_cap, n0));
-  PRNN_TRY(cudaMemcpyAsync(h->hx, x, nx * 4, cudaMemcpyHostToDevice, s));
   if (h0) PRNN_TRY(cudaMemcpyAsync(h->hh0, h0, n0 * 4, cudaMemcpyHostToDevice, s));
   const bool mirror = recurrence_mirrors(h);
   const prnn_status_t st =
-      forward_impl(h, T, B, h->hx, h0 ? h->hh0 : nullptr, h->hy, mirror ? ydev : nullptr, s);
+      forward_impl(h, T, B, xin, h0 ? h->hh0 : nullptr, h->hy, mirror ? ydev : nullptr, s);
   if (st != PRNN_OK) return st;
   if (!mirror) PRNN_TRY(cudaMemcpyAsync(y, h->hy, ny * 4, cudaMemcpyDeviceToHost, s));
   return PRNN_OK;
