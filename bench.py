@@ -69,6 +69,9 @@ def parse_args(argv=None):
     ap.add_argument("--trace-out", default="", help="save the raw trace records (.npy)")
     ap.add_argument("--backward", action="store_true",
                     help="training step (forward + backward through time) of the named workloads")
+    ap.add_argument("--cluster-probe", action="store_true",
+                    help="step exchange through distributed shared memory inside thread-block "
+                         "clusters (no arithmetic) beside the L2 exchange floor of the config")
     return ap.parse_args(argv)
 
 
@@ -1207,6 +1210,54 @@ def run_trace(args):
     return 0 if same and st == prnn.PRNN_OK else 1
 
 
+def run_cluster_probe(args):
+    """The exchange of h inside thread-block clusters through distributed
+    shared memory (prnn_probe_cluster_exchange: no arithmetic, every word
+    checked), at the sizes of the named layers, beside the L2 exchange floor
+    of the config's layer (prnn_probe_sync_floor, same grid as its forward).
+    One JSON line: ns per step for each cluster size, with one cluster per
+    batch column of the config (B clusters) and with as many clusters as the
+    device holds at once."""
+    import torch
+    from persistent_rnn_recurrence_gb300 import prnn, synth
+    torch.cuda.init()
+    p = synth.named_problem(args.config)
+    lay = prnn.Layer.from_problem(p)
+    lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+    ys = torch.empty(p.T, p.B, p.H, device="cuda")
+    fl = []
+    for _ in range(7):
+        prnn.prnn_probe_sync_floor(lay.h, p.T, p.B, ys)
+        fl.append(prnn.prnn_get_timing(lay.h)[1])
+    lay.close()
+    fl.sort()
+    out = {"metric": "step exchange ns per step (no arithmetic)", "config": {"workload": args.config},
+           "l2_sync_floor_ns_per_step": 1e6 * fl[len(fl) // 2] / p.T, "cluster": []}
+    steps = 400
+    for H in (p.H, 5760):
+        for cs in (2, 4, 8, 16):
+            row = {"hidden": H, "cluster_size": cs}
+            if H % (4 * cs):
+                continue
+            for key, n in (("b_clusters", p.B), ("max_clusters", 152 // cs)):
+                while n >= 1:
+                    try:
+                        ns, bad = prnn.prnn_probe_cluster_exchange(H, cs, n, steps)
+                        best = ns
+                        for _ in range(2):  # best of three
+                            ns, b2 = prnn.prnn_probe_cluster_exchange(H, cs, n, steps)
+                            best, bad = min(best, ns), bad + b2
+                        row[key] = {"clusters": n, "ns_per_step": best, "wrong_words": bad}
+                        break
+                    except prnn.PrnnError as e:
+                        if e.status != prnn.PRNN_ERR_UNSUPPORTED:
+                            raise
+                        n -= 1
+            out["cluster"].append(row)
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -1225,6 +1276,8 @@ def main(argv=None):
         return run_trace(args)
     if args.vendor:
         return run_vendor(args)
+    if args.cluster_probe:
+        return run_cluster_probe(args)
     return run_ours(args)
 
 

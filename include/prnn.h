@@ -316,6 +316,32 @@ prnn_status_t prnn_set_trace_buffer(prnn_t h, void* buffer, size_t bytes);
 prnn_status_t prnn_probe_sync_floor(prnn_t h, int T, int B, float* y, void* stream);
 
 /*
+ * Diagnostic (no handle): the step exchange of h inside thread-block clusters,
+ * through distributed shared memory, with no arithmetic -- the alternative to
+ * the L2 exchange of the persistent kernels (prnn_probe_sync_floor), measured
+ * on the device.  `clusters` clusters of `cluster_size` CTAs (2, 4, 8 or 16)
+ * each exchange a vector of `hidden` floats per step for `steps` steps
+ * (hidden a multiple of 4 * cluster_size, at most 16384; steps >= 2): CTA r
+ * owns rows [r*R, (r+1)*R), R = hidden / cluster_size, and pushes them into
+ * the shared memory of every CTA of its cluster (its own included) with
+ * st.async, 16 bytes at a time, completing on the receiver's mbarrier; a CTA
+ * waits for the whole vector of a step before it sends its rows of the next
+ * step.  Every received word is checked, one step late (off the exchange's
+ * critical path).
+ * Outputs: *ns_per_step, the mean over clusters of each cluster's exchange
+ * time (globaltimer, its first CTA) divided by steps; *mismatches, the words
+ * received with a wrong value (0 unless the exchange is broken).
+ * Synchronous: runs on the current device's default stream and waits for it;
+ * allocates and frees a few bytes of device memory.
+ * Errors: INVALID_ARG for a size outside the above or a NULL output;
+ * UNSUPPORTED when the device cannot launch clusters or cannot hold all the
+ * clusters at once (cudaOccupancyMaxActiveClusters: on GB300, 9 sixteen-CTA
+ * clusters of this probe); TIMEOUT when a wait ran out (1 s); CUDA, OOM.
+ */
+prnn_status_t prnn_probe_cluster_exchange(int hidden, int cluster_size, int clusters, int steps,
+                                          double* ns_per_step, long long* mismatches);
+
+/*
  * Host only (no GPU): the packing the persistent sparse kernel applies to
  * row-balanced weights, exposed so the layout can be checked bit for bit.
  * Rows are split over n_cta CTAs of rows_per_cta rows; each row over

@@ -36,6 +36,7 @@ PRNN_STACK_WAVEFRONT, PRNN_STACK_LAYERWISE = 0, 1
 EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
            "prnn_forward", "prnn_forward_host", "prnn_destroy", "prnn_get_status", "prnn_status_string",
            "prnn_set_option", "prnn_get_info", "prnn_get_timing", "prnn_probe_sync_floor",
+           "prnn_probe_cluster_exchange",
            "prnn_set_trace_buffer",
            "prnn_pack_sparse_host", "prnn_pack_sparse_host_placed", "prnn_forward_dense_noalloc",
            "prnn_set_weights_csr",
@@ -84,6 +85,8 @@ _sig = {
     "prnn_get_info": ([_P, ctypes.POINTER(prnn_info_t)], _I),
     "prnn_get_timing": ([_P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)], _I),
     "prnn_probe_sync_floor": ([_P, _I, _I, _P, _P], _I),
+    "prnn_probe_cluster_exchange": ([_I, _I, _I, _I, ctypes.POINTER(ctypes.c_double),
+                                     ctypes.POINTER(ctypes.c_longlong)], _I),
     "prnn_set_trace_buffer": ([_P, _P, ctypes.c_size_t], _I),
     "prnn_pack_sparse_host": ([_I, _I, _I, _I, _I, _P, _P, _P, ctypes.c_size_t,
                                ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
@@ -232,6 +235,17 @@ def prnn_pack_sparse_host_placed(hidden, k, n_cta, rows_per_cta, threads_per_row
 def prnn_probe_sync_floor(h: int, T: int, B: int, y, stream=None) -> None:
     _check(_lib.prnn_probe_sync_floor(h, T, B, _ptr(y), _stream(stream)),
            "prnn_probe_sync_floor")
+
+
+def prnn_probe_cluster_exchange(hidden: int, cluster_size: int, clusters: int,
+                                steps: int) -> tuple:
+    """(ns per step, wrong words received) of the cluster exchange probe."""
+    ns = ctypes.c_double(0.0)
+    bad = ctypes.c_longlong(0)
+    _check(_lib.prnn_probe_cluster_exchange(hidden, cluster_size, clusters, steps,
+                                            ctypes.byref(ns), ctypes.byref(bad)),
+           "prnn_probe_cluster_exchange")
+    return ns.value, bad.value
 
 
 def prnn_set_trace_buffer(h: int, buf, nbytes: int) -> None:

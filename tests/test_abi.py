@@ -129,3 +129,22 @@ def test_stack_and_backward_argument_checks_without_gpu(lib):
                            None, None) == prnn.PRNN_ERR_INVALID_ARG
     assert f.prnn_set_weights_csr(None, None, 0, None, None, None, None, None) == \
         prnn.PRNN_ERR_INVALID_ARG
+
+
+def test_cluster_probe_argument_checks_without_gpu(lib):
+    """The cluster exchange probe rejects its bad arguments before any CUDA call."""
+    from persistent_rnn_recurrence_gb300 import prnn
+    f = prnn._lib
+    ns, bad = ctypes.c_double(), ctypes.c_longlong()
+    out = (ctypes.byref(ns), ctypes.byref(bad))
+    for hidden, cs, ncl, steps in ((1792, 3, 1, 10),     # cluster size not 2, 4, 8 or 16
+                                   (1790, 4, 1, 10),     # not a multiple of 4 * cluster size
+                                   (1800, 16, 1, 10),    # 1800 % 64 != 0
+                                   (32, 16, 1, 10),      # fewer than 4 rows per CTA
+                                   (20480, 2, 1, 10),    # beyond 16384
+                                   (1792, 4, 0, 10),     # no cluster
+                                   (1792, 4, 1, 1)):     # fewer than 2 steps
+        assert f.prnn_probe_cluster_exchange(hidden, cs, ncl, steps, *out) == \
+            prnn.PRNN_ERR_INVALID_ARG, (hidden, cs, ncl, steps)
+    assert f.prnn_probe_cluster_exchange(1792, 4, 1, 10, None, ctypes.byref(bad)) == \
+        prnn.PRNN_ERR_INVALID_ARG

@@ -812,3 +812,20 @@ def test_dense_wide_batch_times_out_cleanly(env):
     lay.close()
     y, _ = run_gpu(env, p)
     check(y, o.forward(p), "f16", "after timeout")
+
+
+# --- the cluster exchange probe (a diagnostic of the step exchange) --------------------
+def test_cluster_exchange_probe(env):
+    """Every word pushed through distributed shared memory arrives with its
+    value, at every cluster size; more clusters than the device can hold at
+    once are refused."""
+    _, prnn, _ = env
+    for cs, ncl in ((2, 8), (4, 8), (8, 4), (16, 2), (16, 1)):
+        ns, bad = prnn.prnn_probe_cluster_exchange(1792, cs, ncl, 200)
+        assert bad == 0, (cs, ncl)
+        assert 0.0 < ns < 1e5, (cs, ncl, ns)
+    ns, bad = prnn.prnn_probe_cluster_exchange(5760, 16, 1, 50)
+    assert bad == 0 and ns > 0.0
+    with pytest.raises(prnn.PrnnError) as e:
+        prnn.prnn_probe_cluster_exchange(1792, 16, 1000, 10)
+    assert e.value.status == prnn.PRNN_ERR_UNSUPPORTED
