@@ -50,6 +50,9 @@ constexpr int BM = 128, BK = 64;
 // The projection GEMM starts as the programmatic dependent of the x staging
 // kernel (its set-up and first weight stages overlap the staging).
 constexpr bool kProjectionPdl = true;
+// P written through shared memory by TMA stores (whole 128-byte lines)
+// instead of each thread storing its own row of the tile.
+constexpr bool kTmaStoreEpilogue = true;
 constexpr int kThreads = 128;
 constexpr uint32_t kTileA = BM * BK * 2;  // 16 KiB
 constexpr long long kWaitNs = 200LL * 1000 * 1000;                   // 200 ms per wait
@@ -84,12 +87,24 @@ struct TcKernelArgs {
   float* y_fill;
   int* status;
   uint32_t idesc;
+  int tma_out;           // 1: P written by TMA tensor stores through shared memory (tmC)
 };
+
+// Store one 32-float x 128-row block of P from shared memory (128-byte
+// swizzled rows) at column c0, row r0; the tensor map clips what lies
+// outside P.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0,
+                                             int r0) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(r0)
+               : "memory");
+}
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     proj_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcKernelArgs a) {
+                   const __grid_constant__ CUtensorMap tmC, const TcKernelArgs a) {
   constexpr uint32_t kTileB = TileCfg<BN>::kTileB;
   constexpr uint32_t kStageBytes = TileCfg<BN>::kStageBytes;
   constexpr uint32_t kTmemCols = TileCfg<BN>::kTmemCols;
@@ -192,7 +207,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!ok) atomicExch(&s_err, 1);
   __syncthreads();
   const bool good = (s_err == 0);
-  if (good) {
+  if (good && a.tma_out) {
+    // The ring is idle once the accumulator is complete: column block j of
+    // the tile (32 columns x 128 rows) is staged at base + j * 16 KiB, row r
+    // at 128 r bytes with 16-byte chunk c at c ^ (r % 8) (the 128-byte
+    // swizzle of the output tensor map), then written by one TMA store.  A
+    // warp's 8-lane phases hit 8 different chunks: no bank conflicts.
+    const int r = warp * 32 + lane;
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+      uint32_t v[32];
+      tmem_load_32cols(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * 32), v);
+      const int nb = n0 + j * 32;
+      unsigned char* blk = smem_raw + (base - smem_u32(smem_raw)) + (size_t)j * 16384;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float4 o;
+        o.x = __uint_as_float(v[4 * c + 0]);
+        o.y = __uint_as_float(v[4 * c + 1]);
+        o.z = __uint_as_float(v[4 * c + 2]);
+        o.w = __uint_as_float(v[4 * c + 3]);
+        if (a.bias) {
+          const int n = nb + 4 * c;
+          o.x += n + 0 < a.N ? __ldg(a.bias + n + 0) : 0.f;
+          o.y += n + 1 < a.N ? __ldg(a.bias + n + 1) : 0.f;
+          o.z += n + 2 < a.N ? __ldg(a.bias + n + 2) : 0.f;
+          o.w += n + 3 < a.N ? __ldg(a.bias + n + 3) : 0.f;
+        }
+        *reinterpret_cast<float4*>(blk + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+      for (int j = 0; j < BN / 32; ++j) tma_store_2d(&tmC, base + (uint32_t)j * 16384u, n0 + 32 * j, m0);
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    // the sentinel fill of y: row segments, consecutive lanes on consecutive
+    // float4s (the fill depends on nothing in the tile)
+    if (a.y_fill) {
+      const float sv = __uint_as_float(kSentinel);
+      const float4 s4 = make_float4(sv, sv, sv, sv);
+      constexpr int kQ = BN / 4;
+      for (int i = tid; i < BM * kQ; i += kThreads) {
+        const int m = m0 + i / kQ, n = n0 + 4 * (i % kQ);
+        if (m >= a.M) break;
+        float* yrow = a.y_fill + (size_t)m * a.N;
+        if (n + 3 < a.N) {
+          *reinterpret_cast<float4*>(yrow + n) = s4;
+        } else {
+          for (int q = 0; q < 4; ++q)
+            if (n + q < a.N) yrow[n + q] = sv;
+        }
+      }
+    }
+    // the stores must have read the staged tile before the CTA leaves
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  } else if (good) {
     const int m = m0 + warp * 32 + lane;
     const bool vec = (a.N & 3) == 0;
 #pragma unroll 1
@@ -316,6 +387,20 @@ bool encode_kmajor(CUtensorMap* map, const void* base, int Kp, int rows, int box
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// P [M][N] fp32 as the destination of 32-column x 128-row TMA stores from
+// 128-byte swizzled shared memory (needs N % 4 == 0 and a 16-byte aligned P).
+bool encode_out(CUtensorMap* map, float* P, int N, int M) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || (N & 3) != 0 || (reinterpret_cast<uintptr_t>(P) & 15u) != 0) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)N * 4};
+  const cuuint32_t box[2] = {32, (cuuint32_t)BM};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, P, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool projection_tc_supported() { return encode_fn() != nullptr; }
@@ -345,8 +430,9 @@ int pick_bn(int M, int N) {
 // after_producer: launch as the programmatic dependent of the kernel before
 // it on the stream (that kernel must not write B, P or the y fill)
 template <int BN>
-cudaError_t launch_tc_bn(const CUtensorMap& tmA, const void* Bp, int Kp, int N, bool bf16,
-                         const TcKernelArgs& ka, bool after_producer, cudaStream_t s) {
+cudaError_t launch_tc_bn(const CUtensorMap& tmA, const CUtensorMap& tmC, const void* Bp, int Kp,
+                         int N, bool bf16, const TcKernelArgs& ka, bool after_producer,
+                         cudaStream_t s) {
   CUtensorMap tmB;
   if (!encode_kmajor(&tmB, Bp, Kp, N, BN, bf16)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel<BN>,
@@ -363,19 +449,23 @@ cudaError_t launch_tc_bn(const CUtensorMap& tmA, const void* Bp, int Kp, int N, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = after_producer ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, proj_tc_kernel<BN>, tmA, tmB, ka);
+  return cudaLaunchKernelEx(&cfg, proj_tc_kernel<BN>, tmA, tmB, tmC, ka);
 }
 
 cudaError_t launch_tc(const void* A, const void* B, int M, int N, int Kp, bool bf16,
                       TcKernelArgs ka, bool after_producer, cudaStream_t s) {
-  CUtensorMap tmA;
+  CUtensorMap tmA, tmC;
   if (!encode_kmajor(&tmA, A, Kp, M, BM, bf16)) return cudaErrorInvalidValue;
+  // the TMA-store epilogue where P's rows allow it; otherwise per-thread row
+  // stores (tmC is then unused: any valid map stands in)
+  ka.tma_out = kTmaStoreEpilogue && encode_out(&tmC, ka.P, N, M) ? 1 : 0;
+  if (!ka.tma_out) tmC = tmA;
   const int bn = pick_bn(M, N);
   ka.idesc = bf16 ? bf16_idesc(BM, bn) : f16_idesc(BM, bn);
   switch (bn) {
-    case 64: return launch_tc_bn<64>(tmA, B, Kp, N, bf16, ka, after_producer, s);
-    case 96: return launch_tc_bn<96>(tmA, B, Kp, N, bf16, ka, after_producer, s);
-    default: return launch_tc_bn<128>(tmA, B, Kp, N, bf16, ka, after_producer, s);
+    case 64: return launch_tc_bn<64>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s);
+    case 96: return launch_tc_bn<96>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s);
+    default: return launch_tc_bn<128>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s);
   }
 }
 
@@ -394,14 +484,14 @@ cudaError_t launch_projection_tc(const ProjTcArgs& a, int* status, cudaStream_t 
     if (e != cudaSuccess) return e;
   }
   // 2. tensor-core GEMM
-  TcKernelArgs ka{a.M, a.N, a.Kp, a.bias, a.P, a.y_fill, status, 0u};
+  TcKernelArgs ka{a.M, a.N, a.Kp, a.bias, a.P, a.y_fill, status, 0u, 0};
   return launch_tc(a.x16, a.Wx16, a.M, a.N, a.Kp, false, ka, kProjectionPdl, s);
 }
 
 cudaError_t launch_gemm_tc(const GemmTcArgs& g, int* status, cudaStream_t s) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   if (g.Kp % BK != 0) return cudaErrorInvalidValue;
-  TcKernelArgs ka{g.M, g.N, g.Kp, nullptr, g.C, nullptr, status, 0u};
+  TcKernelArgs ka{g.M, g.N, g.Kp, nullptr, g.C, nullptr, status, 0u, 0};
   return launch_tc(g.A, g.B, g.M, g.N, g.Kp, g.bf16, ka, false, s);
 }
 
