@@ -154,6 +154,22 @@ def test_tensor_core_projection_matches_cuda_core(env, spec):
     assert np.abs(y_tc - y_cc).max() <= 5e-3 * np.abs(ref).max()
 
 
+def test_tensor_core_projection_ragged_rows(env):
+    """H % 4 != 0 (the per-step path; the persistent kernels need H % 4 == 0):
+    P's rows are not 16-byte multiples, so the tcgen05 projection stores its
+    tiles thread by thread instead of by TMA, and still agrees with the
+    CUDA-core projection and the oracle."""
+    _, prnn, o = env
+    p = synth.make_problem(H=301, I=77, B=3, T=5, wdtype="f16", seed=34, h0_std=0.3)
+    y_tc, info = run_gpu(env, p, algo="per_step")
+    assert info["projection_tensor_cores"] == 1
+    y_cc, _ = run_gpu(env, p, algo="per_step", options={prnn.PRNN_OPT_PROJECTION: 1})
+    ref = o.forward(p)
+    check(y_tc, ref, "f16", "tc ragged")
+    check(y_cc, ref, "f16", "cuda cores ragged")
+    assert np.abs(y_tc - y_cc).max() <= 5e-3 * np.abs(ref).max()
+
+
 def test_h0_none_equals_zeros(env):
     torch, prnn, _ = env
     p = synth.make_problem(H=256, B=2, T=4, k=20, seed=32)
