@@ -655,6 +655,14 @@ def run_sweep(args):
                           "timesteps_per_s": 1e3 * p.T / (rec + proj),
                           "status": prnn.prnn_status_string(st),
                           "groups": info["cta_groups"], "n_cta": info["n_cta"]}
+            if p.sparse and algo == "persistent":
+                # the sparse gathers' shared-memory bound: every entry x batch
+                # column reads its own 4-byte h word, plus the 4-byte entries
+                smem_bw = (info["sm_count"] or 152) * 128 * \
+                    load_peaks().get("sm_max_mhz", 2070.0) * 1e6
+                t_smem = (4.0 * p.nnz * p.B + 4.0 * p.nnz) / smem_bw
+                line[algo]["frac_of_smem_gather_bound"] = t_smem / (1e-6 * line[algo][
+                    "recurrence_us_per_step"])
         if "recurrence_us_per_step" in line.get("persistent", {}) and \
                 "recurrence_us_per_step" in line.get("per_step", {}):
             line["persistent_speedup"] = (line["per_step"]["recurrence_us_per_step"]
