@@ -45,7 +45,7 @@ struct prnn_handle {
   bool rtc = false;
   int t_n_cta = 0, t_R = 0, t_G = 1, t_cpg = 0, t_N = 0, t_ring = 0;
   void* Wimg = nullptr;
-  int wide_loads = 1, bank_aware = 1, staged_order = 0;
+  int wide_loads = 1, bank_aware = 1, staged_order = 2;
   int regw_opt = 1;  // sparse: register-weight build of the kernel where its plan fits
   int depth_opt = 1; // sparse: staging depth matched to the plan (0: always 12)
   size_t onchip_bytes = 0, smem_at_max = 0;
@@ -490,10 +490,12 @@ RecurCommon common_args(const prnn_handle* h, int T, int B, const float* h0, flo
 
 // Plan and pack [H][k] row-padded sparse rows for the persistent kernel:
 // the first plan (fastest by the model) whose packing fits shared memory.
-static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
-                          const std::vector<uint16_t>& hc, SparsePlan* plan,
-                          std::vector<uint32_t>* pk, PackStats* pst,
-                          std::vector<uint32_t>* place) {
+// place: nullptr for column order, else it receives each CTA's staging order
+// (left empty where the layer cannot use one).
+static bool plan_and_pack_order(prnn_t h, int k, const std::vector<uint16_t>& hv,
+                                const std::vector<uint16_t>& hc, SparsePlan* plan,
+                                std::vector<uint32_t>* pk, PackStats* pst,
+                                std::vector<uint32_t>* place) {
   const int H = h->H;
   for (const SparsePlan& cand : plan_sparse(h, k)) {
     // largest entries-per-thread whose weights plus one h column fit in smem
@@ -502,14 +504,50 @@ static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
     const int max_ept = (int)(((h->smem_optin - hs1) / ((size_t)cand.R * cand.tpr * 4)) / 4 * 4);
     *plan = cand;
     plan->ept = pack_sparse_rows(H, k, plan->R, plan->cpg, plan->tpr, hv.data(), hc.data(), *pk,
-                                 pst, max_ept, h->bank_aware != 0,
-                                 h->staged_order ? place : nullptr);
+                                 pst, max_ept, h->bank_aware != 0, place);
     if (plan->ept > 0) {
       plan->kp = plan->ept * plan->tpr;
       return true;
     }
   }
   return false;
+}
+
+// The staging order of a packing: PRNN_OPT_STAGED_ORDER 0 column order, 1 each
+// CTA's bank-balancing order, 2 (default) the order this rule picks from
+// both packings: the staged order when it needs fewer padded entries per row
+// than column order, or when batch passes hold at least 4 columns, rows at
+// least 256 entries and the staged order at most 12 % more.  Fitted to
+// measurements of both orders at every sparse point of the H x B x density
+// sweep: the staged order's scattered staging stores cost more than its
+// conflict-free gathers save unless the gathers dominate the step (wide
+// batch, many entries) or its packing is the tighter one.
+static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
+                          const std::vector<uint16_t>& hc, SparsePlan* plan,
+                          std::vector<uint32_t>* pk, PackStats* pst,
+                          std::vector<uint32_t>* place) {
+  place->clear();
+  if (h->staged_order != 2)
+    return plan_and_pack_order(h, k, hv, hc, plan, pk, pst, h->staged_order ? place : nullptr);
+  const bool okc = plan_and_pack_order(h, k, hv, hc, plan, pk, pst, nullptr);
+  if (!h->bank_aware || !staging_placement_supported(h->H)) return okc;
+  SparsePlan ps{};
+  std::vector<uint32_t> pks, pls;
+  PackStats sts;
+  if (!plan_and_pack_order(h, k, hv, hc, &ps, &pks, &sts, &pls) || pls.empty()) return okc;
+  bool staged = !okc;
+  if (okc) {
+    const int cols = (h->maxB + plan->G - 1) / plan->G;  // batch columns of a group
+    staged = ps.kp < plan->kp ||
+             (cols >= 4 && plan->kp >= 256 && (long long)ps.kp * 100 <= (long long)plan->kp * 112);
+  }
+  if (staged) {
+    *plan = ps;
+    pk->swap(pks);
+    *pst = sts;
+    place->swap(pls);
+  }
+  return true;
 }
 
 // Plan, pack and upload row-padded sparse weights (hv/hc [H][k], each row
@@ -1378,7 +1416,7 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
       h->rtc_opt = (int)value;
       return PRNN_OK;
     case PRNN_OPT_STAGED_ORDER:
-      if (value != 0 && value != 1) return PRNN_ERR_INVALID_ARG;
+      if (value < 0 || value > 2) return PRNN_ERR_INVALID_ARG;
       h->staged_order = (int)value;
       return PRNN_OK;
     case PRNN_OPT_SPARSE_REG_WEIGHTS:

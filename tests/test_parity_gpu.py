@@ -559,14 +559,17 @@ def test_poll_delay_changes_timing_not_results(env, spec):
                                   dict(H=256, B=32, T=6, k=40),
                                   dict(H=300, B=3, T=8, k=17)])
 def test_staged_order_matches_column_order(env, spec):
-    """Each CTA staging h_{t-1} in its own bank-balancing order (opt-in)
-    changes where the gathers read, not what they read: both orders match the
-    oracle, and ragged H (not a multiple of 128) keeps column order."""
+    """Each CTA staging h_{t-1} in its own bank-balancing order changes where
+    the gathers read, not what they read: both orders match the oracle, and
+    ragged H (not a multiple of 128) keeps column order.  At these sizes the
+    automatic choice (the default) is column order."""
     torch, prnn, o = env
     p = synth.make_problem(seed=81, **spec)
     ref = o.forward(p)
     y_on, info_on = run_gpu(env, p, pre_options={prnn.PRNN_OPT_STAGED_ORDER: 1})
-    y_off, info_off = run_gpu(env, p)  # column order is the default
+    y_off, info_off = run_gpu(env, p, pre_options={prnn.PRNN_OPT_STAGED_ORDER: 0})
+    _, info_auto = run_gpu(env, p)
+    assert info_auto["sparse_staged_order"] == 0
     check(y_on, ref, "f16", "staged order")
     check(y_off, ref, "f16", "column order")
     assert info_on["sparse_staged_order"] == (1 if p.H % 128 == 0 else 0)
@@ -580,10 +583,25 @@ def test_staged_order_matches_column_order(env, spec):
     lay = prnn.Layer.from_problem(p)
     try:
         with pytest.raises(prnn.PrnnError) as e:
-            lay.set_option(prnn.PRNN_OPT_STAGED_ORDER, 2)
+            lay.set_option(prnn.PRNN_OPT_STAGED_ORDER, 3)
         assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
     finally:
         lay.close()
+
+
+def test_staged_order_automatic_choice(env):
+    """By default each packing picks its staging order by the measured rule:
+    the staged order for a wide batch of a 25 % layer, column order for the
+    headline layer (B = 4); the chosen forwards match the oracle."""
+    _, prnn, o = env
+    p = synth.make_problem(H=2304, B=32, T=6, k=576, seed=82, h0_std=0.3)
+    y, info = run_gpu(env, p)
+    assert info["sparse_staged_order"] == 1
+    check(y, o.forward(p), "f16", "automatic staging order")
+    q = synth.named_problem("sparse_f16_h1792_d10_b4_t256", T=4)
+    yq, info_q = run_gpu(env, q)
+    assert info_q["sparse_staged_order"] == 0
+    check(yq, o.forward(q), "f16", "automatic staging order, headline")
 
 
 @pytest.mark.parametrize("spec,algo,opts", [
