@@ -503,8 +503,9 @@ def measure_extras(args, p, lay, x, h0, y, flush, stream, dev, world):
     from persistent_rnn_recurrence_gb300 import prnn
     out = {}
     K = max(3, min(args.steps, 10))
-    # end to end from pinned host memory: prnn_forward_host (x and h0 copied in,
-    # y written to the host by the recurrent kernel as it is published), and for
+    # end to end from pinned host memory: prnn_forward_host (x read over the host
+    # link by the projection's staging kernel, h0 copied in, y written to the host
+    # by the recurrent kernel as it is published), and for
     # comparison host copies around prnn_forward on device buffers
     xh = torch.from_numpy(p.x).pin_memory()
     h0h = None if h0 is None else h0.cpu().pin_memory()
