@@ -20,11 +20,14 @@
 // into shared memory by one bulk TMA copy (cp.async.bulk, mbarrier
 // complete_tx), issued one pass ahead into a second buffer, so the copy of
 // pass p+1 overlaps the arithmetic of pass p.  A prefetch can run ahead of a
-// slow producer and bring the "not yet written" pattern, so once a copy has
-// landed every thread scans its share of the staged rows and re-polls the
-// stale float4s with relaxed loads (bounded), all of them together.  Results
-// are published in y exactly as by the other persistent kernels (flag in the
-// data).
+// slow producer and bring the "not yet written" pattern.  With three or more
+// passes a step the copy is issued long after its rows were published and is
+// nearly always clean: the arithmetic runs at once, and a NaN in any thread's
+// accumulators sends the whole CTA back to scan its staged rows, re-poll the
+// stale float4s with relaxed loads (bounded, all of them together) and
+// compute the pass again.  With two passes the copy is nearly always stale,
+// so the scan and re-poll come before the arithmetic.  Results are published
+// in y exactly as by the other persistent kernels (flag in the data).
 #include "persistent_common.cuh"
 #include "tc_common.cuh"
 
