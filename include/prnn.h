@@ -78,8 +78,9 @@ typedef enum {
                                      takes effect at the next set_weights call                 */
   PRNN_OPT_POLL_DELAY_NS = 9,     /* persistent: pause after publishing a step before the first
                                      poll of the next, ns, 0 .. 10000 (default: dense 100, or
-                                     200 when a step is one batch pass polling more than 16 KiB
-                                     of h per CTA; stacked 100; sparse 0, or 100 for H > 4096)  */
+                                     200 when a step is one batch pass of one column or polling
+                                     more than 16 KiB of h per CTA; stacked 100; sparse 0, or
+                                     100 for H > 4096)                                          */
   PRNN_OPT_POLL_BACKOFF_NS = 10,  /* persistent: pause before re-polling stale step data, ns,
                                      doubling per round up to 4x; 0 .. 10000 (default: 0, and
                                      250 for stacks)                                            */

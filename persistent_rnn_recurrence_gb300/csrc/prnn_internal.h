@@ -64,9 +64,12 @@ constexpr int kDenseDelayNs = 100;
 // columns of B = 4 in one pass (one CTA group), H=1792 runs 4.4-7.5 us/step at
 // 100 ns and 2.4 at 200 ns, H=2048 6.0-7.0 and 2.4 (about 10 at 0 ns for H =
 // 1536 .. 2048).  With several passes the first pass reads data published
-// passes earlier, and 200 ns only costs 1-2 %.
+// passes earlier, and 200 ns only costs 1-2 %.  A single-column pass (B = 1)
+// is bimodal at 100 ns too (H=1152: 1.1 or 2.1 us/step from run to run,
+// H=4096: 3.5-5.5) and steady at 200 (1.17, 3.7; H=2304 1.76 against a
+// 1.68 median with a 2.1 tail).
 __host__ __device__ constexpr int dense_delay_ns(int H, int bw, int passes) {
-  return passes == 1 && (long long)bw * H * 4 > 16384 ? 200 : kDenseDelayNs;
+  return passes == 1 && (bw == 1 || (long long)bw * H * 4 > 16384) ? 200 : kDenseDelayNs;
 }
 __host__ __device__ constexpr int sparse_delay_ns(int H) { return H > 4096 ? 100 : 0; }
 // Default first pause (ns) before re-polling stale step data (Waiter::pause):
