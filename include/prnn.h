@@ -92,12 +92,12 @@ typedef enum {
   PRNN_OPT_STAGED_ORDER = 12,     /* sparse, bank-aware, H % 128 == 0: 1 = each CTA stages h in
                                      its own bank-balancing order (one lane per bank in every
                                      gather slot, at the cost of scattered staging stores);
-                                     0 = column order; 2 = chosen per packing (default): the
-                                     staged order when it packs rows tighter than column order,
-                                     or when batch passes hold >= 4 columns, rows >= 256
-                                     entries and it packs at most 12 % looser (measured: it
-                                     wins at wide batch and many entries, loses at B <= 4 and
-                                     at 1 % density).  Applies to Wh and to the backward's Wh^T
+                                     0 = column order; 2 = chosen per packing (default): with
+                                     batch passes of >= 4 columns, the staged order when it
+                                     packs rows tighter than column order, or when rows hold
+                                     >= 256 entries and it packs at most 12 % looser (measured:
+                                     it wins at wide batch and many entries, loses at B <= 4
+                                     and at 1 % density).  Applies to Wh and to the backward's Wh^T
                                      alike; takes effect at the next set_weights call          */
   PRNN_OPT_SPARSE_REG_WEIGHTS = 13,/* sparse persistent: 1 = the register-weight build of the
                                      kernel (launch bound 384 threads, each thread's first 24

@@ -515,13 +515,15 @@ static bool plan_and_pack_order(prnn_t h, int k, const std::vector<uint16_t>& hv
 
 // The staging order of a packing: PRNN_OPT_STAGED_ORDER 0 column order, 1 each
 // CTA's bank-balancing order, 2 (default) the order this rule picks from
-// both packings: the staged order when it needs fewer padded entries per row
-// than column order, or when batch passes hold at least 4 columns, rows at
-// least 256 entries and the staged order at most 12 % more.  Fitted to
+// both packings: with batch passes of at least 4 columns, the staged order
+// when it needs fewer padded entries per row than column order, or when rows
+// hold at least 256 entries and it needs at most 12 % more.  Fitted to
 // measurements of both orders at every sparse point of the H x B x density
-// sweep: the staged order's scattered staging stores cost more than its
-// conflict-free gathers save unless the gathers dominate the step (wide
-// batch, many entries) or its packing is the tighter one.
+// sweep and the named layers: the staged order's scattered staging stores
+// cost more than its conflict-free gathers save unless the gathers dominate
+// the step (wide batch, many entries); with one or two columns a pass it
+// loses even where it packs tighter (H=5760 5 %, B=4: 4.10 against 3.40 us
+// per step).
 static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
                           const std::vector<uint16_t>& hc, SparsePlan* plan,
                           std::vector<uint32_t>* pk, PackStats* pst,
@@ -538,8 +540,8 @@ static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
   bool staged = !okc;
   if (okc) {
     const int cols = (h->maxB + plan->G - 1) / plan->G;  // batch columns of a group
-    staged = ps.kp < plan->kp ||
-             (cols >= 4 && plan->kp >= 256 && (long long)ps.kp * 100 <= (long long)plan->kp * 112);
+    staged = cols >= 4 && (ps.kp < plan->kp || (plan->kp >= 256 && (long long)ps.kp * 100 <=
+                                                                        (long long)plan->kp * 112));
   }
   if (staged) {
     *plan = ps;

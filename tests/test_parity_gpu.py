@@ -602,6 +602,14 @@ def test_staged_order_automatic_choice(env):
     yq, info_q = run_gpu(env, q)
     assert info_q["sparse_staged_order"] == 0
     check(yq, o.forward(q), "f16", "automatic staging order, headline")
+    # every named sparse layer (B = 4: one column a pass) keeps column order,
+    # including H=5760 5 %, where the staged order packs tighter yet is slower
+    for name in [n for n in synth.NAMED if n.startswith("sparse")]:
+        lay = prnn.Layer.from_problem(synth.named_problem(name, T=1))
+        try:
+            assert lay.info()["sparse_staged_order"] == 0, name
+        finally:
+            lay.close()
 
 
 @pytest.mark.parametrize("spec,algo,opts", [
