@@ -59,15 +59,15 @@ constexpr long long kWaitNs = 200LL * 1000 * 1000;                   // 200 ms p
 // Per tile width: B tile bytes, stage bytes (a multiple of 1024, so every
 // tile of the ring stays 1024-byte aligned for the 128-byte swizzle), TMEM
 // columns (a power of two >= 32 holding the BN fp32 accumulator columns).
-template <int BN>
+// ST: the ring's depth, chosen per launch (see launch_tc).
+template <int BN, int ST>
 struct TileCfg {
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 128, "tile width");
+  static_assert(ST >= 2 && ST <= 8, "ring depth");
   static constexpr uint32_t kTileB = BN * BK * 2;
   static constexpr uint32_t kStageBytes = kTileA + kTileB;
   static constexpr uint32_t kTmemCols = BN <= 64 ? 64 : 128;
-  // a 4-stage ring: 7 or 8 stages (as many as shared memory holds) measured
-  // slower, at M = 1024 (+2 us) and M = 8192 (1.7x the GEMM time)
-  static constexpr int kStages = 4;
+  static constexpr int kStages = ST;
   static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;  // + alignment slack
 };
 
@@ -101,14 +101,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 
-template <int BN>
+template <int BN, int ST>
 __global__ void __launch_bounds__(kThreads, 1)
     proj_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcKernelArgs a) {
-  constexpr uint32_t kTileB = TileCfg<BN>::kTileB;
-  constexpr uint32_t kStageBytes = TileCfg<BN>::kStageBytes;
-  constexpr uint32_t kTmemCols = TileCfg<BN>::kTmemCols;
-  constexpr int kStages = TileCfg<BN>::kStages;
+  constexpr uint32_t kTileB = TileCfg<BN, ST>::kTileB;
+  constexpr uint32_t kStageBytes = TileCfg<BN, ST>::kStageBytes;
+  constexpr uint32_t kTmemCols = TileCfg<BN, ST>::kTmemCols;
+  constexpr int kStages = TileCfg<BN, ST>::kStages;
   (void)kTileB;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -409,11 +409,15 @@ namespace {
 
 // Tile width for an M x N product: the fewest waves of one CTA per SM, each
 // wave costing in proportion to the tile's width (its MMAs and loads).
-int pick_bn(int M, int N) {
+int sm_count() {
   int sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     sms = 1;
+  return sms;
+}
+
+int pick_bn(int M, int N, int sms) {
   int best = 128;
   long long best_cost = -1;
   for (int bn : {128, 96, 64}) {
@@ -429,27 +433,27 @@ int pick_bn(int M, int N) {
 
 // after_producer: launch as the programmatic dependent of the kernel before
 // it on the stream (that kernel must not write B, P or the y fill)
-template <int BN>
+template <int BN, int ST>
 cudaError_t launch_tc_bn(const CUtensorMap& tmA, const CUtensorMap& tmC, const void* Bp, int Kp,
                          int N, bool bf16, const TcKernelArgs& ka, bool after_producer,
                          cudaStream_t s) {
   CUtensorMap tmB;
   if (!encode_kmajor(&tmB, Bp, Kp, N, BN, bf16)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel<BN>,
+  cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel<BN, ST>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)TileCfg<BN>::kSmemBytes);
+                                       (int)TileCfg<BN, ST>::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((ka.N + BN - 1) / BN, (ka.M + BM - 1) / BM);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
+  cfg.dynamicSmemBytes = TileCfg<BN, ST>::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = after_producer ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, proj_tc_kernel<BN>, tmA, tmB, tmC, ka);
+  return cudaLaunchKernelEx(&cfg, proj_tc_kernel<BN, ST>, tmA, tmB, tmC, ka);
 }
 
 cudaError_t launch_tc(const void* A, const void* B, int M, int N, int Kp, bool bf16,
@@ -460,12 +464,27 @@ cudaError_t launch_tc(const void* A, const void* B, int M, int N, int Kp, bool b
   // stores (tmC is then unused: any valid map stands in)
   ka.tma_out = kTmaStoreEpilogue && encode_out(&tmC, ka.P, N, M) ? 1 : 0;
   if (!ka.tma_out) tmC = tmA;
-  const int bn = pick_bn(M, N);
+  const int sms = sm_count();
+  const int bn = pick_bn(M, N, sms);
   ka.idesc = bf16 ? bf16_idesc(BM, bn) : f16_idesc(BM, bn);
+  // The ring's depth. With more tiles than SMs a 3-stage ring (97-113 KB)
+  // lets two CTAs share an SM, so one CTA's epilogue and prologue hide
+  // behind the other's main loop: at M = 8192, K = 4096 the GEMM took 245 us
+  // against 303 us with 4 stages (and 566 us with 6). Within one wave the
+  // second CTA slot has no tile to run, and 4 stages measured faster there
+  // (16.0 against 18.0 us at M = 1024, K = 1792).
+  const long long tiles = (long long)((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  const bool multi_wave = tiles > sms;
   switch (bn) {
-    case 64: return launch_tc_bn<64>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s);
-    case 96: return launch_tc_bn<96>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s);
-    default: return launch_tc_bn<128>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s);
+    case 64:
+      return multi_wave ? launch_tc_bn<64, 3>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s)
+                        : launch_tc_bn<64, 4>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s);
+    case 96:
+      return multi_wave ? launch_tc_bn<96, 3>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s)
+                        : launch_tc_bn<96, 4>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s);
+    default:
+      return multi_wave ? launch_tc_bn<128, 3>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s)
+                        : launch_tc_bn<128, 4>(tmA, tmC, B, Kp, N, bf16, ka, after_producer, s);
   }
 }
 
