@@ -109,7 +109,7 @@ typedef enum {
                                      flight per thread (2 or 6) that cover the thread's share of
                                      a pass in one round (default); 0 = always 12.  The sync
                                      floor probe follows the same choice                       */
-  PRNN_OPT_DENSE_WIDE = 15        /* dense fp16 persistent, flags in the data, H % 128 == 0 and
+  PRNN_OPT_DENSE_WIDE = 15,       /* dense fp16 persistent, flags in the data, H % 128 == 0 and
                                      H / 16 CTAs fit: the wide-batch kernel (CTAs of 8 or 16
                                      rows, passes of 8 batch columns staged by bulk copies a
                                      pass ahead) for forwards of B >= 16.  1 = where it
@@ -117,6 +117,17 @@ typedef enum {
                                      H >= 1024, or B >= 16 with H >= 2048 (default); 2 = for
                                      every B >= 16; 0 = never.  Takes effect at the next
                                      forward                                                    */
+  PRNN_OPT_DENSE_KSPLIT = 16      /* dense fp16 persistent, flags in the data, H % 128 == 0 and
+                                     all H / 128 clusters of 2 .. 8 CTAs resident at once, one
+                                     CTA per SM (on 152 SMs: clusters of 8 up to H = 1920, of
+                                     6 up to 2304): the tensor-core kernel that splits each
+                                     step's product over K inside clusters (h split into fp16
+                                     hi + lo parts, about 22 bits; partial sums reduced through
+                                     distributed shared memory) for forwards of B <= 32.
+                                     1 = for B >= 16 (default); 2 = for every B <= 32; 0 =
+                                     never.  Its weight image is built at set_weights when
+                                     max_batch >= 16 or the option is 2; it takes precedence
+                                     over PRNN_OPT_DENSE_WIDE                                  */
 } prnn_option_t;
 
 /* Plan and sizes chosen at create / set_weights time (read-only report). */
@@ -139,6 +150,11 @@ typedef struct {
   int dense_wide_batch;            /* dense: 1 if the forward at max_batch runs the
                                       wide-batch kernel (PRNN_OPT_DENSE_WIDE); the plan
                                       fields above then describe that kernel's launch       */
+  int dense_ksplit;                /* dense: if the forward at max_batch runs the
+                                      tensor-core K-split kernel (PRNN_OPT_DENSE_KSPLIT),
+                                      its cluster size (2 .. 8), else 0; the plan fields
+                                      above then describe its launch (rows_per_cta: the
+                                      128 rows of a cluster)                                */
 } prnn_info_t;
 
 /*

@@ -40,6 +40,12 @@ struct prnn_handle {
   size_t w_smem = 0;
   void* Wpk_wide = nullptr;
   float* zeros = nullptr;
+  // dense fp16 for wide batches on the tensor cores, K split in clusters:
+  // its plan and weight image
+  int ks_opt = 1;
+  bool ks = false;
+  int ks_cs = 0, ks_nat = 0;
+  void* Wimg_ks = nullptr;
   // tensor-core dense recurrence (wide batch): its own plan and weight image
   int rtc_opt = 1;  // the tensor-core recurrence is opt-in (slower than the CUDA cores so far)
   bool rtc = false;
@@ -448,6 +454,7 @@ void free_weights(prnn_handle* h) {
   free_dev(h->Wimg);
   h->rtc = false;
   free_dev(h->Wpk_wide);
+  free_dev(h->Wimg_ks);
   free_dev(h->zeros);
   h->wide = false;
   free_dev(h->cols_pad);
@@ -835,6 +842,39 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
       h->w_depth = wD;
       h->w_smem = wsm;
     }
+    // wide batches on the tensor cores: per CTA (cluster-major, then K slice
+    // j) nat atoms of 128 rows x 64 columns, 16-byte chunk q of row m at
+    // q ^ (m & 7) (the 128-byte swizzle of the K-major MMA operand)
+    const int kcs = h->wdtype == PRNN_F16 && (h->maxB >= kKsplitMinB || h->ks_opt == 2)
+                        ? recur_dense_ksplit_plan(H)
+                        : 0;
+    if (kcs > 0) {
+      const int nblk = H / 128, knat = ksplit_nat(H, kcs);
+      const uint16_t* w16 = reinterpret_cast<const uint16_t*>(wh.data());
+      std::vector<uint16_t> img((size_t)nblk * kcs * knat * 128 * 64, 0);
+      for (int bk = 0; bk < nblk; ++bk)
+        for (int j = 0; j < kcs; ++j) {
+          const int k0 = ksplit_k0(H, kcs, j), kl = ksplit_kl(H, kcs, j);
+          for (int at = 0; at < knat; ++at)
+            for (int m = 0; m < 128; ++m)
+              for (int q = 0; q < 8; ++q)
+                for (int e = 0; e < 8; ++e) {
+                  const int kcol = at * 64 + q * 8 + e;  // column within the slice
+                  if (kcol >= kl) continue;
+                  const size_t atom = ((size_t)bk * kcs + j) * knat + at;
+                  img[atom * 128 * 64 + (size_t)m * 64 + ((q ^ (m & 7)) * 8) + e] =
+                      w16[(size_t)(bk * 128 + m) * H + k0 + kcol];
+                }
+        }
+      PRNN_TRY(upload(&h->Wimg_ks, img.data(), img.size() * 2));
+      if (!h->zeros) {
+        std::vector<float> z((size_t)h->maxB * H, 0.f);
+        PRNN_TRY(upload(&h->zeros, z.data(), z.size() * sizeof(float)));
+      }
+      h->ks = true;
+      h->ks_cs = kcs;
+      h->ks_nat = knat;
+    }
     h->n_cta = plan.n_cta;
     h->R = plan.R;
     h->G = plan.G;
@@ -968,6 +1008,15 @@ static bool dense_wide_for(const prnn_t h, int B) {
   return h->wide_opt == 2 || (passes >= 3 ? h->H >= 1024 : h->H >= 2048);
 }
 
+// Whether a dense persistent forward of B columns runs the tensor-core
+// K-split kernel: planned at set_weights, enabled, flags in the data, B <= 32.
+static bool dense_ksplit_for(const prnn_t h, int B) {
+  if (h->algo != PRNN_ALGO_PERSISTENT || h->sparse || !h->ks || h->ks_opt == 0 ||
+      h->sync_mode != 0 || h->rtc || B < 1 || B > kKsplitMaxB)
+    return false;
+  return h->ks_opt == 2 || B >= kKsplitMinB;
+}
+
 // Whether the recurrent kernel prnn_forward would launch can also write every
 // output into a second buffer (the persistent CUDA-core kernels can).
 static bool recurrence_mirrors(const prnn_t h) {
@@ -1040,6 +1089,16 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
       a.nslices = h->H / 64;
       a.nring = h->t_ring;
       PRNN_TRY(launch_recur_dense_tc(a, s));
+    } else if (dense_ksplit_for(h, B)) {
+      c.n_cta = h->H / 128 * h->ks_cs;
+      c.R = 128;
+      c.cpg = c.n_cta;
+      c.G = 1;
+      c.nthreads = 256;
+      c.smem = recur_dense_ksplit_smem(h->ks_nat, B, h->ks_cs);
+      if (h->poll_delay_ns < 0) c.poll_delay = 0;  // measured: no pause is fastest here
+      DenseSplitArgs a{c, h->Wimg_ks, h0 ? h0 : h->zeros, h->ks_cs, h->ks_nat};
+      PRNN_TRY(launch_recur_dense_ksplit(a, s));
     } else if (dense_wide_for(h, B)) {
       c.R = h->w_R;
       c.cpg = (h->H + h->w_R - 1) / h->w_R;
@@ -1433,6 +1492,10 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
       if (value < 0 || value > 2) return PRNN_ERR_INVALID_ARG;
       h->wide_opt = (int)value;
       return PRNN_OK;
+    case PRNN_OPT_DENSE_KSPLIT:
+      if (value < 0 || value > 2) return PRNN_ERR_INVALID_ARG;
+      h->ks_opt = (int)value;
+      return PRNN_OK;
   }
   return PRNN_ERR_INVALID_ARG;
 }
@@ -1472,7 +1535,14 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
             ? 1
             : 0;
   }
-  if (h->weights_set && dense_wide_for(h, h->maxB)) {
+  if (h->weights_set && dense_ksplit_for(h, h->maxB)) {
+    info->dense_ksplit = h->ks_cs;
+    info->n_cta = h->H / 128 * h->ks_cs;
+    info->rows_per_cta = 128;
+    info->threads_per_cta = 256;
+    info->cta_groups = 1;
+    info->smem_bytes = recur_dense_ksplit_smem(h->ks_nat, h->maxB, h->ks_cs);
+  } else if (h->weights_set && dense_wide_for(h, h->maxB)) {
     info->dense_wide_batch = 1;
     info->n_cta = (h->H + h->w_R - 1) / h->w_R;
     info->rows_per_cta = h->w_R;

@@ -1,0 +1,516 @@
+// persistent_dense_ksplit.cu -- the persistent dense recurrence for wide
+// batches (fp16 weights, up to 32 batch columns) on the tcgen05 tensor cores,
+// with each step's product split over K inside thread-block clusters.
+//
+// At B = 16-32 a step is a small matrix product s = Wh h_{t-1} (H x H by
+// H x B).  On CUDA cores it is bound by instruction issue (the FMAs plus the
+// fp16 conversions and shared loads that feed them).  On the tensor cores a
+// tcgen05.mma with M = 128 and N <= 128 costs about the same whatever N is,
+// so the count of MMAs per SM sets the time: a CTA that owned 128 rows for all
+// of K would issue H / 16 of them in a chain.  Here each of the H / 128 row
+// blocks gets a cluster of CS CTAs (CS <= 8, the largest for which all the
+// clusters are resident at once), and CTA j of a cluster multiplies the
+// block's rows by K slice j only: about H / (16 CS) MMAs of K = 16.
+//
+// Per step, in CTA j of a cluster:
+//  1. all threads poll h_{t-1}[b][K slice j] for the batch columns (flag in
+//     the data, relaxed loads, bounded) and split each fp32 value into
+//     hi = fp16(h) and lo = fp16(h - hi), so hi + lo carries about 22 bits of
+//     h; the two go side by side into the B operand: rows 0 .. BP-1 hold hi,
+//     rows BP .. 2BP-1 lo (BP = the batch padded to 8, 16 or 32; N = 2 BP),
+//     so one MMA per K step multiplies both;
+//  2. one thread issues the slice's MMAs (M = 128 rows of Wh, kept in shared
+//     memory for the whole sequence as the A operand) into a TMEM accumulator
+//     [128 lanes x N columns];
+//  3. four warps read the accumulator back (lane = row), add the hi and lo
+//     columns and stage the partial sums column by column; CTA o of the
+//     cluster owns batch columns [o B / CS, (o + 1) B / CS), and one thread
+//     sends each owner its columns with a bulk copy into the owner's shared
+//     memory (cp.async.bulk shared::cta -> shared::cluster, completing on
+//     the owner's mbarrier);
+//  4. the owner waits for the CS - 1 blocks, sums the CS partials and P_t,
+//     applies ReLU and publishes its columns of the block's 128 rows of h_t
+//     into y, as the other persistent kernels do.
+// The exchange of h between clusters stays the flag-in-data L2 broadcast;
+// only the K reduction runs through distributed shared memory.
+//
+// h is fp32 in y.  A value of 2^15 or more would overflow the fp16 split: a
+// step whose slice holds one is scaled by a power of two first (exact), and
+// the partial sums are scaled back.  Every wait is bounded: on a timeout the
+// CTA records the status; all CTAs leave the step loop together (the
+// decisions are taken at CTA barriers), wait for their MMAs, free TMEM and
+// meet their cluster peers once more before leaving, so no bulk copy targets
+// the shared memory of a CTA that has left.
+#include "persistent_common.cuh"
+#include "tc_common.cuh"
+
+namespace prnn {
+
+using namespace pk;
+using namespace tc;
+
+namespace {
+
+constexpr int kSplitThreads = 256;     // 8 warps; warps 4..7 read TMEM lanes 0..127
+constexpr int kSplitPollMax = 12;      // float4 polls a thread keeps in flight
+constexpr uint32_t kAtomA = 128 * 128;  // bytes of one A atom: 128 rows x 64 fp16
+constexpr int kSplitTmemCols = 64;     // N <= 64
+constexpr float kSplitLarge = 32768.f; // |h| from here on would overflow the fp16 split
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared-memory location in CTA `rank`
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// bulk copy of `bytes` from this CTA's shared memory into a peer's, completing
+// transaction bytes on the peer's mbarrier (both given as shared::cluster
+// addresses)
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for an mbarrier phase.  The timer is read only once the phase
+// is not complete at the first test; the wait also ends when another CTA has
+// recorded a failure.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, long long limit_ns,
+                                           const int* status) {
+  if (try_wait_cluster(bar, parity)) return true;
+  const uint64_t deadline = global_ns() + (uint64_t)limit_ns;
+  uint32_t n = 0;
+  while (!try_wait_cluster(bar, parity)) {
+    if ((++n & 255u) == 0u && (global_ns() > deadline || ld_relaxed_i(status) != 0)) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// 2^e for |e| < 127, exactly
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// Split four values (scaled by `scale`, a power of two) into their fp16 hi
+// and lo parts and store them into the B operand: column b, K index k (a
+// multiple of 4) of the slice.  Row n of an atom holds 128 bytes, its 16-byte
+// chunk q at q ^ (n & 7); hi goes to row b, lo to row BP + b.
+template <int BP>
+__device__ __forceinline__ void store_split(unsigned char* gB, uint32_t atom_bytes, float4 v,
+                                            float scale, int b, int k) {
+  const float x[4] = {v.x * scale, v.y * scale, v.z * scale, v.w * scale};
+  float hi[4], lo[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half h = __float2half_rn(x[i]);
+    hi[i] = __half2float(h);
+    lo[i] = x[i] - hi[i];
+  }
+  const int a = k >> 6, kk = k & 63;
+  const uint32_t off = (uint32_t)((((kk >> 3) ^ (b & 7)) << 4) + ((kk & 7) << 1));
+  unsigned char* atom = gB + (size_t)a * atom_bytes;
+  *reinterpret_cast<uint2*>(atom + b * 128 + off) =
+      make_uint2(pack_half2(hi[0], hi[1]), pack_half2(hi[2], hi[3]));
+  *reinterpret_cast<uint2*>(atom + (BP + b) * 128 + off) =
+      make_uint2(pack_half2(lo[0], lo[1]), pack_half2(lo[2], lo[3]));
+}
+
+template <int BP>
+__global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(const DenseSplitArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t mma_bar;
+  __shared__ __align__(8) uint64_t recv_bar[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_large[2];
+  __shared__ float s_red[kSplitThreads / 32];
+
+  constexpr int N = 2 * BP;
+  constexpr uint32_t kAtomB = (uint32_t)N * 128;  // bytes of one B atom: N rows x 64 fp16
+  const RecurCommon& c = a.c;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = c.H, B = c.B, T = c.T, cs = a.cs, nat = a.nat;
+  const int j = (int)cluster_rank();                  // K slice of this CTA
+  const int row0 = blockIdx.x / cs * 128;            // the cluster's row block
+  const int k0 = ksplit_k0(H, cs, j), kl = ksplit_kl(H, cs, j);
+  const int cb0 = j * B / cs, ncol = (j + 1) * B / cs - cb0;  // the batch columns it finalizes
+  const int maxcol = (B + cs - 1) / cs;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - smem_u32(smem_raw));
+  const uint32_t sA = base;
+  const uint32_t sB = sA + (uint32_t)nat * kAtomA;
+  unsigned char* gB = gbase + (size_t)nat * kAtomA;
+  // partial sums out, [2][B][128] (column b of the block: 128 rows), and in,
+  // [2][cs][maxcol][128] (slot i: CTA i's partials of this CTA's columns)
+  float* stage = reinterpret_cast<float*>(gB + (size_t)nat * kAtomB);
+  float* recv = stage + 2 * B * 128;
+  const uint32_t in_bytes = (uint32_t)(cs - 1) * (uint32_t)ncol * 512u;
+
+  // Wh rows of the block x K slice (the A operand, for the whole sequence);
+  // the B operand zeroed: its rows past the batch stay zero
+  {
+    const uint4* src =
+        reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.Wimg) +
+                                       (size_t)blockIdx.x * nat * kAtomA);
+    uint4* dst = reinterpret_cast<uint4*>(gbase);
+    const int na = nat * (int)kAtomA / 16;
+    for (int i = tid; i < na; i += kSplitThreads) dst[i] = __ldg(src + i);
+    uint4* bz = reinterpret_cast<uint4*>(gB);
+    for (int i = tid; i < nat * (int)kAtomB / 16; i += kSplitThreads) bz[i] = make_uint4(0, 0, 0, 0);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (tid == 0) {
+    mbar_init(&mma_bar, 1);
+    mbar_init(&recv_bar[0], 1);
+    mbar_init(&recv_bar[1], 1);
+    s_large[0] = s_large[1] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the partial blocks of steps 0 and 1 (cs - 1 peers x ncol columns)
+    if (T > 0) mbar_arrive_expect_tx(&recv_bar[0], in_bytes);
+    if (T > 1) mbar_arrive_expect_tx(&recv_bar[1], in_bytes);
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&s_tmem)),
+                 "r"(kSplitTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = s_tmem;
+  cluster_sync_all();  // every peer's mbarriers exist before the first copy
+
+  const uint32_t idesc = f16_idesc(128, N);
+  const int q4 = kl >> 2;  // float4 per batch column of the slice
+  const int nf4 = B * q4;
+  const int nout = ncol * 128;  // outputs this CTA finalizes: column cb0 + o / 128, row o % 128
+  Waiter w;
+  w.status = c.status;
+  w.timeout_ns = c.timeout_ns;
+  w.backoff = c.poll_backoff;
+  constexpr int kOutMax = (kKsplitMaxB + 1) / 2 * 128 / kSplitThreads;  // cs >= 2
+  float pn[kOutMax];  // projection values of the next step's outputs
+  auto load_p = [&](int t) {
+#pragma unroll
+    for (int u = 0; u < kOutMax; ++u) {
+      const int o = tid + u * kSplitThreads;
+      pn[u] = o < nout ? ld_nc_pinned(c.P + ((size_t)t * B + cb0 + (o >> 7)) * H + row0 + (o & 127))
+                       : 0.f;
+    }
+  };
+  if (T > 0) load_p(0);
+  bool bad = false;       // this thread saw a failed wait
+  bool aborted = false;   // uniform: the CTA left the step loop early
+  int last_mma = -1;      // thread 0: the last step whose MMAs it issued
+  for (int t = 0; t < T; ++t) {
+    const int par = t & 1;
+    w.new_step();
+    float pv[kOutMax];
+#pragma unroll
+    for (int u = 0; u < kOutMax; ++u) pv[u] = pn[u];
+    if (t + 1 < T) load_p(t + 1);
+    // ---- 1. h_{t-1} of the slice -> hi / lo fp16 in the B operand ----
+    const float* src = (t == 0 ? a.h0_rows : c.y + (size_t)(t - 1) * B * H) + k0;
+    const bool poll = t > 0;
+    if (poll) spin_cycles(c.poll_delay);
+    bool large = false;
+    for (int i0 = tid; i0 < nf4 && !bad; i0 += kSplitPollMax * kSplitThreads) {
+      float4 v[kSplitPollMax];
+#pragma unroll
+      for (int u = 0; u < kSplitPollMax; ++u) {
+        const int i = i0 + u * kSplitThreads;
+        if (i < nf4) {
+          const float* p = src + (size_t)(i / q4) * H + 4 * (i % q4);
+          v[u] = poll ? ld_relaxed_f4(p) : __ldg(reinterpret_cast<const float4*>(p));
+        }
+      }
+      // each float4 is split and stored as soon as it is fresh, so the
+      // conversions of early data overlap the wait for late data
+      unsigned pending = 0;
+#pragma unroll
+      for (int u = 0; u < kSplitPollMax; ++u)
+        if (i0 + u * kSplitThreads < nf4) pending |= 1u << u;
+      uint32_t spins = 0, round = 0;
+      for (;;) {
+#pragma unroll
+        for (int u = 0; u < kSplitPollMax; ++u)
+          if (((pending >> u) & 1u) && (!poll || ready4(v[u]))) {  // h0 is not polled
+            const int i = i0 + u * kSplitThreads;
+            large |= !(fabsf(v[u].x) < kSplitLarge) | !(fabsf(v[u].y) < kSplitLarge) |
+                     !(fabsf(v[u].z) < kSplitLarge) | !(fabsf(v[u].w) < kSplitLarge);
+            store_split<BP>(gB, kAtomB, v[u], 1.f, i / q4, 4 * (i % q4));
+            pending &= ~(1u << u);
+          }
+        if (pending == 0u) break;
+        if (!w.still_ok(spins)) {
+          report_timeout(c.status, t, blockIdx.x);
+          bad = true;
+          break;
+        }
+        w.pause(round);
+#pragma unroll
+        for (int u = 0; u < kSplitPollMax; ++u)
+          if ((pending >> u) & 1u) {
+            const int i = i0 + u * kSplitThreads;
+            v[u] = ld_relaxed_f4(src + (size_t)(i / q4) * H + 4 * (i % q4));
+          }
+      }
+      if (bad) break;
+    }
+    if (large) s_large[par] = 1;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (__syncthreads_or(bad)) {
+      aborted = true;
+      break;
+    }
+    // a value too large for the fp16 split (rare): scale the slice by 2^-e
+    int e = 0;
+    if (s_large[par]) {
+      float m = 0.f;
+      for (int i = tid; i < nf4; i += kSplitThreads) {
+        const float* q = src + (size_t)(i / q4) * H + 4 * (i % q4);
+        const float4 v = poll ? ld_relaxed_f4(q) : __ldg(reinterpret_cast<const float4*>(q));
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) s_red[warp] = m;
+      __syncthreads();
+      m = 0.f;
+#pragma unroll
+      for (int k = 0; k < kSplitThreads / 32; ++k) m = fmaxf(m, s_red[k]);
+      // m * 2^-e < 2^15; an infinite value is left as it is
+      if (m >= kSplitLarge && m <= 3.0e38f) e = ilogbf(m) - 14;
+      const float scale = pow2i(-e);
+      for (int i = tid; i < nf4; i += kSplitThreads) {
+        const float* q = src + (size_t)(i / q4) * H + 4 * (i % q4);
+        const float4 v = poll ? ld_relaxed_f4(q) : __ldg(reinterpret_cast<const float4*>(q));
+        store_split<BP>(gB, kAtomB, v, scale, i / q4, 4 * (i % q4));
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncthreads();
+    }
+    // ---- 2. the block's partial product over the slice: kl / 16 MMAs ----
+    if (tid == 0) {
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int nks = kl >> 4;
+      // K advances by 16 fp16 = 32 bytes inside the 128-byte swizzle atom:
+      // the descriptors' start-address fields (bytes / 16) step by 2 within
+      // an atom and by the atom size between atoms
+      const uint64_t ad0 = sw128_kmajor_desc(sA), bd0 = sw128_kmajor_desc(sB);
+      for (int ks = 0; ks < nks; ++ks) {
+        const uint32_t at = (uint32_t)(ks >> 2), s4 = (uint32_t)(ks & 3);
+        umma_f16(tmem, ad0 + ((at * kAtomA + s4 * 32u) >> 4), bd0 + ((at * kAtomB + s4 * 32u) >> 4),
+                 idesc, ks > 0 ? 1u : 0u);
+      }
+      umma_commit(&mma_bar);
+      last_mma = t;
+    }
+    // ---- 3. warps 4..7: accumulator -> partial sums by column -> owners ----
+    if (warp >= 4) {
+      const int wq = warp - 4;  // TMEM lanes (block rows) 32 wq .. 32 wq + 31
+      if (!wait_phase(&mma_bar, (uint32_t)t & 1u, c.timeout_ns, c.status)) {
+        report_timeout(c.status, t, blockIdx.x);
+        bad = true;
+      }
+      // the TMEM loads below are warp-wide: one decision per warp
+      bad = __any_sync(0xffffffffu, bad);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      float* dst = stage + (size_t)par * B * 128 + wq * 32 + lane;  // row wq * 32 + lane
+      if (!bad) {
+        uint32_t v[32];
+        tmem_load_32cols(tmem + ((uint32_t)(wq * 32) << 16), v);
+        const float unscale = pow2i(e);
+        if constexpr (BP == 32) {
+          uint32_t u[32];
+          tmem_load_32cols(tmem + ((uint32_t)(wq * 32) << 16) + 32u, u);
+#pragma unroll
+          for (int b = 0; b < BP; ++b)
+            if (b < B) dst[b * 128] = (__uint_as_float(v[b]) + __uint_as_float(u[b])) * unscale;
+        } else {
+#pragma unroll
+          for (int b = 0; b < BP; ++b)
+            if (b < B) dst[b * 128] = (__uint_as_float(v[b]) + __uint_as_float(v[BP + b])) * unscale;
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      // lane o of warp 4 sends owner o its columns
+      if (warp == 4 && lane < cs && lane != j && !bad) {
+        const int o = lane, ob = o * B / cs, on = (o + 1) * B / cs - ob;
+        if (on > 0)
+          bulk_to_peer(peer_addr(smem_u32(recv + ((size_t)par * cs + j) * maxcol * 128), (uint32_t)o),
+                       smem_u32(stage + ((size_t)par * B + ob) * 128), (uint32_t)on * 512u,
+                       peer_addr(smem_u32(&recv_bar[par]), (uint32_t)o));
+      }
+    }
+    if (__syncthreads_or(bad)) {
+      aborted = true;
+      break;
+    }
+    // ---- 4. owner: cs partials + P_t -> ReLU -> h_t ----
+    if (!wait_phase(&recv_bar[par], (uint32_t)(t >> 1) & 1u, c.timeout_ns, c.status)) {
+      report_timeout(c.status, t, blockIdx.x);
+      bad = true;
+    }
+    if (!bad) {
+      const bool publish = !(blockIdx.x == c.drop_cta && t == c.drop_step);
+      const float* own = stage + ((size_t)par * B + cb0) * 128;
+      const float* in = recv + (size_t)par * cs * maxcol * 128;
+#pragma unroll
+      for (int u = 0; u < kOutMax; ++u) {
+        const int o = tid + u * kSplitThreads;
+        if (o < nout) {
+          // slices in order 0 .. cs-1 whichever CTA owns the column, so a
+          // column's bits do not depend on the batch around it (the loads
+          // first, all independent; adding the zeros past cs changes nothing)
+          float part[kKsplitMaxCluster];
+#pragma unroll
+          for (int k = 0; k < kKsplitMaxCluster; ++k)
+            part[k] = k >= cs ? 0.f : (k == j ? own[o] : in[(size_t)k * maxcol * 128 + o]);
+          float sum = pv[u];
+#pragma unroll
+          for (int k = 0; k < kKsplitMaxCluster; ++k) sum += part[k];
+          if (publish) {
+            const float out = relu(sum);
+            const size_t yo = ((size_t)t * B + cb0 + (o >> 7)) * H + row0 + (o & 127);
+            st_relaxed_f(c.y + yo, out);
+            if (c.y_mirror) c.y_mirror[yo] = out;
+          }
+        }
+      }
+    }
+    if (tid == 0) {
+      // this parity's flag and mbarrier serve step t + 2 next (every thread
+      // read the flag before the last barrier; no peer copies step t + 2's
+      // blocks before this CTA has published all of step t).  The mbarrier is
+      // armed again only once this thread has seen its phase complete: an
+      // arrival on a phase that has none pending is not allowed
+      s_large[par] = 0;
+      if (t + 2 < T && !bad) mbar_arrive_expect_tx(&recv_bar[par], in_bytes);
+    }
+  }
+  // ---- leave: MMAs retired, TMEM freed, then meet the cluster peers ----
+  if (tid == 0 && last_mma >= 0)
+    wait_phase(&mma_bar, (uint32_t)last_mma & 1u, c.timeout_ns, c.status);
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  // a wait that gave up in the last step counts as leaving early too
+  aborted = __syncthreads_or(aborted || bad) != 0;
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kSplitTmemCols)
+                 : "memory");
+  cluster_sync_all();  // every peer has issued its last copy
+  if (aborted) {
+    // a copy issued by a peer before it left may still be landing here
+    const uint64_t until = global_ns() + 50000ull;
+    while (global_ns() < until) {
+    }
+  }
+}
+
+}  // namespace
+
+size_t recur_dense_ksplit_smem(int nat, int B, int cs) {
+  const int bp = B <= 8 ? 8 : (B <= 16 ? 16 : 32);
+  const int maxcol = (B + cs - 1) / cs;
+  return 1024 + (size_t)nat * kAtomA + (size_t)nat * (2 * bp) * 128 +
+         (size_t)2 * B * 128 * sizeof(float) + (size_t)2 * cs * maxcol * 128 * sizeof(float);
+}
+
+namespace {
+
+template <int BP>
+cudaError_t launch_bp(const DenseSplitArgs& a, cudaStream_t s, bool query_only, int* clusters_fit) {
+  const size_t smem = recur_dense_ksplit_smem(a.nat, a.c.B, a.cs);
+  cudaError_t e = cudaFuncSetAttribute(recur_dense_ksplit_kernel<BP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.c.n_cta);
+  cfg.blockDim = dim3(kSplitThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)a.cs;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeCooperative;
+  at[1].val.cooperative = 1;
+  cfg.attrs = at;
+  if (query_only) {
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters_fit, recur_dense_ksplit_kernel<BP>, &cfg);
+  }
+  // every CTA waits on CTAs of other clusters: the cooperative launch makes
+  // the grid co-resident (or fails rather than run part of it)
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, recur_dense_ksplit_kernel<BP>, a);
+}
+
+}  // namespace
+
+int recur_dense_ksplit_plan(int H) {
+  if (H < 128 || H % 128 != 0) return 0;
+  int dev = 0, cl = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&cl, cudaDevAttrClusterLaunch, dev) != cudaSuccess || !cl ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return 0;
+  const int nblk = H / 128;
+  for (int cs = kKsplitMaxCluster; cs >= 2; --cs) {
+    if (H / 16 < cs) continue;  // every slice holds at least one K step
+    DenseSplitArgs a{};
+    a.c.B = kKsplitMaxB;  // the widest batch takes the most shared memory
+    a.c.n_cta = nblk * cs;
+    a.cs = cs;
+    a.nat = ksplit_nat(H, cs);
+    if (recur_dense_ksplit_smem(a.nat, kKsplitMaxB, cs) > (size_t)optin) continue;
+    int fit = 0;
+    if (launch_bp<32>(a, nullptr, true, &fit) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    if (fit >= nblk) return cs;
+  }
+  return 0;
+}
+
+cudaError_t launch_recur_dense_ksplit(const DenseSplitArgs& a, cudaStream_t s) {
+  const int B = a.c.B, H = a.c.H;
+  if (B < 1 || B > kKsplitMaxB || H % 128 != 0 || a.cs < 2 || a.cs > kKsplitMaxCluster ||
+      a.c.n_cta != H / 128 * a.cs || a.nat != ksplit_nat(H, a.cs))
+    return cudaErrorInvalidValue;
+  if (B <= 8) return launch_bp<8>(a, s, false, nullptr);
+  if (B <= 16) return launch_bp<16>(a, s, false, nullptr);
+  return launch_bp<32>(a, s, false, nullptr);
+}
+
+}  // namespace prnn

@@ -134,6 +134,40 @@ cudaError_t launch_recur_dense_wide(const DenseWideArgs& a, cudaStream_t s);
 bool recur_dense_wide_plan(int H, int sm_count, size_t smem_optin, int* R, int* S, int* depth,
                            size_t* smem);
 
+// Dense fp16 for wide batches on the tensor cores with the product split over
+// K inside clusters (persistent_dense_ksplit.cu): H / 128 clusters of cs CTAs
+// (2 <= cs <= 8); CTA j of cluster c multiplies rows [128c, 128c + 128) of Wh
+// by K slice j of h_{t-1} (ksplit_slice: the H / 16 K steps of 16 columns
+// shared out as evenly as they go) and finalizes batch columns
+// [j B / cs, (j + 1) B / cs) of those rows.  Wimg per CTA (cluster-major, then
+// j): nat atoms of 128 rows x 128 bytes, fp16, K-major, 16-byte chunk q of
+// row m at q ^ (m & 7) (the 128-byte swizzle), columns past the slice zero;
+// nat = the widest slice's 64-column atoms.
+constexpr int kKsplitMaxCluster = 8;
+constexpr int kKsplitMaxB = 32;
+constexpr int kKsplitMinB = 16;  // the default rule's smallest batch
+struct DenseSplitArgs {
+  RecurCommon c;
+  const void* Wimg;
+  const float* h0_rows;  // [B][H]: h0, or zeros
+  int cs, nat;
+};
+// K slice j of cs: first column k0 and width kl (multiples of 16)
+__host__ __device__ constexpr int ksplit_k0(int H, int cs, int j) { return j * (H / 16) / cs * 16; }
+__host__ __device__ constexpr int ksplit_kl(int H, int cs, int j) {
+  return ksplit_k0(H, cs, j + 1) - ksplit_k0(H, cs, j);
+}
+__host__ __device__ constexpr int ksplit_nat(int H, int cs) {
+  return ((H / 16 + cs - 1) / cs + 3) / 4;
+}
+// Dynamic shared memory of the kernel for a batch of B columns.
+size_t recur_dense_ksplit_smem(int nat, int B, int cs);
+// The largest cluster size (8 .. 2) for which all H / 128 clusters of the
+// kernel are resident at once (one CTA per SM) and its shared memory fits;
+// 0 when none does or H % 128 != 0.
+int recur_dense_ksplit_plan(int H);
+cudaError_t launch_recur_dense_ksplit(const DenseSplitArgs& a, cudaStream_t s);
+
 // Dense fp16 on the tensor cores (persistent_dense_tc.cu): per CTA an image of
 // its rows of Wh, nslices = H/64 K slices of N rows x 128 bytes (fp16,
 // 128-byte swizzle, rows past R zero), N = R rounded up to 16, N <= 32; the

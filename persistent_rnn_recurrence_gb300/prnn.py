@@ -29,7 +29,8 @@ PRNN_ALGO_PERSISTENT, PRNN_ALGO_PER_STEP = 0, 1
  PRNN_OPT_DEBUG_DROP_STEP, PRNN_OPT_TIMING, PRNN_OPT_PROJECTION, PRNN_OPT_CTA_GROUPS,
  PRNN_OPT_WIDE_LOADS, PRNN_OPT_BANK_AWARE, PRNN_OPT_POLL_DELAY_NS,
  PRNN_OPT_POLL_BACKOFF_NS, PRNN_OPT_RECURRENT_TC, PRNN_OPT_STAGED_ORDER,
- PRNN_OPT_SPARSE_REG_WEIGHTS, PRNN_OPT_SPARSE_STAGING_DEPTH, PRNN_OPT_DENSE_WIDE) = range(16)
+ PRNN_OPT_SPARSE_REG_WEIGHTS, PRNN_OPT_SPARSE_STAGING_DEPTH, PRNN_OPT_DENSE_WIDE,
+ PRNN_OPT_DENSE_KSPLIT) = range(17)
 
 PRNN_STACK_WAVEFRONT, PRNN_STACK_LAYERWISE = 0, 1
 
@@ -53,7 +54,7 @@ class prnn_info_t(ctypes.Structure):
         ("smem_bytes", ctypes.c_size_t), ("onchip_weight_bytes", ctypes.c_size_t),
         ("nnz", ctypes.c_size_t), ("recurrent_tensor_cores", ctypes.c_int),
         ("sparse_staged_order", ctypes.c_int), ("sparse_reg_weights", ctypes.c_int),
-        ("dense_wide_batch", ctypes.c_int)]
+        ("dense_wide_batch", ctypes.c_int), ("dense_ksplit", ctypes.c_int)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -760,12 +760,14 @@ def test_dense_wide_batch_matches_oracle(env, spec):
     _, prnn, o = env
     p = synth.make_problem(seed=95, **spec)
     ref = o.forward(p)
-    y, info = run_gpu(env, p, options={prnn.PRNN_OPT_DENSE_WIDE: 2})
+    y, info = run_gpu(env, p, options={prnn.PRNN_OPT_DENSE_WIDE: 2,
+                                       prnn.PRNN_OPT_DENSE_KSPLIT: 0})
     assert info["dense_wide_batch"] == 1 and info["rows_per_cta"] in (8, 16)
     assert info["n_cta"] == p.H // info["rows_per_cta"] <= info["sm_count"]
     check(y, ref, "f16", f"wide {spec}")
-    y_old, info_old = run_gpu(env, p, options={prnn.PRNN_OPT_DENSE_WIDE: 0})
-    assert info_old["dense_wide_batch"] == 0
+    y_old, info_old = run_gpu(env, p, options={prnn.PRNN_OPT_DENSE_WIDE: 0,
+                                               prnn.PRNN_OPT_DENSE_KSPLIT: 0})
+    assert info_old["dense_wide_batch"] == 0 and info_old["dense_ksplit"] == 0
     check(y_old, ref, "f16", f"wide off {spec}")
 
 
@@ -778,6 +780,7 @@ def test_dense_wide_batch_exact_properties(env):
     p = synth.make_problem(H=1152, B=32, T=16, wdtype="f16", seed=96, h0_std=0.1)
     lay = prnn.Layer.from_problem(p)
     try:
+        lay.set_option(prnn.PRNN_OPT_DENSE_KSPLIT, 0)
         assert lay.info()["dense_wide_batch"] == 1  # by default: 4 passes, H >= 1024
         lay.set_option(prnn.PRNN_OPT_DENSE_WIDE, 2)  # and for the B = 16 forwards below
         info = lay.info()
@@ -810,8 +813,9 @@ def test_dense_wide_batch_full_size_teacher_forced(env):
     """H = 2304, B = 32, T = 256 (a sweep point): sampled outputs against one
     oracle step on the GPU's own previous state."""
     _, _, o = env
+    _, prnn, _ = env
     p = synth.make_problem(H=2304, B=32, T=256, wdtype="f16", seed=97)
-    y, info = run_gpu(env, p)
+    y, info = run_gpu(env, p, options={prnn.PRNN_OPT_DENSE_KSPLIT: 0})
     assert info["dense_wide_batch"] == 1 and np.isfinite(y).all()
     rng = np.random.default_rng(11)
     samples = [(int(t), int(b), int(r)) for t, b, r in zip(
@@ -833,6 +837,7 @@ def test_dense_wide_batch_default_rule(env):
         try:
             p = synth.make_problem(H=H, B=B, T=1, wdtype="f16", seed=99)
             lay.set_problem_weights(p)
+            lay.set_option(prnn.PRNN_OPT_DENSE_KSPLIT, 0)
             assert lay.info()["dense_wide_batch"] == want, (H, B)
             lay.set_option(prnn.PRNN_OPT_DENSE_WIDE, 0)
             assert lay.info()["dense_wide_batch"] == 0
@@ -848,6 +853,7 @@ def test_dense_wide_batch_times_out_cleanly(env):
     torch, prnn, o = env
     p = synth.make_problem(H=1152, B=24, T=6, wdtype="f16", seed=98)
     lay = prnn.Layer.from_problem(p)
+    lay.set_option(prnn.PRNN_OPT_DENSE_KSPLIT, 0)
     assert lay.info()["dense_wide_batch"] == 1
     lay.set_option(prnn.PRNN_OPT_WAIT_TIMEOUT_US, 20000)
     lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_CTA, 5)
@@ -874,3 +880,125 @@ def test_cluster_exchange_probe(env):
     with pytest.raises(prnn.PrnnError) as e:
         prnn.prnn_probe_cluster_exchange(1792, 16, 1000, 10)
     assert e.value.status == prnn.PRNN_ERR_UNSUPPORTED
+
+
+# --- dense fp16, wide batches on the tensor cores, K split over clusters of 8 ------------
+KSPLIT = [dict(H=2304, B=32, T=24, wdtype="f16", h0_std=0.2),  # 18 clusters, K slices of 288
+          dict(H=1152, B=32, T=40, wdtype="f16"),
+          dict(H=1152, B=16, T=40, wdtype="f16"),              # N = 32 (hi 16 + lo 16)
+          dict(H=1152, B=21, T=20, wdtype="f16", h0_std=0.5),  # odd B: unpadded owner blocks
+          dict(H=640, I=200, B=24, T=16, wdtype="f16", h0_std=1.0),  # slices of 80: a half atom
+          dict(H=256, B=17, T=30, wdtype="f16"),               # slices of 32
+          dict(H=1792, B=20, T=20, wdtype="f16"),
+          dict(H=2048, B=16, T=12, wdtype="f16", h0_std=0.3),
+          dict(H=128, I=64, B=32, T=50, wdtype="f16"),         # one cluster, one K step
+          dict(H=512, B=1, T=20, wdtype="f16", h0_std=0.5),    # N = 16 (hi 8 + lo 8)
+          dict(H=384, B=5, T=10, wdtype="f16"),
+          dict(H=1024, B=8, T=16, wdtype="f16", h0_std=0.2)]
+
+
+@pytest.mark.parametrize("spec", KSPLIT)
+def test_dense_ksplit_matches_oracle(env, spec):
+    """The tensor-core K-split kernel (forced on for every B <= 32; clusters
+    of the largest size whose clusters are all resident) stays within the
+    rule, and within it of the CUDA-core kernels."""
+    _, prnn, o = env
+    p = synth.make_problem(seed=105, **spec)
+    ref = o.forward(p)
+    y, info = run_gpu(env, p, options={prnn.PRNN_OPT_DENSE_KSPLIT: 2},
+                      pre_options={prnn.PRNN_OPT_DENSE_KSPLIT: 2})
+    cs = info["dense_ksplit"]  # the cluster size
+    assert 2 <= cs <= 8 and info["dense_wide_batch"] == 0
+    assert info["n_cta"] == p.H // 128 * cs and info["rows_per_cta"] == 128
+    check(y, ref, "f16", f"ksplit {spec}")
+    y_cc, info_cc = run_gpu(env, p, options={prnn.PRNN_OPT_DENSE_KSPLIT: 0})
+    assert info_cc["dense_ksplit"] == 0
+    assert np.abs(y - y_cc).max() <= TOL["f16"] * float(np.abs(ref).max())
+
+
+def test_dense_ksplit_exact_properties(env):
+    """Determinism, chaining, and batch independence: a column's products do
+    not depend on the other columns of its launch (same operand width)."""
+    torch, prnn, o = env
+    p = synth.make_problem(H=1152, B=32, T=16, wdtype="f16", seed=106, h0_std=0.1)
+    lay = prnn.Layer.from_problem(p)
+    try:
+        info = lay.info()
+        assert info["dense_ksplit"] == 8 and info["n_cta"] == 72  # the default at B >= 16
+        x = torch.from_numpy(p.x).cuda()
+        h0 = torch.from_numpy(p.h0).cuda()
+        y = lay.forward(x, h0)
+        y_again = lay.forward(x, h0)
+        ya = lay.forward(x[:7].contiguous(), h0)
+        yb = lay.forward(x[7:].contiguous(), ya[-1].contiguous())
+        y20 = lay.forward(x[:, 5:25].contiguous(), h0[5:25].contiguous())
+        y16 = lay.forward(x[:, 16:].contiguous(), h0[16:].contiguous())
+        torch.cuda.synchronize()
+        assert lay.status() == prnn.PRNN_OK
+    finally:
+        lay.close()
+    assert torch.equal(y, y_again)
+    assert torch.equal(torch.cat([ya, yb]), y)
+    assert torch.equal(y20, y[:, 5:25])
+    ref = o.forward(p)
+    check(y.cpu().numpy(), ref, "f16", "ksplit")
+    check(y16.cpu().numpy(), ref[:, 16:], "f16", "ksplit, 16 columns")
+
+
+def test_dense_ksplit_large_values_are_scaled(env):
+    """h of 2^15 or more would overflow the fp16 split: such steps are scaled
+    by a power of two first, and the result still follows the oracle."""
+    _, prnn, o = env
+    p = synth.make_problem(H=512, B=16, T=6, wdtype="f16", seed=107, h0_std=2.0e5)
+    ref = o.forward(p)
+    assert np.abs(p.h0).max() > 32768.0 and np.abs(ref).max() > 32768.0
+    y, info = run_gpu(env, p)
+    assert info["dense_ksplit"] >= 2
+    check(y, ref, "f16", "ksplit, large h")
+
+
+def test_dense_ksplit_full_size_matches_oracle(env):
+    """H = 2304, B = 32 (a sweep point) over the full T = 256, element by
+    element against the oracle on every host core."""
+    import os
+    _, prnn, o = env
+    p = synth.make_problem(H=2304, B=32, T=256, wdtype="f16", seed=108)
+    y, info = run_gpu(env, p)
+    assert info["dense_ksplit"] >= 2 and info["n_cta"] == 18 * info["dense_ksplit"]
+    ref = o.forward(p, threads=max(1, os.cpu_count() or 1))
+    check(y, ref, "f16", "ksplit full size")
+
+
+def test_dense_ksplit_default_rule(env):
+    """Option 1 (default) runs the K-split kernel for B >= 16 where it is
+    planned (H % 128 == 0, every cluster resident); 0 never; 2 for any B."""
+    _, prnn, _ = env
+    cases = [(1152, 32, 1), (1152, 16, 1), (2304, 32, 1), (640, 24, 1), (1152, 8, 0),
+             (4096, 32, 0), (1000, 32, 0)]
+    for H, B, want in cases:
+        lay = prnn.Layer(H, H, B, "f16", "persistent")
+        try:
+            p = synth.make_problem(H=H, B=B, T=1, wdtype="f16", seed=109)
+            lay.set_problem_weights(p)
+            assert (lay.info()["dense_ksplit"] > 0) == want, (H, B)
+            lay.set_option(prnn.PRNN_OPT_DENSE_KSPLIT, 0)
+            assert lay.info()["dense_ksplit"] == 0
+            with pytest.raises(prnn.PrnnError):
+                lay.set_option(prnn.PRNN_OPT_DENSE_KSPLIT, 3)
+        finally:
+            lay.close()
+
+
+def test_dense_ksplit_times_out_cleanly(env):
+    torch, prnn, o = env
+    p = synth.make_problem(H=1152, B=24, T=6, wdtype="f16", seed=110)
+    lay = prnn.Layer.from_problem(p)
+    assert lay.info()["dense_ksplit"] == 8
+    lay.set_option(prnn.PRNN_OPT_WAIT_TIMEOUT_US, 20000)
+    lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_CTA, 13)
+    lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_STEP, 2)
+    lay.forward(torch.from_numpy(p.x).cuda())
+    assert lay.status() == prnn.PRNN_ERR_TIMEOUT
+    lay.close()
+    y, _ = run_gpu(env, p)
+    check(y, o.forward(p), "f16", "after timeout")
