@@ -1154,9 +1154,13 @@ def run_trace(args):
     import torch
     from persistent_rnn_recurrence_gb300 import prnn, synth
     dev = torch.device("cuda", 0)
-    p = synth.named_problem(args.config, T=args.trace_steps)
+    if args.config.startswith("sweep_"):  # a point of the sweep, by name
+        kw = dict(synth.sweep_points())[args.config]
+        p = synth.make_problem(name=args.config, **{**kw, "T": args.trace_steps})
+    else:
+        p = synth.named_problem(args.config, T=args.trace_steps)
     if not p.sparse:
-        raise SystemExit("--trace needs a sparse layer")
+        return run_trace_ksplit(args, p)
     lay = prnn.Layer.from_problem(p)
     lay.set_option(prnn.PRNN_OPT_TIMING, 1)
     info = lay.info()
@@ -1215,6 +1219,101 @@ def run_trace(args):
                        "frac_ctas_first_poll_fresh": float((ph["rounds"] == 0).mean()),
                        "max_rounds": int(ph["rounds"].max())},
             "globaltimer_resolution_ns": ph["globaltimer_resolution_ns"]}
+    print(json.dumps(line), flush=True)
+    return 0 if same and st == prnn.PRNN_OK else 1
+
+
+KSPLIT_PHASES = [("fill_own", 4, 5), ("fill_wait", 5, 6), ("mma", 6, 7), ("mma_issue", 6, 13),
+                 ("stage", 7, 8), ("send", 8, 9), ("barrier2", 9, 10), ("receive", 10, 11),
+                 ("publish", 11, 12)]
+
+
+def ksplit_trace_phases(rec, clock_mhz):
+    """Where a step of the dense K-split kernel goes, from trace records rec
+    [R, T, n_cta, 20] (uint32 words of the kernel's record).  Per CTA and step
+    1 .. T-1: SM-clock differences between its stamps (ns), the step (step
+    start to step start), and from the globaltimer readings the exchange: its
+    first barrier minus the last publish of the previous step over all CTAs
+    (the slices draw on several clusters), and the spread of each step's
+    publishes across CTAs."""
+    import numpy as np
+    r = rec.astype(np.int64)
+    ns = 1e3 / clock_mhz
+    d = lambda a, b: ((((b - a) + (1 << 31)) & 0xffffffff) - (1 << 31)).astype(np.float64)
+    sl = slice(1, r.shape[1])
+    out = {name: d(r[:, sl, :, a], r[:, sl, :, b]).ravel() * ns for name, a, b in KSPLIT_PHASES}
+    out["step"] = d(r[:, :-1, :, 4], r[:, sl, :, 4]).ravel() * ns
+    gbar = (r[..., 15] << 32) | r[..., 14]
+    gpub = (r[..., 17] << 32) | r[..., 16]
+    last_pub = gpub.max(axis=2)                       # [R, T]
+    out["exchange"] = (gbar[:, sl, :] - last_pub[:, :-1, None]).astype(np.float64).ravel()
+    out["publish_skew"] = (gpub.max(axis=2) - gpub.min(axis=2))[:, sl].astype(np.float64).ravel()
+    out["rounds"] = r[:, sl, :, 18].ravel()
+    return out
+
+
+def run_trace_ksplit(args, p):
+    """--trace for a dense layer that runs the K-split kernel: per-phase
+    medians and spreads (ns) of its steps, the traced output checked against
+    the untraced one bit for bit."""
+    import numpy as np
+    import torch
+    from persistent_rnn_recurrence_gb300 import prnn
+    dev = torch.device("cuda", 0)
+    lay = prnn.Layer.from_problem(p)
+    lay.set_option(prnn.PRNN_OPT_TIMING, 1)
+    info = lay.info()
+    if not info["dense_ksplit"]:
+        lay.close()
+        raise SystemExit("--trace needs a sparse layer or a dense one that runs the K-split kernel")
+    x = torch.from_numpy(p.x).to(dev)
+    y0 = torch.empty(p.T, p.B, p.H, device=dev)
+    y1 = torch.empty_like(y0)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    n_cta = info["n_cta"]
+    W = 17 * 16
+    buf = torch.full((p.T * n_cta * W,), -1, dtype=torch.int32, device=dev)
+    reps = max(3, min(args.steps, 20))
+
+    def runs(traced):
+        prnn.prnn_set_trace_buffer(lay.h, buf if traced else None, buf.numel() * 4)
+        ms, recs = [], []
+        for i in range(reps + 2):
+            flush.fill_(1.0)
+            prnn.prnn_forward(lay.h, p.T, p.B, x, None, y1 if traced else y0)
+            t = prnn.prnn_get_timing(lay.h)[1]
+            if i >= 2:
+                ms.append(t)
+                if traced:
+                    recs.append(buf.view(p.T, n_cta, W)[..., :20].cpu().numpy().view(np.uint32).copy())
+        return sorted(ms)[len(ms) // 2], recs
+
+    ms_plain, _ = runs(False)
+    ms_traced, recs = runs(True)
+    prnn.prnn_set_trace_buffer(lay.h, None, 0)
+    torch.cuda.synchronize()
+    st = lay.status()
+    lay.close()
+    same = bool(torch.equal(y0, y1))
+    clock_mhz = load_peaks().get("sm_max_mhz", 2070.0)
+    ph = ksplit_trace_phases(np.stack(recs), clock_mhz)
+
+    def stats(a):
+        a = np.sort(np.asarray(a, dtype=np.float64))
+        q = lambda f: float(a[min(len(a) - 1, int(f * len(a)))])
+        return {"median": q(0.5), "p10": q(0.1), "p90": q(0.9), "mean": float(a.mean())}
+
+    names = [n for n, _, _ in KSPLIT_PHASES] + ["step", "exchange", "publish_skew"]
+    line = {"trace": p.name, "kernel": "recur_dense_ksplit_kernel", "T": p.T, "B": p.B, "H": p.H,
+            "n_cta": n_cta, "cluster_size": info["dense_ksplit"],
+            "status": prnn.prnn_status_string(st), "traced_equals_untraced": same,
+            "clock_mhz_assumed": clock_mhz,
+            "recurrence_us_per_step": {"plain": 1e3 * ms_plain / p.T,
+                                       "traced": 1e3 * ms_traced / p.T},
+            "samples": int(ph["step"].size),
+            "phases_ns": {k: stats(ph[k]) for k in names},
+            "repoll": {"mean_rounds": float(ph["rounds"].mean()),
+                       "max_rounds": int(ph["rounds"].max())}}
     print(json.dumps(line), flush=True)
     return 0 if same and st == prnn.PRNN_OK else 1
 

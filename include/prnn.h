@@ -124,10 +124,12 @@ typedef enum {
                                      step's product over K inside clusters (h split into fp16
                                      hi + lo parts, about 22 bits; partial sums reduced through
                                      distributed shared memory) for forwards of B <= 32.
-                                     1 = for B >= 16 (default); 2 = for every B <= 32; 0 =
+                                     1 = where it measured faster than the CUDA-core kernels
+                                     (default): H >= 2048 and B >= 8, H >= 1152 and B >= 12,
+                                     or H >= 640 and B >= 24; 2 = for every B <= 32; 0 =
                                      never.  Its weight image is built at set_weights when
-                                     max_batch >= 16 or the option is 2; it takes precedence
-                                     over PRNN_OPT_DENSE_WIDE                                  */
+                                     the default covers max_batch or the option is 2; it
+                                     takes precedence over PRNN_OPT_DENSE_WIDE                  */
 } prnn_option_t;
 
 /* Plan and sizes chosen at create / set_weights time (read-only report). */
@@ -303,10 +305,11 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info);
 prnn_status_t prnn_get_timing(prnn_t h, float* ms_projection, float* ms_recurrence);
 
 /*
- * Phase trace of the sparse persistent kernel (a diagnostic; off unless a
- * buffer is set).  While `buffer` (a DEVICE pointer, 16-byte aligned, owned by
- * the caller) is set, every prnn_forward / prnn_forward_host of this handle
- * runs the trace build of the sparse kernel, which writes one record of
+ * Phase trace of the sparse persistent kernel and of the dense K-split
+ * kernel (a diagnostic; off unless a buffer is set).  While `buffer` (a
+ * DEVICE pointer, 16-byte aligned, owned by the caller) is set, every
+ * prnn_forward / prnn_forward_host of this handle runs the trace build of its
+ * recurrent kernel.  The sparse kernel writes one record of
  * 17 x 16 uint32 words per step and CTA, [T][n_cta][17][16], for the step's
  * first batch pass.  Slot 0: SM id, CTA index, number of warps, then unused.
  * Slot 1 + w, warp w: SM clock (low 32 bits) at pass start, after its
@@ -318,12 +321,21 @@ prnn_status_t prnn_get_timing(prnn_t h, float* ms_projection, float* ms_recurren
  * the SM clock after those readings; 2 unused.  Slots of warps the CTA does
  * not have, and records of CTAs whose group has no batch column, are left as
  * they were.
+ * The dense K-split kernel (PRNN_OPT_DENSE_KSPLIT) writes the first 20 words
+ * of each record: SM id, CTA index, cluster size, K slice; SM-clock stamps of
+ * its first epilogue thread at step start, its polls done, the CTA barrier
+ * after the fill, the MMAs seen complete, partial sums staged, copies issued,
+ * the second CTA barrier, the peers' partial sums received, publish done; the
+ * MMA-issuing thread's clock after its last MMA; globaltimer ns after the
+ * first barrier (low, high) and after the publish (low, high); the most
+ * re-poll rounds of that thread; 1 unused.
  * The pages time the effect of each measure on whole steps (Sparse
  * Persistent RNNs, measured-effects table); this records where inside a step
  * the time goes.  Results are the same bits as without the trace.  Requires
  * `bytes` >= T * n_cta * 1088 at each forward (PRNN_ERR_INVALID_ARG otherwise)
- * and a sparse layer on the persistent path with column-order, wide staging
- * (PRNN_ERR_UNSUPPORTED otherwise).  buffer = NULL turns the trace off.
+ * and a sparse layer on the persistent path with column-order, wide staging,
+ * or a forward that runs the K-split kernel (PRNN_ERR_UNSUPPORTED otherwise).
+ * buffer = NULL turns the trace off.
  * Errors: INVALID_ARG for a misaligned, too small or non-device buffer.
  */
 prnn_status_t prnn_set_trace_buffer(prnn_t h, void* buffer, size_t bytes);

@@ -845,7 +845,7 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
     // wide batches on the tensor cores: per CTA (cluster-major, then K slice
     // j) nat atoms of 128 rows x 64 columns, 16-byte chunk q of row m at
     // q ^ (m & 7) (the 128-byte swizzle of the K-major MMA operand)
-    const int kcs = h->wdtype == PRNN_F16 && (h->maxB >= kKsplitMinB || h->ks_opt == 2)
+    const int kcs = h->wdtype == PRNN_F16 && (ksplit_default(H, h->maxB) || h->ks_opt == 2)
                         ? recur_dense_ksplit_plan(H)
                         : 0;
     if (kcs > 0) {
@@ -1009,12 +1009,13 @@ static bool dense_wide_for(const prnn_t h, int B) {
 }
 
 // Whether a dense persistent forward of B columns runs the tensor-core
-// K-split kernel: planned at set_weights, enabled, flags in the data, B <= 32.
+// K-split kernel: planned at set_weights, enabled, flags in the data, B <= 32,
+// and by default only where it measured faster (ksplit_default).
 static bool dense_ksplit_for(const prnn_t h, int B) {
   if (h->algo != PRNN_ALGO_PERSISTENT || h->sparse || !h->ks || h->ks_opt == 0 ||
       h->sync_mode != 0 || h->rtc || B < 1 || B > kKsplitMaxB)
     return false;
-  return h->ks_opt == 2 || B >= kKsplitMinB;
+  return h->ks_opt == 2 || ksplit_default(h->H, B);
 }
 
 // Whether the recurrent kernel prnn_forward would launch can also write every
@@ -1028,10 +1029,13 @@ static bool recurrence_mirrors(const prnn_t h) {
 // output as the recurrence publishes it.  Arguments are checked by the callers.
 static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const float* h0,
                                   float* y, float* y_mirror, cudaStream_t s) {
-  if (h->trace) {  // the phase trace: sparse persistent kernel, column order, wide staging
-    if (h->algo != PRNN_ALGO_PERSISTENT || !h->sparse || h->place || !h->wide_loads)
+  if (h->trace) {  // the phase trace: sparse persistent kernel (column order, wide
+                   // staging) or the dense K-split kernel
+    const bool ks = dense_ksplit_for(h, B);
+    if (!ks && (h->algo != PRNN_ALGO_PERSISTENT || !h->sparse || h->place || !h->wide_loads))
       return PRNN_ERR_UNSUPPORTED;
-    if ((size_t)T * h->n_cta * kTraceWords > h->trace_words) return PRNN_ERR_INVALID_ARG;
+    const size_t n_cta = ks ? (size_t)(h->H / 128 * h->ks_cs) : (size_t)h->n_cta;
+    if ((size_t)T * n_cta * kTraceWords > h->trace_words) return PRNN_ERR_INVALID_ARG;
   }
   const size_t ny = (size_t)T * B * h->H;
   PRNN_TRY(ensure_P(h, ny));
@@ -1097,7 +1101,7 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
       c.nthreads = 256;
       c.smem = recur_dense_ksplit_smem(h->ks_nat, B, h->ks_cs);
       if (h->poll_delay_ns < 0) c.poll_delay = 0;  // measured: no pause is fastest here
-      DenseSplitArgs a{c, h->Wimg_ks, h0 ? h0 : h->zeros, h->ks_cs, h->ks_nat};
+      DenseSplitArgs a{c, h->Wimg_ks, h0 ? h0 : h->zeros, h->ks_cs, h->ks_nat, h->trace};
       PRNN_TRY(launch_recur_dense_ksplit(a, s));
     } else if (dense_wide_for(h, B)) {
       c.R = h->w_R;

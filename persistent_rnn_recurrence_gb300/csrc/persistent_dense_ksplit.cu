@@ -53,6 +53,8 @@ namespace {
 
 constexpr int kSplitThreads = 256;     // 8 warps; warps 4..7 read TMEM lanes 0..127
 constexpr int kSplitPollMax = 12;      // float4 polls a thread keeps in flight
+static_assert(kSplitPollMax * kSplitThreads * 4 >= kKsplitMaxB * kKsplitMaxSlice,
+              "one poll round covers the widest slice of the widest batch");
 constexpr uint32_t kAtomA = 128 * 128;  // bytes of one A atom: 128 rows x 64 fp16
 constexpr int kSplitTmemCols = 64;     // N <= 64
 constexpr float kSplitLarge = 32768.f; // |h| from here on would overflow the fp16 split
@@ -115,12 +117,11 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
 
 // Split four values (scaled by `scale`, a power of two) into their fp16 hi
-// and lo parts and store them into the B operand: column b, K index k (a
-// multiple of 4) of the slice.  Row n of an atom holds 128 bytes, its 16-byte
-// chunk q at q ^ (n & 7); hi goes to row b, lo to row BP + b.
+// and lo parts and store them into the B operand at `hi` (4 consecutive K
+// indices of one batch row n; lo goes to row BP + n, BP * 128 bytes on).
+// Row n of an atom holds 128 bytes, its 16-byte chunk q at q ^ (n & 7).
 template <int BP>
-__device__ __forceinline__ void store_split(unsigned char* gB, uint32_t atom_bytes, float4 v,
-                                            float scale, int b, int k) {
+__device__ __forceinline__ void store_split(unsigned char* hi_dst, float4 v, float scale) {
   const float x[4] = {v.x * scale, v.y * scale, v.z * scale, v.w * scale};
   float hi[4], lo[4];
 #pragma unroll
@@ -129,16 +130,13 @@ __device__ __forceinline__ void store_split(unsigned char* gB, uint32_t atom_byt
     hi[i] = __half2float(h);
     lo[i] = x[i] - hi[i];
   }
-  const int a = k >> 6, kk = k & 63;
-  const uint32_t off = (uint32_t)((((kk >> 3) ^ (b & 7)) << 4) + ((kk & 7) << 1));
-  unsigned char* atom = gB + (size_t)a * atom_bytes;
-  *reinterpret_cast<uint2*>(atom + b * 128 + off) =
-      make_uint2(pack_half2(hi[0], hi[1]), pack_half2(hi[2], hi[3]));
-  *reinterpret_cast<uint2*>(atom + (BP + b) * 128 + off) =
+  *reinterpret_cast<uint2*>(hi_dst) = make_uint2(pack_half2(hi[0], hi[1]), pack_half2(hi[2], hi[3]));
+  *reinterpret_cast<uint2*>(hi_dst + BP * 128) =
       make_uint2(pack_half2(lo[0], lo[1]), pack_half2(lo[2], lo[3]));
 }
 
-template <int BP>
+// TR: the phase-trace build (records per step and CTA in a.trace)
+template <int BP, bool TR>
 __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(const DenseSplitArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t mma_bar;
@@ -152,6 +150,17 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
   const RecurCommon& c = a.c;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = c.H, B = c.B, T = c.T, cs = a.cs, nat = a.nat;
+  {
+    // launched in clusters of any other size (a launch that lost its cluster
+    // shape), every peer address below would be wrong: record the failure
+    // (step -1) and leave before touching TMEM or a peer
+    uint32_t ncl;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncl));
+    if ((int)ncl != cs || (int)gridDim.x != c.n_cta) {
+      if (tid == 0) report_timeout(c.status, -1, blockIdx.x);
+      return;
+    }
+  }
   const int j = (int)cluster_rank();                  // K slice of this CTA
   const int row0 = blockIdx.x / cs * 128;            // the cluster's row block
   const int k0 = ksplit_k0(H, cs, j), kl = ksplit_kl(H, cs, j);
@@ -208,26 +217,66 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
   const int q4 = kl >> 2;  // float4 per batch column of the slice
   const int nf4 = B * q4;
   const int nout = ncol * 128;  // outputs this CTA finalizes: column cb0 + o / 128, row o % 128
+  // The thread's float4 items of the slice (at most kSplitPollMax: the plan
+  // keeps kl <= kKsplitMaxSlice, so B * kl / 4 <= kSplitPollMax * 256), with
+  // their offsets in a step's h (floats) and in the B operand (bytes, hi),
+  // computed once: dividing by the launch-time slice width in every step
+  // measured slower than the step's whole arithmetic (dependent integer
+  // chains with 8 warps per SM to hide them)
+  int goff[kSplitPollMax];
+  uint32_t soff[kSplitPollMax];
+  unsigned items = 0;
+#pragma unroll
+  for (int u = 0; u < kSplitPollMax; ++u) {
+    const int i = tid + u * kSplitThreads;
+    goff[u] = 0;
+    soff[u] = 0;
+    if (i < nf4) {
+      const int b = i / q4, k = 4 * (i % q4);
+      goff[u] = b * H + k;
+      soff[u] = (uint32_t)((k >> 6) * (int)kAtomB + b * 128 +
+                           ((((k & 63) >> 3) ^ (b & 7)) << 4) + ((k & 7) << 1));
+      items |= 1u << u;
+    }
+  }
   Waiter w;
   w.status = c.status;
   w.timeout_ns = c.timeout_ns;
   w.backoff = c.poll_backoff;
   constexpr int kOutMax = (kKsplitMaxB + 1) / 2 * 128 / kSplitThreads;  // cs >= 2
+  // output o = tid + u * 256 (o < nout) sits at ooff[u] in a step of P and y
+  int ooff[kOutMax];
+#pragma unroll
+  for (int u = 0; u < kOutMax; ++u) {
+    const int o = tid + u * kSplitThreads;
+    ooff[u] = (cb0 + (o >> 7)) * H + row0 + (o & 127);
+  }
+  const size_t step_floats = (size_t)B * H;
   float pn[kOutMax];  // projection values of the next step's outputs
   auto load_p = [&](int t) {
+    const float* pt = c.P + (size_t)t * step_floats;
 #pragma unroll
-    for (int u = 0; u < kOutMax; ++u) {
-      const int o = tid + u * kSplitThreads;
-      pn[u] = o < nout ? ld_nc_pinned(c.P + ((size_t)t * B + cb0 + (o >> 7)) * H + row0 + (o & 127))
-                       : 0.f;
-    }
+    for (int u = 0; u < kOutMax; ++u)
+      pn[u] = tid + u * kSplitThreads < nout ? ld_nc_pinned(pt + ooff[u]) : 0.f;
   };
   if (T > 0) load_p(0);
   bool bad = false;       // this thread saw a failed wait
   bool aborted = false;   // uniform: the CTA left the step loop early
   int last_mma = -1;      // thread 0: the last step whose MMAs it issued
+  uint32_t tr[kKsplitTraceWords];  // thread 128's record of the step (trace build)
+  auto stamp = [&](int k) {
+    if constexpr (TR) tr[k] = (uint32_t)clock64();
+  };
+  auto stamp_ns = [&](int k) {
+    if constexpr (TR) {
+      const uint64_t g = global_ns();
+      tr[k] = (uint32_t)g;
+      tr[k + 1] = (uint32_t)(g >> 32);
+    }
+  };
   for (int t = 0; t < T; ++t) {
     const int par = t & 1;
+    stamp(4);
     w.new_step();
     float pv[kOutMax];
 #pragma unroll
@@ -238,31 +287,27 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
     const bool poll = t > 0;
     if (poll) spin_cycles(c.poll_delay);
     bool large = false;
-    for (int i0 = tid; i0 < nf4 && !bad; i0 += kSplitPollMax * kSplitThreads) {
+    uint32_t round_max = 0;
+    {
       float4 v[kSplitPollMax];
 #pragma unroll
-      for (int u = 0; u < kSplitPollMax; ++u) {
-        const int i = i0 + u * kSplitThreads;
-        if (i < nf4) {
-          const float* p = src + (size_t)(i / q4) * H + 4 * (i % q4);
-          v[u] = poll ? ld_relaxed_f4(p) : __ldg(reinterpret_cast<const float4*>(p));
-        }
-      }
-      // each float4 is split and stored as soon as it is fresh, so the
-      // conversions of early data overlap the wait for late data
-      unsigned pending = 0;
-#pragma unroll
       for (int u = 0; u < kSplitPollMax; ++u)
-        if (i0 + u * kSplitThreads < nf4) pending |= 1u << u;
+        if ((items >> u) & 1u)
+          v[u] = poll ? ld_relaxed_f4(src + goff[u])
+                      : __ldg(reinterpret_cast<const float4*>(src + goff[u]));
+      // each float4 is split and stored as soon as it is fresh, so the
+      // conversions of early data overlap the loads still in flight (checking
+      // all of them first and converting in one straight run measured slower:
+      // H=1152 B=32 3.40 -> 4.24 us per step)
+      unsigned pending = items;
       uint32_t spins = 0, round = 0;
-      for (;;) {
+      while (pending != 0u) {
 #pragma unroll
         for (int u = 0; u < kSplitPollMax; ++u)
           if (((pending >> u) & 1u) && (!poll || ready4(v[u]))) {  // h0 is not polled
-            const int i = i0 + u * kSplitThreads;
             large |= !(fabsf(v[u].x) < kSplitLarge) | !(fabsf(v[u].y) < kSplitLarge) |
                      !(fabsf(v[u].z) < kSplitLarge) | !(fabsf(v[u].w) < kSplitLarge);
-            store_split<BP>(gB, kAtomB, v[u], 1.f, i / q4, 4 * (i % q4));
+            store_split<BP>(gB + soff[u], v[u], 1.f);
             pending &= ~(1u << u);
           }
         if (pending == 0u) break;
@@ -272,30 +317,33 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
           break;
         }
         w.pause(round);
+        if constexpr (TR) round_max = round > round_max ? round : round_max;
 #pragma unroll
         for (int u = 0; u < kSplitPollMax; ++u)
-          if ((pending >> u) & 1u) {
-            const int i = i0 + u * kSplitThreads;
-            v[u] = ld_relaxed_f4(src + (size_t)(i / q4) * H + 4 * (i % q4));
-          }
+          if ((pending >> u) & 1u) v[u] = ld_relaxed_f4(src + goff[u]);
       }
-      if (bad) break;
     }
+    stamp(5);
+    if constexpr (TR) tr[18] = round_max;
     if (large) s_large[par] = 1;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (__syncthreads_or(bad)) {
       aborted = true;
       break;
     }
+    stamp(6);
+    stamp_ns(14);
     // a value too large for the fp16 split (rare): scale the slice by 2^-e
     int e = 0;
     if (s_large[par]) {
       float m = 0.f;
-      for (int i = tid; i < nf4; i += kSplitThreads) {
-        const float* q = src + (size_t)(i / q4) * H + 4 * (i % q4);
-        const float4 v = poll ? ld_relaxed_f4(q) : __ldg(reinterpret_cast<const float4*>(q));
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-      }
+#pragma unroll
+      for (int u = 0; u < kSplitPollMax; ++u)
+        if ((items >> u) & 1u) {
+          const float* q = src + goff[u];
+          const float4 v = poll ? ld_relaxed_f4(q) : __ldg(reinterpret_cast<const float4*>(q));
+          m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       if (lane == 0) s_red[warp] = m;
@@ -306,11 +354,13 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
       // m * 2^-e < 2^15; an infinite value is left as it is
       if (m >= kSplitLarge && m <= 3.0e38f) e = ilogbf(m) - 14;
       const float scale = pow2i(-e);
-      for (int i = tid; i < nf4; i += kSplitThreads) {
-        const float* q = src + (size_t)(i / q4) * H + 4 * (i % q4);
-        const float4 v = poll ? ld_relaxed_f4(q) : __ldg(reinterpret_cast<const float4*>(q));
-        store_split<BP>(gB, kAtomB, v, scale, i / q4, 4 * (i % q4));
-      }
+#pragma unroll
+      for (int u = 0; u < kSplitPollMax; ++u)
+        if ((items >> u) & 1u) {
+          const float* q = src + goff[u];
+          const float4 v = poll ? ld_relaxed_f4(q) : __ldg(reinterpret_cast<const float4*>(q));
+          store_split<BP>(gB + soff[u], v, scale);
+        }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncthreads();
     }
@@ -329,6 +379,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
       }
       umma_commit(&mma_bar);
       last_mma = t;
+      if constexpr (TR) {
+        const uint32_t ck = (uint32_t)clock64();
+        if (a.trace) a.trace[((size_t)t * c.n_cta + blockIdx.x) * kTraceWords + 13] = ck;
+      }
     }
     // ---- 3. warps 4..7: accumulator -> partial sums by column -> owners ----
     if (warp >= 4) {
@@ -340,6 +394,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
       // the TMEM loads below are warp-wide: one decision per warp
       bad = __any_sync(0xffffffffu, bad);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      stamp(7);
       float* dst = stage + (size_t)par * B * 128 + wq * 32 + lane;  // row wq * 32 + lane
       if (!bad) {
         uint32_t v[32];
@@ -357,6 +412,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
             if (b < B) dst[b * 128] = (__uint_as_float(v[b]) + __uint_as_float(v[BP + b])) * unscale;
         }
       }
+      stamp(8);
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -368,16 +424,19 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
                        smem_u32(stage + ((size_t)par * B + ob) * 128), (uint32_t)on * 512u,
                        peer_addr(smem_u32(&recv_bar[par]), (uint32_t)o));
       }
+      stamp(9);
     }
     if (__syncthreads_or(bad)) {
       aborted = true;
       break;
     }
     // ---- 4. owner: cs partials + P_t -> ReLU -> h_t ----
+    stamp(10);
     if (!wait_phase(&recv_bar[par], (uint32_t)(t >> 1) & 1u, c.timeout_ns, c.status)) {
       report_timeout(c.status, t, blockIdx.x);
       bad = true;
     }
+    stamp(11);
     if (!bad) {
       const bool publish = !(blockIdx.x == c.drop_cta && t == c.drop_step);
       const float* own = stage + ((size_t)par * B + cb0) * 128;
@@ -398,11 +457,28 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
           for (int k = 0; k < kKsplitMaxCluster; ++k) sum += part[k];
           if (publish) {
             const float out = relu(sum);
-            const size_t yo = ((size_t)t * B + cb0 + (o >> 7)) * H + row0 + (o & 127);
+            const size_t yo = (size_t)t * step_floats + ooff[u];
             st_relaxed_f(c.y + yo, out);
             if (c.y_mirror) c.y_mirror[yo] = out;
           }
         }
+      }
+    }
+    if constexpr (TR) {
+      if (tid == 128 && a.trace) {
+        stamp(12);
+        stamp_ns(16);
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        tr[0] = smid;
+        tr[1] = blockIdx.x;
+        tr[2] = (uint32_t)cs;
+        tr[3] = (uint32_t)j;
+        tr[19] = 0;
+        uint32_t* rec = a.trace + ((size_t)t * c.n_cta + blockIdx.x) * kTraceWords;
+#pragma unroll
+        for (int k = 0; k < kKsplitTraceWords; ++k)
+          if (k != 13) rec[k] = tr[k];
       }
     }
     if (tid == 0) {
@@ -446,10 +522,10 @@ size_t recur_dense_ksplit_smem(int nat, int B, int cs) {
 
 namespace {
 
-template <int BP>
+template <int BP, bool TR>
 cudaError_t launch_bp(const DenseSplitArgs& a, cudaStream_t s, bool query_only, int* clusters_fit) {
   const size_t smem = recur_dense_ksplit_smem(a.nat, a.c.B, a.cs);
-  cudaError_t e = cudaFuncSetAttribute(recur_dense_ksplit_kernel<BP>,
+  cudaError_t e = cudaFuncSetAttribute(recur_dense_ksplit_kernel<BP, TR>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -467,12 +543,12 @@ cudaError_t launch_bp(const DenseSplitArgs& a, cudaStream_t s, bool query_only, 
   cfg.attrs = at;
   if (query_only) {
     cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(clusters_fit, recur_dense_ksplit_kernel<BP>, &cfg);
+    return cudaOccupancyMaxActiveClusters(clusters_fit, recur_dense_ksplit_kernel<BP, TR>, &cfg);
   }
   // every CTA waits on CTAs of other clusters: the cooperative launch makes
   // the grid co-resident (or fails rather than run part of it)
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, recur_dense_ksplit_kernel<BP>, a);
+  return cudaLaunchKernelEx(&cfg, recur_dense_ksplit_kernel<BP, TR>, a);
 }
 
 }  // namespace
@@ -487,6 +563,7 @@ int recur_dense_ksplit_plan(int H) {
   const int nblk = H / 128;
   for (int cs = kKsplitMaxCluster; cs >= 2; --cs) {
     if (H / 16 < cs) continue;  // every slice holds at least one K step
+    if ((H / 16 + cs - 1) / cs * 16 > kKsplitMaxSlice) continue;  // one poll round per thread
     DenseSplitArgs a{};
     a.c.B = kKsplitMaxB;  // the widest batch takes the most shared memory
     a.c.n_cta = nblk * cs;
@@ -494,7 +571,7 @@ int recur_dense_ksplit_plan(int H) {
     a.nat = ksplit_nat(H, cs);
     if (recur_dense_ksplit_smem(a.nat, kKsplitMaxB, cs) > (size_t)optin) continue;
     int fit = 0;
-    if (launch_bp<32>(a, nullptr, true, &fit) != cudaSuccess) {
+    if (launch_bp<32, false>(a, nullptr, true, &fit) != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
@@ -506,11 +583,17 @@ int recur_dense_ksplit_plan(int H) {
 cudaError_t launch_recur_dense_ksplit(const DenseSplitArgs& a, cudaStream_t s) {
   const int B = a.c.B, H = a.c.H;
   if (B < 1 || B > kKsplitMaxB || H % 128 != 0 || a.cs < 2 || a.cs > kKsplitMaxCluster ||
-      a.c.n_cta != H / 128 * a.cs || a.nat != ksplit_nat(H, a.cs))
+      a.c.n_cta != H / 128 * a.cs || a.nat != ksplit_nat(H, a.cs) ||
+      (H / 16 + a.cs - 1) / a.cs * 16 > kKsplitMaxSlice)
     return cudaErrorInvalidValue;
-  if (B <= 8) return launch_bp<8>(a, s, false, nullptr);
-  if (B <= 16) return launch_bp<16>(a, s, false, nullptr);
-  return launch_bp<32>(a, s, false, nullptr);
+  if (a.trace) {
+    if (B <= 8) return launch_bp<8, true>(a, s, false, nullptr);
+    if (B <= 16) return launch_bp<16, true>(a, s, false, nullptr);
+    return launch_bp<32, true>(a, s, false, nullptr);
+  }
+  if (B <= 8) return launch_bp<8, false>(a, s, false, nullptr);
+  if (B <= 16) return launch_bp<16, false>(a, s, false, nullptr);
+  return launch_bp<32, false>(a, s, false, nullptr);
 }
 
 }  // namespace prnn

@@ -144,14 +144,36 @@ bool recur_dense_wide_plan(int H, int sm_count, size_t smem_optin, int* R, int* 
 // row m at q ^ (m & 7) (the 128-byte swizzle), columns past the slice zero;
 // nat = the widest slice's 64-column atoms.
 constexpr int kKsplitMaxCluster = 8;
+constexpr int kKsplitMaxSlice = 384;  // K columns per CTA at most (plans with wider slices are not made)
 constexpr int kKsplitMaxB = 32;
-constexpr int kKsplitMinB = 16;  // the default rule's smallest batch
+// The default rule (PRNN_OPT_DENSE_KSPLIT = 1): where the kernel measured
+// faster than the CUDA-core kernels on GB300.  Its step has a fixed cost of
+// about 3.5 us (the L2 exchange, the MMA chain, the reduction through
+// distributed shared memory), so it wins once their arithmetic per step is
+// larger: H=2304 B=8 4.7 against 5.5 us, H=1152 B=12 3.8 / 4.2, H=640 B=32
+// 4.3 / 5.9; it loses at H=1152 B=8 (4.6 / 2.4), H=1024 B=16 (3.9 / 3.2) and
+// H=512 B=32 (4.3 / 2.7).  Monotone in B.
+__host__ __device__ constexpr bool ksplit_default(int H, int B) {
+  return (H >= 2048 && B >= 8) || (H >= 1152 && B >= 12) || (H >= 640 && B >= 24);
+}
 struct DenseSplitArgs {
   RecurCommon c;
   const void* Wimg;
   const float* h0_rows;  // [B][H]: h0, or zeros
   int cs, nat;
+  uint32_t* trace;       // null, or [T][n_cta][kTraceWords] phase records (the
+                         // first 20 words of each; see kKsplitTrace*)
 };
+// Phase-trace record of the K-split kernel (one step, one CTA), words:
+// 0 SM id, 1 CTA index, 2 cluster size, 3 K slice; SM-clock stamps (low 32
+// bits) of thread 128 (the first epilogue thread) at 4 step start, 5 its own
+// polls done, 6 the CTA barrier after the fill, 7 the MMAs seen complete,
+// 8 partial sums staged, 9 copies issued, 10 the second CTA barrier, 11 the
+// peers' partial sums received, 12 publish done; 13 thread 0's clock after it
+// issued the MMAs; 14-15 globaltimer ns after the first barrier (low, high),
+// 16-17 after the publish (low, high); 18 the most re-poll rounds of thread
+// 128; 19 unused.
+constexpr int kKsplitTraceWords = 20;
 // K slice j of cs: first column k0 and width kl (multiples of 16)
 __host__ __device__ constexpr int ksplit_k0(int H, int cs, int j) { return j * (H / 16) / cs * 16; }
 __host__ __device__ constexpr int ksplit_kl(int H, int cs, int j) {

@@ -525,7 +525,7 @@ def test_phase_trace(env, spec):
     gbar = (rec[:, :, 1:1 + nw, 10] << 32) | rec[:, :, 1:1 + nw, 9]
     gpub = (rec[:, :, 1:1 + nw, 12] << 32) | rec[:, :, 1:1 + nw, 11]
     assert (gpub >= gbar).all() and (np.diff(gpub.max(axis=2), axis=0) > 0).all()
-    # a dense layer has no traced kernel
+    # a dense layer outside the K-split kernel has no traced kernel
     q = synth.make_problem(H=256, B=2, T=3, wdtype="f16", seed=85)
     lay = prnn.Layer.from_problem(q)
     try:
@@ -952,7 +952,8 @@ def test_dense_ksplit_large_values_are_scaled(env):
     p = synth.make_problem(H=512, B=16, T=6, wdtype="f16", seed=107, h0_std=2.0e5)
     ref = o.forward(p)
     assert np.abs(p.h0).max() > 32768.0 and np.abs(ref).max() > 32768.0
-    y, info = run_gpu(env, p)
+    y, info = run_gpu(env, p, options={prnn.PRNN_OPT_DENSE_KSPLIT: 2},
+                      pre_options={prnn.PRNN_OPT_DENSE_KSPLIT: 2})
     assert info["dense_ksplit"] >= 2
     check(y, ref, "f16", "ksplit, large h")
 
@@ -970,11 +971,13 @@ def test_dense_ksplit_full_size_matches_oracle(env):
 
 
 def test_dense_ksplit_default_rule(env):
-    """Option 1 (default) runs the K-split kernel for B >= 16 where it is
-    planned (H % 128 == 0, every cluster resident); 0 never; 2 for any B."""
+    """Option 1 (default) runs the K-split kernel where it measured faster
+    (H >= 2048 and B >= 8, H >= 1152 and B >= 12, H >= 640 and B >= 24) and
+    it is planned (H % 128 == 0, every cluster resident); 0 never; 2 for any B."""
     _, prnn, _ = env
-    cases = [(1152, 32, 1), (1152, 16, 1), (2304, 32, 1), (640, 24, 1), (1152, 8, 0),
-             (4096, 32, 0), (1000, 32, 0)]
+    cases = [(1152, 32, 1), (1152, 16, 1), (1152, 12, 1), (2304, 32, 1), (2304, 8, 1),
+             (640, 24, 1), (1152, 8, 0), (1024, 16, 0), (512, 32, 0), (4096, 32, 0),
+             (1000, 32, 0)]
     for H, B, want in cases:
         lay = prnn.Layer(H, H, B, "f16", "persistent")
         try:
@@ -1002,3 +1005,45 @@ def test_dense_ksplit_times_out_cleanly(env):
     lay.close()
     y, _ = run_gpu(env, p)
     check(y, o.forward(p), "f16", "after timeout")
+
+
+def test_dense_ksplit_phase_trace(env):
+    """The trace build of the K-split kernel gives the same bits, and every
+    record names its CTA, cluster size and K slice, with its stamps in step
+    order."""
+    torch, prnn, o = env
+    p = synth.make_problem(H=1152, B=32, T=8, wdtype="f16", seed=111, h0_std=0.2)
+    lay = prnn.Layer.from_problem(p)
+    try:
+        info = lay.info()
+        cs, n = info["dense_ksplit"], info["n_cta"]
+        assert cs == 8 and n == 72
+        x = torch.from_numpy(p.x).cuda()
+        h0 = torch.from_numpy(p.h0).cuda()
+        y0 = lay.forward(x, h0)
+        buf = torch.full((p.T * n * 272,), -1, dtype=torch.int32, device="cuda")
+        with pytest.raises(prnn.PrnnError) as e:  # one step short
+            prnn.prnn_set_trace_buffer(lay.h, buf, (p.T - 1) * n * 1088)
+            lay.forward(x, h0)
+        assert e.value.status == prnn.PRNN_ERR_INVALID_ARG
+        prnn.prnn_set_trace_buffer(lay.h, buf, buf.numel() * 4)
+        y1 = lay.forward(x, h0)
+        prnn.prnn_set_trace_buffer(lay.h, None, 0)
+        torch.cuda.synchronize()
+        assert lay.status() == prnn.PRNN_OK
+    finally:
+        lay.close()
+    assert torch.equal(y0, y1)
+    check(y1.cpu().numpy(), o.forward(p), "f16", "ksplit traced")
+    rec = buf.view(p.T, n, 272)[..., :20].cpu().numpy().view(np.uint32).astype(np.int64)
+    assert (rec[..., 1] == np.arange(n)[None, :]).all()
+    assert (rec[..., 2] == cs).all() and (rec[..., 3] == np.arange(n)[None, :] % cs).all()
+    assert (rec[..., 0] < info["sm_count"]).all()
+    steps = rec[..., 4:13]
+    gaps = (steps[..., 1:] - steps[..., :-1]) & 0xffffffff
+    assert (gaps < (1 << 30)).all()  # each stamp at or after the one before it (mod 2^32)
+    issue = (rec[..., 13] - rec[..., 6]) & 0xffffffff
+    assert (issue < (1 << 30)).all()  # the MMA issuer's stamp follows the first barrier
+    gbar = (rec[..., 15] << 32) | rec[..., 14]
+    gpub = (rec[..., 17] << 32) | rec[..., 16]
+    assert (gpub > gbar).all() and (gbar[1:].min(axis=1) > gpub[:-1].min(axis=1)).all()
