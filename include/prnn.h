@@ -125,8 +125,8 @@ typedef enum {
                                      hi + lo parts, about 22 bits; partial sums reduced through
                                      distributed shared memory) for forwards of B <= 32.
                                      1 = where it measured faster than the CUDA-core kernels
-                                     (default): H >= 2048 and B >= 8, H >= 1152 and B >= 12,
-                                     or H >= 640 and B >= 24; 2 = for every B <= 32; 0 =
+                                     (default): H >= 1792 and B >= 8, H >= 1152 and B >= 12,
+                                     or H >= 640 and B >= 16; 2 = for every B <= 32; 0 =
                                      never.  Its weight image is built at set_weights when
                                      the default covers max_batch or the option is 2; it
                                      takes precedence over PRNN_OPT_DENSE_WIDE                  */

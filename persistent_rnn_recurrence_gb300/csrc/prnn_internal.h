@@ -148,13 +148,13 @@ constexpr int kKsplitMaxSlice = 384;  // K columns per CTA at most (plans with w
 constexpr int kKsplitMaxB = 32;
 // The default rule (PRNN_OPT_DENSE_KSPLIT = 1): where the kernel measured
 // faster than the CUDA-core kernels on GB300.  Its step has a fixed cost of
-// about 3.5 us (the L2 exchange, the MMA chain, the reduction through
+// about 2.5 us (the L2 exchange, the MMA chain, the reduction through
 // distributed shared memory), so it wins once their arithmetic per step is
-// larger: H=2304 B=8 4.7 against 5.5 us, H=1152 B=12 3.8 / 4.2, H=640 B=32
-// 4.3 / 5.9; it loses at H=1152 B=8 (4.6 / 2.4), H=1024 B=16 (3.9 / 3.2) and
-// H=512 B=32 (4.3 / 2.7).  Monotone in B.
+// larger: H=640 B=16 2.7 against 3.1 us, H=1152 B=12 2.9 / 4.0, H=1792 B=8
+// 2.9 / 4.4; it loses at H=512 B=32 (2.9 / 2.7), H=1152 B=8 (2.7 / 2.2) and
+// H=2304 B=4 (3.2 / 3.0).  Monotone in B.
 __host__ __device__ constexpr bool ksplit_default(int H, int B) {
-  return (H >= 2048 && B >= 8) || (H >= 1152 && B >= 12) || (H >= 640 && B >= 24);
+  return (H >= 1792 && B >= 8) || (H >= 1152 && B >= 12) || (H >= 640 && B >= 16);
 }
 struct DenseSplitArgs {
   RecurCommon c;

@@ -972,12 +972,12 @@ def test_dense_ksplit_full_size_matches_oracle(env):
 
 def test_dense_ksplit_default_rule(env):
     """Option 1 (default) runs the K-split kernel where it measured faster
-    (H >= 2048 and B >= 8, H >= 1152 and B >= 12, H >= 640 and B >= 24) and
+    (H >= 1792 and B >= 8, H >= 1152 and B >= 12, H >= 640 and B >= 16) and
     it is planned (H % 128 == 0, every cluster resident); 0 never; 2 for any B."""
     _, prnn, _ = env
     cases = [(1152, 32, 1), (1152, 16, 1), (1152, 12, 1), (2304, 32, 1), (2304, 8, 1),
-             (640, 24, 1), (1152, 8, 0), (1024, 16, 0), (512, 32, 0), (4096, 32, 0),
-             (1000, 32, 0)]
+             (1792, 8, 1), (640, 16, 1), (1024, 16, 1), (1152, 8, 0), (1536, 8, 0),
+             (640, 12, 0), (512, 32, 0), (2304, 4, 0), (4096, 32, 0), (1000, 32, 0)]
     for H, B, want in cases:
         lay = prnn.Layer(H, H, B, "f16", "persistent")
         try:
