@@ -656,9 +656,12 @@ def run_sweep(args):
                           "timesteps_per_s": 1e3 * p.T / (rec + proj),
                           "status": prnn.prnn_status_string(st),
                           "groups": info["cta_groups"], "n_cta": info["n_cta"]}
-            if p.sparse and algo == "persistent":
-                # the sparse gathers' shared-memory bound: every entry x batch
-                # column reads its own 4-byte h word, plus the 4-byte entries
+            if algo == "persistent":
+                line[algo]["kernel"] = ("ksplit" if info["dense_ksplit"]
+                                        else "sparse" if p.sparse else "dense")
+            if p.sparse and algo == "persistent" and not info["dense_ksplit"]:
+                # the sparse kernel's gathers' shared-memory bound: every entry x
+                # batch column reads its own 4-byte h word, plus the 4-byte entries
                 smem_bw = (info["sm_count"] or 152) * 128 * \
                     load_peaks().get("sm_max_mhz", 2070.0) * 1e6
                 t_smem = (4.0 * p.nnz * p.B + 4.0 * p.nnz) / smem_bw

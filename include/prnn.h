@@ -117,7 +117,7 @@ typedef enum {
                                      H >= 1024, or B >= 16 with H >= 2048 (default); 2 = for
                                      every B >= 16; 0 = never.  Takes effect at the next
                                      forward                                                    */
-  PRNN_OPT_DENSE_KSPLIT = 16      /* dense fp16 persistent, flags in the data, H % 128 == 0 and
+  PRNN_OPT_DENSE_KSPLIT = 16,     /* dense fp16 persistent, flags in the data, H % 128 == 0 and
                                      all H / 128 clusters of 2 .. 8 CTAs resident at once, one
                                      CTA per SM (on 152 SMs: clusters of 8 up to H = 1920, of
                                      6 up to 2304): the tensor-core kernel that splits each
@@ -130,6 +130,15 @@ typedef enum {
                                      never.  Its weight image is built at set_weights when
                                      the default covers max_batch or the option is 2; it
                                      takes precedence over PRNN_OPT_DENSE_WIDE                  */
+  PRNN_OPT_SPARSE_KSPLIT = 17     /* sparse persistent, flags in the data: run the layer's
+                                     densified matrix (fp16, the same values) on the
+                                     K-split kernel of PRNN_OPT_DENSE_KSPLIT for forwards
+                                     of B <= 32.  1 = where it measured faster than the
+                                     sparse kernel (default): H >= 1536, the dense rule of
+                                     PRNN_OPT_DENSE_KSPLIT, and (stored entries / H) x B
+                                     >= 4096; 2 = for every B <= 32; 0 = never.
+                                     Its image is built at set_weights when the default
+                                     covers max_batch or the option is 2                     */
 } prnn_option_t;
 
 /* Plan and sizes chosen at create / set_weights time (read-only report). */
@@ -152,8 +161,9 @@ typedef struct {
   int dense_wide_batch;            /* dense: 1 if the forward at max_batch runs the
                                       wide-batch kernel (PRNN_OPT_DENSE_WIDE); the plan
                                       fields above then describe that kernel's launch       */
-  int dense_ksplit;                /* dense: if the forward at max_batch runs the
-                                      tensor-core K-split kernel (PRNN_OPT_DENSE_KSPLIT),
+  int dense_ksplit;                /* if the forward at max_batch runs the tensor-core
+                                      K-split kernel (PRNN_OPT_DENSE_KSPLIT; a sparse
+                                      layer's densified matrix: PRNN_OPT_SPARSE_KSPLIT),
                                       its cluster size (2 .. 8), else 0; the plan fields
                                       above then describe its launch (rows_per_cta: the
                                       128 rows of a cluster)                                */

@@ -43,6 +43,8 @@ struct prnn_handle {
   // dense fp16 for wide batches on the tensor cores, K split in clusters:
   // its plan and weight image
   int ks_opt = 1;
+  int sks_opt = 1;    // sparse layers on the K-split kernel (their densified matrix)
+  size_t ks_nnz = 0;  // sparse: stored entries behind the K-split image
   bool ks = false;
   int ks_cs = 0, ks_nat = 0;
   void* Wimg_ks = nullptr;
@@ -455,6 +457,7 @@ void free_weights(prnn_handle* h) {
   h->rtc = false;
   free_dev(h->Wpk_wide);
   free_dev(h->Wimg_ks);
+  h->ks = false;
   free_dev(h->zeros);
   h->wide = false;
   free_dev(h->cols_pad);
@@ -565,6 +568,41 @@ static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
 // compressed-row entry points.
 // caller_pos[r*k + j] is the index of padded entry (r, j) in the caller's
 // value array, -1 for padding.
+// The K-split kernel's weight image from Wh as fp16 [H][H] (row-major), if
+// the device can hold the plan: per CTA (cluster-major, then K slice j) nat
+// atoms of 128 rows x 64 columns, 16-byte chunk q of row m at q ^ (m & 7)
+// (the 128-byte swizzle of the K-major MMA operand).  Sets h->ks.
+static prnn_status_t install_ksplit(prnn_t h, const uint16_t* w16) {
+  const int H = h->H;
+  const int kcs = recur_dense_ksplit_plan(H);
+  if (kcs == 0) return PRNN_OK;
+  const int nblk = H / 128, knat = ksplit_nat(H, kcs);
+  std::vector<uint16_t> img((size_t)nblk * kcs * knat * 128 * 64, 0);
+  for (int bk = 0; bk < nblk; ++bk)
+    for (int j = 0; j < kcs; ++j) {
+      const int k0 = ksplit_k0(H, kcs, j), kl = ksplit_kl(H, kcs, j);
+      for (int at = 0; at < knat; ++at)
+        for (int m = 0; m < 128; ++m)
+          for (int q = 0; q < 8; ++q)
+            for (int e = 0; e < 8; ++e) {
+              const int kcol = at * 64 + q * 8 + e;  // column within the slice
+              if (kcol >= kl) continue;
+              const size_t atom = ((size_t)bk * kcs + j) * knat + at;
+              img[atom * 128 * 64 + (size_t)m * 64 + ((q ^ (m & 7)) * 8) + e] =
+                  w16[(size_t)(bk * 128 + m) * H + k0 + kcol];
+            }
+    }
+  PRNN_TRY(upload(&h->Wimg_ks, img.data(), img.size() * 2));
+  if (!h->zeros) {
+    std::vector<float> z((size_t)h->maxB * H, 0.f);
+    PRNN_TRY(upload(&h->zeros, z.data(), z.size() * sizeof(float)));
+  }
+  h->ks = true;
+  h->ks_cs = kcs;
+  h->ks_nat = knat;
+  return PRNN_OK;
+}
+
 static prnn_status_t install_sparse(prnn_t h, const void* Wx, const float* bias,
                                     std::vector<uint16_t>& hv, std::vector<uint16_t>& hc, int k,
                                     const std::vector<int32_t>& caller_pos) {
@@ -649,6 +687,21 @@ static prnn_status_t install_sparse(prnn_t h, const void* Wx, const float* bias,
       size_t n = 0;
       for (int32_t p : caller_pos) n += p >= 0 ? 1 : 0;
       h->n_caller = n;
+    }
+    // wide batches: the densified matrix on the K-split kernel, where that
+    // measured faster than the sparse kernel (its gathers are bound by
+    // shared memory at wide batch)
+    size_t nnz = 0;
+    for (int32_t p : caller_pos) nnz += p >= 0 ? 1 : 0;
+    if (h->sks_opt == 2 || (h->sks_opt == 1 && ksplit_sparse_default(H, nnz, h->maxB))) {
+      std::vector<uint16_t> dense((size_t)H * H, 0);
+      for (int r = 0; r < H; ++r)
+        for (int j = 0; j < k; ++j)
+          if (caller_pos[(size_t)r * k + j] >= 0)
+            dense[(size_t)r * H + hc[(size_t)r * k + j]] = hv[(size_t)r * k + j];
+      const prnn_status_t kst = install_ksplit(h, dense.data());
+      if (kst != PRNN_OK) return kst;
+      h->ks_nnz = nnz;
     }
   } else {
     std::vector<uint32_t> ws((size_t)H * k);
@@ -842,38 +895,10 @@ prnn_status_t prnn_set_weights_dense(prnn_t h, const void* Wx, const void* Wh,
       h->w_depth = wD;
       h->w_smem = wsm;
     }
-    // wide batches on the tensor cores: per CTA (cluster-major, then K slice
-    // j) nat atoms of 128 rows x 64 columns, 16-byte chunk q of row m at
-    // q ^ (m & 7) (the 128-byte swizzle of the K-major MMA operand)
-    const int kcs = h->wdtype == PRNN_F16 && (ksplit_default(H, h->maxB) || h->ks_opt == 2)
-                        ? recur_dense_ksplit_plan(H)
-                        : 0;
-    if (kcs > 0) {
-      const int nblk = H / 128, knat = ksplit_nat(H, kcs);
-      const uint16_t* w16 = reinterpret_cast<const uint16_t*>(wh.data());
-      std::vector<uint16_t> img((size_t)nblk * kcs * knat * 128 * 64, 0);
-      for (int bk = 0; bk < nblk; ++bk)
-        for (int j = 0; j < kcs; ++j) {
-          const int k0 = ksplit_k0(H, kcs, j), kl = ksplit_kl(H, kcs, j);
-          for (int at = 0; at < knat; ++at)
-            for (int m = 0; m < 128; ++m)
-              for (int q = 0; q < 8; ++q)
-                for (int e = 0; e < 8; ++e) {
-                  const int kcol = at * 64 + q * 8 + e;  // column within the slice
-                  if (kcol >= kl) continue;
-                  const size_t atom = ((size_t)bk * kcs + j) * knat + at;
-                  img[atom * 128 * 64 + (size_t)m * 64 + ((q ^ (m & 7)) * 8) + e] =
-                      w16[(size_t)(bk * 128 + m) * H + k0 + kcol];
-                }
-        }
-      PRNN_TRY(upload(&h->Wimg_ks, img.data(), img.size() * 2));
-      if (!h->zeros) {
-        std::vector<float> z((size_t)h->maxB * H, 0.f);
-        PRNN_TRY(upload(&h->zeros, z.data(), z.size() * sizeof(float)));
-      }
-      h->ks = true;
-      h->ks_cs = kcs;
-      h->ks_nat = knat;
+    // wide batches on the tensor cores (the K-split kernel)
+    if (h->wdtype == PRNN_F16 && (ksplit_default(H, h->maxB) || h->ks_opt == 2)) {
+      const prnn_status_t kst = install_ksplit(h, reinterpret_cast<const uint16_t*>(wh.data()));
+      if (kst != PRNN_OK) return kst;
     }
     h->n_cta = plan.n_cta;
     h->R = plan.R;
@@ -1008,13 +1033,15 @@ static bool dense_wide_for(const prnn_t h, int B) {
   return h->wide_opt == 2 || (passes >= 3 ? h->H >= 1024 : h->H >= 2048);
 }
 
-// Whether a dense persistent forward of B columns runs the tensor-core
-// K-split kernel: planned at set_weights, enabled, flags in the data, B <= 32,
-// and by default only where it measured faster (ksplit_default).
-static bool dense_ksplit_for(const prnn_t h, int B) {
-  if (h->algo != PRNN_ALGO_PERSISTENT || h->sparse || !h->ks || h->ks_opt == 0 ||
-      h->sync_mode != 0 || h->rtc || B < 1 || B > kKsplitMaxB)
+// Whether a persistent forward of B columns runs the tensor-core K-split
+// kernel: planned at set_weights, enabled, flags in the data, B <= 32, and by
+// default only where it measured faster (ksplit_default for dense layers,
+// ksplit_sparse_default for sparse ones, which run their densified matrix).
+static bool ksplit_for(const prnn_t h, int B) {
+  if (h->algo != PRNN_ALGO_PERSISTENT || !h->ks || h->sync_mode != 0 || B < 1 || B > kKsplitMaxB)
     return false;
+  if (h->sparse) return h->sks_opt == 2 || (h->sks_opt == 1 && ksplit_sparse_default(h->H, h->ks_nnz, B));
+  if (h->ks_opt == 0 || h->rtc) return false;
   return h->ks_opt == 2 || ksplit_default(h->H, B);
 }
 
@@ -1031,7 +1058,7 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
                                   float* y, float* y_mirror, cudaStream_t s) {
   if (h->trace) {  // the phase trace: sparse persistent kernel (column order, wide
                    // staging) or the dense K-split kernel
-    const bool ks = dense_ksplit_for(h, B);
+    const bool ks = ksplit_for(h, B);
     if (!ks && (h->algo != PRNN_ALGO_PERSISTENT || !h->sparse || h->place || !h->wide_loads))
       return PRNN_ERR_UNSUPPORTED;
     const size_t n_cta = ks ? (size_t)(h->H / 128 * h->ks_cs) : (size_t)h->n_cta;
@@ -1060,7 +1087,17 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
     RecurCommon c = common_args(h, T, B, h0, y);
     c.y_mirror = y_mirror;
     if (h->sync_mode == 1) PRNN_TRY(cudaMemsetAsync(h->bar, 0, sizeof(unsigned), s));
-    if (h->sparse) {
+    if (ksplit_for(h, B)) {  // dense, or a sparse layer's densified matrix
+      c.n_cta = h->H / 128 * h->ks_cs;
+      c.R = 128;
+      c.cpg = c.n_cta;
+      c.G = 1;
+      c.nthreads = 256;
+      c.smem = recur_dense_ksplit_smem(h->ks_nat, B, h->ks_cs);
+      if (h->poll_delay_ns < 0) c.poll_delay = 0;  // measured: no pause is fastest here
+      DenseSplitArgs a{c, h->Wimg_ks, h0 ? h0 : h->zeros, h->ks_cs, h->ks_nat, h->trace};
+      PRNN_TRY(launch_recur_dense_ksplit(a, s));
+    } else if (h->sparse) {
       SparseRecurArgs a{};
       int bg = 4;
       bool db = false;
@@ -1093,16 +1130,6 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
       a.nslices = h->H / 64;
       a.nring = h->t_ring;
       PRNN_TRY(launch_recur_dense_tc(a, s));
-    } else if (dense_ksplit_for(h, B)) {
-      c.n_cta = h->H / 128 * h->ks_cs;
-      c.R = 128;
-      c.cpg = c.n_cta;
-      c.G = 1;
-      c.nthreads = 256;
-      c.smem = recur_dense_ksplit_smem(h->ks_nat, B, h->ks_cs);
-      if (h->poll_delay_ns < 0) c.poll_delay = 0;  // measured: no pause is fastest here
-      DenseSplitArgs a{c, h->Wimg_ks, h0 ? h0 : h->zeros, h->ks_cs, h->ks_nat, h->trace};
-      PRNN_TRY(launch_recur_dense_ksplit(a, s));
     } else if (dense_wide_for(h, B)) {
       c.R = h->w_R;
       c.cpg = (h->H + h->w_R - 1) / h->w_R;
@@ -1500,6 +1527,10 @@ prnn_status_t prnn_set_option(prnn_t h, prnn_option_t opt, long long value) {
       if (value < 0 || value > 2) return PRNN_ERR_INVALID_ARG;
       h->ks_opt = (int)value;
       return PRNN_OK;
+    case PRNN_OPT_SPARSE_KSPLIT:
+      if (value < 0 || value > 2) return PRNN_ERR_INVALID_ARG;
+      h->sks_opt = (int)value;
+      return PRNN_OK;
   }
   return PRNN_ERR_INVALID_ARG;
 }
@@ -1539,7 +1570,7 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
             ? 1
             : 0;
   }
-  if (h->weights_set && dense_ksplit_for(h, h->maxB)) {
+  if (h->weights_set && ksplit_for(h, h->maxB)) {
     info->dense_ksplit = h->ks_cs;
     info->n_cta = h->H / 128 * h->ks_cs;
     info->rows_per_cta = 128;

@@ -156,6 +156,17 @@ constexpr int kKsplitMaxB = 32;
 __host__ __device__ constexpr bool ksplit_default(int H, int B) {
   return (H >= 1792 && B >= 8) || (H >= 1152 && B >= 12) || (H >= 640 && B >= 16);
 }
+// Sparse layers run their densified matrix on the K-split kernel by default
+// (PRNN_OPT_SPARSE_KSPLIT = 1) where that measured faster than the sparse
+// kernel, whose gathers are bound by shared memory at wide batch: from about
+// 4096 entries per row x batch column at H >= 1536 (H=2304 25 % B=32 4.5
+// against 9.9 us, 10 % B=32 4.5 / 6.2, H=2048 25 % B=8 2.9 / 4.7, H=1536 10 %
+// B=32 3.6 / 4.0); the sparse kernel stays faster at 5 % (H=2304 B=32 4.3 /
+// 4.5), below that product (H=2048 10 % B=16 3.2 / 3.4) and at H=1152
+// (25 % B=32 3.3 / 3.4).  Monotone in B.
+__host__ __device__ constexpr bool ksplit_sparse_default(int H, size_t nnz, int B) {
+  return ksplit_default(H, B) && H >= 1536 && nnz * (size_t)B >= (size_t)4096 * H;
+}
 struct DenseSplitArgs {
   RecurCommon c;
   const void* Wimg;

@@ -30,7 +30,7 @@ PRNN_ALGO_PERSISTENT, PRNN_ALGO_PER_STEP = 0, 1
  PRNN_OPT_WIDE_LOADS, PRNN_OPT_BANK_AWARE, PRNN_OPT_POLL_DELAY_NS,
  PRNN_OPT_POLL_BACKOFF_NS, PRNN_OPT_RECURRENT_TC, PRNN_OPT_STAGED_ORDER,
  PRNN_OPT_SPARSE_REG_WEIGHTS, PRNN_OPT_SPARSE_STAGING_DEPTH, PRNN_OPT_DENSE_WIDE,
- PRNN_OPT_DENSE_KSPLIT) = range(17)
+ PRNN_OPT_DENSE_KSPLIT, PRNN_OPT_SPARSE_KSPLIT) = range(18)
 
 PRNN_STACK_WAVEFRONT, PRNN_STACK_LAYERWISE = 0, 1
 

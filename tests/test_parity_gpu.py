@@ -1047,3 +1047,64 @@ def test_dense_ksplit_phase_trace(env):
     gbar = (rec[..., 15] << 32) | rec[..., 14]
     gpub = (rec[..., 17] << 32) | rec[..., 16]
     assert (gpub > gbar).all() and (gbar[1:].min(axis=1) > gpub[:-1].min(axis=1)).all()
+
+
+SPARSE_KSPLIT = [dict(H=2304, B=32, T=16, k=576, h0_std=0.2),   # 25 %: the default there
+                 dict(H=1152, B=20, T=20, k=115),
+                 dict(H=640, I=200, B=17, T=12, k=64, h0_std=0.5),
+                 dict(H=256, B=3, T=10, k=20)]
+
+
+@pytest.mark.parametrize("spec", SPARSE_KSPLIT)
+def test_sparse_layer_on_ksplit_matches_oracle(env, spec):
+    """A sparse layer's densified matrix on the K-split kernel (forced on)
+    stays within the rule and within it of the sparse kernel."""
+    _, prnn, o = env
+    p = synth.make_problem(seed=112, **spec)
+    ref = o.forward(p)
+    y, info = run_gpu(env, p, options={prnn.PRNN_OPT_SPARSE_KSPLIT: 2},
+                      pre_options={prnn.PRNN_OPT_SPARSE_KSPLIT: 2})
+    assert info["sparse"] == 1 and info["dense_ksplit"] >= 2
+    check(y, ref, "f16", f"sparse on ksplit {spec}")
+    y_sp, info_sp = run_gpu(env, p, options={prnn.PRNN_OPT_SPARSE_KSPLIT: 0},
+                            pre_options={prnn.PRNN_OPT_SPARSE_KSPLIT: 0})
+    assert info_sp["dense_ksplit"] == 0
+    assert np.abs(y - y_sp).max() <= TOL["f16"] * float(np.abs(ref).max())
+
+
+def test_csr_layer_on_ksplit_matches_oracle(env):
+    """An unbalanced (CSR) layer's densified matrix on the K-split kernel."""
+    torch, prnn, o = env
+    p, _ = synth.make_pruned_pair(H=1152, B=16, T=12, density=0.10, seed=113)
+    lay = prnn.Layer(p.H, p.I, p.B, "f16", "persistent")
+    try:
+        lay.set_option(prnn.PRNN_OPT_SPARSE_KSPLIT, 2)
+        lay.set_problem_weights(p)
+        assert lay.info()["dense_ksplit"] >= 2
+        y = lay.forward(torch.from_numpy(p.x).cuda())
+        torch.cuda.synchronize()
+        assert lay.status() == prnn.PRNN_OK
+    finally:
+        lay.close()
+    check(y.cpu().numpy(), o.forward(p), "f16", "csr on ksplit")
+
+
+def test_sparse_ksplit_default_rule(env):
+    """Option 1 (default) runs a sparse layer's densified matrix on the
+    K-split kernel at H >= 1536 where (entries per row) x B >= 4096 and the
+    dense rule holds; 0 never; 3 is refused."""
+    _, prnn, _ = env
+    cases = [(2304, 0.25, 32, 1), (2304, 0.10, 32, 1), (2304, 0.25, 8, 1), (2048, 0.10, 32, 1),
+             (2304, 0.05, 32, 0), (2304, 0.10, 16, 0), (1152, 0.25, 32, 0), (2304, 0.25, 4, 0)]
+    for H, d, B, want in cases:
+        p = synth.make_problem(H=H, B=B, T=1, k=synth.sparse_k(H, d), seed=114)
+        lay = prnn.Layer(H, H, B, "f16", "persistent")
+        try:
+            lay.set_problem_weights(p)
+            assert (lay.info()["dense_ksplit"] > 0) == bool(want), (H, d, B)
+            lay.set_option(prnn.PRNN_OPT_SPARSE_KSPLIT, 0)
+            assert lay.info()["dense_ksplit"] == 0
+            with pytest.raises(prnn.PrnnError):
+                lay.set_option(prnn.PRNN_OPT_SPARSE_KSPLIT, 3)
+        finally:
+            lay.close()
