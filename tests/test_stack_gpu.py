@@ -179,3 +179,13 @@ def test_stack_dropped_publish_times_out_cleanly(env):
     st.close()
     y, _ = run_stack(env, p, "wavefront")
     check_layers(y, o.forward(p), "f16", "after timeout")
+
+
+def test_layerwise_stack_at_wide_batch(env):
+    """A layer-by-layer stack at a wide batch: each dense fp16 layer's
+    forward runs the tensor-core K-split kernel (the single-layer default at
+    H=1152, B=16), and every layer matches the oracle."""
+    _, _, o = env
+    p = synth.make_stack_problem(L=2, H=1152, B=16, T=10, wdtype="f16", seed=425, h0_std=0.2)
+    y, _ = run_stack(env, p, "layerwise")
+    check_layers(y, o.forward(p), "f16", "layerwise stack, wide batch")
