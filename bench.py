@@ -870,10 +870,22 @@ def run_stack(args):
     return 0
 
 
+def problem_by_name(name, T=None):
+    """A named workload, or a point of the sweep by its name (sweep_h..._b..._d...)."""
+    from persistent_rnn_recurrence_gb300 import synth
+    if name.startswith("sweep_"):
+        kw = dict(synth.sweep_points())[name]
+        if T is not None:
+            kw = {**kw, "T": T}
+        return synth.make_problem(name=name, **kw)
+    return synth.named_problem(name, T=T)
+
+
 def run_backward(args):
     """Training-step timing (forward + backward through time) for the named
-    workloads at T = 256: the forward, the reverse recurrence and the batched
-    gradient products, CUDA events, L2 flushed before every step."""
+    workloads and two wide-batch sweep points at T = 256: the forward, the
+    reverse recurrence and the batched gradient products, CUDA events, L2
+    flushed before every step."""
     import numpy as np
     import torch
     from persistent_rnn_recurrence_gb300 import prnn, synth
@@ -882,9 +894,11 @@ def run_backward(args):
     reps = max(5, min(args.steps, 20))
     out = []
     for name in ("sparse_f16_h1792_d10_b4_t256", "dense_f16_h1152_b4_t256",
-                 "sparse_f16_h5760_d1_b4_t256", "sparse_f16_h5760_d5_b4_t256"):
-        p = synth.named_problem(name)
+                 "sparse_f16_h5760_d1_b4_t256", "sparse_f16_h5760_d5_b4_t256",
+                 "sweep_h1152_b32_d100", "sweep_h2304_b32_d100"):
+        p = problem_by_name(name)
         lay = prnn.Layer.from_problem(p)
+        kernel = "ksplit" if lay.info()["dense_ksplit"] else ("sparse" if p.sparse else "dense")
         lay.set_option(prnn.PRNN_OPT_TIMING, 1)
         x = torch.from_numpy(p.x).to(dev)
         h0 = None if p.h0 is None else torch.from_numpy(p.h0).to(dev)
@@ -911,7 +925,8 @@ def run_backward(args):
         assert lay.status() == prnn.PRNN_OK
         lay.close()
         med = lambda v: sorted(v)[len(v) // 2]
-        out.append({"workload": name, "ms_train_step": med(tot), "ms_forward": med(fwd),
+        out.append({"workload": name, "recurrent_kernel": kernel,
+                    "ms_train_step": med(tot), "ms_forward": med(fwd),
                     "ms_reverse_recurrence": med(rev), "ms_gradient_products": med(prod),
                     "us_per_step_reverse": 1e3 * med(rev) / p.T,
                     "train_timesteps_per_s": p.T / (med(tot) * 1e-3)})
@@ -1157,11 +1172,7 @@ def run_trace(args):
     import torch
     from persistent_rnn_recurrence_gb300 import prnn, synth
     dev = torch.device("cuda", 0)
-    if args.config.startswith("sweep_"):  # a point of the sweep, by name
-        kw = dict(synth.sweep_points())[args.config]
-        p = synth.make_problem(name=args.config, **{**kw, "T": args.trace_steps})
-    else:
-        p = synth.named_problem(args.config, T=args.trace_steps)
+    p = problem_by_name(args.config, T=args.trace_steps)
     if not p.sparse:
         return run_trace_ksplit(args, p)
     lay = prnn.Layer.from_problem(p)

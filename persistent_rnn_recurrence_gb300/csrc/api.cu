@@ -48,6 +48,7 @@ struct prnn_handle {
   bool ks = false;
   int ks_cs = 0, ks_nat = 0;
   void* Wimg_ks = nullptr;
+  void* WimgT_ks = nullptr;  // the same for Wh^T (the backward's reverse recurrence)
   // tensor-core dense recurrence (wide batch): its own plan and weight image
   int rtc_opt = 1;  // the tensor-core recurrence is opt-in (slower than the CUDA cores so far)
   bool rtc = false;
@@ -457,6 +458,7 @@ void free_weights(prnn_handle* h) {
   h->rtc = false;
   free_dev(h->Wpk_wide);
   free_dev(h->Wimg_ks);
+  free_dev(h->WimgT_ks);
   h->ks = false;
   free_dev(h->zeros);
   h->wide = false;
@@ -568,31 +570,35 @@ static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
 // compressed-row entry points.
 // caller_pos[r*k + j] is the index of padded entry (r, j) in the caller's
 // value array, -1 for padding.
-// The K-split kernel's weight image from Wh as fp16 [H][H] (row-major), if
-// the device can hold the plan: per CTA (cluster-major, then K slice j) nat
-// atoms of 128 rows x 64 columns, 16-byte chunk q of row m at q ^ (m & 7)
-// (the 128-byte swizzle of the K-major MMA operand).  Sets h->ks.
+// The K-split kernel's weight images from Wh as fp16 [H][H] (row-major), if
+// the device can hold the plan: for Wh and for Wh^T (the backward's reverse
+// recurrence), per CTA (cluster-major, then K slice j) nat atoms of 128 rows x
+// 64 columns, 16-byte chunk q of row m at q ^ (m & 7) (the 128-byte swizzle of
+// the K-major MMA operand).  Sets h->ks.
 static prnn_status_t install_ksplit(prnn_t h, const uint16_t* w16) {
   const int H = h->H;
   const int kcs = recur_dense_ksplit_plan(H);
   if (kcs == 0) return PRNN_OK;
   const int nblk = H / 128, knat = ksplit_nat(H, kcs);
   std::vector<uint16_t> img((size_t)nblk * kcs * knat * 128 * 64, 0);
-  for (int bk = 0; bk < nblk; ++bk)
-    for (int j = 0; j < kcs; ++j) {
-      const int k0 = ksplit_k0(H, kcs, j), kl = ksplit_kl(H, kcs, j);
-      for (int at = 0; at < knat; ++at)
-        for (int m = 0; m < 128; ++m)
-          for (int q = 0; q < 8; ++q)
-            for (int e = 0; e < 8; ++e) {
-              const int kcol = at * 64 + q * 8 + e;  // column within the slice
-              if (kcol >= kl) continue;
-              const size_t atom = ((size_t)bk * kcs + j) * knat + at;
-              img[atom * 128 * 64 + (size_t)m * 64 + ((q ^ (m & 7)) * 8) + e] =
-                  w16[(size_t)(bk * 128 + m) * H + k0 + kcol];
-            }
-    }
-  PRNN_TRY(upload(&h->Wimg_ks, img.data(), img.size() * 2));
+  for (int tr = 0; tr < 2; ++tr) {  // Wh, then Wh^T
+    for (int bk = 0; bk < nblk; ++bk)
+      for (int j = 0; j < kcs; ++j) {
+        const int k0 = ksplit_k0(H, kcs, j), kl = ksplit_kl(H, kcs, j);
+        for (int at = 0; at < knat; ++at)
+          for (int m = 0; m < 128; ++m)
+            for (int q = 0; q < 8; ++q)
+              for (int e = 0; e < 8; ++e) {
+                const int kcol = at * 64 + q * 8 + e;  // column within the slice
+                if (kcol >= kl) continue;
+                const size_t atom = ((size_t)bk * kcs + j) * knat + at;
+                const size_t r = (size_t)(bk * 128 + m), cc = (size_t)(k0 + kcol);
+                img[atom * 128 * 64 + (size_t)m * 64 + ((q ^ (m & 7)) * 8) + e] =
+                    tr ? w16[cc * H + r] : w16[r * H + cc];
+              }
+      }
+    PRNN_TRY(upload(tr ? &h->WimgT_ks : &h->Wimg_ks, img.data(), img.size() * 2));
+  }
   if (!h->zeros) {
     std::vector<float> z((size_t)h->maxB * H, 0.f);
     PRNN_TRY(upload(&h->zeros, z.data(), z.size() * sizeof(float)));
@@ -1325,7 +1331,17 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
   c.reverse = 1;
   c.p_masked = 1;
   c.sync_mode = 0;
-  if (h->sparse) {  // Wh^T has its own plan (its rows are Wh's columns)
+  if (ksplit_for(h, B) && h->WimgT_ks) {  // wide batch: Wh^T on the K-split kernel
+    c.n_cta = h->H / 128 * h->ks_cs;
+    c.R = 128;
+    c.cpg = c.n_cta;
+    c.G = 1;
+    c.nthreads = 256;
+    c.smem = recur_dense_ksplit_smem(h->ks_nat, B, h->ks_cs);
+    if (h->poll_delay_ns < 0) c.poll_delay = 0;
+    DenseSplitArgs a{c, h->WimgT_ks, h->zeros, h->ks_cs, h->ks_nat, nullptr};
+    PRNN_TRY(launch_recur_dense_ksplit(a, s));
+  } else if (h->sparse) {  // Wh^T has its own plan (its rows are Wh's columns)
     c.n_cta = h->b_n_cta;
     c.R = h->b_R;
     c.G = h->b_G;

@@ -272,7 +272,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
     for (int u = 0; u < kOutMax; ++u)
       pn[u] = tid + u * kSplitThreads < nout ? ld_nc_pinned(pt + ooff[u]) : 0.f;
   };
-  if (T > 0) load_p(0);
+  // Reverse mode (the backward pass): steps run T-1 .. 0, the previous
+  // step's h is y[ts + 1] (the deltas), P is the masked dy, and the output
+  // is P + sum, or 0 where P holds the mask marker
+  const bool rev = c.reverse != 0;
+  if (T > 0) load_p(rev ? T - 1 : 0);
   bool bad = false;       // this thread saw a failed wait
   bool aborted = false;   // uniform: the CTA left the step loop early
   int last_mma = -1;      // thread 0: the last step whose MMAs it issued
@@ -289,14 +293,15 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
   };
   for (int t = 0; t < T; ++t) {
     const int par = t & 1;
+    const int ts = rev ? T - 1 - t : t;  // the step computed (t counts the steps done)
     stamp(4);
     w.new_step();
     float pv[kOutMax];
 #pragma unroll
     for (int u = 0; u < kOutMax; ++u) pv[u] = pn[u];
-    if (t + 1 < T) load_p(t + 1);
+    if (t + 1 < T) load_p(rev ? ts - 1 : ts + 1);
     // ---- 1. h_{t-1} of the slice -> hi / lo fp16 in the B operand ----
-    const float* src = (t == 0 ? a.h0_rows : c.y + (size_t)(t - 1) * B * H) + k0;
+    const float* src = (t == 0 ? a.h0_rows : c.y + (size_t)(rev ? ts + 1 : ts - 1) * B * H) + k0;
     const bool poll = t > 0;
     if (poll) spin_cycles(c.poll_delay);
     bool large = false;
@@ -489,8 +494,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
 #pragma unroll
           for (int k = 0; k < kKsplitMaxCluster; ++k) sum += part[k];
           if (publish) {
-            const float out = relu(sum);
-            const size_t yo = (size_t)t * step_floats + ooff[u];
+            const float out =
+                c.p_masked ? (__float_as_uint(pv[u]) == kMaskedMarker ? 0.f : sum) : relu(sum);
+            const size_t yo = (size_t)ts * step_floats + ooff[u];
             st_relaxed_f(c.y + yo, out);
             if (c.y_mirror) c.y_mirror[yo] = out;
           }

@@ -384,3 +384,43 @@ def test_tensor_core_gradients_match_cuda_core(env, spec):
         assert rel_err(g_tc[k], g_cc[k]) <= 1e-2, (k, rel_err(g_tc[k], g_cc[k]))
     for k in ("delta", "db", "dh0"):
         assert np.array_equal(g_tc[k], g_cc[k]), k
+
+
+@pytest.mark.parametrize("kind", ["dense", "sparse", "csr"])
+def test_ksplit_backward_exact_problems(env, kind):
+    """At a wide batch the forward and the backward's reverse recurrence run
+    on the tensor-core K-split kernel (Wh, then Wh^T; a sparse or CSR layer's
+    densified matrix when forced on). On dyadic problems every h and delta
+    splits exactly into fp16 hi + lo and every fp32 sum is exact, so the
+    forward equals the oracle's bit for bit and delta, db, dh0 match the
+    oracle's gradients within 1e-6 (the bf16 products within their bound)."""
+    torch, prnn, o = env
+    shape = dict(H=1152, I=1152, B=16, T=6)
+    if kind == "dense":
+        p, dy = dyadic_problem(960, wdtype="f16", **shape)
+        opts = {}
+    else:
+        p, dy = dyadic_sparse_problem(961, k=3, csr=kind == "csr", **shape)
+        opts = {prnn.PRNN_OPT_SPARSE_KSPLIT: 2}
+    lay = prnn.Layer(p.H, p.I, p.B, p.wdtype, "persistent")
+    try:
+        for k, v in opts.items():
+            lay.set_option(k, v)
+        lay.set_problem_weights(p)
+        assert lay.info()["dense_ksplit"] == 8  # H=1152: clusters of 8
+    finally:
+        lay.close()
+    y, g = run(env, p, dy.astype(np.float32), options=opts or None, pre_options=opts or None)
+    assert np.array_equal(y, o.forward(p)), "forward not exact: masks could differ"
+    ref = o.backward(p, dy)
+    for k in ("delta", "db", "dh0"):
+        assert rel_err(g[k], ref[k]) <= 1e-6, (k, rel_err(g[k], ref[k]))
+    for k in ("dWx", "dx", "dWh"):
+        sparse = kind != "dense"
+        want = ref["dvals"].ravel() if (sparse and k == "dWh") else ref[k]
+        got = g[k].ravel() if (sparse and k == "dWh") else g[k]
+        assert rel_err(got, want) <= BF16_PRODUCT_TOL, (k, rel_err(got, want))
+    # the same gradients with the K-split kernel off
+    off = {prnn.PRNN_OPT_DENSE_KSPLIT: 0, prnn.PRNN_OPT_SPARSE_KSPLIT: 0}
+    _, g_off = run(env, p, dy.astype(np.float32), options=off, pre_options=off)
+    assert np.array_equal(g["delta"], g_off["delta"])
