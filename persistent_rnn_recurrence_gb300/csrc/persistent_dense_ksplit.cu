@@ -19,18 +19,22 @@
 //     h; the two go side by side into the B operand: rows 0 .. BP-1 hold hi,
 //     rows BP .. 2BP-1 lo (BP = the batch padded to 8, 16 or 32; N = 2 BP),
 //     so one MMA per K step multiplies both;
-//  2. one thread issues the slice's MMAs (M = 128 rows of Wh, kept in shared
-//     memory for the whole sequence as the A operand) into a TMEM accumulator
-//     [128 lanes x N columns];
-//  3. four warps read the accumulator back (lane = row), add the hi and lo
-//     columns and stage the partial sums column by column; CTA o of the
-//     cluster owns batch columns [o B / CS, (o + 1) B / CS), and one thread
-//     sends each owner its columns with a bulk copy into the owner's shared
-//     memory (cp.async.bulk shared::cta -> shared::cluster, completing on
-//     the owner's mbarrier);
-//  4. the owner waits for the CS - 1 blocks, sums the CS partials and P_t,
-//     applies ReLU and publishes its columns of the block's 128 rows of h_t
-//     into y, as the other persistent kernels do.
+//  2. two threads in different warps issue the slice's MMAs, half of the K
+//     steps each (M = 128 rows of Wh, kept in shared memory for the whole
+//     sequence as the A operand), into two TMEM accumulators [128 lanes x N
+//     columns];
+//  3. four warps read the accumulators back (lane = row), add the hi and lo
+//     columns of both and stage the partial sums column by column; CTA o of
+//     the cluster owns batch columns [o B / CS, (o + 1) B / CS), and lane o
+//     of warp 4 sends owner o its columns with a bulk copy into the owner's
+//     shared memory (cp.async.bulk shared::cta -> shared::cluster, completing
+//     on the owner's mbarrier);
+//  4. the owner waits for the CS - 1 blocks, sums the CS partials (slice
+//     order) and P_t, applies ReLU and publishes its columns of the block's
+//     128 rows of h_t into y, as the other persistent kernels do.
+// In reverse mode (the backward pass) the steps run T-1 .. 0 over Wh^T's
+// image, h_prev is the next step's delta, and the output is P + sum, or 0
+// where P holds the mask marker.
 // The exchange of h between clusters stays the flag-in-data L2 broadcast;
 // only the K reduction runs through distributed shared memory.
 //
@@ -112,6 +116,15 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, long 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+// Bounded wait for the MMAs this CTA issued, before TMEM is freed: by time
+// only (another CTA's failure does not end it; the MMAs always complete).
+__device__ __forceinline__ void wait_own_mmas(uint64_t* bar, uint32_t parity) {
+  if (try_wait_cluster(bar, parity)) return;
+  const uint64_t deadline = global_ns() + 100ull * 1000 * 1000;  // 100 ms
+  uint32_t n = 0;
+  while (!try_wait_cluster(bar, parity))
+    if ((++n & 255u) == 0u && global_ns() > deadline) return;
 }
 // 2^e for |e| < 127, exactly
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
@@ -279,7 +292,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
   if (T > 0) load_p(rev ? T - 1 : 0);
   bool bad = false;       // this thread saw a failed wait
   bool aborted = false;   // uniform: the CTA left the step loop early
-  int last_mma = -1;      // thread 0: the last step whose MMAs it issued
+  int last_mma = -1;      // threads 0 and 32: the last step whose MMAs they issued
   uint32_t tr[kKsplitTraceWords];  // thread 128's record of the step (trace build)
   auto stamp = [&](int k) {
     if constexpr (TR) tr[k] = (uint32_t)clock64();
@@ -531,8 +544,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
     }
   }
   // ---- leave: MMAs retired, TMEM freed, then meet the cluster peers ----
-  if ((tid == 0 || tid == 32) && last_mma >= 0)
-    wait_phase(&mma_bar, (uint32_t)last_mma & 1u, c.timeout_ns, c.status);
+  if ((tid == 0 || tid == 32) && last_mma >= 0) wait_own_mmas(&mma_bar, (uint32_t)last_mma & 1u);
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   // a wait that gave up in the last step counts as leaving early too
   aborted = __syncthreads_or(aborted || bad) != 0;
