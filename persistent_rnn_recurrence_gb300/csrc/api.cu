@@ -1098,7 +1098,7 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
       c.R = 128;
       c.cpg = c.n_cta;
       c.G = 1;
-      c.nthreads = 256;
+      c.nthreads = 512;
       c.smem = recur_dense_ksplit_smem(h->ks_nat, B, h->ks_cs);
       if (h->poll_delay_ns < 0) c.poll_delay = 0;  // measured: no pause is fastest here
       DenseSplitArgs a{c, h->Wimg_ks, h0 ? h0 : h->zeros, h->ks_cs, h->ks_nat, h->trace};
@@ -1336,7 +1336,7 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
     c.R = 128;
     c.cpg = c.n_cta;
     c.G = 1;
-    c.nthreads = 256;
+    c.nthreads = 512;
     c.smem = recur_dense_ksplit_smem(h->ks_nat, B, h->ks_cs);
     if (h->poll_delay_ns < 0) c.poll_delay = 0;
     DenseSplitArgs a{c, h->WimgT_ks, h->zeros, h->ks_cs, h->ks_nat, nullptr};
@@ -1590,7 +1590,7 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
     info->dense_ksplit = h->ks_cs;
     info->n_cta = h->H / 128 * h->ks_cs;
     info->rows_per_cta = 128;
-    info->threads_per_cta = 256;
+    info->threads_per_cta = 512;
     info->cta_groups = 1;
     info->smem_bytes = recur_dense_ksplit_smem(h->ks_nat, h->maxB, h->ks_cs);
   } else if (h->weights_set && dense_wide_for(h, h->maxB)) {
