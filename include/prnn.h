@@ -125,8 +125,8 @@ typedef enum {
                                      hi + lo parts, about 22 bits; partial sums reduced through
                                      distributed shared memory) for forwards of B <= 32.
                                      1 = where it measured faster than the CUDA-core kernels
-                                     (default): H >= 1792 and B >= 8, H >= 1152 and B >= 12,
-                                     or H >= 640 and B >= 16; 2 = for every B <= 32; 0 =
+                                     (default): H >= 2048 and B >= 4, H >= 1536 and B >= 8,
+                                     or H >= 640 and B >= 12; 2 = for every B <= 32; 0 =
                                      never.  Its weight image is built at set_weights when
                                      the default covers max_batch or the option is 2; it
                                      takes precedence over PRNN_OPT_DENSE_WIDE                  */
@@ -134,9 +134,10 @@ typedef enum {
                                      densified matrix (fp16, the same values) on the
                                      K-split kernel of PRNN_OPT_DENSE_KSPLIT for forwards
                                      of B <= 32.  1 = where it measured faster than the
-                                     sparse kernel (default): H >= 1536, the dense rule of
+                                     sparse kernel (default): the dense rule of
                                      PRNN_OPT_DENSE_KSPLIT, and (stored entries / H) x B
-                                     >= 4096; 2 = for every B <= 32; 0 = never.
+                                     >= 3600 at H >= 1536 or >= 8192 at H >= 1152; 2 = for
+                                     every B <= 32; 0 = never.
                                      Its image is built at set_weights when the default
                                      covers max_batch or the option is 2                     */
 } prnn_option_t;

@@ -150,22 +150,22 @@ constexpr int kKsplitMaxB = 32;
 // faster than the CUDA-core kernels on GB300.  Its step has a fixed cost of
 // about 2.5 us (the L2 exchange, the MMA chain, the reduction through
 // distributed shared memory), so it wins once their arithmetic per step is
-// larger: H=640 B=16 2.7 against 3.1 us, H=1152 B=12 2.9 / 4.0, H=1792 B=8
-// 2.9 / 4.4; it loses at H=512 B=32 (2.9 / 2.7), H=1152 B=8 (2.7 / 2.2) and
-// H=2304 B=4 (3.2 / 3.0).  Monotone in B.
+// larger: H=2304 B=4 2.65 against 2.97 us, H=1536 B=8 2.54 / 4.30, H=640
+// B=12 2.47 / 3.03; it loses at H=1152 B=8 (2.49 / 2.21).  Monotone in B.
 __host__ __device__ constexpr bool ksplit_default(int H, int B) {
-  return (H >= 1792 && B >= 8) || (H >= 1152 && B >= 12) || (H >= 640 && B >= 16);
+  return (H >= 2048 && B >= 4) || (H >= 1536 && B >= 8) || (H >= 640 && B >= 12);
 }
 // Sparse layers run their densified matrix on the K-split kernel by default
 // (PRNN_OPT_SPARSE_KSPLIT = 1) where that measured faster than the sparse
 // kernel, whose gathers are bound by shared memory at wide batch: from about
-// 4096 entries per row x batch column at H >= 1536 (H=2304 25 % B=32 4.5
-// against 9.9 us, 10 % B=32 4.5 / 6.2, H=2048 25 % B=8 2.9 / 4.7, H=1536 10 %
-// B=32 3.6 / 4.0); the sparse kernel stays faster at 5 % (H=2304 B=32 4.3 /
-// 4.5), below that product (H=2048 10 % B=16 3.2 / 3.4) and at H=1152
-// (25 % B=32 3.3 / 3.4).  Monotone in B.
+// 3600 entries per row x batch column at H >= 1536 (H=2304 10 % B=16 3.22
+// against 3.54 us, 5 % B=32 4.14 / 4.27, H=1792 25 % B=8 2.62 / 2.78), and
+// from 8192 at H >= 1152 (25 % B=32 3.06 / 3.25); the sparse kernel stays
+// faster below (H=1792 10 % B=16 2.91 / 2.31, H=1152 25 % B=16 2.61 / 2.26).
+// Monotone in B.
 __host__ __device__ constexpr bool ksplit_sparse_default(int H, size_t nnz, int B) {
-  return ksplit_default(H, B) && H >= 1536 && nnz * (size_t)B >= (size_t)4096 * H;
+  return ksplit_default(H, B) && ((H >= 1536 && nnz * (size_t)B >= (size_t)3600 * H) ||
+                                  (H >= 1152 && nnz * (size_t)B >= (size_t)8192 * H));
 }
 struct DenseSplitArgs {
   RecurCommon c;

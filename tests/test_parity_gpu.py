@@ -444,6 +444,7 @@ def test_register_weight_build_gives_the_same_bits(env, spec):
     for regw, depth in ((1, 1), (0, 0), (1, 0), (0, 1)):
         lay = prnn.Layer.from_problem(p)
         try:
+            lay.set_option(prnn.PRNN_OPT_SPARSE_KSPLIT, 0)  # the sparse kernel's builds
             lay.set_option(prnn.PRNN_OPT_SPARSE_REG_WEIGHTS, regw)
             lay.set_option(prnn.PRNN_OPT_SPARSE_STAGING_DEPTH, depth)
             info = lay.info()
@@ -598,8 +599,10 @@ def test_staged_order_automatic_choice(env):
     headline layer (B = 4); the chosen forwards match the oracle."""
     _, prnn, o = env
     p = synth.make_problem(H=2304, B=32, T=6, k=576, seed=82, h0_std=0.3)
-    y, info = run_gpu(env, p)
-    assert info["sparse_staged_order"] == 1
+    # the sparse kernel (by default this layer runs its densified matrix on
+    # the K-split kernel)
+    y, info = run_gpu(env, p, options={prnn.PRNN_OPT_SPARSE_KSPLIT: 0})
+    assert info["sparse_staged_order"] == 1 and info["dense_ksplit"] == 0
     check(y, o.forward(p), "f16", "automatic staging order")
     q = synth.named_problem("sparse_f16_h1792_d10_b4_t256", T=4)
     yq, info_q = run_gpu(env, q)
@@ -972,12 +975,13 @@ def test_dense_ksplit_full_size_matches_oracle(env):
 
 def test_dense_ksplit_default_rule(env):
     """Option 1 (default) runs the K-split kernel where it measured faster
-    (H >= 1792 and B >= 8, H >= 1152 and B >= 12, H >= 640 and B >= 16) and
+    (H >= 2048 and B >= 4, H >= 1536 and B >= 8, H >= 640 and B >= 12) and
     it is planned (H % 128 == 0, every cluster resident); 0 never; 2 for any B."""
     _, prnn, _ = env
     cases = [(1152, 32, 1), (1152, 16, 1), (1152, 12, 1), (2304, 32, 1), (2304, 8, 1),
-             (1792, 8, 1), (640, 16, 1), (1024, 16, 1), (1152, 8, 0), (1536, 8, 0),
-             (640, 12, 0), (512, 32, 0), (2304, 4, 0), (4096, 32, 0), (1000, 32, 0)]
+             (2304, 4, 1), (1536, 8, 1), (640, 12, 1), (1024, 16, 1), (1152, 8, 0),
+             (1024, 8, 0), (2304, 3, 0), (640, 8, 0), (512, 32, 0), (4096, 32, 0),
+             (1000, 32, 0)]
     for H, B, want in cases:
         lay = prnn.Layer(H, H, B, "f16", "persistent")
         try:
@@ -1091,11 +1095,12 @@ def test_csr_layer_on_ksplit_matches_oracle(env):
 
 def test_sparse_ksplit_default_rule(env):
     """Option 1 (default) runs a sparse layer's densified matrix on the
-    K-split kernel at H >= 1536 where (entries per row) x B >= 4096 and the
-    dense rule holds; 0 never; 3 is refused."""
+    K-split kernel where the dense rule holds and (entries per row) x B is at
+    least 3600 at H >= 1536 or 8192 at H >= 1152; 0 never; 3 is refused."""
     _, prnn, _ = env
     cases = [(2304, 0.25, 32, 1), (2304, 0.10, 32, 1), (2304, 0.25, 8, 1), (2048, 0.10, 32, 1),
-             (2304, 0.05, 32, 0), (2304, 0.10, 16, 0), (1152, 0.25, 32, 0), (2304, 0.25, 4, 0)]
+             (2304, 0.05, 32, 1), (2304, 0.10, 16, 1), (1152, 0.25, 32, 1), (1152, 0.25, 16, 0),
+             (1792, 0.10, 16, 0), (2304, 0.05, 16, 0), (2304, 0.10, 8, 0), (2304, 0.25, 4, 0)]
     for H, d, B, want in cases:
         p = synth.make_problem(H=H, B=B, T=1, k=synth.sparse_k(H, d), seed=114)
         lay = prnn.Layer(H, H, B, "f16", "persistent")
