@@ -47,6 +47,7 @@ struct prnn_handle {
   size_t ks_nnz = 0;  // sparse: stored entries behind the K-split image
   bool ks = false;
   int ks_cs = 0, ks_nat = 0;
+  bool ks_stream = false;  // Wh streamed through rings (it does not fit on chip), B <= 16
   void* Wimg_ks = nullptr;
   void* WimgT_ks = nullptr;  // the same for Wh^T (the backward's reverse recurrence)
   // tensor-core dense recurrence (wide batch): its own plan and weight image
@@ -577,7 +578,8 @@ static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
 // the K-major MMA operand).  Sets h->ks.
 static prnn_status_t install_ksplit(prnn_t h, const uint16_t* w16) {
   const int H = h->H;
-  const int kcs = recur_dense_ksplit_plan(H);
+  bool stream = false;
+  const int kcs = recur_dense_ksplit_plan(H, &stream);
   if (kcs == 0) return PRNN_OK;
   const int nblk = H / 128, knat = ksplit_nat(H, kcs);
   std::vector<uint16_t> img((size_t)nblk * kcs * knat * 128 * 64, 0);
@@ -606,6 +608,7 @@ static prnn_status_t install_ksplit(prnn_t h, const uint16_t* w16) {
   h->ks = true;
   h->ks_cs = kcs;
   h->ks_nat = knat;
+  h->ks_stream = stream;
   return PRNN_OK;
 }
 
@@ -1046,6 +1049,7 @@ static bool dense_wide_for(const prnn_t h, int B) {
 static bool ksplit_for(const prnn_t h, int B) {
   if (h->algo != PRNN_ALGO_PERSISTENT || !h->ks || h->sync_mode != 0 || B < 1 || B > kKsplitMaxB)
     return false;
+  if (h->ks_stream && B > 16) return false;  // the streamed plan serves up to 16 columns
   if (h->sparse) return h->sks_opt == 2 || (h->sks_opt == 1 && ksplit_sparse_default(h->H, h->ks_nnz, B));
   if (h->ks_opt == 0 || h->rtc) return false;
   return h->ks_opt == 2 || ksplit_default(h->H, B);
@@ -1099,9 +1103,10 @@ static prnn_status_t forward_impl(prnn_t h, int T, int B, const float* x, const 
       c.cpg = c.n_cta;
       c.G = 1;
       c.nthreads = 512;
-      c.smem = recur_dense_ksplit_smem(h->ks_nat, B, h->ks_cs);
+      c.smem = recur_dense_ksplit_smem(h->ks_nat, B, h->ks_cs, h->ks_stream);
       if (h->poll_delay_ns < 0) c.poll_delay = 0;  // measured: no pause is fastest here
-      DenseSplitArgs a{c, h->Wimg_ks, h0 ? h0 : h->zeros, h->ks_cs, h->ks_nat, h->trace};
+      DenseSplitArgs a{c, h->Wimg_ks, h0 ? h0 : h->zeros, h->ks_cs, h->ks_nat, h->trace,
+                       h->ks_stream ? 1 : 0};
       PRNN_TRY(launch_recur_dense_ksplit(a, s));
     } else if (h->sparse) {
       SparseRecurArgs a{};
@@ -1337,9 +1342,9 @@ prnn_status_t prnn_backward(prnn_t h, int T, int B, const float* x, const float*
     c.cpg = c.n_cta;
     c.G = 1;
     c.nthreads = 512;
-    c.smem = recur_dense_ksplit_smem(h->ks_nat, B, h->ks_cs);
+    c.smem = recur_dense_ksplit_smem(h->ks_nat, B, h->ks_cs, h->ks_stream);
     if (h->poll_delay_ns < 0) c.poll_delay = 0;
-    DenseSplitArgs a{c, h->WimgT_ks, h->zeros, h->ks_cs, h->ks_nat, nullptr};
+    DenseSplitArgs a{c, h->WimgT_ks, h->zeros, h->ks_cs, h->ks_nat, nullptr, h->ks_stream ? 1 : 0};
     PRNN_TRY(launch_recur_dense_ksplit(a, s));
   } else if (h->sparse) {  // Wh^T has its own plan (its rows are Wh's columns)
     c.n_cta = h->b_n_cta;
@@ -1592,7 +1597,7 @@ prnn_status_t prnn_get_info(prnn_t h, prnn_info_t* info) {
     info->rows_per_cta = 128;
     info->threads_per_cta = 512;
     info->cta_groups = 1;
-    info->smem_bytes = recur_dense_ksplit_smem(h->ks_nat, h->maxB, h->ks_cs);
+    info->smem_bytes = recur_dense_ksplit_smem(h->ks_nat, h->maxB, h->ks_cs, h->ks_stream);
   } else if (h->weights_set && dense_wide_for(h, h->maxB)) {
     info->dense_wide_batch = 1;
     info->n_cta = (h->H + h->w_R - 1) / h->w_R;

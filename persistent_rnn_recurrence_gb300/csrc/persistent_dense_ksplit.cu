@@ -62,6 +62,15 @@ constexpr int kSplitPollMax = 6;       // float4 polls a thread keeps in flight
 static_assert(kSplitPollMax * kSplitThreads * 4 >= kKsplitMaxB * kKsplitMaxSlice,
               "one poll round covers the widest slice of the widest batch");
 constexpr uint32_t kAtomA = 128 * 128;  // bytes of one A atom: 128 rows x 64 fp16
+// Streamed A (layers whose weights do not fit beside the operand tiles): each
+// MMA issuer has a ring of kNsq A stages refilled by bulk copies from the
+// weight image (it stays in L2), kNsq - 1 atoms ahead of its MMAs, across
+// steps; 8 polls per thread cover a slice of up to kKsplitMaxSliceStream
+// columns at B <= 16
+constexpr int kNsq = 4;
+constexpr int kStreamPollMax = 8;
+static_assert(kStreamPollMax * kSplitThreads * 4 >= 16 * kKsplitMaxSliceStream,
+              "one poll round covers the widest streamed slice at B <= 16");
 constexpr int kSplitTmemCols = 128;    // two accumulators of N <= 64 columns
 constexpr float kSplitLarge = 32768.f; // |h| from here on would overflow the fp16 split
 
@@ -89,6 +98,15 @@ __device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_
       "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
       "[%3];" ::"r"(dst),
       "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// bulk copy global -> this CTA's shared memory, completing on its mbarrier
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 __device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
@@ -162,8 +180,9 @@ __device__ __forceinline__ void store_split(unsigned char* hi_dst, float4 v, flo
       make_uint2(pack_half2(lo[0], lo[1]), pack_half2(lo[2], lo[3]));
 }
 
-// TR: the phase-trace build (records per step and CTA in a.trace)
-template <int BP, bool TR>
+// TR: the phase-trace build (records per step and CTA in a.trace); STR: A
+// streamed through per-issuer rings instead of resident
+template <int BP, bool TR, bool STR>
 __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(const DenseSplitArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t mma_bar;
@@ -171,6 +190,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
   __shared__ uint32_t s_tmem;
   __shared__ int s_large[2];
   __shared__ float s_red[kSplitThreads / 32];
+  __shared__ __align__(8) uint64_t a_full[2][kNsq];   // streamed A: stage loaded
+  __shared__ __align__(8) uint64_t a_empty[2][kNsq];  // streamed A: its MMAs done
+  constexpr int PM = STR ? kStreamPollMax : kSplitPollMax;  // polls per thread
 
   constexpr int N = 2 * BP;
   constexpr uint32_t kAtomB = (uint32_t)N * 128;  // bytes of one B atom: N rows x 64 fp16
@@ -195,9 +217,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
   const int maxcol = (B + cs - 1) / cs;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - smem_u32(smem_raw));
+  const int a_atoms = STR ? 2 * kNsq : nat;  // A in shared memory: all atoms, or the rings
   const uint32_t sA = base;
-  const uint32_t sB = sA + (uint32_t)nat * kAtomA;
-  unsigned char* gB = gbase + (size_t)nat * kAtomA;
+  const uint32_t sB = sA + (uint32_t)a_atoms * kAtomA;
+  unsigned char* gB = gbase + (size_t)a_atoms * kAtomA;
   // partial sums out, [2][B][128] (column b of the block: 128 rows), and in,
   // [2][cs][maxcol][128] (slot i: CTA i's partials of this CTA's columns)
   float* stage = reinterpret_cast<float*>(gB + (size_t)nat * kAtomB);
@@ -211,7 +234,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
         reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.Wimg) +
                                        (size_t)blockIdx.x * nat * kAtomA);
     uint4* dst = reinterpret_cast<uint4*>(gbase);
-    const int na = nat * (int)kAtomA / 16;
+    const int na = STR ? 0 : nat * (int)kAtomA / 16;
     for (int i = tid; i < na; i += kSplitThreads) dst[i] = __ldg(src + i);
     uint4* bz = reinterpret_cast<uint4*>(gB);
     for (int i = tid; i < nat * (int)kAtomB / 16; i += kSplitThreads) bz[i] = make_uint4(0, 0, 0, 0);
@@ -222,6 +245,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
     mbar_init(&recv_bar[0], 1);
     mbar_init(&recv_bar[1], 1);
     s_large[0] = s_large[1] = 0;
+    if constexpr (STR)
+      for (int q = 0; q < 2; ++q)
+        for (int st = 0; st < kNsq; ++st) {
+          mbar_init(&a_full[q][st], 1);
+          mbar_init(&a_empty[q][st], 1);
+        }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // the partial blocks of steps 0 and 1 (cs - 1 peers x ncol columns)
     if (T > 0) mbar_arrive_expect_tx(&recv_bar[0], in_bytes);
@@ -240,22 +269,42 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
   const uint32_t tmem = s_tmem;
   cluster_sync_all();  // every peer's mbarriers exist before the first copy
 
+  // Streamed A: issuer q (threads 0 and 32) takes atoms [a_lo, a_lo + naq) of
+  // the slice; its n-th atom overall (step n / naq) sits in ring stage
+  // n % kNsq, loaded kNsq - 1 atoms ahead of the MMAs that read it
+  const int qi = tid == 0 ? 0 : 1;
+  const int na0 = (nat + 1) / 2;
+  const int a_lo = qi == 0 ? 0 : na0, naq = qi == 0 ? na0 : nat - na0;
+  const int n_total = STR && (tid == 0 || tid == 32) ? T * naq : 0;
+  int n_issued = 0, n_cons = 0;
+  const unsigned char* wimg =
+      static_cast<const unsigned char*>(a.Wimg) + (size_t)blockIdx.x * nat * kAtomA;
+  auto a_copy = [&](int n) {  // atom n of this issuer into its stage n % kNsq
+    const int st = n % kNsq;
+    mbar_arrive_expect_tx(&a_full[qi][st], kAtomA);
+    bulk_g2s(sA + (uint32_t)(qi * kNsq + st) * kAtomA, wimg + (size_t)(a_lo + n % naq) * kAtomA,
+             kAtomA, &a_full[qi][st]);
+  };
+  if constexpr (STR)
+    for (; n_issued < kNsq - 1 && n_issued < n_total; ++n_issued) a_copy(n_issued);
+
   const uint32_t idesc = f16_idesc(128, N);
   const int nks = kl >> 4, nks_half = (nks + 1) >> 1;  // K steps: issuer 0 takes the first half
   const int q4 = kl >> 2;  // float4 per batch column of the slice
   const int nf4 = B * q4;
   const int nout = ncol * 128;  // outputs this CTA finalizes: column cb0 + o / 128, row o % 128
-  // The thread's float4 items of the slice (at most kSplitPollMax: the plan
-  // keeps kl <= kKsplitMaxSlice, so B * kl / 4 <= kSplitPollMax * 256), with
+  // The thread's float4 items of the slice (at most PM: the plan keeps kl <=
+  // kKsplitMaxSlice, or kKsplitMaxSliceStream at B <= 16, so B * kl / 4 <= PM *
+  // kSplitThreads), with
   // their offsets in a step's h (floats) and in the B operand (bytes, hi),
   // computed once: dividing by the launch-time slice width in every step
   // measured slower than the step's whole arithmetic (dependent integer
   // chains with 8 warps per SM to hide them)
-  int goff[kSplitPollMax];
-  uint32_t soff[kSplitPollMax];
+  int goff[PM];
+  uint32_t soff[PM];
   unsigned items = 0;
 #pragma unroll
-  for (int u = 0; u < kSplitPollMax; ++u) {
+  for (int u = 0; u < PM; ++u) {
     const int i = tid + u * kSplitThreads;
     goff[u] = 0;
     soff[u] = 0;
@@ -322,9 +371,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
     bool large = false;
     uint32_t round_max = 0;
     {
-      float4 v[kSplitPollMax];
+      float4 v[PM];
 #pragma unroll
-      for (int u = 0; u < kSplitPollMax; ++u)
+      for (int u = 0; u < PM; ++u)
         if ((items >> u) & 1u)
           v[u] = poll ? ld_relaxed_f4(src + goff[u])
                       : __ldg(reinterpret_cast<const float4*>(src + goff[u]));
@@ -336,7 +385,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
       uint32_t spins = 0, round = 0;
       while (pending != 0u) {
 #pragma unroll
-        for (int u = 0; u < kSplitPollMax; ++u)
+        for (int u = 0; u < PM; ++u)
           if (((pending >> u) & 1u) && (!poll || ready4(v[u]))) {  // h0 is not polled
             large |= !(fabsf(v[u].x) < kSplitLarge) | !(fabsf(v[u].y) < kSplitLarge) |
                      !(fabsf(v[u].z) < kSplitLarge) | !(fabsf(v[u].w) < kSplitLarge);
@@ -352,7 +401,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
         w.pause(round);
         if constexpr (TR) round_max = round > round_max ? round : round_max;
 #pragma unroll
-        for (int u = 0; u < kSplitPollMax; ++u)
+        for (int u = 0; u < PM; ++u)
           if ((pending >> u) & 1u) v[u] = ld_relaxed_f4(src + goff[u]);
       }
     }
@@ -371,7 +420,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
     if (s_large[par]) {
       float m = 0.f;
 #pragma unroll
-      for (int u = 0; u < kSplitPollMax; ++u)
+      for (int u = 0; u < PM; ++u)
         if ((items >> u) & 1u) {
           const float* q = src + goff[u];
           const float4 v = poll ? ld_relaxed_f4(q) : __ldg(reinterpret_cast<const float4*>(q));
@@ -388,7 +437,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
       if (m >= kSplitLarge && m <= 3.0e38f) e = ilogbf(m) - 14;
       const float scale = pow2i(-e);
 #pragma unroll
-      for (int u = 0; u < kSplitPollMax; ++u)
+      for (int u = 0; u < PM; ++u)
         if ((items >> u) & 1u) {
           const float* q = src + goff[u];
           const float4 v = poll ? ld_relaxed_f4(q) : __ldg(reinterpret_cast<const float4*>(q));
@@ -410,10 +459,44 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
       // the descriptors' start-address fields (bytes / 16) step by 2 within
       // an atom and by the atom size between atoms
       const uint64_t ad0 = sw128_kmajor_desc(sA), bd0 = sw128_kmajor_desc(sB);
-      for (int ks = ks_lo; ks < ks_hi; ++ks) {
-        const uint32_t at = (uint32_t)(ks >> 2), s4 = (uint32_t)(ks & 3);
-        umma_f16(acc, ad0 + ((at * kAtomA + s4 * 32u) >> 4), bd0 + ((at * kAtomB + s4 * 32u) >> 4),
-                 idesc, ks > ks_lo ? 1u : 0u);
+      if constexpr (STR) {
+        // the issuer's atoms from its ring, each released by a commit; then
+        // the stage of the atom before it is refilled kNsq - 1 atoms ahead
+        for (int ai = 0; ai < naq; ++ai) {
+          const int n = n_cons, st = n % kNsq;
+          if (!wait_phase(&a_full[qi][st], (uint32_t)(n / kNsq) & 1u, c.timeout_ns, c.status)) {
+            report_timeout(c.status, t, blockIdx.x);
+            bad = true;
+            break;
+          }
+          ++n_cons;
+          const uint32_t at = (uint32_t)(a_lo + ai);
+          const uint64_t ad = sw128_kmajor_desc(sA + (uint32_t)(qi * kNsq + st) * kAtomA);
+          const int k_hi = min(4, nks - 4 * (int)at);
+          for (int s4 = 0; s4 < k_hi; ++s4)
+            umma_f16(acc, ad + (((uint32_t)s4 * 32u) >> 4),
+                     bd0 + ((at * kAtomB + (uint32_t)s4 * 32u) >> 4), idesc,
+                     (ai > 0 || s4 > 0) ? 1u : 0u);
+          umma_commit(&a_empty[qi][st]);
+          const int nn = n + kNsq - 1;  // into the stage of atom n - 1
+          if (nn < n_total && nn == n_issued) {
+            if (nn >= kNsq &&
+                !wait_phase(&a_empty[qi][(nn - kNsq) % kNsq], (uint32_t)((nn - kNsq) / kNsq) & 1u,
+                            c.timeout_ns, c.status)) {
+              report_timeout(c.status, t, blockIdx.x);
+              bad = true;
+              break;
+            }
+            a_copy(nn);
+            ++n_issued;
+          }
+        }
+      } else {
+        for (int ks = ks_lo; ks < ks_hi; ++ks) {
+          const uint32_t at = (uint32_t)(ks >> 2), s4 = (uint32_t)(ks & 3);
+          umma_f16(acc, ad0 + ((at * kAtomA + s4 * 32u) >> 4), bd0 + ((at * kAtomB + s4 * 32u) >> 4),
+                   idesc, ks > ks_lo ? 1u : 0u);
+        }
       }
       umma_commit(&mma_bar);  // with no MMA of its own it arrives at once
       last_mma = t;
@@ -447,7 +530,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
           uint32_t hv[16], lv[16];
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
-            if (q == 1 && nks <= 1) break;  // issuer 1 had no K step
+            if (q == 1 && (STR ? nat <= 1 : nks <= 1)) break;  // issuer 1 had no K step
             const uint32_t accq = lanes + 64u * (uint32_t)q;
             if constexpr (BP == 8) {  // hi and lo in one 16-column load
               tmem_load_16cols(accq, hv);
@@ -550,6 +633,15 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
   }
   // ---- leave: MMAs retired, TMEM freed, then meet the cluster peers ----
   if ((tid == 0 || tid == 32) && last_mma >= 0) wait_own_mmas(&mma_bar, (uint32_t)last_mma & 1u);
+  if constexpr (STR) {
+    if (tid == 0 || tid == 32) {
+      // every MMA this thread issued (its last commit covers them all), and
+      // the A copies still in flight into its ring
+      if (n_cons > 0) wait_own_mmas(&a_empty[qi][(n_cons - 1) % kNsq], (uint32_t)((n_cons - 1) / kNsq) & 1u);
+      for (int n = n_cons; n < n_issued; ++n)
+        wait_own_mmas(&a_full[qi][n % kNsq], (uint32_t)(n / kNsq) & 1u);
+    }
+  }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   // a wait that gave up in the last step counts as leaving early too
   aborted = __syncthreads_or(aborted || bad) != 0;
@@ -569,19 +661,19 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
 
 }  // namespace
 
-size_t recur_dense_ksplit_smem(int nat, int B, int cs) {
+size_t recur_dense_ksplit_smem(int nat, int B, int cs, bool stream) {
   const int bp = B <= 8 ? 8 : (B <= 16 ? 16 : 32);
   const int maxcol = (B + cs - 1) / cs;
-  return 1024 + (size_t)nat * kAtomA + (size_t)nat * (2 * bp) * 128 +
+  return 1024 + (size_t)(stream ? 2 * kNsq : nat) * kAtomA + (size_t)nat * (2 * bp) * 128 +
          (size_t)2 * B * 128 * sizeof(float) + (size_t)2 * cs * maxcol * 128 * sizeof(float);
 }
 
 namespace {
 
-template <int BP, bool TR>
+template <int BP, bool TR, bool STR>
 cudaError_t launch_bp(const DenseSplitArgs& a, cudaStream_t s, bool query_only, int* clusters_fit) {
-  const size_t smem = recur_dense_ksplit_smem(a.nat, a.c.B, a.cs);
-  cudaError_t e = cudaFuncSetAttribute(recur_dense_ksplit_kernel<BP, TR>,
+  const size_t smem = recur_dense_ksplit_smem(a.nat, a.c.B, a.cs, STR);
+  cudaError_t e = cudaFuncSetAttribute(recur_dense_ksplit_kernel<BP, TR, STR>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -599,17 +691,18 @@ cudaError_t launch_bp(const DenseSplitArgs& a, cudaStream_t s, bool query_only, 
   cfg.attrs = at;
   if (query_only) {
     cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(clusters_fit, recur_dense_ksplit_kernel<BP, TR>, &cfg);
+    return cudaOccupancyMaxActiveClusters(clusters_fit, recur_dense_ksplit_kernel<BP, TR, STR>, &cfg);
   }
   // every CTA waits on CTAs of other clusters: the cooperative launch makes
   // the grid co-resident (or fails rather than run part of it)
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, recur_dense_ksplit_kernel<BP, TR>, a);
+  return cudaLaunchKernelEx(&cfg, recur_dense_ksplit_kernel<BP, TR, STR>, a);
 }
 
 }  // namespace
 
-int recur_dense_ksplit_plan(int H) {
+int recur_dense_ksplit_plan(int H, bool* stream) {
+  *stream = false;
   if (H < 128 || H % 128 != 0) return 0;
   int dev = 0, cl = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -625,13 +718,34 @@ int recur_dense_ksplit_plan(int H) {
     a.c.n_cta = nblk * cs;
     a.cs = cs;
     a.nat = ksplit_nat(H, cs);
-    if (recur_dense_ksplit_smem(a.nat, kKsplitMaxB, cs) > (size_t)optin) continue;
+    if (recur_dense_ksplit_smem(a.nat, kKsplitMaxB, cs, false) > (size_t)optin) continue;
     int fit = 0;
-    if (launch_bp<32, false>(a, nullptr, true, &fit) != cudaSuccess) {
+    if (launch_bp<32, false, false>(a, nullptr, true, &fit) != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
     if (fit >= nblk) return cs;
+  }
+  // the weights do not fit beside the operand tiles: A streamed from the
+  // image through rings, for batches of up to 16 columns
+  for (int cs = kKsplitMaxCluster; cs >= 2; --cs) {
+    if (H / 16 < 2 * 4 * cs) continue;  // two atoms per slice at least
+    if ((H / 16 + cs - 1) / cs * 16 > kKsplitMaxSliceStream) continue;
+    DenseSplitArgs a{};
+    a.c.B = 16;
+    a.c.n_cta = nblk * cs;
+    a.cs = cs;
+    a.nat = ksplit_nat(H, cs);
+    if (recur_dense_ksplit_smem(a.nat, 16, cs, true) > (size_t)optin) continue;
+    int fit = 0;
+    if (launch_bp<16, false, true>(a, nullptr, true, &fit) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    if (fit >= nblk) {
+      *stream = true;
+      return cs;
+    }
   }
   return 0;
 }
@@ -639,17 +753,26 @@ int recur_dense_ksplit_plan(int H) {
 cudaError_t launch_recur_dense_ksplit(const DenseSplitArgs& a, cudaStream_t s) {
   const int B = a.c.B, H = a.c.H;
   if (B < 1 || B > kKsplitMaxB || H % 128 != 0 || a.cs < 2 || a.cs > kKsplitMaxCluster ||
-      a.c.n_cta != H / 128 * a.cs || a.nat != ksplit_nat(H, a.cs) ||
-      (H / 16 + a.cs - 1) / a.cs * 16 > kKsplitMaxSlice)
+      a.c.n_cta != H / 128 * a.cs || a.nat != ksplit_nat(H, a.cs))
     return cudaErrorInvalidValue;
-  if (a.trace) {
-    if (B <= 8) return launch_bp<8, true>(a, s, false, nullptr);
-    if (B <= 16) return launch_bp<16, true>(a, s, false, nullptr);
-    return launch_bp<32, true>(a, s, false, nullptr);
+  if (a.stream) {
+    if (B > 16 || (H / 16 + a.cs - 1) / a.cs * 16 > kKsplitMaxSliceStream)
+      return cudaErrorInvalidValue;
+    if (a.trace)
+      return B <= 8 ? launch_bp<8, true, true>(a, s, false, nullptr)
+                    : launch_bp<16, true, true>(a, s, false, nullptr);
+    return B <= 8 ? launch_bp<8, false, true>(a, s, false, nullptr)
+                  : launch_bp<16, false, true>(a, s, false, nullptr);
   }
-  if (B <= 8) return launch_bp<8, false>(a, s, false, nullptr);
-  if (B <= 16) return launch_bp<16, false>(a, s, false, nullptr);
-  return launch_bp<32, false>(a, s, false, nullptr);
+  if ((H / 16 + a.cs - 1) / a.cs * 16 > kKsplitMaxSlice) return cudaErrorInvalidValue;
+  if (a.trace) {
+    if (B <= 8) return launch_bp<8, true, false>(a, s, false, nullptr);
+    if (B <= 16) return launch_bp<16, true, false>(a, s, false, nullptr);
+    return launch_bp<32, true, false>(a, s, false, nullptr);
+  }
+  if (B <= 8) return launch_bp<8, false, false>(a, s, false, nullptr);
+  if (B <= 16) return launch_bp<16, false, false>(a, s, false, nullptr);
+  return launch_bp<32, false, false>(a, s, false, nullptr);
 }
 
 }  // namespace prnn

@@ -145,6 +145,7 @@ bool recur_dense_wide_plan(int H, int sm_count, size_t smem_optin, int* R, int* 
 // nat = the widest slice's 64-column atoms.
 constexpr int kKsplitMaxCluster = 8;
 constexpr int kKsplitMaxSlice = 384;  // K columns per CTA at most (plans with wider slices are not made)
+constexpr int kKsplitMaxSliceStream = 1024;  // the same for the streamed-A plan (B <= 16)
 constexpr int kKsplitMaxB = 32;
 // The default rule (PRNN_OPT_DENSE_KSPLIT = 1): where the kernel measured
 // faster than the CUDA-core kernels on GB300.  Its step has a fixed cost of
@@ -172,7 +173,8 @@ struct DenseSplitArgs {
   const void* Wimg;
   const float* h0_rows;  // [B][H]: h0, or zeros
   int cs, nat;
-  uint32_t* trace;       // null, or [T][n_cta][kTraceWords] phase records (the
+  uint32_t* trace;
+  int stream;            // 1: Wh streamed from Wimg through rings (B <= 16), not resident       // null, or [T][n_cta][kTraceWords] phase records (the
                          // first 20 words of each; see kKsplitTrace*)
 };
 // Phase-trace record of the K-split kernel (one step, one CTA), words:
@@ -194,11 +196,12 @@ __host__ __device__ constexpr int ksplit_nat(int H, int cs) {
   return ((H / 16 + cs - 1) / cs + 3) / 4;
 }
 // Dynamic shared memory of the kernel for a batch of B columns.
-size_t recur_dense_ksplit_smem(int nat, int B, int cs);
+size_t recur_dense_ksplit_smem(int nat, int B, int cs, bool stream);
 // The largest cluster size (8 .. 2) for which all H / 128 clusters of the
 // kernel are resident at once (one CTA per SM) and its shared memory fits;
-// 0 when none does or H % 128 != 0.
-int recur_dense_ksplit_plan(int H);
+// 0 when none does or H % 128 != 0.  When Wh does not fit on chip beside the
+// operand tiles, the plan streams it (*stream = true; batches of <= 16).
+int recur_dense_ksplit_plan(int H, bool* stream);
 cudaError_t launch_recur_dense_ksplit(const DenseSplitArgs& a, cudaStream_t s);
 
 // Dense fp16 on the tensor cores (persistent_dense_tc.cu): per CTA an image of

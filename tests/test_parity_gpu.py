@@ -1113,3 +1113,53 @@ def test_sparse_ksplit_default_rule(env):
                 lay.set_option(prnn.PRNN_OPT_SPARSE_KSPLIT, 3)
         finally:
             lay.close()
+
+
+# --- the K-split kernel with Wh streamed (it does not fit on chip beside the tiles) --------
+STREAMED = [dict(H=4096, B=16, T=6, wdtype="f16", h0_std=0.2),   # clusters of 4, slices of 1024
+            dict(H=4096, B=11, T=5, wdtype="f16", h0_std=0.5),
+            dict(H=4096, I=300, B=4, T=6, wdtype="f16"),          # N = 16 (hi 8 + lo 8)
+            dict(H=4096, B=16, T=6, k=1024, h0_std=0.3)]           # a sparse layer, densified
+
+
+@pytest.mark.parametrize("spec", STREAMED)
+def test_ksplit_streamed_matches_oracle(env, spec):
+    """H = 4096: the weights stream from their image through each MMA issuer's
+    ring of shared-memory stages every step; the result stays within the rule
+    and within it of the CUDA-core kernels."""
+    _, prnn, o = env
+    p = synth.make_problem(seed=115, **spec)
+    opts = {prnn.PRNN_OPT_DENSE_KSPLIT: 2, prnn.PRNN_OPT_SPARSE_KSPLIT: 2}
+    ref = o.forward(p)
+    y, info = run_gpu(env, p, options=opts, pre_options=opts)
+    assert info["dense_ksplit"] == 4 and info["n_cta"] == 128
+    check(y, ref, "f16", f"streamed {spec}")
+    off = {prnn.PRNN_OPT_DENSE_KSPLIT: 0, prnn.PRNN_OPT_SPARSE_KSPLIT: 0}
+    y_cc, info_cc = run_gpu(env, p, options=off, pre_options=off)
+    assert info_cc["dense_ksplit"] == 0
+    assert np.abs(y - y_cc).max() <= TOL["f16"] * float(np.abs(ref).max())
+
+
+def test_ksplit_streamed_batch_limit_and_timeout(env):
+    """The streamed plan serves up to 16 columns (a forward of 32 runs the
+    CUDA-core kernel), and a dropped publish ends it in a clean timeout."""
+    torch, prnn, o = env
+    p = synth.make_problem(H=4096, B=32, T=3, wdtype="f16", seed=116)
+    lay = prnn.Layer.from_problem(p)
+    try:
+        assert lay.info()["dense_ksplit"] == 0
+        x = torch.from_numpy(p.x).cuda()
+        y32 = lay.forward(x)
+        y16 = lay.forward(x[:, :16].contiguous())
+        torch.cuda.synchronize()
+        assert lay.status() == prnn.PRNN_OK
+        lay.set_option(prnn.PRNN_OPT_WAIT_TIMEOUT_US, 20000)
+        lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_CTA, 37)
+        lay.set_option(prnn.PRNN_OPT_DEBUG_DROP_STEP, 1)
+        lay.forward(x[:, :16].contiguous())
+        assert lay.status() == prnn.PRNN_ERR_TIMEOUT
+    finally:
+        lay.close()
+    ref = o.forward(p)
+    check(y32.cpu().numpy(), ref, "f16", "H=4096 B=32")
+    check(y16.cpu().numpy(), ref[:, :16], "f16", "H=4096 B=16 streamed")
