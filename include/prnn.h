@@ -120,7 +120,9 @@ typedef enum {
   PRNN_OPT_DENSE_KSPLIT = 16,     /* dense fp16 persistent, flags in the data, H % 128 == 0 and
                                      all H / 128 clusters of 2 .. 8 CTAs resident at once, one
                                      CTA per SM (on 152 SMs: clusters of 8 up to H = 1920, of
-                                     6 up to 2304): the tensor-core kernel that splits each
+                                     6 up to 2304; from H = 2560 to 4096 clusters of 4 with
+                                     Wh streamed from L2 each step, for B <= 16): the
+                                     tensor-core kernel that splits each
                                      step's product over K inside clusters (h split into fp16
                                      hi + lo parts, about 22 bits; partial sums reduced through
                                      distributed shared memory) for forwards of B <= 32.
@@ -136,8 +138,9 @@ typedef enum {
                                      of B <= 32.  1 = where it measured faster than the
                                      sparse kernel (default): the dense rule of
                                      PRNN_OPT_DENSE_KSPLIT, and (stored entries / H) x B
-                                     >= 3600 at H >= 1536 or >= 8192 at H >= 1152; 2 = for
-                                     every B <= 32; 0 = never.
+                                     >= 8192 at H >= 1152, >= 3600 at H >= 1536, >= 6000 at
+                                     H >= 2560 (streamed weights); 2 = for every B <= 32
+                                     (16 with streamed weights); 0 = never.
                                      Its image is built at set_weights when the default
                                      covers max_batch or the option is 2                     */
 } prnn_option_t;

@@ -163,10 +163,14 @@ __host__ __device__ constexpr bool ksplit_default(int H, int B) {
 // against 3.54 us, 5 % B=32 4.14 / 4.27, H=1792 25 % B=8 2.62 / 2.78), and
 // from 8192 at H >= 1152 (25 % B=32 3.06 / 3.25); the sparse kernel stays
 // faster below (H=1792 10 % B=16 2.91 / 2.31, H=1152 25 % B=16 2.61 / 2.26).
-// Monotone in B.
+// Where the weights are streamed (H >= 2560: the step costs about 7.3 us
+// whatever the batch) it takes 6000: H=4096 10 % B=16 8.8 against 11.1 us,
+// while 25 % B=4 stays on the sparse kernel (6.3 us).  Monotone in B.
+__host__ __device__ constexpr size_t ksplit_sparse_threshold(int H) {
+  return H >= 2560 ? 6000 : (H >= 1536 ? 3600 : (H >= 1152 ? 8192 : (size_t)1 << 40));
+}
 __host__ __device__ constexpr bool ksplit_sparse_default(int H, size_t nnz, int B) {
-  return ksplit_default(H, B) && ((H >= 1536 && nnz * (size_t)B >= (size_t)3600 * H) ||
-                                  (H >= 1152 && nnz * (size_t)B >= (size_t)8192 * H));
+  return ksplit_default(H, B) && nnz * (size_t)B >= ksplit_sparse_threshold(H) * (size_t)H;
 }
 struct DenseSplitArgs {
   RecurCommon c;

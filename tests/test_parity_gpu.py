@@ -1096,11 +1096,13 @@ def test_csr_layer_on_ksplit_matches_oracle(env):
 def test_sparse_ksplit_default_rule(env):
     """Option 1 (default) runs a sparse layer's densified matrix on the
     K-split kernel where the dense rule holds and (entries per row) x B is at
-    least 3600 at H >= 1536 or 8192 at H >= 1152; 0 never; 3 is refused."""
+    least 8192 at H >= 1152, 3600 at H >= 1536, 6000 at H >= 2560 (streamed
+    weights, B <= 16); 0 never; 3 is refused."""
     _, prnn, _ = env
     cases = [(2304, 0.25, 32, 1), (2304, 0.10, 32, 1), (2304, 0.25, 8, 1), (2048, 0.10, 32, 1),
              (2304, 0.05, 32, 1), (2304, 0.10, 16, 1), (1152, 0.25, 32, 1), (1152, 0.25, 16, 0),
-             (1792, 0.10, 16, 0), (2304, 0.05, 16, 0), (2304, 0.10, 8, 0), (2304, 0.25, 4, 0)]
+             (1792, 0.10, 16, 0), (2304, 0.05, 16, 0), (2304, 0.10, 8, 0), (2304, 0.25, 4, 0),
+             (4096, 0.10, 16, 1), (4096, 0.25, 4, 0), (4096, 0.25, 32, 0)]
     for H, d, B, want in cases:
         p = synth.make_problem(H=H, B=B, T=1, k=synth.sparse_k(H, d), seed=114)
         lay = prnn.Layer(H, H, B, "f16", "persistent")
