@@ -344,20 +344,30 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
   bool bad = false;       // this thread saw a failed wait
   bool aborted = false;   // uniform: the CTA left the step loop early
   int last_mma = -1;      // threads 0 and 32: the last step whose MMAs they issued
-  uint32_t tr[kKsplitTraceWords];  // thread 128's record of the step (trace build)
+  // trace build: thread 128 stores each stamp straight into the step's record
+  // (a record held in registers until the step's end made every thread spill,
+  // and the reloads inflated the phases they fell in)
+  uint32_t* rec = nullptr;  // thread 128's record of the current step, else null
   auto stamp = [&](int k) {
-    if constexpr (TR) tr[k] = (uint32_t)clock64();
+    if constexpr (TR) {
+      if (rec) rec[k] = (uint32_t)clock64();
+    }
   };
   auto stamp_ns = [&](int k) {
     if constexpr (TR) {
-      const uint64_t g = global_ns();
-      tr[k] = (uint32_t)g;
-      tr[k + 1] = (uint32_t)(g >> 32);
+      if (rec) {
+        const uint64_t g = global_ns();
+        rec[k] = (uint32_t)g;
+        rec[k + 1] = (uint32_t)(g >> 32);
+      }
     }
   };
   for (int t = 0; t < T; ++t) {
     const int par = t & 1;
     const int ts = rev ? T - 1 - t : t;  // the step computed (t counts the steps done)
+    if constexpr (TR)
+      rec = tid == 128 && a.trace ? a.trace + ((size_t)t * c.n_cta + blockIdx.x) * kTraceWords
+                                  : nullptr;
     stamp(4);
     w.new_step();
     float pv[kOutMax];
@@ -406,7 +416,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
       }
     }
     stamp(5);
-    if constexpr (TR) tr[18] = round_max;
+    if constexpr (TR) {
+      if (rec) rec[18] = round_max;
+    }
     if (large) s_large[par] = 1;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (__syncthreads_or(bad)) {
@@ -605,20 +617,16 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
       }
     }
     if constexpr (TR) {
-      if (tid == 128 && a.trace) {
+      if (rec) {
         stamp(12);
         stamp_ns(16);
         uint32_t smid;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        tr[0] = smid;
-        tr[1] = blockIdx.x;
-        tr[2] = (uint32_t)cs;
-        tr[3] = (uint32_t)j;
-        tr[19] = 0;
-        uint32_t* rec = a.trace + ((size_t)t * c.n_cta + blockIdx.x) * kTraceWords;
-#pragma unroll
-        for (int k = 0; k < kKsplitTraceWords; ++k)
-          if (k != 13) rec[k] = tr[k];
+        rec[0] = smid;
+        rec[1] = blockIdx.x;
+        rec[2] = (uint32_t)cs;
+        rec[3] = (uint32_t)j;
+        rec[19] = 0;
       }
     }
     if (tid == 0) {
