@@ -25,10 +25,10 @@
 //     columns];
 //  3. four warps read the accumulators back (lane = row), add the hi and lo
 //     columns of both and stage the partial sums column by column; CTA o of
-//     the cluster owns batch columns [o B / CS, (o + 1) B / CS), and lane o
-//     of warp 4 sends owner o its columns with a bulk copy into the owner's
-//     shared memory (cp.async.bulk shared::cta -> shared::cluster, completing
-//     on the owner's mbarrier);
+//     the cluster owns batch columns [o B / CS, (o + 1) B / CS), and lane
+//     o / 4 of warp 4 + o % 4 sends owner o its columns with a bulk copy
+//     into the owner's shared memory (cp.async.bulk shared::cta ->
+//     shared::cluster, completing on the owner's mbarrier);
 //  4. the owner waits for the CS - 1 blocks, sums the CS partials (slice
 //     order) and P_t, applies ReLU and publishes its columns of the block's
 //     128 rows of h_t into y, as the other persistent kernels do.
@@ -567,9 +567,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("bar.sync 1, 128;" ::: "memory");
-      // lane o of warp 4 sends owner o its columns
-      if (warp == 4 && lane < cs && lane != j && !bad) {
-        const int o = lane, ob = o * B / cs, on = (o + 1) * B / cs - ob;
+      // lane o / 4 of warp 4 + o % 4 sends owner o its columns (issue spread
+      // over the four warps: H=1152 B=16 2.61 -> 2.54 us per step against
+      // lanes 0 .. cs-1 of warp 4 alone)
+      const int o_send = (lane << 2) | (warp - 4);
+      if (lane < 2 && o_send < cs && o_send != j && !bad) {
+        const int o = o_send, ob = o * B / cs, on = (o + 1) * B / cs - ob;
         if (on > 0)
           bulk_to_peer(peer_addr(smem_u32(recv + ((size_t)par * cs + j) * maxcol * 128), (uint32_t)o),
                        smem_u32(stage + ((size_t)par * B + ob) * 128), (uint32_t)on * 512u,
