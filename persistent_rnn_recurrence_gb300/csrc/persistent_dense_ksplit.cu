@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) recur_dense_ksplit_kernel(co
   w.timeout_ns = c.timeout_ns;
   w.backoff = c.poll_backoff;
   constexpr int kOutMax = (kKsplitMaxB + 1) / 2 * 128 / kSplitThreads;  // cs >= 2
-  // output o = tid + u * 256 (o < nout) sits at ooff[u] in a step of P and y
+  // output o = tid + u * kSplitThreads (o < nout) sits at ooff[u] in a step of P and y
   int ooff[kOutMax];
 #pragma unroll
   for (int u = 0; u < kOutMax; ++u) {
