@@ -32,6 +32,11 @@
 //  4. the owner waits for the CS - 1 blocks, sums the CS partials (slice
 //     order) and P_t, applies ReLU and publishes its columns of the block's
 //     128 rows of h_t into y, as the other persistent kernels do.
+// Where a slice of Wh does not fit in shared memory beside the operand tiles
+// (H above 2304), the A operand is not resident: each MMA issuer streams its
+// atoms of the slice from the image in global memory, every step, through a
+// ring of four 16 KB stages (bulk copies, full / empty mbarriers), for
+// batches of up to 16 columns; the step is then bound by that stream.
 // In reverse mode (the backward pass) the steps run T-1 .. 0 over Wh^T's
 // image, h_prev is the next step's delta, and the output is P + sum, or 0
 // where P holds the mask marker.
