@@ -177,9 +177,9 @@ struct DenseSplitArgs {
   const void* Wimg;
   const float* h0_rows;  // [B][H]: h0, or zeros
   int cs, nat;
-  uint32_t* trace;
-  int stream;            // 1: Wh streamed from Wimg through rings (B <= 16), not resident       // null, or [T][n_cta][kTraceWords] phase records (the
-                         // first 20 words of each; see kKsplitTrace*)
+  uint32_t* trace;       // null, or [T][n_cta][kTraceWords] phase records (the
+                         // first kKsplitTraceWords words of each, below)
+  int stream;            // 1: Wh streamed from Wimg through rings (B <= 16), not resident
 };
 // Phase-trace record of the K-split kernel (one step, one CTA), words:
 // 0 SM id, 1 CTA index, 2 cluster size, 3 K slice; SM-clock stamps (low 32
