@@ -582,6 +582,10 @@ static prnn_status_t install_ksplit(prnn_t h, const uint16_t* w16) {
   const int kcs = recur_dense_ksplit_plan(H, &stream);
   if (kcs == 0) return PRNN_OK;
   const int nblk = H / 128, knat = ksplit_nat(H, kcs);
+  // The A operand's image: for row block bk and K slice j, knat atoms of
+  // 128 rows x 64 fp16 (K-major, 128 bytes a row), each row's 16-byte chunks
+  // in the 128-byte swizzle (chunk q of row m at q ^ (m mod 8)); zeros past
+  // the slice's width.  The transposed image serves the reverse recurrence.
   std::vector<uint16_t> img((size_t)nblk * kcs * knat * 128 * 64, 0);
   for (int tr = 0; tr < 2; ++tr) {  // Wh, then Wh^T
     for (int bk = 0; bk < nblk; ++bk)
