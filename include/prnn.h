@@ -437,6 +437,34 @@ prnn_status_t prnn_pack_sparse_host_placed(int hidden, int k, int n_cta, int row
                                            int* bank_cap, int* placed);
 
 /*
+ * Host only (no GPU): the weight image the tensor-core K-split kernel keeps
+ * in shared memory (dense fp16 layers at wide batch), so that its index
+ * handling can be checked without a device.  The layer's rows are split into
+ * hidden/128 blocks of 128 rows; each block's K (the columns) into
+ * cluster_size slices of whole 16-column steps, slice j starting at column
+ * k0(j) = 16 * floor(j * (hidden/16) / cluster_size); each slice is stored as
+ * nat = ceil(ceil((hidden/16) / cluster_size) / 4) atoms of 128 rows x 64
+ * columns.  Element (row r, column c) of the block-row bk = r / 128, slice j
+ * (k0(j) <= c < k0(j+1)), kc = c - k0(j), m = r mod 128 sits at
+ *     ((bk * cluster_size + j) * nat + kc / 64) * 8192
+ *       + m * 64 + (((kc mod 64) / 8) XOR (m mod 8)) * 8 + kc mod 8,
+ * the 128-byte swizzle of the tensor cores' K-major shared-memory operand; every
+ * other element is 0.
+ *   wh16 [hidden][hidden]: fp16 bits of Wh, row-major (input, caller-owned).
+ *   transpose != 0 builds the image of Wh^T (the reverse recurrence's).
+ *   image [capacity_elems] uint16: output, caller-owned.
+ *   *image_elems receives the elements needed.
+ * hidden must be a multiple of 128 (at most 65536), 2 <= cluster_size <= 8
+ * and hidden/16 >= cluster_size; otherwise, or when wh16 or image_elems is
+ * NULL, PRNN_ERR_INVALID_ARG.  When image is NULL or too small the call sets
+ * *image_elems and returns PRNN_ERR_INVALID_ARG, so the caller can size the
+ * buffer and call again.
+ */
+prnn_status_t prnn_pack_dense_ksplit_host(int hidden, int cluster_size, const uint16_t* wh16,
+                                          int transpose, uint16_t* image, size_t capacity_elems,
+                                          size_t* image_elems);
+
+/*
  * Forward pass that allocates no device memory.  The pages have no
  * counterpart to this call: it exists for callers that cannot call
  * cudaMalloc -- code in a latency-critical loop where cudaMalloc/cudaFree may

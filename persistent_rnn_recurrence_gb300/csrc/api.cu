@@ -576,33 +576,42 @@ static bool plan_and_pack(prnn_t h, int k, const std::vector<uint16_t>& hv,
 // recurrence), per CTA (cluster-major, then K slice j) nat atoms of 128 rows x
 // 64 columns, 16-byte chunk q of row m at q ^ (m & 7) (the 128-byte swizzle of
 // the K-major MMA operand).  Sets h->ks.
+// The A operand's image of the K-split kernel: for row block bk and K slice j
+// of cs, nat atoms of 128 rows x 64 fp16 (K-major, 128 bytes a row), each
+// row's 16-byte chunks in the 128-byte swizzle (chunk q of row m at
+// q ^ (m mod 8)); zeros past the slice's width.  The transposed image (rows
+// of Wh^T) serves the reverse recurrence.  img must hold
+// (H / 128) * cs * nat * 8192 elements and be zero-filled.
+static void build_ksplit_image(int H, int cs, int nat, const uint16_t* w16, bool transpose,
+                               uint16_t* img) {
+  const int nblk = H / 128;
+  for (int bk = 0; bk < nblk; ++bk)
+    for (int j = 0; j < cs; ++j) {
+      const int k0 = ksplit_k0(H, cs, j), kl = ksplit_kl(H, cs, j);
+      for (int at = 0; at < nat; ++at)
+        for (int m = 0; m < 128; ++m)
+          for (int q = 0; q < 8; ++q)
+            for (int e = 0; e < 8; ++e) {
+              const int kcol = at * 64 + q * 8 + e;  // column within the slice
+              if (kcol >= kl) continue;
+              const size_t atom = ((size_t)bk * cs + j) * nat + at;
+              const size_t r = (size_t)(bk * 128 + m), cc = (size_t)(k0 + kcol);
+              img[atom * 128 * 64 + (size_t)m * 64 + ((q ^ (m & 7)) * 8) + e] =
+                  transpose ? w16[cc * H + r] : w16[r * H + cc];
+            }
+    }
+}
+
 static prnn_status_t install_ksplit(prnn_t h, const uint16_t* w16) {
   const int H = h->H;
   bool stream = false;
   const int kcs = recur_dense_ksplit_plan(H, &stream);
   if (kcs == 0) return PRNN_OK;
   const int nblk = H / 128, knat = ksplit_nat(H, kcs);
-  // The A operand's image: for row block bk and K slice j, knat atoms of
-  // 128 rows x 64 fp16 (K-major, 128 bytes a row), each row's 16-byte chunks
-  // in the 128-byte swizzle (chunk q of row m at q ^ (m mod 8)); zeros past
-  // the slice's width.  The transposed image serves the reverse recurrence.
-  std::vector<uint16_t> img((size_t)nblk * kcs * knat * 128 * 64, 0);
+  std::vector<uint16_t> img((size_t)nblk * kcs * knat * 128 * 64);
   for (int tr = 0; tr < 2; ++tr) {  // Wh, then Wh^T
-    for (int bk = 0; bk < nblk; ++bk)
-      for (int j = 0; j < kcs; ++j) {
-        const int k0 = ksplit_k0(H, kcs, j), kl = ksplit_kl(H, kcs, j);
-        for (int at = 0; at < knat; ++at)
-          for (int m = 0; m < 128; ++m)
-            for (int q = 0; q < 8; ++q)
-              for (int e = 0; e < 8; ++e) {
-                const int kcol = at * 64 + q * 8 + e;  // column within the slice
-                if (kcol >= kl) continue;
-                const size_t atom = ((size_t)bk * kcs + j) * knat + at;
-                const size_t r = (size_t)(bk * 128 + m), cc = (size_t)(k0 + kcol);
-                img[atom * 128 * 64 + (size_t)m * 64 + ((q ^ (m & 7)) * 8) + e] =
-                    tr ? w16[cc * H + r] : w16[r * H + cc];
-              }
-      }
+    std::fill(img.begin(), img.end(), (uint16_t)0);
+    build_ksplit_image(H, kcs, knat, w16, tr != 0, img.data());
     PRNN_TRY(upload(tr ? &h->WimgT_ks : &h->Wimg_ks, img.data(), img.size() * 2));
   }
   if (!h->zeros) {
@@ -1707,6 +1716,22 @@ prnn_status_t prnn_pack_sparse_host(int hidden, int k, int n_cta, int rows_per_c
   if (bank_cap) *bank_cap = st.cap;
   if (!packed || capacity_words < pk.size()) return PRNN_ERR_INVALID_ARG;
   std::memcpy(packed, pk.data(), pk.size() * sizeof(uint32_t));
+  return PRNN_OK;
+}
+
+prnn_status_t prnn_pack_dense_ksplit_host(int hidden, int cluster_size, const uint16_t* wh16,
+                                          int transpose, uint16_t* image, size_t capacity_elems,
+                                          size_t* image_elems) {
+  const int H = hidden, cs = cluster_size;
+  if (H < 128 || H % 128 != 0 || H > 65536 || cs < 2 || cs > kKsplitMaxCluster || H / 16 < cs)
+    return PRNN_ERR_INVALID_ARG;
+  if (!wh16 || !image_elems) return PRNN_ERR_INVALID_ARG;
+  const int nat = ksplit_nat(H, cs);
+  const size_t need = (size_t)(H / 128) * cs * nat * 128 * 64;
+  *image_elems = need;
+  if (!image || capacity_elems < need) return PRNN_ERR_INVALID_ARG;
+  std::fill(image, image + need, (uint16_t)0);
+  build_ksplit_image(H, cs, nat, wh16, transpose != 0, image);
   return PRNN_OK;
 }
 

@@ -39,7 +39,8 @@ EXPORTS = ["prnn_create", "prnn_set_weights_dense", "prnn_set_weights_sparse",
            "prnn_set_option", "prnn_get_info", "prnn_get_timing", "prnn_probe_sync_floor",
            "prnn_probe_cluster_exchange",
            "prnn_set_trace_buffer",
-           "prnn_pack_sparse_host", "prnn_pack_sparse_host_placed", "prnn_forward_dense_noalloc",
+           "prnn_pack_sparse_host", "prnn_pack_sparse_host_placed", "prnn_pack_dense_ksplit_host",
+           "prnn_forward_dense_noalloc",
            "prnn_set_weights_csr",
            "prnn_stack_create", "prnn_stack_set_layer", "prnn_stack_forward",
            "prnn_stack_get_status", "prnn_stack_set_option", "prnn_stack_get_timing",
@@ -94,6 +95,8 @@ _sig = {
     "prnn_pack_sparse_host_placed": ([_I, _I, _I, _I, _I, _P, _P, _P, ctypes.c_size_t, _P,
                                       ctypes.c_size_t, ctypes.POINTER(_I), ctypes.POINTER(_I),
                                       ctypes.POINTER(_I)], _I),
+    "prnn_pack_dense_ksplit_host": ([_I, _I, _P, _I, _P, ctypes.c_size_t,
+                                     ctypes.POINTER(ctypes.c_size_t)], _I),
     "prnn_forward_dense_noalloc": ([_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
     "prnn_set_weights_csr": ([_P, _P, _I, _P, _P, _P, _P, _P], _I),
     "prnn_stack_create": ([ctypes.POINTER(_P), _I, _I, _I, _I, _I, _I], _I),
@@ -253,6 +256,26 @@ def prnn_set_trace_buffer(h: int, buf, nbytes: int) -> None:
     """Set (or, with buf None, clear) the device buffer of the sparse
     kernel's phase trace: [T][n_cta][12] uint32 records per forward."""
     _check(_lib.prnn_set_trace_buffer(h, _ptr(buf), int(nbytes)), "prnn_set_trace_buffer")
+
+
+def prnn_pack_dense_ksplit_host(hidden, cluster_size, wh16, transpose=False):
+    """Host-only image of the K-split kernel's weights (numpy fp16 [H, H] in,
+    numpy uint16 [H/128, cluster_size, nat, 128, 64] out)."""
+    import numpy as np
+    w = np.ascontiguousarray(wh16).view(np.uint16)
+    if w.shape != (hidden, hidden):
+        raise ValueError("wh16 must be [hidden, hidden]")
+    need = ctypes.c_size_t()
+    st = _lib.prnn_pack_dense_ksplit_host(hidden, cluster_size, w.ctypes.data, int(transpose),
+                                          None, 0, ctypes.byref(need))
+    if st != PRNN_ERR_INVALID_ARG or need.value == 0:
+        _check(st if st != PRNN_OK else PRNN_ERR_INVALID_ARG, "prnn_pack_dense_ksplit_host")
+    nat = need.value // ((hidden // 128) * cluster_size * 8192)
+    out = np.zeros((hidden // 128, cluster_size, nat, 128, 64), dtype=np.uint16)
+    _check(_lib.prnn_pack_dense_ksplit_host(hidden, cluster_size, w.ctypes.data, int(transpose),
+                                            out.ctypes.data, out.size, ctypes.byref(need)),
+           "prnn_pack_dense_ksplit_host")
+    return out
 
 
 def prnn_pack_sparse_host(hidden, k, n_cta, rows_per_cta, threads_per_row, vals, cols):

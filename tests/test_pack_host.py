@@ -251,3 +251,71 @@ def test_random_layouts_pack_exactly(prnn, H, k, tpr, R, n, seed):
                     addrs = np.unique(lanes[:, j])
                     assert np.bincount(addrs % 32, minlength=32).max() <= max(cap, 1), \
                         (placed, c, w, j)
+
+
+# ---- the tensor-core K-split kernel's weight image (prnn_pack_dense_ksplit_host) ----
+
+KSPLIT_CASES = [(128, 2), (128, 8), (384, 7), (640, 8), (1152, 8), (1152, 5), (2304, 6), (4096, 4)]
+
+
+def _unswizzle(img):
+    """[nblk, cs, nat, 128, 64] -> [nblk, cs, 128, nat * 64]: each row's
+    16-byte chunk p holds logical chunk p XOR (row mod 8) (the 128-byte
+    swizzle), atoms of one slice side by side in K."""
+    m = np.arange(128)[:, None]
+    L = np.arange(64)[None, :]
+    idx = ((L // 8) ^ (m % 8)) * 8 + L % 8                      # [128, 64]
+    u = np.take_along_axis(img, np.broadcast_to(idx, img.shape), axis=-1)
+    nblk, cs, nat = img.shape[:3]
+    return u.transpose(0, 1, 3, 2, 4).reshape(nblk, cs, 128, nat * 64)
+
+
+@pytest.mark.parametrize("H,cs", KSPLIT_CASES)
+def test_ksplit_image_places_every_weight_once(prnn, H, cs):
+    r, c = np.meshgrid(np.arange(H), np.arange(H), indexing="ij")
+    rows = prnn.prnn_pack_dense_ksplit_host(H, cs, (r + 1).astype(np.uint16))
+    cols = _unswizzle(prnn.prnn_pack_dense_ksplit_host(H, cs, (c + 1).astype(np.uint16)))
+    rows = _unswizzle(rows)
+    nblk, cs_, _, width = cols.shape
+    assert (nblk, cs_) == (H // 128, cs)
+    # slice widths: whole 16-column steps, as even as possible, tiling 0 .. H-1
+    kl = [(cols[0, j, 0] != 0).sum() for j in range(cs)]
+    assert sum(kl) == H and all(w % 16 == 0 for w in kl) and max(kl) - min(kl) <= 16
+    assert width == -(-max(kl) // 64) * 64                     # whole atoms, no spare one
+    k0 = np.concatenate([[0], np.cumsum(kl)[:-1]])
+    for j in range(cs):
+        w = kl[j]
+        # every row of the slice holds columns k0 .. k0 + kl - 1 in order, then zeros
+        assert (cols[:, j, :, :w] == (k0[j] + np.arange(w) + 1)[None, None, :]).all()
+        assert (cols[:, j, :, w:] == 0).all() and (rows[:, j, :, w:] == 0).all()
+        # lane m of block bk is row 128 bk + m of Wh
+        want_r = (np.arange(nblk)[:, None] * 128 + np.arange(128)[None, :] + 1)
+        assert (rows[:, j, :, :w] == want_r[:, :, None]).all()
+
+
+@pytest.mark.parametrize("H,cs", [(256, 3), (640, 8)])
+def test_ksplit_transposed_image_is_the_image_of_the_transpose(prnn, H, cs):
+    rng = np.random.default_rng(H + cs)
+    w = rng.normal(size=(H, H)).astype(np.float16)
+    a = prnn.prnn_pack_dense_ksplit_host(H, cs, w, transpose=True)
+    b = prnn.prnn_pack_dense_ksplit_host(H, cs, np.ascontiguousarray(w.T))
+    assert np.array_equal(a, b)
+    assert not np.array_equal(a, prnn.prnn_pack_dense_ksplit_host(H, cs, w))
+
+
+def test_ksplit_image_errors(prnn):
+    w = np.zeros((256, 256), dtype=np.float16)
+    for H, cs in ((256, 1), (256, 9)):
+        with pytest.raises(prnn.PrnnError):
+            prnn.prnn_pack_dense_ksplit_host(H, cs, w)
+    with pytest.raises(prnn.PrnnError):                         # not a multiple of 128
+        prnn.prnn_pack_dense_ksplit_host(200, 2, np.zeros((200, 200), dtype=np.float16))
+    with pytest.raises(prnn.PrnnError):                         # 128 / 16 = 8 steps < 9 slices
+        prnn.prnn_pack_dense_ksplit_host(128, 9, np.zeros((128, 128), dtype=np.float16))
+    import ctypes
+    need = ctypes.c_size_t()
+    small = np.zeros(10, dtype=np.uint16)
+    st = prnn._lib.prnn_pack_dense_ksplit_host(256, 2, w.ctypes.data, 0, small.ctypes.data,
+                                              small.size, ctypes.byref(need))
+    assert st == prnn.PRNN_ERR_INVALID_ARG and need.value == 2 * 2 * 2 * 8192
+    assert (small == 0).all()                                   # nothing written
