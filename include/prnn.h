@@ -121,7 +121,7 @@ typedef enum {
                                      all H / 128 clusters of 2 .. 8 CTAs resident at once, one
                                      CTA per SM (on 152 SMs: clusters of 8 up to H = 1920, of
                                      6 up to 2304; from H = 2560 to 4096 clusters of 4 with
-                                     Wh streamed from L2 each step, for B <= 16): the
+                                     Wh streamed from device memory each step, B <= 16): the
                                      tensor-core kernel that splits each
                                      step's product over K inside clusters (h split into fp16
                                      hi + lo parts, about 22 bits; partial sums reduced through

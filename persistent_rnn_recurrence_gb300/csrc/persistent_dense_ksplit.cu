@@ -69,7 +69,7 @@ static_assert(kSplitPollMax * kSplitThreads * 4 >= kKsplitMaxB * kKsplitMaxSlice
 constexpr uint32_t kAtomA = 128 * 128;  // bytes of one A atom: 128 rows x 64 fp16
 // Streamed A (layers whose weights do not fit beside the operand tiles): each
 // MMA issuer has a ring of kNsq A stages refilled by bulk copies from the
-// weight image (it stays in L2), kNsq - 1 atoms ahead of its MMAs, across
+// weight image in device memory, kNsq - 1 atoms ahead of its MMAs, across
 // steps; 8 polls per thread cover a slice of up to kKsplitMaxSliceStream
 // columns at B <= 16
 constexpr int kNsq = 4;
