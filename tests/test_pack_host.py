@@ -319,3 +319,25 @@ def test_ksplit_image_errors(prnn):
                                               small.size, ctypes.byref(need))
     assert st == prnn.PRNN_ERR_INVALID_ARG and need.value == 2 * 2 * 2 * 8192
     assert (small == 0).all()                                   # nothing written
+
+
+@pytest.mark.parametrize("H,cs", [(384, 7), (1152, 8)])
+def test_ksplit_image_matches_the_header_formula(prnn, H, cs):
+    """The element placement include/prnn.h documents for
+    prnn_pack_dense_ksplit_host, evaluated for every weight."""
+    rng = np.random.default_rng(7 * H + cs)
+    w = rng.integers(1, 1 << 15, size=(H, H), dtype=np.uint16)  # no zero weights
+    flat = prnn.prnn_pack_dense_ksplit_host(H, cs, w).ravel()
+    steps = H // 16
+    k0 = [16 * (j * steps // cs) for j in range(cs + 1)]
+    nat = -(-(-(-steps // cs)) // 4)
+    assert flat.size == (H // 128) * cs * nat * 8192
+    r, c = np.meshgrid(np.arange(H), np.arange(H), indexing="ij")
+    j = np.searchsorted(np.array(k0), c, side="right") - 1
+    kc = c - np.array(k0)[j]
+    bk, m = r // 128, r % 128
+    pos = ((bk * cs + j) * nat + kc // 64) * 8192 + m * 64 + (((kc % 64) // 8) ^ (m % 8)) * 8 + kc % 8
+    assert np.array_equal(flat[pos], w)
+    rest = np.ones(flat.size, dtype=bool)
+    rest[pos.ravel()] = False
+    assert (flat[rest] == 0).all()
