@@ -122,10 +122,10 @@ typedef enum {
                                      CTA per SM (on 152 SMs: clusters of 8 up to H = 1920, of
                                      6 up to 2304; from H = 2560 to 4096 clusters of 4 with
                                      Wh streamed from device memory each step, B <= 16): the
-                                     tensor-core kernel that splits each
-                                     step's product over K inside clusters (h split into fp16
-                                     hi + lo parts, about 22 bits; partial sums reduced through
-                                     distributed shared memory) for forwards of B <= 32.
+                                     tensor-core kernel that splits each step's product over
+                                     K inside clusters (h split into fp16 hi + lo parts,
+                                     about 22 bits; partial sums reduced through distributed
+                                     shared memory) for forwards of B <= 32.
                                      1 = where it measured faster than the CUDA-core kernels
                                      (default): H >= 2048 and B >= 4, H >= 1536 and B >= 8,
                                      or H >= 640 and B >= 12; 2 = for every B <= 32; 0 =
